@@ -1,0 +1,308 @@
+/*
+ * si_oracle.c -- plain, slow CPU oracle for the indexer -> Top-K -> sparse
+ * attention path.  TEST INFRASTRUCTURE ONLY: it is built by build() and used by
+ * the tests, the smoke check and the CPU-baseline leg of the benchmark; the
+ * product library never links or calls it, and it shares no code, header or
+ * table with the CUDA sources.
+ *
+ * Every value is computed in double precision straight from the definitions
+ * on the page "Day0 Inference Support and Performance Optimization for New
+ * Architecture LLMs" (Baidu Cloud), section 2.2 "Sparse Attention: Indexer
+ * Filtering Top-K Historical Positions" and section 4 ("4.1 Overall Indexer
+ * Fusion", "4.2 Index-Based Reading for Sparse Attention"):
+ *
+ *   1. the indexer scores each query against every earlier position,
+ *      score(t,s) = sum_h w[t,h] * ReLU(q_idx[t,h,:] . k_idx[s,:])
+ *      (head-weighted aggregation of per-head relevance; ReLU per head);
+ *   2. the Top-K positions by score are selected (ties -> lower position);
+ *   3. attention reads only the selected K/V rows and returns the
+ *      softmax-weighted sum of their values.
+ *
+ * Keys live in a paged cache ("reads data directly from the paged K-cache",
+ * section 4.1): logical position s of sequence q is physical row
+ * block_table[q][s / page] * page + s % page.
+ *
+ * Storage codes: 0 = float32, 1 = bfloat16 bit patterns, 2 = FP8 e4m3 codes
+ * (OCP definition: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits; code
+ * S.1111.111 is NaN, there are no infinities).
+ *
+ * No blocking, fusion or reordering: loops run in the order of the
+ * definitions; a library sort (qsort) orders the candidates.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+
+typedef struct {
+    int32_t n_seq;
+    int32_t max_blocks;
+    int32_t page;
+    int32_t n_q;
+    const int32_t *block_table; /* [n_seq, max_blocks] */
+    const int32_t *ctx_len;     /* [n_seq] */
+    const int32_t *q_seq;       /* [n_q] */
+    const int32_t *q_pos;       /* [n_q] */
+} orc_batch;
+
+/* ---------------------------------------------------------------- decoding */
+
+double orc_bf16_to_f64(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16; /* bf16 is the top half of an IEEE float32 */
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double orc_e4m3_to_f64(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 15;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);            /* subnormal: 0.m * 2^(1-7) */
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);     /* normal: 1.m * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+static double elem(const void *base, int type, int64_t i)
+{
+    switch (type) {
+    case ORC_F32: return (double)((const float *)base)[i];
+    case ORC_BF16: return orc_bf16_to_f64(((const uint16_t *)base)[i]);
+    default: return orc_e4m3_to_f64(((const uint8_t *)base)[i]);
+    }
+}
+
+/* physical row of logical position s of sequence q */
+static int64_t page_row(const orc_batch *b, int32_t q, int64_t s)
+{
+    int32_t blk = b->block_table[(int64_t)q * b->max_blocks + s / b->page];
+    return (int64_t)blk * b->page + s % b->page;
+}
+
+/* ------------------------------------------------------------ thread pool */
+
+typedef struct {
+    void (*fn)(void *ctx, int64_t i);
+    void *ctx;
+    int64_t n;
+    int tid, nthreads;
+} orc_job;
+
+static void *orc_worker(void *p)
+{
+    orc_job *j = (orc_job *)p;
+    for (int64_t i = j->tid; i < j->n; i += j->nthreads)
+        j->fn(j->ctx, i);
+    return NULL;
+}
+
+static void orc_parallel(void (*fn)(void *, int64_t), void *ctx, int64_t n, int nthreads)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    pthread_t th[256];
+    orc_job jobs[256];
+    for (int t = 0; t < nthreads; t++) {
+        jobs[t].fn = fn; jobs[t].ctx = ctx; jobs[t].n = n;
+        jobs[t].tid = t; jobs[t].nthreads = nthreads;
+        if (t > 0)
+            pthread_create(&th[t], NULL, orc_worker, &jobs[t]);
+    }
+    orc_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; t++)
+        pthread_join(th[t], NULL);
+}
+
+/* --------------------------------------------------------------- indexer */
+
+typedef struct {
+    const orc_batch *b;
+    const int32_t *rows; /* which query rows (NULL = 0..n_rows-1) */
+    int32_t Hi, Di;
+    const void *q_idx; int q_type;      /* [n_q, Hi, Di] */
+    const float *w;                     /* [n_q, Hi] */
+    const void *k; int k_type;          /* paged [n_blocks, page, k_stride] */
+    const float *k_scale;               /* [n_blocks, page] or NULL */
+    int64_t k_stride;
+    double *scores; int64_t ld;         /* [n_rows, ld] */
+} idx_ctx;
+
+static void idx_row(void *p, int64_t i)
+{
+    const idx_ctx *c = (const idx_ctx *)p;
+    const orc_batch *b = c->b;
+    int32_t r = c->rows ? c->rows[i] : (int32_t)i;
+    int32_t seq = b->q_seq[r];
+    int64_t pos = b->q_pos[r];
+    double *out = c->scores + i * c->ld;
+    for (int64_t s = 0; s < c->ld; s++) {
+        if (s > pos) {            /* causal: only positions s <= pos are scored */
+            out[s] = -INFINITY;
+            continue;
+        }
+        int64_t row = page_row(b, seq, s);
+        double kscale = c->k_scale ? (double)c->k_scale[row] : 1.0;
+        double score = 0.0;
+        for (int32_t h = 0; h < c->Hi; h++) {
+            double dot = 0.0;
+            for (int32_t d = 0; d < c->Di; d++) {
+                double qv = elem(c->q_idx, c->q_type, ((int64_t)r * c->Hi + h) * c->Di + d);
+                double kv = elem(c->k, c->k_type, row * c->k_stride + d) * kscale;
+                dot += qv * kv;
+            }
+            double relu = dot > 0.0 ? dot : 0.0;
+            score += (double)c->w[(int64_t)r * c->Hi + h] * relu;
+        }
+        out[s] = score + 0.0; /* -0.0 -> +0.0 */
+    }
+}
+
+void oracle_indexer_scores(const orc_batch *b, const int32_t *rows, int32_t n_rows,
+                           int32_t Hi, int32_t Di, const void *q_idx, int q_type,
+                           const float *w, const void *k, int k_type, const float *k_scale,
+                           int64_t k_stride, double *scores, int64_t ld, int nthreads)
+{
+    idx_ctx c = { b, rows, Hi, Di, q_idx, q_type, w, k, k_type, k_scale, k_stride, scores, ld };
+    orc_parallel(idx_row, &c, n_rows, nthreads);
+}
+
+/* ------------------------------------------------------------------ top-k */
+
+typedef struct { double score; int64_t pos; } orc_cand;
+
+/* descending score; equal scores -> ascending position */
+static int cand_cmp(const void *x, const void *y)
+{
+    const orc_cand *a = (const orc_cand *)x, *b = (const orc_cand *)y;
+    if (a->score > b->score) return -1;
+    if (a->score < b->score) return 1;
+    return (a->pos > b->pos) - (a->pos < b->pos);
+}
+
+static int i32_cmp(const void *x, const void *y)
+{
+    int32_t a = *(const int32_t *)x, b = *(const int32_t *)y;
+    return (a > b) - (a < b);
+}
+
+typedef struct {
+    const orc_batch *b;
+    const int32_t *rows;
+    const double *scores; int64_t ld;
+    int32_t K;
+    int32_t *idx;         /* [n_rows, K] */
+    double *kth;          /* [n_rows, 2]: K-th and (K+1)-th score, or NaN */
+} topk_ctx;
+
+static void topk_row(void *p, int64_t i)
+{
+    const topk_ctx *c = (const topk_ctx *)p;
+    int32_t r = c->rows ? c->rows[i] : (int32_t)i;
+    int64_t n = (int64_t)c->b->q_pos[r] + 1;   /* candidates: positions 0..pos */
+    int32_t *out = c->idx + i * c->K;
+    orc_cand *cand = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)(n > 0 ? n : 1));
+    for (int64_t s = 0; s < n; s++) {
+        cand[s].score = c->scores[i * c->ld + s];
+        cand[s].pos = s;
+    }
+    qsort(cand, (size_t)n, sizeof(orc_cand), cand_cmp);
+    int64_t m = n < c->K ? n : c->K;          /* all of them if pos + 1 <= K */
+    for (int64_t j = 0; j < m; j++)
+        out[j] = (int32_t)cand[j].pos;
+    qsort(out, (size_t)m, sizeof(int32_t), i32_cmp);   /* ascending positions */
+    for (int64_t j = m; j < c->K; j++)
+        out[j] = -1;
+    if (c->kth) {
+        c->kth[2 * i] = (n >= c->K) ? cand[c->K - 1].score : NAN;
+        c->kth[2 * i + 1] = (n > c->K) ? cand[c->K].score : NAN;
+    }
+    free(cand);
+}
+
+void oracle_topk(const orc_batch *b, const int32_t *rows, int32_t n_rows, const double *scores,
+                 int64_t ld, int32_t K, int32_t *idx, double *kth, int nthreads)
+{
+    topk_ctx c = { b, rows, scores, ld, K, idx, kth };
+    orc_parallel(topk_row, &c, n_rows, nthreads);
+}
+
+/* --------------------------------------------------------- sparse attention */
+
+typedef struct {
+    const orc_batch *b;
+    const int32_t *rows;
+    int32_t Hq, Dqk, Dv;
+    const void *q; int q_type;          /* [n_q, Hq, Dqk] */
+    const void *k; const void *v; int kv_type;
+    int64_t k_stride, v_stride;         /* V row = first Dv entries of its row */
+    const int32_t *idx; int32_t K;      /* [n_rows, K], -1 = unused */
+    double scale;
+    double *out;                        /* [n_rows, Hq, Dv] */
+    double *lse;                        /* [n_rows, Hq] or NULL */
+} attn_ctx;
+
+static void attn_row(void *p, int64_t i)
+{
+    const attn_ctx *c = (const attn_ctx *)p;
+    const orc_batch *b = c->b;
+    int32_t r = c->rows ? c->rows[i] : (int32_t)i;
+    int32_t seq = b->q_seq[r];
+    const int32_t *sel = c->idx + i * c->K;
+    double *z = (double *)malloc(sizeof(double) * (size_t)c->K);
+    int64_t *prow = (int64_t *)malloc(sizeof(int64_t) * (size_t)c->K);
+    int32_t n = 0;
+    for (int32_t j = 0; j < c->K; j++)
+        if (sel[j] >= 0)
+            prow[n++] = page_row(b, seq, sel[j]);
+    for (int32_t h = 0; h < c->Hq; h++) {
+        double *o = c->out + ((int64_t)i * c->Hq + h) * c->Dv;
+        int64_t qoff = ((int64_t)r * c->Hq + h) * c->Dqk;
+        double zmax = -INFINITY;
+        for (int32_t j = 0; j < n; j++) {       /* logits over the selected rows */
+            double dot = 0.0;
+            for (int32_t d = 0; d < c->Dqk; d++)
+                dot += elem(c->q, c->q_type, qoff + d) *
+                       elem(c->k, c->kv_type, prow[j] * c->k_stride + d);
+            z[j] = c->scale * dot;
+            if (z[j] > zmax) zmax = z[j];
+        }
+        double l = 0.0;
+        for (int32_t j = 0; j < n; j++) {       /* softmax weights */
+            z[j] = exp(z[j] - zmax);
+            l += z[j];
+        }
+        for (int32_t d = 0; d < c->Dv; d++) {   /* weighted sum of values */
+            double acc = 0.0;
+            for (int32_t j = 0; j < n; j++)
+                acc += z[j] * elem(c->v, c->kv_type, prow[j] * c->v_stride + d);
+            o[d] = n > 0 ? acc / l : 0.0;
+        }
+        if (c->lse)
+            c->lse[(int64_t)i * c->Hq + h] = n > 0 ? zmax + log(l) : -INFINITY;
+    }
+    free(z);
+    free(prow);
+}
+
+void oracle_sparse_attn(const orc_batch *b, const int32_t *rows, int32_t n_rows, int32_t Hq,
+                        int32_t Dqk, int32_t Dv, const void *q, int q_type, const void *k,
+                        const void *v, int kv_type, int64_t k_stride, int64_t v_stride,
+                        const int32_t *idx, int32_t K, double scale, double *out, double *lse,
+                        int nthreads)
+{
+    attn_ctx c = { b, rows, Hq, Dqk, Dv, q, q_type, k, v, kv_type, k_stride, v_stride,
+                   idx, K, scale, out, lse };
+    orc_parallel(attn_row, &c, n_rows, nthreads);
+}

@@ -1,0 +1,341 @@
+"""Seeded synthetic inputs for the indexer -> Top-K -> sparse-attention path.
+
+This module only *generates* data.  It holds none of the method's arithmetic
+(no scoring, selection or attention); both the CPU oracle and the CUDA path
+consume the bytes it produces.  Everything is drawn from one numpy PCG64
+stream per (config, seed) in a fixed order, so a workload is reproducible
+byte-for-byte on any host.
+
+Workload shapes follow the five synthetic configurations of the hot path:
+
+  c0  tiny causal prefill, fp32: 1 sequence of 256 tokens, indexer 4x32,
+      Top-K 32, attention 4 heads x 64 with separate K and V caches.
+  c1  decode, batch 64, context 8192; indexer 64 heads x 128 with FP8 e4m3
+      keys (per-token fp32 scale) and bf16 queries; Top-K 2048; attention
+      128 query heads over one shared latent row of 576 bf16 (V = first 512).
+  c2  causal prefill of 16384 tokens, shapes as c1.
+  c3  decode, batch 16, context 131072, shapes as c1, 1% of key positions
+      planted with +3 sigma alignment to every indexer head of the query.
+  c4  ragged batch of 32 requests with log-uniform contexts in [1024, 65536]:
+      28 single-token decodes and 4 chunks of 2048 prefill rows.
+
+Draw order (per config): context lengths (c4 only) -> physical block
+permutation -> q_idx -> w -> indexer keys (sequence by sequence, logical
+order) -> planted positions and offsets (c3) -> attention q -> K/V rows
+(sequence by sequence).  Unused slots of a sequence's last page and the
+spare pages of the pool are filled with NaN so that any read outside a
+sequence's context poisons the result.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+F32, BF16, E4M3 = "f32", "bf16", "e4m3"
+PAGE = 64
+E4M3_MAX = 448.0
+
+# Base configurations (names c0..c4).  Overrides shrink them for tests.
+CONFIGS = {
+    "c0": dict(kind="prefill", L=256, Hi=4, Di=32, K=32, Hq=4, Dqk=64, Dv=64,
+               dtype=F32, split_kv=True, q_idx_std=1 / math.sqrt(32),
+               k_idx_std=1 / math.sqrt(32), w_scale=1.0, scale=1 / math.sqrt(64),
+               seed=0),
+    "c1": dict(kind="decode", batch=64, ctx=8192, Hi=64, Di=128, K=2048, Hq=128,
+               Dqk=576, Dv=512, dtype=BF16, split_kv=False,
+               q_idx_std=1 / math.sqrt(128), k_idx_std=1.0, w_scale=1 / 64,
+               scale=1 / math.sqrt(576), seed=1),
+    "c2": dict(kind="prefill", L=16384, Hi=64, Di=128, K=2048, Hq=128, Dqk=576,
+               Dv=512, dtype=BF16, split_kv=False, q_idx_std=1 / math.sqrt(128),
+               k_idx_std=1.0, w_scale=1 / 64, scale=1 / math.sqrt(576), seed=2),
+    "c3": dict(kind="decode", batch=16, ctx=131072, Hi=64, Di=128, K=2048,
+               Hq=128, Dqk=576, Dv=512, dtype=BF16, split_kv=False,
+               q_idx_std=1 / math.sqrt(128), k_idx_std=1.0, w_scale=1 / 64,
+               scale=1 / math.sqrt(576), planted=0.01, seed=3),
+    "c4": dict(kind="mixed", n_req=32, n_prefill=4, chunk=2048, ctx_lo=1024,
+               ctx_hi=65536, Hi=64, Di=128, K=2048, Hq=128, Dqk=576, Dv=512,
+               dtype=BF16, split_kv=False, q_idx_std=1 / math.sqrt(128),
+               k_idx_std=1.0, w_scale=1 / 64, scale=1 / math.sqrt(576), seed=4),
+}
+
+
+@dataclasses.dataclass
+class Workload:
+    """Host-side arrays of one workload (all numpy, C-contiguous).
+
+    Storage conventions (shared by oracle and CUDA path):
+      * bf16 tensors are uint16 bit patterns, e4m3 tensors uint8 codes.
+      * caches are paged: [n_blocks, page, row] in the physical order given
+        by ``block_table`` ([n_seq, max_blocks], int32, -1 = unused).
+      * query row r belongs to sequence ``q_seq[r]`` at absolute position
+        ``q_pos[r]`` and may look at key positions 0..q_pos[r].
+    """
+    name: str
+    Hi: int
+    Di: int
+    Hq: int
+    Dqk: int
+    Dv: int
+    K: int
+    page: int
+    scale: float                 # softmax scale of the attention logits
+    block_table: np.ndarray      # int32 [n_seq, max_blocks]
+    ctx_len: np.ndarray          # int32 [n_seq]
+    q_seq: np.ndarray            # int32 [n_q]
+    q_pos: np.ndarray            # int32 [n_q]
+    q_idx: np.ndarray            # f32 or bf16 bits [n_q, Hi, Di]
+    q_idx_dtype: str
+    w: np.ndarray                # f32 [n_q, Hi]
+    k_idx: np.ndarray            # f32 or e4m3 codes [n_blocks, page, Di]
+    k_idx_dtype: str
+    k_scale: Optional[np.ndarray]  # f32 [n_blocks, page] or None (=1)
+    q: np.ndarray                # f32 or bf16 bits [n_q, Hq, Dqk]
+    kv_dtype: str
+    k: np.ndarray                # [n_blocks, page, Dqk] (row stride = last dim)
+    v: Optional[np.ndarray]      # [n_blocks, page, Dv]; None = V is the first Dv cols of k
+    planted: Optional[list] = None  # c3: per-sequence arrays of planted positions
+
+    @property
+    def n_q(self) -> int:
+        return int(self.q_pos.shape[0])
+
+    @property
+    def n_seq(self) -> int:
+        return int(self.ctx_len.shape[0])
+
+    @property
+    def max_ctx(self) -> int:
+        return int(self.q_pos.max()) + 1 if self.n_q else 0
+
+    @property
+    def n_blocks(self) -> int:
+        return int(self.k.shape[0])
+
+
+# ---------------------------------------------------------------- encoders
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (nearest, ties to even); NaN kept."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    out = r.astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = 0x7FC0
+    return out
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Encode values with |x| <= 448 as OCP FP8 e4m3 codes (nearest, ties to
+    even, saturating at 448).  Input generation only."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    _, ex = np.frexp(a)                       # a = m * 2**ex, m in [0.5, 1)
+    e = np.maximum(ex - 1, -6)                # binade exponent, subnormals share -6
+    quantum = np.ldexp(1.0, e - 3)            # 3 mantissa bits
+    qv = np.minimum(np.round(a / quantum) * quantum, E4M3_MAX)
+    _, ex2 = np.frexp(qv)
+    e2 = ex2 - 1
+    normal = (qv >= 2.0 ** -6)
+    exp_field = np.where(normal, e2 + 7, 0)
+    mant = np.where(normal, np.round((qv / np.ldexp(1.0, e2) - 1.0) * 8.0),
+                    np.round(qv / 2.0 ** -9))
+    code = (exp_field.astype(np.int64) << 3) | mant.astype(np.int64)
+    code = np.where(qv == 0, 0, code)
+    sign = np.where((x < 0) & (qv != 0), 0x80, 0)
+    return (code | sign).astype(np.uint8)
+
+
+def quantize_rows_e4m3(rows: np.ndarray):
+    """Per-row (per-token) FP8 storage: scale = amax(|row|)/448, codes =
+    e4m3(row/scale).  Returns (codes uint8, scale float32)."""
+    rows = np.asarray(rows, dtype=np.float32)
+    amax = np.abs(rows).max(axis=-1)
+    scale = (np.maximum(amax, 1e-30) / E4M3_MAX).astype(np.float32)
+    codes = f32_to_e4m3_bits(rows.astype(np.float64) / scale[..., None].astype(np.float64))
+    return codes, scale
+
+
+# ---------------------------------------------------------------- layout
+
+def _paged_pool(rng, ctx_len, page, spare=2):
+    """Shuffled physical page assignment: logical block j of sequence i lives
+    at physical block ``block_table[i, j]``."""
+    nb = [(c + page - 1) // page for c in ctx_len]
+    total = int(sum(nb)) + spare
+    perm = rng.permutation(total).astype(np.int32)
+    max_blocks = max(nb) if nb else 1
+    bt = np.full((len(ctx_len), max_blocks), -1, dtype=np.int32)
+    off = 0
+    for i, n in enumerate(nb):
+        bt[i, :n] = perm[off:off + n]
+        off += n
+    return bt, total
+
+
+def _scatter_rows(pool, bt, seq, rows, page):
+    """Write logical rows [0, len(rows)) of sequence ``seq`` into the pool."""
+    n = rows.shape[0]
+    for j in range((n + page - 1) // page):
+        lo, hi = j * page, min(n, (j + 1) * page)
+        pool[bt[seq, j], : hi - lo] = rows[lo:hi]
+
+
+def _normal(rng, shape, std=1.0):
+    return (rng.standard_normal(size=shape, dtype=np.float32) * np.float32(std))
+
+
+# ---------------------------------------------------------------- builder
+
+def config(name: str, **over) -> dict:
+    cfg = dict(CONFIGS[name])
+    cfg.update(over)
+    return cfg
+
+
+def make(name: str, seed: Optional[int] = None, **over) -> Workload:
+    """Build workload ``name`` (c0..c4) with optional size overrides, e.g.
+    ``make("c1", batch=4, ctx=3000)``.  ``seed`` defaults to the config's."""
+    cfg = config(name, **over)
+    if seed is None:
+        seed = cfg["seed"]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    page = cfg.get("page", PAGE)
+    Hi, Di, Hq, Dqk, Dv = cfg["Hi"], cfg["Di"], cfg["Hq"], cfg["Dqk"], cfg["Dv"]
+    kind = cfg["kind"]
+
+    # 1. request structure: (ctx_len per sequence, query rows)
+    if kind == "prefill":
+        L = cfg["L"]
+        ctx_len = np.array([L], dtype=np.int32)
+        q_seq = np.zeros(L, dtype=np.int32)
+        q_pos = np.arange(L, dtype=np.int32)
+    elif kind == "decode":
+        B, ctx = cfg["batch"], cfg["ctx"]
+        ctxs = cfg.get("ctx_list")
+        ctx_len = np.array(ctxs if ctxs is not None else [ctx] * B, dtype=np.int32)
+        q_seq = np.arange(len(ctx_len), dtype=np.int32)
+        q_pos = ctx_len - 1
+    elif kind == "mixed":
+        n_req, n_pf, chunk = cfg["n_req"], cfg["n_prefill"], cfg["chunk"]
+        lo, hi = math.log(cfg["ctx_lo"]), math.log(cfg["ctx_hi"])
+        existing = np.exp(rng.uniform(lo, hi, size=n_req)).astype(np.int64)
+        existing = np.clip(existing, cfg["ctx_lo"], cfg["ctx_hi"]).astype(np.int32)
+        # the first n_req - n_pf requests decode one token, the rest prefill a chunk
+        new_tok = np.array([1] * (n_req - n_pf) + [chunk] * n_pf, dtype=np.int32)
+        ctx_len = (existing + new_tok).astype(np.int32)
+        q_seq_l, q_pos_l = [], []
+        for i in range(n_req):
+            q_seq_l.append(np.full(new_tok[i], i, dtype=np.int32))
+            q_pos_l.append(np.arange(existing[i], existing[i] + new_tok[i], dtype=np.int32))
+        q_seq = np.concatenate(q_seq_l)
+        q_pos = np.concatenate(q_pos_l)
+    else:
+        raise ValueError(kind)
+    n_seq = len(ctx_len)
+    n_q = len(q_pos)
+
+    # 2. physical page placement (shared by the indexer-key and KV caches)
+    bt, n_blocks = _paged_pool(rng, ctx_len.tolist(), page)
+
+    fp32 = cfg["dtype"] == F32
+
+    # 3. indexer queries and head weights
+    qi = _normal(rng, (n_q, Hi, Di), cfg["q_idx_std"])
+    q_idx = qi if fp32 else f32_to_bf16_bits(qi)
+    w = (rng.random(size=(n_q, Hi), dtype=np.float32) * np.float32(cfg["w_scale"])).astype(np.float32)
+
+    # 4. indexer keys, logical order, sequence by sequence
+    k_idx = np.full((n_blocks, page, Di), np.nan if fp32 else 0, dtype=np.float32 if fp32 else np.uint8)
+    if not fp32:
+        k_idx[:] = 0x7F                       # e4m3 NaN in unused slots
+    k_scale = None if fp32 else np.full((n_blocks, page), np.nan, dtype=np.float32)
+    planted = None
+    raw_keys = []
+    for i in range(n_seq):
+        raw_keys.append(_normal(rng, (int(ctx_len[i]), Di), cfg["k_idx_std"]))
+
+    # 5. planted structure (c3): 1% of positions aligned with every head of
+    # the sequence's query by +3 sigma, sigma = ||q_h|| (std of q_h . k, k ~ N(0, I)).
+    if cfg.get("planted"):
+        planted = []
+        for i in range(n_seq):
+            c = int(ctx_len[i])
+            n_pl = int(round(cfg["planted"] * c))
+            pos = np.sort(rng.choice(c, size=n_pl, replace=False)).astype(np.int32)
+            rows = np.nonzero(q_seq == i)[0]
+            qmat = (qi[rows[-1]] if fp32 else _bf16_bits_to_f32(q_idx[rows[-1]])).astype(np.float64)
+            target = 3.0 * np.linalg.norm(qmat, axis=1)
+            delta = qmat.T @ np.linalg.solve(qmat @ qmat.T, target)   # min-norm solution
+            raw_keys[i][pos] += delta.astype(np.float32)
+            planted.append(pos)
+
+    for i in range(n_seq):
+        if fp32:
+            _scatter_rows(k_idx, bt, i, raw_keys[i], page)
+        else:
+            codes, sc = quantize_rows_e4m3(raw_keys[i])
+            _scatter_rows(k_idx, bt, i, codes, page)
+            _scatter_rows(k_scale, bt, i, sc, page)
+    del raw_keys
+
+    # 6. attention queries
+    qa = _normal(rng, (n_q, Hq, Dqk))
+    q = qa if fp32 else f32_to_bf16_bits(qa)
+    del qa
+
+    # 7. K/V rows
+    if cfg["split_kv"]:
+        k = np.full((n_blocks, page, Dqk), np.nan, dtype=np.float32)
+        v = np.full((n_blocks, page, Dv), np.nan, dtype=np.float32)
+        for i in range(n_seq):
+            c = int(ctx_len[i])
+            _scatter_rows(k, bt, i, _normal(rng, (c, Dqk)), page)
+            _scatter_rows(v, bt, i, _normal(rng, (c, Dv)), page)
+        if not fp32:
+            k, v = f32_to_bf16_bits(k), f32_to_bf16_bits(v)
+    else:
+        k = np.full((n_blocks, page, Dqk), np.nan if fp32 else 0x7FC0,
+                    dtype=np.float32 if fp32 else np.uint16)
+        v = None
+        for i in range(n_seq):
+            c = int(ctx_len[i])
+            # draw in pieces to bound host memory for long contexts
+            step = 16384
+            for s0 in range(0, c, step):
+                s1 = min(c, s0 + step)
+                rows = _normal(rng, (s1 - s0, Dqk))
+                rows = rows if fp32 else f32_to_bf16_bits(rows)
+                for j in range(s0 // page, (s1 + page - 1) // page):
+                    lo, hi = j * page, min(s1, (j + 1) * page)
+                    k[bt[i, j], lo - j * page: hi - j * page] = rows[lo - s0: hi - s0]
+
+    return Workload(
+        name=name, Hi=Hi, Di=Di, Hq=Hq, Dqk=Dqk, Dv=Dv, K=int(cfg["K"]), page=page,
+        scale=float(cfg["scale"]), block_table=bt, ctx_len=ctx_len, q_seq=q_seq,
+        q_pos=q_pos, q_idx=q_idx, q_idx_dtype=F32 if fp32 else BF16, w=w,
+        k_idx=k_idx, k_idx_dtype=F32 if fp32 else E4M3, k_scale=k_scale, q=q,
+        kv_dtype=F32 if fp32 else BF16, k=k, v=v, planted=planted)
+
+
+def _bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def permute_pages(wl: Workload, seed: int) -> Workload:
+    """Same logical content, different physical page placement."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    perm = rng.permutation(wl.n_blocks).astype(np.int32)     # old block b -> new perm[b]
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(wl.n_blocks, dtype=np.int32)
+
+    def mv(a):
+        return None if a is None else np.ascontiguousarray(a[inv])
+
+    bt = np.where(wl.block_table >= 0, perm[np.maximum(wl.block_table, 0)], -1).astype(np.int32)
+    return dataclasses.replace(wl, block_table=bt, k_idx=mv(wl.k_idx), k_scale=mv(wl.k_scale),
+                               k=mv(wl.k), v=mv(wl.v))

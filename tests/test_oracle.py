@@ -1,0 +1,313 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself
+(hand-computed values, library routines, closed forms, invariants)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------ format decoders
+
+def test_e4m3_decoder_all_codes_match_torch():
+    """Every one of the 256 FP8 e4m3 codes decodes like torch's float8_e4m3fn."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_f64(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_decoder_hand_values():
+    """Known codes of the OCP e4m3 format: max normal 448, min subnormal 2^-9,
+    min normal 2^-6, one, minus two."""
+    assert oracle.e4m3_to_f64(0x7E) == 448.0
+    assert oracle.e4m3_to_f64(0x01) == 2.0 ** -9
+    assert oracle.e4m3_to_f64(0x08) == 2.0 ** -6
+    assert oracle.e4m3_to_f64(0x38) == 1.0
+    assert oracle.e4m3_to_f64(0xC0) == -2.0
+    assert oracle.e4m3_to_f64(0x07) == 7 * 2.0 ** -9
+    assert math.isnan(oracle.e4m3_to_f64(0x7F))
+
+
+def test_bf16_decoder_matches_torch():
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 1 << 16, size=4000, dtype=np.uint16)
+    bits = bits[((bits >> 7) & 0xFF) != 0xFF]          # finite patterns only
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_to_f64(int(b)) for b in bits])
+    assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------ hand-computed fixture
+
+def _golden():
+    with open(os.path.join(GOLDEN, "tiny_indexer_topk_attn.json")) as f:
+        return json.load(f)
+
+
+def _golden_batch(g, pos_list):
+    page = g["page"]
+    bt = np.array(g["block_table"], dtype=np.int32)
+    n_blocks = int(bt.max()) + 1
+    k = np.full((n_blocks, page, 2), np.nan, dtype=np.float32)
+    for s, row in enumerate(g["k_idx_logical"]):
+        k[bt[0, s // page], s % page] = row
+    b = oracle.Batch(bt, g["ctx_len"], np.zeros(len(pos_list), np.int32), pos_list, page)
+    return b, k, bt, n_blocks
+
+
+def test_golden_scores_and_topk():
+    g = _golden()
+    rows = g["rows"]
+    b, k, _, _ = _golden_batch(g, [r["pos"] for r in rows])
+    q_idx = np.array([r["q_idx"] for r in rows], dtype=np.float32)
+    w = np.array([r["w"] for r in rows], dtype=np.float32)
+    sc = oracle.indexer_scores(b, q_idx, "f32", w, k, "f32", None, 2, 2, ld=5)
+    for i, r in enumerate(rows):
+        exp = np.array([float(x) for x in r["scores"]])
+        assert np.array_equal(sc[i], exp), (i, sc[i], exp)
+        for K, want in r["topk"].items():
+            K = int(K)
+            idx = oracle.topk(b, sc, K)
+            assert idx[i].tolist() == want, (i, K, idx[i])
+
+
+def test_golden_attention():
+    g = _golden()
+    a = g["attention"]
+    b, _, bt, n_blocks = _golden_batch(g, [g["rows"][0]["pos"]])
+    page = g["page"]
+    kc = np.full((n_blocks, page, 2), np.nan, dtype=np.float32)
+    vc = np.full((n_blocks, page, 1), np.nan, dtype=np.float32)
+    for s, row in a["k_logical"].items():
+        s = int(s)
+        kc[bt[0, s // page], s % page] = row
+        vc[bt[0, s // page], s % page] = a["v_logical"][str(s)]
+    idx = np.array([a["selected"]], dtype=np.int32)
+    q = np.array([a["q"]], dtype=np.float32)
+    out, lse = oracle.sparse_attn(b, q, "f32", kc, vc, "f32", idx, a["K"], 1, 2, 1, a["scale"])
+    assert abs(out[0, 0, 0] - a["out"][0][0]) < 1e-6
+    assert abs(lse[0, 0] - a["lse"][0]) < 1e-6
+
+
+# ------------------------------------------------------------- library pins
+
+def _tiny(seed=0, L=40, Hi=3, Di=5, Hq=2, D=6, K=7, page=4):
+    return synth.make("c0", seed=seed, L=L, Hi=Hi, Di=Di, Hq=Hq, Dqk=D, Dv=D, K=K, page=page)
+
+
+def test_topk_matches_library_sort_with_many_ties():
+    """Top-K of integer-valued scores (many ties) equals a lexsort by
+    (score descending, position ascending)."""
+    rng = np.random.default_rng(1)
+    n_q, ld, K = 30, 50, 9
+    pos = rng.integers(0, ld, size=n_q).astype(np.int32)
+    scores = rng.integers(-3, 4, size=(n_q, ld)).astype(np.float64)
+    b = oracle.Batch(np.zeros((1, 1), np.int32), [ld], np.zeros(n_q, np.int32), pos, ld)
+    idx = oracle.topk(b, scores, K)
+    for r in range(n_q):
+        n = pos[r] + 1
+        order = np.lexsort((np.arange(n), -scores[r, :n]))
+        want = np.sort(order[:min(K, n)])
+        got = idx[r]
+        assert got[:len(want)].tolist() == want.tolist()
+        assert (got[len(want):] == -1).all()
+
+
+def test_dense_limit_equals_library_causal_attention():
+    """With K >= pos + 1 every earlier position is selected, so the path is
+    dense causal attention: compare with torch's scaled_dot_product_attention
+    (float64, is_causal=True) on the logical (unpaged) tensors."""
+    wl = _tiny(seed=3, L=37, K=64)
+    b = oracle.Batch.of(wl)
+    sc = oracle.indexer_scores(b, wl.q_idx, "f32", wl.w, wl.k_idx, "f32", None, wl.Hi, wl.Di, 37)
+    idx = oracle.topk(b, sc, wl.K)
+    out, lse = oracle.sparse_attn(b, wl.q, "f32", wl.k, wl.v, "f32", idx, wl.K, wl.Hq, wl.Dqk,
+                                  wl.Dv, wl.scale)
+    L = 37
+    rows_k = np.stack([wl.k[wl.block_table[0, s // wl.page], s % wl.page] for s in range(L)])
+    rows_v = np.stack([wl.v[wl.block_table[0, s // wl.page], s % wl.page] for s in range(L)])
+    q = torch.from_numpy(wl.q.astype(np.float64)).transpose(0, 1)      # [Hq, L, D]
+    kk = torch.from_numpy(rows_k.astype(np.float64))[None].expand(wl.Hq, L, wl.Dqk)
+    vv = torch.from_numpy(rows_v.astype(np.float64))[None].expand(wl.Hq, L, wl.Dv)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=True,
+                                                           scale=wl.scale)
+    assert np.abs(out - ref.transpose(0, 1).numpy()).max() < 1e-12
+    # log-sum-exp against torch.logsumexp over the causal logits
+    z = (q @ kk.transpose(1, 2)) * wl.scale
+    z = z.masked_fill(torch.ones(L, L, dtype=torch.bool).triu(1), float("-inf"))
+    assert np.abs(lse - torch.logsumexp(z, -1).transpose(0, 1).numpy()).max() < 1e-12
+
+
+def test_sparse_attention_equals_masked_library_attention():
+    """Attention over a Top-K set equals dense attention with every other
+    position masked out (torch SDPA with a boolean mask)."""
+    wl = _tiny(seed=4, L=33, K=5)
+    b = oracle.Batch.of(wl)
+    sc = oracle.indexer_scores(b, wl.q_idx, "f32", wl.w, wl.k_idx, "f32", None, wl.Hi, wl.Di, 33)
+    idx = oracle.topk(b, sc, wl.K)
+    out, _ = oracle.sparse_attn(b, wl.q, "f32", wl.k, wl.v, "f32", idx, wl.K, wl.Hq, wl.Dqk,
+                                wl.Dv, wl.scale)
+    L = 33
+    mask = torch.zeros(L, L, dtype=torch.bool)
+    for r in range(L):
+        for s in idx[r]:
+            if s >= 0:
+                mask[r, s] = True
+    rows_k = np.stack([wl.k[wl.block_table[0, s // wl.page], s % wl.page] for s in range(L)])
+    rows_v = np.stack([wl.v[wl.block_table[0, s // wl.page], s % wl.page] for s in range(L)])
+    q = torch.from_numpy(wl.q.astype(np.float64)).transpose(0, 1)
+    kk = torch.from_numpy(rows_k.astype(np.float64))[None].expand(wl.Hq, L, wl.Dqk)
+    vv = torch.from_numpy(rows_v.astype(np.float64))[None].expand(wl.Hq, L, wl.Dv)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=mask,
+                                                           scale=wl.scale)
+    assert np.abs(out - ref.transpose(0, 1).numpy()).max() < 1e-12
+
+
+def test_single_head_unit_weight_is_argtopk_of_dot_products():
+    """H=1, w=1 and all dot products positive: the score is the dot product
+    itself, so the selection is numpy's arg-top-K of q.k (ties excluded)."""
+    rng = np.random.default_rng(7)
+    L, D, K, page = 50, 4, 8, 8
+    keys = rng.uniform(0.5, 1.5, size=(L, D)).astype(np.float32)
+    qi = rng.uniform(0.5, 1.5, size=(L, 1, D)).astype(np.float32)
+    bt = np.arange((L + page - 1) // page, dtype=np.int32)[::-1].copy()[None]
+    kc = np.full((bt.size, page, D), np.nan, dtype=np.float32)
+    for s in range(L):
+        kc[bt[0, s // page], s % page] = keys[s]
+    b = oracle.Batch(bt, [L], np.zeros(L, np.int32), np.arange(L), page)
+    sc = oracle.indexer_scores(b, qi, "f32", np.ones((L, 1), np.float32), kc, "f32", None, 1, D, L)
+    idx = oracle.topk(b, sc, K)
+    for r in range(K, L):
+        dots = keys[: r + 1].astype(np.float64) @ qi[r, 0].astype(np.float64)
+        want = np.sort(np.argsort(-dots, kind="stable")[:K])
+        assert idx[r].tolist() == want.tolist()
+
+
+# -------------------------------------------------------------- closed forms
+
+def test_first_position_returns_its_value_row():
+    """t = 0 selects only position 0, so the output is v[0] exactly."""
+    wl = _tiny(seed=5)
+    b = oracle.Batch.of(wl)
+    idx = np.full((wl.n_q, wl.K), -1, np.int32)
+    idx[:, 0] = 0
+    out, lse = oracle.sparse_attn(b, wl.q, "f32", wl.k, wl.v, "f32", idx, wl.K, wl.Hq, wl.Dqk,
+                                  wl.Dv, wl.scale)
+    v0 = wl.v[wl.block_table[0, 0], 0].astype(np.float64)
+    assert np.array_equal(out, np.broadcast_to(v0, out.shape))
+
+
+def test_identical_keys_give_mean_of_values():
+    """All selected key rows equal -> uniform softmax -> mean of the values."""
+    wl = _tiny(seed=6, L=20, K=6)
+    kc = wl.k.copy()
+    kc[:] = kc[wl.block_table[0, 0], 0]
+    b = oracle.Batch.of(wl)
+    idx = np.tile(np.array([1, 3, 4, 9, 10, 11], np.int32), (wl.n_q, 1))
+    out, lse = oracle.sparse_attn(b, wl.q, "f32", kc, wl.v, "f32", idx, 6, wl.Hq, wl.Dqk,
+                                  wl.Dv, wl.scale)
+    vs = np.stack([wl.v[wl.block_table[0, s // wl.page], s % wl.page] for s in idx[0]])
+    assert np.abs(out - vs.astype(np.float64).mean(0)).max() < 1e-13
+
+
+def test_zero_weights_select_lowest_positions():
+    """w = 0 makes every score 0: all ties, so the K lowest positions win."""
+    wl = _tiny(seed=8, L=30, K=4)
+    b = oracle.Batch.of(wl)
+    sc = oracle.indexer_scores(b, wl.q_idx, "f32", np.zeros_like(wl.w), wl.k_idx, "f32", None,
+                               wl.Hi, wl.Di, 30)
+    for r in range(30):
+        assert (sc[r, : r + 1] == 0).all() and np.isneginf(sc[r, r + 1:]).all()
+    idx = oracle.topk(b, sc, 4)
+    for r in range(30):
+        n = min(4, r + 1)
+        assert idx[r, :n].tolist() == list(range(n))
+
+
+def test_per_token_scale_and_fp8_dequantisation():
+    """FP8 keys with per-token scale c: score equals the fp32 score of the
+    dequantised keys code*c (checked against keys decoded by torch)."""
+    wl = synth.make("c1", batch=2, ctx=70, Hi=3, Di=16, Hq=2, Dqk=8, Dv=4, K=5)
+    b = oracle.Batch.of(wl)
+    sc = oracle.indexer_scores(b, wl.q_idx, "bf16", wl.w, wl.k_idx, "e4m3", wl.k_scale, wl.Hi,
+                               wl.Di, wl.max_ctx)
+    deq = (torch.from_numpy(wl.k_idx).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+           * wl.k_scale.astype(np.float64)[..., None])
+    sc2 = oracle.indexer_scores(b, wl.q_idx, "bf16", wl.w, deq.astype(np.float32), "f32", None,
+                                wl.Hi, wl.Di, wl.max_ctx)
+    # dequantised value code*scale is exact in fp64 but rounded in fp32
+    assert np.allclose(sc, sc2, rtol=1e-6, atol=1e-9)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_page_placement_does_not_change_results():
+    wl = synth.make("c1", batch=3, ctx=150, Hi=4, Di=16, Hq=2, Dqk=12, Dv=8, K=10)
+    wl2 = synth.permute_pages(wl, seed=11)
+    assert not np.array_equal(wl.block_table, wl2.block_table)
+    r1 = oracle.run(wl)
+    r2 = oracle.run(wl2)
+    for a, c in zip(r1, r2):
+        assert np.array_equal(a, c, equal_nan=True)
+
+
+def test_selected_index_order_does_not_change_attention():
+    wl = _tiny(seed=9, L=25, K=6)
+    b = oracle.Batch.of(wl)
+    sc = oracle.indexer_scores(b, wl.q_idx, "f32", wl.w, wl.k_idx, "f32", None, wl.Hi, wl.Di, 25)
+    idx = oracle.topk(b, sc, wl.K)
+    out, lse = oracle.sparse_attn(b, wl.q, "f32", wl.k, wl.v, "f32", idx, wl.K, wl.Hq, wl.Dqk,
+                                  wl.Dv, wl.scale)
+    rng = np.random.default_rng(0)
+    idx2 = np.stack([rng.permutation(r) for r in idx])
+    out2, lse2 = oracle.sparse_attn(b, wl.q, "f32", wl.k, wl.v, "f32", idx2, wl.K, wl.Hq, wl.Dqk,
+                                    wl.Dv, wl.scale)
+    assert np.abs(out - out2).max() < 1e-13 and np.abs(lse - lse2).max() < 1e-13
+
+
+def test_permuting_key_positions_permutes_selection():
+    """Swapping the content of two key positions (indexer key and K/V row)
+    swaps them in the selected set for a query that sees both."""
+    wl = _tiny(seed=10, L=24, K=5)
+    b = oracle.Batch.of(wl)
+    r = 23
+    sc = oracle.indexer_scores(b, wl.q_idx, "f32", wl.w, wl.k_idx, "f32", None, wl.Hi, wl.Di, 24)
+    idx = oracle.topk(b, sc, wl.K)
+    a = int(idx[r, 0])
+    c = next(s for s in range(24) if s not in idx[r])
+    wl2 = synth.make("c0", seed=10, L=24, Hi=3, Di=5, Hq=2, Dqk=6, Dv=6, K=5, page=4)
+    for arr in (wl2.k_idx, wl2.k, wl2.v):
+        pa = (wl2.block_table[0, a // 4], a % 4)
+        pc = (wl2.block_table[0, c // 4], c % 4)
+        tmp = arr[pa].copy()
+        arr[pa] = arr[pc]
+        arr[pc] = tmp
+    sc2 = oracle.indexer_scores(b, wl2.q_idx, "f32", wl2.w, wl2.k_idx, "f32", None, 3, 5, 24)
+    idx2 = oracle.topk(b, sc2, 5)
+    want = sorted(c if s == a else s for s in idx[r])
+    assert idx2[r].tolist() == want
+    o1, _ = oracle.sparse_attn(b, wl.q, "f32", wl.k, wl.v, "f32", idx[[r]], 5, 2, 6, 6, wl.scale,
+                               rows=[r])
+    o2, _ = oracle.sparse_attn(b, wl2.q, "f32", wl2.k, wl2.v, "f32", idx2[[r]], 5, 2, 6, 6,
+                               wl.scale, rows=[r])
+    assert np.abs(o1 - o2).max() < 1e-13
+
+
+def test_rows_subset_equals_full_run():
+    wl = synth.make("c4", n_req=4, n_prefill=1, chunk=40, ctx_lo=60, ctx_hi=300, Hi=4, Di=16,
+                    Hq=2, Dqk=12, Dv=8, K=16)
+    full = oracle.run(wl)
+    rows = [0, 3, wl.n_q - 1, 5]
+    part = oracle.run(wl, rows=rows)
+    for a, c in zip(full, part):
+        assert np.array_equal(a[rows], c, equal_nan=True)

@@ -1,0 +1,54 @@
+"""The input generator's format encoders agree with torch's conversions."""
+import numpy as np
+import torch
+
+import synth
+
+
+def test_e4m3_encoder_matches_torch_rounding():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(20000) * 50, rng.standard_normal(5000) * 0.01,
+                        np.array([448.0, -448.0, 0.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -11,
+                                  1.0625, 1.1875, 240.0, 232.0])]).astype(np.float32)
+    x = np.clip(x, -448, 448)
+    got = synth.f32_to_e4m3_bits(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # torch keeps the sign of values that round to zero; the generator writes +0
+    zero = (ref & 0x7F) == 0
+    assert np.array_equal(got[~zero], ref[~zero])
+    assert (got[zero] == 0).all()
+
+
+def test_bf16_encoder_matches_torch_rounding():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal(50000) * 10.0 ** rng.integers(-20, 20, 50000)).astype(np.float32)
+    got = synth.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_workload_structure():
+    wl = synth.make("c4", n_req=6, n_prefill=2, chunk=50, ctx_lo=64, ctx_hi=400, Hi=2, Di=16,
+                    Hq=2, Dqk=8, Dv=4, K=8)
+    assert wl.n_q == 4 + 2 * 50
+    for i in range(wl.n_seq):
+        rows = np.nonzero(wl.q_seq == i)[0]
+        assert wl.q_pos[rows].max() == wl.ctx_len[i] - 1
+        nb = (wl.ctx_len[i] + wl.page - 1) // wl.page
+        assert (wl.block_table[i, :nb] >= 0).all() and (wl.block_table[i, nb:] == -1).all()
+    used = wl.block_table[wl.block_table >= 0]
+    assert len(np.unique(used)) == len(used)
+
+
+def test_planted_keys_raise_every_head_by_three_sigma():
+    wl = synth.make("c3", batch=2, ctx=2000, K=64)
+    from synth import _bf16_bits_to_f32
+    for i in range(2):
+        pos = wl.planted[i]
+        assert len(pos) == 20
+        q = _bf16_bits_to_f32(wl.q_idx[i]).astype(np.float64)
+        deq = torch.from_numpy(wl.k_idx).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        rows = [wl.block_table[i, p // 64] * 64 + p % 64 for p in pos]
+        k = deq.reshape(-1, wl.Di)[rows] * wl.k_scale.reshape(-1)[rows, None]
+        z = (k @ q.T) / np.linalg.norm(q, axis=1)      # per-head logit in units of sigma
+        assert z.mean() > 2.0                          # 3 sigma shift + N(0,1) noise
