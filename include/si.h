@@ -1,0 +1,189 @@
+/*
+ * si.h -- C ABI of libsi: indexer-driven Top-K sparse attention on GB300.
+ *
+ * The operation follows the page "Day0 Inference Support and Performance
+ * Optimization for New Architecture LLMs" (Baidu Cloud):
+ *   section 2.2  -- a lightweight indexer scores each query against all earlier
+ *                   positions, the per-head scores are aggregated with head
+ *                   weights, the Top-K positions are kept, and the sparse
+ *                   attention core reads only the KV rows at those positions;
+ *   section 4.1  -- scoring, head weighting and Top-K form one fused operator
+ *                   that reads the paged K-cache directly and never stores the
+ *                   full score matrix;
+ *   section 4.2  -- the attention core gathers the selected rows from the main
+ *                   KV cache by the position list the indexer produced.
+ * The score of query row t against key position s is
+ *   score(t,s) = k_scale[s] * sum_h w[t,h] * ReLU(q_idx[t,h,:] . k_idx[s,:])
+ * (k_scale is the per-token FP8 dequantisation scale; it is positive, so
+ * applying it after the ReLU equals scoring the dequantised key).
+ *
+ * Conventions for every entry point
+ *   * All pointers named "device" are CUDA device pointers owned by the
+ *     caller; the library never allocates, frees or retains them.
+ *   * Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  A call that returns SI_OK has only enqueued work.
+ *   * Host-side argument errors return a non-zero status before anything is
+ *     launched.  A failed launch returns SI_ERR_CUDA.  si_last_error() gives
+ *     a human-readable detail for the calling thread.
+ *   * Device-side problems (a block-table entry or a selected index out of
+ *     range, a bounded wait that gave up) never fault: the offending access is
+ *     skipped and a bit is OR-ed into the sticky status word that lives in the
+ *     first 16 bytes of the workspace.  Zero the workspace once after
+ *     allocating it; read the word with si_workspace_status().
+ *   * The library holds no global mutable state; calls from several host
+ *     threads are safe as long as they use different workspaces.
+ *
+ * Paged caches: logical position s of sequence q is physical row
+ *   block_table[q * max_blocks + s / page_size] * page_size + s % page_size
+ * of a cache laid out [n_blocks, page_size, row_stride] (section 4.1's paged
+ * K-cache).  The indexer-key cache and the KV cache share the block table.
+ */
+#ifndef SI_H_
+#define SI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SI_VERSION 1
+
+typedef enum si_status {
+    SI_OK = 0,
+    SI_ERR_INVALID_ARG = 1, /* null pointer, bad size or inconsistent shapes */
+    SI_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+    SI_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
+    SI_ERR_CUDA = 4,        /* a CUDA call or launch failed */
+    SI_ERR_DEVICE = 5       /* si_workspace_status found device-side flags */
+} si_status;
+
+typedef enum si_dtype {
+    SI_F32 = 0,  /* IEEE float32 */
+    SI_BF16 = 1, /* bfloat16 */
+    SI_E4M3 = 2  /* OCP FP8 e4m3 (finite, max 448) */
+} si_dtype;
+
+/* Device status flags (sticky, OR-ed into the workspace status word). */
+#define SI_DEVFLAG_BAD_BLOCK 0x1u /* block-table entry outside [0, n_blocks) */
+#define SI_DEVFLAG_BAD_INDEX 0x2u /* selected index outside [0, pos] (not -1) */
+#define SI_DEVFLAG_TIMEOUT 0x4u   /* a bounded on-chip wait gave up */
+
+/* Workspace must be at least this aligned. */
+#define SI_WORKSPACE_ALIGN 256
+
+/* Ragged batch of query rows over paged sequences (section 2.2: each query
+ * looks at all of its sequence's earlier positions). */
+typedef struct si_batch {
+    const int32_t *block_table; /* device [n_seq, max_blocks] physical page ids */
+    const int32_t *ctx_len;     /* device [n_seq] cached positions per sequence */
+    const int32_t *q_seq;       /* device [n_q] sequence of each query row */
+    const int32_t *q_pos;       /* device [n_q] absolute position of the row; it
+                                   may look at key positions 0..q_pos inclusive.
+                                   Requires q_pos < ctx_len[q_seq]. */
+    int32_t n_seq;
+    int32_t max_blocks;
+    int32_t n_q;                /* number of query rows (0 is allowed: no-op) */
+    int32_t page_size;          /* rows per page, 1..1024 */
+    int32_t max_ctx;            /* host-known bound: q_pos + 1 <= max_ctx for all
+                                   rows; sizes grids, scores and workspaces */
+    int32_t n_blocks;           /* physical pages in each cache */
+} si_batch;
+
+/* One paged cache: [n_blocks, page_size, row_stride] elements of dtype. */
+typedef struct si_paged {
+    const void *data;    /* device; 16-byte aligned */
+    const float *scale;  /* device [n_blocks, page_size] per-row dequantisation
+                            scale (> 0), or NULL for 1 */
+    si_dtype dtype;
+    int32_t row_dim;     /* elements used per row */
+    int64_t row_stride;  /* elements between consecutive rows, >= row_dim */
+} si_paged;
+
+/* Indexer operands (section 2.2: lightweight multi-head indexer; section 5.1
+ * stores its keys in FP8). */
+typedef struct si_indexer {
+    const void *q;       /* device [n_q, n_heads, head_dim], SI_F32 or SI_BF16 */
+    si_dtype q_dtype;
+    const float *w;      /* device [n_q, n_heads] head weights */
+    int32_t n_heads;     /* 1..128 */
+    int32_t head_dim;    /* 1..256 */
+    si_paged k;          /* indexer keys: SI_F32, SI_BF16 or SI_E4M3 (+scale) */
+} si_indexer;
+
+/* Sparse attention operands: one shared KV head (MQA / latent KV). */
+typedef struct si_attention {
+    const void *q;       /* device [n_q, n_heads, d_qk], SI_F32 or SI_BF16 */
+    si_dtype q_dtype;
+    int32_t n_heads;     /* query heads sharing each KV row, 1..256 */
+    int32_t d_qk;        /* logit dims, 1..1024 */
+    int32_t d_v;         /* value dims, 1..1024 */
+    si_paged k;          /* key rows: row_dim >= d_qk, same dtype as q */
+    si_paged v;          /* value rows: row_dim >= d_v; may alias k (the value
+                            is then the first d_v entries of the key row) */
+    float softmax_scale; /* logits are softmax_scale * q . k */
+} si_attention;
+
+typedef enum si_op {
+    SI_OP_INDEXER = 0,
+    SI_OP_TOPK = 1,
+    SI_OP_ATTN = 2,
+    SI_OP_FUSED = 3
+} si_op;
+
+/* Bytes of workspace the operation `op` wants for this batch (the status
+ * word included).  For SI_OP_FUSED this is the size that scores all rows in
+ * one strip, capped at 256 MiB; any workspace of at least
+ * si_workspace_min(SI_OP_FUSED, ...) works, with fewer rows per strip.
+ * Arguments not used by `op` may be NULL.  Returns 0 on invalid arguments. */
+size_t si_workspace_size(si_op op, const si_batch *b, const si_indexer *ix,
+                         const si_attention *at, int32_t k_top);
+size_t si_workspace_min(si_op op, const si_batch *b, const si_indexer *ix,
+                        const si_attention *at, int32_t k_top);
+
+/* Indexer scores (section 2.2, first two bullets).
+ * scores: device float [n_q, ld_scores], ld_scores >= max_ctx.  Row r gets
+ * score(r, s) for s <= q_pos[r] and -inf for q_pos[r] < s < ld_scores. */
+si_status si_indexer_scores(const si_batch *b, const si_indexer *ix, float *scores,
+                            int64_t ld_scores, void *ws, size_t ws_bytes, void *stream);
+
+/* Top-K selection (section 2.2, second bullet), never a full sort.
+ * idx: device int32 [n_q, k_top].  Row r receives the k_top positions with
+ * the largest scores among 0..q_pos[r] (equal scores: the lower position
+ * wins; -0 equals +0), in ascending order; if q_pos[r] + 1 <= k_top it
+ * receives all of them followed by -1 padding.  Scores must not be NaN. */
+si_status si_topk(const si_batch *b, const float *scores, int64_t ld_scores, int32_t k_top,
+                  int32_t *idx, void *ws, size_t ws_bytes, void *stream);
+
+/* Sparse attention over selected rows (section 2.2 third bullet; 4.2).
+ * idx: device int32 [n_q, k_top], entries -1 are skipped.
+ * out: device [n_q, n_heads, d_v] of out_dtype (SI_F32 or SI_BF16),
+ *   out[r,h] = sum_j softmax_j(softmax_scale * q[r,h] . k[idx_j]) * v[idx_j];
+ *   a row with no valid index gets zeros.
+ * lse: device float [n_q, n_heads] natural-log sum-exp of the logits, or NULL. */
+si_status si_sparse_attn(const si_batch *b, const si_attention *at, const int32_t *idx,
+                         int32_t k_top, void *out, si_dtype out_dtype, float *lse, void *ws,
+                         size_t ws_bytes, void *stream);
+
+/* The whole path in one call (section 4.1 fused indexer + 4.2 gather
+ * attention): scores -> Top-K -> attention for every query row.  Scores
+ * live only in the workspace, a strip of rows at a time; idx receives the
+ * selected positions exactly as si_topk would write them. */
+si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_attention *at,
+                          int32_t k_top, int32_t *idx, void *out, si_dtype out_dtype,
+                          float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, then reads the sticky device status word of `ws`
+ * into *flags (SI_DEVFLAG_*).  Returns SI_ERR_DEVICE if any flag is set. */
+si_status si_workspace_status(const void *ws, uint32_t *flags, void *stream);
+
+const char *si_status_string(si_status s);
+const char *si_last_error(void);
+int32_t si_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SI_H_ */

@@ -1,0 +1,340 @@
+// si_api.cu -- the extern "C" boundary of libsi: argument validation,
+// workspace layout, kernel selection and the fused call.
+//
+// The path is the "select first, compute later" sparse attention of "Day0
+// Inference Support and Performance Optimization for New Architecture LLMs"
+// (section 2.2), with the fused indexer of section 4.1 and the index-based
+// gather of section 4.2.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "si_common.cuh"
+#include "si_internal.h"
+
+namespace {
+
+thread_local char g_err[512];
+
+si_status fail(si_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+si_status fail(si_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+si_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(SI_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr size_t kFusedCap = (size_t)256 << 20;  // preferred fused workspace cap
+constexpr int kMaxTop = 16384;
+
+si_status check_batch(const si_batch *b)
+{
+    if (!b)
+        return fail(SI_ERR_INVALID_ARG, "batch is NULL");
+    if (b->n_q < 0)
+        return fail(SI_ERR_INVALID_ARG, "n_q = %d < 0", b->n_q);
+    if (b->n_q == 0)
+        return SI_OK;
+    if (!b->block_table || !b->ctx_len || !b->q_seq || !b->q_pos)
+        return fail(SI_ERR_INVALID_ARG, "batch has a NULL device array");
+    if (b->n_seq < 1 || b->max_blocks < 1 || b->n_blocks < 1)
+        return fail(SI_ERR_INVALID_ARG, "n_seq, max_blocks and n_blocks must be >= 1");
+    if (b->page_size < 1 || b->page_size > 1024)
+        return fail(SI_ERR_INVALID_ARG, "page_size %d outside 1..1024", b->page_size);
+    if (b->max_ctx < 1 || (int64_t)b->max_ctx > (int64_t)b->max_blocks * b->page_size)
+        return fail(SI_ERR_INVALID_ARG, "max_ctx %d outside 1..max_blocks*page_size", b->max_ctx);
+    if (b->max_ctx > (1 << 26))
+        return fail(SI_ERR_UNSUPPORTED, "max_ctx %d above 2^26", b->max_ctx);
+    return SI_OK;
+}
+
+si_status check_paged(const si_paged &p, const char *name, int need_dim)
+{
+    if (!p.data)
+        return fail(SI_ERR_INVALID_ARG, "%s.data is NULL", name);
+    if (!aligned(p.data, 16))
+        return fail(SI_ERR_INVALID_ARG, "%s.data is not 16-byte aligned", name);
+    if (p.dtype != SI_F32 && p.dtype != SI_BF16 && p.dtype != SI_E4M3)
+        return fail(SI_ERR_INVALID_ARG, "%s.dtype %d unknown", name, (int)p.dtype);
+    if (p.row_dim < need_dim)
+        return fail(SI_ERR_INVALID_ARG, "%s.row_dim %d < %d", name, p.row_dim, need_dim);
+    if (p.row_stride < p.row_dim)
+        return fail(SI_ERR_INVALID_ARG, "%s.row_stride %lld < row_dim %d", name,
+                    (long long)p.row_stride, p.row_dim);
+    return SI_OK;
+}
+
+si_status check_indexer(const si_indexer *ix)
+{
+    if (!ix)
+        return fail(SI_ERR_INVALID_ARG, "indexer operands are NULL");
+    if (!ix->q || !ix->w)
+        return fail(SI_ERR_INVALID_ARG, "indexer q or w is NULL");
+    if (ix->q_dtype != SI_F32 && ix->q_dtype != SI_BF16)
+        return fail(SI_ERR_INVALID_ARG, "indexer q dtype must be f32 or bf16");
+    if (ix->n_heads < 1 || ix->n_heads > 128)
+        return fail(SI_ERR_INVALID_ARG, "indexer n_heads %d outside 1..128", ix->n_heads);
+    if (ix->head_dim < 1 || ix->head_dim > 256)
+        return fail(SI_ERR_INVALID_ARG, "indexer head_dim %d outside 1..256", ix->head_dim);
+    return check_paged(ix->k, "indexer k", ix->head_dim);
+}
+
+si_status check_attention(const si_attention *at)
+{
+    if (!at)
+        return fail(SI_ERR_INVALID_ARG, "attention operands are NULL");
+    if (!at->q)
+        return fail(SI_ERR_INVALID_ARG, "attention q is NULL");
+    if (at->q_dtype != SI_F32 && at->q_dtype != SI_BF16)
+        return fail(SI_ERR_INVALID_ARG, "attention q dtype must be f32 or bf16");
+    if (at->n_heads < 1 || at->n_heads > 256)
+        return fail(SI_ERR_INVALID_ARG, "attention n_heads %d outside 1..256", at->n_heads);
+    if (at->d_qk < 1 || at->d_qk > 1024 || at->d_v < 1 || at->d_v > 1024)
+        return fail(SI_ERR_INVALID_ARG, "attention d_qk/d_v outside 1..1024");
+    si_status s = check_paged(at->k, "attention k", at->d_qk);
+    if (s != SI_OK)
+        return s;
+    s = check_paged(at->v, "attention v", at->d_v);
+    if (s != SI_OK)
+        return s;
+    if (at->k.dtype != at->q_dtype || at->v.dtype != at->q_dtype)
+        return fail(SI_ERR_UNSUPPORTED, "attention q, k and v must share one dtype (f32 or bf16)");
+    return SI_OK;
+}
+
+si_status check_ws(void *ws, size_t ws_bytes, size_t need)
+{
+    if (!ws)
+        return fail(SI_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(ws, SI_WORKSPACE_ALIGN))
+        return fail(SI_ERR_WORKSPACE, "workspace is not %d-byte aligned", SI_WORKSPACE_ALIGN);
+    if (ws_bytes < need)
+        return fail(SI_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+    return SI_OK;
+}
+
+si_status check_k(int32_t k_top)
+{
+    if (k_top < 1 || k_top > kMaxTop)
+        return fail(SI_ERR_INVALID_ARG, "k_top %d outside 1..%d", k_top, kMaxTop);
+    return SI_OK;
+}
+
+int64_t scores_ld(const si_batch *b) { return (int64_t)round_up((size_t)b->max_ctx, 64); }
+
+// Sub-batch of rows [r0, r0 + n) (device pointers advanced).
+si_batch row_slice(const si_batch &b, int32_t r0, int32_t n)
+{
+    si_batch s = b;
+    s.q_seq = b.q_seq + r0;
+    s.q_pos = b.q_pos + r0;
+    s.n_q = n;
+    return s;
+}
+
+size_t dtype_bytes(si_dtype t) { return t == SI_F32 ? 4 : (t == SI_BF16 ? 2 : 1); }
+
+// Indexer operands of rows [r0, ...): query and head-weight pointers advanced.
+si_indexer indexer_slice(const si_indexer &ix, int32_t r0)
+{
+    si_indexer s = ix;
+    s.q = static_cast<const char *>(ix.q) +
+          (size_t)r0 * ix.n_heads * ix.head_dim * dtype_bytes(ix.q_dtype);
+    s.w = ix.w + (size_t)r0 * ix.n_heads;
+    return s;
+}
+
+unsigned int *status_word(void *ws) { return reinterpret_cast<unsigned int *>(ws); }
+
+si_status run_indexer(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
+                      unsigned int *st, cudaStream_t s)
+{
+    cudaError_t e = si::launch_indexer_generic(b, ix, scores, ld, st, s);
+    return e == cudaSuccess ? SI_OK : cuda_fail(e, "indexer launch");
+}
+
+si_status run_topk(const si_batch &b, const float *scores, int64_t ld, int k_top, int32_t *idx,
+                   unsigned int *st, cudaStream_t s)
+{
+    cudaError_t e = si::launch_topk(b, scores, ld, k_top, idx, st, s);
+    return e == cudaSuccess ? SI_OK : cuda_fail(e, "top-k launch");
+}
+
+si_status run_attn(const si_batch &b, const si_attention &at, const int32_t *idx, int k_top,
+                   void *out, si_dtype odt, float *lse, unsigned int *st, cudaStream_t s)
+{
+    cudaError_t e = si::launch_attn_generic(b, at, idx, k_top, out, odt, lse, st, s);
+    return e == cudaSuccess ? SI_OK : cuda_fail(e, "attention launch");
+}
+
+size_t ws_need(si_op op, const si_batch *b, const si_indexer *ix, const si_attention *at,
+               int32_t k_top, bool minimal)
+{
+    (void)ix;
+    (void)at;
+    (void)k_top;
+    size_t n = si::kStatusBytes;
+    if (op == SI_OP_FUSED && b->n_q > 0) {
+        const size_t row_bytes = (size_t)scores_ld(b) * sizeof(float);
+        size_t rows = minimal ? 1 : (size_t)b->n_q;
+        if (!minimal && rows * row_bytes > kFusedCap)
+            rows = std::max<size_t>(1, kFusedCap / row_bytes);
+        n += round_up(rows * row_bytes, 256);
+    }
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t si_workspace_size(si_op op, const si_batch *b, const si_indexer *ix,
+                         const si_attention *at, int32_t k_top)
+{
+    if (check_batch(b) != SI_OK)
+        return 0;
+    return ws_need(op, b, ix, at, k_top, false);
+}
+
+size_t si_workspace_min(si_op op, const si_batch *b, const si_indexer *ix,
+                        const si_attention *at, int32_t k_top)
+{
+    if (check_batch(b) != SI_OK)
+        return 0;
+    return ws_need(op, b, ix, at, k_top, true);
+}
+
+si_status si_indexer_scores(const si_batch *b, const si_indexer *ix, float *scores,
+                            int64_t ld_scores, void *ws, size_t ws_bytes, void *stream)
+{
+    si_status st = check_batch(b);
+    if (st != SI_OK || b->n_q == 0)
+        return st;
+    if ((st = check_indexer(ix)) != SI_OK)
+        return st;
+    if (!scores)
+        return fail(SI_ERR_INVALID_ARG, "scores is NULL");
+    if (ld_scores < b->max_ctx)
+        return fail(SI_ERR_INVALID_ARG, "ld_scores %lld < max_ctx %d", (long long)ld_scores,
+                    b->max_ctx);
+    if ((st = check_ws(ws, ws_bytes, ws_need(SI_OP_INDEXER, b, ix, nullptr, 0, true))) != SI_OK)
+        return st;
+    return run_indexer(*b, *ix, scores, ld_scores, status_word(ws), (cudaStream_t)stream);
+}
+
+si_status si_topk(const si_batch *b, const float *scores, int64_t ld_scores, int32_t k_top,
+                  int32_t *idx, void *ws, size_t ws_bytes, void *stream)
+{
+    si_status st = check_batch(b);
+    if (st != SI_OK || b->n_q == 0)
+        return st;
+    if ((st = check_k(k_top)) != SI_OK)
+        return st;
+    if (!scores || !idx)
+        return fail(SI_ERR_INVALID_ARG, "scores or idx is NULL");
+    if (ld_scores < b->max_ctx)
+        return fail(SI_ERR_INVALID_ARG, "ld_scores %lld < max_ctx %d", (long long)ld_scores,
+                    b->max_ctx);
+    if ((st = check_ws(ws, ws_bytes, ws_need(SI_OP_TOPK, b, nullptr, nullptr, k_top, true))) !=
+        SI_OK)
+        return st;
+    return run_topk(*b, scores, ld_scores, k_top, idx, status_word(ws), (cudaStream_t)stream);
+}
+
+si_status si_sparse_attn(const si_batch *b, const si_attention *at, const int32_t *idx,
+                         int32_t k_top, void *out, si_dtype out_dtype, float *lse, void *ws,
+                         size_t ws_bytes, void *stream)
+{
+    si_status st = check_batch(b);
+    if (st != SI_OK || b->n_q == 0)
+        return st;
+    if ((st = check_attention(at)) != SI_OK || (st = check_k(k_top)) != SI_OK)
+        return st;
+    if (!idx || !out)
+        return fail(SI_ERR_INVALID_ARG, "idx or out is NULL");
+    if (out_dtype != SI_F32 && out_dtype != SI_BF16)
+        return fail(SI_ERR_INVALID_ARG, "out dtype must be f32 or bf16");
+    if ((st = check_ws(ws, ws_bytes, ws_need(SI_OP_ATTN, b, nullptr, at, k_top, true))) != SI_OK)
+        return st;
+    return run_attn(*b, *at, idx, k_top, out, out_dtype, lse, status_word(ws),
+                    (cudaStream_t)stream);
+}
+
+si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_attention *at,
+                          int32_t k_top, int32_t *idx, void *out, si_dtype out_dtype,
+                          float *lse, void *ws, size_t ws_bytes, void *stream)
+{
+    si_status st = check_batch(b);
+    if (st != SI_OK || b->n_q == 0)
+        return st;
+    if ((st = check_indexer(ix)) != SI_OK || (st = check_attention(at)) != SI_OK ||
+        (st = check_k(k_top)) != SI_OK)
+        return st;
+    if (!idx || !out)
+        return fail(SI_ERR_INVALID_ARG, "idx or out is NULL");
+    if (out_dtype != SI_F32 && out_dtype != SI_BF16)
+        return fail(SI_ERR_INVALID_ARG, "out dtype must be f32 or bf16");
+    if ((st = check_ws(ws, ws_bytes, ws_need(SI_OP_FUSED, b, ix, at, k_top, true))) != SI_OK)
+        return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    unsigned int *stw = status_word(ws);
+    const int64_t ld = scores_ld(b);
+    const size_t row_bytes = (size_t)ld * sizeof(float);
+    float *scores = reinterpret_cast<float *>(static_cast<char *>(ws) + si::kStatusBytes);
+    const int64_t strip = (int64_t)((ws_bytes - si::kStatusBytes) / row_bytes);
+    for (int64_t r0 = 0; r0 < b->n_q; r0 += strip) {
+        const int32_t n = (int32_t)std::min<int64_t>(strip, b->n_q - r0);
+        const si_batch sb = row_slice(*b, (int32_t)r0, n);
+        const si_indexer si_ = indexer_slice(*ix, (int32_t)r0);
+        if ((st = run_indexer(sb, si_, scores, ld, stw, s)) != SI_OK)
+            return st;
+        if ((st = run_topk(sb, scores, ld, k_top, idx + r0 * k_top, stw, s)) != SI_OK)
+            return st;
+    }
+    return run_attn(*b, *at, idx, k_top, out, out_dtype, lse, stw, s);
+}
+
+si_status si_workspace_status(const void *ws, uint32_t *flags, void *stream)
+{
+    if (!ws || !flags)
+        return fail(SI_ERR_INVALID_ARG, "ws or flags is NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "stream synchronize");
+    e = cudaMemcpy(flags, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "status read");
+    return *flags ? fail(SI_ERR_DEVICE, "device flags 0x%x", *flags) : SI_OK;
+}
+
+const char *si_status_string(si_status s)
+{
+    switch (s) {
+    case SI_OK: return "ok";
+    case SI_ERR_INVALID_ARG: return "invalid argument";
+    case SI_ERR_UNSUPPORTED: return "unsupported";
+    case SI_ERR_WORKSPACE: return "workspace error";
+    case SI_ERR_CUDA: return "cuda error";
+    case SI_ERR_DEVICE: return "device-side flag raised";
+    }
+    return "unknown status";
+}
+
+const char *si_last_error(void) { return g_err; }
+
+int32_t si_version(void) { return SI_VERSION; }
+
+}  // extern "C"

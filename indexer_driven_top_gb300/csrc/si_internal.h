@@ -1,0 +1,22 @@
+// si_internal.h -- launchers shared between the libsi translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "si.h"
+
+namespace si {
+
+// Generic CUDA-core kernels: any supported dtype and shape, fp32 arithmetic.
+cudaError_t launch_indexer_generic(const si_batch &b, const si_indexer &ix, float *scores,
+                                   int64_t ld, unsigned int *st, cudaStream_t s);
+cudaError_t launch_attn_generic(const si_batch &b, const si_attention &at, const int32_t *idx,
+                                int k_top, void *out, si_dtype out_dtype, float *lse,
+                                unsigned int *st, cudaStream_t s);
+
+// Radix select of the k_top best scores per row.
+cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,
+                        int32_t *idx, unsigned int *st, cudaStream_t s);
+
+}  // namespace si

@@ -1,0 +1,97 @@
+"""The C-ABI library loads, exports every symbol include/si.h declares, and
+rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def si():
+    __graft_entry__.build()
+    import indexer_driven_top_gb300 as si
+    return si
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(si_[a-z0-9_]+)\s*\(", txt))
+    return names
+
+
+def test_every_declared_symbol_is_exported(si):
+    names = _declared()
+    assert {"si_indexer_scores", "si_topk", "si_sparse_attn", "si_fused_decode"} <= names
+    lib = si.load()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(si.EXPORTED) <= names
+
+
+def test_version_and_status_strings(si):
+    lib = si.load()
+    assert lib.si_version() == 1
+    assert lib.si_status_string(0) == b"ok"
+    assert lib.si_status_string(3) == b"workspace error"
+
+
+def _batch(si, **kw):
+    b = si.c_batch(1 << 20, 2 << 20, 3 << 20, 4 << 20, 1, 4, 2, 64, 256, 4)
+    for k, v in kw.items():
+        setattr(b, k, v)
+    return b
+
+
+def test_host_validation_rejects_bad_arguments(si):
+    lib = si.load()
+    P = ctypes.c_void_p
+    fake = 1 << 20
+    ws = 256 << 20   # 256-aligned fake device address, never dereferenced
+    # NULL batch
+    assert lib.si_topk(None, P(fake), 256, 8, P(fake), P(ws), 4096, None) == 1
+    # k_top out of range
+    assert lib.si_topk(ctypes.byref(_batch(si)), P(fake), 256, 0, P(fake), P(ws), 4096, None) == 1
+    # ld_scores below max_ctx
+    assert lib.si_topk(ctypes.byref(_batch(si)), P(fake), 100, 8, P(fake), P(ws), 4096, None) == 1
+    assert b"ld_scores" in lib.si_last_error()
+    # max_ctx beyond the block table
+    assert lib.si_topk(ctypes.byref(_batch(si, max_ctx=999)), P(fake), 1024, 8, P(fake), P(ws),
+                       4096, None) == 1
+    # workspace: NULL, misaligned, too small
+    b = ctypes.byref(_batch(si))
+    assert lib.si_topk(b, P(fake), 256, 8, P(fake), None, 4096, None) == 3
+    assert lib.si_topk(b, P(fake), 256, 8, P(fake), P(ws + 16), 4096, None) == 3
+    assert lib.si_topk(b, P(fake), 256, 8, P(fake), P(ws), 16, None) == 3
+    # attention: dtype mismatch and bad dims
+    kp = si.c_paged(fake, None, si.E4M3, 64, 64)
+    at = si.c_attention(fake, si.BF16, 4, 64, 64, kp, kp, 0.125)
+    assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
+                              4096, None) == 2
+    at = si.c_attention(fake, si.BF16, 4, 2000, 64, kp, kp, 0.125)
+    assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
+                              4096, None) == 1
+    # indexer: misaligned key cache, bad head count
+    ix = si.c_indexer(fake, si.BF16, fake, 64, 128, si.c_paged(fake + 3, None, si.E4M3, 128, 128))
+    assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 1
+    ix = si.c_indexer(fake, si.BF16, fake, 0, 128, si.c_paged(fake, None, si.E4M3, 128, 128))
+    assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 1
+    # empty batch is a no-op that succeeds without touching anything
+    assert lib.si_topk(ctypes.byref(_batch(si, n_q=0)), None, 0, 8, None, None, 0, None) == 0
+
+
+def test_workspace_sizes(si):
+    lib = si.load()
+    b = _batch(si)
+    fused = lib.si_workspace_size(3, ctypes.byref(b), None, None, 8)
+    mn = lib.si_workspace_min(3, ctypes.byref(b), None, None, 8)
+    assert fused >= mn >= 256 + 256 * 4
+    assert lib.si_workspace_size(1, None, None, None, 8) == 0

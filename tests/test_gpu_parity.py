@@ -1,0 +1,166 @@
+"""CUDA path vs the CPU oracle on seeded synthetic inputs (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _parity import ATOL_BF16, ATOL_F32, check_topk, max_abs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def si():
+    import __graft_entry__
+    __graft_entry__.build()
+    import indexer_driven_top_gb300 as si
+    return si
+
+
+def _run_separate(si, dw, out_dtype=torch.float32):
+    b = dw.batch
+    ld = b.max_ctx
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, dw.indexer, dw.attention, dw.k_top))
+    scores = torch.empty((dw.n_q, ld), dtype=torch.float32, device="cuda")
+    idx = torch.empty((dw.n_q, dw.k_top), dtype=torch.int32, device="cuda")
+    out = torch.empty((dw.n_q, dw.attention.q.shape[1], dw.attention.d_v), dtype=out_dtype,
+                      device="cuda")
+    lse = torch.empty((dw.n_q, dw.attention.q.shape[1]), dtype=torch.float32, device="cuda")
+    si.indexer_scores(b, dw.indexer, scores, ws)
+    si.topk(b, scores, dw.k_top, idx, ws)
+    si.sparse_attn(b, dw.attention, idx, dw.k_top, out, ws, lse=lse)
+    assert si.workspace_status(ws) == 0
+    return scores.cpu().numpy(), idx.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _run_fused(si, dw, out_dtype=torch.float32, ws_bytes=None):
+    b = dw.batch
+    n = ws_bytes or si.workspace_size(si.OP_FUSED, b, dw.indexer, dw.attention, dw.k_top)
+    ws = si.alloc_workspace(n)
+    idx = torch.empty((dw.n_q, dw.k_top), dtype=torch.int32, device="cuda")
+    out = torch.empty((dw.n_q, dw.attention.q.shape[1], dw.attention.d_v), dtype=out_dtype,
+                      device="cuda")
+    lse = torch.empty((dw.n_q, dw.attention.q.shape[1]), dtype=torch.float32, device="cuda")
+    si.fused_decode(b, dw.indexer, dw.attention, dw.k_top, idx, out, ws, lse=lse)
+    assert si.workspace_status(ws) == 0
+    return idx.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _attn_ref(wl, g_idx, rows=None):
+    return oracle.sparse_attn(oracle.Batch.of(wl), wl.q, wl.kv_dtype, wl.k, wl.v, wl.kv_dtype,
+                              g_idx, wl.K, wl.Hq, wl.Dqk, wl.Dv, wl.scale, rows=rows)
+
+
+def _full_check(si, wl, atol):
+    dw = si.upload(wl)
+    g_sc, g_idx, g_out, g_lse = _run_separate(si, dw)
+    o_sc, o_idx, _, _, _ = oracle.run(wl)
+    # indexer scores: fp32 accumulation vs fp64
+    fin = np.isfinite(o_sc)
+    assert np.array_equal(np.isfinite(g_sc), fin)
+    scale = np.abs(o_sc[fin]).max() + 1e-30
+    assert np.abs(g_sc[fin] - o_sc[fin]).max() <= 1e-5 * scale
+    check_topk(g_idx, o_idx, o_sc, wl.q_pos, wl.K)
+    ref, ref_lse = _attn_ref(wl, g_idx)
+    assert max_abs(g_out, ref) <= atol
+    assert max_abs(g_lse, ref_lse) <= atol
+    f_idx, f_out, f_lse = _run_fused(si, dw)
+    assert np.array_equal(f_idx, g_idx)
+    assert np.array_equal(f_out, g_out)
+    return g_idx, o_idx
+
+
+def test_c0_tiny_prefill_fp32(si):
+    wl = synth.make("c0")
+    g_idx, o_idx = _full_check(si, wl, ATOL_F32)
+    assert np.array_equal(g_idx, o_idx)
+
+
+def test_decode_ragged_bf16_fp8(si):
+    wl = synth.make("c1", batch=3, ctx_list=[3001, 2048, 130], K=2048)
+    _full_check(si, wl, ATOL_BF16)
+
+
+def test_planted_long_decode(si):
+    wl = synth.make("c3", batch=2, ctx=9000, K=256)
+    g_idx, _ = _full_check(si, wl, ATOL_BF16)
+    for i in range(2):       # every planted key is selected (they beat the rest by ~3 sigma)
+        assert np.isin(wl.planted[i], g_idx[i]).mean() > 0.95
+
+
+def test_prefill_chunk_small(si):
+    wl = synth.make("c2", L=300, K=64)
+    _full_check(si, wl, ATOL_BF16)
+
+
+def test_mixed_ragged_batch(si):
+    wl = synth.make("c4", n_req=5, n_prefill=1, chunk=40, ctx_lo=100, ctx_hi=1500, K=128)
+    _full_check(si, wl, ATOL_BF16)
+
+
+def test_fused_small_workspace_uses_strips(si):
+    wl = synth.make("c4", n_req=4, n_prefill=1, chunk=30, ctx_lo=100, ctx_hi=900, K=64)
+    dw = si.upload(wl)
+    a_idx, a_out, _ = _run_fused(si, dw)
+    mn = si.workspace_min(si.OP_FUSED, dw.batch, dw.indexer, dw.attention, wl.K)
+    b_idx, b_out, _ = _run_fused(si, dw, ws_bytes=mn + 3 * 4 * wl.max_ctx)
+    assert np.array_equal(a_idx, b_idx) and np.array_equal(a_out, b_out)
+
+
+def test_topk_exact_on_identical_scores(si):
+    """si_topk and the oracle's Top-K on the same float32 scores agree bit
+    for bit, including heavy ties (integer scores) and -0/+0."""
+    rng = np.random.default_rng(3)
+    n_q, ld = 40, 5000
+    pos = np.concatenate([rng.integers(0, ld, n_q - 4), [0, 9, 10, ld - 1]]).astype(np.int32)
+    sc = rng.integers(-20, 20, size=(n_q, ld)).astype(np.float32)
+    sc[1::3] = rng.standard_normal((len(sc[1::3]), ld)).astype(np.float32)
+    sc[2, :100] = -0.0
+    import indexer_driven_top_gb300 as si_
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    b = si_.Batch(dev(np.zeros((1, 100), np.int32)), dev(np.array([ld], np.int32)),
+                  dev(np.zeros(n_q, np.int32)), dev(pos), 64, ld, 100)
+    ws = si_.alloc_workspace(256)
+    for K in (1, 10, 64, 2048):
+        idx = torch.empty((n_q, K), dtype=torch.int32, device="cuda")
+        si_.topk(b, dev(sc), K, idx, ws)
+        ob = oracle.Batch(np.zeros((1, 100), np.int32), [ld], np.zeros(n_q, np.int32), pos, 64)
+        want = oracle.topk(ob, sc.astype(np.float64), K)
+        assert np.array_equal(idx.cpu().numpy(), want), K
+
+
+def test_bad_block_and_bad_index_raise_flags(si):
+    wl = synth.make("c1", batch=2, ctx=200, Hi=4, Di=32, Hq=4, Dqk=64, Dv=32, K=16)
+    bt = wl.block_table.copy()
+    bt[1, 1] = 10_000                       # outside the cache
+    wl2 = synth.Workload(**{**wl.__dict__, "block_table": bt})
+    dw = si.upload(wl2)
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, dw.batch, dw.indexer, dw.attention, 16))
+    sc = torch.empty((2, wl.max_ctx), dtype=torch.float32, device="cuda")
+    si.indexer_scores(dw.batch, dw.indexer, sc, ws)
+    assert si.workspace_status(ws) & si.DEVFLAG_BAD_BLOCK
+    # row 0 unaffected, row 1's bad page scores -inf (skipped)
+    s = sc.cpu().numpy()
+    assert np.isfinite(s[0, :200]).all() and np.isneginf(s[1, 64:128]).all()
+    dw = si.upload(wl)
+    ws = si.alloc_workspace(4096)
+    idx = torch.tensor([[0, 5, 199, -1] + [-1] * 12, [3, 250, -7, -1] + [-1] * 12],
+                       dtype=torch.int32, device="cuda")
+    out = torch.empty((2, 4, 32), dtype=torch.float32, device="cuda")
+    si.sparse_attn(dw.batch, dw.attention, idx, 16, out, ws)
+    assert si.workspace_status(ws) == si.DEVFLAG_BAD_INDEX
+    ref, _ = _attn_ref(wl, np.where(idx.cpu().numpy() > 199, -1, np.maximum(idx.cpu().numpy(), -1)))
+    assert max_abs(out.cpu().numpy(), ref) <= ATOL_BF16
+
+
+def test_empty_batch_is_noop(si):
+    wl = synth.make("c0", L=64)
+    dw = si.upload(wl)
+    b = dw.batch
+    empty = si.Batch(b.block_table, b.ctx_len, b.q_seq[:0], b.q_pos[:0], b.page_size, 1, b.n_blocks)
+    ws = si.alloc_workspace(256)
+    out = torch.empty((0, 4, 64), device="cuda")
+    idx = torch.empty((0, 32), dtype=torch.int32, device="cuda")
+    si.fused_decode(empty, dw.indexer, dw.attention, 32, idx, out, ws)
+    assert si.workspace_status(ws) == 0
