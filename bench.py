@@ -1,0 +1,389 @@
+"""Benchmark of the indexer -> Top-K -> sparse-attention decode step.
+
+Default workload: decode, batch 64, context 8192 (indexer 64 heads x 128 with
+FP8 keys, Top-K 2048, attention 128 heads over a 576-dim bf16 latent row),
+synthetic seeded inputs resident in HBM.  One step is one pass of the whole
+path over the batch: indexer scores, Top-K selection, sparse attention.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl si|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
+(requests are independent: weak scaling, no collective on the data path; the
+only collectives are the timing barrier and a max over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("decode queries/s + achieved HBM GB/s (% of 8 TB/s); "
+          "prefill indexer TFLOP/s (% peak)")
+NOMINAL_HBM_GBS = 8000.0
+L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]), "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "src": "fallback"}
+
+
+# ---------------------------------------------------------------- bytes/flops
+
+def algorithmic_bytes(wl):
+    """Bytes the method must move per step, by kernel (decode rows).
+
+    indexer: every visible key (e4m3 row + fp32 scale), the query's indexer
+             heads (bf16) and weights (fp32), and the fp32 scores written.
+    topk:    the scores read, the indices written.
+    attn:    the selected latent rows (bf16), the query heads (bf16), the
+             output (fp32) and the indices read."""
+    n_keys = int((wl.q_pos.astype("int64") + 1).sum())
+    n_sel = int(sum(min(wl.K, int(p) + 1) for p in wl.q_pos))
+    esz = 2 if wl.kv_dtype == "bf16" else 4
+    kesz = 1 if wl.k_idx_dtype == "e4m3" else 4
+    idx_b = n_keys * (wl.Di * kesz + (4 if wl.k_scale is not None else 0)) \
+        + wl.n_q * (wl.Hi * wl.Di * 2 + wl.Hi * 4) + n_keys * 4
+    topk_b = n_keys * 4 + wl.n_q * wl.K * 4
+    attn_b = n_sel * wl.Dqk * esz + wl.n_q * wl.Hq * wl.Dqk * esz + wl.n_q * wl.Hq * wl.Dv * 4 \
+        + wl.n_q * wl.K * 4
+    flops_idx = 2 * n_keys * wl.Hi * wl.Di
+    flops_attn = 2 * n_sel * wl.Hq * (wl.Dqk + wl.Dv)
+    return {"indexer": idx_b, "topk": topk_b, "attn": attn_b,
+            "flops_indexer": flops_idx, "flops_attn": flops_attn}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _kernel_traffic(kernel: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's
+    source is unchanged since the counters were taken; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+        with open(os.path.join(ROOT, "indexer_driven_top_gb300", "csrc", source), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        if rec and rec.get("source_sha") == sha:
+            return rec.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def cpu_baseline(wl, rows, threads):
+    """The CPU oracle, as it stands, on a bounded sample of query rows."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.run(wl, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": len(rows) / dt, "unit": "queries/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} of {wl.n_q} decode rows of workload {wl.name}, "
+                      f"full indexer + Top-K + attention per row, {dt:.1f} s"}
+
+
+def _threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference
+
+def run_reference(args):
+    """Reference arm: the CPU oracle timed on the host cores."""
+    import synth
+    wl = synth.make(args.workload)
+    threads = _threads()
+    rows_per_step = max(threads, 16)
+    rows = [i % wl.n_q for i in range(rows_per_step)]
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle.run(wl, rows=rows[:threads], threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.run(wl, rows=rows, threads=threads)
+        times.append(time.perf_counter() - t0)
+    per_q = sum(times) / (args.steps * len(rows))
+    value = 1.0 / per_q
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * per_q * wl.n_q, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_name(wl), "rows_per_timed_step": len(rows)},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{len(rows)} decode rows per step of {wl.n_q}"},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _workload_name(wl):
+    if wl.name == "c1":
+        return "decode batch 64 x context 8192, indexer 64x128 fp8, top-k 2048, MLA 128x576 bf16"
+    return wl.name
+
+
+# ---------------------------------------------------------------- main arm
+
+def run_si(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import indexer_driven_top_gb300 as si
+    import synth
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = synth.make(args.workload, seed=synth.CONFIGS[args.workload]["seed"] + 1000 * rank)
+    dw = si.upload(wl, dev)
+    b, ix, at, K = dw.batch, dw.indexer, dw.attention, dw.k_top
+    n_q = wl.n_q
+    ld = b.max_ctx
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, ix, at, K), dev)
+    scores = torch.empty((n_q, ld), dtype=torch.float32, device=dev)
+    idx = torch.empty((n_q, K), dtype=torch.int32, device=dev)
+    out = torch.empty((n_q, wl.Hq, wl.Dv), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        si.indexer_scores(b, ix, scores, ws, stream)
+        if ev:
+            ev[1].record(stream)
+        si.topk(b, scores, K, idx, ws, stream)
+        if ev:
+            ev[2].record(stream)
+        si.sparse_attn(b, at, idx, K, out, ws, stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    assert si.workspace_status(ws, stream) == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = si.launch_count()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)            # evict the previous step's data from L2
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    launches = si.launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    assert si.workspace_status(ws, stream) == 0
+
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    t_k = {"indexer": [e[0].elapsed_time(e[1]) for e in evs],
+           "topk": [e[1].elapsed_time(e[2]) for e in evs],
+           "attn": [e[2].elapsed_time(e[3]) for e in evs]}
+    ms = sum(t_step) / args.steps
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * n_q / (ms_max / 1e3)
+
+    # ---- end to end: host (pinned) buffers in and out, through the fused call
+    h_qidx = torch.from_numpy(wl.q_idx).view(torch.bfloat16).pin_memory()
+    h_w = torch.from_numpy(wl.w).pin_memory()
+    h_q = torch.from_numpy(wl.q).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_idx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+    ws_f = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, ix, at, K), dev)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+
+    def e2e_step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        ix.q.copy_(h_qidx, non_blocking=True)
+        ix.w.copy_(h_w, non_blocking=True)
+        at.q.copy_(h_q, non_blocking=True)
+        si.fused_decode(b, ix, at, K, idx, out, ws_f, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        h_idx.copy_(idx, non_blocking=True)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e2e_step(e2e_ev[i])
+    torch.cuda.synchronize(dev)
+    assert si.workspace_status(ws_f, stream) == 0
+    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = h_qidx.numel() * 2 + h_w.numel() * 4 + h_q.numel() * 2
+    d2h = h_out.numel() * 4 + h_idx.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel
+    peaks = _peaks()
+    algo = algorithmic_bytes(wl)
+    mean_k = {k: sum(v) / len(v) for k, v in t_k.items()}
+    dom = max(mean_k, key=mean_k.get)
+    src = {"indexer": "si_generic.cu", "topk": "si_topk.cu", "attn": "si_generic.cu"}[dom]
+    kname = {"indexer": "k_indexer_generic", "topk": "k_topk_rows", "attn": "k_attn_generic"}[dom]
+    achieved = algo[dom] / (mean_k[dom] / 1e3) / 1e9
+    roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "peak_src": peaks["src"] + " (hbm_gbs, copy)",
+            "traffic": _kernel_traffic(kname, src),
+            "algorithmic_bytes_per_launch": algo[dom], "ms_per_launch": mean_k[dom]}
+    total_bytes = algo["indexer"] + algo["topk"] + algo["attn"]
+    step_gbs = total_bytes / (ms / 1e3) / 1e9
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        threads = _threads()
+        cpu = cpu_baseline(wl, list(range(n_q)), threads)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": _workload_name(wl), "batch": n_q, "context": ld, "top_k": K,
+                   "indexer": f"{wl.Hi}x{wl.Di} e4m3 keys + fp32 scale, bf16 q",
+                   "attention": f"{wl.Hq} heads x {wl.Dqk} (v {wl.Dv}) bf16, fp32 out",
+                   "page": wl.page, "l2": "flushed between steps (512 MiB write)",
+                   "step": "si_indexer_scores + si_topk + si_sparse_attn",
+                   "parallelism": f"dp{world} (independent requests per rank)"},
+        "hbm": {"algorithmic_bytes_per_step": total_bytes, "achieved_gbs": step_gbs,
+                "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                "frac_of_measured": step_gbs / peaks["hbm_gbs"]},
+        "kernels_ms": mean_k,
+        "clocks": clk,
+        "e2e": {"value": world * n_q / (e2e_ms / 1e3), "unit": "queries/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "call": "si_fused_decode with pinned host inputs/outputs"},
+        "gpu_launches": int(launches),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["si", "reference"], default="si")
+    ap.add_argument("--workload", default="c1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        world, rank, _ = _dist()
+        if rank == 0:
+            run_reference(args)
+        return
+    run_si(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -30,8 +30,9 @@
  *     skipped and a bit is OR-ed into the sticky status word that lives in the
  *     first 16 bytes of the workspace.  Zero the workspace once after
  *     allocating it; read the word with si_workspace_status().
- *   * The library holds no global mutable state; calls from several host
- *     threads are safe as long as they use different workspaces.
+ *   * Apart from a diagnostic launch counter the library holds no global
+ *     mutable state; calls from several host threads are safe as long as
+ *     they use different workspaces.
  *
  * Paged caches: logical position s of sequence q is physical row
  *   block_table[q * max_blocks + s / page_size] * page_size + s % page_size
@@ -177,6 +178,10 @@ si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_atte
 /* Synchronises `stream`, then reads the sticky device status word of `ws`
  * into *flags (SI_DEVFLAG_*).  Returns SI_ERR_DEVICE if any flag is set. */
 si_status si_workspace_status(const void *ws, uint32_t *flags, void *stream);
+
+/* Process-wide count of kernels this library has launched (diagnostic; the
+ * only mutable state the library keeps, updated with an atomic add). */
+uint64_t si_launch_count(void);
 
 const char *si_status_string(si_status s);
 const char *si_last_error(void);

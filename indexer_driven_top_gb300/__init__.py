@@ -83,6 +83,7 @@ def load() -> ctypes.CDLL:
         "si_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "si_last_error": (ctypes.c_char_p, []),
         "si_version": (I32, []),
+        "si_launch_count": (ctypes.c_uint64, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -96,7 +97,7 @@ load()
 
 EXPORTED = ("si_workspace_size", "si_workspace_min", "si_indexer_scores", "si_topk",
             "si_sparse_attn", "si_fused_decode", "si_workspace_status", "si_status_string",
-            "si_last_error", "si_version")
+            "si_last_error", "si_version", "si_launch_count")
 
 
 def _check(status: int):
@@ -236,6 +237,11 @@ def fused_decode(b: Batch, ix: Indexer, at: Attention, k_top: int, idx: torch.Te
     _check(load().si_fused_decode(ctypes.byref(cb), ctypes.byref(ci), ctypes.byref(ca), k_top,
                                   _ptr(idx), _ptr(out), _out_dtype(out), _ptr(lse), _ptr(ws),
                                   ws.numel(), _stream(stream)))
+
+
+def launch_count() -> int:
+    """Kernels launched by libsi in this process so far."""
+    return int(load().si_launch_count())
 
 
 def workspace_status(ws: torch.Tensor, stream=None) -> int:

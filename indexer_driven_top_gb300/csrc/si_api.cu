@@ -10,9 +10,15 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "si_common.cuh"
 #include "si_internal.h"
+
+namespace si {
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace si
 
 namespace {
 
@@ -334,6 +340,8 @@ const char *si_status_string(si_status s)
 }
 
 const char *si_last_error(void) { return g_err; }
+
+uint64_t si_launch_count(void) { return si::g_launches.load(std::memory_order_relaxed); }
 
 int32_t si_version(void) { return SI_VERSION; }
 

@@ -185,6 +185,7 @@ cudaError_t launch_indexer_generic(const si_batch &b, const si_indexer &ix, floa
     if (e != cudaSuccess)
         return e;
     dim3 grid((unsigned)b.n_q, (unsigned)((ld + kIdxKeys - 1) / kIdxKeys));
+    count_launch();
     k_indexer_generic<<<grid, kIdxKeys, smem, s>>>(b, ix, scores, ld, st);
     return cudaGetLastError();
 }
@@ -199,6 +200,7 @@ cudaError_t launch_attn_generic(const si_batch &b, const si_attention &at, const
     if (e != cudaSuccess)
         return e;
     dim3 grid((unsigned)b.n_q, (unsigned)at.n_heads);
+    count_launch();
     k_attn_generic<<<grid, kAttnThreads, smem, s>>>(b, at, idx, k_top, out, out_dtype, lse, st);
     return cudaGetLastError();
 }

@@ -8,6 +8,9 @@
 
 namespace si {
 
+// Counts one kernel launch (process-wide diagnostic, see si_launch_count).
+void count_launch(int n = 1);
+
 // Generic CUDA-core kernels: any supported dtype and shape, fp32 arithmetic.
 cudaError_t launch_indexer_generic(const si_batch &b, const si_indexer &ix, float *scores,
                                    int64_t ld, unsigned int *st, cudaStream_t s);

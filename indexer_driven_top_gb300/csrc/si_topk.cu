@@ -104,6 +104,7 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
                         int32_t *idx, unsigned int *st, cudaStream_t s)
 {
     (void)st;
+    count_launch();
     k_topk_rows<<<b.n_q, kTopkThreads, 0, s>>>(b, scores, ld, k_top, idx);
     return cudaGetLastError();
 }
