@@ -14,9 +14,14 @@ namespace si {
 // The first 16 bytes of every workspace hold the sticky device status word.
 constexpr size_t kStatusBytes = 256;
 
+// Launchers keep a few per-device facts (SM count, shared-memory opt-in).
+constexpr int kMaxDevices = 64;
+
+// A null status pointer means "do not report" (used by redundant lanes).
 __device__ __forceinline__ void raise_flag(unsigned int *st, unsigned int f)
 {
-    atomicOr(st, f);
+    if (st)
+        atomicOr(st, f);
 }
 
 // Physical row of logical position s of sequence seq in a paged cache

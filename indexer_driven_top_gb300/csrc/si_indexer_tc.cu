@@ -1,0 +1,469 @@
+// si_indexer_tc.cu -- tensor-core indexer over a paged FP8 key cache.
+//
+// "Day0 Inference Support and Performance Optimization for New Architecture
+// LLMs": section 2.2 (the indexer scores a query against every earlier
+// position and aggregates the per-head scores with head weights), section
+// 4.1 (the scoring reads the paged K-cache directly and never stores the
+// intermediate per-head scores) and section 5.1 (the indexer path is stored in
+// FP8).  Score of key s for query row r:
+//     k_scale[s] * sum_h w[r,h] * ReLU(q[r,h,:] . k[s,:])
+//
+// GB300 mapping.  A tile is 128 consecutive key positions of one query row;
+// its FP8 key rows are the UMMA A operand (M = 128, K = 128 bytes) exactly as
+// the TMA engine lands them in shared memory, so keys are never converted.
+// The bf16 query is made FP8 without loss: per head h a power of two s_h
+// brings max|q_h| into (224, 448], and the scaled head is written as
+// q_hi + q_lo with q_hi = e4m3(q) and q_lo = e4m3(q - q_hi).  A bf16 value
+// has 8 significant bits and each term carries 4, so the split is exact
+// except where q_lo falls below e4m3's subnormal step (|q| < max|q_h| / 1800,
+// error < 2^-10 of the head's scale).  The 64 q_hi heads and the 64 q_lo heads
+// form one 128-row B operand; the MMA (kind::f8f6f4, fp32 accumulate) writes
+// D[key, 0..63] = q_hi . k and D[key, 64..127] = q_lo . k, one key per TMEM
+// lane.  Each epilogue thread then reduces its own key:
+//     k_scale * sum_h (w_h * s_h) * ReLU(D[h] + D[64 + h])
+// (s_h > 0 is a power of two, so folding it into the weight is exact).
+//
+// One persistent CTA per SM runs a warp-specialised pipeline:
+//   2 producer warps -- per tile, TMA tensor copies of its key pages (128-byte
+//                       swizzle) into a ten-stage ring; tiles alternate
+//                       between the warps because a bulk copy holds its
+//                       issuing warp for several hundred cycles;
+//   2 lanes of work  -- tiles alternate between two (MMA warp, epilogue
+//                       warpgroup) pairs: the MMA warp issues four FP8 UMMAs
+//                       per tile into its two TMEM accumulators (128 columns
+//                       each), the epilogue group fetches the keys' scales,
+//                       reduces its accumulator and stores the scores; two
+//                       pairs hide UMMA issue and TMEM-load latency;
+//   q-prep warpgroup -- splits each query row into the FP8 B operand and the
+//                       scaled head weights (double-buffered per row).
+// Work is the flattened list of (query row, tile) items split into equal
+// contiguous ranges, one per CTA.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "si_common.cuh"
+#include "si_internal.h"
+#include "si_sm100.cuh"
+#include "si_tmap.h"
+
+namespace si {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kKeys = 128;        // keys per tile = UMMA M
+constexpr int kHeads = 64;        // indexer heads
+constexpr int kDim = 128;         // head dim = bytes per e4m3 key row = UMMA K
+constexpr int kN = 2 * kHeads;    // B rows: q_hi heads, then q_lo heads = UMMA N
+constexpr int kStages = 10;       // key-tile ring depth
+constexpr int kPairs = 2;         // (MMA warp, epilogue group) pairs, alternate tiles
+constexpr int kAccPerPair = 2;    // TMEM accumulators per pair (4 x 128 = 512 columns)
+// warp roles
+constexpr int kWarpProd0 = 0, kWarpProd1 = 2;   // producers
+constexpr int kWarpMma0 = 1, kWarpMma1 = 3;     // MMA warps of pair 0 and pair 1
+constexpr int kWarpPrep0 = 4;                   // q-prep: 4..7
+constexpr int kWarpEpi0 = 8;                    // epilogue groups: 8..11 and 12..15
+constexpr int kThreads = 16 * 32;
+
+constexpr uint32_t kTile = kKeys * kDim;    // 16 KB, SW128 K-major
+constexpr uint32_t kTileB = kN * kDim;      // 16 KB, SW128 K-major
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffQ = kOffStage + kStages * kTile;            // [2]
+constexpr uint32_t kOffW = kOffQ + 2 * kTileB;                      // [2][64] fp32 (w * s_h)
+constexpr uint32_t kOffWin = kOffW + 2 * kHeads * 4;                // 2 producers x 32 int
+constexpr uint32_t kOffBar = kOffWin + 2 * 32 * 4;
+constexpr uint32_t kSmemBytes = kOffBar + 1024 + 1024;             // + alignment slack
+
+// Advances (row, tile) by `n` items of a row-major list with `tpr` tiles per row.
+__device__ __forceinline__ void advance(int &r, int &t, int n, int tpr)
+{
+    t += n;
+    while (t >= tpr) {
+        t -= tpr;
+        ++r;
+    }
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v)
+{
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+    return make_float2(__half2float(__ushort_as_half(h.x)), __half2float(__ushort_as_half(h.y)));
+}
+
+__device__ __forceinline__ uint16_t float2_to_e4m3x2(float a, float b)
+{
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix, float *scores,
+             int64_t ld, int64_t total_items, int tiles_per_row, unsigned int *st)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(gbase + kOffBar);  // [kStages]
+    uint64_t *empty_bar = full_bar + kStages;                             // [kStages]
+    uint64_t *cfull_bar = empty_bar + kStages;                            // [kPairs][kAccPerPair]
+    uint64_t *cempty_bar = cfull_bar + kPairs * kAccPerPair;              // [kPairs][kAccPerPair]
+    uint64_t *qfull_bar = cempty_bar + kPairs * kAccPerPair;              // [2]
+    uint64_t *qempty_bar = qfull_bar + 2;                                 // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qempty_bar + 2);
+    float *w_s = reinterpret_cast<float *>(gbase + kOffW);
+    volatile int *win_all = reinterpret_cast<volatile int *>(gbase + kOffWin);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t G = gridDim.x;
+    const int64_t j0 = total_items * blockIdx.x / G;
+    const int64_t j1 = total_items * (blockIdx.x + 1) / G;
+    const int64_t n_items = j1 - j0;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; i++) {
+            mbar_init(full_bar + i, 1);     // producer's expect_tx arrival
+            mbar_init(empty_bar + i, 1);    // MMA commit (or plain arrive)
+        }
+        for (int i = 0; i < kPairs * kAccPerPair; i++) {
+            mbar_init(cfull_bar + i, 1);    // MMA commit
+            mbar_init(cempty_bar + i, 128); // epilogue group
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(qfull_bar + i, 128);                   // q-prep threads
+            mbar_init(qempty_bar + i, kPairs + kPairs * 128); // MMA commits + epilogues
+        }
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma0) {
+        tmem_alloc(tmem_slot, kPairs * kAccPerPair * kN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int P = b.page_size;
+    const int lp = 31 - __clz(P);  // page_size is a power of two >= 8
+
+    if (warp == kWarpProd0 || warp == kWarpProd1) {
+        // ------------------------------------------------------------ producer
+        const int pw = warp == kWarpProd0 ? 0 : 1;  // takes items pw, pw + 2, ...
+        volatile int *win_s = win_all + pw * 32;
+        const int span = min(P, kKeys);             // keys of one page inside one tile
+        int r = (int)(j0 / tiles_per_row), t = (int)(j0 % tiles_per_row);
+        advance(r, t, pw, tiles_per_row);
+        int pf_row = -1, pf_pos = -1, pf_seq = 0;
+        // window of 32 block-table entries: win_s[l] = page win + l of win_row
+        int win_row = -1, win = 0;
+        for (int64_t it = pw; it < n_items; it += 2) {
+            const int stg = (int)(it % kStages);
+            if (it >= kStages &&
+                !mbar_wait(empty_bar + stg, (uint32_t)((it / kStages) - 1) & 1, st))
+                break;
+            if (r != pf_row) {
+                pf_row = r;
+                pf_pos = __ldg(b.q_pos + r);
+                pf_seq = __ldg(b.q_seq + r);
+            }
+            const int s0 = t * kKeys;
+            const bool live = s0 <= pf_pos;
+            const int first = s0 >> lp;
+            const int last = min(s0 + kKeys - 1, pf_pos) >> lp;
+            if (live && (win_row != r || last >= win + 32)) {
+                win_row = r;
+                win = first;
+                const int lb = first + lane;
+                int v = -1;
+                if ((unsigned)pf_seq < (unsigned)b.n_seq && lb < b.max_blocks)
+                    v = __ldg(b.block_table + (int64_t)pf_seq * b.max_blocks + lb);
+                win_s[lane] = v;
+                __syncwarp();
+            }
+            // lane l handles page first + l of the tile
+            const int lb = first + lane;
+            bool copy = false;
+            int row = 0, k_lo = 0;
+            if (live && lane < 16 && lb <= last) {
+                const int blk = win_s[lb - win];
+                if (lb < b.max_blocks && (unsigned)blk < (unsigned)b.n_blocks) {
+                    copy = true;
+                    k_lo = max(lb << lp, s0) - s0;
+                    row = (blk << lp) + (s0 + k_lo - (lb << lp));
+                } else {
+                    raise_flag(st, SI_DEVFLAG_BAD_BLOCK);
+                }
+            }
+            const uint32_t n_copies = __popc(__ballot_sync(0xffffffffu, copy));
+            if (lane == 0)
+                mbar_arrive_expect_tx(full_bar + stg, n_copies * span * kDim);
+            __syncwarp();
+            if (copy)
+                tma_load_2d(base + kOffStage + stg * kTile + k_lo * kDim, &tmap, 0, row,
+                            full_bar + stg);
+            advance(r, t, 2, tiles_per_row);
+        }
+    } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+        // ----------------------------------------------------------------- MMA
+        const int pr = warp == kWarpMma0 ? 0 : 1;  // pair: items pr, pr + 2, ...
+        const uint32_t idesc = idesc_e4m3(kKeys, kN);
+        int r = (int)(j0 / tiles_per_row), t = (int)(j0 % tiles_per_row);
+        int cur = -1, ri = -1, pos = -1, p = 0;
+        int64_t m = 0;  // live tiles of this pair so far
+        for (int64_t it = 0; it < n_items; it++) {
+            if (r != cur) {
+                cur = r;
+                ++ri;
+                p = ri & 1;
+                pos = __ldg(b.q_pos + r);
+                if (!mbar_wait(qfull_bar + p, (uint32_t)(ri >> 1) & 1, st))
+                    break;
+            }
+            const bool mine = (int)(it & 1) == pr;
+            const int stg = (int)(it % kStages);
+            const bool live = t * kKeys <= pos;
+            advance(r, t, 1, tiles_per_row);
+            const bool row_ends = (it + 1 == n_items) || (r != cur);
+            if (mine) {
+                if (!mbar_wait(full_bar + stg, (uint32_t)(it / kStages) & 1, st))
+                    break;
+                if (live) {
+                    const int c = (int)(m % kAccPerPair);
+                    uint64_t *cf = cfull_bar + pr * kAccPerPair + c;
+                    if (m >= kAccPerPair &&
+                        !mbar_wait(cempty_bar + pr * kAccPerPair + c,
+                                   (uint32_t)((m / kAccPerPair) - 1) & 1, st))
+                        break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t d = tmem + (pr * kAccPerPair + c) * kN;
+#pragma unroll
+                        for (int kk = 0; kk < kDim / 32; kk++) {
+                            const uint64_t ad = smem_desc(base + kOffStage + stg * kTile + kk * 32,
+                                                          16, 1024, kSwizzle128B);
+                            const uint64_t bd = smem_desc(base + kOffQ + p * kTileB + kk * 32, 16,
+                                                          1024, kSwizzle128B);
+                            umma_f8_ss(d, ad, bd, idesc, kk > 0);
+                        }
+                        umma_commit(empty_bar + stg);
+                        umma_commit(cf);
+                    }
+                    m++;
+                } else if (lane == 0) {
+                    mbar_arrive(empty_bar + stg);  // nothing was copied; release the slot
+                }
+            }
+            if (row_ends && lane == 0)
+                umma_commit(qempty_bar + p);  // the row's B operand is free once read
+            __syncwarp();
+        }
+    } else if (warp >= kWarpPrep0 && warp < kWarpEpi0) {
+        // -------------------------------------------------------------- q-prep
+        // Thread pt splits dims [64 * half, +64) of head h into q_hi / q_lo.
+        const int pt = tid - kWarpPrep0 * 32;
+        const int h = pt >> 1, half = pt & 1;
+        const int r_first = (int)(j0 / tiles_per_row);
+        const int r_last = n_items > 0 ? (int)((j1 - 1) / tiles_per_row) : r_first - 1;
+        for (int r = r_first; r <= r_last; r++) {
+            const int ri = r - r_first, p = ri & 1;
+            if (ri >= 2 && !mbar_wait(qempty_bar + p, (uint32_t)((ri - 2) >> 1) & 1, st))
+                break;
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const uint16_t *>(ix.q) + ((int64_t)r * kHeads + h) * kDim + half * 64);
+            uint32_t q2[32];  // 64 bf16 dims, two per word
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const uint4 v = __ldg(src + i);
+                q2[4 * i] = v.x;
+                q2[4 * i + 1] = v.y;
+                q2[4 * i + 2] = v.z;
+                q2[4 * i + 3] = v.w;
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+                amax = fmaxf(amax, fabsf(__uint_as_float(q2[i] << 16)));
+                amax = fmaxf(amax, fabsf(__uint_as_float(q2[i] & 0xFFFF0000u)));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            // s_h = 2^e with max|q_h| / s_h in (224, 448]
+            int e = 0;
+            if (amax > 0.f) {
+                e = (int)ceilf(log2f(amax / 448.f));
+                while (ldexpf(amax, -e) > 448.f)
+                    e++;
+                while (ldexpf(amax, -(e - 1)) <= 448.f)
+                    e--;
+            }
+            const uint32_t qb = base + kOffQ + p * kTileB;
+#pragma unroll
+            for (int c = 0; c < 4; c++) {  // 16 dims per 16-byte unit
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int j = 0; j < 4; j++) {  // 4 dims per output word
+                    uint32_t hw = 0, lw = 0;
+#pragma unroll
+                    for (int pr2 = 0; pr2 < 2; pr2++) {
+                        const uint32_t word = q2[8 * c + 2 * j + pr2];  // dims 16c+4j+2pr2, +1
+                        const float x0 = ldexpf(__uint_as_float(word << 16), -e);
+                        const float x1 = ldexpf(__uint_as_float(word & 0xFFFF0000u), -e);
+                        const uint16_t h2 = float2_to_e4m3x2(x0, x1);
+                        const float2 hf = e4m3x2_to_float2(h2);
+                        const uint16_t l2 = float2_to_e4m3x2(x0 - hf.x, x1 - hf.y);
+                        hw |= (uint32_t)h2 << (16 * pr2);
+                        lw |= (uint32_t)l2 << (16 * pr2);
+                    }
+                    hi[j] = hw;
+                    lo[j] = lw;
+                }
+                const uint32_t u = (uint32_t)(half * 4 + c);
+                st_shared_v4(qb + sw128_offset(h, u), hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(qb + sw128_offset(kHeads + h, u), lo[0], lo[1], lo[2], lo[3]);
+            }
+            if (half == 0)
+                w_s[p * kHeads + h] = ldexpf(__ldg(ix.w + (int64_t)r * kHeads + h), e);
+            fence_async_smem();
+            mbar_arrive(qfull_bar + p);
+        }
+    } else if (warp >= kWarpEpi0) {
+        // ------------------------------------------------------------ epilogue
+        // Group g pairs with MMA warp g and owns items g, g + 2, ...; it walks
+        // every item to keep the row bookkeeping.
+        const int g = (warp - kWarpEpi0) >> 2;
+        const int et = (tid - kWarpEpi0 * 32) & 127;  // key row = TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        int r = (int)(j0 / tiles_per_row), t = (int)(j0 % tiles_per_row);
+        int cur = -1, ri = -1, pos = -1, p = 0, seq = 0;
+        int64_t m = 0;
+        for (int64_t it = 0; it < n_items; it++) {
+            if (r != cur) {
+                cur = r;
+                ++ri;
+                p = ri & 1;
+                pos = __ldg(b.q_pos + r);
+                seq = __ldg(b.q_seq + r);
+                if (!mbar_wait(qfull_bar + p, (uint32_t)(ri >> 1) & 1, st))
+                    break;
+            }
+            const int rr = r, s0 = t * kKeys, s = s0 + et;
+            advance(r, t, 1, tiles_per_row);
+            const bool row_ends = (it + 1 == n_items) || (r != cur);
+            const bool live = s0 <= pos;
+            if ((int)(it & 1) == g) {
+                if (live) {
+                    // this key's scale (issued before the accumulator wait):
+                    // -1 marks a key that must score -inf, 1 an unscaled key
+                    float sc = -1.f;
+                    if (s <= pos) {
+                        const int lb = s >> lp;
+                        int blk = -1;
+                        if ((unsigned)seq < (unsigned)b.n_seq && lb < b.max_blocks)
+                            blk = __ldg(b.block_table + (int64_t)seq * b.max_blocks + lb);
+                        if ((unsigned)blk < (unsigned)b.n_blocks)
+                            sc = ix.k.scale ? __ldg(ix.k.scale + ((int64_t)blk << lp) + (s & (P - 1)))
+                                            : 1.f;
+                    }
+                    const int c = (int)(m % kAccPerPair);
+                    if (!mbar_wait(cfull_bar + g * kAccPerPair + c,
+                                   (uint32_t)(m / kAccPerPair) & 1, st))
+                        break;
+                    tc_fence_after();
+                    const float4 *w4 = reinterpret_cast<const float4 *>(w_s + p * kHeads);
+                    const uint32_t acc = tmem + (g * kAccPerPair + c) * kN + lane_off;
+                    float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int hh = 0; hh < 2; hh++) {  // heads [32 hh, 32 hh + 32)
+                        uint32_t vh[32], vl[32];
+                        tmem_ld32(acc + hh * 32, vh);
+                        tmem_ld32(acc + kHeads + hh * 32, vl);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 wv = w4[(hh * 32 + i) >> 2];
+                            const float wq[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                            for (int k = 0; k < 4; k++) {
+                                const float lg =
+                                    __uint_as_float(vh[i + k]) + __uint_as_float(vl[i + k]);
+                                part[k] = fmaf(wq[k], fmaxf(lg, 0.f), part[k]);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(cempty_bar + g * kAccPerPair + c);
+                    const float sum = (part[0] + part[1]) + (part[2] + part[3]);
+                    if (s < ld)
+                        scores[(int64_t)rr * ld + s] = sc > 0.f ? sum * sc + 0.0f : -INFINITY;
+                    m++;
+                } else if (s < ld) {
+                    scores[(int64_t)rr * ld + s] = -INFINITY;  // tile after the query
+                }
+            }
+            if (row_ends)
+                mbar_arrive(qempty_bar + p);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma0)
+        tmem_dealloc(tmem, kPairs * kAccPerPair * kN);
+}
+
+}  // namespace
+
+bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld)
+{
+    (void)ld;
+    // whole pages are copied as tensor boxes: rows packed (stride 128 bytes),
+    // page size a power of two >= 8, physical row indices within int32
+    const bool pow2_page = b.page_size >= 8 && (b.page_size & (b.page_size - 1)) == 0;
+    return pow2_page && ix.q_dtype == SI_BF16 && ix.k.dtype == SI_E4M3 && ix.n_heads == kHeads &&
+           ix.head_dim == kDim && ix.k.row_stride == kDim &&
+           (int64_t)b.n_blocks * b.page_size < (int64_t)INT32_MAX &&
+           ((uintptr_t)ix.q % 16) == 0 && ((uintptr_t)ix.k.data % 16) == 0;
+}
+
+cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
+                              unsigned int *st, cudaStream_t s)
+{
+    // Per-device launch facts (SM count, shared-memory opt-in), set up once.
+    static std::once_flag once[kMaxDevices];
+    static int sms_of[kMaxDevices];
+    static cudaError_t err_of[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(k_indexer_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
+        err_of[dev] = r;
+    });
+    if (err_of[dev] != cudaSuccess)
+        return err_of[dev];
+    CUtensorMap tmap;
+    e = make_tmap_2d_u8_sw128(&tmap, ix.k.data, kDim, (uint64_t)b.n_blocks * b.page_size,
+                              (uint64_t)ix.k.row_stride, kDim,
+                              (uint32_t)std::min(b.page_size, kKeys));
+    if (e != cudaSuccess)
+        return e;
+    const int tiles_per_row = (int)((ld + kKeys - 1) / kKeys);
+    const int64_t total = (int64_t)b.n_q * tiles_per_row;
+    const int64_t grid = std::min<int64_t>(total, (int64_t)sms_of[dev]);  // one CTA per SM
+    count_launch();
+    k_indexer_tc<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores, ld, total,
+                                                              tiles_per_row, st);
+    return cudaGetLastError();
+}
+
+}  // namespace si

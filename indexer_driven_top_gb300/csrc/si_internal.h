@@ -18,6 +18,11 @@ cudaError_t launch_attn_generic(const si_batch &b, const si_attention &at, const
                                 int k_top, void *out, si_dtype out_dtype, float *lse,
                                 unsigned int *st, cudaStream_t s);
 
+// Tensor-core indexer: bf16 query, e4m3 keys, 64 heads x 128 dims.
+bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld);
+cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
+                              unsigned int *st, cudaStream_t s);
+
 // Radix select of the k_top best scores per row.
 cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,
                         int32_t *idx, unsigned int *st, cudaStream_t s);

@@ -164,3 +164,42 @@ def test_empty_batch_is_noop(si):
     idx = torch.empty((0, 32), dtype=torch.int32, device="cuda")
     si.fused_decode(empty, dw.indexer, dw.attention, 32, idx, out, ws)
     assert si.workspace_status(ws) == 0
+
+
+def _scores_check(si, wl, wl_ref=None):
+    """GPU scores of ``wl``; oracle scores of ``wl_ref`` (default ``wl``; the
+    oracle must only ever see a valid block table)."""
+    dw = si.upload(wl)
+    ws = si.alloc_workspace(4096)
+    sc = torch.empty((wl.n_q, wl.max_ctx), dtype=torch.float32, device="cuda")
+    si.indexer_scores(dw.batch, dw.indexer, sc, ws)
+    flags = si.workspace_status(ws)
+    g = sc.cpu().numpy()
+    r = wl_ref or wl
+    o = oracle.indexer_scores(oracle.Batch.of(r), r.q_idx, r.q_idx_dtype, r.w, r.k_idx,
+                              r.k_idx_dtype, r.k_scale, r.Hi, r.Di, r.max_ctx)
+    return g, o, flags
+
+
+@pytest.mark.parametrize("page", [16, 256])
+def test_tensor_core_indexer_page_sizes(si, page):
+    wl = synth.make("c1", batch=3, ctx_list=[1000, 300, 77], K=64, page=page)
+    g, o, flags = _scores_check(si, wl)
+    assert flags == 0
+    fin = np.isfinite(o)
+    assert np.array_equal(np.isfinite(g), fin)
+    assert np.abs(g[fin] - o[fin]).max() <= 1e-5 * np.abs(o[fin]).max()
+
+
+def test_tensor_core_indexer_bad_block(si):
+    wl = synth.make("c1", batch=2, ctx=300, K=64)
+    bt = wl.block_table.copy()
+    bt[1, 2] = 1 << 20                     # page 2 of row 1 points outside the cache
+    wl2 = synth.Workload(**{**wl.__dict__, "block_table": bt})
+    g, o, flags = _scores_check(si, wl2, wl_ref=wl)
+    assert flags & si.DEVFLAG_BAD_BLOCK
+    assert np.isneginf(g[1, 128:192]).all()
+    ok = np.ones_like(g, dtype=bool)
+    ok[1, 128:192] = False
+    fin = np.isfinite(o) & ok
+    assert np.abs(g[fin] - o[fin]).max() <= 1e-5 * np.abs(o[fin]).max()
