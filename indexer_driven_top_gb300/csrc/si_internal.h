@@ -23,6 +23,12 @@ bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld);
 cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
                               unsigned int *st, cudaStream_t s);
 
+// Tensor-core sparse attention: bf16, 128 heads, 576-dim latent rows (V = first 512).
+bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top);
+cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int32_t *idx,
+                           int k_top, void *out, si_dtype out_dtype, float *lse, unsigned int *st,
+                           cudaStream_t s);
+
 // Radix select of the k_top best scores per row.
 cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,
                         int32_t *idx, unsigned int *st, cudaStream_t s);
