@@ -57,7 +57,7 @@ constexpr int kChunksPerTile = kQChunks + kVChunks;  // 13
 constexpr int kRing = 3;
 constexpr int kLoaderWarps = 8;
 constexpr int kLoaders = kLoaderWarps * 32;
-constexpr int kInFlight = 3;      // chunks in flight per loader thread (registers)
+constexpr int kInFlight = kRing;  // chunks in flight per loader thread (registers), one per slot
 constexpr int kWarpSoft0 = 8;     // softmax warps 8..11 (TMEM lanes by warp % 4)
 constexpr int kWarpMma = 12;
 constexpr int kThreads = 13 * 32;
@@ -200,30 +200,47 @@ __device__ __forceinline__ void start_tile(LoaderState &ls, const si_batch &b, c
     load_idx(idx, r, k_top, tile + 2, T, n_valid, kr0, ls.sv2);
 }
 
-// Issues the loads of chunk g into register set g % kInFlight.
-__device__ __forceinline__ void issue_chunk(LoaderState &ls, uint4 (&buf)[kInFlight][4],
-                                            const si_batch &b, const int32_t *idx, int r,
-                                            int k_top, int T, int n_valid, int seq, int pos,
-                                            int64_t row_bytes, int kr0, int u, uint8_t *mask_s,
-                                            unsigned int *st, const uint8_t *kv, int half, int g)
+// Brings the next tile's key rows into L2 (each thread: its four rows, dim
+// chunks u and u + 8), so the chunk loads of that tile hit L2 instead of
+// paying a DRAM round trip per 128-byte piece.  Uses the lookahead entries
+// of tile + 1 (block table loaded one tile earlier).
+__device__ __forceinline__ void prefetch_next_tile(const LoaderState &ls, const si_batch &b,
+                                                   int pos, int64_t row_bytes, int u,
+                                                   const uint8_t *kv)
+{
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int sp = ls.sv1[i], bk = ls.bk1[i];
+        if (sp >= 0 && sp <= pos && (unsigned)bk < (unsigned)b.n_blocks) {
+            const uint8_t *row = kv + ((int64_t)bk * b.page_size + sp % b.page_size) * row_bytes;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(row + u * 128));
+            if (u == 0)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 8 * 128));
+        }
+    }
+}
+
+// Issues the loads of chunk g into `bb` (one 16-byte unit of four key rows).
+__device__ __forceinline__ void issue_chunk(LoaderState &ls, uint4 (&bb)[4], const si_batch &b,
+                                            const int32_t *idx, int r, int k_top, int T,
+                                            int n_valid, int seq, int pos, int64_t row_bytes,
+                                            int kr0, int u, uint8_t *mask_s, unsigned int *st,
+                                            const uint8_t *kv, int half, int g)
 {
     const ChunkId id = chunk_of(g, T, half);
     if (id.tile > ls.have_tile)
         start_tile(ls, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s, st,
                    id.tile);
+    if (id.v < 0 && id.c == 3 && id.tile + 1 < T)
+        prefetch_next_tile(ls, b, pos, row_bytes, u, kv);
     const bool odd = id.tile & 1;
-    const int slot = g % kInFlight;
 #pragma unroll
-    for (int s2 = 0; s2 < kInFlight; s2++)
-        if (s2 == slot) {
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int row = odd ? ls.rb1[i] : ls.rb0[i];
-                buf[s2][i] = row >= 0 ? __ldg(reinterpret_cast<const uint4 *>(
-                                            kv + (int64_t)row * row_bytes + id.c * 128 + u * 16))
-                                      : make_uint4(0, 0, 0, 0);
-            }
-        }
+    for (int i = 0; i < 4; i++) {
+        const int row = odd ? ls.rb1[i] : ls.rb0[i];
+        bb[i] = row >= 0 ? __ldg(reinterpret_cast<const uint4 *>(kv + (int64_t)row * row_bytes +
+                                                                 id.c * 128 + u * 16))
+                         : make_uint4(0, 0, 0, 0);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -303,34 +320,40 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
         load_idx(idx, r, k_top, 0, T, n_valid, kr0, ls.sv1);
         load_blk(b, seq, pos, ls.sv1, ls.bk1);
         load_idx(idx, r, k_top, 1, T, n_valid, kr0, ls.sv2);
-        uint4 buf[kInFlight][4];
-        for (int g = 0; g < min(kInFlight, n_chunks); g++)
-            issue_chunk(ls, buf, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s,
-                        st, kv, half, g);
+        // Chunk g lives in register set g % 3 and ring slot g % 3; the loop
+        // is unrolled by three so both indices are compile-time constants.
+        uint4 buf0[4], buf1[4], buf2[4];
+        if (n_chunks > 0)
+            issue_chunk(ls, buf0, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s,
+                        st, kv, half, 0);
+        if (n_chunks > 1)
+            issue_chunk(ls, buf1, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s,
+                        st, kv, half, 1);
+        if (n_chunks > 2)
+            issue_chunk(ls, buf2, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s,
+                        st, kv, half, 2);
         int mask_published = -1;
-        for (int g = 0; g < n_chunks; g++) {
+        bool stop = false;
+        // store chunk g from bb into ring slot `slot`, then reload bb with chunk g + 3
+        auto step = [&](int g, uint4 (&bb)[4], int slot) {
             const ChunkId id = chunk_of(g, T, half);
-            const int slot = g % kRing;
-            if (g >= kRing && !mbar_wait(empty_bar + slot, (uint32_t)((g / kRing) - 1) & 1, st))
-                break;
+            if (g >= kRing && !mbar_wait(empty_bar + slot, (uint32_t)((g / kRing) - 1) & 1, st)) {
+                stop = true;
+                return;
+            }
             const uint32_t dst = base + kOffRing + slot * kChunk;
-            const int rs = g % kInFlight;
             const bool to_f16 = id.v >= 0;  // value chunks feed the f16 P.V product
 #pragma unroll
-            for (int s2 = 0; s2 < kInFlight; s2++)
-                if (s2 == rs) {
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        uint4 x = buf[s2][i];
-                        if (to_f16) {
-                            x.x = bf16x2_to_f16x2(x.x);
-                            x.y = bf16x2_to_f16x2(x.y);
-                            x.z = bf16x2_to_f16x2(x.z);
-                            x.w = bf16x2_to_f16x2(x.w);
-                        }
-                        st_shared_v4(dst + sw128_offset(kr0 + 32 * i, u), x.x, x.y, x.z, x.w);
-                    }
+            for (int i = 0; i < 4; i++) {
+                uint4 x = bb[i];
+                if (to_f16) {
+                    x.x = bf16x2_to_f16x2(x.x);
+                    x.y = bf16x2_to_f16x2(x.y);
+                    x.z = bf16x2_to_f16x2(x.z);
+                    x.w = bf16x2_to_f16x2(x.w);
                 }
+                st_shared_v4(dst + sw128_offset(kr0 + 32 * i, u), x.x, x.y, x.z, x.w);
+            }
             fence_async_smem();
             mbar_arrive(full_bar + slot);
             if (id.v < 0 && id.c == 0 && id.tile > mask_published) {
@@ -339,9 +362,16 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                 mask_published = id.tile;
                 mbar_arrive(mask_bar + (id.tile % kMaskSlots));
             }
-            if (g + kInFlight < n_chunks)
-                issue_chunk(ls, buf, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u,
-                            mask_s, st, kv, half, g + kInFlight);
+            if (g + kRing < n_chunks)
+                issue_chunk(ls, bb, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u,
+                            mask_s, st, kv, half, g + kRing);
+        };
+        for (int g = 0; g < n_chunks && !stop; g += kRing) {
+            step(g, buf0, 0);
+            if (g + 1 < n_chunks && !stop)
+                step(g + 1, buf1, 1);
+            if (g + 2 < n_chunks && !stop)
+                step(g + 2, buf2, 2);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA
