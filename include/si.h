@@ -175,6 +175,41 @@ si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_atte
                           int32_t k_top, int32_t *idx, void *out, si_dtype out_dtype,
                           float *lse, void *ws, size_t ws_bytes, void *stream);
 
+/* si_fused_decode without a workspace, for callers that cannot allocate
+ * device memory (for instance code running inside an allocator's callbacks,
+ * a process whose device memory another runtime has fully reserved, or a
+ * plain C host without an allocator).  The pages describe no such call: it
+ * is an interface convenience of this library and computes exactly what
+ * si_fused_decode computes, with the same kernels.
+ *
+ * Scratch: a fixed array of SI_NOALLOC_SCRATCH_BYTES bytes inside the
+ * library's device image (one per device) takes the workspace's place.  The
+ * call allocates nothing -- no cudaMalloc, no cudaFree, no allocating library
+ * routine.  Its first 256 bytes are the sticky status word, which must be
+ * zero when the kernels start: the call enqueues a clear of those bytes on
+ * `stream` before its kernels, so each call's flags are its own.  The rest is
+ * the score strip and needs no initial value.
+ * Limit: a request whose minimum fused workspace (si_workspace_min with
+ *   SI_OP_FUSED, i.e. 256 + 4 * max_ctx bytes rounded up) exceeds the scratch
+ *   -- max_ctx above about 2.09 million positions -- returns
+ *   SI_ERR_WORKSPACE before any CUDA call; use si_fused_decode for those.
+ * Set-up: the first call on each device (with that device current) looks up
+ *   the scratch address once (cudaGetSymbolAddress), which may load the
+ *   library's device module.  Make that first call before any stream
+ *   capture.
+ * Concurrency: all calls on one device share the one scratch.  Calls issued
+ *   in order on a single stream are fine; calls that overlap -- on different
+ *   streams, or from several host threads without ordering -- race on the
+ *   scratch and give undefined results.
+ * scratch: if not NULL, *scratch receives the device address of the scratch
+ *   (NULL on error), so si_workspace_status(*scratch, ...) reads the flags
+ *   of the latest call. */
+#define SI_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+si_status si_fused_decode_noalloc(const si_batch *b, const si_indexer *ix,
+                                  const si_attention *at, int32_t k_top, int32_t *idx,
+                                  void *out, si_dtype out_dtype, float *lse,
+                                  const void **scratch, void *stream);
+
 /* Synchronises `stream`, then reads the sticky device status word of `ws`
  * into *flags (SI_DEVFLAG_*).  Returns SI_ERR_DEVICE if any flag is set. */
 si_status si_workspace_status(const void *ws, uint32_t *flags, void *stream);

@@ -6,8 +6,8 @@ the path runs in the CUDA kernels of ``libsi.so``.  There is no CPU or
 PyTorch fallback: if the library is missing, importing this package raises.
 
 Entry points (same names as the C ABI, minus the ``si_`` prefix):
-  indexer_scores, topk, sparse_attn, fused_decode, workspace_size,
-  workspace_min, workspace_status.
+  indexer_scores, topk, sparse_attn, fused_decode, fused_decode_noalloc,
+  workspace_size, workspace_min, workspace_status.
 """
 from __future__ import annotations
 
@@ -79,6 +79,8 @@ def load() -> ctypes.CDLL:
         "si_topk": (ctypes.c_int, [B, P, I64, I32, P, P, SZ, P]),
         "si_sparse_attn": (ctypes.c_int, [B, AT, P, I32, P, ctypes.c_int, P, P, SZ, P]),
         "si_fused_decode": (ctypes.c_int, [B, IX, AT, I32, P, P, ctypes.c_int, P, P, SZ, P]),
+        "si_fused_decode_noalloc": (ctypes.c_int, [B, IX, AT, I32, P, P, ctypes.c_int, P,
+                                                   ctypes.POINTER(ctypes.c_void_p), P]),
         "si_workspace_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), P]),
         "si_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "si_last_error": (ctypes.c_char_p, []),
@@ -96,7 +98,8 @@ def load() -> ctypes.CDLL:
 load()
 
 EXPORTED = ("si_workspace_size", "si_workspace_min", "si_indexer_scores", "si_topk",
-            "si_sparse_attn", "si_fused_decode", "si_workspace_status", "si_status_string",
+            "si_sparse_attn", "si_fused_decode", "si_fused_decode_noalloc", "si_workspace_status",
+            "si_status_string",
             "si_last_error", "si_version", "si_launch_count")
 
 
@@ -237,6 +240,29 @@ def fused_decode(b: Batch, ix: Indexer, at: Attention, k_top: int, idx: torch.Te
     _check(load().si_fused_decode(ctypes.byref(cb), ctypes.byref(ci), ctypes.byref(ca), k_top,
                                   _ptr(idx), _ptr(out), _out_dtype(out), _ptr(lse), _ptr(ws),
                                   ws.numel(), _stream(stream)))
+
+
+def fused_decode_noalloc(b: Batch, ix: Indexer, at: Attention, k_top: int, idx: torch.Tensor,
+                         out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                         stream=None) -> int:
+    """si_fused_decode_noalloc: the fused path on the library's static scratch
+    (nothing is allocated).  Returns the scratch's device address, which
+    ``workspace_status_at`` reads.  Overlapping calls on one device race."""
+    cb, ci, ca = b.c(), ix.c(), at.c()
+    scratch = ctypes.c_void_p(0)
+    _check(load().si_fused_decode_noalloc(ctypes.byref(cb), ctypes.byref(ci), ctypes.byref(ca),
+                                          k_top, _ptr(idx), _ptr(out), _out_dtype(out),
+                                          _ptr(lse), ctypes.byref(scratch), _stream(stream)))
+    return int(scratch.value or 0)
+
+
+def workspace_status_at(addr: int, stream=None) -> int:
+    """Synchronise and return the device flags of the status word at `addr`."""
+    flags = ctypes.c_uint32(0)
+    st = load().si_workspace_status(addr, ctypes.byref(flags), _stream(stream))
+    if st not in (0, 5):
+        _check(st)
+    return int(flags.value)
 
 
 def launch_count() -> int:

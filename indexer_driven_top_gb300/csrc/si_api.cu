@@ -34,6 +34,19 @@ si_status fail(si_status s, const char *fmt, ...)
     return s;
 }
 
+}  // namespace
+
+si_status si::set_error(si_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+namespace {
+
 si_status cuda_fail(cudaError_t e, const char *what)
 {
     return fail(SI_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -190,6 +203,27 @@ si_status run_attn(const si_batch &b, const si_attention &at, const int32_t *idx
     return e == cudaSuccess ? SI_OK : cuda_fail(e, "attention launch");
 }
 
+}  // namespace
+
+si_status si::check_fused_args(const si_batch *b, const si_indexer *ix, const si_attention *at,
+                               int32_t k_top, const int32_t *idx, const void *out,
+                               si_dtype out_dtype)
+{
+    si_status st = check_batch(b);
+    if (st != SI_OK || b->n_q == 0)
+        return st;
+    if ((st = check_indexer(ix)) != SI_OK || (st = check_attention(at)) != SI_OK ||
+        (st = check_k(k_top)) != SI_OK)
+        return st;
+    if (!idx || !out)
+        return fail(SI_ERR_INVALID_ARG, "idx or out is NULL");
+    if (out_dtype != SI_F32 && out_dtype != SI_BF16)
+        return fail(SI_ERR_INVALID_ARG, "out dtype must be f32 or bf16");
+    return SI_OK;
+}
+
+namespace {
+
 size_t ws_need(si_op op, const si_batch *b, const si_indexer *ix, const si_attention *at,
                int32_t k_top, bool minimal)
 {
@@ -287,16 +321,9 @@ si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_atte
                           int32_t k_top, int32_t *idx, void *out, si_dtype out_dtype,
                           float *lse, void *ws, size_t ws_bytes, void *stream)
 {
-    si_status st = check_batch(b);
+    si_status st = si::check_fused_args(b, ix, at, k_top, idx, out, out_dtype);
     if (st != SI_OK || b->n_q == 0)
         return st;
-    if ((st = check_indexer(ix)) != SI_OK || (st = check_attention(at)) != SI_OK ||
-        (st = check_k(k_top)) != SI_OK)
-        return st;
-    if (!idx || !out)
-        return fail(SI_ERR_INVALID_ARG, "idx or out is NULL");
-    if (out_dtype != SI_F32 && out_dtype != SI_BF16)
-        return fail(SI_ERR_INVALID_ARG, "out dtype must be f32 or bf16");
     if ((st = check_ws(ws, ws_bytes, ws_need(SI_OP_FUSED, b, ix, at, k_top, true))) != SI_OK)
         return st;
     cudaStream_t s = (cudaStream_t)stream;

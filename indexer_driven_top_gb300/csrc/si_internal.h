@@ -11,6 +11,15 @@ namespace si {
 // Counts one kernel launch (process-wide diagnostic, see si_launch_count).
 void count_launch(int n = 1);
 
+// Records the calling thread's error detail (what si_last_error returns) and
+// passes `s` through.
+si_status set_error(si_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+
+// Host validation of si_fused_decode's arguments other than the workspace
+// (SI_OK for a valid or empty batch; records the error detail otherwise).
+si_status check_fused_args(const si_batch *b, const si_indexer *ix, const si_attention *at,
+                           int32_t k_top, const int32_t *idx, const void *out, si_dtype out_dtype);
+
 // Generic CUDA-core kernels: any supported dtype and shape, fp32 arithmetic.
 cudaError_t launch_indexer_generic(const si_batch &b, const si_indexer &ix, float *scores,
                                    int64_t ld, unsigned int *st, cudaStream_t s);
