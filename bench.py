@@ -143,6 +143,20 @@ def _kernel_traffic(kernel: str, source: str):
     return None
 
 
+def _kernel_of(wl):
+    """The CUDA kernel (and its source file) each step of the path runs for
+    this workload: the tensor-core kernels where their shape conditions hold
+    (64 x 128 indexer with bf16 q and e4m3 keys; 128 heads x 576 bf16 latent
+    rows), the generic ones otherwise."""
+    tc_ix = wl.Hi == 64 and wl.Di == 128 and wl.q_idx_dtype == "bf16" and wl.k_idx_dtype == "e4m3"
+    tc_at = wl.Hq == 128 and wl.Dqk == 576 and wl.Dv == 512 and wl.kv_dtype == "bf16"
+    return {"indexer": ("k_indexer_tc", "si_indexer_tc.cu") if tc_ix
+            else ("k_indexer_generic", "si_generic.cu"),
+            "topk": ("k_topk_rows", "si_topk.cu"),
+            "attn": ("k_attn_tc", "si_attn_tc.cu") if tc_at
+            else ("k_attn_generic", "si_generic.cu")}
+
+
 def cpu_baseline(wl, rows, threads):
     """The CPU oracle, as it stands, on a bounded sample of query rows."""
     import oracle
@@ -324,8 +338,7 @@ def run_si(args):
     algo = algorithmic_bytes(wl)
     mean_k = {k: sum(v) / len(v) for k, v in t_k.items()}
     dom = max(mean_k, key=mean_k.get)
-    src = {"indexer": "si_generic.cu", "topk": "si_topk.cu", "attn": "si_generic.cu"}[dom]
-    kname = {"indexer": "k_indexer_generic", "topk": "k_topk_rows", "attn": "k_attn_generic"}[dom]
+    kname, src = _kernel_of(wl)[dom]
     achieved = algo[dom] / (mean_k[dom] / 1e3) / 1e9
     roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
@@ -355,6 +368,7 @@ def run_si(args):
                 "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                 "frac_of_measured": step_gbs / peaks["hbm_gbs"]},
         "kernels_ms": mean_k,
+        "kernels": {k: v[0] for k, v in _kernel_of(wl).items()},
         "clocks": clk,
         "e2e": {"value": world * n_q / (e2e_ms / 1e3), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -371,8 +385,8 @@ def run_si(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["si", "reference"], default="si")
     ap.add_argument("--workload", default="c1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
