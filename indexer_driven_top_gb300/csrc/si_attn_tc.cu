@@ -14,9 +14,14 @@
 // processed in tiles of 128 (UMMA N = 128).  A tile's key rows stream through
 // shared memory as "dim chunks" of 128 keys x 64 dims (16 KB) in a three-slot
 // ring: nine chunks build S = q . k^T in TMEM (fp32, double-buffered), four
-// more (this CTA's 256 value dims) feed O += P . V.  Chunks are gathered by
-// eight loader warps with 16-byte vector loads that keep four chunks in
-// flight in registers, so the ring itself stays small.  The chunk sequence
+// more (this CTA's 256 value dims) feed O += P . V.  Eight loader warps
+// gather each chunk with 16-byte cp.async copies straight into its ring slot;
+// the copies signal the slot's mbarrier when they land, so no thread waits
+// on them and no register holds data in flight.  (Staging through registers
+// caps the stream: the proxy fence and the release arrive each loader must
+// issue per chunk also wait for that thread's outstanding loads, which
+// serialises the chunks.)  Three converter warps rewrite the value chunks
+// from bf16 to f16 in place.  The chunk sequence
 // interleaves S of tile t with P.V of tile t-1, so the tensor core computes
 // the next scores while the softmax warpgroup works on the current ones.
 //
@@ -57,10 +62,11 @@ constexpr int kChunksPerTile = kQChunks + kVChunks;  // 13
 constexpr int kRing = 3;
 constexpr int kLoaderWarps = 8;
 constexpr int kLoaders = kLoaderWarps * 32;
-constexpr int kInFlight = kRing;  // chunks in flight per loader thread (registers), one per slot
 constexpr int kWarpSoft0 = 8;     // softmax warps 8..11 (TMEM lanes by warp % 4)
 constexpr int kWarpMma = 12;
-constexpr int kThreads = 13 * 32;
+constexpr int kWarpConv0 = 13;    // value-chunk converters: warps 13..15
+constexpr int kConverters = 3 * 32;
+constexpr int kThreads = 16 * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 constexpr uint32_t kChunk = 128 * 128;           // 16 KB: 128 rows x 128 bytes, SW128
@@ -200,46 +206,46 @@ __device__ __forceinline__ void start_tile(LoaderState &ls, const si_batch &b, c
     load_idx(idx, r, k_top, tile + 2, T, n_valid, kr0, ls.sv2);
 }
 
-// Brings the next tile's key rows into L2 (each thread: its four rows, dim
-// chunks u and u + 8), so the chunk loads of that tile hit L2 instead of
-// paying a DRAM round trip per 128-byte piece.  Uses the lookahead entries
-// of tile + 1 (block table loaded one tile earlier).
-__device__ __forceinline__ void prefetch_next_tile(const LoaderState &ls, const si_batch &b,
-                                                   int pos, int64_t row_bytes, int u,
-                                                   const uint8_t *kv)
+// 16-byte global -> shared copy that lands asynchronously; src_bytes = 0
+// writes zeros without reading.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
 {
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int sp = ls.sv1[i], bk = ls.bk1[i];
-        if (sp >= 0 && sp <= pos && (unsigned)bk < (unsigned)b.n_blocks) {
-            const uint8_t *row = kv + ((int64_t)bk * b.page_size + sp % b.page_size) * row_bytes;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(row + u * 128));
-            if (u == 0)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 8 * 128));
-        }
-    }
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
 }
 
-// Issues the loads of chunk g into `bb` (one 16-byte unit of four key rows).
-__device__ __forceinline__ void issue_chunk(LoaderState &ls, uint4 (&bb)[4], const si_batch &b,
+// The mbarrier receives one arrival once all of this thread's earlier
+// cp.async copies have landed (its expected count includes these arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Issues this thread's copies of chunk g (one 16-byte unit of four key rows)
+// into the ring slot at `dst`.  The first chunk of a tile also publishes the
+// tile's key-valid bytes.
+__device__ __forceinline__ void issue_chunk(LoaderState &ls, uint32_t dst, const si_batch &b,
                                             const int32_t *idx, int r, int k_top, int T,
                                             int n_valid, int seq, int pos, int64_t row_bytes,
-                                            int kr0, int u, uint8_t *mask_s, unsigned int *st,
-                                            const uint8_t *kv, int half, int g)
+                                            int kr0, int u, uint8_t *mask_s, uint64_t *mask_bar,
+                                            unsigned int *st, const uint8_t *kv, int half, int g)
 {
     const ChunkId id = chunk_of(g, T, half);
-    if (id.tile > ls.have_tile)
+    if (id.tile > ls.have_tile) {
         start_tile(ls, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s, st,
                    id.tile);
-    if (id.v < 0 && id.c == 3 && id.tile + 1 < T)
-        prefetch_next_tile(ls, b, pos, row_bytes, u, kv);
+        mbar_arrive(mask_bar + (id.tile % kMaskSlots));
+    }
     const bool odd = id.tile & 1;
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         const int row = odd ? ls.rb1[i] : ls.rb0[i];
-        bb[i] = row >= 0 ? __ldg(reinterpret_cast<const uint4 *>(kv + (int64_t)row * row_bytes +
-                                                                 id.c * 128 + u * 16))
-                         : make_uint4(0, 0, 0, 0);
+        const uint8_t *src = row >= 0 ? kv + (int64_t)row * row_bytes + id.c * 128 + u * 16 : kv;
+        cp_async_16(dst + sw128_offset(kr0 + 32 * i, u), src, row >= 0 ? 16u : 0u);
     }
 }
 
@@ -251,7 +257,7 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
     uint8_t *mask_s = gbase + kOffMask;                                     // [kMaskSlots][128]
-    uint64_t *full_bar = reinterpret_cast<uint64_t *>(gbase + kOffBar);    // [kRing]
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(gbase + kOffBar);    // [kRing] score chunks
     uint64_t *empty_bar = full_bar + kRing;                                 // [kRing]
     uint64_t *sfull_bar = empty_bar + kRing;                                // [2]
     uint64_t *sempty_bar = sfull_bar + 2;                                   // [2]
@@ -259,7 +265,9 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
     uint64_t *qready_bar = mask_bar + kMaskSlots;
     uint64_t *pfull_bar = qready_bar + 1;
     uint64_t *pvdone_bar = pfull_bar + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pvdone_bar + 1);
+    uint64_t *vfull_bar = pvdone_bar + 1;                                   // [kVChunks]
+    uint64_t *conv_bar = vfull_bar + kVChunks;                              // [kVChunks]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(conv_bar + kVChunks);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = blockIdx.x >> 1, half = blockIdx.x & 1;
@@ -269,9 +277,17 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
     const int n_chunks = kChunksPerTile * T;
 
     if (tid == 0) {
+        // Landing barriers, one cp.async arrival per loader thread per phase:
+        // full_bar[slot] for score chunks (a phase per score chunk in that
+        // slot), vfull_bar[v] for value chunk v (a phase per key tile).  Each
+        // waiter observes every phase of the barriers it waits on, in order.
         for (int i = 0; i < kRing; i++) {
             mbar_init(full_bar + i, kLoaders);
             mbar_init(empty_bar + i, 1);
+        }
+        for (int i = 0; i < kVChunks; i++) {
+            mbar_init(vfull_bar + i, kLoaders);
+            mbar_init(conv_bar + i, kConverters);
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(sfull_bar + i, 1);
@@ -320,64 +336,22 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
         load_idx(idx, r, k_top, 0, T, n_valid, kr0, ls.sv1);
         load_blk(b, seq, pos, ls.sv1, ls.bk1);
         load_idx(idx, r, k_top, 1, T, n_valid, kr0, ls.sv2);
-        // Chunk g lives in register set g % 3 and ring slot g % 3; the loop
-        // is unrolled by three so both indices are compile-time constants.
-        uint4 buf0[4], buf1[4], buf2[4];
-        if (n_chunks > 0)
-            issue_chunk(ls, buf0, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s,
-                        st, kv, half, 0);
-        if (n_chunks > 1)
-            issue_chunk(ls, buf1, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s,
-                        st, kv, half, 1);
-        if (n_chunks > 2)
-            issue_chunk(ls, buf2, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s,
-                        st, kv, half, 2);
-        int mask_published = -1;
-        bool stop = false;
-        // store chunk g from bb into ring slot `slot`, then reload bb with chunk g + 3
-        auto step = [&](int g, uint4 (&bb)[4], int slot) {
+        for (int g = 0; g < n_chunks; g++) {
+            const int slot = g % kRing;
+            if (g >= kRing && !mbar_wait(empty_bar + slot, (uint32_t)((g / kRing) - 1) & 1, st))
+                break;
+            issue_chunk(ls, base + kOffRing + slot * kChunk, b, idx, r, k_top, T, n_valid, seq,
+                        pos, row_bytes, kr0, u, mask_s, mask_bar, st, kv, half, g);
             const ChunkId id = chunk_of(g, T, half);
-            if (g >= kRing && !mbar_wait(empty_bar + slot, (uint32_t)((g / kRing) - 1) & 1, st)) {
-                stop = true;
-                return;
-            }
-            const uint32_t dst = base + kOffRing + slot * kChunk;
-            const bool to_f16 = id.v >= 0;  // value chunks feed the f16 P.V product
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                uint4 x = bb[i];
-                if (to_f16) {
-                    x.x = bf16x2_to_f16x2(x.x);
-                    x.y = bf16x2_to_f16x2(x.y);
-                    x.z = bf16x2_to_f16x2(x.z);
-                    x.w = bf16x2_to_f16x2(x.w);
-                }
-                st_shared_v4(dst + sw128_offset(kr0 + 32 * i, u), x.x, x.y, x.z, x.w);
-            }
-            fence_async_smem();
-            mbar_arrive(full_bar + slot);
-            if (id.v < 0 && id.c == 0 && id.tile > mask_published) {
-                // every loader wrote its key-valid bytes in start_tile(), which
-                // ran when this chunk was issued
-                mask_published = id.tile;
-                mbar_arrive(mask_bar + (id.tile % kMaskSlots));
-            }
-            if (g + kRing < n_chunks)
-                issue_chunk(ls, bb, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u,
-                            mask_s, st, kv, half, g + kRing);
-        };
-        for (int g = 0; g < n_chunks && !stop; g += kRing) {
-            step(g, buf0, 0);
-            if (g + 1 < n_chunks && !stop)
-                step(g + 1, buf1, 1);
-            if (g + 2 < n_chunks && !stop)
-                step(g + 2, buf2, 2);
+            cp_async_arrive(id.v < 0 ? full_bar + slot : vfull_bar + id.v);
         }
+        cp_async_wait_all();  // nothing may land after the block has moved on
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA
         const uint32_t idesc_s = idesc_f16(kHeads, kTile, 1, 0, 0);   // bf16, K-major A/B
         const uint32_t idesc_pv = idesc_f16(kHeads, 64, 0, 0, 1);     // f16; B (V) MN-major
         bool ok = mbar_wait(qready_bar, 0, st);
+        uint32_t s_par = 0;  // phase parity of each slot's score-chunk landings
         for (int g = 0; ok && g < n_chunks; g++) {
             const ChunkId id = chunk_of(g, T, half);
             const int slot = g % kRing;
@@ -392,8 +366,17 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                 if (!mbar_wait(pfull_bar, (uint32_t)id.tile & 1, st))
                     break;
             }
-            if (!mbar_wait(full_bar + slot, (uint32_t)(g / kRing) & 1, st))
-                break;
+            if (id.v < 0) {
+                // score chunk: the loaders' copies have landed; make them
+                // visible to the tensor core (async proxy)
+                const uint32_t par = (s_par >> slot) & 1u;
+                s_par ^= 1u << slot;
+                if (!mbar_wait(full_bar + slot, par, st))
+                    break;
+                fence_async_smem();
+            } else if (!mbar_wait(conv_bar + id.v, (uint32_t)id.tile & 1, st)) {
+                break;  // value chunk: converted to f16 (the converters fenced)
+            }
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t chunk = base + kOffRing + slot * kChunk;
@@ -427,7 +410,28 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
             }
             __syncwarp();
         }
-    } else if (warp >= kWarpSoft0 && warp < kWarpSoft0 + 4) {
+    } else if (warp >= kWarpConv0) {
+        // ----------------------------------------------------------- converters
+        // Value chunks feed the f16 P.V product: rewrite them bf16 -> f16 in
+        // place once their copies have landed.
+        const int ct = tid - kWarpConv0 * 32;
+        for (int g = 0; g < n_chunks; g++) {
+            const ChunkId id = chunk_of(g, T, half);
+            if (id.v < 0)
+                continue;
+            const int slot = g % kRing;
+            if (!mbar_wait(vfull_bar + id.v, (uint32_t)id.tile & 1, st))
+                break;
+            const uint32_t src = base + kOffRing + slot * kChunk;
+            for (int i = ct; i < (int)(kChunk / 16); i += kConverters) {
+                const uint4 x = ld_shared_v4(src + i * 16);
+                st_shared_v4(src + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
+                             bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+            }
+            fence_async_smem();
+            mbar_arrive(conv_bar + id.v);
+        }
+    } else {
         // -------------------------------------------------------------- softmax
         const int h = tid - kWarpSoft0 * 32;   // head = TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
