@@ -8,31 +8,35 @@
 // row, V = its first 512 entries):
 //     out[r,h] = sum_j softmax_j(scale * q[r,h] . k[idx_j]) * v[idx_j]
 //
-// GB300 mapping.  One CTA per (query row, half of the 512 value dims).  The
-// 128 heads are the UMMA M dimension and stay resident in shared memory (the
-// whole 128 x 576 query, 147 KB, 128-byte swizzle).  Selected keys are
-// processed in tiles of 128 (UMMA N = 128).  A tile's key rows stream through
-// shared memory as "dim chunks" of 128 keys x 64 dims (16 KB) in a three-slot
-// ring: nine chunks build S = q . k^T in TMEM (fp32, double-buffered), four
-// more (this CTA's 256 value dims) feed O += P . V.  Eight loader warps
-// gather each chunk with 16-byte cp.async copies straight into its ring slot;
-// the copies signal the slot's mbarrier when they land, so no thread waits
-// on them and no register holds data in flight.  (Staging through registers
-// caps the stream: the proxy fence and the release arrive each loader must
-// issue per chunk also wait for that thread's outstanding loads, which
-// serialises the chunks.)  Three converter warps rewrite the value chunks
-// from bf16 to f16 in place.  The chunk sequence
-// interleaves S of tile t with P.V of tile t-1, so the tensor core computes
-// the next scores while the softmax warpgroup works on the current ones.
+// GB300 mapping.  Each query row gets a cluster of two CTAs with different
+// jobs, because one SM cannot hold the row's query (128 x 576 bf16, 147 KB of
+// shared memory), its output accumulator (128 x 512 fp32, all 512 TMEM
+// columns) and enough rows in flight at once:
 //
-// Softmax: one thread per head, online in the log2 domain with fp32 state; the
-// running maximum used for the exponent is only raised when a tile's maximum
-// exceeds it by more than 8 (then O is rescaled in TMEM), so most tiles need
-// no O traffic.  P is rounded to f16 (11 significant bits; bf16's 8 would
-// cost up to ~2^-9 of the value spread when few keys dominate) and the
-// denominator sums the same rounded values.  The P.V operands must share a
-// type, so value chunks are converted from bf16 to f16 as they are stored
-// (exact for 2^-14 <= |v| <= 65504).  Positions that are -1 or outside
+//   score CTA (rank 0) -- keeps the whole query in shared memory (128-byte
+//       swizzle) and streams the selected keys through a five-slot ring in
+//       "dim chunks" of 128 keys x 64 dims (16 KB).  Nine chunks build the
+//       tile's logits S = q . k^T (UMMA M = 128 heads, N = 128 keys) in TMEM
+//       (double-buffered).  Its softmax warpgroup (one thread per head) turns
+//       a tile into weights P (f16) and writes them, with one rescale factor
+//       per head, straight into the value CTA's shared memory.
+//   value CTA (rank 1) -- keeps O (128 heads x 512 value dims, fp32) in TMEM
+//       and streams the same rows' first 512 entries through a five-slot ring
+//       of 128-dim groups (32 KB).  Three warps rewrite each group from bf16
+//       to f16 in place (P.V needs one operand type), the MMA warp issues
+//       O[:, group] += P . V_group (N = 128), and a warpgroup applies the
+//       score CTA's rescale factors to O between tiles and normalises at the
+//       end.
+//
+// Rows are gathered by eight loader warps per CTA with 16-byte cp.async
+// copies straight into ring slots; the copies arrive on the slot's mbarrier
+// when they land, so no thread stalls on them.  Every wait is bounded.
+//
+// Softmax: online in the log2 domain with fp32 state; the exponent reference
+// is only raised when a tile's maximum exceeds it by more than 8, so most
+// tiles leave O untouched.  P is rounded to f16 (11 significant bits) and the
+// denominator sums the same rounded values.  Value rows are converted bf16 ->
+// f16 (exact for 2^-14 <= |v| <= 65504).  Positions that are -1 or outside
 // 0..pos get zero rows and zero weight.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -51,69 +55,62 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kHeads = 128;       // query heads = UMMA M
-constexpr int kDqk = 576;         // logit dims
-constexpr int kDv = 512;          // value dims
-constexpr int kDvHalf = 256;      // value dims per CTA
-constexpr int kTile = 128;        // selected keys per tile = UMMA N of S
-constexpr int kQChunks = kDqk / 64;   // 9 dim chunks of 64
-constexpr int kVChunks = kDvHalf / 64; // 4
-constexpr int kChunksPerTile = kQChunks + kVChunks;  // 13
-constexpr int kRing = 3;
+constexpr int kHeads = 128;              // query heads = UMMA M
+constexpr int kDqk = 576;                // logit dims
+constexpr int kDv = 512;                 // value dims
+constexpr int kTile = 128;               // selected keys per tile
+constexpr int kQChunks = kDqk / 64;      // 9 score chunks per tile
+constexpr int kVGroups = kDv / 128;      // 4 value groups per tile
+constexpr uint32_t kChunk = 128 * 128;   // 16 KB: 128 rows x 128 bytes, SW128
+constexpr uint32_t kGroup = 2 * kChunk;  // 32 KB: 128 keys x 128 value dims
+
 constexpr int kLoaderWarps = 8;
 constexpr int kLoaders = kLoaderWarps * 32;
-constexpr int kWarpSoft0 = 8;     // softmax warps 8..11 (TMEM lanes by warp % 4)
+constexpr int kWarpQuad = 8;      // warps 8..11 (TMEM lanes by warp % 4)
 constexpr int kWarpMma = 12;
-constexpr int kWarpConv0 = 13;    // value-chunk converters: warps 13..15
+constexpr int kWarpConv0 = 13;    // value CTA: converters, warps 13..15
 constexpr int kConverters = 3 * 32;
 constexpr int kThreads = 16 * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
-constexpr uint32_t kChunk = 128 * 128;           // 16 KB: 128 rows x 128 bytes, SW128
-constexpr uint32_t kOffQ = 0;                      // kQChunks x [128 heads x 64 dims]
-constexpr uint32_t kOffP = kOffQ + kQChunks * kChunk;   // 2 x [128 heads x 64 keys]
-constexpr uint32_t kOffRing = kOffP + 2 * kChunk;       // kRing x [128 keys x 64 dims]
-constexpr int kMaskSlots = 4;
-constexpr uint32_t kOffMask = kOffRing + kRing * kChunk;  // kMaskSlots x 128 key-valid bytes
-constexpr uint32_t kOffBar = kOffMask + kMaskSlots * kTile;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // + alignment slack
+// score CTA layout
+constexpr int kRingS = 5;
+constexpr uint32_t kOffQ = 0;                                  // 9 x [128 heads x 64 dims]
+constexpr uint32_t kOffRingS = kQChunks * kChunk;              // kRingS x [128 keys x 64 dims]
+constexpr uint32_t kOffMask = kOffRingS + kRingS * kChunk;     // 4 tiles x 4 key-valid words
+// value CTA layout
+constexpr int kRingV = 5;
+constexpr uint32_t kOffP = 0;                                  // 2 x (2 x [128 heads x 64 keys])
+constexpr uint32_t kOffRingV = 4 * kChunk;                     // kRingV x (2 x [128 keys x 64 dims])
+constexpr uint32_t kOffF = kOffRingV + kRingV * kGroup;        // 2 x 128 floats
+// both
+constexpr uint32_t kOffBar = kOffF + 2 * kHeads * 4;
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;          // + alignment slack
+static_assert(kOffMask + 4 * 4 * 4 <= kOffBar, "mask words overlap the barriers");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
-// TMEM columns: O (this CTA's 256 value dims) then two S buffers.
-constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemCols = 512;
-
-struct ChunkId {
-    int tile;  // key tile
-    int v;     // -1: score chunk, else value chunk 0..3
-    int c;     // dim chunk index of the row (0..8)
+// mbarriers: one array at kOffBar in both CTAs (a barrier that the other CTA
+// arrives on lives at the same offset in both)
+enum : int {
+    B_FULL = 0,     // [ring] copies of a ring slot landed (cp.async arrivals)
+    B_EMPTY = 5,    // [ring] ring slot consumed (MMA commit)
+    B_CONV = 10,    // [ring] value: group converted to f16
+    B_SFULL = 15,   // [2] score: S of a tile complete
+    B_SEMPTY = 17,  // [2] score: softmax done with an S buffer
+    B_MASK = 19,    // [4] score: key-valid words of a tile written
+    B_QREADY = 23,  // score: query resident
+    B_PEMPTY = 24,  // [2] score: value CTA finished P.V from a P buffer (remote commit)
+    B_PFULL = 26,   // [2] value: P and factors of a tile written (remote arrivals)
+    B_OCORR = 28,   // value: O rescaled (if needed) for the next tile
+    B_PVDONE = 29,  // value: P.V of a tile complete
+    B_FINAL = 30,   // value: row sums l written (remote arrivals)
+    B_COUNT = 31
 };
-
-// g-th chunk of the stream: S(0); then per t >= 1: S(t), V(t-1); finally V(T-1).
-__device__ __forceinline__ ChunkId chunk_of(int g, int T, int half)
-{
-    ChunkId id;
-    if (g < kQChunks) {
-        id.tile = 0;
-        id.v = -1;
-        id.c = g;
-        return id;
-    }
-    const int h = g - kQChunks;
-    const int blk = h / kChunksPerTile + 1, o = h % kChunksPerTile;
-    if (blk < T && o < kQChunks) {
-        id.tile = blk;
-        id.v = -1;
-        id.c = o;
-    } else {
-        const int vv = blk < T ? o - kQChunks : o;
-        id.tile = blk - 1;
-        id.v = vv;
-        id.c = half * kVChunks + vv;
-    }
-    return id;
-}
+constexpr uint32_t kTmemSlot = 8 * 32;  // byte offset of the TMEM base within the barrier area
+static_assert(B_COUNT * 8 <= (int)kTmemSlot, "barrier area");
 
 // 2^x with the hardware approximation (ex2.approx: ~2 ulp), ample for a
-// softmax whose weights are rounded to bf16.
+// softmax whose weights are rounded to f16.
 __device__ __forceinline__ float ex2(float x)
 {
     float y;
@@ -139,9 +136,29 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
     return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// Loader state of one thread: physical row byte offsets of its four keys for
-// the even and the odd tile in flight, and the two-tile lookahead (index list
-// values of tile t+2, block-table entries of tile t+1).
+// 16-byte global -> shared copy that lands asynchronously; src_bytes = 0
+// writes zeros without reading.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// The mbarrier receives one arrival once all of this thread's earlier
+// cp.async copies have landed (its expected count includes these arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Loader state of one thread: physical rows of its four keys (kr0 + 32 i)
+// for the even and the odd tile, and the lookahead (index-list values of
+// tile t+2, block-table entries of tile t+1) so that the dependent lookups
+// never stall the stream.
 struct LoaderState {
     int rb0[4], rb1[4];  // physical rows (< 2^31), -1 = zero row
     int sv1[4], bk1[4], sv2[4];
@@ -171,15 +188,24 @@ __device__ __forceinline__ void load_blk(const si_batch &b, int seq, int pos, co
     }
 }
 
-// Makes `tile` current: row offsets and key-valid bytes from the lookahead,
-// then shifts the lookahead by one tile.
+__device__ __forceinline__ void loader_init(LoaderState &ls, const si_batch &b, const int32_t *idx,
+                                            int r, int k_top, int T, int n_valid, int seq, int pos,
+                                            int kr0)
+{
+    ls.have_tile = -1;
+    load_idx(idx, r, k_top, 0, T, n_valid, kr0, ls.sv1);
+    load_blk(b, seq, pos, ls.sv1, ls.bk1);
+    load_idx(idx, r, k_top, 1, T, n_valid, kr0, ls.sv2);
+}
+
+// Makes `tile` current: row offsets (and, if `mask` is given, the tile's
+// key-valid bits) from the lookahead, then shifts the lookahead by a tile.
 __device__ __forceinline__ void start_tile(LoaderState &ls, const si_batch &b, const int32_t *idx,
                                            int r, int k_top, int T, int n_valid, int seq, int pos,
-                                           int64_t row_bytes, int kr0, int u, uint8_t *mask_s,
-                                           unsigned int *st, int tile)
+                                           int kr0, int u, uint32_t *mask, unsigned int *st,
+                                           int tile)
 {
     ls.have_tile = tile;
-    uint8_t *mb = mask_s + (tile % kMaskSlots) * kTile;
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         const int sp = ls.sv1[i], bk = ls.bk1[i];
@@ -196,8 +222,13 @@ __device__ __forceinline__ void start_tile(LoaderState &ls, const si_batch &b, c
             ls.rb1[i] = off;
         else
             ls.rb0[i] = off;
-        if (u == 0)
-            mb[kr0 + 32 * i] = ok ? 1 : 0;
+        // key kr0 + 32 i is bit kr0 of word i; only this thread touches it
+        if (mask && u == 0) {
+            if (ok)
+                atomicOr(mask + i, 1u << kr0);
+            else
+                atomicAnd(mask + i, ~(1u << kr0));
+        }
     }
 #pragma unroll
     for (int i = 0; i < 4; i++)
@@ -206,269 +237,250 @@ __device__ __forceinline__ void start_tile(LoaderState &ls, const si_batch &b, c
     load_idx(idx, r, k_top, tile + 2, T, n_valid, kr0, ls.sv2);
 }
 
-// 16-byte global -> shared copy that lands asynchronously; src_bytes = 0
-// writes zeros without reading.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
+// This thread's copies of dim chunk c (16-byte unit u of its four key rows)
+// of the current tile into the 16 KB chunk buffer at `dst`.
+__device__ __forceinline__ void issue_chunk(const LoaderState &ls, uint32_t dst, const uint8_t *kv,
+                                            int64_t row_bytes, int tile, int c, int kr0, int u)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
-// The mbarrier receives one arrival once all of this thread's earlier
-// cp.async copies have landed (its expected count includes these arrivals).
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// Issues this thread's copies of chunk g (one 16-byte unit of four key rows)
-// into the ring slot at `dst`.  The first chunk of a tile also publishes the
-// tile's key-valid bytes.
-__device__ __forceinline__ void issue_chunk(LoaderState &ls, uint32_t dst, const si_batch &b,
-                                            const int32_t *idx, int r, int k_top, int T,
-                                            int n_valid, int seq, int pos, int64_t row_bytes,
-                                            int kr0, int u, uint8_t *mask_s, uint64_t *mask_bar,
-                                            unsigned int *st, const uint8_t *kv, int half, int g)
-{
-    const ChunkId id = chunk_of(g, T, half);
-    if (id.tile > ls.have_tile) {
-        start_tile(ls, b, idx, r, k_top, T, n_valid, seq, pos, row_bytes, kr0, u, mask_s, st,
-                   id.tile);
-        mbar_arrive(mask_bar + (id.tile % kMaskSlots));
-    }
-    const bool odd = id.tile & 1;
+    const bool odd = tile & 1;
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         const int row = odd ? ls.rb1[i] : ls.rb0[i];
-        const uint8_t *src = row >= 0 ? kv + (int64_t)row * row_bytes + id.c * 128 + u * 16 : kv;
+        const uint8_t *src = row >= 0 ? kv + (int64_t)row * row_bytes + c * 128 + u * 16 : kv;
         cp_async_16(dst + sw128_offset(kr0 + 32 * i, u), src, row >= 0 ? 16u : 0u);
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
           si_dtype out_dtype, float *lse, unsigned int *st)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
-    uint8_t *mask_s = gbase + kOffMask;                                     // [kMaskSlots][128]
-    uint64_t *full_bar = reinterpret_cast<uint64_t *>(gbase + kOffBar);    // [kRing] score chunks
-    uint64_t *empty_bar = full_bar + kRing;                                 // [kRing]
-    uint64_t *sfull_bar = empty_bar + kRing;                                // [2]
-    uint64_t *sempty_bar = sfull_bar + 2;                                   // [2]
-    uint64_t *mask_bar = sempty_bar + 2;                                    // [kMaskSlots]
-    uint64_t *qready_bar = mask_bar + kMaskSlots;
-    uint64_t *pfull_bar = qready_bar + 1;
-    uint64_t *pvdone_bar = pfull_bar + 1;
-    uint64_t *vfull_bar = pvdone_bar + 1;                                   // [kVChunks]
-    uint64_t *conv_bar = vfull_bar + kVChunks;                              // [kVChunks]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(conv_bar + kVChunks);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + kOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffBar + kTmemSlot);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = blockIdx.x >> 1, half = blockIdx.x & 1;
+    const uint32_t rank = cluster_rank();   // 0: score CTA, 1: value CTA
+    const bool score_cta = rank == 0;
+    const int r = blockIdx.x >> 1;
     const int pos = __ldg(b.q_pos + r), seq = __ldg(b.q_seq + r);
     const int n_valid = max(0, min(k_top, pos + 1));
     const int T = (n_valid + kTile - 1) / kTile;  // key tiles
-    const int n_chunks = kChunksPerTile * T;
 
     if (tid == 0) {
-        // Landing barriers, one cp.async arrival per loader thread per phase:
-        // full_bar[slot] for score chunks (a phase per score chunk in that
-        // slot), vfull_bar[v] for value chunk v (a phase per key tile).  Each
-        // waiter observes every phase of the barriers it waits on, in order.
-        for (int i = 0; i < kRing; i++) {
-            mbar_init(full_bar + i, kLoaders);
-            mbar_init(empty_bar + i, 1);
-        }
-        for (int i = 0; i < kVChunks; i++) {
-            mbar_init(vfull_bar + i, kLoaders);
-            mbar_init(conv_bar + i, kConverters);
+        for (int i = 0; i < kRingS; i++) {
+            mbar_init(bars + B_FULL + i, kLoaders);
+            mbar_init(bars + B_EMPTY + i, 1);
+            mbar_init(bars + B_CONV + i, kConverters);
         }
         for (int i = 0; i < 2; i++) {
-            mbar_init(sfull_bar + i, 1);
-            mbar_init(sempty_bar + i, 128);
+            mbar_init(bars + B_SFULL + i, 1);
+            mbar_init(bars + B_SEMPTY + i, kHeads);
+            mbar_init(bars + B_PEMPTY + i, 1);
+            mbar_init(bars + B_PFULL + i, kHeads);
         }
-        for (int i = 0; i < kMaskSlots; i++)
-            mbar_init(mask_bar + i, kLoaders);
-        mbar_init(qready_bar, kLoaders);
-        mbar_init(pfull_bar, 128);
-        mbar_init(pvdone_bar, 1);
+        for (int i = 0; i < 4; i++)
+            mbar_init(bars + B_MASK + i, kLoaders);
+        mbar_init(bars + B_QREADY, kLoaders);
+        mbar_init(bars + B_OCORR, kHeads);
+        mbar_init(bars + B_PVDONE, 1);
+        mbar_init(bars + B_FINAL, kHeads);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
-        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_alloc(tmem_slot, score_cta ? 256u : 512u);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrival
     const uint32_t tmem = *tmem_slot;
 
     const uint8_t *kv = static_cast<const uint8_t *>(at.k.data);
     const int64_t row_bytes = at.k.row_stride * 2;
+    // value-CTA buffers as seen from the score CTA
+    const uint32_t peer_p = mapa_shared(base + kOffP, 1);
+    const uint32_t peer_f = mapa_shared(base + kOffF, 1);
+    const uint32_t peer_pfull = mapa_shared(smem_u32(bars + B_PFULL), 1);
+    const uint32_t peer_final = mapa_shared(smem_u32(bars + B_FINAL), 1);
 
     if (warp < kLoaderWarps) {
         // -------------------------------------------------------------- loaders
-        // Thread t owns 16-byte unit u = t & 7 of key rows kr_i = (t >> 3) + 32 i
-        // in every chunk.
+        // Thread t owns 16-byte unit u = t & 7 of key rows (t >> 3) + 32 i.
         const int u = tid & 7, kr0 = tid >> 3;
-        // query: 128 heads x 9 chunks x 8 units, SW128 K-major per chunk
-        {
-            const uint4 *qsrc = reinterpret_cast<const uint4 *>(at.q) + (int64_t)r * kHeads * (kDqk / 8);
-            for (int i = tid; i < kHeads * kQChunks * 8; i += kLoaders) {
-                const int h = i / (kQChunks * 8), rem = i % (kQChunks * 8);
-                const int c = rem >> 3, uu = rem & 7;
-                const uint4 v = __ldg(qsrc + (int64_t)h * (kDqk / 8) + rem);
-                st_shared_v4(base + kOffQ + c * kChunk + sw128_offset(h, uu), v.x, v.y, v.z, v.w);
-            }
-            fence_async_smem();
-            mbar_arrive(qready_bar);
-        }
-        // Physical rows of this thread's 4 keys are looked up two tiles ahead
-        // (LoaderState) so the dependent loads never stall the stream.
         LoaderState ls;
-        ls.have_tile = -1;
-        load_idx(idx, r, k_top, 0, T, n_valid, kr0, ls.sv1);
-        load_blk(b, seq, pos, ls.sv1, ls.bk1);
-        load_idx(idx, r, k_top, 1, T, n_valid, kr0, ls.sv2);
-        for (int g = 0; g < n_chunks; g++) {
-            const int slot = g % kRing;
-            if (g >= kRing && !mbar_wait(empty_bar + slot, (uint32_t)((g / kRing) - 1) & 1, st))
-                break;
-            issue_chunk(ls, base + kOffRing + slot * kChunk, b, idx, r, k_top, T, n_valid, seq,
-                        pos, row_bytes, kr0, u, mask_s, mask_bar, st, kv, half, g);
-            const ChunkId id = chunk_of(g, T, half);
-            cp_async_arrive(id.v < 0 ? full_bar + slot : vfull_bar + id.v);
+        if (score_cta) {
+            {
+                // query: 128 heads x 9 chunks x 8 units, SW128 K-major per chunk
+                const uint4 *qsrc =
+                    reinterpret_cast<const uint4 *>(at.q) + (int64_t)r * kHeads * (kDqk / 8);
+                for (int i = tid; i < kHeads * kQChunks * 8; i += kLoaders) {
+                    const int h = i / (kQChunks * 8), rem = i % (kQChunks * 8);
+                    const int c = rem >> 3, uu = rem & 7;
+                    const uint4 v = __ldg(qsrc + (int64_t)h * (kDqk / 8) + rem);
+                    st_shared_v4(base + kOffQ + c * kChunk + sw128_offset(h, uu), v.x, v.y, v.z,
+                                 v.w);
+                }
+                fence_async_smem();
+                mbar_arrive(bars + B_QREADY);
+            }
+            uint32_t *mask = reinterpret_cast<uint32_t *>(gbase + kOffMask);
+            loader_init(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0);
+            const int n_chunks = kQChunks * T;
+            for (int g = 0; g < n_chunks; g++) {
+                const int slot = g % kRingS, tile = g / kQChunks, c = g % kQChunks;
+                if (g >= kRingS &&
+                    !mbar_wait(bars + B_EMPTY + slot, (uint32_t)((g / kRingS) - 1) & 1, st))
+                    break;
+                if (tile > ls.have_tile) {
+                    start_tile(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0, u,
+                               mask + (tile % 4) * 4, st, tile);
+                    mbar_arrive(bars + B_MASK + (tile % 4));
+                }
+                issue_chunk(ls, base + kOffRingS + slot * kChunk, kv, row_bytes, tile, c, kr0, u);
+                cp_async_arrive(bars + B_FULL + slot);
+            }
+        } else {
+            loader_init(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0);
+            const int n_groups = kVGroups * T;
+            for (int g = 0; g < n_groups; g++) {
+                const int slot = g % kRingV, tile = g / kVGroups, j = g % kVGroups;
+                if (g >= kRingV &&
+                    !mbar_wait(bars + B_EMPTY + slot, (uint32_t)((g / kRingV) - 1) & 1, st))
+                    break;
+                if (tile > ls.have_tile)
+                    start_tile(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0, u, nullptr, st,
+                               tile);
+                const uint32_t dst = base + kOffRingV + slot * kGroup;
+                issue_chunk(ls, dst, kv, row_bytes, tile, 2 * j, kr0, u);
+                issue_chunk(ls, dst + kChunk, kv, row_bytes, tile, 2 * j + 1, kr0, u);
+                cp_async_arrive(bars + B_FULL + slot);
+            }
         }
         cp_async_wait_all();  // nothing may land after the block has moved on
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA
-        const uint32_t idesc_s = idesc_f16(kHeads, kTile, 1, 0, 0);   // bf16, K-major A/B
-        const uint32_t idesc_pv = idesc_f16(kHeads, 64, 0, 0, 1);     // f16; B (V) MN-major
-        bool ok = mbar_wait(qready_bar, 0, st);
-        uint32_t s_par = 0;  // phase parity of each slot's score-chunk landings
-        for (int g = 0; ok && g < n_chunks; g++) {
-            const ChunkId id = chunk_of(g, T, half);
-            const int slot = g % kRing;
-            if (id.v < 0 && id.c == 0) {
+        if (score_cta) {
+            const uint32_t idesc = idesc_f16(kHeads, kTile, 1, 0, 0);  // bf16, K-major A/B
+            bool ok = mbar_wait(bars + B_QREADY, 0, st);
+            const int n_chunks = kQChunks * T;
+            for (int g = 0; ok && g < n_chunks; g++) {
+                const int slot = g % kRingS, tile = g / kQChunks, c = g % kQChunks;
                 // S buffer of this tile must be free (softmax read S of tile - 2)
-                if (id.tile >= 2 &&
-                    !mbar_wait(sempty_bar + (id.tile & 1), (uint32_t)((id.tile >> 1) - 1) & 1, st))
+                if (c == 0 && tile >= 2 &&
+                    !mbar_wait(bars + B_SEMPTY + (tile & 1), (uint32_t)((tile >> 1) - 1) & 1, st))
                     break;
-            }
-            if (id.v == 0) {
-                // P of this tile is in shared memory
-                if (!mbar_wait(pfull_bar, (uint32_t)id.tile & 1, st))
+                if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingS) & 1, st))
                     break;
-            }
-            if (id.v < 0) {
-                // score chunk: the loaders' copies have landed; make them
-                // visible to the tensor core (async proxy)
-                const uint32_t par = (s_par >> slot) & 1u;
-                s_par ^= 1u << slot;
-                if (!mbar_wait(full_bar + slot, par, st))
-                    break;
-                fence_async_smem();
-            } else if (!mbar_wait(conv_bar + id.v, (uint32_t)id.tile & 1, st)) {
-                break;  // value chunk: converted to f16 (the converters fenced)
-            }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t chunk = base + kOffRing + slot * kChunk;
-                if (id.v < 0) {
-                    const uint32_t d = tmem + kTmemS + (id.tile & 1) * kTile;
+                fence_async_smem();  // landed copies -> tensor core (async proxy)
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t d = tmem + (tile & 1) * kTile;
+                    const uint32_t chunk = base + kOffRingS + slot * kChunk;
 #pragma unroll
                     for (int kk = 0; kk < 4; kk++) {
-                        const uint64_t ad = smem_desc(base + kOffQ + id.c * kChunk + kk * 32, 16,
-                                                      1024, kSwizzle128B);
+                        const uint64_t ad =
+                            smem_desc(base + kOffQ + c * kChunk + kk * 32, 16, 1024, kSwizzle128B);
                         const uint64_t bd = smem_desc(chunk + kk * 32, 16, 1024, kSwizzle128B);
-                        umma_f16_ss(d, ad, bd, idesc_s, id.c > 0 || kk > 0);
+                        umma_f16_ss(d, ad, bd, idesc, c > 0 || kk > 0);
                     }
-                    umma_commit(empty_bar + slot);
-                    if (id.c == kQChunks - 1)
-                        umma_commit(sfull_bar + (id.tile & 1));
-                } else {
-                    // O[:, 64 v .. +64] += P[128 x 128 keys] . V_chunk[128 keys x 64]
-                    const uint32_t d = tmem + kTmemO + id.v * 64;
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; kk++) {
-                        const uint64_t ad = smem_desc(base + kOffP + (kk >> 2) * kChunk +
-                                                          (kk & 3) * 32,
-                                                      16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(chunk + kk * 2048, 4096, 1024, kSwizzle128B);
-                        umma_f16_ss(d, ad, bd, idesc_pv, id.tile > 0 || kk > 0);
-                    }
-                    umma_commit(empty_bar + slot);
-                    if (id.v == kVChunks - 1)
-                        umma_commit(pvdone_bar);
+                    umma_commit(bars + B_EMPTY + slot);
+                    if (c == kQChunks - 1)
+                        umma_commit(bars + B_SFULL + (tile & 1));
                 }
+                __syncwarp();
             }
-            __syncwarp();
+        } else {
+            // O[:, 128 j .. +128] += P[128 heads x 128 keys] . V_group j
+            const uint32_t idesc = idesc_f16(kHeads, 128, 0, 0, 1);  // f16; B (V) MN-major
+            bool ok = true;
+            for (int t = 0; ok && t < T; t++) {
+                const int pb = t & 1;
+                if (!mbar_wait_cluster(bars + B_PFULL + pb, (uint32_t)(t >> 1) & 1, st) ||
+                    !mbar_wait(bars + B_OCORR, (uint32_t)t & 1, st))
+                    break;
+                fence_async_smem();  // P written by the score CTA -> tensor core
+                for (int j = 0; j < kVGroups; j++) {
+                    const int g = t * kVGroups + j, slot = g % kRingV;
+                    if (!mbar_wait(bars + B_CONV + slot, (uint32_t)(g / kRingV) & 1, st)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t grp = base + kOffRingV + slot * kGroup;
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; kk++) {
+                            const uint64_t ad =
+                                smem_desc(base + kOffP + pb * 2 * kChunk + (kk >> 2) * kChunk +
+                                              (kk & 3) * 32,
+                                          16, 1024, kSwizzle128B);
+                            const uint64_t bd =
+                                smem_desc(grp + kk * 2048, kChunk, 1024, kSwizzle128B);
+                            umma_f16_ss(tmem + 128 * j, ad, bd, idesc, t > 0 || kk > 0);
+                        }
+                        umma_commit(bars + B_EMPTY + slot);
+                    }
+                    __syncwarp();
+                }
+                if (!ok)
+                    break;
+                if (lane == 0) {
+                    umma_commit(bars + B_PVDONE);
+                    umma_commit_multicast(bars + B_PEMPTY + pb, 0x1);  // P buffer free (score CTA)
+                }
+                __syncwarp();
+            }
         }
     } else if (warp >= kWarpConv0) {
         // ----------------------------------------------------------- converters
-        // Value chunks feed the f16 P.V product: rewrite them bf16 -> f16 in
-        // place once their copies have landed.
-        const int ct = tid - kWarpConv0 * 32;
-        for (int g = 0; g < n_chunks; g++) {
-            const ChunkId id = chunk_of(g, T, half);
-            if (id.v < 0)
-                continue;
-            const int slot = g % kRing;
-            if (!mbar_wait(vfull_bar + id.v, (uint32_t)id.tile & 1, st))
-                break;
-            const uint32_t src = base + kOffRing + slot * kChunk;
-            for (int i = ct; i < (int)(kChunk / 16); i += kConverters) {
-                const uint4 x = ld_shared_v4(src + i * 16);
-                st_shared_v4(src + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
-                             bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+        if (!score_cta) {
+            const int ct = tid - kWarpConv0 * 32;
+            const int n_groups = kVGroups * T;
+            for (int g = 0; g < n_groups; g++) {
+                const int slot = g % kRingV;
+                if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingV) & 1, st))
+                    break;
+                const uint32_t src = base + kOffRingV + slot * kGroup;
+                for (int i = ct; i < (int)(kGroup / 16); i += kConverters) {
+                    const uint4 x = ld_shared_v4(src + i * 16);
+                    st_shared_v4(src + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
+                                 bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+                }
+                fence_async_smem();
+                mbar_arrive(bars + B_CONV + slot);
             }
-            fence_async_smem();
-            mbar_arrive(conv_bar + id.v);
         }
-    } else {
+    } else if (score_cta) {
         // -------------------------------------------------------------- softmax
-        const int h = tid - kWarpSoft0 * 32;   // head = TMEM lane
+        const int h = tid - kWarpQuad * 32;  // head = TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const float sl2 = at.softmax_scale * 1.4426950408889634f;  // scale * log2(e)
+        const uint32_t *mask = reinterpret_cast<const uint32_t *>(gbase + kOffMask);
         float m_used = -INFINITY;  // exponent reference (log2 units)
         float l = 0.f;
         bool ok = true;
         for (int t = 0; t < T && ok; t++) {
             const int sb = t & 1;
-            if (!mbar_wait(mask_bar + (t % kMaskSlots), (uint32_t)(t / kMaskSlots) & 1, st) ||
-                !mbar_wait(sfull_bar + sb, (uint32_t)(t >> 1) & 1, st)) {
+            if (!mbar_wait(bars + B_MASK + (t % 4), (uint32_t)(t / 4) & 1, st) ||
+                !mbar_wait(bars + B_SFULL + sb, (uint32_t)(t >> 1) & 1, st)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // key-valid bits of the tile (bytes 0/1 -> one bit per key)
             uint32_t mw[4];
-            {
-                const uint32_t *mb = reinterpret_cast<const uint32_t *>(mask_s + (t % kMaskSlots) * kTile);
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    uint32_t bits = 0;
-#pragma unroll
-                    for (int w = 0; w < 8; w++) {
-                        const uint32_t x = mb[q * 8 + w];
-                        bits |= ((x & 1u) | ((x >> 7) & 2u) | ((x >> 14) & 4u) | ((x >> 21) & 8u))
-                                << (4 * w);
-                    }
-                    mw[q] = bits;
-                }
-            }
+            for (int q = 0; q < 4; q++)
+                mw[q] = mask[(t % 4) * 4 + q];
             // pass 1: tile maximum of the valid logits
             float tmax = -INFINITY;
 #pragma unroll 1
             for (int q = 0; q < 4; q++) {
                 uint32_t v[32];
-                tmem_ld32(tmem + kTmemS + sb * kTile + lane_off + q * 32, v);
+                tmem_ld32(tmem + sb * kTile + lane_off + q * 32, v);
                 tmem_wait_ld();
                 const uint32_t mwq = mw[q];
 #pragma unroll
@@ -476,36 +488,23 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                     if (mwq & (1u << i))
                         tmax = fmaxf(tmax, __uint_as_float(v[i]) * sl2);
             }
-            // P.V of the previous tile must be done before P and O are touched
-            if (t > 0 && !mbar_wait(pvdone_bar, (uint32_t)(t - 1) & 1, st)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
+            float f = 1.f;  // factor the value CTA applies to O before this tile
             if (tmax > m_used + kRescaleThreshold) {
-                // raise the exponent reference; rescale O and l accordingly
-                const float f = ex2(m_used - tmax);
-                if (t > 0) {
-#pragma unroll 1
-                    for (int q = 0; q < kDvHalf / 32; q++) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem + kTmemO + lane_off + q * 32, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; i++)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                        tmem_st32(tmem + kTmemO + lane_off + q * 32, v);
-                    }
-                    tmem_wait_st();
-                }
+                f = ex2(m_used - tmax);
                 l *= f;
                 m_used = tmax;
             }
-            // pass 2: p = 2^(x - m_used) as f16 into P (two 64-key chunks)
+            // the value CTA's P buffer sb is free once its P.V of tile t - 2 is done
+            if (t >= 2 &&
+                !mbar_wait_cluster(bars + B_PEMPTY + sb, (uint32_t)((t >> 1) - 1) & 1, st)) {
+                ok = false;
+                break;
+            }
+            // pass 2: p = 2^(x - m_used) as f16, into the value CTA's P buffer sb
 #pragma unroll 1
             for (int q = 0; q < 4; q++) {
                 uint32_t v[32];
-                tmem_ld32(tmem + kTmemS + sb * kTile + lane_off + q * 32, v);
+                tmem_ld32(tmem + sb * kTile + lane_off + q * 32, v);
                 tmem_wait_ld();
                 const uint32_t mwq = mw[q];
                 uint32_t pk[16];
@@ -519,28 +518,80 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                     l += __low2float(pr) + __high2float(pr);
                 }
                 // keys 32q .. 32q+31 -> P chunk q/2, 16-byte units 4(q&1) .. +3
-                const uint32_t pc = base + kOffP + (q >> 1) * kChunk;
+                const uint32_t pc = peer_p + sb * 2 * kChunk + (q >> 1) * kChunk;
 #pragma unroll
                 for (int w = 0; w < 4; w++)
-                    st_shared_v4(pc + sw128_offset(h, (q & 1) * 4 + w), pk[4 * w], pk[4 * w + 1],
-                                 pk[4 * w + 2], pk[4 * w + 3]);
+                    st_cluster_v4(pc + sw128_offset(h, (q & 1) * 4 + w), pk[4 * w], pk[4 * w + 1],
+                                  pk[4 * w + 2], pk[4 * w + 3]);
+            }
+            st_cluster_f32(peer_f + (sb * kHeads + h) * 4, f);
+            tc_fence_before();
+            mbar_arrive(bars + B_SEMPTY + sb);
+            fence_async_cluster();
+            mbar_arrive_remote(peer_pfull + sb * 8);
+        }
+        // Row sum to the value CTA (into F buffer T & 1, free once P.V of
+        // tile T - 2 is done), then wait until the value CTA's last P.V is
+        // done so that its final commit has landed here before this CTA ends.
+        const int fb = T & 1;
+        if (ok && T >= 2 &&
+            !mbar_wait_cluster(bars + B_PEMPTY + fb, (uint32_t)((T >> 1) - 1) & 1, st))
+            ok = false;
+        st_cluster_f32(peer_f + (fb * kHeads + h) * 4, ok ? l : 0.f);
+        mbar_arrive_remote(peer_final);
+        if (ok && T >= 1)
+            mbar_wait_cluster(bars + B_PEMPTY + ((T - 1) & 1), (uint32_t)((T - 1) >> 1) & 1, st);
+        if (lse)
+            lse[(int64_t)r * kHeads + h] =
+                (ok && l > 0.f) ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    } else {
+        // ------------------------------------------- O rescale and epilogue
+        const int h = tid - kWarpQuad * 32;  // head = TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const float *fac = reinterpret_cast<const float *>(gbase + kOffF);
+        bool ok = true;
+        for (int t = 0; t < T; t++) {
+            const int pb = t & 1;
+            if (!mbar_wait_cluster(bars + B_PFULL + pb, (uint32_t)(t >> 1) & 1, st)) {
+                ok = false;
+                break;
+            }
+            const float f = fac[pb * kHeads + h];
+            // P.V of tile t - 1 must be complete before O is touched
+            if (t >= 1 && !mbar_wait(bars + B_PVDONE, (uint32_t)(t - 1) & 1, st)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (t >= 1 && f != 1.f) {
+#pragma unroll 1
+                for (int q = 0; q < kDv / 32; q++) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + q * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                    tmem_st32(tmem + lane_off + q * 32, v);
+                }
+                tmem_wait_st();
             }
             tc_fence_before();
-            mbar_arrive(sempty_bar + sb);
-            fence_async_smem();
-            mbar_arrive(pfull_bar);
+            mbar_arrive(bars + B_OCORR);
         }
-        // epilogue: wait for the last P.V, normalise, store
-        if (ok && T > 0 && !mbar_wait(pvdone_bar, (uint32_t)(T - 1) & 1, st))
+        if (ok && T >= 1 && !mbar_wait(bars + B_PVDONE, (uint32_t)(T - 1) & 1, st))
+            ok = false;
+        if (!mbar_wait_cluster(bars + B_FINAL, 0, st))
             ok = false;
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int64_t obase = ((int64_t)r * kHeads + h) * kDv + half * kDvHalf;
+        const float lsum = fac[(T & 1) * kHeads + h];
+        const float inv = (ok && lsum > 0.f) ? 1.f / lsum : 0.f;
+        const int64_t obase = ((int64_t)r * kHeads + h) * kDv;
 #pragma unroll 1
-        for (int q = 0; q < kDvHalf / 32; q++) {
+        for (int q = 0; q < kDv / 32; q++) {
             uint32_t v[32];
             if (ok && T > 0) {
-                tmem_ld32(tmem + kTmemO + lane_off + q * 32, v);
+                tmem_ld32(tmem + lane_off + q * 32, v);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -567,16 +618,14 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                         pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
             }
         }
-        if (lse && half == 0)
-            lse[(int64_t)r * kHeads + h] =
-                l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpMma)
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, score_cta ? 256u : 512u);
+    cluster_sync();  // neither CTA leaves while the other may still write into it
 }
 
 }  // namespace

@@ -82,6 +82,92 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     }
 }
 
+// ------------------------------------------------------------------ clusters
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Every thread of every CTA in the cluster arrives and waits (release /
+// acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrival on an mbarrier of another CTA of the cluster (`addr` from
+// mapa_shared), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// mbar_wait for barriers that other CTAs of the cluster arrive on: acquires
+// at cluster scope, so their writes before the arrival are visible.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, unsigned int *st)
+{
+    const uint32_t a = smem_u32(bar);
+    for (int i = 0; i < 16; i++)
+        if (mbar_try_wait_cluster(a, parity))
+            return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        for (int i = 0; i < 64; i++)
+            if (mbar_try_wait_cluster(a, parity))
+                return true;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            raise_flag(st, SI_DEVFLAG_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy writes to shared memory anywhere in the
+// cluster before later async-proxy (tensor core) reads.
+__device__ __forceinline__ void fence_async_cluster()
+{
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
 // Named barrier over `count` threads that also ORs a predicate across them,
 // so every participant takes the same decision.
 __device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t count, bool pred)
@@ -244,6 +330,17 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// Like umma_commit, but the arrival lands on the mbarrier at the same
+// shared-memory offset in every CTA of the cluster named in `cta_mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
         : "memory");
 }
 
