@@ -17,20 +17,26 @@
 //       swizzle) and streams the selected keys through a five-slot ring in
 //       "dim chunks" of 128 keys x 64 dims (16 KB).  Nine chunks build the
 //       tile's logits S = q . k^T (UMMA M = 128 heads, N = 128 keys) in TMEM
-//       (double-buffered).  Its softmax warpgroup (one thread per head) turns
-//       a tile into weights P (f16) and writes them, with one rescale factor
-//       per head, straight into the value CTA's shared memory.
+//       (double-buffered).  Eight softmax warps (two threads per head, each
+//       taking half of the tile's keys) turn a tile into weights P (f16) and
+//       write them, with one rescale factor per head, straight into the value
+//       CTA's shared memory.  A row warp resolves each tile's selected
+//       positions to physical rows (block table) and key-valid bits ahead of
+//       the loaders and the softmax.
 //   value CTA (rank 1) -- keeps O (128 heads x 512 value dims, fp32) in TMEM
 //       and streams the same rows' first 512 entries through a five-slot ring
-//       of 128-dim groups (32 KB).  Three warps rewrite each group from bf16
-//       to f16 in place (P.V needs one operand type), the MMA warp issues
+//       of 128-dim groups (32 KB).  Five warps rewrite each group from bf16 to
+//       f16 in place (P.V needs one operand type), the MMA warp issues
 //       O[:, group] += P . V_group (N = 128), and a warpgroup applies the
 //       score CTA's rescale factors to O between tiles and normalises at the
 //       end.
 //
 // Rows are gathered by eight loader warps per CTA with 16-byte cp.async
 // copies straight into ring slots; the copies arrive on the slot's mbarrier
-// when they land, so no thread stalls on them.  Every wait is bounded.
+// when they land, so no thread stalls on them.  Lookups that feed the copies
+// (index list, block table) are done by other warps or issued tiles ahead:
+// a thread's plain loads complete behind its own copies in flight, and a
+// release-ordered arrive waits for them.  Every wait is bounded.
 //
 // Softmax: online in the log2 domain with fp32 state; the exponent reference
 // is only raised when a tile's maximum exceeds it by more than 8, so most
@@ -64,29 +70,35 @@ constexpr int kVGroups = kDv / 128;      // 4 value groups per tile
 constexpr uint32_t kChunk = 128 * 128;   // 16 KB: 128 rows x 128 bytes, SW128
 constexpr uint32_t kGroup = 2 * kChunk;  // 32 KB: 128 keys x 128 value dims
 
-constexpr int kLoaderWarps = 8;
+constexpr int kLoaderWarps = 8;   // warps 0..7
 constexpr int kLoaders = kLoaderWarps * 32;
-constexpr int kWarpQuad = 8;      // warps 8..11 (TMEM lanes by warp % 4)
-constexpr int kWarpMma = 12;
-constexpr int kWarpConv0 = 13;    // value CTA: converters, warps 13..15
-constexpr int kConverters = 3 * 32;
-constexpr int kThreads = 16 * 32;
+constexpr int kRowsPerLoader = kTile / (kLoaders / 8);  // 4 rows x one 16-byte unit each
+constexpr int kWarpSoft0 = 8;     // score CTA: softmax warps 8..15, two per TMEM lane quarter
+constexpr int kSoftmax = 8 * 32;
+constexpr int kWarpQuad = 8;      // value CTA: O rescale / epilogue warps 8..11
+constexpr int kWarpMma = 16;
+constexpr int kWarpRows = 17;     // score CTA: physical rows and key-valid bits of each tile
+constexpr int kConverters = 5 * 32;  // value CTA: warps 12..15 and 17
+constexpr int kThreads = 18 * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 // score CTA layout
 constexpr int kRingS = 5;
 constexpr uint32_t kOffQ = 0;                                  // 9 x [128 heads x 64 dims]
 constexpr uint32_t kOffRingS = kQChunks * kChunk;              // kRingS x [128 keys x 64 dims]
-constexpr uint32_t kOffMask = kOffRingS + kRingS * kChunk;     // 4 tiles x 4 key-valid words
+constexpr int kRowSlots = 2;                                   // tiles of row tables in flight
+constexpr uint32_t kOffRows = kOffRingS + kRingS * kChunk;     // 2 x 128 physical rows (int32)
+constexpr uint32_t kOffMask = kOffRows + kRowSlots * kTile * 4; // 2 x 4 key-valid words
 // value CTA layout
+constexpr int kPBufs = 2;                                      // P buffers (tiles) in flight
 constexpr int kRingV = 5;
-constexpr uint32_t kOffP = 0;                                  // 2 x (2 x [128 heads x 64 keys])
-constexpr uint32_t kOffRingV = 4 * kChunk;                     // kRingV x (2 x [128 keys x 64 dims])
-constexpr uint32_t kOffF = kOffRingV + kRingV * kGroup;        // 2 x 128 floats
+constexpr uint32_t kOffP = 0;                                  // kPBufs x (2 x [128 heads x 64 keys])
+constexpr uint32_t kOffRingV = kPBufs * 2 * kChunk;            // kRingV x (2 x [128 keys x 64 dims])
+constexpr uint32_t kOffF = kOffRingV + kRingV * kGroup;        // kPBufs x 128 floats
 // both
-constexpr uint32_t kOffBar = kOffF + 2 * kHeads * 4;
+constexpr uint32_t kOffBar = std::max(kOffF + kPBufs * kHeads * 4, kOffMask + kRowSlots * 16);
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;          // + alignment slack
-static_assert(kOffMask + 4 * 4 * 4 <= kOffBar, "mask words overlap the barriers");
+static_assert(kOffMask + kRowSlots * 16 <= kOffBar, "score scratch overlaps the barriers");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 // mbarriers: one array at kOffBar in both CTAs (a barrier that the other CTA
@@ -97,24 +109,26 @@ enum : int {
     B_CONV = 10,    // [ring] value: group converted to f16
     B_SFULL = 15,   // [2] score: S of a tile complete
     B_SEMPTY = 17,  // [2] score: softmax done with an S buffer
-    B_MASK = 19,    // [4] score: key-valid words of a tile written
+    B_MASK = 19,    // [2] score: row table and key-valid words of a tile written
     B_QREADY = 23,  // score: query resident
-    B_PEMPTY = 24,  // [2] score: value CTA finished P.V from a P buffer (remote commit)
-    B_PFULL = 26,   // [2] value: P and factors of a tile written (remote arrivals)
-    B_OCORR = 28,   // value: O rescaled (if needed) for the next tile
-    B_PVDONE = 29,  // value: P.V of a tile complete
-    B_FINAL = 30,   // value: row sums l written (remote arrivals)
-    B_COUNT = 31
+    B_PEMPTY = 24,  // [3] score: value CTA finished P.V from a P buffer (remote commit)
+    B_PFULL = 27,   // [3] value: P and factors of a tile written (remote arrivals)
+    B_OCORR = 30,   // value: O rescaled (if needed) for the next tile
+    B_PVDONE = 31,  // value: P.V of a tile complete
+    B_FINAL = 32,   // value: row sums l written (remote arrivals)
+    B_MEMPTY = 33,  // [2] score: loaders and softmax done with a tile's row table / words
+    B_COUNT = 35
 };
-constexpr uint32_t kTmemSlot = 8 * 32;  // byte offset of the TMEM base within the barrier area
+constexpr uint32_t kTmemSlot = 8 * 40;  // byte offset of the TMEM base within the barrier area
 static_assert(B_COUNT * 8 <= (int)kTmemSlot, "barrier area");
 
-// 2^x with the hardware approximation (ex2.approx: ~2 ulp), ample for a
-// softmax whose weights are rounded to f16.
+// 2^x with the hardware approximation (ex2.approx: ~2 ulp, subnormal
+// results flushed to zero), ample for a softmax whose weights are rounded to
+// f16.
 __device__ __forceinline__ float ex2(float x)
 {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -155,31 +169,33 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Loader state of one thread: physical rows of its four keys (kr0 + 32 i)
-// for the even and the odd tile, and the lookahead (index-list values of
-// tile t+2, block-table entries of tile t+1) so that the dependent lookups
-// never stall the stream.
+// Loader state of one thread: physical rows of its keys (kr0 + 16 i) for
+// the even and the odd tile, and the lookahead: index-list values of tiles
+// t+1 .. t+3 and block-table entries of tiles t+1, t+2.  The lookups are
+// plain loads that complete behind the thread's in-flight copies, so they are
+// issued two to three tiles before they are needed.
+constexpr int kR = kRowsPerLoader;
 struct LoaderState {
-    int rb0[4], rb1[4];  // physical rows (< 2^31), -1 = zero row
-    int sv1[4], bk1[4], sv2[4];
+    int rb0[kR], rb1[kR];  // physical rows (< 2^31), -1 = zero row
+    int sv1[kR], bk1[kR], sv2[kR], bk2[kR], sv3[kR];
     int have_tile;
 };
 
 __device__ __forceinline__ void load_idx(const int32_t *idx, int r, int k_top, int tile, int T,
-                                         int n_valid, int kr0, int (&sv)[4])
+                                         int n_valid, int kr0, int (&sv)[kR])
 {
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int j = tile * kTile + kr0 + 32 * i;
+    for (int i = 0; i < kR; i++) {
+        const int j = tile * kTile + kr0 + (kTile / kR) * i;
         sv[i] = (tile < T && j < n_valid) ? __ldg(idx + (int64_t)r * k_top + j) : -1;
     }
 }
 
-__device__ __forceinline__ void load_blk(const si_batch &b, int seq, int pos, const int (&sv)[4],
-                                         int (&bk)[4])
+__device__ __forceinline__ void load_blk(const si_batch &b, int seq, int pos, const int (&sv)[kR],
+                                         int (&bk)[kR])
 {
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
+    for (int i = 0; i < kR; i++) {
         bk[i] = -1;
         const int sp = sv[i];
         if (sp >= 0 && sp <= pos && (unsigned)seq < (unsigned)b.n_seq &&
@@ -194,20 +210,19 @@ __device__ __forceinline__ void loader_init(LoaderState &ls, const si_batch &b, 
 {
     ls.have_tile = -1;
     load_idx(idx, r, k_top, 0, T, n_valid, kr0, ls.sv1);
-    load_blk(b, seq, pos, ls.sv1, ls.bk1);
     load_idx(idx, r, k_top, 1, T, n_valid, kr0, ls.sv2);
+    load_idx(idx, r, k_top, 2, T, n_valid, kr0, ls.sv3);
+    load_blk(b, seq, pos, ls.sv1, ls.bk1);
+    load_blk(b, seq, pos, ls.sv2, ls.bk2);
 }
 
-// Makes `tile` current: row offsets (and, if `mask` is given, the tile's
-// key-valid bits) from the lookahead, then shifts the lookahead by a tile.
-__device__ __forceinline__ void start_tile(LoaderState &ls, const si_batch &b, const int32_t *idx,
-                                           int r, int k_top, int T, int n_valid, int seq, int pos,
-                                           int kr0, int u, uint32_t *mask, unsigned int *st,
-                                           int tile)
+// Makes `tile` current: row offsets from the lookahead (-1: zero row).
+__device__ __forceinline__ void activate_tile(LoaderState &ls, const si_batch &b, int pos, int u,
+                                              unsigned int *st, int tile)
 {
     ls.have_tile = tile;
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
+    for (int i = 0; i < kR; i++) {
         const int sp = ls.sv1[i], bk = ls.bk1[i];
         bool ok = false;
         if (sp >= 0 && sp <= pos) {
@@ -222,32 +237,36 @@ __device__ __forceinline__ void start_tile(LoaderState &ls, const si_batch &b, c
             ls.rb1[i] = off;
         else
             ls.rb0[i] = off;
-        // key kr0 + 32 i is bit kr0 of word i; only this thread touches it
-        if (mask && u == 0) {
-            if (ok)
-                atomicOr(mask + i, 1u << kr0);
-            else
-                atomicAnd(mask + i, ~(1u << kr0));
-        }
     }
-#pragma unroll
-    for (int i = 0; i < 4; i++)
-        ls.sv1[i] = ls.sv2[i];
-    load_blk(b, seq, pos, ls.sv1, ls.bk1);
-    load_idx(idx, r, k_top, tile + 2, T, n_valid, kr0, ls.sv2);
 }
 
-// This thread's copies of dim chunk c (16-byte unit u of its four key rows)
-// of the current tile into the 16 KB chunk buffer at `dst`.
+// Shifts the lookahead by one tile (issues the dependent lookups of the next
+// tiles; they complete while this tile streams).
+__device__ __forceinline__ void advance_lookahead(LoaderState &ls, const si_batch &b,
+                                                  const int32_t *idx, int r, int k_top, int T,
+                                                  int n_valid, int seq, int pos, int kr0, int tile)
+{
+#pragma unroll
+    for (int i = 0; i < kR; i++) {
+        ls.sv1[i] = ls.sv2[i];
+        ls.bk1[i] = ls.bk2[i];
+        ls.sv2[i] = ls.sv3[i];
+    }
+    load_blk(b, seq, pos, ls.sv2, ls.bk2);
+    load_idx(idx, r, k_top, tile + 3, T, n_valid, kr0, ls.sv3);
+}
+
+// This thread's copies of dim chunk c (16-byte unit u of its key rows) of
+// the current tile into the 16 KB chunk buffer at `dst`.
 __device__ __forceinline__ void issue_chunk(const LoaderState &ls, uint32_t dst, const uint8_t *kv,
                                             int64_t row_bytes, int tile, int c, int kr0, int u)
 {
     const bool odd = tile & 1;
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
+    for (int i = 0; i < kR; i++) {
         const int row = odd ? ls.rb1[i] : ls.rb0[i];
         const uint8_t *src = row >= 0 ? kv + (int64_t)row * row_bytes + c * 128 + u * 16 : kv;
-        cp_async_16(dst + sw128_offset(kr0 + 32 * i, u), src, row >= 0 ? 16u : 0u);
+        cp_async_16(dst + sw128_offset(kr0 + (kTile / kR) * i, u), src, row >= 0 ? 16u : 0u);
     }
 }
 
@@ -277,12 +296,16 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(bars + B_SFULL + i, 1);
-            mbar_init(bars + B_SEMPTY + i, kHeads);
-            mbar_init(bars + B_PEMPTY + i, 1);
-            mbar_init(bars + B_PFULL + i, kHeads);
+            mbar_init(bars + B_SEMPTY + i, kSoftmax);
         }
-        for (int i = 0; i < 4; i++)
-            mbar_init(bars + B_MASK + i, kLoaders);
+        for (int i = 0; i < kPBufs; i++) {
+            mbar_init(bars + B_PEMPTY + i, 1);
+            mbar_init(bars + B_PFULL + i, kSoftmax);
+        }
+        for (int i = 0; i < kRowSlots; i++) {
+            mbar_init(bars + B_MASK + i, 32);
+            mbar_init(bars + B_MEMPTY + i, kSoftmax + kLoaders);
+        }
         mbar_init(bars + B_QREADY, kLoaders);
         mbar_init(bars + B_OCORR, kHeads);
         mbar_init(bars + B_PVDONE, 1);
@@ -290,7 +313,7 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
-        tmem_alloc(tmem_slot, score_cta ? 256u : 512u);
+        tmem_alloc(tmem_slot, 512u);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -327,8 +350,9 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                 fence_async_smem();
                 mbar_arrive(bars + B_QREADY);
             }
-            uint32_t *mask = reinterpret_cast<uint32_t *>(gbase + kOffMask);
-            loader_init(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0);
+            // physical rows come from the row table the row warp fills
+            const int *rows = reinterpret_cast<const int *>(gbase + kOffRows);
+            ls.have_tile = -1;
             const int n_chunks = kQChunks * T;
             for (int g = 0; g < n_chunks; g++) {
                 const int slot = g % kRingS, tile = g / kQChunks, c = g % kQChunks;
@@ -336,9 +360,19 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                     !mbar_wait(bars + B_EMPTY + slot, (uint32_t)((g / kRingS) - 1) & 1, st))
                     break;
                 if (tile > ls.have_tile) {
-                    start_tile(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0, u,
-                               mask + (tile % 4) * 4, st, tile);
-                    mbar_arrive(bars + B_MASK + (tile % 4));
+                    const int rs = tile % kRowSlots;
+                    if (!mbar_wait(bars + B_MASK + rs, (uint32_t)(tile / kRowSlots) & 1, st))
+                        break;
+                    ls.have_tile = tile;
+#pragma unroll
+                    for (int i = 0; i < kR; i++) {
+                        const int row = rows[rs * kTile + kr0 + (kTile / kR) * i];
+                        if (tile & 1)
+                            ls.rb1[i] = row;
+                        else
+                            ls.rb0[i] = row;
+                    }
+                    mbar_arrive(bars + B_MEMPTY + rs);
                 }
                 issue_chunk(ls, base + kOffRingS + slot * kChunk, kv, row_bytes, tile, c, kr0, u);
                 cp_async_arrive(bars + B_FULL + slot);
@@ -351,9 +385,10 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                 if (g >= kRingV &&
                     !mbar_wait(bars + B_EMPTY + slot, (uint32_t)((g / kRingV) - 1) & 1, st))
                     break;
-                if (tile > ls.have_tile)
-                    start_tile(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0, u, nullptr, st,
-                               tile);
+                if (tile > ls.have_tile) {
+                    activate_tile(ls, b, pos, u, st, tile);
+                    advance_lookahead(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0, tile);
+                }
                 const uint32_t dst = base + kOffRingV + slot * kGroup;
                 issue_chunk(ls, dst, kv, row_bytes, tile, 2 * j, kr0, u);
                 issue_chunk(ls, dst + kChunk, kv, row_bytes, tile, 2 * j + 1, kr0, u);
@@ -398,8 +433,8 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
             const uint32_t idesc = idesc_f16(kHeads, 128, 0, 0, 1);  // f16; B (V) MN-major
             bool ok = true;
             for (int t = 0; ok && t < T; t++) {
-                const int pb = t & 1;
-                if (!mbar_wait_cluster(bars + B_PFULL + pb, (uint32_t)(t >> 1) & 1, st) ||
+                const int pb = t % kPBufs;
+                if (!mbar_wait_cluster(bars + B_PFULL + pb, (uint32_t)(t / kPBufs) & 1, st) ||
                     !mbar_wait(bars + B_OCORR, (uint32_t)t & 1, st))
                     break;
                 fence_async_smem();  // P written by the score CTA -> tensor core
@@ -435,115 +470,211 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                 __syncwarp();
             }
         }
-    } else if (warp >= kWarpConv0) {
-        // ----------------------------------------------------------- converters
-        if (!score_cta) {
-            const int ct = tid - kWarpConv0 * 32;
-            const int n_groups = kVGroups * T;
-            for (int g = 0; g < n_groups; g++) {
-                const int slot = g % kRingV;
-                if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingV) & 1, st))
-                    break;
-                const uint32_t src = base + kOffRingV + slot * kGroup;
-                for (int i = ct; i < (int)(kGroup / 16); i += kConverters) {
-                    const uint4 x = ld_shared_v4(src + i * 16);
-                    st_shared_v4(src + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
-                                 bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
-                }
-                fence_async_smem();
-                mbar_arrive(bars + B_CONV + slot);
-            }
-        }
     } else if (score_cta) {
-        // -------------------------------------------------------------- softmax
-        const int h = tid - kWarpQuad * 32;  // head = TMEM lane
-        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const float sl2 = at.softmax_scale * 1.4426950408889634f;  // scale * log2(e)
-        const uint32_t *mask = reinterpret_cast<const uint32_t *>(gbase + kOffMask);
-        float m_used = -INFINITY;  // exponent reference (log2 units)
-        float l = 0.f;
-        bool ok = true;
-        for (int t = 0; t < T && ok; t++) {
-            const int sb = t & 1;
-            if (!mbar_wait(bars + B_MASK + (t % 4), (uint32_t)(t / 4) & 1, st) ||
-                !mbar_wait(bars + B_SFULL + sb, (uint32_t)(t >> 1) & 1, st)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t mw[4];
-#pragma unroll
-            for (int q = 0; q < 4; q++)
-                mw[q] = mask[(t % 4) * 4 + q];
-            // pass 1: tile maximum of the valid logits
-            float tmax = -INFINITY;
-#pragma unroll 1
-            for (int q = 0; q < 4; q++) {
-                uint32_t v[32];
-                tmem_ld32(tmem + sb * kTile + lane_off + q * 32, v);
-                tmem_wait_ld();
-                const uint32_t mwq = mw[q];
-#pragma unroll
-                for (int i = 0; i < 32; i++)
-                    if (mwq & (1u << i))
-                        tmax = fmaxf(tmax, __uint_as_float(v[i]) * sl2);
-            }
-            float f = 1.f;  // factor the value CTA applies to O before this tile
-            if (tmax > m_used + kRescaleThreshold) {
-                f = ex2(m_used - tmax);
-                l *= f;
-                m_used = tmax;
-            }
-            // the value CTA's P buffer sb is free once its P.V of tile t - 2 is done
-            if (t >= 2 &&
-                !mbar_wait_cluster(bars + B_PEMPTY + sb, (uint32_t)((t >> 1) - 1) & 1, st)) {
-                ok = false;
-                break;
-            }
-            // pass 2: p = 2^(x - m_used) as f16, into the value CTA's P buffer sb
-#pragma unroll 1
-            for (int q = 0; q < 4; q++) {
-                uint32_t v[32];
-                tmem_ld32(tmem + sb * kTile + lane_off + q * 32, v);
-                tmem_wait_ld();
-                const uint32_t mwq = mw[q];
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float p0 = (mwq & (1u << i)) ? ex2(__uint_as_float(v[i]) * sl2 - m_used) : 0.f;
-                    const float p1 =
-                        (mwq & (1u << (i + 1))) ? ex2(__uint_as_float(v[i + 1]) * sl2 - m_used) : 0.f;
-                    pk[i >> 1] = pack_f16x2(p0, p1);
-                    const __half2 pr = *reinterpret_cast<__half2 *>(&pk[i >> 1]);
-                    l += __low2float(pr) + __high2float(pr);
+        if (warp >= kWarpSoft0 && warp < kWarpSoft0 + 8) {
+            // ---------------------------------------------------------- softmax
+            // Two threads per head (TMEM lane): warps 4..7 take keys 0..63 of
+            // each tile, warps 8..11 keys 64..127.  They share the tile
+            // maximum through shared memory and keep partial row sums.
+            const int quarter = warp & 3, kh = (warp - kWarpSoft0) >> 2;
+            const int h = quarter * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const float sl2 = at.softmax_scale * 1.4426950408889634f;  // scale * log2(e)
+            const uint32_t *mask = reinterpret_cast<const uint32_t *>(gbase + kOffMask);
+            // the two threads of a head share TMEM lane h: column 256 + kh is
+            // this thread's exchange cell
+            const uint32_t xmine = tmem + 256 + kh + lane_off, xother = tmem + 257 - kh + lane_off;
+            float m_used = -INFINITY;  // exponent reference (log2 units)
+            float l = 0.f;             // this half's row sum
+            bool ok = true;
+            int unpublished = -1;  // tile whose P is written but not yet announced
+            // Announces P of tile `pt` to the value CTA.  Done one step late
+            // (after the next tile's first pass), so that the cluster-scope
+            // release does not wait on the remote stores' round trip.
+            auto publish = [&](int pt) {
+                fence_async_cluster();
+                mbar_arrive_remote(peer_pfull + (pt % kPBufs) * 8);
+            };
+            for (int t = 0; t < T; t++) {
+                const int sb = t & 1;
+                const int rs = t % kRowSlots;
+                const bool got =
+                    mbar_wait(bars + B_MASK + rs, (uint32_t)(t / kRowSlots) & 1, st) &&
+                    mbar_wait(bars + B_SFULL + sb, (uint32_t)(t >> 1) & 1, st);
+                // all 256 threads take the same branch (bar.red over the flag)
+                if (bar_sync_or(1, kSoftmax, !got)) {
+                    ok = false;
+                    break;
                 }
-                // keys 32q .. 32q+31 -> P chunk q/2, 16-byte units 4(q&1) .. +3
-                const uint32_t pc = peer_p + sb * 2 * kChunk + (q >> 1) * kChunk;
+                tc_fence_after();
+                const uint32_t mw0 = mask[rs * 4 + 2 * kh], mw1 = mask[rs * 4 + 2 * kh + 1];
+                mbar_arrive(bars + B_MEMPTY + rs);
+                // pass 1: maximum of this half's valid logits, then of the tile
+                float tmax = -INFINITY;
+#pragma unroll 1
+                for (int q = 0; q < 2; q++) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + sb * kTile + 64 * kh + lane_off + 32 * q, v);
+                    tmem_wait_ld();
+                    const uint32_t mwq = q ? mw1 : mw0;
 #pragma unroll
-                for (int w = 0; w < 4; w++)
-                    st_cluster_v4(pc + sw128_offset(h, (q & 1) * 4 + w), pk[4 * w], pk[4 * w + 1],
-                                  pk[4 * w + 2], pk[4 * w + 3]);
+                    for (int i = 0; i < 32; i++)
+                        if (mwq & (1u << i))
+                            tmax = fmaxf(tmax, __uint_as_float(v[i]) * sl2);
+                }
+                tmem_st1(xmine, __float_as_uint(tmax));
+                tmem_wait_st();
+                tc_fence_before();
+                bar_sync_or(1, kSoftmax, false);
+                tc_fence_after();
+                tmax = fmaxf(tmax, __uint_as_float(tmem_ld1(xother)));
+                tmem_wait_ld();
+                float f = 1.f;  // factor the value CTA applies to O before this tile
+                if (tmax > m_used + kRescaleThreshold) {
+                    f = ex2(m_used - tmax);
+                    l *= f;
+                    m_used = tmax;
+                }
+                if (unpublished >= 0) {
+                    publish(unpublished);
+                    unpublished = -1;
+                }
+                // the value CTA's P buffer pb is free once its P.V of tile t - 3
+                // is done; the bar.red also orders this tile's reads of the
+                // exchange cell before the next tile's writes
+                const int pb = t % kPBufs;
+                const bool free_ =
+                    t < kPBufs ||
+                    mbar_wait_cluster(bars + B_PEMPTY + pb, (uint32_t)((t / kPBufs) - 1) & 1, st);
+                if (bar_sync_or(1, kSoftmax, !free_)) {
+                    ok = false;
+                    break;
+                }
+                // pass 2: p = 2^(x - m_used) as f16, into the value CTA's P buffer
+                // pb, chunk kh (this half's 64 keys)
+                const uint32_t pc = peer_p + pb * 2 * kChunk + kh * kChunk;
+#pragma unroll 1
+                for (int q = 0; q < 2; q++) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + sb * kTile + 64 * kh + lane_off + 32 * q, v);
+                    tmem_wait_ld();
+                    if (q == 1) {
+                        tc_fence_before();
+                        mbar_arrive(bars + B_SEMPTY + sb);  // S buffer sb may be overwritten
+                    }
+                    const uint32_t mwq = q ? mw1 : mw0;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float x0 = __uint_as_float(v[i]);
+                        const float x1 = __uint_as_float(v[i + 1]);
+                        const float p0 = (mwq & (1u << i)) ? ex2(x0 * sl2 - m_used) : 0.f;
+                        const float p1 = (mwq & (1u << (i + 1))) ? ex2(x1 * sl2 - m_used) : 0.f;
+                        pk[i >> 1] = pack_f16x2(p0, p1);
+                        const __half2 pr = *reinterpret_cast<__half2 *>(&pk[i >> 1]);
+                        l += __low2float(pr) + __high2float(pr);
+                    }
+#pragma unroll
+                    for (int w = 0; w < 4; w++)
+                        st_cluster_v4(pc + sw128_offset(h, q * 4 + w), pk[4 * w], pk[4 * w + 1],
+                                      pk[4 * w + 2], pk[4 * w + 3]);
+                }
+                if (kh == 0)
+                    st_cluster_f32(peer_f + (pb * kHeads + h) * 4, f);
+                unpublished = t;
             }
-            st_cluster_f32(peer_f + (sb * kHeads + h) * 4, f);
+            if (unpublished >= 0)
+                publish(unpublished);
+            // Row sums: combine the halves.  Then wait until the value CTA's
+            // P.V of the last (up to) kPBufs tiles is done -- so its commits
+            // have landed here before this CTA ends, and F buffer T % kPBufs
+            // is free -- and send l.
+            tmem_st1(xmine, __float_as_uint(l));
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bars + B_SEMPTY + sb);
-            fence_async_cluster();
-            mbar_arrive_remote(peer_pfull + sb * 8);
+            bar_sync_or(1, kSoftmax, false);
+            tc_fence_after();
+            l += __uint_as_float(tmem_ld1(xother));
+            tmem_wait_ld();
+            if (kh == 0) {
+                for (int tt = max(0, T - kPBufs); ok && tt < T; tt++)
+                    if (!mbar_wait_cluster(bars + B_PEMPTY + tt % kPBufs,
+                                           (uint32_t)(tt / kPBufs) & 1, st))
+                        ok = false;
+                st_cluster_f32(peer_f + ((T % kPBufs) * kHeads + h) * 4, ok ? l : 0.f);
+                mbar_arrive_remote(peer_final);
+                if (lse)
+                    lse[(int64_t)r * kHeads + h] =
+                        (ok && l > 0.f) ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+            }
         }
-        // Row sum to the value CTA (into F buffer T & 1, free once P.V of
-        // tile T - 2 is done), then wait until the value CTA's last P.V is
-        // done so that its final commit has landed here before this CTA ends.
-        const int fb = T & 1;
-        if (ok && T >= 2 &&
-            !mbar_wait_cluster(bars + B_PEMPTY + fb, (uint32_t)((T >> 1) - 1) & 1, st))
-            ok = false;
-        st_cluster_f32(peer_f + (fb * kHeads + h) * 4, ok ? l : 0.f);
-        mbar_arrive_remote(peer_final);
-        if (ok && T >= 1)
-            mbar_wait_cluster(bars + B_PEMPTY + ((T - 1) & 1), (uint32_t)((T - 1) >> 1) & 1, st);
-        if (lse)
-            lse[(int64_t)r * kHeads + h] =
-                (ok && l > 0.f) ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        if (warp == kWarpRows) {
+            // ------------------------------------------------- row table, key-valid bits
+            // For each tile: the physical row of every selected key (-1: none,
+            // the loaders then write zeros) and bit i of word w set when key
+            // 32 w + i is valid.  Up to two tiles ahead of its consumers.
+            int *rows = reinterpret_cast<int *>(gbase + kOffRows);
+            uint32_t *mask = reinterpret_cast<uint32_t *>(gbase + kOffMask);
+            for (int t = 0; t < T; t++) {
+                const int rs = t % kRowSlots;
+                if (t >= kRowSlots &&
+                    !mbar_wait(bars + B_MEMPTY + rs, (uint32_t)((t / kRowSlots) - 1) & 1, st))
+                    break;
+                int sp[4], blk[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int j = t * kTile + 32 * i + lane;
+                    sp[i] = j < n_valid ? __ldg(idx + (int64_t)r * k_top + j) : -1;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    blk[i] = -1;
+                    if (sp[i] >= 0 && sp[i] <= pos && (unsigned)seq < (unsigned)b.n_seq &&
+                        sp[i] / b.page_size < b.max_blocks)
+                        blk[i] = __ldg(b.block_table + (int64_t)seq * b.max_blocks +
+                                       sp[i] / b.page_size);
+                }
+                uint32_t word = 0;
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    bool ok = false;
+                    if (sp[i] >= 0 && sp[i] <= pos) {
+                        ok = (unsigned)blk[i] < (unsigned)b.n_blocks;
+                        if (!ok)
+                            raise_flag(st, SI_DEVFLAG_BAD_BLOCK);
+                    } else if (sp[i] != -1) {
+                        raise_flag(st, SI_DEVFLAG_BAD_INDEX);
+                    }
+                    rows[rs * kTile + 32 * i + lane] =
+                        ok ? blk[i] * b.page_size + sp[i] % b.page_size : -1;
+                    const uint32_t w = __ballot_sync(0xffffffffu, ok);
+                    if (lane == i)
+                        word = w;
+                }
+                if (lane < 4)
+                    mask[rs * 4 + lane] = word;
+                mbar_arrive(bars + B_MASK + rs);
+            }
+        }
+    } else if (warp >= kWarpQuad + 4) {
+        // ----------------------------------------------------------- converters
+        // Value groups feed the f16 P.V product: rewrite them bf16 -> f16 in
+        // place once their copies have landed (warps 12..15 and 17).
+        const int ct = warp < kWarpMma ? tid - (kWarpQuad + 4) * 32 : 4 * 32 + lane;
+        const int n_groups = kVGroups * T;
+        for (int g = 0; g < n_groups; g++) {
+            const int slot = g % kRingV;
+            if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingV) & 1, st))
+                break;
+            const uint32_t src = base + kOffRingV + slot * kGroup;
+            for (int i = ct; i < (int)(kGroup / 16); i += kConverters) {
+                const uint4 x = ld_shared_v4(src + i * 16);
+                st_shared_v4(src + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
+                             bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+            }
+            fence_async_smem();
+            mbar_arrive(bars + B_CONV + slot);
+        }
     } else {
         // ------------------------------------------- O rescale and epilogue
         const int h = tid - kWarpQuad * 32;  // head = TMEM lane
@@ -551,8 +682,8 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
         const float *fac = reinterpret_cast<const float *>(gbase + kOffF);
         bool ok = true;
         for (int t = 0; t < T; t++) {
-            const int pb = t & 1;
-            if (!mbar_wait_cluster(bars + B_PFULL + pb, (uint32_t)(t >> 1) & 1, st)) {
+            const int pb = t % kPBufs;
+            if (!mbar_wait_cluster(bars + B_PFULL + pb, (uint32_t)(t / kPBufs) & 1, st)) {
                 ok = false;
                 break;
             }
@@ -584,7 +715,7 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
         if (!mbar_wait_cluster(bars + B_FINAL, 0, st))
             ok = false;
         tc_fence_after();
-        const float lsum = fac[(T & 1) * kHeads + h];
+        const float lsum = fac[(T % kPBufs) * kHeads + h];
         const float inv = (ok && lsum > 0.f) ? 1.f / lsum : 0.f;
         const int64_t obase = ((int64_t)r * kHeads + h) * kDv;
 #pragma unroll 1
@@ -624,7 +755,7 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpMma)
-        tmem_dealloc(tmem, score_cta ? 256u : 512u);
+        tmem_dealloc(tmem, 512u);
     cluster_sync();  // neither CTA leaves while the other may still write into it
 }
 
