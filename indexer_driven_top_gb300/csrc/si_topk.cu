@@ -6,6 +6,10 @@
 // the exact K-th largest score by three histogram passes over an
 // order-preserving 32-bit key (11 + 11 + 10 bits), then emits every position
 // above that threshold plus the lowest-positioned ties, in ascending order.
+//
+// One 1024-thread CTA per query row.  Rows of up to 16384 candidates are read
+// once into registers (thread t holds E consecutive positions) and every pass
+// runs on the cached keys; longer rows stream from global memory per pass.
 #include "si_common.cuh"
 #include "si_internal.h"
 
@@ -15,6 +19,104 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kRadixBins = 2048;
+
+// Finds, among the cached keys, the digit of the k-th largest key at `shift`
+// (bins in descending order) and how many of the k fall in that digit's bin.
+// Every thread returns the same (digit, remaining).
+__device__ __forceinline__ void radix_step(uint32_t *hist, int *sbuf, uint32_t *sh_digit,
+                                           int *sh_rem, int nbins, int &remaining)
+{
+    const int tid = threadIdx.x;
+    const int per = nbins / kTopkThreads;
+    int local = 0;
+    for (int k = 0; k < per; k++)
+        local += hist[nbins - 1 - (tid * per + k)];
+    int total;
+    int c = block_exclusive_scan(local, &total, sbuf);
+    for (int k = 0; k < per; k++) {
+        const int d = nbins - 1 - (tid * per + k);
+        const int h = hist[d];
+        if (c < remaining && c + h >= remaining) {
+            *sh_digit = (uint32_t)d;
+            *sh_rem = remaining - c;
+        }
+        c += h;
+    }
+    __syncthreads();
+    remaining = *sh_rem;
+}
+
+// Row of n <= E * kTopkThreads candidates (n > k_top): keys cached in
+// registers, thread t owning positions [t E, t E + E).
+template <int E>
+__device__ __forceinline__ void topk_cached(const float *row, int n, int k_top, int32_t *out,
+                                            uint32_t *hist, int *sbuf, uint32_t *sh_digit,
+                                            int *sh_rem)
+{
+    const int tid = threadIdx.x;
+    const int p0 = tid * E;
+    uint32_t key[E];
+    uint32_t valid = 0;  // bit e: position p0 + e < n
+    // vector loads need a 16-byte aligned row start (p0 is a multiple of 8)
+    if (p0 + E <= n && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+#pragma unroll
+        for (int e = 0; e < E; e += 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(row + p0 + e));
+            key[e] = order_key(v.x);
+            key[e + 1] = order_key(v.y);
+            key[e + 2] = order_key(v.z);
+            key[e + 3] = order_key(v.w);
+        }
+        valid = (E == 32) ? 0xffffffffu : ((1u << E) - 1);
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const bool in = p0 + e < n;
+            key[e] = in ? order_key(__ldg(row + p0 + e)) : 0u;
+            valid |= (in ? 1u : 0u) << e;
+        }
+    }
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k_top;
+    for (int pass = 0; pass < 3; pass++) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nbins = pass == 2 ? 1024 : 2048;
+        for (int i = tid; i < nbins; i += kTopkThreads)
+            hist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; e++)
+            if (((valid >> e) & 1u) && (key[e] & mask) == prefix)
+                atomicAdd(&hist[(key[e] >> shift) & (nbins - 1)], 1u);
+        __syncthreads();
+        radix_step(hist, sbuf, sh_digit, sh_rem, nbins, remaining);
+        prefix |= *sh_digit << shift;
+        mask |= (uint32_t)(nbins - 1) << shift;
+        __syncthreads();
+    }
+    // emit: keys above the threshold, then the first `remaining` ties
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        const bool in = (valid >> e) & 1u;
+        gt += in && key[e] > prefix;
+        eq += in && key[e] == prefix;
+    }
+    int total;
+    const int eq_before = block_exclusive_scan(eq, &total, sbuf);
+    int take_eq = max(0, min(eq, remaining - eq_before));
+    int o = block_exclusive_scan(gt + take_eq, &total, sbuf);
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+        const bool in = (valid >> e) & 1u;
+        const bool tie = in && key[e] == prefix;
+        const bool take = (in && key[e] > prefix) || (tie && take_eq > 0);
+        if (tie && take)
+            take_eq--;
+        if (take && o < k_top)
+            out[o++] = p0 + e;
+    }
+}
 
 __global__ void __launch_bounds__(kTopkThreads)
 k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx)
@@ -34,6 +136,14 @@ k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx
     if (n <= k_top) {  // everything is selected
         for (int i = tid; i < k_top; i += kTopkThreads)
             out[i] = i < n ? i : -1;
+        return;
+    }
+    if (n <= 8 * kTopkThreads) {
+        topk_cached<8>(row, (int)n, k_top, out, hist, sbuf, &sh_digit, &sh_rem);
+        return;
+    }
+    if (n <= 16 * kTopkThreads) {
+        topk_cached<16>(row, (int)n, k_top, out, hist, sbuf, &sh_digit, &sh_rem);
         return;
     }
 
