@@ -62,6 +62,7 @@ constexpr int kHeads = 64;        // indexer heads
 constexpr int kDim = 128;         // head dim = bytes per e4m3 key row = UMMA K
 constexpr int kN = 2 * kHeads;    // B rows: q_hi heads, then q_lo heads = UMMA N
 constexpr int kStages = 10;       // key-tile ring depth
+constexpr int kScStages = kStages / 2;  // per-producer ring of tile scales (128 floats each)
 constexpr int kPairs = 2;         // (MMA warp, epilogue group) pairs, alternate tiles
 constexpr int kAccPerPair = 2;    // TMEM accumulators per pair (4 x 128 = 512 columns)
 // warp roles
@@ -77,7 +78,8 @@ constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffQ = kOffStage + kStages * kTile;            // [2]
 constexpr uint32_t kOffW = kOffQ + 2 * kTileB;                      // [2][64] fp32 (w * s_h)
 constexpr uint32_t kOffWin = kOffW + 2 * kHeads * 4;                // 2 producers x 32 int
-constexpr uint32_t kOffBar = kOffWin + 2 * 32 * 4;
+constexpr uint32_t kOffSc = kOffWin + 2 * 32 * 4;                   // [2][kScStages][128] fp32
+constexpr uint32_t kOffBar = kOffSc + 2 * kScStages * kKeys * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 1024 + 1024;             // + alignment slack
 
 // Advances (row, tile) by `n` items of a row-major list with `tpr` tiles per row.
@@ -114,7 +116,10 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
     uint64_t *cempty_bar = cfull_bar + kPairs * kAccPerPair;              // [kPairs][kAccPerPair]
     uint64_t *qfull_bar = cempty_bar + kPairs * kAccPerPair;              // [2]
     uint64_t *qempty_bar = qfull_bar + 2;                                 // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qempty_bar + 2);
+    uint64_t *scfull_bar = qempty_bar + 2;                                // [2][kScStages]
+    uint64_t *scempty_bar = scfull_bar + 2 * kScStages;                   // [2][kScStages]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(scempty_bar + 2 * kScStages);
+    float *sc_s = reinterpret_cast<float *>(gbase + kOffSc);
     float *w_s = reinterpret_cast<float *>(gbase + kOffW);
     volatile int *win_all = reinterpret_cast<volatile int *>(gbase + kOffWin);
 
@@ -136,6 +141,10 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
         for (int i = 0; i < 2; i++) {
             mbar_init(qfull_bar + i, 128);                   // q-prep threads
             mbar_init(qempty_bar + i, kPairs + kPairs * 128); // MMA commits + epilogues
+        }
+        for (int i = 0; i < 2 * kScStages; i++) {
+            mbar_init(scfull_bar + i, 32);    // producer lanes (copy landed or sentinel)
+            mbar_init(scempty_bar + i, 128);  // epilogue group read the scales
         }
         fence_barrier_init();
     }
@@ -205,6 +214,34 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
             if (copy)
                 tma_load_2d(base + kOffStage + stg * kTile + k_lo * kDim, &tmap, 0, row,
                             full_bar + stg);
+            // The tile's per-key scales into this producer's scale ring (read
+            // by the paired epilogue group): lane l copies keys s0 + 4 l .. +3
+            // (one page), or writes -1 where the page has no valid block.
+            const int64_t kit = it >> 1;
+            const int ss = (int)(kit % kScStages);
+            uint64_t *sf = scfull_bar + pw * kScStages + ss;
+            if (kit >= kScStages &&
+                !mbar_wait(scempty_bar + pw * kScStages + ss, (uint32_t)((kit / kScStages) - 1) & 1,
+                           st))
+                break;
+            {
+                const int s4 = s0 + 4 * lane, lb4 = s4 >> lp;
+                int blk4 = -1;
+                if (live && lb4 <= last && lb4 < b.max_blocks) {
+                    const int v = win_s[lb4 - win];
+                    if ((unsigned)v < (unsigned)b.n_blocks)
+                        blk4 = v;
+                }
+                const uint32_t d = smem_u32(sc_s + (pw * kScStages + ss) * kKeys + 4 * lane);
+                if (blk4 >= 0 && ix.k.scale) {
+                    cp_async_16(d, ix.k.scale + ((int64_t)blk4 << lp) + (s4 & (P - 1)));
+                    cp_async_arrive_noinc(sf);
+                } else {
+                    const uint32_t v = __float_as_uint(blk4 >= 0 ? 1.f : -1.f);
+                    st_shared_v4(d, v, v, v, v);
+                    mbar_arrive(sf);
+                }
+            }
             advance(r, t, 2, tiles_per_row);
         }
     } else if (warp == kWarpMma0 || warp == kWarpMma1) {
@@ -337,7 +374,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
         const int et = (tid - kWarpEpi0 * 32) & 127;  // key row = TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         int r = (int)(j0 / tiles_per_row), t = (int)(j0 % tiles_per_row);
-        int cur = -1, ri = -1, pos = -1, p = 0, seq = 0;
+        int cur = -1, ri = -1, pos = -1, p = 0;
         int64_t m = 0;
         for (int64_t it = 0; it < n_items; it++) {
             if (r != cur) {
@@ -345,7 +382,6 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                 ++ri;
                 p = ri & 1;
                 pos = __ldg(b.q_pos + r);
-                seq = __ldg(b.q_seq + r);
                 if (!mbar_wait(qfull_bar + p, (uint32_t)(ri >> 1) & 1, st))
                     break;
             }
@@ -354,19 +390,16 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
             const bool row_ends = (it + 1 == n_items) || (r != cur);
             const bool live = s0 <= pos;
             if ((int)(it & 1) == g) {
+                // this key's scale from the producer's ring: -1 marks a key
+                // without a valid block (scores -inf), 1 an unscaled cache
+                const int64_t kit = it >> 1;
+                const int ss = (int)(kit % kScStages);
+                if (!mbar_wait(scfull_bar + g * kScStages + ss, (uint32_t)(kit / kScStages) & 1, st))
+                    break;
+                const float scv = sc_s[(g * kScStages + ss) * kKeys + et];
+                mbar_arrive(scempty_bar + g * kScStages + ss);
                 if (live) {
-                    // this key's scale (issued before the accumulator wait):
-                    // -1 marks a key that must score -inf, 1 an unscaled key
-                    float sc = -1.f;
-                    if (s <= pos) {
-                        const int lb = s >> lp;
-                        int blk = -1;
-                        if ((unsigned)seq < (unsigned)b.n_seq && lb < b.max_blocks)
-                            blk = __ldg(b.block_table + (int64_t)seq * b.max_blocks + lb);
-                        if ((unsigned)blk < (unsigned)b.n_blocks)
-                            sc = ix.k.scale ? __ldg(ix.k.scale + ((int64_t)blk << lp) + (s & (P - 1)))
-                                            : 1.f;
-                    }
+                    const float sc = s <= pos ? scv : -1.f;
                     const int c = (int)(m % kAccPerPair);
                     if (!mbar_wait(cfull_bar + g * kAccPerPair + c,
                                    (uint32_t)(m / kAccPerPair) & 1, st))
@@ -397,7 +430,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                     mbar_arrive(cempty_bar + g * kAccPerPair + c);
                     const float sum = (part[0] + part[1]) + (part[2] + part[3]);
                     if (s < ld)
-                        scores[(int64_t)rr * ld + s] = sc > 0.f ? sum * sc + 0.0f : -INFINITY;
+                        scores[(int64_t)rr * ld + s] = sc >= 0.f ? sum * sc + 0.0f : -INFINITY;
                     m++;
                 } else if (s < ld) {
                     scores[(int64_t)rr * ld + s] = -INFINITY;  // tile after the query
@@ -426,7 +459,8 @@ bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld)
     return pow2_page && ix.q_dtype == SI_BF16 && ix.k.dtype == SI_E4M3 && ix.n_heads == kHeads &&
            ix.head_dim == kDim && ix.k.row_stride == kDim &&
            (int64_t)b.n_blocks * b.page_size < (int64_t)INT32_MAX &&
-           ((uintptr_t)ix.q % 16) == 0 && ((uintptr_t)ix.k.data % 16) == 0;
+           ((uintptr_t)ix.q % 16) == 0 && ((uintptr_t)ix.k.data % 16) == 0 &&
+           ((uintptr_t)ix.k.scale % 16) == 0;
 }
 
 cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,

@@ -1,0 +1,108 @@
+"""Parity at full size: the decode workload the benchmark times (batch 64 x
+context 8192, indexer 64 x 128 FP8, Top-K 2048, 128 heads over 576-dim latent
+rows), run through exactly the calls the benchmark makes, checked against the
+oracle on sampled query rows.  Plus long-context and mixed/prefill workloads
+at full per-row size on fewer rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _parity import ATOL_BF16, check_topk, max_abs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def si():
+    import __graft_entry__
+    __graft_entry__.build()
+    import indexer_driven_top_gb300 as si
+    return si
+
+
+def _separate(si, dw):
+    """The benchmark's timed step: scores, Top-K, attention as three calls."""
+    b = dw.batch
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, dw.indexer, dw.attention, dw.k_top))
+    scores = torch.empty((dw.n_q, b.max_ctx), dtype=torch.float32, device="cuda")
+    idx = torch.empty((dw.n_q, dw.k_top), dtype=torch.int32, device="cuda")
+    out = torch.empty((dw.n_q, dw.attention.q.shape[1], dw.attention.d_v), dtype=torch.float32,
+                      device="cuda")
+    si.indexer_scores(b, dw.indexer, scores, ws)
+    si.topk(b, scores, dw.k_top, idx, ws)
+    si.sparse_attn(b, dw.attention, idx, dw.k_top, out, ws)
+    assert si.workspace_status(ws) == 0
+    return scores, idx, out
+
+
+def _fused(si, dw):
+    """The end-to-end call: si_fused_decode with a workspace."""
+    b = dw.batch
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, dw.indexer, dw.attention, dw.k_top))
+    idx = torch.empty((dw.n_q, dw.k_top), dtype=torch.int32, device="cuda")
+    out = torch.empty((dw.n_q, dw.attention.q.shape[1], dw.attention.d_v), dtype=torch.float32,
+                      device="cuda")
+    si.fused_decode(b, dw.indexer, dw.attention, dw.k_top, idx, out, ws)
+    assert si.workspace_status(ws) == 0
+    return idx, out
+
+
+def _check_rows(wl, rows, g_scores, g_idx, g_out):
+    """Oracle on the sampled rows only; scores, Top-K and attention."""
+    o_sc, o_idx, _, _, _ = oracle.run(wl, rows=rows)
+    for i, r in enumerate(rows):
+        o = o_sc[i]
+        fin = np.isfinite(o)
+        g = g_scores[r][: len(o)]
+        assert np.array_equal(np.isfinite(g), fin)
+        assert np.abs(g[fin] - o[fin]).max() <= 1e-5 * (np.abs(o[fin]).max() + 1e-30)
+    check_topk(g_idx[rows], o_idx, o_sc, wl.q_pos, wl.K, rows=rows)
+    # row i of the index list belongs to rows[i]
+    ref, _ = oracle.sparse_attn(oracle.Batch.of(wl), wl.q, wl.kv_dtype, wl.k, wl.v, wl.kv_dtype,
+                                g_idx[rows], wl.K, wl.Hq, wl.Dqk, wl.Dv, wl.scale, rows=rows)
+    assert max_abs(g_out[rows], ref) <= ATOL_BF16
+
+
+def _run(si, wl, rows):
+    dw = si.upload(wl)
+    scores, idx, out = _separate(si, dw)
+    g_scores, g_idx, g_out = scores.cpu().numpy(), idx.cpu().numpy(), out.cpu().numpy()
+    _check_rows(wl, rows, g_scores, g_idx, g_out)
+    f_idx, f_out = _fused(si, dw)
+    assert np.array_equal(f_idx.cpu().numpy(), g_idx)
+    assert max_abs(f_out.cpu().numpy(), g_out) <= ATOL_BF16
+    return dw
+
+
+def test_benchmark_workload_full_size_sampled_rows(si):
+    wl = synth.make("c1")
+    assert wl.n_q == 64 and wl.max_ctx == 8192 and wl.K == 2048
+    _run(si, wl, rows=[0, 31, 63])
+
+
+def test_long_context_planted_full_size(si):
+    """Batch 16 x context 131072 with 1 % planted keys; Top-K over 131072
+    scores takes the streaming path."""
+    wl = synth.make("c3")
+    assert wl.n_q == 16 and wl.max_ctx == 131072
+    _run(si, wl, rows=[0, 7, 15])
+
+
+def test_mixed_batch_full_size(si):
+    """32 requests with log-uniform contexts in [1024, 65536]: 28 decode rows
+    and 4 prefill chunks of 2048 rows that cross K = pos + 1 nowhere but
+    still span many tiles."""
+    wl = synth.make("c4")
+    assert wl.n_q == 28 + 4 * 2048
+    _run(si, wl, rows=[0, 13, 27, 28, 28 + 2047, wl.n_q - 1])
+
+
+def test_causal_prefill_full_size(si):
+    """Causal prefill of 16384 rows: rows below K = 2048 keep every position,
+    later rows select."""
+    wl = synth.make("c2")
+    assert wl.n_q == 16384
+    _run(si, wl, rows=[0, 100, 2047, 2048, 9000, 16383])
