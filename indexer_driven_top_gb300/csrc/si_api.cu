@@ -181,7 +181,9 @@ unsigned int *status_word(void *ws) { return reinterpret_cast<unsigned int *>(ws
 si_status run_indexer(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
                       unsigned int *st, cudaStream_t s)
 {
-    cudaError_t e = si::indexer_tc_supported(b, ix, ld)
+    cudaError_t e = si::indexer_prefill_supported(b, ix, ld)
+                        ? si::launch_indexer_prefill(b, ix, scores, ld, st, s)
+                    : si::indexer_tc_supported(b, ix, ld)
                         ? si::launch_indexer_tc(b, ix, scores, ld, st, s)
                         : si::launch_indexer_generic(b, ix, scores, ld, st, s);
     return e == cudaSuccess ? SI_OK : cuda_fail(e, "indexer launch");

@@ -1,0 +1,524 @@
+// si_indexer_prefill.cu -- tensor-core indexer for a causal prefill: many
+// query rows of one sequence over a paged FP8 key cache.
+//
+// "Day0 Inference Support and Performance Optimization for New Architecture
+// LLMs": section 2.2 (every query row scores all earlier positions; per-head
+// scores are aggregated with head weights), section 4.1 (the scoring reads
+// the paged K-cache directly) and section 6.2 (in a causal prefill the
+// scoring work of a row grows with its position).  Score of key s for row r:
+//     k_scale[s] * sum_h w[r,h] * ReLU(q[r,h,:] . k[s,:])
+//
+// GB300 mapping.  All rows of a prefill score the same keys, so one key tile
+// (128 keys x 128 e4m3 bytes, UMMA A operand, landed by TMA) serves a block
+// of two query rows at once: the B operand holds both rows' 64 heads, each
+// split exactly into two e4m3 terms as in the decode indexer (q = s_h (q_hi +
+// q_lo), s_h a power of two folded into the head weight), so N = 2 x 128 =
+// 256 and every key byte brought in feeds a full-width UMMA.  The causal
+// triangle is balanced by dealing row blocks to CTAs in head/tail pairs
+// (block b together with block nb-1-b, the pairing section 6.3 uses for
+// context-parallel shards): every pair holds the same number of causal
+// (row, key) pairs.
+//
+// One persistent CTA per SM, 16 warps:
+//   warp 0      -- producer: per item (block, key tile) the TMA copies of the
+//                  tile's key pages into an eight-stage ring, and the keys'
+//                  scales into a ring per epilogue group (cp.async);
+//   warp 1      -- MMA: four kind::f8f6f4 UMMAs (M 128, N 256, K 32) per item
+//                  into one of two TMEM accumulators (256 columns each);
+//   warps 4..7  -- q-prep: splits each block's two query rows into the B
+//                  operand (double-buffered) and writes -inf into the rows'
+//                  score columns past the block's last live tile;
+//   warps 8..15 -- two epilogue groups that take alternate items: per key
+//                  (TMEM lane) and row, ReLU, head weights, scale, store.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "si_common.cuh"
+#include "si_internal.h"
+#include "si_sm100.cuh"
+#include "si_tmap.h"
+
+namespace si {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kKeys = 128;            // keys per tile = UMMA M
+constexpr int kHeads = 64;            // indexer heads
+constexpr int kDim = 128;             // head dim = bytes per e4m3 key row = UMMA K
+constexpr int kRows = 2;              // query rows per block
+constexpr int kRowN = 2 * kHeads;     // B rows per query row: q_hi heads, then q_lo heads
+constexpr int kN = kRows * kRowN;     // 256 = UMMA N
+constexpr int kStages = 8;            // key-tile ring depth
+constexpr int kScStages = 4;          // scale ring depth per epilogue group
+constexpr int kThreads = 16 * 32;
+constexpr int kWarpProd = 0, kWarpMma = 1, kWarpPrep0 = 4, kWarpEpi0 = 8;
+
+constexpr uint32_t kTile = kKeys * kDim;    // 16 KB, SW128 K-major
+constexpr uint32_t kTileB = kN * kDim;      // 32 KB, SW128 K-major
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffQ = kOffStage + kStages * kTile;               // [2] B operands
+constexpr uint32_t kOffW = kOffQ + 2 * kTileB;                         // [2][kRows][64] w * s_h
+constexpr uint32_t kOffWin = kOffW + 2 * kRows * kHeads * 4;           // 32 block-table entries
+constexpr uint32_t kOffSc = kOffWin + 32 * 4;                          // [2][kScStages][128]
+constexpr uint32_t kOffBar = kOffSc + 2 * kScStages * kKeys * 4;
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;                  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v)
+{
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+    return make_float2(__half2float(__ushort_as_half(h.x)), __half2float(__ushort_as_half(h.y)));
+}
+
+__device__ __forceinline__ uint16_t float2_to_e4m3x2(float a, float b)
+{
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// The CTA's row blocks, in processing order: pairs p = blockIdx.x,
+// blockIdx.x + G, ...; within a pair block p, then block nb - 1 - p.
+struct BlockWalk {
+    int64_t pair, npairs, G;
+    int nb, side;
+    __device__ BlockWalk(int nb_, int64_t G_) : pair(blockIdx.x), npairs((nb_ + 1) / 2), G(G_),
+                                                nb(nb_), side(0) {}
+    // next block index, or -1 when done
+    __device__ int next()
+    {
+        for (;;) {
+            if (pair >= npairs)
+                return -1;
+            const int blk = side == 0 ? (int)pair : nb - 1 - (int)pair;
+            const bool dup = side == 1 && blk == (int)pair;
+            if (side == 0) {
+                side = 1;
+            } else {
+                side = 0;
+                pair += G;
+            }
+            if (!dup)
+                return blk;
+        }
+    }
+};
+
+// Rows of block `blk` and its live key tiles (those holding a key at or
+// before the block's last position).
+__device__ __forceinline__ void block_shape(const si_batch &b, int blk, int tiles_ld, int &r0,
+                                            int &nrows, int &T)
+{
+    r0 = blk * kRows;
+    nrows = min(kRows, b.n_q - r0);
+    int pmax = -1;
+    for (int j = 0; j < nrows; j++)
+        pmax = max(pmax, __ldg(b.q_pos + r0 + j));
+    T = min(tiles_ld, (pmax + kKeys) / kKeys);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix,
+                  float *scores, int64_t ld, int n_blocks_rows, unsigned int *st)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(gbase + kOffBar);  // [kStages]
+    uint64_t *empty_bar = full_bar + kStages;                             // [kStages]
+    uint64_t *cfull_bar = empty_bar + kStages;                            // [2]
+    uint64_t *cempty_bar = cfull_bar + 2;                                 // [2]
+    uint64_t *qfull_bar = cempty_bar + 2;                                 // [2]
+    uint64_t *qempty_bar = qfull_bar + 2;                                 // [2]
+    uint64_t *scfull_bar = qempty_bar + 2;                                // [2][kScStages]
+    uint64_t *scempty_bar = scfull_bar + 2 * kScStages;                   // [2][kScStages]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(scempty_bar + 2 * kScStages);
+    float *w_s = reinterpret_cast<float *>(gbase + kOffW);
+    volatile int *win_s = reinterpret_cast<volatile int *>(gbase + kOffWin);
+    float *sc_s = reinterpret_cast<float *>(gbase + kOffSc);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t G = gridDim.x;
+    const int tiles_ld = (int)((ld + kKeys - 1) / kKeys);
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; i++) {
+            mbar_init(full_bar + i, 1);   // producer's expect_tx arrival
+            mbar_init(empty_bar + i, 1);  // MMA commit
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(cfull_bar + i, 1);             // MMA commit
+            mbar_init(cempty_bar + i, 128);          // epilogue group
+            mbar_init(qfull_bar + i, 128);           // q-prep threads
+            mbar_init(qempty_bar + i, 1 + 2 * 128);  // MMA commit + both epilogue groups
+        }
+        for (int i = 0; i < 2 * kScStages; i++) {
+            mbar_init(scfull_bar + i, 32);    // producer lanes (copy landed or sentinel)
+            mbar_init(scempty_bar + i, 128);  // epilogue group read the scales
+        }
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(tmem_slot, 2 * kN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int P = b.page_size;
+    const int lp = 31 - __clz(P);  // page_size is a power of two >= 8
+    const int seq = __ldg(b.q_seq);  // every row belongs to this sequence
+
+    if (warp == kWarpProd) {
+        // ------------------------------------------------------------ producer
+        const int span = min(P, kKeys);  // keys of one page inside one tile
+        int win = -1;                    // window: win_s[l] = block-table entry win + l
+        BlockWalk walk(n_blocks_rows, G);
+        int64_t it = 0;
+        bool ok = true;
+        for (int blk = walk.next(); ok && blk >= 0; blk = walk.next()) {
+            int r0, nrows, T;
+            block_shape(b, blk, tiles_ld, r0, nrows, T);
+            int pmax = -1;
+            for (int j = 0; j < nrows; j++)
+                pmax = max(pmax, __ldg(b.q_pos + r0 + j));
+            for (int t = 0; t < T; t++, it++) {
+                const int stg = (int)(it % kStages);
+                if (it >= kStages &&
+                    !mbar_wait(empty_bar + stg, (uint32_t)((it / kStages) - 1) & 1, st)) {
+                    ok = false;
+                    break;
+                }
+                const int s0 = t * kKeys;
+                const int first = s0 >> lp;
+                const int last = min(s0 + kKeys - 1, pmax) >> lp;
+                if (win < 0 || first < win || last >= win + 32) {
+                    win = first;
+                    const int lb = first + lane;
+                    int v = -1;
+                    if ((unsigned)seq < (unsigned)b.n_seq && lb < b.max_blocks)
+                        v = __ldg(b.block_table + (int64_t)seq * b.max_blocks + lb);
+                    win_s[lane] = v;
+                    __syncwarp();
+                }
+                // lane l handles page first + l of the tile
+                const int lb = first + lane;
+                bool copy = false;
+                int row = 0, k_lo = 0;
+                if (lane < 16 && lb <= last) {
+                    const int blkid = win_s[lb - win];
+                    if (lb < b.max_blocks && (unsigned)blkid < (unsigned)b.n_blocks) {
+                        copy = true;
+                        k_lo = max(lb << lp, s0) - s0;
+                        row = (blkid << lp) + (s0 + k_lo - (lb << lp));
+                    } else {
+                        raise_flag(st, SI_DEVFLAG_BAD_BLOCK);
+                    }
+                }
+                const uint32_t n_copies = __popc(__ballot_sync(0xffffffffu, copy));
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full_bar + stg, n_copies * span * kDim);
+                __syncwarp();
+                if (copy)
+                    tma_load_2d(base + kOffStage + stg * kTile + k_lo * kDim, &tmap, 0, row,
+                                full_bar + stg);
+                // scales of the tile's keys into the ring of epilogue group it & 1
+                const int g = (int)(it & 1);
+                const int64_t kit = it >> 1;
+                const int ss = (int)(kit % kScStages);
+                uint64_t *sf = scfull_bar + g * kScStages + ss;
+                if (kit >= kScStages &&
+                    !mbar_wait(scempty_bar + g * kScStages + ss,
+                               (uint32_t)((kit / kScStages) - 1) & 1, st)) {
+                    ok = false;
+                    break;
+                }
+                const int s4 = s0 + 4 * lane, lb4 = s4 >> lp;
+                int blk4 = -1;
+                if (lb4 <= last && lb4 < b.max_blocks) {
+                    const int v = win_s[lb4 - win];
+                    if ((unsigned)v < (unsigned)b.n_blocks)
+                        blk4 = v;
+                }
+                const uint32_t d = smem_u32(sc_s + (g * kScStages + ss) * kKeys + 4 * lane);
+                if (blk4 >= 0 && ix.k.scale) {
+                    cp_async_16(d, ix.k.scale + ((int64_t)blk4 << lp) + (s4 & (P - 1)));
+                    cp_async_arrive_noinc(sf);
+                } else {
+                    const uint32_t v = __float_as_uint(blk4 >= 0 ? 1.f : -1.f);
+                    st_shared_v4(d, v, v, v, v);
+                    mbar_arrive(sf);
+                }
+            }
+        }
+        cp_async_commit();
+        cp_async_wait<0>();  // nothing may land after the block has moved on
+    } else if (warp == kWarpMma) {
+        // ----------------------------------------------------------------- MMA
+        const uint32_t idesc = idesc_e4m3(kKeys, kN);
+        BlockWalk walk(n_blocks_rows, G);
+        int64_t it = 0;
+        int bi = 0;
+        bool ok = true;
+        for (int blk = walk.next(); ok && blk >= 0; blk = walk.next(), bi++) {
+            int r0, nrows, T;
+            block_shape(b, blk, tiles_ld, r0, nrows, T);
+            const int p = bi & 1;
+            if (!mbar_wait(qfull_bar + p, (uint32_t)(bi >> 1) & 1, st))
+                break;
+            for (int t = 0; t < T; t++, it++) {
+                const int stg = (int)(it % kStages);
+                const int g = (int)(it & 1);
+                const int64_t mg = it >> 1;  // this accumulator's use count
+                if (!mbar_wait(full_bar + stg, (uint32_t)(it / kStages) & 1, st) ||
+                    (mg >= 1 && !mbar_wait(cempty_bar + g, (uint32_t)(mg - 1) & 1, st))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t dacc = tmem + g * kN;
+#pragma unroll
+                    for (int kk = 0; kk < kDim / 32; kk++) {
+                        const uint64_t ad = smem_desc(base + kOffStage + stg * kTile + kk * 32, 16,
+                                                      1024, kSwizzle128B);
+                        const uint64_t bd =
+                            smem_desc(base + kOffQ + p * kTileB + kk * 32, 16, 1024, kSwizzle128B);
+                        umma_f8_ss(dacc, ad, bd, idesc, kk > 0);
+                    }
+                    umma_commit(empty_bar + stg);
+                    umma_commit(cfull_bar + g);
+                }
+                __syncwarp();
+            }
+            if (ok && lane == 0)
+                umma_commit(qempty_bar + p);  // the block's B operand is free once read
+            __syncwarp();
+        }
+    } else if (warp >= kWarpPrep0 && warp < kWarpEpi0) {
+        // -------------------------------------------------------------- q-prep
+        // Thread pt splits dims [64 half, +64) of head h of both rows.
+        const int pt = tid - kWarpPrep0 * 32;
+        const int h = pt >> 1, half = pt & 1;
+        BlockWalk walk(n_blocks_rows, G);
+        int bi = 0;
+        for (int blk = walk.next(); blk >= 0; blk = walk.next(), bi++) {
+            int r0, nrows, T;
+            block_shape(b, blk, tiles_ld, r0, nrows, T);
+            const int p = bi & 1;
+            if (bi >= 2 && !mbar_wait(qempty_bar + p, (uint32_t)((bi - 2) >> 1) & 1, st))
+                break;
+            const uint32_t qb = base + kOffQ + p * kTileB;
+            for (int j = 0; j < kRows; j++) {
+                const bool have = j < nrows;
+                uint32_t q2[32];  // 64 bf16 dims, two per word
+                if (have) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        static_cast<const uint16_t *>(ix.q) +
+                        ((int64_t)(r0 + j) * kHeads + h) * kDim + half * 64);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        const uint4 v = __ldg(src + i);
+                        q2[4 * i] = v.x;
+                        q2[4 * i + 1] = v.y;
+                        q2[4 * i + 2] = v.z;
+                        q2[4 * i + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        q2[i] = 0;
+                }
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    amax = fmaxf(amax, fabsf(__uint_as_float(q2[i] << 16)));
+                    amax = fmaxf(amax, fabsf(__uint_as_float(q2[i] & 0xFFFF0000u)));
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                // s_h = 2^e with max|q_h| / s_h in (224, 448]
+                int e = 0;
+                if (amax > 0.f) {
+                    e = (int)ceilf(log2f(amax / 448.f));
+                    while (ldexpf(amax, -e) > 448.f)
+                        e++;
+                    while (ldexpf(amax, -(e - 1)) <= 448.f)
+                        e--;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; c++) {  // 16 dims per 16-byte unit
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; jj++) {  // 4 dims per output word
+                        uint32_t hw = 0, lw = 0;
+#pragma unroll
+                        for (int pr2 = 0; pr2 < 2; pr2++) {
+                            const uint32_t word = q2[8 * c + 2 * jj + pr2];
+                            const float x0 = ldexpf(__uint_as_float(word << 16), -e);
+                            const float x1 = ldexpf(__uint_as_float(word & 0xFFFF0000u), -e);
+                            const uint16_t h2 = float2_to_e4m3x2(x0, x1);
+                            const float2 hf = e4m3x2_to_float2(h2);
+                            const uint16_t l2 = float2_to_e4m3x2(x0 - hf.x, x1 - hf.y);
+                            hw |= (uint32_t)h2 << (16 * pr2);
+                            lw |= (uint32_t)l2 << (16 * pr2);
+                        }
+                        hi[jj] = hw;
+                        lo[jj] = lw;
+                    }
+                    const uint32_t u = (uint32_t)(half * 4 + c);
+                    st_shared_v4(qb + sw128_offset(j * kRowN + h, u), hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(qb + sw128_offset(j * kRowN + kHeads + h, u), lo[0], lo[1], lo[2],
+                                 lo[3]);
+                }
+                if (half == 0)
+                    w_s[(p * kRows + j) * kHeads + h] =
+                        have ? ldexpf(__ldg(ix.w + (int64_t)(r0 + j) * kHeads + h), e) : 0.f;
+            }
+            fence_async_smem();
+            mbar_arrive(qfull_bar + p);
+            // score columns past the block's live tiles are -inf
+            const int64_t c0 = (int64_t)T * kKeys;
+            for (int j = 0; j < nrows; j++)
+                for (int64_t c = c0 + pt; c < ld; c += 128)
+                    scores[(int64_t)(r0 + j) * ld + c] = -INFINITY;
+        }
+    } else if (warp >= kWarpEpi0) {
+        // ------------------------------------------------------------ epilogue
+        // Group g takes items g, g + 2, ...; it walks every item to keep the
+        // block bookkeeping.
+        const int g = (warp - kWarpEpi0) >> 2;
+        const int et = (tid - kWarpEpi0 * 32) & 127;  // key row = TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        BlockWalk walk(n_blocks_rows, G);
+        int64_t it = 0;
+        int bi = 0;
+        bool ok = true;
+        for (int blk = walk.next(); ok && blk >= 0; blk = walk.next(), bi++) {
+            int r0, nrows, T;
+            block_shape(b, blk, tiles_ld, r0, nrows, T);
+            const int p = bi & 1;
+            int pos[kRows];
+#pragma unroll
+            for (int j = 0; j < kRows; j++)
+                pos[j] = j < nrows ? __ldg(b.q_pos + r0 + j) : -1;
+            if (!mbar_wait(qfull_bar + p, (uint32_t)(bi >> 1) & 1, st))
+                break;
+            for (int t = 0; t < T; t++, it++) {
+                if ((int)(it & 1) != g)
+                    continue;
+                const int64_t kit = it >> 1;
+                const int ss = (int)(kit % kScStages);
+                if (!mbar_wait(scfull_bar + g * kScStages + ss, (uint32_t)(kit / kScStages) & 1,
+                               st)) {
+                    ok = false;
+                    break;
+                }
+                const float scv = sc_s[(g * kScStages + ss) * kKeys + et];
+                mbar_arrive(scempty_bar + g * kScStages + ss);
+                if (!mbar_wait(cfull_bar + g, (uint32_t)kit & 1, st)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int s = t * kKeys + et;
+                const uint32_t acc = tmem + g * kN + lane_off;
+                float sum[kRows];
+#pragma unroll
+                for (int j = 0; j < kRows; j++) {
+                    const float4 *w4 =
+                        reinterpret_cast<const float4 *>(w_s + (p * kRows + j) * kHeads);
+                    float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int hh = 0; hh < 2; hh++) {  // heads [32 hh, 32 hh + 32)
+                        uint32_t vh[32], vl[32];
+                        tmem_ld32(acc + j * kRowN + hh * 32, vh);
+                        tmem_ld32(acc + j * kRowN + kHeads + hh * 32, vl);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 wv = w4[(hh * 32 + i) >> 2];
+                            const float wq[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                            for (int k = 0; k < 4; k++) {
+                                const float lg =
+                                    __uint_as_float(vh[i + k]) + __uint_as_float(vl[i + k]);
+                                part[k] = fmaf(wq[k], fmaxf(lg, 0.f), part[k]);
+                            }
+                        }
+                    }
+                    sum[j] = (part[0] + part[1]) + (part[2] + part[3]);
+                }
+                tc_fence_before();
+                mbar_arrive(cempty_bar + g);
+                if (s < ld) {
+#pragma unroll
+                    for (int j = 0; j < kRows; j++)
+                        if (j < nrows)
+                            scores[(int64_t)(r0 + j) * ld + s] =
+                                (s <= pos[j] && scv >= 0.f) ? sum[j] * scv + 0.0f : -INFINITY;
+                }
+            }
+            if (ok)
+                mbar_arrive(qempty_bar + p);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma)
+        tmem_dealloc(tmem, 2 * kN);
+}
+
+}  // namespace
+
+bool indexer_prefill_supported(const si_batch &b, const si_indexer &ix, int64_t ld)
+{
+    // one sequence (so every row scores the same keys), enough rows to share
+    // tiles, and the decode indexer's operand conditions
+    return b.n_seq == 1 && b.n_q >= 64 && indexer_tc_supported(b, ix, ld);
+}
+
+cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, float *scores,
+                                   int64_t ld, unsigned int *st, cudaStream_t s)
+{
+    static std::once_flag once[kMaxDevices];
+    static int sms_of[kMaxDevices];
+    static cudaError_t err_of[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(k_indexer_prefill,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        err_of[dev] = r;
+    });
+    if (err_of[dev] != cudaSuccess)
+        return err_of[dev];
+    CUtensorMap tmap;
+    e = make_tmap_2d_u8_sw128(&tmap, ix.k.data, kDim, (uint64_t)b.n_blocks * b.page_size,
+                              (uint64_t)ix.k.row_stride, kDim,
+                              (uint32_t)std::min(b.page_size, kKeys));
+    if (e != cudaSuccess)
+        return e;
+    const int nb = (b.n_q + kRows - 1) / kRows;
+    const int64_t npairs = (nb + 1) / 2;
+    const int64_t grid = std::min<int64_t>(npairs, (int64_t)sms_of[dev]);
+    count_launch();
+    k_indexer_prefill<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores, ld, nb,
+                                                                   st);
+    return cudaGetLastError();
+}
+
+}  // namespace si

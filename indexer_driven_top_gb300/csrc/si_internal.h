@@ -32,6 +32,12 @@ bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld);
 cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
                               unsigned int *st, cudaStream_t s);
 
+// Tensor-core indexer for a causal prefill of one sequence: blocks of two
+// query rows share each key tile (same operand conditions as above).
+bool indexer_prefill_supported(const si_batch &b, const si_indexer &ix, int64_t ld);
+cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, float *scores,
+                                   int64_t ld, unsigned int *st, cudaStream_t s);
+
 // Tensor-core sparse attention: bf16, 128 heads, 576-dim latent rows (V = first 512).
 bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top);
 cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int32_t *idx,
