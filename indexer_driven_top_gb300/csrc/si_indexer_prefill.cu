@@ -58,15 +58,16 @@ constexpr int kN = kRows * kRowN;     // 256 = UMMA N
 constexpr int kStages = 8;            // key-tile ring depth
 constexpr int kScStages = 4;          // scale ring depth per epilogue group
 constexpr int kThreads = 16 * 32;
-constexpr int kWarpProd = 0, kWarpMma = 1, kWarpPrep0 = 4, kWarpEpi0 = 8;
+constexpr int kWarpProd0 = 0, kWarpProd1 = 2;  // producers: items of parity 0 / 1
+constexpr int kWarpMma = 1, kWarpPrep0 = 4, kWarpEpi0 = 8;
 
 constexpr uint32_t kTile = kKeys * kDim;    // 16 KB, SW128 K-major
 constexpr uint32_t kTileB = kN * kDim;      // 32 KB, SW128 K-major
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffQ = kOffStage + kStages * kTile;               // [2] B operands
 constexpr uint32_t kOffW = kOffQ + 2 * kTileB;                         // [2][kRows][64] w * s_h
-constexpr uint32_t kOffWin = kOffW + 2 * kRows * kHeads * 4;           // 32 block-table entries
-constexpr uint32_t kOffSc = kOffWin + 32 * 4;                          // [2][kScStages][128]
+constexpr uint32_t kOffWin = kOffW + 2 * kRows * kHeads * 4;           // 2 x 32 block-table entries
+constexpr uint32_t kOffSc = kOffWin + 2 * 32 * 4;                      // [2][kScStages][128]
 constexpr uint32_t kOffBar = kOffSc + 2 * kScStages * kKeys * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;                  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -139,7 +140,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
     uint64_t *scempty_bar = scfull_bar + 2 * kScStages;                   // [2][kScStages]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(scempty_bar + 2 * kScStages);
     float *w_s = reinterpret_cast<float *>(gbase + kOffW);
-    volatile int *win_s = reinterpret_cast<volatile int *>(gbase + kOffWin);
+    volatile int *win_all = reinterpret_cast<volatile int *>(gbase + kOffWin);
     float *sc_s = reinterpret_cast<float *>(gbase + kOffSc);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -175,8 +176,13 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
     const int lp = 31 - __clz(P);  // page_size is a power of two >= 8
     const int seq = __ldg(b.q_seq);  // every row belongs to this sequence
 
-    if (warp == kWarpProd) {
+    if (warp == kWarpProd0 || warp == kWarpProd1) {
         // ------------------------------------------------------------ producer
+        // Two producer warps take alternate items (a bulk tensor copy holds
+        // its issuing warp for several hundred cycles); producer pw also
+        // fills the scale ring of epilogue group pw.
+        const int pw = warp == kWarpProd0 ? 0 : 1;
+        volatile int *win_s = win_all + pw * 32;
         const int span = min(P, kKeys);  // keys of one page inside one tile
         int win = -1;                    // window: win_s[l] = block-table entry win + l
         BlockWalk walk(n_blocks_rows, G);
@@ -189,6 +195,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
             for (int j = 0; j < nrows; j++)
                 pmax = max(pmax, __ldg(b.q_pos + r0 + j));
             for (int t = 0; t < T; t++, it++) {
+                if ((int)(it & 1) != pw)
+                    continue;
                 const int stg = (int)(it % kStages);
                 if (it >= kStages &&
                     !mbar_wait(empty_bar + stg, (uint32_t)((it / kStages) - 1) & 1, st)) {
@@ -228,8 +236,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                 if (copy)
                     tma_load_2d(base + kOffStage + stg * kTile + k_lo * kDim, &tmap, 0, row,
                                 full_bar + stg);
-                // scales of the tile's keys into the ring of epilogue group it & 1
-                const int g = (int)(it & 1);
+                // scales of the tile's keys into the ring of epilogue group pw
+                const int g = pw;
                 const int64_t kit = it >> 1;
                 const int ss = (int)(kit % kScStages);
                 uint64_t *sf = scfull_bar + g * kScStages + ss;
