@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define SI_VERSION 1
+#define SI_VERSION 2
 
 typedef enum si_status {
     SI_OK = 0,
@@ -105,8 +105,14 @@ typedef struct si_paged {
 /* Indexer operands (section 2.2: lightweight multi-head indexer; section 5.1
  * stores its keys in FP8). */
 typedef struct si_indexer {
-    const void *q;       /* device [n_q, n_heads, head_dim], SI_F32 or SI_BF16 */
+    const void *q;       /* device [n_q, n_heads, head_dim], SI_F32, SI_BF16 or
+                            SI_E4M3 */
     si_dtype q_dtype;
+    const float *q_scale; /* device [n_q, n_heads] dequantisation scale (> 0) of
+                            an SI_E4M3 query, one per (row, head): the query is
+                            stored quantised per group as in section 4.3's
+                            prolog, a group being one head.  Required for
+                            SI_E4M3, ignored otherwise. */
     const float *w;      /* device [n_q, n_heads] head weights */
     int32_t n_heads;     /* 1..128 */
     int32_t head_dim;    /* 1..256 */

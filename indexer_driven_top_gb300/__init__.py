@@ -49,8 +49,9 @@ class c_paged(ctypes.Structure):
 
 
 class c_indexer(ctypes.Structure):
-    _fields_ = [("q", ctypes.c_void_p), ("q_dtype", ctypes.c_int), ("w", ctypes.c_void_p),
-                ("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("k", c_paged)]
+    _fields_ = [("q", ctypes.c_void_p), ("q_dtype", ctypes.c_int), ("q_scale", ctypes.c_void_p),
+                ("w", ctypes.c_void_p), ("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("k", c_paged)]
 
 
 class c_attention(ctypes.Structure):
@@ -160,10 +161,11 @@ class Indexer:
     q_dtype: str
     w: torch.Tensor             # [n_q, n_heads] float32
     k: Paged
+    q_scale: Optional[torch.Tensor] = None   # [n_q, n_heads] float32 for an e4m3 query
 
     def c(self) -> c_indexer:
-        return c_indexer(_ptr(self.q), DTYPES[self.q_dtype], _ptr(self.w), self.q.shape[1],
-                         self.q.shape[2], self.k.c())
+        return c_indexer(_ptr(self.q), DTYPES[self.q_dtype], _ptr(self.q_scale), _ptr(self.w),
+                         self.q.shape[1], self.q.shape[2], self.k.c())
 
 
 @dataclasses.dataclass
@@ -310,6 +312,8 @@ def upload(wl, device="cuda") -> DeviceWorkload:
     ten["q_seq"] = _dev(wl.q_seq, device)
     ten["q_pos"] = _dev(wl.q_pos, device)
     ten["q_idx"] = _dev(wl.q_idx, device, bf if wl.q_idx_dtype == "bf16" else None)
+    q_scale = getattr(wl, "q_scale", None)
+    ten["q_scale"] = None if q_scale is None else _dev(q_scale, device)
     ten["w"] = _dev(wl.w, device)
     ten["k_idx"] = _dev(wl.k_idx, device)
     ten["k_scale"] = None if wl.k_scale is None else _dev(wl.k_scale, device)
@@ -320,7 +324,7 @@ def upload(wl, device="cuda") -> DeviceWorkload:
     b = Batch(ten["block_table"], ten["ctx_len"], ten["q_seq"], ten["q_pos"], wl.page,
               wl.max_ctx, wl.n_blocks)
     ix = Indexer(ten["q_idx"], wl.q_idx_dtype, ten["w"],
-                 Paged(ten["k_idx"], wl.k_idx_dtype, wl.Di, ten["k_scale"]))
+                 Paged(ten["k_idx"], wl.k_idx_dtype, wl.Di, ten["k_scale"]), ten["q_scale"])
     kp = Paged(ten["k"], wl.kv_dtype, wl.Dqk)
     vp = kp if ten["v"] is None else Paged(ten["v"], wl.kv_dtype, wl.Dv)
     at = Attention(ten["q"], wl.kv_dtype, kp, Paged(vp.data, vp.dtype, wl.Dv), wl.Dv, wl.scale)

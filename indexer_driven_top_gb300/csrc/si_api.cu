@@ -102,8 +102,10 @@ si_status check_indexer(const si_indexer *ix)
         return fail(SI_ERR_INVALID_ARG, "indexer operands are NULL");
     if (!ix->q || !ix->w)
         return fail(SI_ERR_INVALID_ARG, "indexer q or w is NULL");
-    if (ix->q_dtype != SI_F32 && ix->q_dtype != SI_BF16)
-        return fail(SI_ERR_INVALID_ARG, "indexer q dtype must be f32 or bf16");
+    if (ix->q_dtype != SI_F32 && ix->q_dtype != SI_BF16 && ix->q_dtype != SI_E4M3)
+        return fail(SI_ERR_INVALID_ARG, "indexer q dtype must be f32, bf16 or e4m3");
+    if (ix->q_dtype == SI_E4M3 && !ix->q_scale)
+        return fail(SI_ERR_INVALID_ARG, "an e4m3 indexer q needs q_scale");
     if (ix->n_heads < 1 || ix->n_heads > 128)
         return fail(SI_ERR_INVALID_ARG, "indexer n_heads %d outside 1..128", ix->n_heads);
     if (ix->head_dim < 1 || ix->head_dim > 256)
@@ -173,6 +175,8 @@ si_indexer indexer_slice(const si_indexer &ix, int32_t r0)
     s.q = static_cast<const char *>(ix.q) +
           (size_t)r0 * ix.n_heads * ix.head_dim * dtype_bytes(ix.q_dtype);
     s.w = ix.w + (size_t)r0 * ix.n_heads;
+    if (ix.q_scale)
+        s.q_scale = ix.q_scale + (size_t)r0 * ix.n_heads;
     return s;
 }
 

@@ -40,7 +40,8 @@ k_indexer_generic(si_batch b, si_indexer ix, float *scores, int64_t ld, unsigned
     const int seq = b.q_seq[r];
 
     for (int i = tid; i < H * D; i += kIdxKeys)
-        q_s[i] = load_elem(ix.q, ix.q_dtype, (int64_t)r * H * D + i);
+        q_s[i] = load_elem(ix.q, ix.q_dtype, (int64_t)r * H * D + i) *
+                 (ix.q_dtype == SI_E4M3 ? ix.q_scale[(int64_t)r * H + i / D] : 1.f);
     for (int i = tid; i < H; i += kIdxKeys)
         w_s[i] = ix.w[(int64_t)r * H + i];
     const int64_t s = s0 + tid;

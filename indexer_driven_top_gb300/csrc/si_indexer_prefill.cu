@@ -10,24 +10,31 @@
 //
 // GB300 mapping.  All rows of a prefill score the same keys, so one key tile
 // (128 keys x 128 e4m3 bytes, UMMA A operand, landed by TMA) serves a block
-// of two query rows at once: the B operand holds both rows' 64 heads, each
-// split exactly into two e4m3 terms as in the decode indexer (q = s_h (q_hi +
-// q_lo), s_h a power of two folded into the head weight), so N = 2 x 128 =
-// 256 and every key byte brought in feeds a full-width UMMA.  The causal
-// triangle is balanced by dealing row blocks to CTAs in head/tail pairs
-// (block b together with block nb-1-b, the pairing section 6.3 uses for
+// of query rows at once, and the B operand is always 256 rows wide (UMMA N =
+// 256) so that every key byte brought in feeds a full-width UMMA:
+//   * bf16 query: two rows per block, each row's 64 heads split exactly into
+//     two e4m3 terms as in the decode indexer (q = s_h (q_hi + q_lo), s_h a
+//     power of two folded into the head weight): 2 x 128 B rows;
+//   * FP8 query with a per-(row, head) scale (section 4.3 quantises the
+//     indexer query before scoring): four rows per block, 64 heads each, the
+//     scale folded into the head weight: 4 x 64 B rows, twice the scores per
+//     UMMA and per TMEM column read.
+// The causal triangle is balanced by dealing row blocks to CTAs in head/tail
+// pairs (block b together with block nb-1-b, the pairing section 6.3 uses for
 // context-parallel shards): every pair holds the same number of causal
 // (row, key) pairs.
 //
 // One persistent CTA per SM, 16 warps:
-//   warp 0      -- producer: per item (block, key tile) the TMA copies of the
-//                  tile's key pages into an eight-stage ring, and the keys'
-//                  scales into a ring per epilogue group (cp.async);
+//   warps 0, 2  -- producers, alternate items (a bulk tensor copy holds its
+//                  issuing warp for several hundred cycles): per item (block,
+//                  key tile) the TMA copies of the tile's key pages into an
+//                  eight-stage ring, and the keys' scales into the ring of the
+//                  epilogue group that takes the item (cp.async);
 //   warp 1      -- MMA: four kind::f8f6f4 UMMAs (M 128, N 256, K 32) per item
 //                  into one of two TMEM accumulators (256 columns each);
-//   warps 4..7  -- q-prep: splits each block's two query rows into the B
-//                  operand (double-buffered) and writes -inf into the rows'
-//                  score columns past the block's last live tile;
+//   warps 4..7  -- q-prep: writes each block's query rows into the B operand
+//                  (double-buffered) and -inf into the rows' score columns
+//                  past the block's last live tile;
 //   warps 8..15 -- two epilogue groups that take alternate items: per key
 //                  (TMEM lane) and row, ReLU, head weights, scale, store.
 #include <cuda.h>
@@ -52,9 +59,12 @@ using namespace sm100;
 constexpr int kKeys = 128;            // keys per tile = UMMA M
 constexpr int kHeads = 64;            // indexer heads
 constexpr int kDim = 128;             // head dim = bytes per e4m3 key row = UMMA K
-constexpr int kRows = 2;              // query rows per block
-constexpr int kRowN = 2 * kHeads;     // B rows per query row: q_hi heads, then q_lo heads
-constexpr int kN = kRows * kRowN;     // 256 = UMMA N
+constexpr int kN = 256;               // UMMA N: B rows of one block's query rows
+constexpr int kMaxRows = 4;           // query rows per block, FP8 query
+// B rows per query row: a bf16 query takes 64 q_hi heads then 64 q_lo heads,
+// an FP8 query its 64 heads as stored.
+template <bool Q8> constexpr int row_n() { return Q8 ? kHeads : 2 * kHeads; }
+template <bool Q8> constexpr int rows_per_block() { return kN / row_n<Q8>(); }
 constexpr int kStages = 8;            // key-tile ring depth
 constexpr int kScStages = 4;          // scale ring depth per epilogue group
 constexpr int kThreads = 16 * 32;
@@ -65,8 +75,8 @@ constexpr uint32_t kTile = kKeys * kDim;    // 16 KB, SW128 K-major
 constexpr uint32_t kTileB = kN * kDim;      // 32 KB, SW128 K-major
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffQ = kOffStage + kStages * kTile;               // [2] B operands
-constexpr uint32_t kOffW = kOffQ + 2 * kTileB;                         // [2][kRows][64] w * s_h
-constexpr uint32_t kOffWin = kOffW + 2 * kRows * kHeads * 4;           // 2 x 32 block-table entries
+constexpr uint32_t kOffW = kOffQ + 2 * kTileB;                         // [2][rows][64] w * s_h
+constexpr uint32_t kOffWin = kOffW + 2 * kMaxRows * kHeads * 4;        // 2 x 32 block-table entries
 constexpr uint32_t kOffSc = kOffWin + 2 * 32 * 4;                      // [2][kScStages][128]
 constexpr uint32_t kOffBar = kOffSc + 2 * kScStages * kKeys * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;                  // + alignment slack
@@ -112,6 +122,7 @@ struct BlockWalk {
 
 // Rows of block `blk` and its live key tiles (those holding a key at or
 // before the block's last position).
+template <int kRows>
 __device__ __forceinline__ void block_shape(const si_batch &b, int blk, int tiles_ld, int &r0,
                                             int &nrows, int &T)
 {
@@ -123,10 +134,13 @@ __device__ __forceinline__ void block_shape(const si_batch &b, int blk, int tile
     T = min(tiles_ld, (pmax + kKeys) / kKeys);
 }
 
+template <bool Q8>
 __global__ void __launch_bounds__(kThreads, 1)
 k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix,
                   float *scores, int64_t ld, int n_blocks_rows, unsigned int *st)
 {
+    constexpr int kRows = rows_per_block<Q8>();
+    constexpr int kRowN = row_n<Q8>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
@@ -190,7 +204,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
         bool ok = true;
         for (int blk = walk.next(); ok && blk >= 0; blk = walk.next()) {
             int r0, nrows, T;
-            block_shape(b, blk, tiles_ld, r0, nrows, T);
+            block_shape<kRows>(b, blk, tiles_ld, r0, nrows, T);
             int pmax = -1;
             for (int j = 0; j < nrows; j++)
                 pmax = max(pmax, __ldg(b.q_pos + r0 + j));
@@ -276,7 +290,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
         bool ok = true;
         for (int blk = walk.next(); ok && blk >= 0; blk = walk.next(), bi++) {
             int r0, nrows, T;
-            block_shape(b, blk, tiles_ld, r0, nrows, T);
+            block_shape<kRows>(b, blk, tiles_ld, r0, nrows, T);
             const int p = bi & 1;
             if (!mbar_wait(qfull_bar + p, (uint32_t)(bi >> 1) & 1, st))
                 break;
@@ -311,82 +325,102 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
         }
     } else if (warp >= kWarpPrep0 && warp < kWarpEpi0) {
         // -------------------------------------------------------------- q-prep
-        // Thread pt splits dims [64 half, +64) of head h of both rows.
+        // Thread pt prepares dims [64 half, +64) of head h of every row.
         const int pt = tid - kWarpPrep0 * 32;
         const int h = pt >> 1, half = pt & 1;
         BlockWalk walk(n_blocks_rows, G);
         int bi = 0;
         for (int blk = walk.next(); blk >= 0; blk = walk.next(), bi++) {
             int r0, nrows, T;
-            block_shape(b, blk, tiles_ld, r0, nrows, T);
+            block_shape<kRows>(b, blk, tiles_ld, r0, nrows, T);
             const int p = bi & 1;
             if (bi >= 2 && !mbar_wait(qempty_bar + p, (uint32_t)((bi - 2) >> 1) & 1, st))
                 break;
             const uint32_t qb = base + kOffQ + p * kTileB;
-            for (int j = 0; j < kRows; j++) {
-                const bool have = j < nrows;
-                uint32_t q2[32];  // 64 bf16 dims, two per word
-                if (have) {
+            if constexpr (Q8) {
+                // stored FP8 query: codes as they are, the scale joins the weight
+                for (int j = 0; j < kRows; j++) {
+                    const bool have = j < nrows;
+                    const int64_t rh = (int64_t)(r0 + j) * kHeads + h;
                     const uint4 *src = reinterpret_cast<const uint4 *>(
-                        static_cast<const uint16_t *>(ix.q) +
-                        ((int64_t)(r0 + j) * kHeads + h) * kDim + half * 64);
+                        static_cast<const uint8_t *>(ix.q) + rh * kDim + half * 64);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        const uint4 v = __ldg(src + i);
-                        q2[4 * i] = v.x;
-                        q2[4 * i + 1] = v.y;
-                        q2[4 * i + 2] = v.z;
-                        q2[4 * i + 3] = v.w;
+                    for (int c = 0; c < 4; c++) {
+                        const uint4 v = have ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                        st_shared_v4(qb + sw128_offset(j * kRowN + h, (uint32_t)(half * 4 + c)),
+                                     v.x, v.y, v.z, v.w);
                     }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        q2[i] = 0;
+                    if (half == 0)
+                        w_s[(p * kRows + j) * kHeads + h] =
+                            have ? __ldg(ix.w + rh) * __ldg(ix.q_scale + rh) : 0.f;
                 }
-                float amax = 0.f;
+            } else {
+                for (int j = 0; j < kRows; j++) {
+                    const bool have = j < nrows;
+                    uint32_t q2[32];  // 64 bf16 dims, two per word
+                    if (have) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(
+                            static_cast<const uint16_t *>(ix.q) +
+                            ((int64_t)(r0 + j) * kHeads + h) * kDim + half * 64);
 #pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    amax = fmaxf(amax, fabsf(__uint_as_float(q2[i] << 16)));
-                    amax = fmaxf(amax, fabsf(__uint_as_float(q2[i] & 0xFFFF0000u)));
-                }
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                // s_h = 2^e with max|q_h| / s_h in (224, 448]
-                int e = 0;
-                if (amax > 0.f) {
-                    e = (int)ceilf(log2f(amax / 448.f));
-                    while (ldexpf(amax, -e) > 448.f)
-                        e++;
-                    while (ldexpf(amax, -(e - 1)) <= 448.f)
-                        e--;
-                }
-#pragma unroll
-                for (int c = 0; c < 4; c++) {  // 16 dims per 16-byte unit
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; jj++) {  // 4 dims per output word
-                        uint32_t hw = 0, lw = 0;
-#pragma unroll
-                        for (int pr2 = 0; pr2 < 2; pr2++) {
-                            const uint32_t word = q2[8 * c + 2 * jj + pr2];
-                            const float x0 = ldexpf(__uint_as_float(word << 16), -e);
-                            const float x1 = ldexpf(__uint_as_float(word & 0xFFFF0000u), -e);
-                            const uint16_t h2 = float2_to_e4m3x2(x0, x1);
-                            const float2 hf = e4m3x2_to_float2(h2);
-                            const uint16_t l2 = float2_to_e4m3x2(x0 - hf.x, x1 - hf.y);
-                            hw |= (uint32_t)h2 << (16 * pr2);
-                            lw |= (uint32_t)l2 << (16 * pr2);
+                        for (int i = 0; i < 8; i++) {
+                            const uint4 v = __ldg(src + i);
+                            q2[4 * i] = v.x;
+                            q2[4 * i + 1] = v.y;
+                            q2[4 * i + 2] = v.z;
+                            q2[4 * i + 3] = v.w;
                         }
-                        hi[jj] = hw;
-                        lo[jj] = lw;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++)
+                            q2[i] = 0;
                     }
-                    const uint32_t u = (uint32_t)(half * 4 + c);
-                    st_shared_v4(qb + sw128_offset(j * kRowN + h, u), hi[0], hi[1], hi[2], hi[3]);
-                    st_shared_v4(qb + sw128_offset(j * kRowN + kHeads + h, u), lo[0], lo[1], lo[2],
-                                 lo[3]);
+                    float amax = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; i++) {
+                        amax = fmaxf(amax, fabsf(__uint_as_float(q2[i] << 16)));
+                        amax = fmaxf(amax, fabsf(__uint_as_float(q2[i] & 0xFFFF0000u)));
+                    }
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                    // s_h = 2^e with max|q_h| / s_h in (224, 448]
+                    int e = 0;
+                    if (amax > 0.f) {
+                        e = (int)ceilf(log2f(amax / 448.f));
+                        while (ldexpf(amax, -e) > 448.f)
+                            e++;
+                        while (ldexpf(amax, -(e - 1)) <= 448.f)
+                            e--;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {  // 16 dims per 16-byte unit
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int jj = 0; jj < 4; jj++) {  // 4 dims per output word
+                            uint32_t hw = 0, lw = 0;
+#pragma unroll
+                            for (int pr2 = 0; pr2 < 2; pr2++) {
+                                const uint32_t word = q2[8 * c + 2 * jj + pr2];
+                                const float x0 = ldexpf(__uint_as_float(word << 16), -e);
+                                const float x1 = ldexpf(__uint_as_float(word & 0xFFFF0000u), -e);
+                                const uint16_t h2 = float2_to_e4m3x2(x0, x1);
+                                const float2 hf = e4m3x2_to_float2(h2);
+                                const uint16_t l2 = float2_to_e4m3x2(x0 - hf.x, x1 - hf.y);
+                                hw |= (uint32_t)h2 << (16 * pr2);
+                                lw |= (uint32_t)l2 << (16 * pr2);
+                            }
+                            hi[jj] = hw;
+                            lo[jj] = lw;
+                        }
+                        const uint32_t u = (uint32_t)(half * 4 + c);
+                        st_shared_v4(qb + sw128_offset(j * kRowN + h, u), hi[0], hi[1], hi[2],
+                                     hi[3]);
+                        st_shared_v4(qb + sw128_offset(j * kRowN + kHeads + h, u), lo[0], lo[1],
+                                     lo[2], lo[3]);
+                    }
+                    if (half == 0)
+                        w_s[(p * kRows + j) * kHeads + h] =
+                            have ? ldexpf(__ldg(ix.w + (int64_t)(r0 + j) * kHeads + h), e) : 0.f;
                 }
-                if (half == 0)
-                    w_s[(p * kRows + j) * kHeads + h] =
-                        have ? ldexpf(__ldg(ix.w + (int64_t)(r0 + j) * kHeads + h), e) : 0.f;
             }
             fence_async_smem();
             mbar_arrive(qfull_bar + p);
@@ -409,7 +443,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
         bool ok = true;
         for (int blk = walk.next(); ok && blk >= 0; blk = walk.next(), bi++) {
             int r0, nrows, T;
-            block_shape(b, blk, tiles_ld, r0, nrows, T);
+            block_shape<kRows>(b, blk, tiles_ld, r0, nrows, T);
             const int p = bi & 1;
             int pos[kRows];
 #pragma unroll
@@ -446,7 +480,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                     for (int hh = 0; hh < 2; hh++) {  // heads [32 hh, 32 hh + 32)
                         uint32_t vh[32], vl[32];
                         tmem_ld32(acc + j * kRowN + hh * 32, vh);
-                        tmem_ld32(acc + j * kRowN + kHeads + hh * 32, vl);
+                        if constexpr (!Q8)
+                            tmem_ld32(acc + j * kRowN + kHeads + hh * 32, vl);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
@@ -454,8 +489,9 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                             const float wq[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                             for (int k = 0; k < 4; k++) {
-                                const float lg =
-                                    __uint_as_float(vh[i + k]) + __uint_as_float(vl[i + k]);
+                                float lg = __uint_as_float(vh[i + k]);
+                                if constexpr (!Q8)
+                                    lg += __uint_as_float(vl[i + k]);
                                 part[k] = fmaf(wq[k], fmaxf(lg, 0.f), part[k]);
                             }
                         }
@@ -508,7 +544,10 @@ cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, floa
     std::call_once(once[dev], [dev] {
         cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(k_indexer_prefill,
+            r = cudaFuncSetAttribute(k_indexer_prefill<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(k_indexer_prefill<true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         err_of[dev] = r;
     });
@@ -520,12 +559,18 @@ cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, floa
                               (uint32_t)std::min(b.page_size, kKeys));
     if (e != cudaSuccess)
         return e;
-    const int nb = (b.n_q + kRows - 1) / kRows;
+    const bool q8 = ix.q_dtype == SI_E4M3;
+    const int rows = q8 ? rows_per_block<true>() : rows_per_block<false>();
+    const int nb = (b.n_q + rows - 1) / rows;
     const int64_t npairs = (nb + 1) / 2;
     const int64_t grid = std::min<int64_t>(npairs, (int64_t)sms_of[dev]);
     count_launch();
-    k_indexer_prefill<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores, ld, nb,
-                                                                   st);
+    if (q8)
+        k_indexer_prefill<true><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
+                                                                             ld, nb, st);
+    else
+        k_indexer_prefill<false><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
+                                                                              ld, nb, st);
     return cudaGetLastError();
 }
 

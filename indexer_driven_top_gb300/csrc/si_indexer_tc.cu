@@ -22,6 +22,9 @@
 // lane.  Each epilogue thread then reduces its own key:
 //     k_scale * sum_h (w_h * s_h) * ReLU(D[h] + D[64 + h])
 // (s_h > 0 is a power of two, so folding it into the weight is exact).
+// A query already stored in FP8 with a per-(row, head) scale (section 4.3's
+// per-group quantisation, one group per head) needs no split: its codes are
+// q_hi, q_lo is zero and the scale multiplies the head weight.
 //
 // One persistent CTA per SM runs a warp-specialised pipeline:
 //   2 producer warps -- per tile, TMA tensor copies of its key pages (128-byte
@@ -309,6 +312,27 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
             const int ri = r - r_first, p = ri & 1;
             if (ri >= 2 && !mbar_wait(qempty_bar + p, (uint32_t)((ri - 2) >> 1) & 1, st))
                 break;
+            const uint32_t qb = base + kOffQ + p * kTileB;
+            if (ix.q_dtype == SI_E4M3) {
+                // Stored FP8 query: its codes are the B operand (q_lo = 0) and
+                // the per-(row, head) scale joins the head weight.
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    static_cast<const uint8_t *>(ix.q) + ((int64_t)r * kHeads + h) * kDim +
+                    half * 64);
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const uint4 v = __ldg(src + c);
+                    const uint32_t u = (uint32_t)(half * 4 + c);
+                    st_shared_v4(qb + sw128_offset(h, u), v.x, v.y, v.z, v.w);
+                    st_shared_v4(qb + sw128_offset(kHeads + h, u), 0u, 0u, 0u, 0u);
+                }
+                if (half == 0)
+                    w_s[p * kHeads + h] = __ldg(ix.w + (int64_t)r * kHeads + h) *
+                                          __ldg(ix.q_scale + (int64_t)r * kHeads + h);
+                fence_async_smem();
+                mbar_arrive(qfull_bar + p);
+                continue;
+            }
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 static_cast<const uint16_t *>(ix.q) + ((int64_t)r * kHeads + h) * kDim + half * 64);
             uint32_t q2[32];  // 64 bf16 dims, two per word
@@ -336,7 +360,6 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                 while (ldexpf(amax, -(e - 1)) <= 448.f)
                     e--;
             }
-            const uint32_t qb = base + kOffQ + p * kTileB;
 #pragma unroll
             for (int c = 0; c < 4; c++) {  // 16 dims per 16-byte unit
                 uint32_t hi[4], lo[4];
@@ -456,7 +479,8 @@ bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld)
     // whole pages are copied as tensor boxes: rows packed (stride 128 bytes),
     // page size a power of two >= 8, physical row indices within int32
     const bool pow2_page = b.page_size >= 8 && (b.page_size & (b.page_size - 1)) == 0;
-    return pow2_page && ix.q_dtype == SI_BF16 && ix.k.dtype == SI_E4M3 && ix.n_heads == kHeads &&
+    const bool q_ok = ix.q_dtype == SI_BF16 || (ix.q_dtype == SI_E4M3 && ix.q_scale);
+    return pow2_page && q_ok && ix.k.dtype == SI_E4M3 && ix.n_heads == kHeads &&
            ix.head_dim == kDim && ix.k.row_stride == kDim &&
            (int64_t)b.n_blocks * b.page_size < (int64_t)INT32_MAX &&
            ((uintptr_t)ix.q % 16) == 0 && ((uintptr_t)ix.k.data % 16) == 0 &&

@@ -59,7 +59,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB_PATH)
             P, I32, I64, D = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
-            lib.oracle_indexer_scores.argtypes = [P, P, I32, I32, I32, P, ctypes.c_int, P, P,
+            lib.oracle_indexer_scores.argtypes = [P, P, I32, I32, I32, P, ctypes.c_int, P, P, P,
                                                   ctypes.c_int, P, I64, P, I64, ctypes.c_int]
             lib.oracle_topk.argtypes = [P, P, I32, P, I64, I32, P, P, ctypes.c_int]
             lib.oracle_sparse_attn.argtypes = [P, P, I32, I32, I32, I32, P, ctypes.c_int, P, P,
@@ -123,15 +123,19 @@ def bf16_to_f64(bits: int) -> float:
 
 
 def indexer_scores(b: Batch, q_idx, q_type: str, w, k, k_type: str, k_scale, Hi: int, Di: int,
-                   ld: int, rows: Optional[Sequence[int]] = None, threads: Optional[int] = None):
+                   ld: int, rows: Optional[Sequence[int]] = None, threads: Optional[int] = None,
+                   q_scale=None):
     """score[i, s] = sum_h w[r,h] * ReLU(q_idx[r,h,:] . k[s,:]) for s <= pos(r),
-    -inf beyond; r = rows[i].  Keys are dequantised as code * k_scale[row]."""
+    -inf beyond; r = rows[i].  Keys are dequantised as code * k_scale[row];
+    with ``q_scale`` [n_q, Hi] the query too, as code * q_scale[r, h]."""
     lib = _load()
     rr, n = _rows(rows, b.s.n_q)
     q_idx, w, k, k_scale = _c(q_idx), _c(w, np.float32), _c(k), _c(k_scale, np.float32)
+    q_scale = None if q_scale is None else _c(q_scale, np.float32)
     out = np.empty((n, ld), dtype=np.float64)
     lib.oracle_indexer_scores(ctypes.byref(b.s), _ptr(rr), n, Hi, Di, _ptr(q_idx),
-                              TYPE_CODE[q_type], _ptr(w), _ptr(k), TYPE_CODE[k_type],
+                              TYPE_CODE[q_type], _ptr(q_scale), _ptr(w), _ptr(k),
+                              TYPE_CODE[k_type],
                               _ptr(k_scale), k.shape[-1], _ptr(out), ld,
                               threads or default_threads())
     return out
@@ -178,7 +182,8 @@ def run(wl, rows: Optional[Sequence[int]] = None, threads: Optional[int] = None)
     b = Batch.of(wl)
     ld = wl.max_ctx
     sc = indexer_scores(b, wl.q_idx, wl.q_idx_dtype, wl.w, wl.k_idx, wl.k_idx_dtype, wl.k_scale,
-                        wl.Hi, wl.Di, ld, rows=rows, threads=threads)
+                        wl.Hi, wl.Di, ld, rows=rows, threads=threads,
+                        q_scale=getattr(wl, "q_scale", None))
     idx, kth = topk(b, sc, wl.K, rows=rows, threads=threads, return_kth=True)
     out, lse = sparse_attn(b, wl.q, wl.kv_dtype, wl.k, wl.v, wl.kv_dtype, idx, wl.K, wl.Hq,
                            wl.Dqk, wl.Dv, wl.scale, rows=rows, threads=threads)

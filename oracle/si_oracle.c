@@ -132,6 +132,7 @@ typedef struct {
     const int32_t *rows; /* which query rows (NULL = 0..n_rows-1) */
     int32_t Hi, Di;
     const void *q_idx; int q_type;      /* [n_q, Hi, Di] */
+    const float *q_scale;               /* [n_q, Hi] or NULL: q = code * q_scale */
     const float *w;                     /* [n_q, Hi] */
     const void *k; int k_type;          /* paged [n_blocks, page, k_stride] */
     const float *k_scale;               /* [n_blocks, page] or NULL */
@@ -156,9 +157,10 @@ static void idx_row(void *p, int64_t i)
         double kscale = c->k_scale ? (double)c->k_scale[row] : 1.0;
         double score = 0.0;
         for (int32_t h = 0; h < c->Hi; h++) {
+            double qscale = c->q_scale ? (double)c->q_scale[(int64_t)r * c->Hi + h] : 1.0;
             double dot = 0.0;
             for (int32_t d = 0; d < c->Di; d++) {
-                double qv = elem(c->q_idx, c->q_type, ((int64_t)r * c->Hi + h) * c->Di + d);
+                double qv = elem(c->q_idx, c->q_type, ((int64_t)r * c->Hi + h) * c->Di + d) * qscale;
                 double kv = elem(c->k, c->k_type, row * c->k_stride + d) * kscale;
                 dot += qv * kv;
             }
@@ -171,10 +173,12 @@ static void idx_row(void *p, int64_t i)
 
 void oracle_indexer_scores(const orc_batch *b, const int32_t *rows, int32_t n_rows,
                            int32_t Hi, int32_t Di, const void *q_idx, int q_type,
-                           const float *w, const void *k, int k_type, const float *k_scale,
-                           int64_t k_stride, double *scores, int64_t ld, int nthreads)
+                           const float *q_scale, const float *w, const void *k, int k_type,
+                           const float *k_scale, int64_t k_stride, double *scores, int64_t ld,
+                           int nthreads)
 {
-    idx_ctx c = { b, rows, Hi, Di, q_idx, q_type, w, k, k_type, k_scale, k_stride, scores, ld };
+    idx_ctx c = { b, rows, Hi, Di, q_idx, q_type, q_scale, w, k, k_type, k_scale, k_stride,
+                  scores, ld };
     orc_parallel(idx_row, &c, n_rows, nthreads);
 }
 

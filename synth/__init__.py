@@ -19,6 +19,10 @@ Workload shapes follow the five synthetic configurations of the hot path:
   c4  ragged batch of 32 requests with log-uniform contexts in [1024, 65536]:
       28 single-token decodes and 4 chunks of 2048 prefill rows.
 
+Option ``q_idx_fp8=True`` (any config) stores the indexer query quantised the
+way the key cache is: e4m3 codes with one fp32 scale per (row, head), scale =
+max|q_h| / 448, drawn from the same q_idx values.
+
 Draw order (per config): context lengths (c4 only) -> physical block
 permutation -> q_idx -> w -> indexer keys (sequence by sequence, logical
 order) -> planted positions and offsets (c3) -> attention q -> K/V rows
@@ -86,7 +90,7 @@ class Workload:
     ctx_len: np.ndarray          # int32 [n_seq]
     q_seq: np.ndarray            # int32 [n_q]
     q_pos: np.ndarray            # int32 [n_q]
-    q_idx: np.ndarray            # f32 or bf16 bits [n_q, Hi, Di]
+    q_idx: np.ndarray            # f32, bf16 bits or e4m3 codes [n_q, Hi, Di]
     q_idx_dtype: str
     w: np.ndarray                # f32 [n_q, Hi]
     k_idx: np.ndarray            # f32 or e4m3 codes [n_blocks, page, Di]
@@ -97,6 +101,7 @@ class Workload:
     k: np.ndarray                # [n_blocks, page, Dqk] (row stride = last dim)
     v: Optional[np.ndarray]      # [n_blocks, page, Dv]; None = V is the first Dv cols of k
     planted: Optional[list] = None  # c3: per-sequence arrays of planted positions
+    q_scale: Optional[np.ndarray] = None  # f32 [n_q, Hi] when q_idx holds e4m3 codes
 
     @property
     def n_q(self) -> int:
@@ -244,9 +249,17 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
 
     fp32 = cfg["dtype"] == F32
 
-    # 3. indexer queries and head weights
+    # 3. indexer queries and head weights; with q_idx_fp8 the query is
+    # stored as e4m3 codes with one fp32 scale per (row, head)
     qi = _normal(rng, (n_q, Hi, Di), cfg["q_idx_std"])
-    q_idx = qi if fp32 else f32_to_bf16_bits(qi)
+    q8 = bool(cfg.get("q_idx_fp8", False))
+    q_scale = None
+    if q8:
+        q_idx, q_scale = quantize_rows_e4m3(qi)
+        q_idx_dtype = E4M3
+    else:
+        q_idx = qi if fp32 else f32_to_bf16_bits(qi)
+        q_idx_dtype = F32 if fp32 else BF16
     w = (rng.random(size=(n_q, Hi), dtype=np.float32) * np.float32(cfg["w_scale"])).astype(np.float32)
 
     # 4. indexer keys, logical order, sequence by sequence
@@ -268,7 +281,8 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
             n_pl = int(round(cfg["planted"] * c))
             pos = np.sort(rng.choice(c, size=n_pl, replace=False)).astype(np.int32)
             rows = np.nonzero(q_seq == i)[0]
-            qmat = (qi[rows[-1]] if fp32 else _bf16_bits_to_f32(q_idx[rows[-1]])).astype(np.float64)
+            qmat = (qi[rows[-1]] if (fp32 or q8) else _bf16_bits_to_f32(q_idx[rows[-1]]))
+            qmat = qmat.astype(np.float64)
             target = 3.0 * np.linalg.norm(qmat, axis=1)
             delta = qmat.T @ np.linalg.solve(qmat @ qmat.T, target)   # min-norm solution
             raw_keys[i][pos] += delta.astype(np.float32)
@@ -317,9 +331,9 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
     return Workload(
         name=name, Hi=Hi, Di=Di, Hq=Hq, Dqk=Dqk, Dv=Dv, K=int(cfg["K"]), page=page,
         scale=float(cfg["scale"]), block_table=bt, ctx_len=ctx_len, q_seq=q_seq,
-        q_pos=q_pos, q_idx=q_idx, q_idx_dtype=F32 if fp32 else BF16, w=w,
+        q_pos=q_pos, q_idx=q_idx, q_idx_dtype=q_idx_dtype, w=w,
         k_idx=k_idx, k_idx_dtype=F32 if fp32 else E4M3, k_scale=k_scale, q=q,
-        kv_dtype=F32 if fp32 else BF16, k=k, v=v, planted=planted)
+        kv_dtype=F32 if fp32 else BF16, k=k, v=v, planted=planted, q_scale=q_scale)
 
 
 def _bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(si):
 
 def test_version_and_status_strings(si):
     lib = si.load()
-    assert lib.si_version() == 1
+    assert lib.si_version() == 2
     assert lib.si_status_string(0) == b"ok"
     assert lib.si_status_string(3) == b"workspace error"
 
@@ -80,9 +80,15 @@ def test_host_validation_rejects_bad_arguments(si):
     assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
                               4096, None) == 1
     # indexer: misaligned key cache, bad head count
-    ix = si.c_indexer(fake, si.BF16, fake, 64, 128, si.c_paged(fake + 3, None, si.E4M3, 128, 128))
+    kp8 = si.c_paged(fake, None, si.E4M3, 128, 128)
+    ix = si.c_indexer(fake, si.BF16, None, fake, 64, 128,
+                      si.c_paged(fake + 3, None, si.E4M3, 128, 128))
     assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 1
-    ix = si.c_indexer(fake, si.BF16, fake, 0, 128, si.c_paged(fake, None, si.E4M3, 128, 128))
+    # an FP8 query without its scale
+    ix = si.c_indexer(fake, si.E4M3, None, fake, 64, 128, kp8)
+    assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 1
+    assert b"q_scale" in lib.si_last_error()
+    ix = si.c_indexer(fake, si.BF16, None, fake, 0, 128, si.c_paged(fake, None, si.E4M3, 128, 128))
     assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 1
     # empty batch is a no-op that succeeds without touching anything
     assert lib.si_topk(ctypes.byref(_batch(si, n_q=0)), None, 0, 8, None, None, 0, None) == 0

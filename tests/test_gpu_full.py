@@ -106,3 +106,10 @@ def test_causal_prefill_full_size(si):
     wl = synth.make("c2")
     assert wl.n_q == 16384
     _run(si, wl, rows=[0, 100, 2047, 2048, 9000, 16383])
+
+
+def test_causal_prefill_full_size_fp8_query(si):
+    """The same prefill with the indexer query stored in FP8 (per-(row, head)
+    scale): the four-row prefill blocks at full size."""
+    wl = synth.make("c2", q_idx_fp8=True)
+    _run(si, wl, rows=[0, 3, 4, 2047, 2048, 9001, 16383])

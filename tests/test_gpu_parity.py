@@ -94,6 +94,34 @@ def test_prefill_chunk_small(si):
     _full_check(si, wl, ATOL_BF16)
 
 
+def test_fp8_query_decode_tensor_core(si):
+    """FP8 indexer query with a per-(row, head) scale on the 64 x 128
+    tensor-core decode indexer."""
+    wl = synth.make("c1", batch=3, ctx_list=[3001, 2048, 130], K=2048, q_idx_fp8=True)
+    _full_check(si, wl, ATOL_BF16)
+
+
+def test_fp8_query_prefill_ragged_block(si):
+    """Prefill indexer with an FP8 query: blocks of four rows, the last one
+    holding a single row."""
+    wl = synth.make("c2", L=701, K=64, q_idx_fp8=True)
+    _full_check(si, wl, ATOL_BF16)
+
+
+def test_fp8_query_generic_shapes(si):
+    """FP8 query on indexer shapes the tensor-core kernels do not take."""
+    wl = synth.make("c4", n_req=5, n_prefill=1, chunk=40, ctx_lo=100, ctx_hi=1500, K=128,
+                    Hi=4, Di=32, q_idx_fp8=True)
+    _full_check(si, wl, ATOL_BF16)
+
+
+def test_bf16_query_prefill_ragged_block(si):
+    """Prefill indexer with a bf16 query: blocks of two rows, the last one
+    holding a single row."""
+    wl = synth.make("c2", L=301, K=64)
+    _full_check(si, wl, ATOL_BF16)
+
+
 def test_mixed_ragged_batch(si):
     wl = synth.make("c4", n_req=5, n_prefill=1, chunk=40, ctx_lo=100, ctx_hi=1500, K=128)
     _full_check(si, wl, ATOL_BF16)
@@ -177,7 +205,8 @@ def _scores_check(si, wl, wl_ref=None):
     g = sc.cpu().numpy()
     r = wl_ref or wl
     o = oracle.indexer_scores(oracle.Batch.of(r), r.q_idx, r.q_idx_dtype, r.w, r.k_idx,
-                              r.k_idx_dtype, r.k_scale, r.Hi, r.Di, r.max_ctx)
+                              r.k_idx_dtype, r.k_scale, r.Hi, r.Di, r.max_ctx,
+                              q_scale=r.q_scale)
     return g, o, flags
 
 

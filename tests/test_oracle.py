@@ -249,6 +249,45 @@ def test_per_token_scale_and_fp8_dequantisation():
     assert np.allclose(sc, sc2, rtol=1e-6, atol=1e-9)
 
 
+def _e4m3_by_definition(codes):
+    """OCP e4m3 decode written out from the format: sign, 4 exponent bits
+    (bias 7), 3 mantissa bits; exponent field 0 is subnormal (m / 8 * 2^-6)."""
+    c = codes.astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, c & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return sign * val
+
+
+def test_fp8_query_with_per_head_scale_brute_force():
+    """FP8 query codes with one scale per (row, head) (the query quantisation
+    of the indexer prolog): the oracle's score equals the definition evaluated
+    by brute force on the dequantised query and keys, both decoded here from
+    the format's definition."""
+    wl = synth.make("c1", batch=2, ctx_list=[37, 20], Hi=3, Di=16, Hq=2, Dqk=8, Dv=4, K=5,
+                    q_idx_fp8=True)
+    assert wl.q_idx_dtype == "e4m3" and wl.q_scale.shape == (2, 3)
+    b = oracle.Batch.of(wl)
+    sc = oracle.indexer_scores(b, wl.q_idx, "e4m3", wl.w, wl.k_idx, "e4m3", wl.k_scale, wl.Hi,
+                               wl.Di, wl.max_ctx, q_scale=wl.q_scale)
+    q = _e4m3_by_definition(wl.q_idx) * wl.q_scale.astype(np.float64)[..., None]
+    kd = _e4m3_by_definition(wl.k_idx) * wl.k_scale.astype(np.float64)[..., None]
+    for r in range(wl.n_q):
+        seq, pos = wl.q_seq[r], wl.q_pos[r]
+        for s_ in range(wl.max_ctx):
+            if s_ > pos:
+                assert np.isneginf(sc[r, s_])
+                continue
+            krow = kd[wl.block_table[seq, s_ // wl.page], s_ % wl.page]
+            ref = sum(float(wl.w[r, h]) * max(0.0, float(q[r, h] @ krow)) for h in range(wl.Hi))
+            assert abs(sc[r, s_] - ref) <= 1e-12 * (abs(ref) + 1e-30)
+    # dropping the scale (a plausible slip) changes the scores
+    sc_noscale = oracle.indexer_scores(b, wl.q_idx, "e4m3", wl.w, wl.k_idx, "e4m3", wl.k_scale,
+                                       wl.Hi, wl.Di, wl.max_ctx)
+    fin = np.isfinite(sc)
+    assert not np.allclose(sc[fin], sc_noscale[fin])
+
+
 # ---------------------------------------------------------------- invariants
 
 def test_page_placement_does_not_change_results():

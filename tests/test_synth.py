@@ -52,3 +52,20 @@ def test_planted_keys_raise_every_head_by_three_sigma():
         k = deq.reshape(-1, wl.Di)[rows] * wl.k_scale.reshape(-1)[rows, None]
         z = (k @ q.T) / np.linalg.norm(q, axis=1)      # per-head logit in units of sigma
         assert z.mean() > 2.0                          # 3 sigma shift + N(0,1) noise
+
+
+def test_fp8_query_quantisation():
+    """q_idx_fp8 stores the same query draw as e4m3 codes with scale
+    max|q_h| / 448 per (row, head): every head's largest code is 448 and the
+    dequantised query is within e4m3's half-step of the bf16 one."""
+    a = synth.make("c1", batch=3, ctx=100, Hi=4, Di=32, Hq=2, Dqk=8, Dv=4, K=8)
+    b = synth.make("c1", batch=3, ctx=100, Hi=4, Di=32, Hq=2, Dqk=8, Dv=4, K=8, q_idx_fp8=True)
+    assert b.q_idx.dtype == np.uint8 and b.q_scale.dtype == np.float32
+    codes = torch.from_numpy(b.q_idx).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.all(np.abs(codes).max(axis=-1) == 448.0)
+    deq = codes * b.q_scale[..., None]
+    qa = synth._bf16_bits_to_f32(a.q_idx).astype(np.float64)
+    amax = np.abs(qa).max(axis=-1, keepdims=True)
+    assert np.all(np.abs(deq - qa) <= amax / 448 * 16 + amax * 2.0 ** -8)
+    # the rest of the workload is unchanged
+    assert np.array_equal(a.k_idx, b.k_idx) and np.array_equal(a.q, b.q)

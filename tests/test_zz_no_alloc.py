@@ -36,7 +36,7 @@ def test_oversize_request_is_refused_on_the_host(si):
     blocks = (max_ctx + page - 1) // page
     b = si.c_batch(fake, fake, fake, fake, 1, blocks, 1, page, max_ctx, blocks)
     kp = si.c_paged(fake, None, si.E4M3, 128, 128)
-    ix = si.c_indexer(fake, si.BF16, fake, 64, 128, kp)
+    ix = si.c_indexer(fake, si.BF16, None, fake, 64, 128, kp)
     ap = si.c_paged(fake, None, si.BF16, 576, 576)
     at = si.c_attention(fake, si.BF16, 128, 576, 512, ap, ap, 0.04)
     scratch = ctypes.c_void_p(123)
