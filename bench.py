@@ -447,7 +447,16 @@ def main():
     ap.add_argument("--workload", default="c1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prefill indexer (both query formats) and print its record")
     args = ap.parse_args()
+    if args.prefill_only:
+        import torch
+        import indexer_driven_top_gb300 as si
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"prefill_indexer": prefill_indexer(si, dev, args.steps)}), flush=True)
+        return
     if args.impl == "reference":
         world, rank, _ = _dist()
         if rank == 0:

@@ -203,8 +203,10 @@ si_status run_topk(const si_batch &b, const float *scores, int64_t ld, int k_top
 si_status run_attn(const si_batch &b, const si_attention &at, const int32_t *idx, int k_top,
                    void *out, si_dtype odt, float *lse, unsigned int *st, cudaStream_t s)
 {
-    cudaError_t e = si::attn_tc_supported(b, at, k_top)
-                        ? si::launch_attn_tc(b, at, idx, k_top, out, odt, lse, st, s)
+    // the tensor-core kernel stores its output with the tensor engine, which
+    // needs a 16-byte aligned destination
+    const bool tc = si::attn_tc_supported(b, at, k_top) && ((uintptr_t)out % 16) == 0;
+    cudaError_t e = tc ? si::launch_attn_tc(b, at, idx, k_top, out, odt, lse, st, s)
                         : si::launch_attn_generic(b, at, idx, k_top, out, odt, lse, st, s);
     return e == cudaSuccess ? SI_OK : cuda_fail(e, "attention launch");
 }

@@ -54,6 +54,7 @@
 #include "si_common.cuh"
 #include "si_internal.h"
 #include "si_sm100.cuh"
+#include "si_tmap.h"
 
 namespace si {
 
@@ -95,6 +96,8 @@ constexpr int kRingV = 5;
 constexpr uint32_t kOffP = 0;                                  // kPBufs x (2 x [128 heads x 64 keys])
 constexpr uint32_t kOffRingV = kPBufs * 2 * kChunk;            // kRingV x (2 x [128 keys x 64 dims])
 constexpr uint32_t kOffF = kOffRingV + kRingV * kGroup;        // kPBufs x 128 floats
+constexpr int kEpiBufs = 4;  // epilogue staging: 4 KB boxes per epilogue warp, in the value ring
+static_assert(8 * kEpiBufs * 4096 <= kRingV * kGroup, "epilogue staging fits the value ring");
 // both
 constexpr uint32_t kOffBar = std::max(kOffF + kPBufs * kHeads * 4, kOffMask + kRowSlots * 16);
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;          // + alignment slack
@@ -271,8 +274,9 @@ __device__ __forceinline__ void issue_chunk(const LoaderState &ls, uint32_t dst,
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
-          si_dtype out_dtype, float *lse, unsigned int *st)
+k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+          si_batch b, si_attention at, const int32_t *idx, int k_top, si_dtype out_dtype,
+          float *lse, unsigned int *st)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -306,7 +310,7 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
             mbar_init(bars + B_MASK + i, 32);
             mbar_init(bars + B_MEMPTY + i, kSoftmax + kLoaders);
         }
-        mbar_init(bars + B_QREADY, kLoaders);
+        mbar_init(bars + B_QREADY, 1);
         mbar_init(bars + B_OCORR, kHeads);
         mbar_init(bars + B_PVDONE, 1);
         mbar_init(bars + B_FINAL, kHeads);
@@ -336,19 +340,12 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
         const int u = tid & 7, kr0 = tid >> 3;
         LoaderState ls;
         if (score_cta) {
-            {
-                // query: 128 heads x 9 chunks x 8 units, SW128 K-major per chunk
-                const uint4 *qsrc =
-                    reinterpret_cast<const uint4 *>(at.q) + (int64_t)r * kHeads * (kDqk / 8);
-                for (int i = tid; i < kHeads * kQChunks * 8; i += kLoaders) {
-                    const int h = i / (kQChunks * 8), rem = i % (kQChunks * 8);
-                    const int c = rem >> 3, uu = rem & 7;
-                    const uint4 v = __ldg(qsrc + (int64_t)h * (kDqk / 8) + rem);
-                    st_shared_v4(base + kOffQ + c * kChunk + sw128_offset(h, uu), v.x, v.y, v.z,
-                                 v.w);
-                }
-                fence_async_smem();
-                mbar_arrive(bars + B_QREADY);
+            if (tid == 0) {
+                // query: nine tensor copies of [128 heads x 64 dims], SW128 K-major
+                mbar_arrive_expect_tx(bars + B_QREADY, kQChunks * kChunk);
+                for (int c = 0; c < kQChunks; c++)
+                    tma_load_2d(base + kOffQ + c * kChunk, &qmap, c * 128, r * kHeads,
+                                bars + B_QREADY);
             }
             // physical rows come from the row table the row warp fills
             const int *rows = reinterpret_cast<const int *>(gbase + kOffRows);
@@ -656,98 +653,140 @@ k_attn_tc(si_batch b, si_attention at, const int32_t *idx, int k_top, void *out,
                 mbar_arrive(bars + B_MASK + rs);
             }
         }
-    } else if (warp >= kWarpQuad + 4) {
-        // ----------------------------------------------------------- converters
-        // Value groups feed the f16 P.V product: rewrite them bf16 -> f16 in
-        // place once their copies have landed (warps 12..15 and 17).
-        const int ct = warp < kWarpMma ? tid - (kWarpQuad + 4) * 32 : 4 * 32 + lane;
-        const int n_groups = kVGroups * T;
-        for (int g = 0; g < n_groups; g++) {
-            const int slot = g % kRingV;
-            if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingV) & 1, st))
-                break;
-            const uint32_t src = base + kOffRingV + slot * kGroup;
-            for (int i = ct; i < (int)(kGroup / 16); i += kConverters) {
-                const uint4 x = ld_shared_v4(src + i * 16);
-                st_shared_v4(src + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
-                             bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
-            }
-            fence_async_smem();
-            mbar_arrive(bars + B_CONV + slot);
-        }
     } else {
-        // ------------------------------------------- O rescale and epilogue
-        const int h = tid - kWarpQuad * 32;  // head = TMEM lane
-        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const float *fac = reinterpret_cast<const float *>(gbase + kOffF);
+        // value CTA, warps 8..15 and 17
         bool ok = true;
-        for (int t = 0; t < T; t++) {
-            const int pb = t % kPBufs;
-            if (!mbar_wait_cluster(bars + B_PFULL + pb, (uint32_t)(t / kPBufs) & 1, st)) {
-                ok = false;
-                break;
+        if (warp >= kWarpQuad + 4) {
+            // ------------------------------------------------------- converters
+            // Value groups feed the f16 P.V product: rewrite them bf16 -> f16
+            // in place once their copies have landed (warps 12..15 and 17).
+            const int ct = warp < kWarpMma ? tid - (kWarpQuad + 4) * 32 : 4 * 32 + lane;
+            const int n_groups = kVGroups * T;
+            for (int g = 0; g < n_groups; g++) {
+                const int slot = g % kRingV;
+                if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingV) & 1, st))
+                    break;
+                const uint32_t src = base + kOffRingV + slot * kGroup;
+                for (int i = ct; i < (int)(kGroup / 16); i += kConverters) {
+                    const uint4 x = ld_shared_v4(src + i * 16);
+                    st_shared_v4(src + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
+                                 bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+                }
+                fence_async_smem();
+                mbar_arrive(bars + B_CONV + slot);
             }
-            const float f = fac[pb * kHeads + h];
-            // P.V of tile t - 1 must be complete before O is touched
-            if (t >= 1 && !mbar_wait(bars + B_PVDONE, (uint32_t)(t - 1) & 1, st)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (t >= 1 && f != 1.f) {
+        } else {
+            // ------------------------------------------------------ O rescale
+            const int h = tid - kWarpQuad * 32;  // head = TMEM lane
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            const float *fac = reinterpret_cast<const float *>(gbase + kOffF);
+            for (int t = 0; t < T; t++) {
+                const int pb = t % kPBufs;
+                if (!mbar_wait_cluster(bars + B_PFULL + pb, (uint32_t)(t / kPBufs) & 1, st)) {
+                    ok = false;
+                    break;
+                }
+                const float f = fac[pb * kHeads + h];
+                // P.V of tile t - 1 must be complete before O is touched
+                if (t >= 1 && !mbar_wait(bars + B_PVDONE, (uint32_t)(t - 1) & 1, st)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (t >= 1 && f != 1.f) {
 #pragma unroll 1
-                for (int q = 0; q < kDv / 32; q++) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + q * 32, v);
-                    tmem_wait_ld();
+                    for (int q = 0; q < kDv / 32; q++) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + lane_off + q * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i++)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                        tmem_st32(tmem + lane_off + q * 32, v);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                mbar_arrive(bars + B_OCORR);
+            }
+            if (ok && T >= 1 && !mbar_wait(bars + B_PVDONE, (uint32_t)(T - 1) & 1, st))
+                ok = false;
+            if (!mbar_wait_cluster(bars + B_FINAL, 0, st))
+                ok = false;
+        }
+        if (warp < kWarpMma) {
+            // ------------------------------------------------------- epilogue
+            // Warps 8..15 (two per TMEM lane quarter) write out = O / l: each
+            // warp takes half of its 32 heads' columns, 128-byte column blocks
+            // staged in the (now idle) value ring with the 128-byte swizzle and
+            // stored by the tensor engine as [32 rows x 128 bytes] boxes.  The
+            // bar.red gives every warp the same verdict on the waits above.
+            const bool bad = bar_sync_or(2, 8 * 32, !ok);
+            tc_fence_after();
+            const int quarter = warp & 3, half = (warp - kWarpQuad) >> 2;
+            const int h = quarter * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const float *fac = reinterpret_cast<const float *>(gbase + kOffF);
+            const bool good = !bad && T > 0;
+            const float lsum = fac[(T % kPBufs) * kHeads + h];
+            const float inv = (good && lsum > 0.f) ? 1.f / lsum : 0.f;
+            const uint32_t stage = base + kOffRingV + (uint32_t)(warp - kWarpQuad) * kEpiBufs * 4096u;
+            const int orow = r * kHeads + quarter * 32;
+            const bool f32 = out_dtype == SI_F32;
+            const int nblk = f32 ? 8 : 4;  // 32 fp32 or 64 bf16 columns per block
+#pragma unroll 1
+            for (int k = 0; k < nblk; k++) {
+                const uint32_t buf = stage + (uint32_t)(k % kEpiBufs) * 4096u;
+                if (k >= kEpiBufs) {
+                    if (lane == 0)
+                        bulk_wait_read<kEpiBufs - 1>();  // buffer's previous store has read it
+                    __syncwarp();
+                }
+                uint32_t w[32];
+                int xbyte;
+                if (f32) {
+                    const int col0 = half * (kDv / 2) + k * 32;
+                    if (good) {
+                        tmem_ld32(tmem + lane_off + col0, w);
+                        tmem_wait_ld();
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; i++)
-                        v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                    tmem_st32(tmem + lane_off + q * 32, v);
+                        w[i] = good ? __float_as_uint(__uint_as_float(w[i]) * inv) : 0u;
+                    xbyte = col0 * 4;
+                } else {
+                    const int col0 = half * (kDv / 2) + k * 64;
+#pragma unroll
+                    for (int hh = 0; hh < 2; hh++) {
+                        uint32_t v[32];
+                        if (good) {
+                            tmem_ld32(tmem + lane_off + col0 + 32 * hh, v);
+                            tmem_wait_ld();
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; i++)
+                            w[16 * hh + i] =
+                                good ? pack_bf16x2(__uint_as_float(v[2 * i]) * inv,
+                                                   __uint_as_float(v[2 * i + 1]) * inv)
+                                     : 0u;
+                    }
+                    xbyte = col0 * 2;
                 }
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            mbar_arrive(bars + B_OCORR);
-        }
-        if (ok && T >= 1 && !mbar_wait(bars + B_PVDONE, (uint32_t)(T - 1) & 1, st))
-            ok = false;
-        if (!mbar_wait_cluster(bars + B_FINAL, 0, st))
-            ok = false;
-        tc_fence_after();
-        const float lsum = fac[(T % kPBufs) * kHeads + h];
-        const float inv = (ok && lsum > 0.f) ? 1.f / lsum : 0.f;
-        const int64_t obase = ((int64_t)r * kHeads + h) * kDv;
-#pragma unroll 1
-        for (int q = 0; q < kDv / 32; q++) {
-            uint32_t v[32];
-            if (ok && T > 0) {
-                tmem_ld32(tmem + lane_off + q * 32, v);
-                tmem_wait_ld();
-            } else {
 #pragma unroll
-                for (int i = 0; i < 32; i++)
-                    v[i] = 0;
+                for (int u = 0; u < 8; u++)
+                    st_shared_v4(buf + sw128_offset(lane, u), w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                 w[4 * u + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&omap, xbyte, orow, buf);
+                    bulk_commit();
+                }
+                __syncwarp();
             }
-            if (out_dtype == SI_F32) {
-                float4 *o4 = reinterpret_cast<float4 *>(static_cast<float *>(out) + obase + q * 32);
-#pragma unroll
-                for (int i = 0; i < 8; i++)
-                    o4[i] = make_float4(__uint_as_float(v[4 * i]) * inv,
-                                        __uint_as_float(v[4 * i + 1]) * inv,
-                                        __uint_as_float(v[4 * i + 2]) * inv,
-                                        __uint_as_float(v[4 * i + 3]) * inv);
-            } else {
-                uint4 *o4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(out) + obase +
-                                                      q * 32);
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    o4[i] = make_uint4(
-                        pack_bf16x2(__uint_as_float(v[8 * i]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
-                        pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
-                        pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
-                        pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
-            }
+            if (lane == 0)
+                bulk_wait<0>();
+            __syncwarp();
         }
     }
 
@@ -791,8 +830,21 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
     });
     if (err_of[dev] != cudaSuccess)
         return err_of[dev];
+    if (b.n_q <= 0)
+        return cudaSuccess;
+    // q [n_q * 128 rows x 1152 bytes] read as [128 x 128-byte] boxes; out
+    // [n_q * 128 rows x 512 elements] written as [32 x 128-byte] boxes
+    CUtensorMap qmap, omap;
+    const uint64_t rows = (uint64_t)b.n_q * kHeads;
+    e = make_tmap_2d_u8_sw128(&qmap, at.q, kDqk * 2, rows, kDqk * 2, 128, kHeads);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t orow_bytes = (uint64_t)kDv * (out_dtype == SI_F32 ? 4 : 2);
+    e = make_tmap_2d_u8_sw128(&omap, out, orow_bytes, rows, orow_bytes, 128, 32);
+    if (e != cudaSuccess)
+        return e;
     count_launch();
-    k_attn_tc<<<(unsigned)(2 * b.n_q), kThreads, kSmemBytes, s>>>(b, at, idx, k_top, out,
+    k_attn_tc<<<(unsigned)(2 * b.n_q), kThreads, kSmemBytes, s>>>(qmap, omap, b, at, idx, k_top,
                                                                   out_dtype, lse, st);
     return cudaGetLastError();
 }
