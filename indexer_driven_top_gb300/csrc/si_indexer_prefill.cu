@@ -470,33 +470,53 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                 tc_fence_after();
                 const int s = t * kKeys + et;
                 const uint32_t acc = tmem + g * kN + lane_off;
+                // The accumulator is read in 32-register pieces (an FP8 query:
+                // 32 heads of one row; a bf16 query: 16 heads' q_hi and q_lo
+                // columns), each piece's load issued before the previous
+                // piece is reduced.
+                constexpr int kPH = Q8 ? 32 : 16;          // heads per piece
+                constexpr int kPPR = kHeads / kPH;         // pieces per row
+                constexpr int kPieces = kRows * kPPR;
+                auto issue = [&](int pc, uint32_t(&v)[32]) {
+                    const uint32_t col = (uint32_t)((pc / kPPR) * kRowN + (pc % kPPR) * kPH);
+                    if constexpr (Q8) {
+                        tmem_ld32(acc + col, v);
+                    } else {
+                        tmem_ld16(acc + col, v);
+                        tmem_ld16(acc + col + kHeads, v + 16);
+                    }
+                };
                 float sum[kRows];
+                float part[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t va[32], vb[32];
+                issue(0, va);
 #pragma unroll
-                for (int j = 0; j < kRows; j++) {
+                for (int pc = 0; pc < kPieces; pc++) {
+                    uint32_t(&cur)[32] = (pc & 1) ? vb : va;
+                    uint32_t(&nxt)[32] = (pc & 1) ? va : vb;
+                    tmem_wait_ld();
+                    tmem_regs_ready(cur);
+                    if (pc + 1 < kPieces)
+                        issue(pc + 1, nxt);
+                    const int j = pc / kPPR, hq = pc % kPPR;
                     const float4 *w4 =
-                        reinterpret_cast<const float4 *>(w_s + (p * kRows + j) * kHeads);
-                    float part[4] = {0.f, 0.f, 0.f, 0.f};
+                        reinterpret_cast<const float4 *>(w_s + (p * kRows + j) * kHeads + hq * kPH);
 #pragma unroll
-                    for (int hh = 0; hh < 2; hh++) {  // heads [32 hh, 32 hh + 32)
-                        uint32_t vh[32], vl[32];
-                        tmem_ld32(acc + j * kRowN + hh * 32, vh);
-                        if constexpr (!Q8)
-                            tmem_ld32(acc + j * kRowN + kHeads + hh * 32, vl);
-                        tmem_wait_ld();
+                    for (int i = 0; i < kPH; i += 4) {
+                        const float4 wv = w4[i >> 2];
+                        const float wq[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 wv = w4[(hh * 32 + i) >> 2];
-                            const float wq[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                            for (int k = 0; k < 4; k++) {
-                                float lg = __uint_as_float(vh[i + k]);
-                                if constexpr (!Q8)
-                                    lg += __uint_as_float(vl[i + k]);
-                                part[k] = fmaf(wq[k], fmaxf(lg, 0.f), part[k]);
-                            }
+                        for (int k = 0; k < 4; k++) {
+                            float lg = __uint_as_float(cur[i + k]);
+                            if constexpr (!Q8)
+                                lg += __uint_as_float(cur[16 + i + k]);
+                            part[k] = fmaf(wq[k], fmaxf(lg, 0.f), part[k]);
                         }
                     }
-                    sum[j] = (part[0] + part[1]) + (part[2] + part[3]);
+                    if (hq == kPPR - 1) {
+                        sum[j] = (part[0] + part[1]) + (part[2] + part[3]);
+                        part[0] = part[1] = part[2] = part[3] = 0.f;
+                    }
                 }
                 tc_fence_before();
                 mbar_arrive(cempty_bar + g);

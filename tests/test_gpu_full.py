@@ -83,6 +83,42 @@ def test_benchmark_workload_full_size_sampled_rows(si):
     _run(si, wl, rows=[0, 31, 63])
 
 
+def _bf16_step(x):
+    """Spacing of bfloat16 numbers (8 significant bits) around |x|."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def test_benchmark_workload_bf16_output(si):
+    """The benchmarked decode step writes its output in bf16, the activation
+    type the output projection consumes.  Bound: the fp32-output tolerance
+    plus half a bf16 step of the exact value (the final rounding)."""
+    wl = synth.make("c1")
+    dw = si.upload(wl)
+    b = dw.batch
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, dw.indexer, dw.attention, dw.k_top))
+    scores = torch.empty((dw.n_q, b.max_ctx), dtype=torch.float32, device="cuda")
+    idx = torch.empty((dw.n_q, dw.k_top), dtype=torch.int32, device="cuda")
+    out = torch.empty((dw.n_q, wl.Hq, wl.Dv), dtype=torch.bfloat16, device="cuda")
+    si.indexer_scores(b, dw.indexer, scores, ws)
+    si.topk(b, scores, dw.k_top, idx, ws)
+    si.sparse_attn(b, dw.attention, idx, dw.k_top, out, ws)
+    assert si.workspace_status(ws) == 0
+    rows = [0, 40, 63]
+    g_idx = idx.cpu().numpy()
+    g_out = out.float().cpu().numpy()
+    ref, _ = oracle.sparse_attn(oracle.Batch.of(wl), wl.q, wl.kv_dtype, wl.k, wl.v, wl.kv_dtype,
+                                g_idx[rows], wl.K, wl.Hq, wl.Dqk, wl.Dv, wl.scale, rows=rows)
+    err = np.abs(g_out[rows] - ref)
+    assert (err <= ATOL_BF16 + 0.5 * _bf16_step(ref)).all(), float(err.max())
+    # the fused call writes the same bf16 values
+    f_idx = torch.empty_like(idx)
+    f_out = torch.empty_like(out)
+    si.fused_decode(b, dw.indexer, dw.attention, dw.k_top, f_idx, f_out, ws)
+    assert si.workspace_status(ws) == 0
+    assert torch.equal(f_idx, idx) and torch.equal(f_out, out)
+
+
 def test_long_context_planted_full_size(si):
     """Batch 16 x context 131072 with 1 % planted keys; Top-K over 131072
     scores takes the streaming path."""
