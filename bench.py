@@ -127,6 +127,31 @@ def _dist():
     return world, rank, local
 
 
+def rank_seed(workload: str, rank: int) -> int:
+    """Each rank runs its own independent batch of the same shapes: the
+    configuration's seed offset by 1000 x rank."""
+    import synth
+    return synth.CONFIGS[workload]["seed"] + 1000 * rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's figure (a MAX all-reduce: with the timing barrier,
+    the only collective of the benchmark)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, n_q: int, ms_per_step: float) -> float:
+    """Queries per second of the whole job: every rank's rows over the
+    slowest rank's step time."""
+    return world * n_q / (ms_per_step / 1e3)
+
+
 def _kernel_traffic(kernel: str, source: str):
     """DRAM bytes per launch from a committed ncu summary, if the kernel's
     source is unchanged since the counters were taken; else None."""
@@ -359,7 +384,7 @@ def run_si(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    wl = synth.make(args.workload, seed=synth.CONFIGS[args.workload]["seed"] + 1000 * rank)
+    wl = synth.make(args.workload, seed=rank_seed(args.workload, rank))
     dw = si.upload(wl, dev)
     b, ix, at, K = dw.batch, dw.indexer, dw.attention, dw.k_top
     n_q = wl.n_q
@@ -389,7 +414,14 @@ def run_si(args):
     torch.cuda.synchronize(dev)
     assert si.workspace_status(ws, stream) == 0
 
+    # Two timed passes over K steps each, L2 flushed before every step.  The
+    # step pass brackets each step with two events only, so that the three
+    # launches follow one another as they do in use (the Top-K and attention
+    # kernels start while their predecessor drains); it gives `value`.  The
+    # kernel pass puts an event between the launches for the per-kernel
+    # breakdown and the roofline.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     if world > 1:
@@ -398,26 +430,26 @@ def run_si(args):
     launches0 = si.launch_count()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)            # evict the previous step's data from L2
-        step(evs[i])
+        sevs[i][0].record(stream)
+        step()
+        sevs[i][1].record(stream)
     torch.cuda.synchronize(dev)
     launches = si.launch_count() - launches0
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        step(evs[i])
+    torch.cuda.synchronize(dev)
     assert si.workspace_status(ws, stream) == 0
 
-    t_step = [e[0].elapsed_time(e[3]) for e in evs]
     t_k = {"indexer": [e[0].elapsed_time(e[1]) for e in evs],
            "topk": [e[1].elapsed_time(e[2]) for e in evs],
            "attn": [e[2].elapsed_time(e[3]) for e in evs]}
-    ms = sum(t_step) / args.steps
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = world * n_q / (ms_max / 1e3)
-
+    ms = sum(e[0].elapsed_time(e[1]) for e in sevs) / args.steps
+    ms_max = max_over_ranks(ms, world, dev)
+    value = whole_job_rate(world, n_q, ms_max)
     # ---- end to end: host (pinned) buffers in and out, through the fused call
     h_qidx = torch.from_numpy(wl.q_idx).view(torch.bfloat16).pin_memory()
     h_w = torch.from_numpy(wl.w).pin_memory()
@@ -447,19 +479,12 @@ def run_si(args):
         e2e_step(e2e_ev[i])
     torch.cuda.synchronize(dev)
     assert si.workspace_status(ws_f, stream) == 0
-    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / args.steps, world, dev)
     h2d = h_qidx.numel() * 2 + h_w.numel() * 4 + h_q.numel() * 2
     d2h = h_out.numel() * h_out.element_size() + h_idx.numel() * 4
     del ws_f
-    e2e_pipe_ms = e2e_pipelined(si, wl, dw, h_qidx, h_w, h_q, args, dev)
-    if world > 1:
-        t = torch.tensor([e2e_pipe_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_pipe_ms = float(t.item())
+    e2e_pipe_ms = max_over_ranks(e2e_pipelined(si, wl, dw, h_qidx, h_w, h_q, args, dev), world,
+                                 dev)
 
     if rank != 0:
         if world > 1:
@@ -506,7 +531,7 @@ def run_si(args):
         "kernels_ms": mean_k,
         "kernels": {k: v[0] for k, v in _kernel_of(wl).items()},
         "clocks": clk,
-        "e2e": {"value": world * n_q / (e2e_pipe_ms / 1e3), "unit": "queries/s",
+        "e2e": {"value": whole_job_rate(world, n_q, e2e_pipe_ms), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_pipe_ms,
                 "call": "si_fused_decode with pinned host inputs/outputs",
@@ -514,7 +539,7 @@ def run_si(args):
                           f"copies in, fused call and copies out overlap across steps on three "
                           f"streams; {E2E_REPLICAS} device replicas of the resident caches "
                           f"taken in turn so that consecutive steps share no cached data",
-                "serial": {"value": world * n_q / (e2e_ms / 1e3), "ms_per_step": e2e_ms,
+                "serial": {"value": whole_job_rate(world, n_q, e2e_ms), "ms_per_step": e2e_ms,
                            "timing": "each step alone: copies in, fused call, copies out, "
                                      "L2 flushed between steps"}},
         "gpu_launches": int(launches),

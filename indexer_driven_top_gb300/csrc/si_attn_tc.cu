@@ -325,6 +325,15 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
     tc_fence_after();
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrival
     const uint32_t tmem = *tmem_slot;
+    if (score_cta && tid == 0) {
+        // query: nine tensor copies of [128 heads x 64 dims], SW128 K-major
+        mbar_arrive_expect_tx(bars + B_QREADY, kQChunks * kChunk);
+        for (int c = 0; c < kQChunks; c++)
+            tma_load_2d(base + kOffQ + c * kChunk, &qmap, c * 128, r * kHeads, bars + B_QREADY);
+    }
+    // The index list comes from the previous kernel of the stream (Top-K); all
+    // set-up above overlaps its tail.
+    griddep_wait();
 
     const uint8_t *kv = static_cast<const uint8_t *>(at.k.data);
     const int64_t row_bytes = at.k.row_stride * 2;
@@ -340,13 +349,6 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
         const int u = tid & 7, kr0 = tid >> 3;
         LoaderState ls;
         if (score_cta) {
-            if (tid == 0) {
-                // query: nine tensor copies of [128 heads x 64 dims], SW128 K-major
-                mbar_arrive_expect_tx(bars + B_QREADY, kQChunks * kChunk);
-                for (int c = 0; c < kQChunks; c++)
-                    tma_load_2d(base + kOffQ + c * kChunk, &qmap, c * 128, r * kHeads,
-                                bars + B_QREADY);
-            }
             // physical rows come from the row table the row warp fills
             const int *rows = reinterpret_cast<const int *>(gbase + kOffRows);
             ls.have_tile = -1;
@@ -844,9 +846,19 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
     if (e != cudaSuccess)
         return e;
     count_launch();
-    k_attn_tc<<<(unsigned)(2 * b.n_q), kThreads, kSmemBytes, s>>>(qmap, omap, b, at, idx, k_top,
-                                                                  out_dtype, lse, st);
-    return cudaGetLastError();
+    // may overlap the tail of the kernel that wrote idx (programmatic
+    // dependent launch; the kernel waits for it before reading idx)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * b.n_q));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_attn_tc, qmap, omap, b, at, idx, k_top, out_dtype, lse, st);
 }
 
 }  // namespace si

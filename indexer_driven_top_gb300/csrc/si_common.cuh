@@ -18,6 +18,18 @@ constexpr size_t kStatusBytes = 256;
 constexpr int kMaxDevices = 64;
 
 // A null status pointer means "do not report" (used by redundant lanes).
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel of its stream still runs;
+// griddep_wait() returns once that kernel has completed and its writes are
+// visible (at once when there is no such dependency).  griddep_launch_dependents()
+// lets the next kernel of the stream start its own preamble early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void raise_flag(unsigned int *st, unsigned int f)
 {
     if (st)

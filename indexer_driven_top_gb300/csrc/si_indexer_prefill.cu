@@ -158,6 +158,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
     float *sc_s = reinterpret_cast<float *>(gbase + kOffSc);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    griddep_launch_dependents();  // the Top-K kernel may be scheduled as CTAs finish
     const int64_t G = gridDim.x;
     const int tiles_ld = (int)((ld + kKeys - 1) / kKeys);
 

@@ -127,6 +127,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
     volatile int *win_all = reinterpret_cast<volatile int *>(gbase + kOffWin);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    griddep_launch_dependents();  // the Top-K kernel may be scheduled as CTAs finish
     const int64_t G = gridDim.x;
     const int64_t j0 = total_items * blockIdx.x / G;
     const int64_t j1 = total_items * (blockIdx.x + 1) / G;

@@ -126,6 +126,7 @@ k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx
     __shared__ uint32_t sh_digit;
     __shared__ int sh_rem;
 
+    griddep_launch_dependents();  // the attention kernel may set itself up meanwhile
     const int r = blockIdx.x, tid = threadIdx.x;
     int64_t n = (int64_t)b.q_pos[r] + 1;  // candidates 0..pos
     if (n > ld)
@@ -133,6 +134,9 @@ k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx
     const float *row = scores + (int64_t)r * ld;
     int32_t *out = idx + (int64_t)r * k_top;
 
+    // The scores come from the previous kernel of the stream.  Every CTA
+    // waits for it, so that this grid never completes before that one.
+    griddep_wait();
     if (n <= k_top) {  // everything is selected
         for (int i = tid; i < k_top; i += kTopkThreads)
             out[i] = i < n ? i : -1;
@@ -215,8 +219,19 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
 {
     (void)st;
     count_launch();
-    k_topk_rows<<<b.n_q, kTopkThreads, 0, s>>>(b, scores, ld, k_top, idx);
-    return cudaGetLastError();
+    // may overlap the tail of the kernel that wrote the scores (programmatic
+    // dependent launch; the kernel waits for it before reading them)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)b.n_q);
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_topk_rows, b, scores, ld, k_top, idx);
 }
 
 }  // namespace si
