@@ -175,7 +175,9 @@ def _kernel_of(wl):
     rows), the generic ones otherwise."""
     tc_ix = wl.Hi == 64 and wl.Di == 128 and wl.q_idx_dtype == "bf16" and wl.k_idx_dtype == "e4m3"
     tc_at = wl.Hq == 128 and wl.Dqk == 576 and wl.Dv == 512 and wl.kv_dtype == "bf16"
-    return {"indexer": ("k_indexer_tc", "si_indexer_tc.cu") if tc_ix
+    prefill = tc_ix and wl.n_seq == 1 and wl.n_q >= 64
+    return {"indexer": ("k_indexer_prefill", "si_indexer_prefill.cu") if prefill
+            else ("k_indexer_tc", "si_indexer_tc.cu") if tc_ix
             else ("k_indexer_generic", "si_generic.cu"),
             "topk": ("k_topk_rows", "si_topk.cu"),
             "attn": ("k_attn_tc", "si_attn_tc.cu") if tc_at
@@ -363,9 +365,15 @@ def prefill_indexer(si, dev, steps):
 
 
 def _workload_name(wl):
-    if wl.name == "c1":
-        return "decode batch 64 x context 8192, indexer 64x128 fp8, top-k 2048, MLA 128x576 bf16"
-    return wl.name
+    names = {
+        "c1": "decode batch 64 x context 8192, indexer 64x128 fp8, top-k 2048, MLA 128x576 bf16",
+        "c2": "causal prefill 16384 tokens, indexer 64x128 fp8, top-k 2048, MLA 128x576 bf16",
+        "c3": "decode batch 16 x context 131072 (1% planted keys), indexer 64x128 fp8, top-k 2048, "
+              "MLA 128x576 bf16",
+        "c4": "mixed batch: 28 decode rows + 4 prefill chunks of 2048 over contexts 1K-64K, "
+              "indexer 64x128 fp8, top-k 2048, MLA 128x576 bf16",
+    }
+    return names.get(wl.name, wl.name)
 
 
 # ---------------------------------------------------------------- main arm
