@@ -458,46 +458,62 @@ def run_si(args):
     ms = sum(e[0].elapsed_time(e[1]) for e in sevs) / args.steps
     ms_max = max_over_ranks(ms, world, dev)
     value = whole_job_rate(world, n_q, ms_max)
-    # ---- end to end: host (pinned) buffers in and out, through the fused call
-    h_qidx = torch.from_numpy(wl.q_idx).view(torch.bfloat16).pin_memory()
-    h_w = torch.from_numpy(wl.w).pin_memory()
-    h_q = torch.from_numpy(wl.q).view(torch.bfloat16).pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_idx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
-    ws_f = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, ix, at, K), dev)
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    e2e = None
+    if not args.no_e2e:
+        # ---- end to end: host (pinned) buffers in and out, through the fused call
+        h_qidx = torch.from_numpy(wl.q_idx).view(torch.bfloat16).pin_memory()
+        h_w = torch.from_numpy(wl.w).pin_memory()
+        h_q = torch.from_numpy(wl.q).view(torch.bfloat16).pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_idx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+        ws_f = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, ix, at, K), dev)
+        e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
 
-    def e2e_step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        ix.q.copy_(h_qidx, non_blocking=True)
-        ix.w.copy_(h_w, non_blocking=True)
-        at.q.copy_(h_q, non_blocking=True)
-        si.fused_decode(b, ix, at, K, idx, out, ws_f, stream=stream)
-        h_out.copy_(out, non_blocking=True)
-        h_idx.copy_(idx, non_blocking=True)
-        if ev:
-            ev[1].record(stream)
+        def e2e_step(ev=None):
+            if ev:
+                ev[0].record(stream)
+            ix.q.copy_(h_qidx, non_blocking=True)
+            ix.w.copy_(h_w, non_blocking=True)
+            at.q.copy_(h_q, non_blocking=True)
+            si.fused_decode(b, ix, at, K, idx, out, ws_f, stream=stream)
+            h_out.copy_(out, non_blocking=True)
+            h_idx.copy_(idx, non_blocking=True)
+            if ev:
+                ev[1].record(stream)
 
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        e2e_step(e2e_ev[i])
-    torch.cuda.synchronize(dev)
-    assert si.workspace_status(ws_f, stream) == 0
-    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / args.steps, world, dev)
-    h2d = h_qidx.numel() * 2 + h_w.numel() * 4 + h_q.numel() * 2
-    d2h = h_out.numel() * h_out.element_size() + h_idx.numel() * 4
-    del ws_f
-    e2e_pipe_ms = max_over_ranks(e2e_pipelined(si, wl, dw, h_qidx, h_w, h_q, args, dev), world,
-                                 dev)
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            e2e_step(e2e_ev[i])
+        torch.cuda.synchronize(dev)
+        assert si.workspace_status(ws_f, stream) == 0
+        e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / args.steps, world,
+                                dev)
+        h2d = h_qidx.numel() * 2 + h_w.numel() * 4 + h_q.numel() * 2
+        d2h = h_out.numel() * h_out.element_size() + h_idx.numel() * 4
+        del ws_f
+        e2e_pipe_ms = max_over_ranks(e2e_pipelined(si, wl, dw, h_qidx, h_w, h_q, args, dev),
+                                     world, dev)
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
+
+    if not args.no_e2e:
+        e2e = {"value": whole_job_rate(world, n_q, e2e_pipe_ms), "unit": "queries/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_pipe_ms,
+               "call": "si_fused_decode with pinned host inputs/outputs",
+               "timing": f"first input copy to last result copy over {args.steps} steps; "
+                         f"copies in, fused call and copies out overlap across steps on three "
+                         f"streams; {E2E_REPLICAS} device replicas of the resident caches "
+                         f"taken in turn so that consecutive steps share no cached data",
+               "serial": {"value": whole_job_rate(world, n_q, e2e_ms), "ms_per_step": e2e_ms,
+                          "timing": "each step alone: copies in, fused call, copies out, "
+                                    "L2 flushed between steps"}}
 
     # ---- roofline of the dominant kernel
     peaks = _peaks()
@@ -539,17 +555,7 @@ def run_si(args):
         "kernels_ms": mean_k,
         "kernels": {k: v[0] for k, v in _kernel_of(wl).items()},
         "clocks": clk,
-        "e2e": {"value": whole_job_rate(world, n_q, e2e_pipe_ms), "unit": "queries/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_pipe_ms,
-                "call": "si_fused_decode with pinned host inputs/outputs",
-                "timing": f"first input copy to last result copy over {args.steps} steps; "
-                          f"copies in, fused call and copies out overlap across steps on three "
-                          f"streams; {E2E_REPLICAS} device replicas of the resident caches "
-                          f"taken in turn so that consecutive steps share no cached data",
-                "serial": {"value": whole_job_rate(world, n_q, e2e_ms), "ms_per_step": e2e_ms,
-                           "timing": "each step alone: copies in, fused call, copies out, "
-                                     "L2 flushed between steps"}},
+        "e2e": e2e,
         "gpu_launches": int(launches),
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -569,6 +575,7 @@ def main():
     ap.add_argument("--workload", default="c1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end legs")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill indexer (both query formats) and print its record")
     args = ap.parse_args()

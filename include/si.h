@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define SI_VERSION 2
+#define SI_VERSION 3
 
 typedef enum si_status {
     SI_OK = 0,
@@ -92,14 +92,22 @@ typedef struct si_batch {
     int32_t n_blocks;           /* physical pages in each cache */
 } si_batch;
 
-/* One paged cache: [n_blocks, page_size, row_stride] elements of dtype. */
+/* One paged cache: [n_blocks, page_size, row_stride] elements of dtype.
+ * Dequantised entry d of a row = code * scale, the scale taken per row or per
+ * tile of `scale_tile` consecutive entries (section 5.2 stores the KV cache in
+ * FP8 per token and tile of 128 entries). */
 typedef struct si_paged {
     const void *data;    /* device; 16-byte aligned */
-    const float *scale;  /* device [n_blocks, page_size] per-row dequantisation
-                            scale (> 0), or NULL for 1 */
+    const float *scale;  /* device dequantisation scales (> 0), or NULL for 1:
+                            [n_blocks, page_size] when scale_tile == 0,
+                            [n_blocks, page_size, ceil(row_stride / scale_tile)]
+                            otherwise (entry d uses tile d / scale_tile; a
+                            value cache that aliases the key rows shares their
+                            scales) */
     si_dtype dtype;
     int32_t row_dim;     /* elements used per row */
     int64_t row_stride;  /* elements between consecutive rows, >= row_dim */
+    int32_t scale_tile;  /* 0: one scale per row; else entries per scale tile */
 } si_paged;
 
 /* Indexer operands (section 2.2: lightweight multi-head indexer; section 5.1
@@ -126,9 +134,12 @@ typedef struct si_attention {
     int32_t n_heads;     /* query heads sharing each KV row, 1..256 */
     int32_t d_qk;        /* logit dims, 1..1024 */
     int32_t d_v;         /* value dims, 1..1024 */
-    si_paged k;          /* key rows: row_dim >= d_qk, same dtype as q */
-    si_paged v;          /* value rows: row_dim >= d_v; may alias k (the value
-                            is then the first d_v entries of the key row) */
+    si_paged k;          /* key rows: row_dim >= d_qk; the dtype of q, or SI_E4M3
+                            codes with scales (per row or per tile) for a bf16
+                            or f32 q */
+    si_paged v;          /* value rows: row_dim >= d_v, dtype as k; may alias k
+                            (the value is then the first d_v entries of the key
+                            row, with the key row's scales) */
     float softmax_scale; /* logits are softmax_scale * q . k */
 } si_attention;
 

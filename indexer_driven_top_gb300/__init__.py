@@ -45,7 +45,8 @@ class c_batch(ctypes.Structure):
 
 class c_paged(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("dtype", ctypes.c_int),
-                ("row_dim", ctypes.c_int32), ("row_stride", ctypes.c_int64)]
+                ("row_dim", ctypes.c_int32), ("row_stride", ctypes.c_int64),
+                ("scale_tile", ctypes.c_int32)]
 
 
 class c_indexer(ctypes.Structure):
@@ -144,15 +145,17 @@ class Batch:
 
 @dataclasses.dataclass
 class Paged:
-    """Paged cache [n_blocks, page_size, row_stride] with optional per-row scale."""
+    """Paged cache [n_blocks, page_size, row_stride] with optional scales: one
+    per row, or one per `scale_tile` consecutive entries of a row."""
     data: torch.Tensor
     dtype: str                  # "f32" | "bf16" | "e4m3"
     row_dim: int
     scale: Optional[torch.Tensor] = None
+    scale_tile: int = 0
 
     def c(self) -> c_paged:
         return c_paged(_ptr(self.data), _ptr(self.scale), DTYPES[self.dtype], self.row_dim,
-                       self.data.shape[-1])
+                       self.data.shape[-1], self.scale_tile)
 
 
 @dataclasses.dataclass
@@ -318,14 +321,19 @@ def upload(wl, device="cuda") -> DeviceWorkload:
     ten["k_idx"] = _dev(wl.k_idx, device)
     ten["k_scale"] = None if wl.k_scale is None else _dev(wl.k_scale, device)
     kvt = bf if wl.kv_dtype == "bf16" else None
-    ten["q"] = _dev(wl.q, device, kvt)
+    qt = getattr(wl, "attn_q_dtype", "") or wl.kv_dtype
+    ten["q"] = _dev(wl.q, device, bf if qt == "bf16" else None)
     ten["k"] = _dev(wl.k, device, kvt)
     ten["v"] = None if wl.v is None else _dev(wl.v, device, kvt)
+    kv_scale = getattr(wl, "kv_scale", None)
+    ten["kv_scale"] = None if kv_scale is None else _dev(kv_scale, device)
+    tile = getattr(wl, "kv_scale_tile", 0) if kv_scale is not None else 0
     b = Batch(ten["block_table"], ten["ctx_len"], ten["q_seq"], ten["q_pos"], wl.page,
               wl.max_ctx, wl.n_blocks)
     ix = Indexer(ten["q_idx"], wl.q_idx_dtype, ten["w"],
                  Paged(ten["k_idx"], wl.k_idx_dtype, wl.Di, ten["k_scale"]), ten["q_scale"])
-    kp = Paged(ten["k"], wl.kv_dtype, wl.Dqk)
+    kp = Paged(ten["k"], wl.kv_dtype, wl.Dqk, ten["kv_scale"], tile)
     vp = kp if ten["v"] is None else Paged(ten["v"], wl.kv_dtype, wl.Dv)
-    at = Attention(ten["q"], wl.kv_dtype, kp, Paged(vp.data, vp.dtype, wl.Dv), wl.Dv, wl.scale)
+    at = Attention(ten["q"], qt, kp, Paged(vp.data, vp.dtype, wl.Dv, vp.scale, vp.scale_tile),
+                   wl.Dv, wl.scale)
     return DeviceWorkload(b, ix, at, wl.K, wl.n_q, ten)

@@ -93,6 +93,8 @@ si_status check_paged(const si_paged &p, const char *name, int need_dim)
     if (p.row_stride < p.row_dim)
         return fail(SI_ERR_INVALID_ARG, "%s.row_stride %lld < row_dim %d", name,
                     (long long)p.row_stride, p.row_dim);
+    if (p.scale_tile < 0 || (p.scale_tile > 0 && !p.scale))
+        return fail(SI_ERR_INVALID_ARG, "%s.scale_tile %d needs a scale array", name, p.scale_tile);
     return SI_OK;
 }
 
@@ -110,6 +112,8 @@ si_status check_indexer(const si_indexer *ix)
         return fail(SI_ERR_INVALID_ARG, "indexer n_heads %d outside 1..128", ix->n_heads);
     if (ix->head_dim < 1 || ix->head_dim > 256)
         return fail(SI_ERR_INVALID_ARG, "indexer head_dim %d outside 1..256", ix->head_dim);
+    if (ix->k.scale_tile != 0)
+        return fail(SI_ERR_UNSUPPORTED, "indexer keys take one scale per row (scale_tile 0)");
     return check_paged(ix->k, "indexer k", ix->head_dim);
 }
 
@@ -131,8 +135,13 @@ si_status check_attention(const si_attention *at)
     s = check_paged(at->v, "attention v", at->d_v);
     if (s != SI_OK)
         return s;
-    if (at->k.dtype != at->q_dtype || at->v.dtype != at->q_dtype)
-        return fail(SI_ERR_UNSUPPORTED, "attention q, k and v must share one dtype (f32 or bf16)");
+    // keys and values: the dtype of q, or FP8 codes with scales (section 5.2)
+    const bool fp8_kv = at->k.dtype == SI_E4M3 && at->v.dtype == SI_E4M3;
+    if (!fp8_kv && (at->k.dtype != at->q_dtype || at->v.dtype != at->q_dtype))
+        return fail(SI_ERR_UNSUPPORTED,
+                    "attention k and v must share q's dtype, or both be e4m3 with scales");
+    if (fp8_kv && (!at->k.scale || !at->v.scale))
+        return fail(SI_ERR_INVALID_ARG, "e4m3 attention k and v need scales");
     return SI_OK;
 }
 

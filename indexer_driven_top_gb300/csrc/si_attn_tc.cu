@@ -809,7 +809,8 @@ bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top)
     // one shared latent row per position: V is the first 512 entries of the
     // 576-entry key row (the same cache, same stride)
     return at.q_dtype == SI_BF16 && at.n_heads == kHeads && at.d_qk == kDqk && at.d_v == kDv &&
-           at.k.dtype == SI_BF16 && at.v.data == at.k.data && at.v.row_stride == at.k.row_stride &&
+           at.k.dtype == SI_BF16 && !at.k.scale && !at.v.scale && at.v.data == at.k.data &&
+           at.v.row_stride == at.k.row_stride &&
            at.k.row_stride % 8 == 0 && ((uintptr_t)at.k.data % 16) == 0 &&
            ((uintptr_t)at.q % 16) == 0;
 }

@@ -71,6 +71,22 @@ __device__ __forceinline__ float load_elem(const void *p, si_dtype t, int64_t i)
 
 // Order-preserving map of a float score onto uint32 (larger score -> larger
 // key); -0 is folded onto +0 so that the two compare equal.
+// Dequantised entry d of physical row `row` of a paged cache: the stored
+// element times its scale (per row, or per tile of scale_tile entries).
+__device__ __forceinline__ float load_paged(const si_paged &p, int64_t row, int d)
+{
+    float x = load_elem(p.data, p.dtype, row * p.row_stride + d);
+    if (p.scale) {
+        if (p.scale_tile > 0) {
+            const int64_t nt = (p.row_stride + p.scale_tile - 1) / p.scale_tile;
+            x *= p.scale[row * nt + d / p.scale_tile];
+        } else {
+            x *= p.scale[row];
+        }
+    }
+    return x;
+}
+
 __device__ __forceinline__ uint32_t order_key(float f)
 {
     f = f + 0.0f;

@@ -113,7 +113,7 @@ k_attn_generic(si_batch b, si_attention at, const int32_t *idx, int k_top, void 
         float dot = 0.f;
         if (row >= 0)
             for (int d = lane; d < at.d_qk; d += 32)
-                dot = fmaf(q_s[d], load_elem(at.k.data, at.k.dtype, row * at.k.row_stride + d), dot);
+                dot = fmaf(q_s[d], load_paged(at.k, row, d), dot);
         dot = warp_sum(dot);
         if (lane == 0)
             z_s[j] = row >= 0 ? dot * at.softmax_scale : -INFINITY;
@@ -162,7 +162,7 @@ k_attn_generic(si_batch b, si_attention at, const int32_t *idx, int k_top, void 
         for (int j = 0; j < k_top; j++) {
             const int64_t row = rows[j];
             if (row >= 0)
-                acc = fmaf(z_s[j], load_elem(at.v.data, at.v.dtype, row * at.v.row_stride + d), acc);
+                acc = fmaf(z_s[j], load_paged(at.v, row, d), acc);
         }
         acc *= inv;
         if (out_dtype == SI_F32)

@@ -63,8 +63,8 @@ def _load():
                                                   ctypes.c_int, P, I64, P, I64, ctypes.c_int]
             lib.oracle_topk.argtypes = [P, P, I32, P, I64, I32, P, P, ctypes.c_int]
             lib.oracle_sparse_attn.argtypes = [P, P, I32, I32, I32, I32, P, ctypes.c_int, P, P,
-                                               ctypes.c_int, I64, I64, P, I32, D, P, P,
-                                               ctypes.c_int]
+                                               ctypes.c_int, I64, I64, P, P, I32, I32, I32, P,
+                                               I32, D, P, P, ctypes.c_int]
             lib.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
             lib.orc_bf16_to_f64.restype = D
             lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
@@ -158,22 +158,37 @@ def topk(b: Batch, scores, K: int, rows: Optional[Sequence[int]] = None,
 
 def sparse_attn(b: Batch, q, q_type: str, k, v, kv_type: str, idx, K: int, Hq: int, Dqk: int,
                 Dv: int, scale: float, rows: Optional[Sequence[int]] = None,
-                threads: Optional[int] = None):
+                threads: Optional[int] = None, q_dtype: Optional[str] = None, kv_scale=None,
+                scale_tile: int = 0):
     """out[i, h] = softmax over the selected rows of scale * q . k, applied to
     the values; returns (out [n, Hq, Dv], lse [n, Hq]) in float64.  ``v=None``
-    means the value row is the first Dv entries of the key row."""
+    means the value row is the first Dv entries of the key row.  ``q_type`` is
+    the storage type of q and of the caches, unless ``q_dtype`` gives q's own
+    (FP8 caches with a bf16 query).  ``kv_scale`` [n_blocks, page, n_tiles]
+    dequantises the key rows (and the value rows cut from them) per tile of
+    ``scale_tile`` entries."""
     lib = _load()
     rr, n = _rows(rows, b.s.n_q)
     q, k = _c(q), _c(k)
     v = k if v is None else _c(v)
     ix = _c(idx, np.int32)
+    ks = None if kv_scale is None else _c(kv_scale, np.float32)
+    nsc = 0 if ks is None else int(ks.shape[-1]) if scale_tile > 0 else 1
     out = np.empty((n, Hq, Dv), dtype=np.float64)
     lse = np.empty((n, Hq), dtype=np.float64)
     lib.oracle_sparse_attn(ctypes.byref(b.s), _ptr(rr), n, Hq, Dqk, Dv, _ptr(q),
-                           TYPE_CODE[q_type], _ptr(k), _ptr(v), TYPE_CODE[kv_type],
-                           k.shape[-1], v.shape[-1], _ptr(ix), K, scale, _ptr(out),
-                           _ptr(lse), threads or default_threads())
+                           TYPE_CODE[q_dtype or q_type], _ptr(k), _ptr(v), TYPE_CODE[kv_type],
+                           k.shape[-1], v.shape[-1], _ptr(ks), _ptr(ks), scale_tile, nsc, nsc,
+                           _ptr(ix), K, scale, _ptr(out), _ptr(lse), threads or default_threads())
     return out, lse
+
+
+def attn_kv_args(wl) -> dict:
+    """Keyword arguments of sparse_attn for a workload's KV storage: an FP8
+    cache carries per-tile scales and a query of its own type."""
+    if getattr(wl, "kv_scale", None) is None:
+        return {}
+    return {"q_dtype": wl.attn_q_dtype, "kv_scale": wl.kv_scale, "scale_tile": wl.kv_scale_tile}
 
 
 def run(wl, rows: Optional[Sequence[int]] = None, threads: Optional[int] = None):
@@ -186,5 +201,6 @@ def run(wl, rows: Optional[Sequence[int]] = None, threads: Optional[int] = None)
                         q_scale=getattr(wl, "q_scale", None))
     idx, kth = topk(b, sc, wl.K, rows=rows, threads=threads, return_kth=True)
     out, lse = sparse_attn(b, wl.q, wl.kv_dtype, wl.k, wl.v, wl.kv_dtype, idx, wl.K, wl.Hq,
-                           wl.Dqk, wl.Dv, wl.scale, rows=rows, threads=threads)
+                           wl.Dqk, wl.Dv, wl.scale, rows=rows, threads=threads,
+                           **attn_kv_args(wl))
     return sc, idx, kth, out, lse

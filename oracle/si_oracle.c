@@ -251,11 +251,26 @@ typedef struct {
     const void *q; int q_type;          /* [n_q, Hq, Dqk] */
     const void *k; const void *v; int kv_type;
     int64_t k_stride, v_stride;         /* V row = first Dv entries of its row */
+    const float *k_scale, *v_scale;     /* dequantisation scales or NULL (= 1) */
+    int32_t scale_tile;                 /* 0: one scale per row; else entries per scale */
+    int32_t k_nscale, v_nscale;         /* scales per row */
     const int32_t *idx; int32_t K;      /* [n_rows, K], -1 = unused */
     double scale;
     double *out;                        /* [n_rows, Hq, Dv] */
     double *lse;                        /* [n_rows, Hq] or NULL */
 } attn_ctx;
+
+/* Entry d of physical row `row` of a cache, dequantised: code * scale, the
+ * scale per row or per tile of scale_tile entries (section 5.2 "KV Cache: FP8
+ * with Token-Head-Tile Granularity"). */
+static double kv_entry(const void *data, int type, int64_t stride, const float *scale,
+                       int32_t tile, int32_t nscale, int64_t row, int32_t d)
+{
+    double x = elem(data, type, row * stride + d);
+    if (scale)
+        x *= (double)scale[row * nscale + (tile > 0 ? d / tile : 0)];
+    return x;
+}
 
 static void attn_row(void *p, int64_t i)
 {
@@ -278,7 +293,8 @@ static void attn_row(void *p, int64_t i)
             double dot = 0.0;
             for (int32_t d = 0; d < c->Dqk; d++)
                 dot += elem(c->q, c->q_type, qoff + d) *
-                       elem(c->k, c->kv_type, prow[j] * c->k_stride + d);
+                       kv_entry(c->k, c->kv_type, c->k_stride, c->k_scale, c->scale_tile,
+                                c->k_nscale, prow[j], d);
             z[j] = c->scale * dot;
             if (z[j] > zmax) zmax = z[j];
         }
@@ -290,7 +306,8 @@ static void attn_row(void *p, int64_t i)
         for (int32_t d = 0; d < c->Dv; d++) {   /* weighted sum of values */
             double acc = 0.0;
             for (int32_t j = 0; j < n; j++)
-                acc += z[j] * elem(c->v, c->kv_type, prow[j] * c->v_stride + d);
+                acc += z[j] * kv_entry(c->v, c->kv_type, c->v_stride, c->v_scale, c->scale_tile,
+                                       c->v_nscale, prow[j], d);
             o[d] = n > 0 ? acc / l : 0.0;
         }
         if (c->lse)
@@ -303,10 +320,11 @@ static void attn_row(void *p, int64_t i)
 void oracle_sparse_attn(const orc_batch *b, const int32_t *rows, int32_t n_rows, int32_t Hq,
                         int32_t Dqk, int32_t Dv, const void *q, int q_type, const void *k,
                         const void *v, int kv_type, int64_t k_stride, int64_t v_stride,
-                        const int32_t *idx, int32_t K, double scale, double *out, double *lse,
-                        int nthreads)
+                        const float *k_scale, const float *v_scale, int32_t scale_tile,
+                        int32_t k_nscale, int32_t v_nscale, const int32_t *idx, int32_t K,
+                        double scale, double *out, double *lse, int nthreads)
 {
     attn_ctx c = { b, rows, Hq, Dqk, Dv, q, q_type, k, v, kv_type, k_stride, v_stride,
-                   idx, K, scale, out, lse };
+                   k_scale, v_scale, scale_tile, k_nscale, v_nscale, idx, K, scale, out, lse };
     orc_parallel(attn_row, &c, n_rows, nthreads);
 }

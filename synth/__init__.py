@@ -23,6 +23,11 @@ Option ``q_idx_fp8=True`` (any config) stores the indexer query quantised the
 way the key cache is: e4m3 codes with one fp32 scale per (row, head), scale =
 max|q_h| / 448, drawn from the same q_idx values.
 
+Option ``kv_fp8=True`` (latent-row configs) stores the attention KV cache as
+e4m3 codes with one fp32 scale per row and tile of 128 entries (576 entries:
+four full tiles and one of 64), scale = max|tile| / 448, quantised from the
+same N(0,1) draws; the attention query stays bf16.
+
 Draw order (per config): context lengths (c4 only) -> physical block
 permutation -> q_idx -> w -> indexer keys (sequence by sequence, logical
 order) -> planted positions and offsets (c3) -> attention q -> K/V rows
@@ -102,6 +107,9 @@ class Workload:
     v: Optional[np.ndarray]      # [n_blocks, page, Dv]; None = V is the first Dv cols of k
     planted: Optional[list] = None  # c3: per-sequence arrays of planted positions
     q_scale: Optional[np.ndarray] = None  # f32 [n_q, Hi] when q_idx holds e4m3 codes
+    kv_scale: Optional[np.ndarray] = None  # f32 [n_blocks, page, n_tiles] for an e4m3 KV cache
+    kv_scale_tile: int = 0                 # entries per KV scale tile (0: none)
+    attn_q_dtype: str = ""                 # attention q storage ("" = kv_dtype)
 
     @property
     def n_q(self) -> int:
@@ -153,6 +161,25 @@ def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
     code = np.minimum(code, 0x7E)
     code = np.where((x < 0) & (code != 0), code | 0x80, code)
     return code.astype(np.uint8)
+
+
+KV_TILE = 128
+
+
+def quantize_tiles_e4m3(rows: np.ndarray, tile: int = KV_TILE):
+    """Per-(row, tile) FP8 storage along the last axis: each run of `tile`
+    entries (the last one may be shorter) gets scale = amax/448.  Returns
+    (codes uint8 [..., D], scales float32 [..., ceil(D / tile)])."""
+    rows = np.asarray(rows, dtype=np.float32)
+    d = rows.shape[-1]
+    nt = (d + tile - 1) // tile
+    codes = np.empty(rows.shape, dtype=np.uint8)
+    scales = np.empty(rows.shape[:-1] + (nt,), dtype=np.float32)
+    for t in range(nt):
+        c, sc = quantize_rows_e4m3(rows[..., t * tile: min(d, (t + 1) * tile)])
+        codes[..., t * tile: min(d, (t + 1) * tile)] = c
+        scales[..., t] = sc
+    return codes, scales
 
 
 def quantize_rows_e4m3(rows: np.ndarray):
@@ -303,6 +330,12 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
     del qa
 
     # 7. K/V rows
+    kv_scale = None
+    kv_dtype = F32 if fp32 else BF16
+    if cfg.get("kv_fp8") and (cfg["split_kv"] or fp32):
+        raise ValueError("kv_fp8 applies to the bf16 latent-row configurations")
+    if cfg.get("kv_fp8"):
+        kv_dtype = E4M3
     if cfg["split_kv"]:
         k = np.full((n_blocks, page, Dqk), np.nan, dtype=np.float32)
         v = np.full((n_blocks, page, Dv), np.nan, dtype=np.float32)
@@ -313,8 +346,14 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
         if not fp32:
             k, v = f32_to_bf16_bits(k), f32_to_bf16_bits(v)
     else:
-        k = np.full((n_blocks, page, Dqk), np.nan if fp32 else 0x7FC0,
-                    dtype=np.float32 if fp32 else np.uint16)
+        kv8 = bool(cfg.get("kv_fp8", False))
+        if kv8:
+            k = np.full((n_blocks, page, Dqk), 0x7F, dtype=np.uint8)     # e4m3 NaN when unused
+            n_tiles = (Dqk + KV_TILE - 1) // KV_TILE
+            kv_scale = np.full((n_blocks, page, n_tiles), np.nan, dtype=np.float32)
+        else:
+            k = np.full((n_blocks, page, Dqk), np.nan if fp32 else 0x7FC0,
+                        dtype=np.float32 if fp32 else np.uint16)
         v = None
         for i in range(n_seq):
             c = int(ctx_len[i])
@@ -323,17 +362,24 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
             for s0 in range(0, c, step):
                 s1 = min(c, s0 + step)
                 rows = _normal(rng, (s1 - s0, Dqk))
-                rows = rows if fp32 else f32_to_bf16_bits(rows)
+                if kv8:
+                    rows, rsc = quantize_tiles_e4m3(rows)
+                else:
+                    rows = rows if fp32 else f32_to_bf16_bits(rows)
                 for j in range(s0 // page, (s1 + page - 1) // page):
                     lo, hi = j * page, min(s1, (j + 1) * page)
                     k[bt[i, j], lo - j * page: hi - j * page] = rows[lo - s0: hi - s0]
+                    if kv8:
+                        kv_scale[bt[i, j], lo - j * page: hi - j * page] = rsc[lo - s0: hi - s0]
 
     return Workload(
         name=name, Hi=Hi, Di=Di, Hq=Hq, Dqk=Dqk, Dv=Dv, K=int(cfg["K"]), page=page,
         scale=float(cfg["scale"]), block_table=bt, ctx_len=ctx_len, q_seq=q_seq,
         q_pos=q_pos, q_idx=q_idx, q_idx_dtype=q_idx_dtype, w=w,
         k_idx=k_idx, k_idx_dtype=F32 if fp32 else E4M3, k_scale=k_scale, q=q,
-        kv_dtype=F32 if fp32 else BF16, k=k, v=v, planted=planted, q_scale=q_scale)
+        kv_dtype=kv_dtype, k=k, v=v, planted=planted, q_scale=q_scale, kv_scale=kv_scale,
+        kv_scale_tile=KV_TILE if kv_scale is not None else 0,
+        attn_q_dtype=F32 if fp32 else BF16)
 
 
 def _bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -352,4 +398,4 @@ def permute_pages(wl: Workload, seed: int) -> Workload:
 
     bt = np.where(wl.block_table >= 0, perm[np.maximum(wl.block_table, 0)], -1).astype(np.int32)
     return dataclasses.replace(wl, block_table=bt, k_idx=mv(wl.k_idx), k_scale=mv(wl.k_scale),
-                               k=mv(wl.k), v=mv(wl.v))
+                               k=mv(wl.k), v=mv(wl.v), kv_scale=mv(wl.kv_scale))

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(si):
 
 def test_version_and_status_strings(si):
     lib = si.load()
-    assert lib.si_version() == 2
+    assert lib.si_version() == 3
     assert lib.si_status_string(0) == b"ok"
     assert lib.si_status_string(3) == b"workspace error"
 
@@ -71,11 +71,21 @@ def test_host_validation_rejects_bad_arguments(si):
     assert lib.si_topk(b, P(fake), 256, 8, P(fake), None, 4096, None) == 3
     assert lib.si_topk(b, P(fake), 256, 8, P(fake), P(ws + 16), 4096, None) == 3
     assert lib.si_topk(b, P(fake), 256, 8, P(fake), P(ws), 16, None) == 3
-    # attention: dtype mismatch and bad dims
-    kp = si.c_paged(fake, None, si.E4M3, 64, 64)
+    # attention: dtype mismatch, FP8 caches without scales, bad dims
+    kp = si.c_paged(fake, None, si.F32, 64, 64)
     at = si.c_attention(fake, si.BF16, 4, 64, 64, kp, kp, 0.125)
     assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
                               4096, None) == 2
+    kp = si.c_paged(fake, None, si.E4M3, 64, 64)
+    at = si.c_attention(fake, si.BF16, 4, 64, 64, kp, kp, 0.125)
+    assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
+                              4096, None) == 1
+    assert b"need scales" in lib.si_last_error()
+    kp = si.c_paged(fake, None, si.E4M3, 64, 64, 32)      # tiles of 32 entries without scales
+    at = si.c_attention(fake, si.BF16, 4, 64, 64, kp, kp, 0.125)
+    assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
+                              4096, None) == 1
+    kp = si.c_paged(fake, None, si.BF16, 64, 64)
     at = si.c_attention(fake, si.BF16, 4, 2000, 64, kp, kp, 0.125)
     assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
                               4096, None) == 1

@@ -62,7 +62,8 @@ def _check_rows(wl, rows, g_scores, g_idx, g_out):
     check_topk(g_idx[rows], o_idx, o_sc, wl.q_pos, wl.K, rows=rows)
     # row i of the index list belongs to rows[i]
     ref, _ = oracle.sparse_attn(oracle.Batch.of(wl), wl.q, wl.kv_dtype, wl.k, wl.v, wl.kv_dtype,
-                                g_idx[rows], wl.K, wl.Hq, wl.Dqk, wl.Dv, wl.scale, rows=rows)
+                                g_idx[rows], wl.K, wl.Hq, wl.Dqk, wl.Dv, wl.scale, rows=rows,
+                                **oracle.attn_kv_args(wl))
     assert max_abs(g_out[rows], ref) <= ATOL_BF16
 
 
@@ -108,7 +109,8 @@ def test_benchmark_workload_bf16_output(si):
     g_idx = idx.cpu().numpy()
     g_out = out.float().cpu().numpy()
     ref, _ = oracle.sparse_attn(oracle.Batch.of(wl), wl.q, wl.kv_dtype, wl.k, wl.v, wl.kv_dtype,
-                                g_idx[rows], wl.K, wl.Hq, wl.Dqk, wl.Dv, wl.scale, rows=rows)
+                                g_idx[rows], wl.K, wl.Hq, wl.Dqk, wl.Dv, wl.scale, rows=rows,
+                                **oracle.attn_kv_args(wl))
     err = np.abs(g_out[rows] - ref)
     assert (err <= ATOL_BF16 + 0.5 * _bf16_step(ref)).all(), float(err.max())
     # the fused call writes the same bf16 values

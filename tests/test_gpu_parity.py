@@ -49,7 +49,8 @@ def _run_fused(si, dw, out_dtype=torch.float32, ws_bytes=None):
 
 def _attn_ref(wl, g_idx, rows=None):
     return oracle.sparse_attn(oracle.Batch.of(wl), wl.q, wl.kv_dtype, wl.k, wl.v, wl.kv_dtype,
-                              g_idx, wl.K, wl.Hq, wl.Dqk, wl.Dv, wl.scale, rows=rows)
+                              g_idx, wl.K, wl.Hq, wl.Dqk, wl.Dv, wl.scale, rows=rows,
+                              **oracle.attn_kv_args(wl))
 
 
 def _full_check(si, wl, atol):
@@ -112,6 +113,13 @@ def test_fp8_query_generic_shapes(si):
     """FP8 query on indexer shapes the tensor-core kernels do not take."""
     wl = synth.make("c4", n_req=5, n_prefill=1, chunk=40, ctx_lo=100, ctx_hi=1500, K=128,
                     Hi=4, Di=32, q_idx_fp8=True)
+    _full_check(si, wl, ATOL_BF16)
+
+
+def test_fp8_kv_cache(si):
+    """Latent KV rows stored as e4m3 with one scale per 128-entry tile
+    (section 5.2): the whole path against the oracle on the dequantised rows."""
+    wl = synth.make("c1", batch=3, ctx_list=[3001, 2048, 130], K=512, kv_fp8=True)
     _full_check(si, wl, ATOL_BF16)
 
 

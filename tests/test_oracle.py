@@ -350,3 +350,36 @@ def test_rows_subset_equals_full_run():
     part = oracle.run(wl, rows=rows)
     for a, c in zip(full, part):
         assert np.array_equal(a[rows], c, equal_nan=True)
+
+
+def test_fp8_kv_tiles_brute_force():
+    """FP8 KV cache with one scale per row and tile of 128 entries (the last
+    tile of a 576-entry row holds 64): the oracle's attention equals dense
+    softmax attention over the selected rows, computed here in numpy from
+    rows decoded with the format's own definition."""
+    wl = synth.make("c1", batch=2, ctx_list=[90, 40], Hi=4, Di=16, Hq=3, K=16, kv_fp8=True)
+    assert wl.kv_dtype == "e4m3" and wl.kv_scale.shape[-1] == 5 and wl.kv_scale_tile == 128
+    b = oracle.Batch.of(wl)
+    rng = np.random.default_rng(5)
+    idx = np.full((wl.n_q, wl.K), -1, dtype=np.int32)
+    for r in range(wl.n_q):
+        sel = np.sort(rng.choice(int(wl.q_pos[r]) + 1, size=wl.K - 3, replace=False))
+        idx[r, : len(sel)] = sel
+    out, lse = oracle.sparse_attn(b, wl.q, wl.kv_dtype, wl.k, None, wl.kv_dtype, idx, wl.K, wl.Hq,
+                                  wl.Dqk, wl.Dv, wl.scale, **oracle.attn_kv_args(wl))
+    q = synth._bf16_bits_to_f32(wl.q).astype(np.float64)
+    tile_of = np.arange(wl.Dqk) // 128
+    deq = _e4m3_by_definition(wl.k) * wl.kv_scale.astype(np.float64)[..., tile_of]
+    for r in range(wl.n_q):
+        sel = idx[r][idx[r] >= 0]
+        rows = np.array([deq[wl.block_table[wl.q_seq[r], s // wl.page], s % wl.page] for s in sel])
+        z = wl.scale * q[r] @ rows.T                        # [Hq, n]
+        p = np.exp(z - z.max(axis=1, keepdims=True))
+        ref = (p @ rows[:, : wl.Dv]) / p.sum(axis=1, keepdims=True)
+        assert np.abs(out[r] - ref).max() <= 1e-12 * np.abs(ref).max()
+        assert np.abs(lse[r] - (z.max(axis=1) + np.log(p.sum(axis=1)))).max() <= 1e-12
+    # a dropped tile scale (plausible slip: scales per row instead of per tile) is caught
+    out_row, _ = oracle.sparse_attn(b, wl.q, wl.kv_dtype, wl.k, None, wl.kv_dtype, idx, wl.K,
+                                    wl.Hq, wl.Dqk, wl.Dv, wl.scale, q_dtype="bf16",
+                                    kv_scale=wl.kv_scale[..., :1].copy(), scale_tile=0)
+    assert not np.allclose(out, out_row)
