@@ -90,6 +90,13 @@ typedef struct si_batch {
     int32_t max_ctx;            /* host-known bound: q_pos + 1 <= max_ctx for all
                                    rows; sizes grids, scores and workspaces */
     int32_t n_blocks;           /* physical pages in each cache */
+    const int32_t *host_q_seq;  /* optional HOST copy of q_seq [n_q], or NULL.  A
+                                   serving scheduler knows its batch: with it the
+                                   indexer sends each run of >= 64 consecutive
+                                   rows of one sequence (a prefill chunk; section
+                                   6.2) to the prefill kernel, whose key tiles
+                                   serve several rows at once.  It must match
+                                   q_seq; it is read on the host during the call. */
 } si_batch;
 
 /* One paged cache: [n_blocks, page_size, row_stride] elements of dtype.

@@ -40,7 +40,8 @@ class c_batch(ctypes.Structure):
                 ("q_seq", ctypes.c_void_p), ("q_pos", ctypes.c_void_p),
                 ("n_seq", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("n_q", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("max_ctx", ctypes.c_int32), ("n_blocks", ctypes.c_int32)]
+                ("max_ctx", ctypes.c_int32), ("n_blocks", ctypes.c_int32),
+                ("host_q_seq", ctypes.c_void_p)]
 
 
 class c_paged(ctypes.Structure):
@@ -136,11 +137,20 @@ class Batch:
     page_size: int
     max_ctx: int                # host-known bound of q_pos + 1
     n_blocks: int
+    host_q_seq: Optional[object] = None  # host int32 copy of q_seq (numpy), lets prefill
+                                         # chunks of a mixed batch take the prefill kernel
 
     def c(self) -> c_batch:
+        hq = None
+        if self.host_q_seq is not None:
+            import numpy as np
+            self._host_q_seq = np.ascontiguousarray(self.host_q_seq, dtype=np.int32)
+            if self._host_q_seq.shape[0] != self.q_pos.shape[0]:
+                raise ValueError("host_q_seq must have one entry per query row")
+            hq = self._host_q_seq.ctypes.data
         return c_batch(_ptr(self.block_table), _ptr(self.ctx_len), _ptr(self.q_seq),
                        _ptr(self.q_pos), self.ctx_len.shape[0], self.block_table.shape[1],
-                       self.q_pos.shape[0], self.page_size, self.max_ctx, self.n_blocks)
+                       self.q_pos.shape[0], self.page_size, self.max_ctx, self.n_blocks, hq)
 
 
 @dataclasses.dataclass
@@ -329,7 +339,7 @@ def upload(wl, device="cuda") -> DeviceWorkload:
     ten["kv_scale"] = None if kv_scale is None else _dev(kv_scale, device)
     tile = getattr(wl, "kv_scale_tile", 0) if kv_scale is not None else 0
     b = Batch(ten["block_table"], ten["ctx_len"], ten["q_seq"], ten["q_pos"], wl.page,
-              wl.max_ctx, wl.n_blocks)
+              wl.max_ctx, wl.n_blocks, host_q_seq=wl.q_seq)
     ix = Indexer(ten["q_idx"], wl.q_idx_dtype, ten["w"],
                  Paged(ten["k_idx"], wl.k_idx_dtype, wl.Di, ten["k_scale"]), ten["q_scale"])
     kp = Paged(ten["k"], wl.kv_dtype, wl.Dqk, ten["kv_scale"], tile)

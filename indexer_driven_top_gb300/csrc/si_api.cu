@@ -171,6 +171,7 @@ si_batch row_slice(const si_batch &b, int32_t r0, int32_t n)
     si_batch s = b;
     s.q_seq = b.q_seq + r0;
     s.q_pos = b.q_pos + r0;
+    s.host_q_seq = b.host_q_seq ? b.host_q_seq + r0 : nullptr;
     s.n_q = n;
     return s;
 }
@@ -191,14 +192,47 @@ si_indexer indexer_slice(const si_indexer &ix, int32_t r0)
 
 unsigned int *status_word(void *ws) { return reinterpret_cast<unsigned int *>(ws); }
 
+constexpr int32_t kPrefillRun = 64;  // rows of one sequence worth a prefill launch
+
+cudaError_t launch_indexer_rows(const si_batch &b, const si_indexer &ix, float *scores,
+                                int64_t ld, bool one_sequence, unsigned int *st, cudaStream_t s)
+{
+    if (one_sequence && b.n_q >= kPrefillRun && si::indexer_tc_supported(b, ix, ld))
+        return si::launch_indexer_prefill(b, ix, scores, ld, st, s);
+    return si::indexer_tc_supported(b, ix, ld) ? si::launch_indexer_tc(b, ix, scores, ld, st, s)
+                                               : si::launch_indexer_generic(b, ix, scores, ld, st, s);
+}
+
+// With a host copy of q_seq the batch is planned: each run of >= 64 rows of
+// one sequence goes to the prefill kernel, the rows between runs to the
+// decode kernels (one launch per maximal stretch).
 si_status run_indexer(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
                       unsigned int *st, cudaStream_t s)
 {
-    cudaError_t e = si::indexer_prefill_supported(b, ix, ld)
-                        ? si::launch_indexer_prefill(b, ix, scores, ld, st, s)
-                    : si::indexer_tc_supported(b, ix, ld)
-                        ? si::launch_indexer_tc(b, ix, scores, ld, st, s)
-                        : si::launch_indexer_generic(b, ix, scores, ld, st, s);
+    cudaError_t e = cudaSuccess;
+    if (!b.host_q_seq || b.n_seq == 1 || b.n_q < kPrefillRun) {
+        e = launch_indexer_rows(b, ix, scores, ld, b.n_seq == 1, st, s);
+        return e == cudaSuccess ? SI_OK : cuda_fail(e, "indexer launch");
+    }
+    const int32_t *hs = b.host_q_seq;
+    auto run_end = [&](int32_t r) {
+        int32_t e2 = r + 1;
+        while (e2 < b.n_q && hs[e2] == hs[r])
+            e2++;
+        return e2;
+    };
+    int32_t r = 0;
+    while (e == cudaSuccess && r < b.n_q) {
+        int32_t end = run_end(r);
+        const bool chunk = end - r >= kPrefillRun;
+        if (!chunk) {  // extend over short runs up to the next chunk
+            while (end < b.n_q && run_end(end) - end < kPrefillRun)
+                end = run_end(end);
+        }
+        e = launch_indexer_rows(row_slice(b, r, end - r), indexer_slice(ix, r),
+                                scores + (int64_t)r * ld, ld, chunk, st, s);
+        r = end;
+    }
     return e == cudaSuccess ? SI_OK : cuda_fail(e, "indexer launch");
 }
 

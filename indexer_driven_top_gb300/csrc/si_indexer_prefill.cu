@@ -543,13 +543,6 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
 
 }  // namespace
 
-bool indexer_prefill_supported(const si_batch &b, const si_indexer &ix, int64_t ld)
-{
-    // one sequence (so every row scores the same keys), enough rows to share
-    // tiles, and the decode indexer's operand conditions
-    return b.n_seq == 1 && b.n_q >= 64 && indexer_tc_supported(b, ix, ld);
-}
-
 cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, float *scores,
                                    int64_t ld, unsigned int *st, cudaStream_t s)
 {

@@ -32,9 +32,10 @@ bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld);
 cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
                               unsigned int *st, cudaStream_t s);
 
-// Tensor-core indexer for a causal prefill of one sequence: blocks of two
-// query rows share each key tile (same operand conditions as above).
-bool indexer_prefill_supported(const si_batch &b, const si_indexer &ix, int64_t ld);
+// Tensor-core indexer for query rows that all belong to one sequence (a
+// causal prefill or a prefill chunk): blocks of two (bf16 q) or four (FP8 q)
+// rows share each key tile.  Same operand conditions as above; the caller
+// guarantees the single sequence.
 cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, float *scores,
                                    int64_t ld, unsigned int *st, cudaStream_t s);
 

@@ -108,6 +108,25 @@ __device__ __forceinline__ void cluster_sync()
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Atomic add to / load from / store to a 32-bit word in the shared memory
+// of a CTA of this cluster (`addr` from mapa_shared).
+__device__ __forceinline__ void red_cluster_add_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Arrival on an mbarrier of another CTA of the cluster (`addr` from
 // mapa_shared), releasing this thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t addr)

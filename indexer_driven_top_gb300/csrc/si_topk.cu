@@ -9,13 +9,20 @@
 //
 // One 1024-thread CTA per query row.  Rows of up to 16384 candidates are read
 // once into registers (thread t holds E consecutive positions) and every pass
-// runs on the cached keys; longer rows stream from global memory per pass.
+// runs on the cached keys.  Rows of up to 8 x 16384 take a cluster of CTAs
+// (one 16384-position segment each, histograms merged in distributed shared
+// memory); longer rows stream from global memory per pass.
+#include <algorithm>
+
 #include "si_common.cuh"
 #include "si_internal.h"
+#include "si_sm100.cuh"
 
 namespace si {
 
 namespace {
+
+using namespace sm100;
 
 constexpr int kTopkThreads = 1024;
 constexpr int kRadixBins = 2048;
@@ -212,6 +219,139 @@ k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx
     }
 }
 
+// Long rows (16384 < n <= 16384 C): a cluster of C CTAs per row, CTA q
+// caching positions [16384 q, 16384 q + 16384) in registers.  Each radix pass
+// adds every CTA's histogram into a per-pass histogram in CTA 0's shared
+// memory (distributed shared memory atomics), and every CTA then reads the
+// merged counts and takes the same decision.  The emit pass orders the CTAs'
+// selections by their segment: CTA q writes after the selections and the
+// tie quota of CTAs 0..q-1, whose counts it reads from CTA 0.
+constexpr int kClusterE = 16;
+constexpr int kSegment = kClusterE * kTopkThreads;  // positions per CTA
+constexpr int kMaxCluster = 8;
+
+__global__ void __launch_bounds__(kTopkThreads)
+k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx)
+{
+    __shared__ uint32_t hist[kRadixBins];
+    __shared__ uint32_t merged[3][kRadixBins];   // used in CTA 0: one histogram per pass
+    __shared__ uint32_t counts[kMaxCluster][2];  // used in CTA 0: (above, ties) per CTA
+    __shared__ int sbuf[33];
+    __shared__ uint32_t sh_digit;
+    __shared__ int sh_rem;
+
+    griddep_launch_dependents();
+    const uint32_t q = cluster_rank();
+    uint32_t C;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
+    const int r = (int)(blockIdx.x / C), tid = threadIdx.x;
+    int64_t n = (int64_t)b.q_pos[r] + 1;
+    if (n > ld)
+        n = ld;
+    const float *row = scores + (int64_t)r * ld;
+    int32_t *out = idx + (int64_t)r * k_top;
+
+    if (q == 0)
+        for (int i = tid; i < 3 * kRadixBins; i += kTopkThreads)
+            (&merged[0][0])[i] = 0;
+    griddep_wait();  // the scores come from the previous kernel of the stream
+    cluster_sync();  // CTA 0's merged histograms are zero before anyone adds
+
+    if (n <= k_top) {  // everything is selected (the same on every CTA)
+        if (q == 0)
+            for (int i = tid; i < k_top; i += kTopkThreads)
+                out[i] = i < n ? i : -1;
+        cluster_sync();
+        return;
+    }
+    const int64_t p0 = (int64_t)q * kSegment + (int64_t)tid * kClusterE;
+    uint32_t key[kClusterE];
+    uint32_t valid = 0;
+    if (p0 + kClusterE <= n && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+#pragma unroll
+        for (int e = 0; e < kClusterE; e += 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(row + p0 + e));
+            key[e] = order_key(v.x);
+            key[e + 1] = order_key(v.y);
+            key[e + 2] = order_key(v.z);
+            key[e + 3] = order_key(v.w);
+        }
+        valid = 0xffffu;
+    } else {
+#pragma unroll
+        for (int e = 0; e < kClusterE; e++) {
+            const bool in = p0 + e < n;
+            key[e] = in ? order_key(__ldg(row + p0 + e)) : 0u;
+            valid |= (in ? 1u : 0u) << e;
+        }
+    }
+    const uint32_t merged0 = mapa_shared(smem_u32(&merged[0][0]), 0);
+    const uint32_t counts0 = mapa_shared(smem_u32(&counts[0][0]), 0);
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k_top;
+    for (int pass = 0; pass < 3; pass++) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nbins = pass == 2 ? 1024 : 2048;
+        for (int i = tid; i < nbins; i += kTopkThreads)
+            hist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < kClusterE; e++)
+            if (((valid >> e) & 1u) && (key[e] & mask) == prefix)
+                atomicAdd(&hist[(key[e] >> shift) & (nbins - 1)], 1u);
+        __syncthreads();
+        for (int i = tid; i < nbins; i += kTopkThreads)
+            if (hist[i])
+                red_cluster_add_u32(merged0 + (uint32_t)(pass * kRadixBins + i) * 4u, hist[i]);
+        cluster_sync();
+        for (int i = tid; i < nbins; i += kTopkThreads)
+            hist[i] = ld_cluster_u32(merged0 + (uint32_t)(pass * kRadixBins + i) * 4u);
+        __syncthreads();
+        radix_step(hist, sbuf, &sh_digit, &sh_rem, nbins, remaining);
+        prefix |= sh_digit << shift;
+        mask |= (uint32_t)(nbins - 1) << shift;
+        __syncthreads();
+    }
+    // emit
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int e = 0; e < kClusterE; e++) {
+        const bool in = (valid >> e) & 1u;
+        gt += in && key[e] > prefix;
+        eq += in && key[e] == prefix;
+    }
+    int gt_total, eq_total;
+    const int eq_before = block_exclusive_scan(eq, &eq_total, sbuf);
+    block_exclusive_scan(gt, &gt_total, sbuf);
+    if (tid == 0) {
+        st_cluster_u32(counts0 + q * 8u, (uint32_t)gt_total);
+        st_cluster_u32(counts0 + q * 8u + 4u, (uint32_t)eq_total);
+    }
+    cluster_sync();
+    // selections and tie quota of the CTAs before this one
+    int off = 0, eq_prev = 0;
+    for (uint32_t c = 0; c < q; c++) {
+        const int g = (int)ld_cluster_u32(counts0 + c * 8u);
+        const int t = (int)ld_cluster_u32(counts0 + c * 8u + 4u);
+        off += g + max(0, min(t, remaining - eq_prev));
+        eq_prev += t;
+    }
+    int take_eq = max(0, min(eq, remaining - eq_prev - eq_before));
+    int total;
+    int o = off + block_exclusive_scan(gt + take_eq, &total, sbuf);
+#pragma unroll
+    for (int e = 0; e < kClusterE; e++) {
+        const bool in = (valid >> e) & 1u;
+        const bool tie = in && key[e] == prefix;
+        const bool take = (in && key[e] > prefix) || (tie && take_eq > 0);
+        if (tie && take)
+            take_eq--;
+        if (take && o < k_top)
+            out[o++] = (int32_t)(p0 + e);
+    }
+    cluster_sync();  // CTA 0's shared memory stays until every CTA has read it
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,
@@ -222,15 +362,38 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
     // may overlap the tail of the kernel that wrote the scores (programmatic
     // dependent launch; the kernel waits for it before reading them)
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)b.n_q);
     cfg.blockDim = dim3(kTopkThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // Rows longer than one CTA's register cache take a cluster of C CTAs per
+    // row (b.max_ctx bounds every row's candidate count) when one CTA per row
+    // would leave most of the GPU idle; a batch with many rows keeps one CTA
+    // per row and streams.
+    static int sms_of[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        dev = 0;
+    if (sms_of[dev] == 0 &&
+        cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms_of[dev] = 1;
+    const int64_t longest = std::min<int64_t>(b.max_ctx, ld);
+    const int C = (int)((longest + kSegment - 1) / kSegment);
+    if (longest > 16 * kTopkThreads && C <= kMaxCluster &&
+        (int64_t)b.n_q * C <= 2 * (int64_t)sms_of[dev]) {
+        cfg.gridDim = dim3((unsigned)(b.n_q * C));
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)C;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, k_topk_cluster, b, scores, ld, k_top, idx);
+    }
+    cfg.gridDim = dim3((unsigned)b.n_q);
     return cudaLaunchKernelEx(&cfg, k_topk_rows, b, scores, ld, k_top, idx);
 }
 

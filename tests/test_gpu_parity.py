@@ -135,6 +135,34 @@ def test_mixed_ragged_batch(si):
     _full_check(si, wl, ATOL_BF16)
 
 
+def test_mixed_batch_prefill_chunks_take_prefill_kernel(si):
+    """Decode rows followed by two prefill chunks of 100 rows: with the host
+    copy of q_seq the indexer sends each chunk to the prefill kernel (one
+    launch per chunk plus one for the decode rows); the scores match the
+    unplanned single launch and the oracle."""
+    wl = synth.make("c4", n_req=6, n_prefill=2, chunk=100, ctx_lo=200, ctx_hi=3000, K=128)
+    _full_check(si, wl, ATOL_BF16)
+    dw = si.upload(wl)
+    ws = si.alloc_workspace(4096)
+    planned = torch.empty((wl.n_q, wl.max_ctx), dtype=torch.float32, device="cuda")
+    c0 = si.launch_count()
+    si.indexer_scores(dw.batch, dw.indexer, planned, ws)
+    torch.cuda.synchronize()
+    assert si.launch_count() - c0 == 3
+    import dataclasses
+    plain_b = dataclasses.replace(dw.batch, host_q_seq=None)
+    plain = torch.empty_like(planned)
+    c0 = si.launch_count()
+    si.indexer_scores(plain_b, dw.indexer, plain, ws)
+    torch.cuda.synchronize()
+    assert si.launch_count() - c0 == 1
+    assert si.workspace_status(ws) == 0
+    a, b_ = planned.cpu().numpy(), plain.cpu().numpy()
+    fin = np.isfinite(b_)
+    assert np.array_equal(np.isfinite(a), fin)
+    assert np.abs(a[fin] - b_[fin]).max() <= 1e-6 * np.abs(b_[fin]).max()
+
+
 def test_fused_small_workspace_uses_strips(si):
     wl = synth.make("c4", n_req=4, n_prefill=1, chunk=30, ctx_lo=100, ctx_hi=900, K=64)
     dw = si.upload(wl)
@@ -162,6 +190,33 @@ def test_topk_exact_on_identical_scores(si):
         idx = torch.empty((n_q, K), dtype=torch.int32, device="cuda")
         si_.topk(b, dev(sc), K, idx, ws)
         ob = oracle.Batch(np.zeros((1, 100), np.int32), [ld], np.zeros(n_q, np.int32), pos, 64)
+        want = oracle.topk(ob, sc.astype(np.float64), K)
+        assert np.array_equal(idx.cpu().numpy(), want), K
+
+
+@pytest.mark.parametrize("ld", [16385, 40000, 131072])
+def test_topk_exact_long_rows_cluster(si, ld):
+    """Rows longer than one CTA's register cache take a cluster of CTAs
+    (one 16384-position segment each): bit-exact against the oracle with heavy
+    ties spread over segments, rows that select everything, rows inside one
+    segment, and a row ending one past a segment boundary."""
+    rng = np.random.default_rng(ld)
+    n_q = 12
+    pos = np.concatenate([rng.integers(0, ld, n_q - 5),
+                          [0, 100, 16383, 16384, ld - 1]]).astype(np.int32)
+    sc = rng.integers(-30, 30, size=(n_q, ld)).astype(np.float32)   # many equal keys
+    sc[1::3] = rng.standard_normal((len(sc[1::3]), ld)).astype(np.float32)
+    sc[2, :5000] = -0.0
+    import indexer_driven_top_gb300 as si_
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    nb = (ld + 63) // 64
+    b = si_.Batch(dev(np.zeros((1, nb), np.int32)), dev(np.array([ld], np.int32)),
+                  dev(np.zeros(n_q, np.int32)), dev(pos), 64, ld, nb)
+    ws = si_.alloc_workspace(256)
+    ob = oracle.Batch(np.zeros((1, nb), np.int32), [ld], np.zeros(n_q, np.int32), pos, 64)
+    for K in (1, 77, 2048):
+        idx = torch.empty((n_q, K), dtype=torch.int32, device="cuda")
+        si_.topk(b, dev(sc), K, idx, ws)
         want = oracle.topk(ob, sc.astype(np.float64), K)
         assert np.array_equal(idx.cpu().numpy(), want), K
 
