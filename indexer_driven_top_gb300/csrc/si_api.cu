@@ -244,13 +244,15 @@ si_status run_topk(const si_batch &b, const float *scores, int64_t ld, int k_top
 }
 
 si_status run_attn(const si_batch &b, const si_attention &at, const int32_t *idx, int k_top,
-                   void *out, si_dtype odt, float *lse, unsigned int *st, cudaStream_t s)
+                   void *out, si_dtype odt, float *lse, void *scratch, size_t scratch_bytes,
+                   unsigned int *st, cudaStream_t s)
 {
     // the tensor-core kernel stores its output with the tensor engine, which
     // needs a 16-byte aligned destination
     const bool tc = si::attn_tc_supported(b, at, k_top) && ((uintptr_t)out % 16) == 0;
-    cudaError_t e = tc ? si::launch_attn_tc(b, at, idx, k_top, out, odt, lse, st, s)
-                        : si::launch_attn_generic(b, at, idx, k_top, out, odt, lse, st, s);
+    cudaError_t e = tc ? si::launch_attn_tc(b, at, idx, k_top, out, odt, lse, scratch,
+                                            scratch_bytes, st, s)
+                       : si::launch_attn_generic(b, at, idx, k_top, out, odt, lse, st, s);
     return e == cudaSuccess ? SI_OK : cuda_fail(e, "attention launch");
 }
 
@@ -275,21 +277,36 @@ si_status si::check_fused_args(const si_batch *b, const si_indexer *ix, const si
 
 namespace {
 
+// Scratch the attention's split partials would use (0 when the batch is
+// large enough to fill the GPU unsplit, or the shapes take another kernel).
+size_t attn_split_need(const si_batch *b, const si_attention *at, int32_t k_top)
+{
+    if (!at || b->n_q <= 0 || k_top < 1 || !si::attn_tc_supported(*b, *at, k_top))
+        return 0;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return round_up(si::attn_tc_split_bytes(*b, si::attn_tc_split(*b, k_top, sms)), 256);
+}
+
 size_t ws_need(si_op op, const si_batch *b, const si_indexer *ix, const si_attention *at,
                int32_t k_top, bool minimal)
 {
     (void)ix;
-    (void)at;
-    (void)k_top;
     size_t n = si::kStatusBytes;
+    size_t extra = 0;
     if (op == SI_OP_FUSED && b->n_q > 0) {
         const size_t row_bytes = (size_t)scores_ld(b) * sizeof(float);
         size_t rows = minimal ? 1 : (size_t)b->n_q;
         if (!minimal && rows * row_bytes > kFusedCap)
             rows = std::max<size_t>(1, kFusedCap / row_bytes);
-        n += round_up(rows * row_bytes, 256);
+        extra = round_up(rows * row_bytes, 256);
     }
-    return n;
+    // the full size also lets few-row attention split each row's key tiles
+    if (!minimal && (op == SI_OP_FUSED || op == SI_OP_ATTN))
+        extra = std::max(extra, attn_split_need(b, at, k_top));
+    return n + extra;
 }
 
 }  // namespace
@@ -364,8 +381,9 @@ si_status si_sparse_attn(const si_batch *b, const si_attention *at, const int32_
         return fail(SI_ERR_INVALID_ARG, "out dtype must be f32 or bf16");
     if ((st = check_ws(ws, ws_bytes, ws_need(SI_OP_ATTN, b, nullptr, at, k_top, true))) != SI_OK)
         return st;
-    return run_attn(*b, *at, idx, k_top, out, out_dtype, lse, status_word(ws),
-                    (cudaStream_t)stream);
+    return run_attn(*b, *at, idx, k_top, out, out_dtype, lse,
+                    static_cast<char *>(ws) + si::kStatusBytes, ws_bytes - si::kStatusBytes,
+                    status_word(ws), (cudaStream_t)stream);
 }
 
 si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_attention *at,
@@ -392,7 +410,10 @@ si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_atte
         if ((st = run_topk(sb, scores, ld, k_top, idx + r0 * k_top, stw, s)) != SI_OK)
             return st;
     }
-    return run_attn(*b, *at, idx, k_top, out, out_dtype, lse, stw, s);
+    // the score strip is free once every Top-K has run: it may hold the
+    // attention's split partials
+    return run_attn(*b, *at, idx, k_top, out, out_dtype, lse, scores,
+                    ws_bytes - si::kStatusBytes, stw, s);
 }
 
 si_status si_workspace_status(const void *ws, uint32_t *flags, void *stream)

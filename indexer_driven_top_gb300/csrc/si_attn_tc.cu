@@ -82,6 +82,7 @@ constexpr int kWarpRows = 17;     // score CTA: physical rows and key-valid bits
 constexpr int kConverters = 5 * 32;  // value CTA: warps 12..15 and 17
 constexpr int kThreads = 18 * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
+constexpr int kMaxSplit = 8;              // clusters per row at most
 
 // score CTA layout
 constexpr int kRingS = 5;
@@ -276,7 +277,7 @@ __device__ __forceinline__ void issue_chunk(const LoaderState &ls, uint32_t dst,
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
           si_batch b, si_attention at, const int32_t *idx, int k_top, si_dtype out_dtype,
-          float *lse, unsigned int *st)
+          float *lse, int n_split, float *part_ml, unsigned int *st)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -287,10 +288,18 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank();   // 0: score CTA, 1: value CTA
     const bool score_cta = rank == 0;
-    const int r = blockIdx.x >> 1;
+    // Cluster c handles row r = c / n_split and its key tiles
+    // [t0, t1) of split sp = c % n_split (all of them when n_split is 1).
+    const int cl = blockIdx.x >> 1;
+    const int r = cl / n_split, sp = cl % n_split;
     const int pos = __ldg(b.q_pos + r), seq = __ldg(b.q_seq + r);
-    const int n_valid = max(0, min(k_top, pos + 1));
-    const int T = (n_valid + kTile - 1) / kTile;  // key tiles
+    const int n_row = max(0, min(k_top, pos + 1));
+    const int T_row = (n_row + kTile - 1) / kTile;
+    const int t0 = (int)((int64_t)T_row * sp / n_split);
+    const int T = (int)((int64_t)T_row * (sp + 1) / n_split) - t0;  // key tiles of this split
+    const int n_valid = max(0, min(n_row - t0 * kTile, T * kTile));
+    const int32_t *idx_s = idx + (int64_t)r * k_top + (int64_t)t0 * kTile;
+    const bool split = n_split > 1;
 
     if (tid == 0) {
         for (int i = 0; i < kRingS; i++) {
@@ -377,7 +386,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                 cp_async_arrive(bars + B_FULL + slot);
             }
         } else {
-            loader_init(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0);
+            loader_init(ls, b, idx_s, 0, k_top, T, n_valid, seq, pos, kr0);
             const int n_groups = kVGroups * T;
             for (int g = 0; g < n_groups; g++) {
                 const int slot = g % kRingV, tile = g / kVGroups, j = g % kVGroups;
@@ -386,7 +395,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     break;
                 if (tile > ls.have_tile) {
                     activate_tile(ls, b, pos, u, st, tile);
-                    advance_lookahead(ls, b, idx, r, k_top, T, n_valid, seq, pos, kr0, tile);
+                    advance_lookahead(ls, b, idx_s, 0, k_top, T, n_valid, seq, pos, kr0, tile);
                 }
                 const uint32_t dst = base + kOffRingV + slot * kGroup;
                 issue_chunk(ls, dst, kv, row_bytes, tile, 2 * j, kr0, u);
@@ -602,9 +611,15 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                         ok = false;
                 st_cluster_f32(peer_f + ((T % kPBufs) * kHeads + h) * 4, ok ? l : 0.f);
                 mbar_arrive_remote(peer_final);
-                if (lse)
+                if (split) {
+                    // this split's softmax state, for the combine kernel
+                    float *ml = part_ml + ((int64_t)cl * kHeads + h) * 2;
+                    ml[0] = (ok && l > 0.f) ? m_used : -INFINITY;
+                    ml[1] = ok ? l : 0.f;
+                } else if (lse) {
                     lse[(int64_t)r * kHeads + h] =
                         (ok && l > 0.f) ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+                }
             }
         }
         if (warp == kWarpRows) {
@@ -619,33 +634,33 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                 if (t >= kRowSlots &&
                     !mbar_wait(bars + B_MEMPTY + rs, (uint32_t)((t / kRowSlots) - 1) & 1, st))
                     break;
-                int sp[4], blk[4];
+                int sv[4], blk[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     const int j = t * kTile + 32 * i + lane;
-                    sp[i] = j < n_valid ? __ldg(idx + (int64_t)r * k_top + j) : -1;
+                    sv[i] = j < n_valid ? __ldg(idx_s + j) : -1;
                 }
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     blk[i] = -1;
-                    if (sp[i] >= 0 && sp[i] <= pos && (unsigned)seq < (unsigned)b.n_seq &&
-                        sp[i] / b.page_size < b.max_blocks)
+                    if (sv[i] >= 0 && sv[i] <= pos && (unsigned)seq < (unsigned)b.n_seq &&
+                        sv[i] / b.page_size < b.max_blocks)
                         blk[i] = __ldg(b.block_table + (int64_t)seq * b.max_blocks +
-                                       sp[i] / b.page_size);
+                                       sv[i] / b.page_size);
                 }
                 uint32_t word = 0;
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     bool ok = false;
-                    if (sp[i] >= 0 && sp[i] <= pos) {
+                    if (sv[i] >= 0 && sv[i] <= pos) {
                         ok = (unsigned)blk[i] < (unsigned)b.n_blocks;
                         if (!ok)
                             raise_flag(st, SI_DEVFLAG_BAD_BLOCK);
-                    } else if (sp[i] != -1) {
+                    } else if (sv[i] != -1) {
                         raise_flag(st, SI_DEVFLAG_BAD_INDEX);
                     }
                     rows[rs * kTile + 32 * i + lane] =
-                        ok ? blk[i] * b.page_size + sp[i] % b.page_size : -1;
+                        ok ? blk[i] * b.page_size + sv[i] % b.page_size : -1;
                     const uint32_t w = __ballot_sync(0xffffffffu, ok);
                     if (lane == i)
                         word = w;
@@ -731,9 +746,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
             const float *fac = reinterpret_cast<const float *>(gbase + kOffF);
             const bool good = !bad && T > 0;
             const float lsum = fac[(T % kPBufs) * kHeads + h];
-            const float inv = (good && lsum > 0.f) ? 1.f / lsum : 0.f;
+            // a split writes its unnormalised O (fp32); the combine divides
+            const float inv = split ? 1.f : (good && lsum > 0.f) ? 1.f / lsum : 0.f;
             const uint32_t stage = base + kOffRingV + (uint32_t)(warp - kWarpQuad) * kEpiBufs * 4096u;
-            const int orow = r * kHeads + quarter * 32;
+            const int orow = cl * kHeads + quarter * 32;
             const bool f32 = out_dtype == SI_F32;
             const int nblk = f32 ? 8 : 4;  // 32 fp32 or 64 bf16 columns per block
 #pragma unroll 1
@@ -800,7 +816,87 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
     cluster_sync();  // neither CTA leaves while the other may still write into it
 }
 
+// Merges the splits of each row: with per-split state (m_s, l_s) in log2
+// units and unnormalised O_s, out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s
+// with M = max m_s.  One warp per (row, head), 16 of the 512 dims per lane.
+constexpr int kCombineHeads = 8;  // heads per 256-thread block
+
+__global__ void __launch_bounds__(kCombineHeads * 32)
+k_attn_combine(int n_split, const float *part_o, const float *part_ml, void *out,
+               si_dtype out_dtype, float *lse)
+{
+    griddep_wait();  // the partial results come from the previous kernel
+    const int r = blockIdx.x, h = blockIdx.y * kCombineHeads + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    float M = -INFINITY;
+    for (int s = 0; s < n_split; s++) {
+        const float *ml = part_ml + (((int64_t)r * n_split + s) * kHeads + h) * 2;
+        if (ml[1] > 0.f)
+            M = fmaxf(M, ml[0]);
+    }
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++)
+        acc[i] = 0.f;
+    float L = 0.f;
+    for (int s = 0; s < n_split; s++) {
+        const float *ml = part_ml + (((int64_t)r * n_split + s) * kHeads + h) * 2;
+        const float l = ml[1];
+        if (!(l > 0.f))
+            continue;
+        const float wgt = exp2f(ml[0] - M);
+        L += wgt * l;
+        const float4 *o4 = reinterpret_cast<const float4 *>(
+            part_o + (((int64_t)r * n_split + s) * kHeads + h) * kDv + lane * 16);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float4 v = o4[i];
+            acc[4 * i] += wgt * v.x;
+            acc[4 * i + 1] += wgt * v.y;
+            acc[4 * i + 2] += wgt * v.z;
+            acc[4 * i + 3] += wgt * v.w;
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int64_t obase = ((int64_t)r * kHeads + h) * kDv + lane * 16;
+    if (out_dtype == SI_F32) {
+        float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(out) + obase);
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            d[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv,
+                               acc[4 * i + 3] * inv);
+    } else {
+        uint4 *d = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(out) + obase);
+#pragma unroll
+        for (int i = 0; i < 2; i++)
+            d[i] = make_uint4(pack_bf16x2(acc[8 * i] * inv, acc[8 * i + 1] * inv),
+                              pack_bf16x2(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
+                              pack_bf16x2(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
+                              pack_bf16x2(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
+    }
+    if (lse && lane == 0)
+        lse[(int64_t)r * kHeads + h] =
+            L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+}
+
 }  // namespace
+
+int attn_tc_split(const si_batch &b, int k_top, int sms)
+{
+    if (b.n_q <= 0 || sms <= 0)
+        return 1;
+    const int tiles = (k_top + kTile - 1) / kTile;
+    const int s = sms / (2 * b.n_q);  // fill the GPU with clusters of two
+    return std::max(1, std::min(std::min(s, tiles), kMaxSplit));
+}
+
+size_t attn_tc_split_bytes(const si_batch &b, int n_split)
+{
+    if (n_split <= 1)
+        return 0;
+    // unnormalised O (fp32 [128 x 512]) and (m, l) per head, per row and split
+    return (size_t)b.n_q * n_split * ((size_t)kHeads * kDv * 4 + (size_t)kHeads * 8);
+}
 
 bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top)
 {
@@ -816,11 +912,12 @@ bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top)
 }
 
 cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int32_t *idx,
-                           int k_top, void *out, si_dtype out_dtype, float *lse, unsigned int *st,
-                           cudaStream_t s)
+                           int k_top, void *out, si_dtype out_dtype, float *lse, void *scratch,
+                           size_t scratch_bytes, unsigned int *st, cudaStream_t s)
 {
     static std::once_flag once[kMaxDevices];
     static cudaError_t err_of[kMaxDevices];
+    static int sms_of[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -828,29 +925,42 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     std::call_once(once[dev], [dev] {
-        err_of[dev] = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kSmemBytes);
+        cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
+        err_of[dev] = r;
     });
     if (err_of[dev] != cudaSuccess)
         return err_of[dev];
     if (b.n_q <= 0)
         return cudaSuccess;
-    // q [n_q * 128 rows x 1152 bytes] read as [128 x 128-byte] boxes; out
-    // [n_q * 128 rows x 512 elements] written as [32 x 128-byte] boxes
+    // Few rows: each row's key tiles are split over several clusters (when the
+    // scratch holds their partial results) and a combine kernel merges them.
+    int n_split = attn_tc_split(b, k_top, sms_of[dev]);
+    const size_t need = attn_tc_split_bytes(b, n_split);
+    if (n_split > 1 && (!scratch || scratch_bytes < need || ((uintptr_t)scratch % 256) != 0))
+        n_split = 1;
+    float *part_o = static_cast<float *>(scratch);
+    float *part_ml = n_split > 1 ? part_o + (size_t)b.n_q * n_split * kHeads * kDv : nullptr;
+    // q [n_q * 128 rows x 1152 bytes] read as [128 x 128-byte] boxes; out (or
+    // the splits' fp32 O) [rows x 512 elements] written as [32 x 128-byte] boxes
     CUtensorMap qmap, omap;
     const uint64_t rows = (uint64_t)b.n_q * kHeads;
     e = make_tmap_2d_u8_sw128(&qmap, at.q, kDqk * 2, rows, kDqk * 2, 128, kHeads);
     if (e != cudaSuccess)
         return e;
-    const uint64_t orow_bytes = (uint64_t)kDv * (out_dtype == SI_F32 ? 4 : 2);
-    e = make_tmap_2d_u8_sw128(&omap, out, orow_bytes, rows, orow_bytes, 128, 32);
+    const si_dtype kdt = n_split > 1 ? SI_F32 : out_dtype;
+    const uint64_t orow_bytes = (uint64_t)kDv * (kdt == SI_F32 ? 4 : 2);
+    e = make_tmap_2d_u8_sw128(&omap, n_split > 1 ? static_cast<void *>(part_o) : out, orow_bytes,
+                              rows * n_split, orow_bytes, 128, 32);
     if (e != cudaSuccess)
         return e;
     count_launch();
     // may overlap the tail of the kernel that wrote idx (programmatic
     // dependent launch; the kernel waits for it before reading idx)
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * b.n_q));
+    cfg.gridDim = dim3((unsigned)(2 * b.n_q * n_split));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
@@ -859,7 +969,17 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_attn_tc, qmap, omap, b, at, idx, k_top, out_dtype, lse, st);
+    e = cudaLaunchKernelEx(&cfg, k_attn_tc, qmap, omap, b, at, idx, k_top, kdt, lse, n_split,
+                           part_ml, st);
+    if (e != cudaSuccess || n_split == 1)
+        return e;
+    count_launch();
+    cudaLaunchConfig_t c2 = cfg;
+    c2.gridDim = dim3((unsigned)b.n_q, kHeads / kCombineHeads);
+    c2.blockDim = dim3(kCombineHeads * 32);
+    c2.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&c2, k_attn_combine, n_split, (const float *)part_o,
+                              (const float *)part_ml, out, out_dtype, lse);
 }
 
 }  // namespace si

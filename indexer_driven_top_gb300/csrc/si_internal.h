@@ -41,9 +41,13 @@ cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, floa
 
 // Tensor-core sparse attention: bf16, 128 heads, 576-dim latent rows (V = first 512).
 bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top);
+// Splits of one row's key tiles over clusters for a batch of b.n_q rows on
+// `sms` SMs, and the scratch their partial results need (0 when unsplit).
+int attn_tc_split(const si_batch &b, int k_top, int sms);
+size_t attn_tc_split_bytes(const si_batch &b, int n_split);
 cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int32_t *idx,
-                           int k_top, void *out, si_dtype out_dtype, float *lse, unsigned int *st,
-                           cudaStream_t s);
+                           int k_top, void *out, si_dtype out_dtype, float *lse, void *scratch,
+                           size_t scratch_bytes, unsigned int *st, cudaStream_t s);
 
 // Radix select of the k_top best scores per row.
 cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,

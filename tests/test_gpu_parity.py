@@ -163,6 +163,39 @@ def test_mixed_batch_prefill_chunks_take_prefill_kernel(si):
     assert np.abs(a[fin] - b_[fin]).max() <= 1e-6 * np.abs(b_[fin]).max()
 
 
+def test_attention_split_matches_unsplit(si):
+    """A few decode rows: with a full workspace each row's key tiles are
+    split over several clusters and merged by the combine kernel (two
+    launches); with the minimal workspace one cluster takes the whole row
+    (one launch).  Both match the oracle, and each other."""
+    wl = synth.make("c1", batch=3, ctx_list=[9000, 3001, 300], K=2048)
+    dw = si.upload(wl)
+    b = dw.batch
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, dw.indexer, dw.attention, wl.K))
+    sc = torch.empty((wl.n_q, b.max_ctx), dtype=torch.float32, device="cuda")
+    idx = torch.empty((wl.n_q, wl.K), dtype=torch.int32, device="cuda")
+    si.indexer_scores(b, dw.indexer, sc, ws)
+    si.topk(b, sc, wl.K, idx, ws)
+    outs, lses, launches = [], [], []
+    for nbytes in (si.workspace_size(si.OP_ATTN, b, None, dw.attention, wl.K),
+                   si.workspace_min(si.OP_ATTN, b, None, dw.attention, wl.K)):
+        w = si.alloc_workspace(nbytes)
+        out = torch.empty((wl.n_q, 128, 512), dtype=torch.float32, device="cuda")
+        lse = torch.empty((wl.n_q, 128), dtype=torch.float32, device="cuda")
+        c0 = si.launch_count()
+        si.sparse_attn(b, dw.attention, idx, wl.K, out, w, lse=lse)
+        torch.cuda.synchronize()
+        launches.append(si.launch_count() - c0)
+        assert si.workspace_status(w) == 0
+        outs.append(out.cpu().numpy())
+        lses.append(lse.cpu().numpy())
+    assert launches == [2, 1]
+    ref, ref_lse = _attn_ref(wl, idx.cpu().numpy())
+    for o, l in zip(outs, lses):
+        assert max_abs(o, ref) <= ATOL_BF16 and max_abs(l, ref_lse) <= ATOL_BF16
+    assert max_abs(outs[0], outs[1]) <= 1e-3
+
+
 def test_fused_small_workspace_uses_strips(si):
     wl = synth.make("c4", n_req=4, n_prefill=1, chunk=30, ctx_lo=100, ctx_hi=900, K=64)
     dw = si.upload(wl)
