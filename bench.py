@@ -152,13 +152,18 @@ def whole_job_rate(world: int, n_q: int, ms_per_step: float) -> float:
     return world * n_q / (ms_per_step / 1e3)
 
 
-def _kernel_traffic(kernel: str, source: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel's
-    source is unchanged since the counters were taken; else None."""
+# Workload names of the committed ncu captures (profiles/*.md).
+PROFILE_WORKLOAD = {"c1": "decode b64 ctx8192", "c3": "decode b16 ctx131072"}
+
+
+def _kernel_traffic(kernel: str, source: str, workload: str):
+    """DRAM bytes per launch from the committed ncu capture of this kernel on
+    this workload, if the kernel's source is unchanged since the counters
+    were taken; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f).get(kernel)
+            rec = json.load(f).get(f"{kernel}@{PROFILE_WORKLOAD.get(workload, workload)}")
         with open(os.path.join(ROOT, "indexer_driven_top_gb300", "csrc", source), "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
         if rec and rec.get("source_sha") == sha:
@@ -525,7 +530,7 @@ def run_si(args):
     roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "peak_src": peaks["src"] + " (hbm_gbs, copy)",
-            "traffic": _kernel_traffic(kname, src),
+            "traffic": _kernel_traffic(kname, src, wl.name),
             "algorithmic_bytes_per_launch": algo[dom], "ms_per_launch": mean_k[dom]}
     total_bytes = algo["indexer"] + algo["topk"] + algo["attn"]
     step_gbs = total_bytes / (ms / 1e3) / 1e9
