@@ -54,12 +54,15 @@ def algorithmic_bytes(wl, out_bytes=2):
              output (`out_bytes` per element) and the indices read."""
     n_keys = int((wl.q_pos.astype("int64") + 1).sum())
     n_sel = int(sum(min(wl.K, int(p) + 1) for p in wl.q_pos))
-    esz = 2 if wl.kv_dtype == "bf16" else 4
+    esz = {"bf16": 2, "e4m3": 1}.get(wl.kv_dtype, 4)
+    kv_scale_b = 0 if getattr(wl, "kv_scale", None) is None else wl.kv_scale.shape[-1] * 4
     kesz = 1 if wl.k_idx_dtype == "e4m3" else 4
     idx_b = n_keys * (wl.Di * kesz + (4 if wl.k_scale is not None else 0)) \
         + wl.n_q * (wl.Hi * wl.Di * 2 + wl.Hi * 4) + n_keys * 4
     topk_b = n_keys * 4 + wl.n_q * wl.K * 4
-    attn_b = n_sel * wl.Dqk * esz + wl.n_q * wl.Hq * wl.Dqk * esz + wl.n_q * wl.Hq * wl.Dv * out_bytes \
+    qesz = 2 if (getattr(wl, "attn_q_dtype", "") or wl.kv_dtype) == "bf16" else 4
+    attn_b = n_sel * (wl.Dqk * esz + kv_scale_b) + wl.n_q * wl.Hq * wl.Dqk * qesz \
+        + wl.n_q * wl.Hq * wl.Dv * out_bytes \
         + wl.n_q * wl.K * 4
     flops_idx = 2 * n_keys * wl.Hi * wl.Di
     flops_attn = 2 * n_sel * wl.Hq * (wl.Dqk + wl.Dv)
@@ -179,7 +182,7 @@ def _kernel_of(wl):
     (64 x 128 indexer with bf16 q and e4m3 keys; 128 heads x 576 bf16 latent
     rows), the generic ones otherwise."""
     tc_ix = wl.Hi == 64 and wl.Di == 128 and wl.q_idx_dtype == "bf16" and wl.k_idx_dtype == "e4m3"
-    tc_at = wl.Hq == 128 and wl.Dqk == 576 and wl.Dv == 512 and wl.kv_dtype == "bf16"
+    tc_at = wl.Hq == 128 and wl.Dqk == 576 and wl.Dv == 512 and wl.kv_dtype in ("bf16", "e4m3")
     prefill = tc_ix and wl.n_seq == 1 and wl.n_q >= 64
     return {"indexer": ("k_indexer_prefill", "si_indexer_prefill.cu") if prefill
             else ("k_indexer_tc", "si_indexer_tc.cu") if tc_ix
@@ -397,7 +400,8 @@ def run_si(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    wl = synth.make(args.workload, seed=rank_seed(args.workload, rank))
+    wl = synth.make(args.workload, seed=rank_seed(args.workload, rank),
+                    **({"kv_fp8": True} if args.kv_fp8 else {}))
     dw = si.upload(wl, dev)
     b, ix, at, K = dw.batch, dw.indexer, dw.attention, dw.k_top
     n_q = wl.n_q
@@ -549,8 +553,9 @@ def run_si(args):
         "data": "synthetic",
         "config": {"workload": _workload_name(wl), "batch": n_q, "context": ld, "top_k": K,
                    "indexer": f"{wl.Hi}x{wl.Di} e4m3 keys + fp32 scale, bf16 q",
-                   "attention": f"{wl.Hq} heads x {wl.Dqk} (v {wl.Dv}) bf16, fp32 accumulate, "
-                                f"{OUT_DTYPE} out",
+                   "attention": f"{wl.Hq} heads x {wl.Dqk} (v {wl.Dv}) "
+                                f"{'e4m3 cache + fp32 scale per 128-entry tile, bf16 q' if args.kv_fp8 else 'bf16'}, "
+                                f"fp32 accumulate, {OUT_DTYPE} out",
                    "page": wl.page, "l2": "flushed between steps (512 MiB write)",
                    "step": "si_indexer_scores + si_topk + si_sparse_attn",
                    "parallelism": f"dp{world} (independent requests per rank)"},
@@ -581,6 +586,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end legs")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="store the latent KV cache in FP8 (one scale per row and 128-entry tile)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill indexer (both query formats) and print its record")
     args = ap.parse_args()

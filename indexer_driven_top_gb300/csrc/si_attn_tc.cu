@@ -46,6 +46,7 @@
 // 0..pos get zero rows and zero weight.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include <algorithm>
@@ -99,8 +100,31 @@ constexpr uint32_t kOffRingV = kPBufs * 2 * kChunk;            // kRingV x (2 x 
 constexpr uint32_t kOffF = kOffRingV + kRingV * kGroup;        // kPBufs x 128 floats
 constexpr int kEpiBufs = 4;  // epilogue staging: 4 KB boxes per epilogue warp, in the value ring
 static_assert(8 * kEpiBufs * 4096 <= kRingV * kGroup, "epilogue staging fits the value ring");
+// FP8 KV cache (e4m3 rows of 576 codes, one fp32 scale per row and tile of
+// 128 entries): the score CTA dequantises each gathered chunk into an f16
+// ring slot itself, the value CTA's converters dequantise staged groups.
+constexpr int kKvTiles = 5;                                    // scales per 576-entry row
+constexpr int kRing8 = 3;                                      // score: f16 chunk slots
+constexpr int kStg8 = 3;                                       // score: fp8 chunk staging slots
+static_assert(kStg8 <= 5 && kRing8 <= 5, "barrier arrays");
+constexpr uint32_t kStgBytes8 = kTile * 64;                    // 128 keys x 64 codes
+constexpr uint32_t kOffRing8 = kQChunks * kChunk;
+constexpr uint32_t kOffStg8 = kOffRing8 + kRing8 * kChunk;
+constexpr uint32_t kOffScl8 = kOffStg8 + kStg8 * kStgBytes8;   // [row slot][tile][128] fp32
+constexpr uint32_t kOffRows8 = kOffScl8 + kRowSlots * kKvTiles * kTile * 4;
+constexpr uint32_t kOffMask8 = kOffRows8 + kRowSlots * kTile * 4;
+constexpr int kVStg8 = 3;                                      // value: fp8 group staging slots
+constexpr int kVRing8 = 3;                                     // value: f16 group slots
+constexpr uint32_t kVStgBytes8 = kTile * 128 + kTile * 4;      // codes + one scale per key
+constexpr uint32_t kOffVStg8 = kPBufs * 2 * kChunk;
+constexpr uint32_t kOffVRing8 = (kOffVStg8 + kVStg8 * kVStgBytes8 + 1023u) & ~1023u;
+constexpr uint32_t kOffF8 = kOffVRing8 + kVRing8 * kGroup;
+static_assert(kOffVStg8 == kOffRingV && kOffF8 - kOffVStg8 >= 8 * kEpiBufs * 4096,
+              "epilogue staging fits the FP8 value buffers");
 // both
-constexpr uint32_t kOffBar = std::max(kOffF + kPBufs * kHeads * 4, kOffMask + kRowSlots * 16);
+constexpr uint32_t kOffBar = std::max(
+    std::max(kOffF + kPBufs * kHeads * 4, kOffMask + kRowSlots * 16),
+    std::max(kOffF8 + kPBufs * kHeads * 4, kOffMask8 + kRowSlots * 16));
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;          // + alignment slack
 static_assert(kOffMask + kRowSlots * 16 <= kOffBar, "score scratch overlaps the barriers");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -121,9 +145,13 @@ enum : int {
     B_PVDONE = 31,  // value: P.V of a tile complete
     B_FINAL = 32,   // value: row sums l written (remote arrivals)
     B_MEMPTY = 33,  // [2] score: loaders and softmax done with a tile's row table / words
-    B_COUNT = 35
+    B_QCONV = 35,   // score, FP8 cache: query converted to f16
+    B_F16E = 36,    // [3] value, FP8 cache: f16 group slot consumed (MMA commit)
+    B_STF8 = 39,    // [kStg8] score, FP8 cache: staging slot landed (cp.async arrivals)
+    B_STE8 = 44,    // [kStg8] score, FP8 cache: staging slot dequantised
+    B_COUNT = 49
 };
-constexpr uint32_t kTmemSlot = 8 * 40;  // byte offset of the TMEM base within the barrier area
+constexpr uint32_t kTmemSlot = 8 * 50;  // byte offset of the TMEM base within the barrier area
 static_assert(B_COUNT * 8 <= (int)kTmemSlot, "barrier area");
 
 // 2^x with the hardware approximation (ex2.approx: ~2 ulp, subnormal
@@ -152,6 +180,33 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
 {
     return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Two e4m3 codes (low byte first) times a scale, as two f16 (low, high).
+// The decode is exact; the product is rounded once to f16.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint32_t codes2, float sc)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)codes2, __NV_E4M3);
+    return pack_f16x2(__half2float(__ushort_as_half(h.x)) * sc,
+                      __half2float(__ushort_as_half(h.y)) * sc);
+}
+
+// 16 codes (one 16-byte unit) -> 16 f16 in two 16-byte units at dst0, dst1.
+__device__ __forceinline__ void dequant16(uint4 c, float sc, uint32_t dst0, uint32_t dst1)
+{
+    st_shared_v4(dst0, e4m3x2_scaled_f16x2(c.x & 0xFFFFu, sc), e4m3x2_scaled_f16x2(c.x >> 16, sc),
+                 e4m3x2_scaled_f16x2(c.y & 0xFFFFu, sc), e4m3x2_scaled_f16x2(c.y >> 16, sc));
+    st_shared_v4(dst1, e4m3x2_scaled_f16x2(c.z & 0xFFFFu, sc), e4m3x2_scaled_f16x2(c.z >> 16, sc),
+                 e4m3x2_scaled_f16x2(c.w & 0xFFFFu, sc), e4m3x2_scaled_f16x2(c.w >> 16, sc));
+}
+
+// 4-byte global -> shared copy, asynchronous like cp_async_16 (zeros when
+// src_bytes = 0).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
 }
 
 // 16-byte global -> shared copy that lands asynchronously; src_bytes = 0
@@ -274,6 +329,7 @@ __device__ __forceinline__ void issue_chunk(const LoaderState &ls, uint32_t dst,
     }
 }
 
+template <bool KV8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
           si_batch b, si_attention at, const int32_t *idx, int k_top, si_dtype out_dtype,
@@ -303,10 +359,19 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
 
     if (tid == 0) {
         for (int i = 0; i < kRingS; i++) {
-            mbar_init(bars + B_FULL + i, kLoaders);
-            mbar_init(bars + B_EMPTY + i, 1);
+            // FP8 score ring slots are filled by the 128 dequantising threads
+            mbar_init(bars + B_FULL + i, (KV8 && score_cta) ? kLoaders / 2 : kLoaders);
+            // FP8 value staging is released by the converters, rings by the MMA
+            mbar_init(bars + B_EMPTY + i, (KV8 && !score_cta) ? kConverters : 1);
             mbar_init(bars + B_CONV + i, kConverters);
         }
+        for (int i = 0; i < kVRing8; i++)
+            mbar_init(bars + B_F16E + i, 1);
+        for (int i = 0; i < kStg8; i++) {
+            mbar_init(bars + B_STF8 + i, kLoaders / 2);
+            mbar_init(bars + B_STE8 + i, kLoaders / 2);
+        }
+        mbar_init(bars + B_QCONV, kSoftmax);
         for (int i = 0; i < 2; i++) {
             mbar_init(bars + B_SFULL + i, 1);
             mbar_init(bars + B_SEMPTY + i, kSoftmax);
@@ -345,7 +410,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
     griddep_wait();
 
     const uint8_t *kv = static_cast<const uint8_t *>(at.k.data);
-    const int64_t row_bytes = at.k.row_stride * 2;
+    const int64_t row_bytes = at.k.row_stride * (KV8 ? 1 : 2);
     // value-CTA buffers as seen from the score CTA
     const uint32_t peer_p = mapa_shared(base + kOffP, 1);
     const uint32_t peer_f = mapa_shared(base + kOffF, 1);
@@ -357,7 +422,72 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
         // Thread t owns 16-byte unit u = t & 7 of key rows (t >> 3) + 32 i.
         const int u = tid & 7, kr0 = tid >> 3;
         LoaderState ls;
-        if (score_cta) {
+        if (KV8 && score_cta) {
+            // FP8 cache.  Warps 0..3 gather: per dim chunk, thread i copies the
+            // 16-code parts (i & 3) of keys (i >> 2) + 32 m, m < 4, into an fp8
+            // staging slot.  Warps 4..7 dequantise the same pieces of each
+            // landed staging slot into the chunk's f16 ring slot.
+            const int li = tid & 127, part = li & 3, k0 = li >> 2;
+            const int *rows = reinterpret_cast<const int *>(gbase + kOffRows8);
+            const float *scl = reinterpret_cast<const float *>(gbase + kOffScl8);
+            const int n_chunks = kQChunks * T;
+            if (warp < kLoaderWarps / 2) {
+                int rw[4] = {-1, -1, -1, -1};
+                int have_tile = -1;
+                for (int g = 0; g < n_chunks; g++) {
+                    const int tile = g / kQChunks, c = g % kQChunks, s8 = g % kStg8;
+                    if (g >= kStg8 &&
+                        !mbar_wait(bars + B_STE8 + s8, (uint32_t)((g / kStg8) - 1) & 1, st))
+                        break;
+                    if (tile > have_tile) {
+                        const int rs = tile % kRowSlots;
+                        if (!mbar_wait(bars + B_MASK + rs, (uint32_t)(tile / kRowSlots) & 1, st))
+                            break;
+                        have_tile = tile;
+#pragma unroll
+                        for (int m = 0; m < 4; m++)
+                            rw[m] = rows[rs * kTile + k0 + 32 * m];
+                        mbar_arrive(bars + B_MEMPTY + rs);
+                    }
+                    const uint32_t sdst = base + kOffStg8 + s8 * kStgBytes8 + part * 16;
+                    const int64_t col = c * 64 + part * 16;
+#pragma unroll
+                    for (int m = 0; m < 4; m++)
+                        cp_async_16(sdst + (k0 + 32 * m) * 64,
+                                    rw[m] >= 0 ? kv + (int64_t)rw[m] * row_bytes + col : kv,
+                                    rw[m] >= 0 ? 16u : 0u);
+                    cp_async_arrive(bars + B_STF8 + s8);
+                }
+            } else {
+                for (int g = 0; g < n_chunks; g++) {
+                    const int tile = g / kQChunks, c = g % kQChunks, rs = tile % kRowSlots;
+                    const int s8 = g % kStg8, slot = g % kRing8;
+                    // the tile's scales: its row-table phase (already complete, and
+                    // not yet reusable before this group's MEMPTY arrival)
+                    if ((c == 0 &&
+                         !mbar_wait(bars + B_MASK + rs, (uint32_t)(tile / kRowSlots) & 1, st)) ||
+                        !mbar_wait(bars + B_STF8 + s8, (uint32_t)(g / kStg8) & 1, st) ||
+                        (g >= kRing8 &&
+                         !mbar_wait(bars + B_EMPTY + slot, (uint32_t)((g / kRing8) - 1) & 1, st)))
+                        break;
+                    const uint32_t ssrc = base + kOffStg8 + s8 * kStgBytes8 + part * 16;
+                    const uint32_t dst = base + kOffRing8 + slot * kChunk;
+                    const float *sc_t = scl + (rs * kKvTiles + c / 2) * kTile;
+#pragma unroll
+                    for (int m = 0; m < 4; m++) {
+                        const int key = k0 + 32 * m;
+                        dequant16(ld_shared_v4(ssrc + key * 64), sc_t[key],
+                                  dst + sw128_offset(key, 2 * part),
+                                  dst + sw128_offset(key, 2 * part + 1));
+                    }
+                    fence_async_smem();
+                    mbar_arrive(bars + B_FULL + slot);
+                    mbar_arrive(bars + B_STE8 + s8);
+                    if (c == kQChunks - 1)
+                        mbar_arrive(bars + B_MEMPTY + rs);  // done with the tile's scales
+                }
+            }
+        } else if (score_cta) {
             // physical rows come from the row table the row warp fills
             const int *rows = reinterpret_cast<const int *>(gbase + kOffRows);
             ls.have_tile = -1;
@@ -385,6 +515,37 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                 issue_chunk(ls, base + kOffRingS + slot * kChunk, kv, row_bytes, tile, c, kr0, u);
                 cp_async_arrive(bars + B_FULL + slot);
             }
+        } else if (KV8) {
+            // value CTA, FP8 cache: unit u of group j's 128 codes per key into
+            // a staging slot; lane u == 0 also copies its keys' scales of tile j
+            loader_init(ls, b, idx_s, 0, k_top, T, n_valid, seq, pos, kr0);
+            const float *kscale = at.k.scale;
+            const int n_groups = kVGroups * T;
+            for (int g = 0; g < n_groups; g++) {
+                const int slot = g % kVStg8, tile = g / kVGroups, j = g % kVGroups;
+                if (g >= kVStg8 &&
+                    !mbar_wait(bars + B_EMPTY + slot, (uint32_t)((g / kVStg8) - 1) & 1, st))
+                    break;
+                if (tile > ls.have_tile) {
+                    activate_tile(ls, b, pos, u, st, tile);
+                    advance_lookahead(ls, b, idx_s, 0, k_top, T, n_valid, seq, pos, kr0, tile);
+                }
+                const uint32_t dst = base + kOffVStg8 + slot * kVStgBytes8;
+                const bool odd = tile & 1;
+#pragma unroll
+                for (int i = 0; i < kR; i++) {
+                    const int key = kr0 + (kTile / kR) * i;
+                    const int row = odd ? ls.rb1[i] : ls.rb0[i];
+                    cp_async_16(dst + key * 128 + u * 16,
+                                row >= 0 ? kv + (int64_t)row * row_bytes + j * 128 + u * 16 : kv,
+                                row >= 0 ? 16u : 0u);
+                    if (u == 0)
+                        cp_async_4(dst + kTile * 128 + key * 4,
+                                   row >= 0 ? kscale + (int64_t)row * kKvTiles + j : kscale,
+                                   row >= 0 ? 4u : 0u);
+                }
+                cp_async_arrive(bars + B_FULL + slot);
+            }
         } else {
             loader_init(ls, b, idx_s, 0, k_top, T, n_valid, seq, pos, kr0);
             const int n_groups = kVGroups * T;
@@ -407,22 +568,25 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA
         if (score_cta) {
-            const uint32_t idesc = idesc_f16(kHeads, kTile, 1, 0, 0);  // bf16, K-major A/B
-            bool ok = mbar_wait(bars + B_QREADY, 0, st);
+            // bf16 (or, for an FP8 cache, f16 query and dequantised keys), K-major
+            const uint32_t idesc = idesc_f16(kHeads, kTile, KV8 ? 0 : 1, 0, 0);
+            constexpr int kSlots = KV8 ? kRing8 : kRingS;
+            const uint32_t ring = base + (KV8 ? kOffRing8 : kOffRingS);
+            bool ok = mbar_wait(bars + (KV8 ? B_QCONV : B_QREADY), 0, st);
             const int n_chunks = kQChunks * T;
             for (int g = 0; ok && g < n_chunks; g++) {
-                const int slot = g % kRingS, tile = g / kQChunks, c = g % kQChunks;
+                const int slot = g % kSlots, tile = g / kQChunks, c = g % kQChunks;
                 // S buffer of this tile must be free (softmax read S of tile - 2)
                 if (c == 0 && tile >= 2 &&
                     !mbar_wait(bars + B_SEMPTY + (tile & 1), (uint32_t)((tile >> 1) - 1) & 1, st))
                     break;
-                if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingS) & 1, st))
+                if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kSlots) & 1, st))
                     break;
                 fence_async_smem();  // landed copies -> tensor core (async proxy)
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t d = tmem + (tile & 1) * kTile;
-                    const uint32_t chunk = base + kOffRingS + slot * kChunk;
+                    const uint32_t chunk = ring + slot * kChunk;
 #pragma unroll
                     for (int kk = 0; kk < 4; kk++) {
                         const uint64_t ad =
@@ -447,14 +611,15 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     break;
                 fence_async_smem();  // P written by the score CTA -> tensor core
                 for (int j = 0; j < kVGroups; j++) {
-                    const int g = t * kVGroups + j, slot = g % kRingV;
-                    if (!mbar_wait(bars + B_CONV + slot, (uint32_t)(g / kRingV) & 1, st)) {
+                    constexpr int kSlots = KV8 ? kVRing8 : kRingV;
+                    const int g = t * kVGroups + j, slot = g % kSlots;
+                    if (!mbar_wait(bars + B_CONV + slot, (uint32_t)(g / kSlots) & 1, st)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t grp = base + kOffRingV + slot * kGroup;
+                        const uint32_t grp = base + (KV8 ? kOffVRing8 : kOffRingV) + slot * kGroup;
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; kk++) {
                             const uint64_t ad =
@@ -465,7 +630,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                                 smem_desc(grp + kk * 2048, kChunk, 1024, kSwizzle128B);
                             umma_f16_ss(tmem + 128 * j, ad, bd, idesc, t > 0 || kk > 0);
                         }
-                        umma_commit(bars + B_EMPTY + slot);
+                        umma_commit(bars + (KV8 ? B_F16E : B_EMPTY) + slot);
                     }
                     __syncwarp();
                 }
@@ -487,8 +652,22 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
             const int quarter = warp & 3, kh = (warp - kWarpSoft0) >> 2;
             const int h = quarter * 32 + lane;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            if constexpr (KV8) {
+                // FP8 cache: keys are dequantised to f16, so the query becomes
+                // f16 too (one operand type per MMA; exact for |q| >= 2^-14)
+                mbar_wait(bars + B_QREADY, 0, st);
+                const int st_ = tid - kWarpSoft0 * 32;
+                for (int i = st_; i < (int)(kQChunks * kChunk / 16); i += kSoftmax) {
+                    const uint4 x = ld_shared_v4(base + kOffQ + i * 16);
+                    st_shared_v4(base + kOffQ + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
+                                 bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+                }
+                fence_async_smem();
+                mbar_arrive(bars + B_QCONV);
+            }
             const float sl2 = at.softmax_scale * 1.4426950408889634f;  // scale * log2(e)
-            const uint32_t *mask = reinterpret_cast<const uint32_t *>(gbase + kOffMask);
+            const uint32_t *mask =
+                reinterpret_cast<const uint32_t *>(gbase + (KV8 ? kOffMask8 : kOffMask));
             // the two threads of a head share TMEM lane h: column 256 + kh is
             // this thread's exchange cell
             const uint32_t xmine = tmem + 256 + kh + lane_off, xother = tmem + 257 - kh + lane_off;
@@ -627,8 +806,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
             // For each tile: the physical row of every selected key (-1: none,
             // the loaders then write zeros) and bit i of word w set when key
             // 32 w + i is valid.  Up to two tiles ahead of its consumers.
-            int *rows = reinterpret_cast<int *>(gbase + kOffRows);
-            uint32_t *mask = reinterpret_cast<uint32_t *>(gbase + kOffMask);
+            int *rows = reinterpret_cast<int *>(gbase + (KV8 ? kOffRows8 : kOffRows));
+            uint32_t *mask = reinterpret_cast<uint32_t *>(gbase + (KV8 ? kOffMask8 : kOffMask));
+            float *scl = reinterpret_cast<float *>(gbase + kOffScl8);  // FP8 cache: key scales
             for (int t = 0; t < T; t++) {
                 const int rs = t % kRowSlots;
                 if (t >= kRowSlots &&
@@ -659,8 +839,15 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     } else if (sv[i] != -1) {
                         raise_flag(st, SI_DEVFLAG_BAD_INDEX);
                     }
-                    rows[rs * kTile + 32 * i + lane] =
-                        ok ? blk[i] * b.page_size + sv[i] % b.page_size : -1;
+                    const int prow = ok ? blk[i] * b.page_size + sv[i] % b.page_size : -1;
+                    rows[rs * kTile + 32 * i + lane] = prow;
+                    if constexpr (KV8) {
+                        // the key's scales of every 128-entry tile (0 for no key)
+#pragma unroll
+                        for (int q5 = 0; q5 < kKvTiles; q5++)
+                            scl[(rs * kKvTiles + q5) * kTile + 32 * i + lane] =
+                                prow >= 0 ? __ldg(at.k.scale + (int64_t)prow * kKvTiles + q5) : 0.f;
+                    }
                     const uint32_t w = __ballot_sync(0xffffffffu, ok);
                     if (lane == i)
                         word = w;
@@ -679,6 +866,33 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
             // in place once their copies have landed (warps 12..15 and 17).
             const int ct = warp < kWarpMma ? tid - (kWarpQuad + 4) * 32 : 4 * 32 + lane;
             const int n_groups = kVGroups * T;
+            if constexpr (KV8) {
+                // FP8 cache: staged codes times the key's scale into the f16
+                // group slot (two chunks of [128 keys x 64 dims], SW128), then
+                // the staging slot goes back to the loaders
+                for (int g = 0; g < n_groups; g++) {
+                    const int s8 = g % kVStg8, f = g % kVRing8;
+                    if (!mbar_wait(bars + B_FULL + s8, (uint32_t)(g / kVStg8) & 1, st) ||
+                        (g >= kVRing8 &&
+                         !mbar_wait(bars + B_F16E + f, (uint32_t)((g / kVRing8) - 1) & 1, st)))
+                        break;
+                    const uint32_t src = base + kOffVStg8 + s8 * kVStgBytes8;
+                    const float *ksc =
+                        reinterpret_cast<const float *>(gbase + kOffVStg8 + s8 * kVStgBytes8 +
+                                                        kTile * 128);
+                    const uint32_t dst = base + kOffVRing8 + f * kGroup;
+                    for (int i = ct; i < kTile * 8; i += kConverters) {
+                        const int key = i >> 3, uu = i & 7;  // 16 codes: dims 16 uu .. 16 uu + 15
+                        const uint32_t d0 = dst + (uu >> 2) * kChunk;
+                        dequant16(ld_shared_v4(src + key * 128 + uu * 16), ksc[key],
+                                  d0 + sw128_offset(key, 2 * (uu & 3)),
+                                  d0 + sw128_offset(key, 2 * (uu & 3) + 1));
+                    }
+                    fence_async_smem();
+                    mbar_arrive(bars + B_CONV + f);
+                    mbar_arrive(bars + B_EMPTY + s8);
+                }
+            } else
             for (int g = 0; g < n_groups; g++) {
                 const int slot = g % kRingV;
                 if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingV) & 1, st))
@@ -904,11 +1118,18 @@ bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top)
     (void)k_top;
     // one shared latent row per position: V is the first 512 entries of the
     // 576-entry key row (the same cache, same stride)
-    return at.q_dtype == SI_BF16 && at.n_heads == kHeads && at.d_qk == kDqk && at.d_v == kDv &&
-           at.k.dtype == SI_BF16 && !at.k.scale && !at.v.scale && at.v.data == at.k.data &&
-           at.v.row_stride == at.k.row_stride &&
-           at.k.row_stride % 8 == 0 && ((uintptr_t)at.k.data % 16) == 0 &&
-           ((uintptr_t)at.q % 16) == 0;
+    const bool shape = at.q_dtype == SI_BF16 && at.n_heads == kHeads && at.d_qk == kDqk &&
+                       at.d_v == kDv && at.v.data == at.k.data &&
+                       at.v.row_stride == at.k.row_stride && ((uintptr_t)at.k.data % 16) == 0 &&
+                       ((uintptr_t)at.q % 16) == 0;
+    // bf16 latent rows, or FP8 rows of 576 codes with five 128-entry tile scales
+    const bool bf16 = at.k.dtype == SI_BF16 && !at.k.scale && !at.v.scale &&
+                      at.k.row_stride % 8 == 0;
+    const bool fp8 = at.k.dtype == SI_E4M3 && at.v.dtype == SI_E4M3 && at.k.scale &&
+                     at.v.scale == at.k.scale && at.k.scale_tile == 128 &&
+                     at.v.scale_tile == 128 && at.k.row_stride == kDqk &&
+                     ((uintptr_t)at.k.scale % 4) == 0;
+    return shape && (bf16 || fp8);
 }
 
 cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int32_t *idx,
@@ -927,7 +1148,10 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
     std::call_once(once[dev], [dev] {
         cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            r = cudaFuncSetAttribute(k_attn_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(k_attn_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
         err_of[dev] = r;
     });
@@ -969,8 +1193,11 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_attn_tc, qmap, omap, b, at, idx, k_top, kdt, lse, n_split,
-                           part_ml, st);
+    e = at.k.dtype == SI_E4M3
+            ? cudaLaunchKernelEx(&cfg, k_attn_tc<true>, qmap, omap, b, at, idx, k_top, kdt, lse,
+                                 n_split, part_ml, st)
+            : cudaLaunchKernelEx(&cfg, k_attn_tc<false>, qmap, omap, b, at, idx, k_top, kdt, lse,
+                                 n_split, part_ml, st);
     if (e != cudaSuccess || n_split == 1)
         return e;
     count_launch();

@@ -151,3 +151,17 @@ def test_causal_prefill_full_size_fp8_query(si):
     scale): the four-row prefill blocks at full size."""
     wl = synth.make("c2", q_idx_fp8=True)
     _run(si, wl, rows=[0, 3, 4, 2047, 2048, 9001, 16383])
+
+
+def test_benchmark_workload_fp8_kv_cache(si):
+    """The benchmarked decode step over an FP8 latent cache (one scale per row
+    and 128-entry tile) on the tensor-core attention kernel."""
+    wl = synth.make("c1", kv_fp8=True)
+    _run(si, wl, rows=[0, 31, 63])
+
+
+def test_long_context_fp8_kv_cache_split(si):
+    """Long-context decode over an FP8 cache: few rows, so each row's key
+    tiles are split over clusters and merged."""
+    wl = synth.make("c3", batch=4, ctx=40000, kv_fp8=True)
+    _run(si, wl, rows=[0, 3])
