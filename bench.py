@@ -156,7 +156,8 @@ def whole_job_rate(world: int, n_q: int, ms_per_step: float) -> float:
 
 
 # Workload names of the committed ncu captures (profiles/*.md).
-PROFILE_WORKLOAD = {"c1": "decode b64 ctx8192", "c3": "decode b16 ctx131072"}
+PROFILE_WORKLOAD = {"c1": "decode b64 ctx8192", "c3": "decode b16 ctx131072",
+                    "c1:kv8": "decode b64 ctx8192 fp8 kv"}
 
 
 def _kernel_traffic(kernel: str, source: str, workload: str):
@@ -534,7 +535,7 @@ def run_si(args):
     roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "peak_src": peaks["src"] + " (hbm_gbs, copy)",
-            "traffic": _kernel_traffic(kname, src, wl.name),
+            "traffic": _kernel_traffic(kname, src, wl.name + (":kv8" if args.kv_fp8 else "")),
             "algorithmic_bytes_per_launch": algo[dom], "ms_per_launch": mean_k[dom]}
     total_bytes = algo["indexer"] + algo["topk"] + algo["attn"]
     step_gbs = total_bytes / (ms / 1e3) / 1e9

@@ -38,6 +38,19 @@
 // a thread's plain loads complete behind its own copies in flight, and a
 // release-ordered arrive waits for them.  Every wait is bounded.
 //
+// The query arrives by tensor copies; the output leaves by tensor stores of
+// 128-byte column blocks staged in the idle value ring.  With few rows, each
+// row's key tiles are split over up to eight clusters: a split writes its
+// unnormalised O and (m, l) per head to scratch, and k_attn_combine merges
+// the splits.
+//
+// FP8 cache (section 5.2: codes with one scale per token and tile of 128
+// entries; k_attn_tc<true>): the score CTA converts the query to f16 once and
+// dequantises key chunks to f16 (four warps gather codes into staging slots,
+// four dequantise them into the ring), the value CTA's converters dequantise
+// staged value groups; per-tile fp32 scales do not fold into bf16 exactly,
+// f16 keeps 11 significant bits.
+//
 // Softmax: online in the log2 domain with fp32 state; the exponent reference
 // is only raised when a tile's maximum exceeds it by more than 8, so most
 // tiles leave O untouched.  P is rounded to f16 (11 significant bits) and the
