@@ -488,7 +488,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                     }
                 };
                 float sum[kRows];
-                float part[4] = {0.f, 0.f, 0.f, 0.f};
+                // partial head sums in two packed pairs (0.0f has all bits 0)
+                uint64_t p01 = 0, p23 = 0;
                 uint32_t va[32], vb[32];
                 issue(0, va);
 #pragma unroll
@@ -505,18 +506,34 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
 #pragma unroll
                     for (int i = 0; i < kPH; i += 4) {
                         const float4 wv = w4[i >> 2];
-                        const float wq[4] = {wv.x, wv.y, wv.z, wv.w};
+                        float lg[4];
+                        if constexpr (Q8) {
 #pragma unroll
-                        for (int k = 0; k < 4; k++) {
-                            float lg = __uint_as_float(cur[i + k]);
-                            if constexpr (!Q8)
-                                lg += __uint_as_float(cur[16 + i + k]);
-                            part[k] = fmaf(wq[k], fmaxf(lg, 0.f), part[k]);
+                            for (int k = 0; k < 4; k++)
+                                lg[k] = __uint_as_float(cur[i + k]);
+                        } else {
+                            // logit = q_hi term + q_lo term, two heads per add
+#pragma unroll
+                            for (int k = 0; k < 4; k += 2) {
+                                const float2 s2 = f32x2_unpack(f32x2_add(
+                                    f32x2_pack(__uint_as_float(cur[i + k]),
+                                               __uint_as_float(cur[i + k + 1])),
+                                    f32x2_pack(__uint_as_float(cur[16 + i + k]),
+                                               __uint_as_float(cur[16 + i + k + 1]))));
+                                lg[k] = s2.x;
+                                lg[k + 1] = s2.y;
+                            }
                         }
+                        // w_h * ReLU(logit), two heads per fma
+                        f32x2_fma(p01, f32x2_pack(wv.x, wv.y),
+                                  f32x2_pack(fmaxf(lg[0], 0.f), fmaxf(lg[1], 0.f)));
+                        f32x2_fma(p23, f32x2_pack(wv.z, wv.w),
+                                  f32x2_pack(fmaxf(lg[2], 0.f), fmaxf(lg[3], 0.f)));
                     }
                     if (hq == kPPR - 1) {
-                        sum[j] = (part[0] + part[1]) + (part[2] + part[3]);
-                        part[0] = part[1] = part[2] = part[3] = 0.f;
+                        const float2 a = f32x2_unpack(p01), c = f32x2_unpack(p23);
+                        sum[j] = (a.x + a.y) + (c.x + c.y);
+                        p01 = p23 = 0;
                     }
                 }
                 tc_fence_before();

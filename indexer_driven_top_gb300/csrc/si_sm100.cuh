@@ -322,6 +322,38 @@ __device__ __forceinline__ void tmem_wait_st()
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------ packed fp32
+
+// Two fp32 lanes in one 64-bit register pair (sm_100 family packed FP32
+// arithmetic).  Each lane of fma.rn.f32x2 / add.rn.f32x2 is rounded exactly
+// like the scalar instruction, so results are bit-identical to fmaf / +.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 f32x2_unpack(uint64_t v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+// acc = a * b + acc, per lane
+__device__ __forceinline__ void f32x2_fma(uint64_t &acc, uint64_t a, uint64_t b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // --------------------------------------------------------------------- UMMA
 
 // Shared-memory matrix descriptor (tcgen05 format, version 1).
