@@ -431,7 +431,8 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                     tc_fence_after();
                     const float4 *w4 = reinterpret_cast<const float4 *>(w_s + p * kHeads);
                     const uint32_t acc = tmem + (g * kAccPerPair + c) * kN + lane_off;
-                    float part[4] = {0.f, 0.f, 0.f, 0.f};
+                    // partial head sums in two packed pairs (0.0f has all bits 0)
+                    uint64_t p01 = 0, p23 = 0;
 #pragma unroll
                     for (int hh = 0; hh < 2; hh++) {  // heads [32 hh, 32 hh + 32)
                         uint32_t vh[32], vl[32];
@@ -441,18 +442,29 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
                             const float4 wv = w4[(hh * 32 + i) >> 2];
-                            const float wq[4] = {wv.x, wv.y, wv.z, wv.w};
+                            // logit = q_hi term + q_lo term, two heads per add
+                            float lg[4];
 #pragma unroll
-                            for (int k = 0; k < 4; k++) {
-                                const float lg =
-                                    __uint_as_float(vh[i + k]) + __uint_as_float(vl[i + k]);
-                                part[k] = fmaf(wq[k], fmaxf(lg, 0.f), part[k]);
+                            for (int k = 0; k < 4; k += 2) {
+                                const float2 s2 = f32x2_unpack(f32x2_add(
+                                    f32x2_pack(__uint_as_float(vh[i + k]),
+                                               __uint_as_float(vh[i + k + 1])),
+                                    f32x2_pack(__uint_as_float(vl[i + k]),
+                                               __uint_as_float(vl[i + k + 1]))));
+                                lg[k] = s2.x;
+                                lg[k + 1] = s2.y;
                             }
+                            // w_h * ReLU(logit), two heads per fma
+                            f32x2_fma(p01, f32x2_pack(wv.x, wv.y),
+                                      f32x2_pack(fmaxf(lg[0], 0.f), fmaxf(lg[1], 0.f)));
+                            f32x2_fma(p23, f32x2_pack(wv.z, wv.w),
+                                      f32x2_pack(fmaxf(lg[2], 0.f), fmaxf(lg[3], 0.f)));
                         }
                     }
                     tc_fence_before();
                     mbar_arrive(cempty_bar + g * kAccPerPair + c);
-                    const float sum = (part[0] + part[1]) + (part[2] + part[3]);
+                    const float2 pa = f32x2_unpack(p01), pc = f32x2_unpack(p23);
+                    const float sum = (pa.x + pa.y) + (pc.x + pc.y);
                     if (s < ld)
                         scores[(int64_t)rr * ld + s] = sc >= 0.f ? sum * sc + 0.0f : -INFINITY;
                     m++;
