@@ -19,8 +19,11 @@
 //       tile's logits S = q . k^T (UMMA M = 128 heads, N = 128 keys) in TMEM
 //       (double-buffered).  Eight softmax warps (two threads per head, each
 //       taking half of the tile's keys) turn a tile into weights P (f16) and
-//       write them, with one rescale factor per head, straight into the value
-//       CTA's shared memory.  A row warp resolves each tile's selected
+//       stage them, with one rescale factor per head, in local shared memory;
+//       one thread then hands the tile to the value CTA with two bulk copies
+//       into its shared memory (the copy engine moves the 32.5 KB, the
+//       softmax warps go on to the next tile).  A row warp resolves each
+//       tile's selected
 //       positions to physical rows (block table) and key-valid bits ahead of
 //       the loaders and the softmax.
 //   value CTA (rank 1) -- keeps O (128 heads x 512 value dims, fp32) in TMEM
@@ -99,11 +102,13 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kMaxSplit = 8;              // clusters per row at most
 
 // score CTA layout
-constexpr int kRingS = 5;
+constexpr int kRingS = 3;
 constexpr uint32_t kOffQ = 0;                                  // 9 x [128 heads x 64 dims]
 constexpr uint32_t kOffRingS = kQChunks * kChunk;              // kRingS x [128 keys x 64 dims]
+constexpr uint32_t kOffSP = kOffRingS + kRingS * kChunk;       // P staging: 2 x [128 heads x 64 keys]
+constexpr uint32_t kOffSF = kOffSP + 2 * kChunk;               // rescale factor staging: 128 floats
 constexpr int kRowSlots = 2;                                   // tiles of row tables in flight
-constexpr uint32_t kOffRows = kOffRingS + kRingS * kChunk;     // 2 x 128 physical rows (int32)
+constexpr uint32_t kOffRows = kOffSF + kHeads * 4;             // 2 x 128 physical rows (int32)
 constexpr uint32_t kOffMask = kOffRows + kRowSlots * kTile * 4; // 2 x 4 key-valid words
 // value CTA layout
 constexpr int kPBufs = 2;                                      // P buffers (tiles) in flight
@@ -138,7 +143,8 @@ static_assert(kOffVStg8 == kOffRingV && kOffF8 - kOffVStg8 >= 8 * kEpiBufs * 409
 constexpr uint32_t kOffBar = std::max(
     std::max(kOffF + kPBufs * kHeads * 4, kOffMask + kRowSlots * 16),
     std::max(kOffF8 + kPBufs * kHeads * 4, kOffMask8 + kRowSlots * 16));
-constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;          // + alignment slack
+constexpr uint32_t kBarArea = 416;                             // mbarriers + TMEM base word
+constexpr uint32_t kSmemBytes = kOffBar + kBarArea + 1024;     // + alignment slack
 static_assert(kOffMask + kRowSlots * 16 <= kOffBar, "score scratch overlaps the barriers");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
@@ -162,10 +168,13 @@ enum : int {
     B_F16E = 36,    // [3] value, FP8 cache: f16 group slot consumed (MMA commit)
     B_STF8 = 39,    // [kStg8] score, FP8 cache: staging slot landed (cp.async arrivals)
     B_STE8 = 44,    // [kStg8] score, FP8 cache: staging slot dequantised
-    B_COUNT = 49
+    B_SPFREE = 49,  // score, bf16 cache: P staging copied out (remote arrival per tile)
+    B_COUNT = 50
 };
 constexpr uint32_t kTmemSlot = 8 * 50;  // byte offset of the TMEM base within the barrier area
-static_assert(B_COUNT * 8 <= (int)kTmemSlot, "barrier area");
+static_assert(B_COUNT * 8 <= (int)kTmemSlot && kTmemSlot + 4 <= kBarArea, "barrier area");
+static_assert(kRingS <= 5 && kRingV <= 5, "ring barrier arrays");
+static_assert(kOffSP % 1024 == 0, "P staging keeps the 128-byte swizzle atoms of the P buffers");
 
 // 2^x with the hardware approximation (ex2.approx: ~2 ulp, subnormal
 // results flushed to zero), ample for a softmax whose weights are rounded to
@@ -371,7 +380,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
     const bool split = n_split > 1;
 
     if (tid == 0) {
-        for (int i = 0; i < kRingS; i++) {
+        for (int i = 0; i < 5; i++) {
             // FP8 score ring slots are filled by the 128 dequantising threads
             mbar_init(bars + B_FULL + i, (KV8 && score_cta) ? kLoaders / 2 : kLoaders);
             // FP8 value staging is released by the converters, rings by the MMA
@@ -391,13 +400,16 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
         }
         for (int i = 0; i < kPBufs; i++) {
             mbar_init(bars + B_PEMPTY + i, 1);
-            mbar_init(bars + B_PFULL + i, kSoftmax);
+            // bf16 cache: one arrival with the bytes of the bulk copies;
+            // FP8 cache: remote arrivals of the softmax threads
+            mbar_init(bars + B_PFULL + i, KV8 ? kSoftmax : 1);
         }
         for (int i = 0; i < kRowSlots; i++) {
             mbar_init(bars + B_MASK + i, 32);
             mbar_init(bars + B_MEMPTY + i, kSoftmax + kLoaders);
         }
         mbar_init(bars + B_QREADY, 1);
+        mbar_init(bars + B_SPFREE, 1);
         mbar_init(bars + B_OCORR, kHeads);
         mbar_init(bars + B_PVDONE, 1);
         mbar_init(bars + B_FINAL, kHeads);
@@ -429,6 +441,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
     const uint32_t peer_f = mapa_shared(base + kOffF, 1);
     const uint32_t peer_pfull = mapa_shared(smem_u32(bars + B_PFULL), 1);
     const uint32_t peer_final = mapa_shared(smem_u32(bars + B_FINAL), 1);
+    // score-CTA barrier as seen from the value CTA
+    const uint32_t peer_spfree = mapa_shared(smem_u32(bars + B_SPFREE), 0);
 
     if (warp < kLoaderWarps) {
         // -------------------------------------------------------------- loaders
@@ -687,10 +701,13 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
             float m_used = -INFINITY;  // exponent reference (log2 units)
             float l = 0.f;             // this half's row sum
             bool ok = true;
+            // FP8 cache: P goes to the value CTA as remote stores, announced
+            // one step late (after the next tile's first pass), so that the
+            // cluster-scope release does not wait on the stores' round trip.
+            // bf16 cache: P is staged locally and handed over by bulk copies.
+            const bool issuer = tid == kWarpSoft0 * 32;  // issues the bulk copies
+            const uint32_t sp = base + kOffSP;
             int unpublished = -1;  // tile whose P is written but not yet announced
-            // Announces P of tile `pt` to the value CTA.  Done one step late
-            // (after the next tile's first pass), so that the cluster-scope
-            // release does not wait on the remote stores' round trip.
             auto publish = [&](int pt) {
                 fence_async_cluster();
                 mbar_arrive_remote(peer_pfull + (pt % kPBufs) * 8);
@@ -739,20 +756,27 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     publish(unpublished);
                     unpublished = -1;
                 }
-                // the value CTA's P buffer pb is free once its P.V of tile t - 3
-                // is done; the bar.red also orders this tile's reads of the
-                // exchange cell before the next tile's writes
+                // the value CTA's P buffer pb is free once its P.V of tile
+                // t - kPBufs is done; the bf16 staging once the value CTA has
+                // seen tile t - 1's copies land.  The bar.red also orders this
+                // tile's reads of the exchange cell before the next tile's
+                // writes.
                 const int pb = t % kPBufs;
-                const bool free_ =
+                bool free_ =
                     t < kPBufs ||
                     mbar_wait_cluster(bars + B_PEMPTY + pb, (uint32_t)((t / kPBufs) - 1) & 1, st);
+                if (!KV8 && issuer && t >= 1)
+                    free_ = free_ &&
+                            mbar_wait_cluster(bars + B_SPFREE, (uint32_t)(t - 1) & 1, st);
                 if (bar_sync_or(1, kSoftmax, !free_)) {
                     ok = false;
                     break;
                 }
-                // pass 2: p = 2^(x - m_used) as f16, into the value CTA's P buffer
-                // pb, chunk kh (this half's 64 keys)
-                const uint32_t pc = peer_p + pb * 2 * kChunk + kh * kChunk;
+                // pass 2: p = 2^(x - m_used) as f16, chunk kh (this half's 64
+                // keys) of the value CTA's P buffer pb (FP8 cache) or of the
+                // local staging (bf16 cache)
+                const uint32_t pc =
+                    KV8 ? peer_p + pb * 2 * kChunk + kh * kChunk : sp + kh * kChunk;
 #pragma unroll 1
                 for (int q = 0; q < 2; q++) {
                     uint32_t v[32];
@@ -775,13 +799,33 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                         l += __low2float(pr) + __high2float(pr);
                     }
 #pragma unroll
-                    for (int w = 0; w < 4; w++)
-                        st_cluster_v4(pc + sw128_offset(h, q * 4 + w), pk[4 * w], pk[4 * w + 1],
-                                      pk[4 * w + 2], pk[4 * w + 3]);
+                    for (int w = 0; w < 4; w++) {
+                        if constexpr (KV8)
+                            st_cluster_v4(pc + sw128_offset(h, q * 4 + w), pk[4 * w],
+                                          pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                        else
+                            st_shared_v4(pc + sw128_offset(h, q * 4 + w), pk[4 * w],
+                                         pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    }
                 }
-                if (kh == 0)
-                    st_cluster_f32(peer_f + (pb * kHeads + h) * 4, f);
-                unpublished = t;
+                if constexpr (KV8) {
+                    if (kh == 0)
+                        st_cluster_f32(peer_f + (pb * kHeads + h) * 4, f);
+                    unpublished = t;
+                } else {
+                    // staged P and factors -> the value CTA's P buffer pb and
+                    // factor slot pb; its barrier counts the bytes
+                    if (kh == 0)
+                        reinterpret_cast<float *>(gbase + kOffSF)[h] = f;
+                    fence_async_smem();  // staging writes -> bulk copy engine
+                    bar_sync_or(1, kSoftmax, false);
+                    if (issuer) {
+                        const uint32_t bar = peer_pfull + pb * 8;
+                        mbar_arrive_expect_tx_remote(bar, 2 * kChunk + kHeads * 4);
+                        bulk_s2cluster(peer_p + pb * 2 * kChunk, sp, 2 * kChunk, bar);
+                        bulk_s2cluster(peer_f + pb * kHeads * 4, base + kOffSF, kHeads * 4, bar);
+                    }
+                }
             }
             if (unpublished >= 0)
                 publish(unpublished);
@@ -930,6 +974,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     ok = false;
                     break;
                 }
+                // bf16 cache: tile t's copies have landed, so the score CTA may
+                // restage P
+                if (!KV8 && h == 0)
+                    mbar_arrive_remote(peer_spfree);
                 const float f = fac[pb * kHeads + h];
                 // P.V of tile t - 1 must be complete before O is touched
                 if (t >= 1 && !mbar_wait(bars + B_PVDONE, (uint32_t)(t - 1) & 1, st)) {

@@ -443,6 +443,32 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Remote arrival that also raises the expected transaction bytes of an
+// mbarrier in another CTA of the cluster (`addr` from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t addr, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                     addr),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Contiguous copy from this CTA's shared memory into the shared memory of a
+// CTA of the cluster, by the bulk-copy engine: `dst` and `mbar` are cluster
+// addresses in the destination CTA (mapa_shared), completion is reported as
+// transaction bytes on `mbar`.  Addresses 16-byte aligned, bytes a multiple
+// of 16.  The source may be overwritten once the destination's barrier has
+// seen the bytes.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                               uint32_t mbar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(mbar)
+        : "memory");
+}
+
 // Contiguous global -> shared copy by the bulk-copy engine; completion is
 // reported as transaction bytes on `bar`.  dst, src and bytes must be
 // multiples of 16.
