@@ -62,6 +62,9 @@ def _load():
             lib.oracle_indexer_scores.argtypes = [P, P, I32, I32, I32, P, ctypes.c_int, P, P, P,
                                                   ctypes.c_int, P, I64, P, I64, ctypes.c_int]
             lib.oracle_topk.argtypes = [P, P, I32, P, I64, I32, P, P, ctypes.c_int]
+            lib.oracle_topk_cand.argtypes = [P, P, I32, I32, I32, P, ctypes.c_int, P, P, P,
+                                             ctypes.c_int, P, I64, P, I64, I32, I32, P, P, P,
+                                             ctypes.c_int]
             lib.oracle_sparse_attn.argtypes = [P, P, I32, I32, I32, I32, P, ctypes.c_int, P, P,
                                                ctypes.c_int, I64, I64, P, P, I32, I32, I32, P,
                                                I32, D, P, P, ctypes.c_int]
@@ -154,6 +157,31 @@ def topk(b: Batch, scores, K: int, rows: Optional[Sequence[int]] = None,
     lib.oracle_topk(ctypes.byref(b.s), _ptr(rr), n, _ptr(sc), sc.shape[1], K, _ptr(idx),
                     _ptr(kth), threads or default_threads())
     return (idx, kth) if return_kth else idx
+
+
+def topk_cand(b: Batch, q_idx, q_type: str, w, k, k_type: str, k_scale, Hi: int, Di: int,
+              cand, K: int, rows: Optional[Sequence[int]] = None, threads: Optional[int] = None,
+              q_scale=None):
+    """Candidate-restricted selection (the vLLM article on DeepSeek-V4.1,
+    "Kernels": indexer logits over a fixed candidate set per query).  Row r's
+    candidates are the entries s of cand[r] with 0 <= s <= pos(r); each is
+    scored as in indexer_scores and the K best (ties -> lower position) are
+    returned ascending, -1 padded.  Returns (idx [n, K], scores [n, n_cand]
+    with -inf for list entries that are not candidates, kth [n, 2])."""
+    lib = _load()
+    rr, n = _rows(rows, b.s.n_q)
+    q_idx, w, k, k_scale = _c(q_idx), _c(w, np.float32), _c(k), _c(k_scale, np.float32)
+    q_scale = None if q_scale is None else _c(q_scale, np.float32)
+    cd = _c(cand, np.int32)
+    n_cand = int(cd.shape[1])
+    idx = np.empty((n, K), dtype=np.int32)
+    sc = np.empty((n, n_cand), dtype=np.float64)
+    kth = np.empty((n, 2), dtype=np.float64)
+    lib.oracle_topk_cand(ctypes.byref(b.s), _ptr(rr), n, Hi, Di, _ptr(q_idx), TYPE_CODE[q_type],
+                         _ptr(q_scale), _ptr(w), _ptr(k), TYPE_CODE[k_type], _ptr(k_scale),
+                         k.shape[-1], _ptr(cd), n_cand, n_cand, K, _ptr(idx), _ptr(sc), _ptr(kth),
+                         threads or default_threads())
+    return idx, sc, kth
 
 
 def sparse_attn(b: Batch, q, q_type: str, k, v, kv_type: str, idx, K: int, Hq: int, Dqk: int,

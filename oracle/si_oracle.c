@@ -140,6 +140,25 @@ typedef struct {
     double *scores; int64_t ld;         /* [n_rows, ld] */
 } idx_ctx;
 
+/* score(r, s) for the key at physical row `row` of the paged cache */
+static double score_one(const idx_ctx *c, int32_t r, int64_t row)
+{
+    double kscale = c->k_scale ? (double)c->k_scale[row] : 1.0;
+    double score = 0.0;
+    for (int32_t h = 0; h < c->Hi; h++) {
+        double qscale = c->q_scale ? (double)c->q_scale[(int64_t)r * c->Hi + h] : 1.0;
+        double dot = 0.0;
+        for (int32_t d = 0; d < c->Di; d++) {
+            double qv = elem(c->q_idx, c->q_type, ((int64_t)r * c->Hi + h) * c->Di + d) * qscale;
+            double kv = elem(c->k, c->k_type, row * c->k_stride + d) * kscale;
+            dot += qv * kv;
+        }
+        double relu = dot > 0.0 ? dot : 0.0;
+        score += (double)c->w[(int64_t)r * c->Hi + h] * relu;
+    }
+    return score + 0.0; /* -0.0 -> +0.0 */
+}
+
 static void idx_row(void *p, int64_t i)
 {
     const idx_ctx *c = (const idx_ctx *)p;
@@ -153,21 +172,7 @@ static void idx_row(void *p, int64_t i)
             out[s] = -INFINITY;
             continue;
         }
-        int64_t row = page_row(b, seq, s);
-        double kscale = c->k_scale ? (double)c->k_scale[row] : 1.0;
-        double score = 0.0;
-        for (int32_t h = 0; h < c->Hi; h++) {
-            double qscale = c->q_scale ? (double)c->q_scale[(int64_t)r * c->Hi + h] : 1.0;
-            double dot = 0.0;
-            for (int32_t d = 0; d < c->Di; d++) {
-                double qv = elem(c->q_idx, c->q_type, ((int64_t)r * c->Hi + h) * c->Di + d) * qscale;
-                double kv = elem(c->k, c->k_type, row * c->k_stride + d) * kscale;
-                dot += qv * kv;
-            }
-            double relu = dot > 0.0 ? dot : 0.0;
-            score += (double)c->w[(int64_t)r * c->Hi + h] * relu;
-        }
-        out[s] = score + 0.0; /* -0.0 -> +0.0 */
+        out[s] = score_one(c, r, page_row(b, seq, s));
     }
 }
 
@@ -240,6 +245,72 @@ void oracle_topk(const orc_batch *b, const int32_t *rows, int32_t n_rows, const 
 {
     topk_ctx c = { b, rows, scores, ld, K, idx, kth };
     orc_parallel(topk_row, &c, n_rows, nthreads);
+}
+
+/* ------------------------------------------- candidate-restricted selection */
+
+/* The vLLM article on DeepSeek-V4.1 ("Kernels"): the indexer logits are
+ * computed only for a fixed set of candidate positions per query instead of
+ * the whole context.  Row r's candidates are the entries s of its list with
+ * 0 <= s <= pos (other entries, -1 included, are not candidates).  Each is
+ * scored with the same definition as above; the Top-K is taken among the
+ * candidates only (score descending, equal scores -> lower position), and
+ * written as ascending positions, -1 padded when there are fewer than K. */
+typedef struct {
+    idx_ctx ic;
+    const int32_t *cand; int64_t ld_cand; int32_t n_cand;   /* [n_q, ld_cand] */
+    int32_t K;
+    int32_t *idx;          /* [n_rows, K] */
+    double *scores;        /* [n_rows, n_cand]: score of list entry j, -inf if none */
+    double *kth;           /* [n_rows, 2] or NULL */
+} cand_ctx;
+
+static void cand_row(void *p, int64_t i)
+{
+    const cand_ctx *c = (const cand_ctx *)p;
+    const orc_batch *b = c->ic.b;
+    int32_t r = c->ic.rows ? c->ic.rows[i] : (int32_t)i;
+    int32_t seq = b->q_seq[r];
+    int64_t pos = b->q_pos[r];
+    double *sc = c->scores + i * c->n_cand;
+    int32_t *out = c->idx + i * c->K;
+    orc_cand *cand = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)(c->n_cand > 0 ? c->n_cand : 1));
+    int64_t n = 0;
+    for (int32_t j = 0; j < c->n_cand; j++) {
+        int64_t s = c->cand[(int64_t)r * c->ld_cand + j];
+        if (s < 0 || s > pos) {   /* not a candidate of this row */
+            sc[j] = -INFINITY;
+            continue;
+        }
+        sc[j] = score_one(&c->ic, r, page_row(b, seq, s));
+        cand[n].score = sc[j];
+        cand[n].pos = s;
+        n++;
+    }
+    qsort(cand, (size_t)n, sizeof(orc_cand), cand_cmp);
+    int64_t m = n < c->K ? n : c->K;
+    for (int64_t j = 0; j < m; j++)
+        out[j] = (int32_t)cand[j].pos;
+    qsort(out, (size_t)m, sizeof(int32_t), i32_cmp);
+    for (int64_t j = m; j < c->K; j++)
+        out[j] = -1;
+    if (c->kth) {
+        c->kth[2 * i] = (n >= c->K) ? cand[c->K - 1].score : NAN;
+        c->kth[2 * i + 1] = (n > c->K) ? cand[c->K].score : NAN;
+    }
+    free(cand);
+}
+
+void oracle_topk_cand(const orc_batch *b, const int32_t *rows, int32_t n_rows, int32_t Hi,
+                      int32_t Di, const void *q_idx, int q_type, const float *q_scale,
+                      const float *w, const void *k, int k_type, const float *k_scale,
+                      int64_t k_stride, const int32_t *cand, int64_t ld_cand, int32_t n_cand,
+                      int32_t K, int32_t *idx, double *scores, double *kth, int nthreads)
+{
+    cand_ctx c = { { b, rows, Hi, Di, q_idx, q_type, q_scale, w, k, k_type, k_scale, k_stride,
+                     NULL, 0 },
+                   cand, ld_cand, n_cand, K, idx, scores, kth };
+    orc_parallel(cand_row, &c, n_rows, nthreads);
 }
 
 /* --------------------------------------------------------- sparse attention */

@@ -399,3 +399,23 @@ def permute_pages(wl: Workload, seed: int) -> Workload:
     bt = np.where(wl.block_table >= 0, perm[np.maximum(wl.block_table, 0)], -1).astype(np.int32)
     return dataclasses.replace(wl, block_table=bt, k_idx=mv(wl.k_idx), k_scale=mv(wl.k_scale),
                                k=mv(wl.k), v=mv(wl.v), kv_scale=mv(wl.kv_scale))
+
+
+def candidates(wl: Workload, n_cand: int, seed: int = 0, pad_beyond: int = 0) -> np.ndarray:
+    """Candidate position lists [n_q, n_cand] int32 for candidate-restricted
+    selection: row r draws min(n_cand, pos + 1) distinct positions uniformly
+    from 0..pos (its own PCG64 stream, seeded by `seed`), sorted ascending and
+    padded with -1.  With pad_beyond > 0, that many entries after a row's
+    draws (where room is left) are set to positions past the row's pos, which
+    are not candidates."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = np.full((wl.n_q, n_cand), -1, dtype=np.int32)
+    for r in range(wl.n_q):
+        pos = int(wl.q_pos[r])
+        m = min(n_cand, pos + 1)
+        pick = rng.choice(pos + 1, size=m, replace=False) if m < pos + 1 else np.arange(pos + 1)
+        out[r, :m] = np.sort(pick).astype(np.int32)
+        extra = min(pad_beyond, n_cand - m)
+        if extra > 0:
+            out[r, m:m + extra] = pos + 1 + np.arange(extra, dtype=np.int32)
+    return out

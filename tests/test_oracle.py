@@ -383,3 +383,79 @@ def test_fp8_kv_tiles_brute_force():
                                     wl.Hq, wl.Dqk, wl.Dv, wl.scale, q_dtype="bf16",
                                     kv_scale=wl.kv_scale[..., :1].copy(), scale_tile=0)
     assert not np.allclose(out, out_row)
+
+
+# ---------------------------------------- candidate-restricted selection
+
+def test_golden_candidate_topk():
+    """Hand-derived candidate selections on the fixture's keys and queries:
+    only listed positions 0..pos compete, ties go to the lower position."""
+    g = _golden()
+    with open(os.path.join(GOLDEN, "tiny_candidate_topk.json")) as f:
+        gc = json.load(f)
+    rows = g["rows"]
+    b, k, _, _ = _golden_batch(g, [r["pos"] for r in rows])
+    q_idx = np.array([r["q_idx"] for r in rows], dtype=np.float32)
+    w = np.array([r["w"] for r in rows], dtype=np.float32)
+    for case in gc["cases"]:
+        r = case["row"]
+        n = len(case["cand"])
+        cand = np.full((2, n), -1, dtype=np.int32)
+        cand[r] = case["cand"]
+        for K, want in case["topk"].items():
+            idx, sc, _ = oracle.topk_cand(b, q_idx, "f32", w, k, "f32", None, 2, 2, cand, int(K))
+            assert idx[r].tolist() == want, (case, K, idx[r])
+            assert sc[r].tolist() == [float(x) for x in case["scores"]], (case, sc[r])
+
+
+def _cand_args(wl):
+    return (oracle.Batch.of(wl), wl.q_idx, wl.q_idx_dtype, wl.w, wl.k_idx, wl.k_idx_dtype,
+            wl.k_scale, wl.Hi, wl.Di)
+
+
+@pytest.mark.parametrize("name,over", [("c0", {}),
+                                       ("c1", dict(batch=3, ctx=300, K=64, Hq=2, Dqk=16,
+                                                   Dv=8))])
+def test_all_positions_as_candidates_equal_full_selection(name, over):
+    """With every position 0..pos listed, candidate-restricted selection is
+    the full selection (the unrestricted path is pinned above)."""
+    wl = synth.make(name, **over)
+    args = _cand_args(wl)
+    sc = oracle.indexer_scores(args[0], *args[1:], ld=wl.max_ctx)
+    full = oracle.topk(args[0], sc, wl.K)
+    cand = np.tile(np.arange(wl.max_ctx, dtype=np.int32), (wl.n_q, 1))
+    idx, csc, _ = oracle.topk_cand(*args, cand, wl.K)
+    assert np.array_equal(idx, full)
+    assert np.array_equal(csc, sc)
+
+
+def test_candidate_list_order_and_non_candidates_do_not_matter():
+    """Shuffling each row's list, or adding -1 entries and positions past the
+    row, leaves the selection unchanged; each score follows its position."""
+    wl = synth.make("c1", batch=4, ctx=500, K=32, Hq=2, Dqk=16, Dv=8)
+    args = _cand_args(wl)
+    cand = synth.candidates(wl, 96, seed=3)
+    idx, sc, _ = oracle.topk_cand(*args, cand, wl.K)
+    rng = np.random.default_rng(7)
+    perm = np.stack([rng.permutation(cand.shape[1]) for _ in range(wl.n_q)])
+    shuf = np.take_along_axis(cand, perm, axis=1)
+    idx2, sc2, _ = oracle.topk_cand(*args, shuf, wl.K)
+    assert np.array_equal(idx2, idx)
+    assert np.array_equal(sc2, np.take_along_axis(sc, perm, axis=1))
+    extra = np.concatenate([cand, np.full((wl.n_q, 5), -1, np.int32),
+                            (wl.q_pos[:, None] + 1 + np.arange(5)).astype(np.int32)], axis=1)
+    idx3, sc3, _ = oracle.topk_cand(*args, extra, wl.K)
+    assert np.array_equal(idx3, idx)
+    assert np.all(np.isneginf(sc3[:, cand.shape[1]:]))
+
+
+def test_fewer_candidates_than_k_returns_all_of_them():
+    wl = synth.make("c1", batch=3, ctx=400, K=64, Hq=2, Dqk=16, Dv=8)
+    args = _cand_args(wl)
+    cand = synth.candidates(wl, 40, seed=1)
+    idx, _, kth = oracle.topk_cand(*args, cand, wl.K)
+    for r in range(wl.n_q):
+        valid = cand[r][cand[r] >= 0]
+        assert idx[r, :len(valid)].tolist() == sorted(valid.tolist())
+        assert np.all(idx[r, len(valid):] == -1)
+        assert np.isnan(kth[r, 0])
