@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define SI_VERSION 3
+#define SI_VERSION 4
 
 typedef enum si_status {
     SI_OK = 0,
@@ -198,6 +198,35 @@ si_status si_sparse_attn(const si_batch *b, const si_attention *at, const int32_
 si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_attention *at,
                           int32_t k_top, int32_t *idx, void *out, si_dtype out_dtype,
                           float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* Candidate-restricted selection (the vLLM article on DeepSeek-V4.1,
+ * "Kernels": the sparse MQA indexer logits are computed over a fixed set of
+ * candidate positions per query instead of the whole context; the selection
+ * rule is that of section 2.2).
+ * cand: device int32 [n_q, ld_cand], ld_cand >= n_cand >= 1.  Row r's
+ *   candidates are its list entries s with 0 <= s <= q_pos[r]; they must come
+ *   first and in strictly ascending order.  Entries after them that are -1 or
+ *   above q_pos[r] are not candidates.  A candidate that does not follow a
+ *   lower candidate raises SI_DEVFLAG_BAD_INDEX, and the row's result is then
+ *   undefined.  A candidate whose page is invalid raises SI_DEVFLAG_BAD_BLOCK
+ *   and is dropped.
+ * idx: device int32 [n_q, k_top].  Row r receives the k_top candidates with the
+ *   largest score(r, s) (equal scores: the lower position wins; -0 equals +0),
+ *   in ascending order.  A row with fewer than k_top candidates receives all
+ *   of them, followed by -1 padding.
+ * scores: device float [n_q, ld_scores] with ld_scores >= n_cand, or NULL.
+ *   Column j receives the score of list entry j, and -inf where that entry is
+ *   not a candidate; columns n_cand..ld_scores-1 get -inf.
+ * ws: at least si_workspace_size_cand(b, ix, n_cand) bytes.  It holds the
+ *   gathered candidate key rows (n_q x n_cand rounded up to 128, key row
+ *   stride bytes each), their scales, the scores when `scores` is NULL, and
+ *   the status word.
+ * Uses the same indexer operands and kernels as si_indexer_scores / si_topk. */
+size_t si_workspace_size_cand(const si_batch *b, const si_indexer *ix, int32_t n_cand);
+si_status si_indexer_topk_cand(const si_batch *b, const si_indexer *ix, const int32_t *cand,
+                               int32_t n_cand, int64_t ld_cand, int32_t k_top, int32_t *idx,
+                               float *scores, int64_t ld_scores, void *ws, size_t ws_bytes,
+                               void *stream);
 
 /* si_fused_decode without a workspace, for callers that cannot allocate
  * device memory (for instance code running inside an allocator's callbacks,

@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
         "si_fused_decode": (ctypes.c_int, [B, IX, AT, I32, P, P, ctypes.c_int, P, P, SZ, P]),
         "si_fused_decode_noalloc": (ctypes.c_int, [B, IX, AT, I32, P, P, ctypes.c_int, P,
                                                    ctypes.POINTER(ctypes.c_void_p), P]),
+        "si_workspace_size_cand": (SZ, [B, IX, I32]),
+        "si_indexer_topk_cand": (ctypes.c_int, [B, IX, P, I32, I64, I32, P, P, I64, P, SZ, P]),
         "si_workspace_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), P]),
         "si_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "si_last_error": (ctypes.c_char_p, []),
@@ -101,7 +103,8 @@ def load() -> ctypes.CDLL:
 load()
 
 EXPORTED = ("si_workspace_size", "si_workspace_min", "si_indexer_scores", "si_topk",
-            "si_sparse_attn", "si_fused_decode", "si_fused_decode_noalloc", "si_workspace_status",
+            "si_sparse_attn", "si_fused_decode", "si_fused_decode_noalloc",
+            "si_workspace_size_cand", "si_indexer_topk_cand", "si_workspace_status",
             "si_status_string",
             "si_last_error", "si_version", "si_launch_count")
 
@@ -230,6 +233,23 @@ def topk(b: Batch, scores: torch.Tensor, k_top: int, idx: torch.Tensor, ws: torc
     cb = b.c()
     _check(load().si_topk(ctypes.byref(cb), _ptr(scores), scores.shape[-1], k_top, _ptr(idx),
                           _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def workspace_size_cand(b: Batch, ix: Indexer, n_cand: int) -> int:
+    cb, ci = b.c(), ix.c()
+    return int(load().si_workspace_size_cand(ctypes.byref(cb), ctypes.byref(ci), n_cand))
+
+
+def indexer_topk_cand(b: Batch, ix: Indexer, cand: torch.Tensor, k_top: int, idx: torch.Tensor,
+                      ws: torch.Tensor, scores: Optional[torch.Tensor] = None, stream=None):
+    """Candidate-restricted selection: cand [n_q, n_cand] int32 positions per
+    row (candidates first, strictly ascending; -1 or past the row after them)."""
+    cb, ci = b.c(), ix.c()
+    ld_s = scores.shape[-1] if scores is not None else 0
+    _check(load().si_indexer_topk_cand(ctypes.byref(cb), ctypes.byref(ci), _ptr(cand),
+                                       cand.shape[-1], cand.shape[-1], k_top, _ptr(idx),
+                                       _ptr(scores), ld_s, _ptr(ws), ws.numel(),
+                                       _stream(stream)))
 
 
 def _out_dtype(out: torch.Tensor) -> int:

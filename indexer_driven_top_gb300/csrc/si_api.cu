@@ -309,9 +309,119 @@ size_t ws_need(si_op op, const si_batch *b, const si_indexer *ix, const si_atten
     return n + extra;
 }
 
+// Workspace of a candidate-restricted selection: status word, the synthetic
+// batch's arrays, gathered key rows and scales, scores.
+struct CandLayout {
+    si::CandView v;
+    size_t keys, scales, scores, total;
+    int64_t ld;  // scores row stride when they live in the workspace
+};
+
+CandLayout cand_layout(const si_batch &b, const si_indexer &ix, int32_t n_cand, void *ws)
+{
+    CandLayout L{};
+    const int64_t n_q = b.n_q;
+    L.v.n_pad = (int32_t)round_up((size_t)n_cand, si::kCandPage);
+    L.v.blocks_per_row = L.v.n_pad / si::kCandPage;
+    L.v.row_bytes = ix.k.row_stride * (int64_t)dtype_bytes(ix.k.dtype);
+    char *base = static_cast<char *>(ws);
+    size_t off = si::kStatusBytes;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += round_up(bytes, 256);
+        return at;
+    };
+    const size_t bt = take((size_t)n_q * L.v.blocks_per_row * 4);
+    const size_t qs = take((size_t)n_q * 4), qp = take((size_t)n_q * 4),
+                 cl = take((size_t)n_q * 4);
+    L.keys = take((size_t)n_q * L.v.n_pad * L.v.row_bytes);
+    L.scales = take((size_t)n_q * L.v.n_pad * 4);
+    L.ld = (int64_t)round_up((size_t)n_cand, 64);
+    L.scores = take((size_t)n_q * L.ld * 4);
+    L.total = off;
+    if (base) {
+        L.v.block_table = reinterpret_cast<int32_t *>(base + bt);
+        L.v.q_seq = reinterpret_cast<int32_t *>(base + qs);
+        L.v.q_pos = reinterpret_cast<int32_t *>(base + qp);
+        L.v.ctx_len = reinterpret_cast<int32_t *>(base + cl);
+    }
+    return L;
+}
+
+constexpr int32_t kMaxCand = 1 << 24;
+
 }  // namespace
 
 extern "C" {
+
+size_t si_workspace_size_cand(const si_batch *b, const si_indexer *ix, int32_t n_cand)
+{
+    if (check_batch(b) != SI_OK || check_indexer(ix) != SI_OK || n_cand < 1 || n_cand > kMaxCand)
+        return 0;
+    return cand_layout(*b, *ix, n_cand, nullptr).total;
+}
+
+si_status si_indexer_topk_cand(const si_batch *b, const si_indexer *ix, const int32_t *cand,
+                               int32_t n_cand, int64_t ld_cand, int32_t k_top, int32_t *idx,
+                               float *scores, int64_t ld_scores, void *ws, size_t ws_bytes,
+                               void *stream)
+{
+    si_status st = check_batch(b);
+    if (st != SI_OK || b->n_q == 0)
+        return st;
+    if ((st = check_indexer(ix)) != SI_OK || (st = check_k(k_top)) != SI_OK)
+        return st;
+    if (!cand || !idx)
+        return fail(SI_ERR_INVALID_ARG, "cand or idx is NULL");
+    if (n_cand < 1 || n_cand > kMaxCand)
+        return fail(SI_ERR_INVALID_ARG, "n_cand %d outside 1..%d", n_cand, kMaxCand);
+    if (ld_cand < n_cand)
+        return fail(SI_ERR_INVALID_ARG, "ld_cand %lld < n_cand %d", (long long)ld_cand, n_cand);
+    if (scores && ld_scores < n_cand)
+        return fail(SI_ERR_INVALID_ARG, "ld_scores %lld < n_cand %d", (long long)ld_scores,
+                    n_cand);
+    const CandLayout need = cand_layout(*b, *ix, n_cand, nullptr);
+    if ((st = check_ws(ws, ws_bytes, need.total)) != SI_OK)
+        return st;
+    const CandLayout L = cand_layout(*b, *ix, n_cand, ws);
+    cudaStream_t s = (cudaStream_t)stream;
+    unsigned int *stw = status_word(ws);
+    char *base = static_cast<char *>(ws);
+    uint8_t *keys = reinterpret_cast<uint8_t *>(base + L.keys);
+    float *scl = reinterpret_cast<float *>(base + L.scales);
+    // the candidates as one private sequence per query row
+    si_batch cb = *b;
+    cb.block_table = L.v.block_table;
+    cb.ctx_len = L.v.ctx_len;
+    cb.q_seq = L.v.q_seq;
+    cb.q_pos = L.v.q_pos;
+    cb.n_seq = b->n_q;
+    cb.max_blocks = L.v.blocks_per_row;
+    cb.page_size = si::kCandPage;
+    cb.max_ctx = n_cand;
+    cb.n_blocks = b->n_q * L.v.blocks_per_row;
+    cb.host_q_seq = nullptr;
+    si_indexer cix = *ix;
+    cix.k.data = keys;
+    cix.k.scale = scl;
+    float *sc = scores ? scores : reinterpret_cast<float *>(base + L.scores);
+    const int64_t ld = scores ? ld_scores : L.ld;
+    cudaError_t e = si::launch_cand_gather(*b, cand, ld_cand, n_cand, L.v, ix->k, keys, scl, stw, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "candidate gather launch");
+    if ((st = run_indexer(cb, cix, sc, ld, stw, s)) != SI_OK)
+        return st;
+    if (!si::indexer_tc_supported(cb, cix, ld)) {
+        // the CUDA-core indexer multiplies by the -1 scale of an empty slot
+        e = si::launch_cand_mask(b->n_q, n_cand, L.v, scl, sc, ld, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "candidate mask launch");
+    }
+    if ((st = run_topk(cb, sc, ld, k_top, idx, stw, s)) != SI_OK)
+        return st;
+    e = si::launch_cand_map(b->n_q, cand, ld_cand, n_cand, L.v, scl, k_top, idx, s);
+    return e == cudaSuccess ? SI_OK : cuda_fail(e, "candidate map launch");
+}
 
 size_t si_workspace_size(si_op op, const si_batch *b, const si_indexer *ix,
                          const si_attention *at, int32_t k_top)

@@ -1,0 +1,186 @@
+// si_cand.cu -- candidate-restricted selection: the indexer scores only a
+// given list of candidate positions per query row instead of the whole
+// context, and the Top-K is taken among them.
+//
+// The vLLM article on DeepSeek-V4.1 ("Kernels") computes the sparse MQA
+// indexer logits over a fixed candidate set per query; at long contexts that
+// replaces the full-context scoring.  The selection rule is that of "Day0
+// Inference Support and Performance Optimization for New Architecture LLMs",
+// section 2.2 (head-weighted ReLU scores, Top-K, ties to the lower position).
+//
+// GB300 mapping.  The scoring kernels stay as they are: k_cand_gather copies
+// each row's candidate key rows (and their dequantisation scales) out of the
+// paged cache into the workspace, laid out as one private sequence per query
+// row with pages of 128 rows, so that candidate slot j of row r is position j
+// of sequence r.  The tensor-core indexer then scores these sequences exactly
+// as it scores a decode batch (a candidate that is not one -- a -1 entry, a
+// position after the row's own, a bad block -- gets scale -1, which the
+// indexer turns into -inf; the CUDA-core indexer's scores are masked by
+// k_cand_mask instead), the radix Top-K selects candidate slots, and
+// k_cand_map turns the slots back into positions.  Candidate lists hold their
+// candidates first and in strictly ascending order, so slot order is position
+// order: the Top-K's tie rule and ascending output carry over unchanged.
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "si_common.cuh"
+#include "si_internal.h"
+
+namespace si {
+
+namespace {
+
+// Gathers candidate key rows: one thread per (row, slot, unit) with a unit of
+// 16 bytes when the row size allows it, else 1 byte.  Also writes the
+// synthetic batch (identity block table, one sequence per row).
+__global__ void k_cand_gather(si_batch b, const int32_t *cand, int64_t ld_cand, int32_t n_cand,
+                              CandView v, const uint8_t *kdata, const float *kscale,
+                              uint8_t *keys, float *scales, unsigned int *st)
+{
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nth = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = tid; i < (int64_t)b.n_q * v.blocks_per_row; i += nth)
+        v.block_table[i] = (int32_t)i;
+    for (int64_t r = tid; r < b.n_q; r += nth) {
+        v.q_seq[r] = (int32_t)r;
+        v.q_pos[r] = n_cand - 1;
+        v.ctx_len[r] = n_cand;
+    }
+    const int unit = (v.row_bytes % 16 == 0) ? 16 : 1;
+    const int64_t units = v.row_bytes / unit;
+    const int64_t total = (int64_t)b.n_q * v.n_pad * units;
+    for (int64_t u = tid; u < total; u += nth) {
+        const int64_t slot = u / units;  // r * n_pad + j
+        const int64_t uu = u % units;
+        const int r = (int)(slot / v.n_pad), j = (int)(slot % v.n_pad);
+        const int64_t cb = (int64_t)r * ld_cand;
+        const int s = j < n_cand ? __ldg(cand + cb + j) : -1;
+        const int pos = __ldg(b.q_pos + r), seq = __ldg(b.q_seq + r);
+        int64_t prow = -1;
+        if (s >= 0 && s <= pos) {
+            // a candidate follows a candidate with a lower position
+            if (uu == 0 && j > 0) {
+                const int sp = __ldg(cand + cb + j - 1);
+                if (!(sp >= 0 && sp < s))
+                    raise_flag(st, SI_DEVFLAG_BAD_INDEX);
+            }
+            const int lb = s / b.page_size;
+            if ((unsigned)seq < (unsigned)b.n_seq && lb < b.max_blocks) {
+                const int blk = __ldg(b.block_table + (int64_t)seq * b.max_blocks + lb);
+                if ((unsigned)blk < (unsigned)b.n_blocks)
+                    prow = (int64_t)blk * b.page_size + s % b.page_size;
+            }
+            if (prow < 0 && uu == 0)
+                raise_flag(st, SI_DEVFLAG_BAD_BLOCK);
+        }
+        uint8_t *dst = keys + slot * v.row_bytes;
+        if (unit == 16) {
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (prow >= 0)
+                x = __ldg(reinterpret_cast<const uint4 *>(kdata + prow * v.row_bytes) + uu);
+            reinterpret_cast<uint4 *>(dst)[uu] = x;
+        } else {
+            dst[uu] = prow >= 0 ? __ldg(kdata + prow * v.row_bytes + uu) : (uint8_t)0;
+        }
+        if (uu == 0)
+            scales[slot] = prow >= 0 ? (kscale ? __ldg(kscale + prow) : 1.f) : -1.f;
+    }
+}
+
+// -inf for the slots that hold no candidate (CUDA-core indexer path).
+__global__ void k_cand_mask(int32_t n_q, int32_t n_cand, CandView v, const float *scales,
+                            float *scores, int64_t ld)
+{
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nth = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = tid; i < (int64_t)n_q * n_cand; i += nth) {
+        const int64_t r = i / n_cand, j = i % n_cand;
+        if (scales[r * v.n_pad + j] < 0.f)
+            scores[r * ld + j] = -INFINITY;
+    }
+}
+
+constexpr int kMapThreads = 1024;
+constexpr int kMapPer = 16;  // k_top <= 16384 entries per row
+
+// Slots selected by the Top-K -> positions, in place: slots without a
+// candidate (selected only when a row has fewer than k_top candidates) are
+// dropped, the rest keep their ascending order, -1 pads the tail.
+__global__ void __launch_bounds__(kMapThreads)
+k_cand_map(const int32_t *cand, int64_t ld_cand, int32_t n_cand, CandView v, const float *scales,
+           int32_t k_top, int32_t *idx)
+{
+    __shared__ int sbuf[33];
+    const int r = blockIdx.x, tid = threadIdx.x;
+    int32_t *out = idx + (int64_t)r * k_top;
+    const int per = (k_top + kMapThreads - 1) / kMapThreads;
+    int val[kMapPer];
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < kMapPer; e++) {
+        val[e] = -1;
+        const int k = tid * per + e;
+        if (e < per && k < k_top) {
+            const int j = out[k];
+            if (j >= 0 && j < n_cand && scales[(int64_t)r * v.n_pad + j] >= 0.f)
+                val[e] = __ldg(cand + (int64_t)r * ld_cand + j);
+            cnt += val[e] >= 0;
+        }
+    }
+    int total;
+    int o = block_exclusive_scan(cnt, &total, sbuf);  // all reads of out[] happen before
+#pragma unroll
+    for (int e = 0; e < kMapPer; e++)
+        if (val[e] >= 0)
+            out[o++] = val[e];
+    for (int k = total + tid; k < k_top; k += kMapThreads)
+        out[k] = -1;
+}
+
+int grid_for(int64_t work, int threads)
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 1;
+    const int64_t want = (work + threads - 1) / threads;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * 8));
+}
+
+}  // namespace
+
+cudaError_t launch_cand_gather(const si_batch &b, const int32_t *cand, int64_t ld_cand,
+                               int32_t n_cand, const CandView &v, const si_paged &k,
+                               uint8_t *keys, float *scales, unsigned int *st, cudaStream_t s)
+{
+    const int64_t units = v.row_bytes % 16 == 0 ? v.row_bytes / 16 : v.row_bytes;
+    const int grid = grid_for((int64_t)b.n_q * v.n_pad * units, 256);
+    count_launch();
+    k_cand_gather<<<grid, 256, 0, s>>>(b, cand, ld_cand, n_cand, v,
+                                       static_cast<const uint8_t *>(k.data), k.scale, keys,
+                                       scales, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cand_mask(int32_t n_q, int32_t n_cand, const CandView &v, const float *scales,
+                             float *scores, int64_t ld, cudaStream_t s)
+{
+    const int grid = grid_for((int64_t)n_q * n_cand, 256);
+    count_launch();
+    k_cand_mask<<<grid, 256, 0, s>>>(n_q, n_cand, v, scales, scores, ld);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cand_map(int32_t n_q, const int32_t *cand, int64_t ld_cand, int32_t n_cand,
+                            const CandView &v, const float *scales, int32_t k_top, int32_t *idx,
+                            cudaStream_t s)
+{
+    if (k_top > kMapThreads * kMapPer)
+        return cudaErrorInvalidValue;
+    count_launch();
+    k_cand_map<<<n_q, kMapThreads, 0, s>>>(cand, ld_cand, n_cand, v, scales, k_top, idx);
+    return cudaGetLastError();
+}
+
+}  // namespace si

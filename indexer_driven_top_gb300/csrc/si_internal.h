@@ -53,4 +53,32 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
 cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,
                         int32_t *idx, unsigned int *st, cudaStream_t s);
 
+// Candidate-restricted selection (si_cand.cu).  The candidates of query row r
+// are gathered into a private sequence r of a workspace cache with pages of
+// kCandPage rows; CandView holds that synthetic batch's device arrays and the
+// gathered rows' geometry.
+constexpr int32_t kCandPage = 128;
+struct CandView {
+    int32_t *block_table;     // [n_q, blocks_per_row]: identity
+    int32_t *q_seq;           // [n_q]: r
+    int32_t *q_pos;           // [n_q]: n_cand - 1
+    int32_t *ctx_len;         // [n_q]: n_cand
+    int32_t blocks_per_row;   // n_pad / kCandPage
+    int32_t n_pad;            // slots per row: n_cand rounded up to kCandPage
+    int64_t row_bytes;        // bytes per key row (row_stride x element size)
+};
+// Gathers the candidate key rows and scales (scale -1 for a slot without a
+// candidate) and writes the synthetic batch's arrays.
+cudaError_t launch_cand_gather(const si_batch &b, const int32_t *cand, int64_t ld_cand,
+                               int32_t n_cand, const CandView &v, const si_paged &k,
+                               uint8_t *keys, float *scales, unsigned int *st, cudaStream_t s);
+// Sets -inf where a slot holds no candidate (for indexers that do not read
+// the -1 scale as "no key").
+cudaError_t launch_cand_mask(int32_t n_q, int32_t n_cand, const CandView &v, const float *scales,
+                             float *scores, int64_t ld, cudaStream_t s);
+// Turns the selected slots into ascending positions, -1 padded, in place.
+cudaError_t launch_cand_map(int32_t n_q, const int32_t *cand, int64_t ld_cand, int32_t n_cand,
+                            const CandView &v, const float *scales, int32_t k_top, int32_t *idx,
+                            cudaStream_t s);
+
 }  // namespace si

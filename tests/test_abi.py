@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(si):
 
 def test_version_and_status_strings(si):
     lib = si.load()
-    assert lib.si_version() == 3
+    assert lib.si_version() == 4
     assert lib.si_status_string(0) == b"ok"
     assert lib.si_status_string(3) == b"workspace error"
 
@@ -111,3 +111,35 @@ def test_workspace_sizes(si):
     mn = lib.si_workspace_min(3, ctypes.byref(b), None, None, 8)
     assert fused >= mn >= 256 + 256 * 4
     assert lib.si_workspace_size(1, None, None, None, 8) == 0
+
+
+def test_candidate_selection_host_validation_and_sizes(si):
+    """si_indexer_topk_cand rejects bad lists, strides and workspaces on the
+    host; its workspace holds the gathered rows, scales and scores."""
+    lib = si.load()
+    P = ctypes.c_void_p
+    fake = 1 << 20
+    ws = 256 << 20
+    b = ctypes.byref(_batch(si))
+    ix = si.c_indexer(fake, si.BF16, None, fake, 64, 128, si.c_paged(fake, None, si.E4M3, 128, 128))
+    need = lib.si_workspace_size_cand(b, ctypes.byref(ix), 300)
+    # status + 4 small arrays + 2 rows x 384 slots x (128-byte key + 4-byte scale) + scores
+    assert need >= 256 + 2 * 384 * (128 + 4) + 2 * 320 * 4
+    assert lib.si_workspace_size_cand(b, ctypes.byref(ix), 0) == 0
+    args = lambda **kw: dict(dict(cand=P(fake), n_cand=300, ld_cand=300, k_top=8, idx=P(fake),
+                                  scores=None, ld_scores=0, ws=P(ws), ws_bytes=need), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return lib.si_indexer_topk_cand(b, ctypes.byref(ix), a["cand"], a["n_cand"], a["ld_cand"],
+                                        a["k_top"], a["idx"], a["scores"], a["ld_scores"],
+                                        a["ws"], a["ws_bytes"], None)
+    assert call(cand=None) == 1
+    assert call(n_cand=0) == 1
+    assert call(ld_cand=299) == 1 and b"ld_cand" in lib.si_last_error()
+    assert call(scores=P(fake), ld_scores=100) == 1 and b"ld_scores" in lib.si_last_error()
+    assert call(k_top=0) == 1
+    assert call(ws_bytes=need - 1) == 3
+    assert call(ws=P(ws + 16)) == 3
+    assert lib.si_indexer_topk_cand(ctypes.byref(_batch(si, n_q=0)), ctypes.byref(ix), None, 0, 0,
+                                    8, None, None, 0, None, 0, None) == 0
