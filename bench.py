@@ -373,6 +373,71 @@ def prefill_indexer(si, dev, steps):
                                    "executes twice the algorithmic FP8 work"}}
 
 
+def candidate_selection(si, dev, steps, n_cand=16384):
+    """Candidate-restricted selection (the vLLM article on DeepSeek-V4.1,
+    "Kernels": indexer logits over a fixed candidate set per query) on the
+    long-context decode workload (16 rows x 131072 positions, 1 % planted
+    keys) with n_cand seeded candidates per row, timed beside the
+    full-context indexer + Top-K of the same rows.  The attention operands
+    are not needed and are generated at a token size (the indexer inputs are
+    drawn first and do not change).  L2 is flushed before every timed call.
+    Algorithmic bytes of the candidate call: per candidate its list entry
+    (4 B), key row (e4m3) and scale (4 B) and its score (4 B); per row the
+    indexer query (bf16), the head weights and the K output indices."""
+    import torch
+    import synth
+    wl = synth.make("c3", Hq=1, Dqk=64, Dv=64)
+    cand = synth.candidates(wl, n_cand, seed=31)
+    dw = si.upload(wl, dev)
+    b, ix, K = dw.batch, dw.indexer, dw.k_top
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ws_full = si.alloc_workspace(si.workspace_size(si.OP_TOPK, b, ix, None, K), dev)
+    scores = torch.empty((wl.n_q, b.max_ctx), dtype=torch.float32, device=dev)
+    idx = torch.empty((wl.n_q, K), dtype=torch.int32, device=dev)
+    c = torch.from_numpy(cand).to(dev)
+    ws_c = si.alloc_workspace(si.workspace_size_cand(b, ix, n_cand), dev)
+    idx_c = torch.empty((wl.n_q, K), dtype=torch.int32, device=dev)
+
+    def full():
+        si.indexer_scores(b, ix, scores, ws_full, stream)
+        si.topk(b, scores, K, idx, ws_full, stream)
+
+    def restricted():
+        si.indexer_topk_cand(b, ix, c, K, idx_c, ws_c, stream=stream)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        n = max(5, min(steps, 50))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+        for i in range(n):
+            flush.zero_()
+            ev[2 * i].record(stream)
+            fn()
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n)) / n
+
+    ms_full, ms_c = timed(full), timed(restricted)
+    assert si.workspace_status(ws_c, stream) == 0 and si.workspace_status(ws_full, stream) == 0
+    key_bytes = wl.Di + 4
+    nbytes = (wl.n_q * n_cand * (4 + key_bytes + 4)
+              + wl.n_q * (wl.Hi * wl.Di * 2 + wl.Hi * 4 + K * 4))
+    peaks = _peaks()
+    gbs = nbytes / (ms_c / 1e3) / 1e9
+    return {"workload": "decode batch 16 x context 131072 (1% planted keys), "
+                        f"{n_cand} candidates per row, indexer 64x128 fp8, top-k {K}",
+            "call": "si_indexer_topk_cand (gather, indexer, top-k, map)",
+            "ms_per_call": ms_c, "queries_per_s": wl.n_q / (ms_c / 1e3),
+            "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
+            "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+            "full_context": {"call": "si_indexer_scores + si_topk over all 131072 positions",
+                             "ms_per_call": ms_full},
+            "speedup_vs_full_context": ms_full / ms_c,
+            "l2": "flushed before every timed call (512 MiB write)"}
+
+
 def _workload_name(wl):
     names = {
         "c1": "decode batch 64 x context 8192, indexer 64x128 fp8, top-k 2048, MLA 128x576 bf16",
@@ -591,7 +656,18 @@ def main():
                     help="store the latent KV cache in FP8 (one scale per row and 128-entry tile)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill indexer (both query formats) and print its record")
+    ap.add_argument("--cand-only", action="store_true",
+                    help="time only candidate-restricted selection (16 x 131072, 16384 candidates "
+                         "per row) beside the full-context indexer + Top-K, and print its record")
     args = ap.parse_args()
+    if args.cand_only:
+        import torch
+        import indexer_driven_top_gb300 as si
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"candidate_selection": candidate_selection(si, dev, args.steps)}),
+              flush=True)
+        return
     if args.prefill_only:
         import torch
         import indexer_driven_top_gb300 as si

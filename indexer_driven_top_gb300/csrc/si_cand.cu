@@ -31,9 +31,13 @@ namespace si {
 
 namespace {
 
-// Gathers candidate key rows: one thread per (row, slot, unit) with a unit of
-// 16 bytes when the row size allows it, else 1 byte.  Also writes the
-// synthetic batch (identity block table, one sequence per row).
+// Gathers candidate key rows.  A warp takes 32 consecutive slots of one row:
+// lane l resolves slot l (list entry -> block table -> physical row) and
+// writes its scale; then the warp copies the 32 rows in units of 16 bytes
+// (1 byte when the row size is not a multiple of 16), each lane issuing up to
+// eight independent loads before their stores, so that a warp has many row
+// pieces in flight.  Also writes the synthetic batch (identity block table,
+// one sequence per row).
 __global__ void k_cand_gather(si_batch b, const int32_t *cand, int64_t ld_cand, int32_t n_cand,
                               CandView v, const uint8_t *kdata, const float *kscale,
                               uint8_t *keys, float *scales, unsigned int *st)
@@ -47,12 +51,13 @@ __global__ void k_cand_gather(si_batch b, const int32_t *cand, int64_t ld_cand, 
         v.q_pos[r] = n_cand - 1;
         v.ctx_len[r] = n_cand;
     }
-    const int unit = (v.row_bytes % 16 == 0) ? 16 : 1;
-    const int64_t units = v.row_bytes / unit;
-    const int64_t total = (int64_t)b.n_q * v.n_pad * units;
-    for (int64_t u = tid; u < total; u += nth) {
-        const int64_t slot = u / units;  // r * n_pad + j
-        const int64_t uu = u % units;
+    const int lane = threadIdx.x & 31;
+    const bool vec = v.row_bytes % 16 == 0;
+    const int64_t units = vec ? v.row_bytes / 16 : v.row_bytes;  // per key row
+    const int64_t groups = (int64_t)b.n_q * (v.n_pad / 32);       // n_pad is a multiple of 128
+    for (int64_t gi = tid >> 5; gi < groups; gi += nth >> 5) {
+        const int64_t slot0 = gi * 32;
+        const int64_t slot = slot0 + lane;
         const int r = (int)(slot / v.n_pad), j = (int)(slot % v.n_pad);
         const int64_t cb = (int64_t)r * ld_cand;
         const int s = j < n_cand ? __ldg(cand + cb + j) : -1;
@@ -60,7 +65,7 @@ __global__ void k_cand_gather(si_batch b, const int32_t *cand, int64_t ld_cand, 
         int64_t prow = -1;
         if (s >= 0 && s <= pos) {
             // a candidate follows a candidate with a lower position
-            if (uu == 0 && j > 0) {
+            if (j > 0) {
                 const int sp = __ldg(cand + cb + j - 1);
                 if (!(sp >= 0 && sp < s))
                     raise_flag(st, SI_DEVFLAG_BAD_INDEX);
@@ -71,20 +76,43 @@ __global__ void k_cand_gather(si_batch b, const int32_t *cand, int64_t ld_cand, 
                 if ((unsigned)blk < (unsigned)b.n_blocks)
                     prow = (int64_t)blk * b.page_size + s % b.page_size;
             }
-            if (prow < 0 && uu == 0)
+            if (prow < 0)
                 raise_flag(st, SI_DEVFLAG_BAD_BLOCK);
         }
-        uint8_t *dst = keys + slot * v.row_bytes;
-        if (unit == 16) {
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (prow >= 0)
-                x = __ldg(reinterpret_cast<const uint4 *>(kdata + prow * v.row_bytes) + uu);
-            reinterpret_cast<uint4 *>(dst)[uu] = x;
-        } else {
-            dst[uu] = prow >= 0 ? __ldg(kdata + prow * v.row_bytes + uu) : (uint8_t)0;
+        scales[slot] = prow >= 0 ? (kscale ? __ldg(kscale + prow) : 1.f) : -1.f;
+        // unit t of the group (t = k * 32 + lane) is unit t % units of slot t / units
+        for (int64_t k0 = 0; k0 < units; k0 += 8) {
+            if (vec) {
+                uint4 x[8];
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    x[k] = make_uint4(0u, 0u, 0u, 0u);
+                    if (k0 + k < units) {  // the same for every lane
+                        const int64_t t = (k0 + k) * 32 + lane;
+                        const int c = (int)(t / units);
+                        const long long pr = __shfl_sync(0xffffffffu, (long long)prow, c);
+                        if (pr >= 0)
+                            x[k] = __ldg(reinterpret_cast<const uint4 *>(kdata + pr * v.row_bytes) +
+                                         t % units);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    if (k0 + k < units) {
+                        const int64_t t = (k0 + k) * 32 + lane;
+                        reinterpret_cast<uint4 *>(keys + (slot0 + t / units) * v.row_bytes)[t % units] =
+                            x[k];
+                    }
+            } else {
+                for (int k = 0; k < 8 && k0 + k < units; k++) {
+                    const int64_t t = (k0 + k) * 32 + lane;
+                    const int c = (int)(t / units);
+                    const long long pr = __shfl_sync(0xffffffffu, (long long)prow, c);
+                    keys[(slot0 + c) * v.row_bytes + t % units] =
+                        pr >= 0 ? __ldg(kdata + pr * v.row_bytes + t % units) : (uint8_t)0;
+                }
+            }
         }
-        if (uu == 0)
-            scales[slot] = prow >= 0 ? (kscale ? __ldg(kscale + prow) : 1.f) : -1.f;
     }
 }
 
@@ -138,14 +166,13 @@ k_cand_map(const int32_t *cand, int64_t ld_cand, int32_t n_cand, CandView v, con
         out[k] = -1;
 }
 
+// One thread per work item: the gather's loads form a chain (list entry ->
+// block table -> key row), so latency is hidden by many threads in flight,
+// not by a grid-stride loop.
 int grid_for(int64_t work, int threads)
 {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 1;
     const int64_t want = (work + threads - 1) / threads;
-    return (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * 8));
+    return (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)1 << 24));
 }
 
 }  // namespace
@@ -154,8 +181,8 @@ cudaError_t launch_cand_gather(const si_batch &b, const int32_t *cand, int64_t l
                                int32_t n_cand, const CandView &v, const si_paged &k,
                                uint8_t *keys, float *scales, unsigned int *st, cudaStream_t s)
 {
-    const int64_t units = v.row_bytes % 16 == 0 ? v.row_bytes / 16 : v.row_bytes;
-    const int grid = grid_for((int64_t)b.n_q * v.n_pad * units, 256);
+    // one warp per 32 slots
+    const int grid = grid_for((int64_t)b.n_q * v.n_pad, 256);
     count_launch();
     k_cand_gather<<<grid, 256, 0, s>>>(b, cand, ld_cand, n_cand, v,
                                        static_cast<const uint8_t *>(k.data), k.scale, keys,
