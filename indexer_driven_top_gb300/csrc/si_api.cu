@@ -317,9 +317,22 @@ struct CandLayout {
     int64_t ld;  // scores row stride when they live in the workspace
 };
 
+// With the tensor-core indexer the candidates are gathered inside the
+// scoring kernel and the workspace holds only the status word and scores.
+bool cand_fused(const si_batch &b, const si_indexer &ix, int32_t n_cand)
+{
+    return si::indexer_tc_supported(b, ix, (int64_t)round_up((size_t)n_cand, 64));
+}
+
 CandLayout cand_layout(const si_batch &b, const si_indexer &ix, int32_t n_cand, void *ws)
 {
     CandLayout L{};
+    if (cand_fused(b, ix, n_cand)) {
+        L.ld = (int64_t)round_up((size_t)n_cand, 64);
+        L.scores = si::kStatusBytes;
+        L.total = L.scores + round_up((size_t)b.n_q * L.ld * 4, 256);
+        return L;
+    }
     const int64_t n_q = b.n_q;
     L.v.n_pad = (int32_t)round_up((size_t)n_cand, si::kCandPage);
     L.v.blocks_per_row = L.v.n_pad / si::kCandPage;
@@ -387,39 +400,46 @@ si_status si_indexer_topk_cand(const si_batch *b, const si_indexer *ix, const in
     cudaStream_t s = (cudaStream_t)stream;
     unsigned int *stw = status_word(ws);
     char *base = static_cast<char *>(ws);
-    uint8_t *keys = reinterpret_cast<uint8_t *>(base + L.keys);
-    float *scl = reinterpret_cast<float *>(base + L.scales);
-    // the candidates as one private sequence per query row
-    si_batch cb = *b;
-    cb.block_table = L.v.block_table;
-    cb.ctx_len = L.v.ctx_len;
-    cb.q_seq = L.v.q_seq;
-    cb.q_pos = L.v.q_pos;
-    cb.n_seq = b->n_q;
-    cb.max_blocks = L.v.blocks_per_row;
-    cb.page_size = si::kCandPage;
-    cb.max_ctx = n_cand;
-    cb.n_blocks = b->n_q * L.v.blocks_per_row;
-    cb.host_q_seq = nullptr;
-    si_indexer cix = *ix;
-    cix.k.data = keys;
-    cix.k.scale = scl;
     float *sc = scores ? scores : reinterpret_cast<float *>(base + L.scores);
     const int64_t ld = scores ? ld_scores : L.ld;
-    cudaError_t e = si::launch_cand_gather(*b, cand, ld_cand, n_cand, L.v, ix->k, keys, scl, stw, s);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "candidate gather launch");
-    if ((st = run_indexer(cb, cix, sc, ld, stw, s)) != SI_OK)
-        return st;
-    if (!si::indexer_tc_supported(cb, cix, ld)) {
+    cudaError_t e;
+    if (cand_fused(*b, *ix, n_cand)) {
+        e = si::launch_indexer_tc_cand(*b, *ix, cand, ld_cand, n_cand, sc, ld, stw, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "candidate indexer launch");
+    } else {
+        uint8_t *keys = reinterpret_cast<uint8_t *>(base + L.keys);
+        float *scl = reinterpret_cast<float *>(base + L.scales);
+        // other shapes: the candidates gathered into one private sequence per
+        // query row, scored by the CUDA-core indexer
+        si_batch cb = *b;
+        cb.block_table = L.v.block_table;
+        cb.ctx_len = L.v.ctx_len;
+        cb.q_seq = L.v.q_seq;
+        cb.q_pos = L.v.q_pos;
+        cb.n_seq = b->n_q;
+        cb.max_blocks = L.v.blocks_per_row;
+        cb.page_size = si::kCandPage;
+        cb.max_ctx = n_cand;
+        cb.n_blocks = b->n_q * L.v.blocks_per_row;
+        cb.host_q_seq = nullptr;
+        si_indexer cix = *ix;
+        cix.k.data = keys;
+        cix.k.scale = scl;
+        e = si::launch_cand_gather(*b, cand, ld_cand, n_cand, L.v, ix->k, keys, scl, stw, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "candidate gather launch");
+        if ((st = run_indexer(cb, cix, sc, ld, stw, s)) != SI_OK)
+            return st;
         // the CUDA-core indexer multiplies by the -1 scale of an empty slot
         e = si::launch_cand_mask(b->n_q, n_cand, L.v, scl, sc, ld, s);
         if (e != cudaSuccess)
             return cuda_fail(e, "candidate mask launch");
     }
-    if ((st = run_topk(cb, sc, ld, k_top, idx, stw, s)) != SI_OK)
-        return st;
-    e = si::launch_cand_map(b->n_q, cand, ld_cand, n_cand, L.v, scl, k_top, idx, s);
+    e = si::launch_topk(*b, sc, ld, k_top, idx, stw, s, n_cand);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "top-k launch");
+    e = si::launch_cand_map(b->n_q, cand, ld_cand, n_cand, sc, ld, k_top, idx, s);
     return e == cudaSuccess ? SI_OK : cuda_fail(e, "candidate map launch");
 }
 

@@ -8,16 +8,15 @@
 // Inference Support and Performance Optimization for New Architecture LLMs",
 // section 2.2 (head-weighted ReLU scores, Top-K, ties to the lower position).
 //
-// GB300 mapping.  The scoring kernels stay as they are: k_cand_gather copies
-// each row's candidate key rows (and their dequantisation scales) out of the
-// paged cache into the workspace, laid out as one private sequence per query
-// row with pages of 128 rows, so that candidate slot j of row r is position j
-// of sequence r.  The tensor-core indexer then scores these sequences exactly
-// as it scores a decode batch (a candidate that is not one -- a -1 entry, a
-// position after the row's own, a bad block -- gets scale -1, which the
-// indexer turns into -inf; the CUDA-core indexer's scores are masked by
-// k_cand_mask instead), the radix Top-K selects candidate slots, and
-// k_cand_map turns the slots back into positions.  Candidate lists hold their
+// GB300 mapping.  With the 64 x 128 FP8-key shapes, the tensor-core indexer
+// gathers the candidate rows itself (k_indexer_tc<true>).  For other shapes,
+// k_cand_gather copies each row's candidate key rows (and their scales) out
+// of the paged cache into the workspace, laid out as one private sequence per
+// query row with pages of 128 rows, so that candidate slot j of row r is
+// position j of sequence r, and the CUDA-core indexer scores those sequences
+// (k_cand_mask then sets -inf where a slot holds no candidate).  Either way
+// the radix Top-K selects among the first n_cand slots of each row, and
+// k_cand_map turns the selected slots back into positions.  Candidate lists hold their
 // candidates first and in strictly ascending order, so slot order is position
 // order: the Top-K's tie rule and ascending output carry over unchanged.
 #include <stdint.h>
@@ -133,11 +132,12 @@ constexpr int kMapThreads = 1024;
 constexpr int kMapPer = 16;  // k_top <= 16384 entries per row
 
 // Slots selected by the Top-K -> positions, in place: slots without a
-// candidate (selected only when a row has fewer than k_top candidates) are
-// dropped, the rest keep their ascending order, -1 pads the tail.
+// candidate (score -inf; selected only when a row has fewer than k_top
+// candidates) are dropped, the rest keep their ascending order, -1 pads the
+// tail.
 __global__ void __launch_bounds__(kMapThreads)
-k_cand_map(const int32_t *cand, int64_t ld_cand, int32_t n_cand, CandView v, const float *scales,
-           int32_t k_top, int32_t *idx)
+k_cand_map(const int32_t *cand, int64_t ld_cand, int32_t n_cand, const float *scores,
+           int64_t ld_scores, int32_t k_top, int32_t *idx)
 {
     __shared__ int sbuf[33];
     const int r = blockIdx.x, tid = threadIdx.x;
@@ -151,7 +151,7 @@ k_cand_map(const int32_t *cand, int64_t ld_cand, int32_t n_cand, CandView v, con
         const int k = tid * per + e;
         if (e < per && k < k_top) {
             const int j = out[k];
-            if (j >= 0 && j < n_cand && scales[(int64_t)r * v.n_pad + j] >= 0.f)
+            if (j >= 0 && j < n_cand && scores[(int64_t)r * ld_scores + j] != -INFINITY)
                 val[e] = __ldg(cand + (int64_t)r * ld_cand + j);
             cnt += val[e] >= 0;
         }
@@ -200,13 +200,13 @@ cudaError_t launch_cand_mask(int32_t n_q, int32_t n_cand, const CandView &v, con
 }
 
 cudaError_t launch_cand_map(int32_t n_q, const int32_t *cand, int64_t ld_cand, int32_t n_cand,
-                            const CandView &v, const float *scales, int32_t k_top, int32_t *idx,
+                            const float *scores, int64_t ld_scores, int32_t k_top, int32_t *idx,
                             cudaStream_t s)
 {
     if (k_top > kMapThreads * kMapPer)
         return cudaErrorInvalidValue;
     count_launch();
-    k_cand_map<<<n_q, kMapThreads, 0, s>>>(cand, ld_cand, n_cand, v, scales, k_top, idx);
+    k_cand_map<<<n_q, kMapThreads, 0, s>>>(cand, ld_cand, n_cand, scores, ld_scores, k_top, idx);
     return cudaGetLastError();
 }
 

@@ -41,6 +41,15 @@
 //                       scaled head weights (double-buffered per row).
 // Work is the flattened list of (query row, tile) items split into equal
 // contiguous ranges, one per CTA.
+//
+// Candidate lists (k_indexer_tc<true>; the vLLM article on DeepSeek-V4.1,
+// "Kernels": logits over a fixed candidate set per query).  A tile is then
+// 128 consecutive slots of the row's candidate list, not of its positions:
+// the producer lanes resolve each slot (list entry -> block table -> physical
+// row) and gather the key rows with 16-byte cp.async pieces straight into the
+// stage's swizzled layout, and each key's scale into the scale ring; a slot
+// without a candidate gets a zero row and scale -1 (score -inf).  Everything
+// after the stage is the same pipeline.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -106,9 +115,65 @@ __device__ __forceinline__ uint16_t float2_to_e4m3x2(float a, float b)
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
+// Candidate-list operands of k_indexer_tc<true> (row r's list at cand + r * ld,
+// its first n entries scored).
+struct CandArgs {
+    const int32_t *cand;
+    int64_t ld;
+    int32_t n;
+};
+
+__device__ const float kScaleOne = 1.f;    // scale of a key in an unscaled cache
+__device__ const float kScaleNone = -1.f;  // scale of a slot without a candidate
+
+// 16-byte global -> shared copy that lands asynchronously; src_bytes = 0
+// writes zeros without reading.
+__device__ __forceinline__ void cp_async_16z(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// One producer lane's view of the four slots lane + 32 i (i < 4) of one
+// candidate tile: list entries, their block-table entries and the row's
+// position; `prev` (lane 0) is the list entry before the tile.
+struct CandLook {
+    int cv[4], bk[4];
+    int pos, prev;
+};
+
+__device__ __forceinline__ void cand_entries(const CandArgs &ca, const si_batch &b, int r, int t,
+                                             int lane, CandLook &L)
+{
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int j = t * kKeys + lane + 32 * i;
+        L.cv[i] = (r < b.n_q && j < ca.n) ? __ldg(ca.cand + (int64_t)r * ca.ld + j) : -1;
+    }
+    L.prev = (lane == 0 && r < b.n_q && t > 0 && t * kKeys - 1 < ca.n)
+                 ? __ldg(ca.cand + (int64_t)r * ca.ld + t * kKeys - 1)
+                 : -1;
+}
+
+__device__ __forceinline__ void cand_blocks(const si_batch &b, int r, CandLook &L)
+{
+    L.pos = r < b.n_q ? __ldg(b.q_pos + r) : -1;
+    const int seq = r < b.n_q ? __ldg(b.q_seq + r) : -1;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int s = L.cv[i];
+        L.bk[i] = -1;
+        if (s >= 0 && s <= L.pos && (unsigned)seq < (unsigned)b.n_seq &&
+            s / b.page_size < b.max_blocks)
+            L.bk[i] = __ldg(b.block_table + (int64_t)seq * b.max_blocks + s / b.page_size);
+    }
+}
+
+template <bool CAND>
 __global__ void __launch_bounds__(kThreads, 1)
 k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix, float *scores,
-             int64_t ld, int64_t total_items, int tiles_per_row, unsigned int *st)
+             int64_t ld, int64_t total_items, int tiles_per_row, unsigned int *st, CandArgs ca)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -135,7 +200,8 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
 
     if (tid == 0) {
         for (int i = 0; i < kStages; i++) {
-            mbar_init(full_bar + i, 1);     // producer's expect_tx arrival
+            // producer's expect_tx arrival, or its 32 lanes' cp.async arrivals
+            mbar_init(full_bar + i, CAND ? 32 : 1);
             mbar_init(empty_bar + i, 1);    // MMA commit (or plain arrive)
         }
         for (int i = 0; i < kPairs * kAccPerPair; i++) {
@@ -163,7 +229,89 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
     const int P = b.page_size;
     const int lp = 31 - __clz(P);  // page_size is a power of two >= 8
 
-    if (warp == kWarpProd0 || warp == kWarpProd1) {
+    if (CAND && (warp == kWarpProd0 || warp == kWarpProd1)) {
+        // ------------------------------------------------- producer, candidates
+        // Lane l gathers slots t * 128 + l + 32 i of each item.  The lookups
+        // that feed the copies are plain loads, which complete behind the
+        // lane's copies in flight, so they run one (block table) and two
+        // (list entries) of this producer's items ahead of their use.
+        const int pw = warp == kWarpProd0 ? 0 : 1;  // takes items pw, pw + 2, ...
+        const uint8_t *kdata = static_cast<const uint8_t *>(ix.k.data);
+        int rA = (int)(j0 / tiles_per_row), tA = (int)(j0 % tiles_per_row);
+        advance(rA, tA, pw, tiles_per_row);
+        int rB = rA, tB = tA;
+        advance(rB, tB, 2, tiles_per_row);
+        int rC = rB, tC = tB;
+        advance(rC, tC, 2, tiles_per_row);
+        CandLook A, B, C;
+        cand_entries(ca, b, rA, tA, lane, A);
+        cand_blocks(b, rA, A);
+        cand_entries(ca, b, rB, tB, lane, B);
+        cand_blocks(b, rB, B);
+        cand_entries(ca, b, rC, tC, lane, C);
+        for (int64_t it = pw; it < n_items; it += 2) {
+            const int stg = (int)(it % kStages);
+            if (it >= kStages &&
+                !mbar_wait(empty_bar + stg, (uint32_t)((it / kStages) - 1) & 1, st))
+                break;
+            int64_t prow[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int s = A.cv[i];
+                const bool valid = s >= 0 && s <= A.pos;
+                prow[i] = (valid && (unsigned)A.bk[i] < (unsigned)b.n_blocks)
+                              ? (int64_t)A.bk[i] * P + s % P
+                              : -1;
+                if (valid && prow[i] < 0)
+                    raise_flag(st, SI_DEVFLAG_BAD_BLOCK);
+                // a candidate follows a candidate with a lower position
+                int pv = __shfl_up_sync(0xffffffffu, s, 1);
+                const int last = __shfl_sync(0xffffffffu, i > 0 ? A.cv[i > 0 ? i - 1 : 0] : 0, 31);
+                if (lane == 0)
+                    pv = i > 0 ? last : A.prev;
+                const bool first = tA == 0 && lane == 0 && i == 0;
+                if (valid && !first && !(pv >= 0 && pv < s))
+                    raise_flag(st, SI_DEVFLAG_BAD_INDEX);
+            }
+            const uint32_t dst = base + kOffStage + stg * kTile;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int key = lane + 32 * i;
+#pragma unroll
+                for (int u = 0; u < kDim / 16; u++)
+                    cp_async_16z(dst + sw128_offset(key, u),
+                                 prow[i] >= 0 ? kdata + prow[i] * kDim + u * 16 : kdata,
+                                 prow[i] >= 0 ? 16u : 0u);
+            }
+            cp_async_arrive_noinc(full_bar + stg);
+            // the keys' scales into this producer's scale ring
+            const int64_t kit = it >> 1;
+            const int ss = (int)(kit % kScStages);
+            if (kit >= kScStages &&
+                !mbar_wait(scempty_bar + pw * kScStages + ss, (uint32_t)((kit / kScStages) - 1) & 1,
+                           st))
+                break;
+            const uint32_t sd = smem_u32(sc_s + (pw * kScStages + ss) * kKeys);
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                cp_async_4(sd + (lane + 32 * i) * 4,
+                           prow[i] >= 0 ? (ix.k.scale ? ix.k.scale + prow[i] : &kScaleOne)
+                                        : &kScaleNone);
+            cp_async_arrive_noinc(scfull_bar + pw * kScStages + ss);
+            // shift the lookahead by one item of this producer
+            A = B;
+            rA = rB;
+            tA = tB;
+            B = C;
+            rB = rC;
+            tB = tC;
+            cand_blocks(b, rB, B);
+            advance(rC, tC, 2, tiles_per_row);
+            cand_entries(ca, b, rC, tC, lane, C);
+        }
+        // nothing may land after the block has moved on
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == kWarpProd0 || warp == kWarpProd1) {
         // ------------------------------------------------------------ producer
         const int pw = warp == kWarpProd0 ? 0 : 1;  // takes items pw, pw + 2, ...
         volatile int *win_s = win_all + pw * 32;
@@ -260,7 +408,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                 cur = r;
                 ++ri;
                 p = ri & 1;
-                pos = __ldg(b.q_pos + r);
+                pos = CAND ? ca.n - 1 : __ldg(b.q_pos + r);
                 if (!mbar_wait(qfull_bar + p, (uint32_t)(ri >> 1) & 1, st))
                     break;
             }
@@ -272,6 +420,8 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
             if (mine) {
                 if (!mbar_wait(full_bar + stg, (uint32_t)(it / kStages) & 1, st))
                     break;
+                if constexpr (CAND)
+                    fence_async_smem();  // cp.async pieces (generic proxy) -> tensor core
                 if (live) {
                     const int c = (int)(m % kAccPerPair);
                     uint64_t *cf = cfull_bar + pr * kAccPerPair + c;
@@ -405,7 +555,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                 cur = r;
                 ++ri;
                 p = ri & 1;
-                pos = __ldg(b.q_pos + r);
+                pos = CAND ? ca.n - 1 : __ldg(b.q_pos + r);  // candidates: slots 0..n-1
                 if (!mbar_wait(qfull_bar + p, (uint32_t)(ri >> 1) & 1, st))
                     break;
             }
@@ -500,8 +650,10 @@ bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld)
            ((uintptr_t)ix.k.scale % 16) == 0;
 }
 
-cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
-                              unsigned int *st, cudaStream_t s)
+namespace {
+
+cudaError_t launch_indexer_tc_any(const si_batch &b, const si_indexer &ix, const CandArgs &ca,
+                                  float *scores, int64_t ld, unsigned int *st, cudaStream_t s)
 {
     // Per-device launch facts (SM count, shared-memory opt-in), set up once.
     static std::once_flag once[kMaxDevices];
@@ -516,8 +668,11 @@ cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *sc
     std::call_once(once[dev], [dev] {
         cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(k_indexer_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemBytes);
+            r = cudaFuncSetAttribute(k_indexer_tc<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(k_indexer_tc<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         err_of[dev] = r;
     });
     if (err_of[dev] != cudaSuccess)
@@ -532,9 +687,30 @@ cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *sc
     const int64_t total = (int64_t)b.n_q * tiles_per_row;
     const int64_t grid = std::min<int64_t>(total, (int64_t)sms_of[dev]);  // one CTA per SM
     count_launch();
-    k_indexer_tc<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores, ld, total,
-                                                              tiles_per_row, st);
+    if (ca.cand)
+        k_indexer_tc<true><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores, ld,
+                                                                        total, tiles_per_row, st,
+                                                                        ca);
+    else
+        k_indexer_tc<false><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores, ld,
+                                                                         total, tiles_per_row, st,
+                                                                         ca);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
+                              unsigned int *st, cudaStream_t s)
+{
+    return launch_indexer_tc_any(b, ix, CandArgs{nullptr, 0, 0}, scores, ld, st, s);
+}
+
+cudaError_t launch_indexer_tc_cand(const si_batch &b, const si_indexer &ix, const int32_t *cand,
+                                   int64_t ld_cand, int32_t n_cand, float *scores, int64_t ld,
+                                   unsigned int *st, cudaStream_t s)
+{
+    return launch_indexer_tc_any(b, ix, CandArgs{cand, ld_cand, n_cand}, scores, ld, st, s);
 }
 
 }  // namespace si

@@ -31,6 +31,12 @@ cudaError_t launch_attn_generic(const si_batch &b, const si_attention &at, const
 bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld);
 cudaError_t launch_indexer_tc(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
                               unsigned int *st, cudaStream_t s);
+// The same kernel over candidate lists: tile t of row r is slots t*128 .. of
+// cand + r * ld_cand (the first n_cand entries; entries -1 or past q_pos[r]
+// score -inf); scores[r, j] is the score of slot j.  Same operand conditions.
+cudaError_t launch_indexer_tc_cand(const si_batch &b, const si_indexer &ix, const int32_t *cand,
+                                   int64_t ld_cand, int32_t n_cand, float *scores, int64_t ld,
+                                   unsigned int *st, cudaStream_t s);
 
 // Tensor-core indexer for query rows that all belong to one sequence (a
 // causal prefill or a prefill chunk): blocks of two (bf16 q) or four (FP8 q)
@@ -49,9 +55,11 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
                            int k_top, void *out, si_dtype out_dtype, float *lse, void *scratch,
                            size_t scratch_bytes, unsigned int *st, cudaStream_t s);
 
-// Radix select of the k_top best scores per row.
+// Radix select of the k_top best scores per row: among positions 0..q_pos[r],
+// or, with fixed_n > 0, among the first fixed_n entries of every row (q_pos
+// is then not read).
 cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,
-                        int32_t *idx, unsigned int *st, cudaStream_t s);
+                        int32_t *idx, unsigned int *st, cudaStream_t s, int32_t fixed_n = 0);
 
 // Candidate-restricted selection (si_cand.cu).  The candidates of query row r
 // are gathered into a private sequence r of a workspace cache with pages of
@@ -76,9 +84,10 @@ cudaError_t launch_cand_gather(const si_batch &b, const int32_t *cand, int64_t l
 // the -1 scale as "no key").
 cudaError_t launch_cand_mask(int32_t n_q, int32_t n_cand, const CandView &v, const float *scales,
                              float *scores, int64_t ld, cudaStream_t s);
-// Turns the selected slots into ascending positions, -1 padded, in place.
+// Turns the selected slots into ascending positions, -1 padded, in place
+// (a slot whose score is -inf holds no candidate).
 cudaError_t launch_cand_map(int32_t n_q, const int32_t *cand, int64_t ld_cand, int32_t n_cand,
-                            const CandView &v, const float *scales, int32_t k_top, int32_t *idx,
+                            const float *scores, int64_t ld_scores, int32_t k_top, int32_t *idx,
                             cudaStream_t s);
 
 }  // namespace si

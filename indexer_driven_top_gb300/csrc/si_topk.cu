@@ -126,7 +126,7 @@ __device__ __forceinline__ void topk_cached(const float *row, int n, int k_top, 
 }
 
 __global__ void __launch_bounds__(kTopkThreads)
-k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx)
+k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx, int32_t fixed_n)
 {
     __shared__ uint32_t hist[kRadixBins];
     __shared__ int sbuf[33];
@@ -135,7 +135,8 @@ k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx
 
     griddep_launch_dependents();  // the attention kernel may set itself up meanwhile
     const int r = blockIdx.x, tid = threadIdx.x;
-    int64_t n = (int64_t)b.q_pos[r] + 1;  // candidates 0..pos
+    // candidates 0..pos, or the first fixed_n entries of every row
+    int64_t n = fixed_n > 0 ? (int64_t)fixed_n : (int64_t)b.q_pos[r] + 1;
     if (n > ld)
         n = ld;
     const float *row = scores + (int64_t)r * ld;
@@ -231,7 +232,8 @@ constexpr int kSegment = kClusterE * kTopkThreads;  // positions per CTA
 constexpr int kMaxCluster = 8;
 
 __global__ void __launch_bounds__(kTopkThreads)
-k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx)
+k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx,
+               int32_t fixed_n)
 {
     __shared__ uint32_t hist[kRadixBins];
     __shared__ uint32_t merged[3][kRadixBins];   // used in CTA 0: one histogram per pass
@@ -245,7 +247,7 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
     uint32_t C;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
     const int r = (int)(blockIdx.x / C), tid = threadIdx.x;
-    int64_t n = (int64_t)b.q_pos[r] + 1;
+    int64_t n = fixed_n > 0 ? (int64_t)fixed_n : (int64_t)b.q_pos[r] + 1;
     if (n > ld)
         n = ld;
     const float *row = scores + (int64_t)r * ld;
@@ -355,7 +357,7 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
 }  // namespace
 
 cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,
-                        int32_t *idx, unsigned int *st, cudaStream_t s)
+                        int32_t *idx, unsigned int *st, cudaStream_t s, int32_t fixed_n)
 {
     (void)st;
     count_launch();
@@ -381,7 +383,7 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
     if (sms_of[dev] == 0 &&
         cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms_of[dev] = 1;
-    const int64_t longest = std::min<int64_t>(b.max_ctx, ld);
+    const int64_t longest = std::min<int64_t>(fixed_n > 0 ? fixed_n : b.max_ctx, ld);
     const int C = (int)((longest + kSegment - 1) / kSegment);
     if (longest > 16 * kTopkThreads && C <= kMaxCluster &&
         (int64_t)b.n_q * C <= 2 * (int64_t)sms_of[dev]) {
@@ -391,10 +393,10 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        return cudaLaunchKernelEx(&cfg, k_topk_cluster, b, scores, ld, k_top, idx);
+        return cudaLaunchKernelEx(&cfg, k_topk_cluster, b, scores, ld, k_top, idx, fixed_n);
     }
     cfg.gridDim = dim3((unsigned)b.n_q);
-    return cudaLaunchKernelEx(&cfg, k_topk_rows, b, scores, ld, k_top, idx);
+    return cudaLaunchKernelEx(&cfg, k_topk_rows, b, scores, ld, k_top, idx, fixed_n);
 }
 
 }  // namespace si

@@ -123,8 +123,13 @@ def test_candidate_selection_host_validation_and_sizes(si):
     b = ctypes.byref(_batch(si))
     ix = si.c_indexer(fake, si.BF16, None, fake, 64, 128, si.c_paged(fake, None, si.E4M3, 128, 128))
     need = lib.si_workspace_size_cand(b, ctypes.byref(ix), 300)
-    # status + 4 small arrays + 2 rows x 384 slots x (128-byte key + 4-byte scale) + scores
-    assert need >= 256 + 2 * 384 * (128 + 4) + 2 * 320 * 4
+    # 64 x 128 FP8 keys: the tensor-core indexer gathers the candidates itself,
+    # the workspace holds the status word and 2 rows x 320 scores
+    assert need == 256 + 2 * 320 * 4 + 256 * ((-2 * 320 * 4) % 256 > 0)
+    # other shapes gather them into the workspace first: 2 rows x 384 slots x
+    # (128-byte f32 key row + 4-byte scale) besides the scores
+    ixf = si.c_indexer(fake, si.F32, None, fake, 4, 32, si.c_paged(fake, None, si.F32, 32, 32))
+    assert lib.si_workspace_size_cand(b, ctypes.byref(ixf), 300) >= 256 + 2 * 384 * (128 + 4) + 2 * 320 * 4
     assert lib.si_workspace_size_cand(b, ctypes.byref(ix), 0) == 0
     args = lambda **kw: dict(dict(cand=P(fake), n_cand=300, ld_cand=300, k_top=8, idx=P(fake),
                                   scores=None, ld_scores=0, ws=P(ws), ws_bytes=need), **kw)
