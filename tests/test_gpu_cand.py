@@ -172,3 +172,30 @@ def test_candidates_long_context_full_size(si):
     assert flags == 0
     o_idx, o_sc, _ = _oracle(wl, cand)
     _check(wl, cand, g_idx, g_sc, o_idx, o_sc)
+
+
+def test_long_candidate_lists_take_cluster_top_k(si):
+    """40000 candidates per row on two rows: the Top-K over the candidate
+    slots runs as a cluster of three CTAs per row."""
+    wl = synth.make("c3", batch=2, ctx=60000, K=2048, Hq=1, Dqk=16, Dv=8)
+    cand = synth.candidates(wl, 40000, seed=13)
+    dw = si.upload(wl)
+    g_idx, g_sc, flags = _gpu(si, dw, wl, cand)
+    assert flags == 0
+    o_idx, o_sc, _ = _oracle(wl, cand)
+    _check(wl, cand, g_idx, g_sc, o_idx, o_sc)
+
+
+def test_many_long_candidate_lists_take_streamed_top_k(si):
+    """160 rows with 17000 candidates each: too many rows for a cluster per
+    row, so the Top-K streams each row's slots.  Indexer shapes of 4 heads x
+    32 take the gather kernel and the CUDA-core indexer.  Eight sampled rows
+    are checked against the oracle."""
+    wl = synth.make("c1", batch=160, ctx=17500, K=512, Hi=4, Di=32, Hq=1, Dqk=16, Dv=8)
+    cand = synth.candidates(wl, 17000, seed=17)
+    dw = si.upload(wl)
+    g_idx, g_sc, flags = _gpu(si, dw, wl, cand)
+    assert flags == 0
+    rows = [0, 1, 37, 80, 81, 120, 158, 159]
+    o_idx, o_sc, _ = _oracle(wl, cand, rows=rows)
+    _check(wl, cand, g_idx, g_sc, o_idx, o_sc, rows=rows)
