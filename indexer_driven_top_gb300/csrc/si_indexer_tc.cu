@@ -265,8 +265,10 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                 if (valid && prow[i] < 0)
                     raise_flag(st, SI_DEVFLAG_BAD_BLOCK);
                 // a candidate follows a candidate with a lower position
+                // (the slot before lane 0's is lane 31's of the previous group of
+                // 32, or the entry before the tile)
                 int pv = __shfl_up_sync(0xffffffffu, s, 1);
-                const int last = __shfl_sync(0xffffffffu, i > 0 ? A.cv[i > 0 ? i - 1 : 0] : 0, 31);
+                const int last = __shfl_sync(0xffffffffu, A.cv[i > 0 ? i - 1 : 0], 31);
                 if (lane == 0)
                     pv = i > 0 ? last : A.prev;
                 const bool first = tA == 0 && lane == 0 && i == 0;

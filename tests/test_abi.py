@@ -124,8 +124,9 @@ def test_candidate_selection_host_validation_and_sizes(si):
     ix = si.c_indexer(fake, si.BF16, None, fake, 64, 128, si.c_paged(fake, None, si.E4M3, 128, 128))
     need = lib.si_workspace_size_cand(b, ctypes.byref(ix), 300)
     # 64 x 128 FP8 keys: the tensor-core indexer gathers the candidates itself,
-    # the workspace holds the status word and 2 rows x 320 scores
-    assert need == 256 + 2 * 320 * 4 + 256 * ((-2 * 320 * 4) % 256 > 0)
+    # the workspace holds the status word and 2 rows x 320 scores (2560 bytes,
+    # a multiple of the 256-byte region alignment)
+    assert need == 256 + 2 * 320 * 4
     # other shapes gather them into the workspace first: 2 rows x 384 slots x
     # (128-byte f32 key row + 4-byte scale) besides the scores
     ixf = si.c_indexer(fake, si.F32, None, fake, 4, 32, si.c_paged(fake, None, si.F32, 32, 32))
