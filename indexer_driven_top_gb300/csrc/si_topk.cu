@@ -13,6 +13,7 @@
 // (one 16384-position segment each, histograms merged in distributed shared
 // memory); longer rows stream from global memory per pass.
 #include <algorithm>
+#include <mutex>
 
 #include "si_common.cuh"
 #include "si_internal.h"
@@ -220,21 +221,28 @@ k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx
     }
 }
 
-// Long rows (16384 < n <= 16384 C): a cluster of C CTAs per row, CTA q
-// caching positions [16384 q, 16384 q + 16384) in registers.  Each radix pass
+// Long rows (16384 < n <= 32768 C): a cluster of C CTAs per row, CTA q
+// caching positions [32768 q, 32768 q + 32768) in shared memory (128 KB;
+// thread t owns positions 32 t .. 32 t + 31, stored at e * 1024 + t so that a
+// warp's accesses fall in distinct banks).  Holding 32768 keys per CTA keeps
+// the clusters at four CTAs for rows of 131072: clusters of eight CTAs that
+// each fill an SM do not all fit on the GPU at once, and the second wave
+// starts only when the first has finished.  Each radix pass
 // adds every CTA's histogram into a per-pass histogram in CTA 0's shared
 // memory (distributed shared memory atomics), and every CTA then reads the
 // merged counts and takes the same decision.  The emit pass orders the CTAs'
 // selections by their segment: CTA q writes after the selections and the
 // tie quota of CTAs 0..q-1, whose counts it reads from CTA 0.
-constexpr int kClusterE = 16;
+constexpr int kClusterE = 32;
 constexpr int kSegment = kClusterE * kTopkThreads;  // positions per CTA
 constexpr int kMaxCluster = 8;
+constexpr int kClusterSmem = kSegment * 4;          // the CTA's keys (dynamic shared memory)
 
 __global__ void __launch_bounds__(kTopkThreads)
 k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx,
                int32_t fixed_n)
 {
+    extern __shared__ uint32_t ks[];             // [kClusterE][kTopkThreads] keys
     __shared__ uint32_t hist[kRadixBins];
     __shared__ uint32_t merged[3][kRadixBins];   // used in CTA 0: one histogram per pass
     __shared__ uint32_t counts[kMaxCluster][2];  // used in CTA 0: (above, ties) per CTA
@@ -267,23 +275,22 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
         return;
     }
     const int64_t p0 = (int64_t)q * kSegment + (int64_t)tid * kClusterE;
-    uint32_t key[kClusterE];
-    uint32_t valid = 0;
+    uint32_t valid = 0;  // bit e: position p0 + e < n
     if (p0 + kClusterE <= n && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
 #pragma unroll
         for (int e = 0; e < kClusterE; e += 4) {
             const float4 v = __ldg(reinterpret_cast<const float4 *>(row + p0 + e));
-            key[e] = order_key(v.x);
-            key[e + 1] = order_key(v.y);
-            key[e + 2] = order_key(v.z);
-            key[e + 3] = order_key(v.w);
+            ks[(e + 0) * kTopkThreads + tid] = order_key(v.x);
+            ks[(e + 1) * kTopkThreads + tid] = order_key(v.y);
+            ks[(e + 2) * kTopkThreads + tid] = order_key(v.z);
+            ks[(e + 3) * kTopkThreads + tid] = order_key(v.w);
         }
-        valid = 0xffffu;
+        valid = 0xffffffffu;
     } else {
 #pragma unroll
         for (int e = 0; e < kClusterE; e++) {
             const bool in = p0 + e < n;
-            key[e] = in ? order_key(__ldg(row + p0 + e)) : 0u;
+            ks[e * kTopkThreads + tid] = in ? order_key(__ldg(row + p0 + e)) : 0u;
             valid |= (in ? 1u : 0u) << e;
         }
     }
@@ -297,10 +304,12 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
         for (int i = tid; i < nbins; i += kTopkThreads)
             hist[i] = 0;
         __syncthreads();
-#pragma unroll
-        for (int e = 0; e < kClusterE; e++)
-            if (((valid >> e) & 1u) && (key[e] & mask) == prefix)
-                atomicAdd(&hist[(key[e] >> shift) & (nbins - 1)], 1u);
+#pragma unroll 8
+        for (int e = 0; e < kClusterE; e++) {
+            const uint32_t key = ks[e * kTopkThreads + tid];
+            if (((valid >> e) & 1u) && (key & mask) == prefix)
+                atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
+        }
         __syncthreads();
         for (int i = tid; i < nbins; i += kTopkThreads)
             if (hist[i])
@@ -316,11 +325,12 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
     }
     // emit
     int gt = 0, eq = 0;
-#pragma unroll
+#pragma unroll 8
     for (int e = 0; e < kClusterE; e++) {
+        const uint32_t key = ks[e * kTopkThreads + tid];
         const bool in = (valid >> e) & 1u;
-        gt += in && key[e] > prefix;
-        eq += in && key[e] == prefix;
+        gt += in && key > prefix;
+        eq += in && key == prefix;
     }
     int gt_total, eq_total;
     const int eq_before = block_exclusive_scan(eq, &eq_total, sbuf);
@@ -341,11 +351,12 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
     int take_eq = max(0, min(eq, remaining - eq_prev - eq_before));
     int total;
     int o = off + block_exclusive_scan(gt + take_eq, &total, sbuf);
-#pragma unroll
+#pragma unroll 8
     for (int e = 0; e < kClusterE; e++) {
+        const uint32_t key = ks[e * kTopkThreads + tid];
         const bool in = (valid >> e) & 1u;
-        const bool tie = in && key[e] == prefix;
-        const bool take = (in && key[e] > prefix) || (tie && take_eq > 0);
+        const bool tie = in && key == prefix;
+        const bool take = (in && key > prefix) || (tie && take_eq > 0);
         if (tie && take)
             take_eq--;
         if (take && o < k_top)
@@ -377,9 +388,16 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
     // would leave most of the GPU idle; a batch with many rows keeps one CTA
     // per row and streams.
     static int sms_of[kMaxDevices];
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t err_of[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         dev = 0;
+    std::call_once(once[dev], [dev] {
+        err_of[dev] = cudaFuncSetAttribute(k_topk_cluster,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kClusterSmem);
+    });
     if (sms_of[dev] == 0 &&
         cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms_of[dev] = 1;
@@ -387,7 +405,10 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
     const int C = (int)((longest + kSegment - 1) / kSegment);
     if (longest > 16 * kTopkThreads && C <= kMaxCluster &&
         (int64_t)b.n_q * C <= 2 * (int64_t)sms_of[dev]) {
+        if (err_of[dev] != cudaSuccess)
+            return err_of[dev];
         cfg.gridDim = dim3((unsigned)(b.n_q * C));
+        cfg.dynamicSmemBytes = kClusterSmem;
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = (unsigned)C;
         attr[1].val.clusterDim.y = 1;
