@@ -428,7 +428,7 @@ def candidate_selection(si, dev, steps, n_cand=16384):
     gbs = nbytes / (ms_c / 1e3) / 1e9
     return {"workload": "decode batch 16 x context 131072 (1% planted keys), "
                         f"{n_cand} candidates per row, indexer 64x128 fp8, top-k {K}",
-            "call": "si_indexer_topk_cand (indexer gathering the candidate keys, top-k, map)",
+            "call": "si_indexer_topk_cand (indexer gathering the candidate keys, top-k writing positions)",
             "ms_per_call": ms_c, "queries_per_s": wl.n_q / (ms_c / 1e3),
             "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
             "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],

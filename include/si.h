@@ -209,7 +209,8 @@ si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_atte
  *   above q_pos[r] are not candidates.  A candidate that does not follow a
  *   lower candidate raises SI_DEVFLAG_BAD_INDEX, and the row's result is then
  *   undefined.  A candidate whose page is invalid raises SI_DEVFLAG_BAD_BLOCK
- *   and is dropped.
+ *   and is never selected; if the row has fewer than k_top valid candidates
+ *   its output may then hold -1 before later positions.
  * idx: device int32 [n_q, k_top].  Row r receives the k_top candidates with the
  *   largest score(r, s) (equal scores: the lower position wins; -0 equals +0),
  *   in ascending order.  A row with fewer than k_top candidates receives all

@@ -436,11 +436,9 @@ si_status si_indexer_topk_cand(const si_batch *b, const si_indexer *ix, const in
         if (e != cudaSuccess)
             return cuda_fail(e, "candidate mask launch");
     }
-    e = si::launch_topk(*b, sc, ld, k_top, idx, stw, s, n_cand);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "top-k launch");
-    e = si::launch_cand_map(b->n_q, cand, ld_cand, n_cand, sc, ld, k_top, idx, s);
-    return e == cudaSuccess ? SI_OK : cuda_fail(e, "candidate map launch");
+    // Top-K over the slots, each selected slot written as its position
+    e = si::launch_topk(*b, sc, ld, k_top, idx, stw, s, n_cand, cand, ld_cand);
+    return e == cudaSuccess ? SI_OK : cuda_fail(e, "top-k launch");
 }
 
 size_t si_workspace_size(si_op op, const si_batch *b, const si_indexer *ix,

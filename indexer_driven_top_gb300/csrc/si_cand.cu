@@ -15,8 +15,8 @@
 // query row with pages of 128 rows, so that candidate slot j of row r is
 // position j of sequence r, and the CUDA-core indexer scores those sequences
 // (k_cand_mask then sets -inf where a slot holds no candidate).  Either way
-// the radix Top-K selects among the first n_cand slots of each row, and
-// k_cand_map turns the selected slots back into positions.  Candidate lists hold their
+// the radix Top-K selects among the first n_cand slots of each row and
+// writes each selected slot as the position it holds.  Candidate lists hold their
 // candidates first and in strictly ascending order, so slot order is position
 // order: the Top-K's tie rule and ascending output carry over unchanged.
 #include <stdint.h>
@@ -128,44 +128,6 @@ __global__ void k_cand_mask(int32_t n_q, int32_t n_cand, CandView v, const float
     }
 }
 
-constexpr int kMapThreads = 1024;
-constexpr int kMapPer = 16;  // k_top <= 16384 entries per row
-
-// Slots selected by the Top-K -> positions, in place: slots without a
-// candidate (score -inf; selected only when a row has fewer than k_top
-// candidates) are dropped, the rest keep their ascending order, -1 pads the
-// tail.
-__global__ void __launch_bounds__(kMapThreads)
-k_cand_map(const int32_t *cand, int64_t ld_cand, int32_t n_cand, const float *scores,
-           int64_t ld_scores, int32_t k_top, int32_t *idx)
-{
-    __shared__ int sbuf[33];
-    const int r = blockIdx.x, tid = threadIdx.x;
-    int32_t *out = idx + (int64_t)r * k_top;
-    const int per = (k_top + kMapThreads - 1) / kMapThreads;
-    int val[kMapPer];
-    int cnt = 0;
-#pragma unroll
-    for (int e = 0; e < kMapPer; e++) {
-        val[e] = -1;
-        const int k = tid * per + e;
-        if (e < per && k < k_top) {
-            const int j = out[k];
-            if (j >= 0 && j < n_cand && scores[(int64_t)r * ld_scores + j] != -INFINITY)
-                val[e] = __ldg(cand + (int64_t)r * ld_cand + j);
-            cnt += val[e] >= 0;
-        }
-    }
-    int total;
-    int o = block_exclusive_scan(cnt, &total, sbuf);  // all reads of out[] happen before
-#pragma unroll
-    for (int e = 0; e < kMapPer; e++)
-        if (val[e] >= 0)
-            out[o++] = val[e];
-    for (int k = total + tid; k < k_top; k += kMapThreads)
-        out[k] = -1;
-}
-
 // One thread per work item: the gather's loads form a chain (list entry ->
 // block table -> key row), so latency is hidden by many threads in flight,
 // not by a grid-stride loop.
@@ -196,17 +158,6 @@ cudaError_t launch_cand_mask(int32_t n_q, int32_t n_cand, const CandView &v, con
     const int grid = grid_for((int64_t)n_q * n_cand, 256);
     count_launch();
     k_cand_mask<<<grid, 256, 0, s>>>(n_q, n_cand, v, scales, scores, ld);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_cand_map(int32_t n_q, const int32_t *cand, int64_t ld_cand, int32_t n_cand,
-                            const float *scores, int64_t ld_scores, int32_t k_top, int32_t *idx,
-                            cudaStream_t s)
-{
-    if (k_top > kMapThreads * kMapPer)
-        return cudaErrorInvalidValue;
-    count_launch();
-    k_cand_map<<<n_q, kMapThreads, 0, s>>>(cand, ld_cand, n_cand, scores, ld_scores, k_top, idx);
     return cudaGetLastError();
 }
 

@@ -57,9 +57,12 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
 
 // Radix select of the k_top best scores per row: among positions 0..q_pos[r],
 // or, with fixed_n > 0, among the first fixed_n entries of every row (q_pos
-// is then not read).
+// is then not read).  With `cand`, entry p of row r is slot p of the
+// candidate list cand + r * ld_cand, and a selected slot is written as the
+// position it holds (-1 where its score is -inf).
 cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,
-                        int32_t *idx, unsigned int *st, cudaStream_t s, int32_t fixed_n = 0);
+                        int32_t *idx, unsigned int *st, cudaStream_t s, int32_t fixed_n = 0,
+                        const int32_t *cand = nullptr, int64_t ld_cand = 0);
 
 // Candidate-restricted selection (si_cand.cu).  The candidates of query row r
 // are gathered into a private sequence r of a workspace cache with pages of
@@ -84,10 +87,5 @@ cudaError_t launch_cand_gather(const si_batch &b, const int32_t *cand, int64_t l
 // the -1 scale as "no key").
 cudaError_t launch_cand_mask(int32_t n_q, int32_t n_cand, const CandView &v, const float *scales,
                              float *scores, int64_t ld, cudaStream_t s);
-// Turns the selected slots into ascending positions, -1 padded, in place
-// (a slot whose score is -inf holds no candidate).
-cudaError_t launch_cand_map(int32_t n_q, const int32_t *cand, int64_t ld_cand, int32_t n_cand,
-                            const float *scores, int64_t ld_scores, int32_t k_top, int32_t *idx,
-                            cudaStream_t s);
 
 }  // namespace si

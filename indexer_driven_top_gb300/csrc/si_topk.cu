@@ -28,6 +28,24 @@ using namespace sm100;
 constexpr int kTopkThreads = 1024;
 constexpr int kRadixBins = 2048;
 
+// Candidate-restricted selection (si_indexer_topk_cand): the rows are the
+// slots of per-row candidate lists, and a selected slot is written as the
+// position it holds -- -1 for a slot without a candidate, whose score is
+// -inf.  The lists hold their candidates first and ascending, so such slots
+// sort after every candidate and the output stays ascending with -1 last.
+struct SlotMap {
+    const int32_t *cand;  // NULL: write the selected positions themselves
+    int64_t ld;
+};
+constexpr uint32_t kNegInfKey = 0x007FFFFFu;  // order_key(-inf)
+
+__device__ __forceinline__ int32_t out_value(const SlotMap &m, int r, int64_t p, uint32_t key)
+{
+    if (!m.cand)
+        return (int32_t)p;
+    return key == kNegInfKey ? -1 : __ldg(m.cand + (int64_t)r * m.ld + p);
+}
+
 // Finds, among the cached keys, the digit of the k-th largest key at `shift`
 // (bins in descending order) and how many of the k fall in that digit's bin.
 // Every thread returns the same (digit, remaining).
@@ -57,7 +75,8 @@ __device__ __forceinline__ void radix_step(uint32_t *hist, int *sbuf, uint32_t *
 // Row of n <= E * kTopkThreads candidates (n > k_top): keys cached in
 // registers, thread t owning positions [t E, t E + E).
 template <int E>
-__device__ __forceinline__ void topk_cached(const float *row, int n, int k_top, int32_t *out,
+__device__ __forceinline__ void topk_cached(const SlotMap &m, int r, const float *row, int n,
+                                            int k_top, int32_t *out,
                                             uint32_t *hist, int *sbuf, uint32_t *sh_digit,
                                             int *sh_rem)
 {
@@ -122,12 +141,13 @@ __device__ __forceinline__ void topk_cached(const float *row, int n, int k_top, 
         if (tie && take)
             take_eq--;
         if (take && o < k_top)
-            out[o++] = p0 + e;
+            out[o++] = out_value(m, r, p0 + e, key[e]);
     }
 }
 
 __global__ void __launch_bounds__(kTopkThreads)
-k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx, int32_t fixed_n)
+k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx, int32_t fixed_n,
+            SlotMap m)
 {
     __shared__ uint32_t hist[kRadixBins];
     __shared__ int sbuf[33];
@@ -148,15 +168,15 @@ k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx
     griddep_wait();
     if (n <= k_top) {  // everything is selected
         for (int i = tid; i < k_top; i += kTopkThreads)
-            out[i] = i < n ? i : -1;
+            out[i] = i < n ? out_value(m, r, i, m.cand ? order_key(__ldg(row + i)) : 0u) : -1;
         return;
     }
     if (n <= 8 * kTopkThreads) {
-        topk_cached<8>(row, (int)n, k_top, out, hist, sbuf, &sh_digit, &sh_rem);
+        topk_cached<8>(m, r, row, (int)n, k_top, out, hist, sbuf, &sh_digit, &sh_rem);
         return;
     }
     if (n <= 16 * kTopkThreads) {
-        topk_cached<16>(row, (int)n, k_top, out, hist, sbuf, &sh_digit, &sh_rem);
+        topk_cached<16>(m, r, row, (int)n, k_top, out, hist, sbuf, &sh_digit, &sh_rem);
         return;
     }
 
@@ -217,7 +237,7 @@ k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx
         if (key == prefix && take)
             take_eq--;
         if (take && o < k_top)
-            out[o++] = (int32_t)i;
+            out[o++] = out_value(m, r, i, key);
     }
 }
 
@@ -240,7 +260,7 @@ constexpr int kClusterSmem = kSegment * 4;          // the CTA's keys (dynamic s
 
 __global__ void __launch_bounds__(kTopkThreads)
 k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx,
-               int32_t fixed_n)
+               int32_t fixed_n, SlotMap m)
 {
     extern __shared__ uint32_t ks[];             // [kClusterE][kTopkThreads] keys
     __shared__ uint32_t hist[kRadixBins];
@@ -270,7 +290,7 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
     if (n <= k_top) {  // everything is selected (the same on every CTA)
         if (q == 0)
             for (int i = tid; i < k_top; i += kTopkThreads)
-                out[i] = i < n ? i : -1;
+                out[i] = i < n ? out_value(m, r, i, m.cand ? order_key(__ldg(row + i)) : 0u) : -1;
         cluster_sync();
         return;
     }
@@ -360,7 +380,7 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
         if (tie && take)
             take_eq--;
         if (take && o < k_top)
-            out[o++] = (int32_t)(p0 + e);
+            out[o++] = out_value(m, r, p0 + e, key);
     }
     cluster_sync();  // CTA 0's shared memory stays until every CTA has read it
 }
@@ -368,8 +388,10 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
 }  // namespace
 
 cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int k_top,
-                        int32_t *idx, unsigned int *st, cudaStream_t s, int32_t fixed_n)
+                        int32_t *idx, unsigned int *st, cudaStream_t s, int32_t fixed_n,
+                        const int32_t *cand, int64_t ld_cand)
 {
+    const SlotMap m{cand, ld_cand};
     (void)st;
     count_launch();
     // may overlap the tail of the kernel that wrote the scores (programmatic
@@ -414,10 +436,10 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        return cudaLaunchKernelEx(&cfg, k_topk_cluster, b, scores, ld, k_top, idx, fixed_n);
+        return cudaLaunchKernelEx(&cfg, k_topk_cluster, b, scores, ld, k_top, idx, fixed_n, m);
     }
     cfg.gridDim = dim3((unsigned)b.n_q);
-    return cudaLaunchKernelEx(&cfg, k_topk_rows, b, scores, ld, k_top, idx, fixed_n);
+    return cudaLaunchKernelEx(&cfg, k_topk_rows, b, scores, ld, k_top, idx, fixed_n, m);
 }
 
 }  // namespace si
