@@ -27,7 +27,7 @@ _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
 _lib = None
 _lock = threading.Lock()
 
-TYPE_CODE = {"f32": 0, "bf16": 1, "e4m3": 2}
+TYPE_CODE = {"f32": 0, "bf16": 1, "e4m3": 2, "e2m1": 3}
 
 
 def build(force: bool = False) -> str:
@@ -72,6 +72,8 @@ def _load():
             lib.orc_bf16_to_f64.restype = D
             lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
             lib.orc_e4m3_to_f64.restype = D
+            lib.orc_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+            lib.orc_e2m1_to_f64.restype = D
             _lib = lib
     return _lib
 
@@ -119,6 +121,15 @@ def _rows(rows, n_q):
 
 def e4m3_to_f64(code: int) -> float:
     return _load().orc_e4m3_to_f64(code)
+
+
+def e2m1_to_f64(code: int) -> float:
+    return _load().orc_e2m1_to_f64(code)
+
+
+def _elem_stride(a, type_: str) -> int:
+    """Row stride in elements of a cache array (e2m1 packs two per byte)."""
+    return a.shape[-1] * (2 if type_ == "e2m1" else 1)
 
 
 def bf16_to_f64(bits: int) -> float:
@@ -206,7 +217,8 @@ def sparse_attn(b: Batch, q, q_type: str, k, v, kv_type: str, idx, K: int, Hq: i
     lse = np.empty((n, Hq), dtype=np.float64)
     lib.oracle_sparse_attn(ctypes.byref(b.s), _ptr(rr), n, Hq, Dqk, Dv, _ptr(q),
                            TYPE_CODE[q_dtype or q_type], _ptr(k), _ptr(v), TYPE_CODE[kv_type],
-                           k.shape[-1], v.shape[-1], _ptr(ks), _ptr(ks), scale_tile, nsc, nsc,
+                           _elem_stride(k, kv_type), _elem_stride(v, kv_type), _ptr(ks), _ptr(ks),
+                           scale_tile, nsc, nsc,
                            _ptr(ix), K, scale, _ptr(out), _ptr(lse), threads or default_threads())
     return out, lse
 

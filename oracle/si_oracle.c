@@ -24,7 +24,9 @@
  *
  * Storage codes: 0 = float32, 1 = bfloat16 bit patterns, 2 = FP8 e4m3 codes
  * (OCP definition: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits; code
- * S.1111.111 is NaN, there are no infinities).
+ * S.1111.111 is NaN, there are no infinities), 3 = FP4 e2m1 codes, two per
+ * byte with the even element in the low nibble (OCP definition: 1 sign, 2
+ * exponent bits with bias 1, 1 mantissa bit; no NaN or infinity).
  *
  * No blocking, fusion or reordering: loops run in the order of the
  * definitions; a library sort (qsort) orders the candidates.
@@ -35,7 +37,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_E2M1 = 3 };
 
 typedef struct {
     int32_t n_seq;
@@ -73,11 +75,29 @@ double orc_e4m3_to_f64(uint8_t c)
     return sign ? -v : v;
 }
 
+double orc_e2m1_to_f64(uint8_t c)
+{
+    int sign = (c >> 3) & 1;
+    int e = (c >> 1) & 3;
+    int m = c & 1;
+    double v;
+    if (e == 0)
+        v = 0.5 * m;                          /* subnormal: 0.m * 2^(1-1) */
+    else
+        v = ldexp(1.0 + m / 2.0, e - 1);      /* normal: 1.m * 2^(e-1) */
+    return sign ? -v : v;
+}
+
+/* element i of a buffer (for e2m1, i counts 4-bit elements) */
 static double elem(const void *base, int type, int64_t i)
 {
     switch (type) {
     case ORC_F32: return (double)((const float *)base)[i];
     case ORC_BF16: return orc_bf16_to_f64(((const uint16_t *)base)[i]);
+    case ORC_E2M1: {
+        uint8_t byte = ((const uint8_t *)base)[i >> 1];
+        return orc_e2m1_to_f64((i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15));
+    }
     default: return orc_e4m3_to_f64(((const uint8_t *)base)[i]);
     }
 }

@@ -28,6 +28,12 @@ e4m3 codes with one fp32 scale per row and tile of 128 entries (576 entries:
 four full tiles and one of 64), scale = max|tile| / 448, quantised from the
 same N(0,1) draws; the attention query stays bf16.
 
+Option ``kv_fp4=True`` (latent-row configs) stores it as OCP FP4 e2m1 codes,
+two per byte (even entry in the low nibble), in blocks of 16 entries with the
+NVFP4 block scale: e4m3(max|block| / 6) (round to nearest even) times a
+tensor scale of 1, kept as one fp32 per block; codes round to nearest even
+on the e2m1 grid and saturate at +-6.
+
 Draw order (per config): context lengths (c4 only) -> physical block
 permutation -> q_idx -> w -> indexer keys (sequence by sequence, logical
 order) -> planted positions and offsets (c3) -> attention q -> K/V rows
@@ -43,7 +49,7 @@ from typing import Optional
 
 import numpy as np
 
-F32, BF16, E4M3 = "f32", "bf16", "e4m3"
+F32, BF16, E4M3, E2M1 = "f32", "bf16", "e4m3", "e2m1"
 PAGE = 64
 E4M3_MAX = 448.0
 
@@ -164,6 +170,45 @@ def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
 
 
 KV_TILE = 128
+FP4_BLOCK = 16                                   # entries per NVFP4 block scale
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+
+
+def f32_to_e2m1_codes(x: np.ndarray) -> np.ndarray:
+    """OCP FP4 e2m1 codes (uint8, one per value) of x: round to nearest on
+    the grid 0, 0.5, 1, 1.5, 2, 3, 4, 6, ties to the even code (mantissa bit
+    0), saturating at 6; the sign is bit 3."""
+    a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), 6.0)
+    lo = np.searchsorted(E2M1_GRID, a, side="right") - 1       # largest grid value <= a
+    hi = np.minimum(lo + 1, 7)
+    dlo, dhi = a - E2M1_GRID[lo], E2M1_GRID[hi] - a
+    code = np.where(dlo < dhi, lo, np.where(dlo > dhi, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(np.signbit(np.asarray(x, dtype=np.float64)) & (code != 0), code | 8, code)
+    return code.astype(np.uint8)
+
+
+def quantize_blocks_nvfp4(rows: np.ndarray, block: int = FP4_BLOCK):
+    """NVFP4-style storage along the last axis (a multiple of 2 * block):
+    returns (packed codes uint8 [..., D / 2], block scales float32
+    [..., D / block]) with scale = e4m3(max|block| / 6)."""
+    rows = np.asarray(rows, dtype=np.float32)
+    d = rows.shape[-1]
+    assert d % block == 0 and block % 2 == 0
+    blk = rows.reshape(rows.shape[:-1] + (d // block, block))
+    amax = np.abs(blk).max(axis=-1)
+    sc_code = f32_to_e4m3_bits(np.maximum(amax / np.float32(6.0), np.float32(2.0 ** -9)))
+    scale = _e4m3_bits_to_f32(sc_code)
+    codes = f32_to_e2m1_codes(blk / scale[..., None]).reshape(rows.shape)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return packed, scale.astype(np.float32)
+
+
+def _e4m3_bits_to_f32(c: np.ndarray) -> np.ndarray:
+    c = np.asarray(c).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, c & 0x7
+    return (sign * np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))).astype(
+        np.float32)
 
 
 def quantize_tiles_e4m3(rows: np.ndarray, tile: int = KV_TILE):
@@ -332,10 +377,14 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
     # 7. K/V rows
     kv_scale = None
     kv_dtype = F32 if fp32 else BF16
-    if cfg.get("kv_fp8") and (cfg["split_kv"] or fp32):
-        raise ValueError("kv_fp8 applies to the bf16 latent-row configurations")
+    if (cfg.get("kv_fp8") or cfg.get("kv_fp4")) and (cfg["split_kv"] or fp32):
+        raise ValueError("kv_fp8 / kv_fp4 apply to the bf16 latent-row configurations")
+    if cfg.get("kv_fp8") and cfg.get("kv_fp4"):
+        raise ValueError("kv_fp8 and kv_fp4 exclude each other")
     if cfg.get("kv_fp8"):
         kv_dtype = E4M3
+    if cfg.get("kv_fp4"):
+        kv_dtype = E2M1
     if cfg["split_kv"]:
         k = np.full((n_blocks, page, Dqk), np.nan, dtype=np.float32)
         v = np.full((n_blocks, page, Dv), np.nan, dtype=np.float32)
@@ -347,10 +396,15 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
             k, v = f32_to_bf16_bits(k), f32_to_bf16_bits(v)
     else:
         kv8 = bool(cfg.get("kv_fp8", False))
+        kv4 = bool(cfg.get("kv_fp4", False))
         if kv8:
             k = np.full((n_blocks, page, Dqk), 0x7F, dtype=np.uint8)     # e4m3 NaN when unused
             n_tiles = (Dqk + KV_TILE - 1) // KV_TILE
             kv_scale = np.full((n_blocks, page, n_tiles), np.nan, dtype=np.float32)
+        elif kv4:
+            # e2m1 has no NaN: unused slots get NaN block scales instead
+            k = np.zeros((n_blocks, page, Dqk // 2), dtype=np.uint8)
+            kv_scale = np.full((n_blocks, page, Dqk // FP4_BLOCK), np.nan, dtype=np.float32)
         else:
             k = np.full((n_blocks, page, Dqk), np.nan if fp32 else 0x7FC0,
                         dtype=np.float32 if fp32 else np.uint16)
@@ -364,12 +418,14 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
                 rows = _normal(rng, (s1 - s0, Dqk))
                 if kv8:
                     rows, rsc = quantize_tiles_e4m3(rows)
+                elif kv4:
+                    rows, rsc = quantize_blocks_nvfp4(rows)
                 else:
                     rows = rows if fp32 else f32_to_bf16_bits(rows)
                 for j in range(s0 // page, (s1 + page - 1) // page):
                     lo, hi = j * page, min(s1, (j + 1) * page)
                     k[bt[i, j], lo - j * page: hi - j * page] = rows[lo - s0: hi - s0]
-                    if kv8:
+                    if kv8 or kv4:
                         kv_scale[bt[i, j], lo - j * page: hi - j * page] = rsc[lo - s0: hi - s0]
 
     return Workload(
@@ -378,7 +434,7 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
         q_pos=q_pos, q_idx=q_idx, q_idx_dtype=q_idx_dtype, w=w,
         k_idx=k_idx, k_idx_dtype=F32 if fp32 else E4M3, k_scale=k_scale, q=q,
         kv_dtype=kv_dtype, k=k, v=v, planted=planted, q_scale=q_scale, kv_scale=kv_scale,
-        kv_scale_tile=KV_TILE if kv_scale is not None else 0,
+        kv_scale_tile=(FP4_BLOCK if kv_dtype == E2M1 else KV_TILE) if kv_scale is not None else 0,
         attn_q_dtype=F32 if fp32 else BF16)
 
 

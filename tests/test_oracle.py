@@ -459,3 +459,59 @@ def test_fewer_candidates_than_k_returns_all_of_them():
         assert idx[r, :len(valid)].tolist() == sorted(valid.tolist())
         assert np.all(idx[r, len(valid):] == -1)
         assert np.isnan(kth[r, 0])
+
+
+# ---------------------------------------------- NVFP4-style KV cache (e2m1)
+
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]   # OCP FP4: codes 0..7, bit 3 = sign
+
+
+def test_e2m1_decoder_all_codes():
+    """All 16 FP4 e2m1 codes against the format's value table (1 sign, 2
+    exponent bits with bias 1, 1 mantissa bit; no NaN or infinity)."""
+    for c in range(16):
+        want = (-1.0 if c & 8 else 1.0) * E2M1_TABLE[c & 7]
+        got = oracle.e2m1_to_f64(c)
+        assert got == want and (c != 8 or math.copysign(1.0, got) == -1.0), (c, got)
+
+
+def _e2m1_rows_by_definition(packed):
+    """Unpack two codes per byte (even entry in the low nibble) and decode
+    them with the value table."""
+    lo, hi = packed & 0x0F, packed >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(packed.shape[:-1] + (packed.shape[-1] * 2,))
+    table = np.array(E2M1_TABLE)
+    return np.where(codes & 8, -1.0, 1.0) * table[codes & 7]
+
+
+def test_fp4_kv_blocks_brute_force():
+    """FP4 e2m1 KV cache with one scale per block of 16 entries: the oracle's
+    attention equals dense softmax attention over the selected rows, computed
+    here in numpy from rows decoded with the value table."""
+    wl = synth.make("c1", batch=2, ctx_list=[90, 40], Hi=4, Di=16, Hq=3, K=16, kv_fp4=True)
+    assert wl.kv_dtype == "e2m1" and wl.kv_scale_tile == 16
+    assert wl.k.shape[-1] * 2 == wl.Dqk and wl.kv_scale.shape[-1] == wl.Dqk // 16
+    b = oracle.Batch.of(wl)
+    rng = np.random.default_rng(6)
+    idx = np.full((wl.n_q, wl.K), -1, dtype=np.int32)
+    for r in range(wl.n_q):
+        sel = np.sort(rng.choice(int(wl.q_pos[r]) + 1, size=wl.K - 2, replace=False))
+        idx[r, : len(sel)] = sel
+    out, lse = oracle.sparse_attn(b, wl.q, wl.kv_dtype, wl.k, None, wl.kv_dtype, idx, wl.K, wl.Hq,
+                                  wl.Dqk, wl.Dv, wl.scale, **oracle.attn_kv_args(wl))
+    q = synth._bf16_bits_to_f32(wl.q).astype(np.float64)
+    blk_of = np.arange(wl.Dqk) // 16
+    deq = _e2m1_rows_by_definition(wl.k) * wl.kv_scale.astype(np.float64)[..., blk_of]
+    for r in range(wl.n_q):
+        sel = idx[r][idx[r] >= 0]
+        rows = np.array([deq[wl.block_table[wl.q_seq[r], s // wl.page], s % wl.page] for s in sel])
+        z = wl.scale * q[r] @ rows.T
+        p = np.exp(z - z.max(axis=1, keepdims=True))
+        ref = (p @ rows[:, : wl.Dv]) / p.sum(axis=1, keepdims=True)
+        assert np.abs(out[r] - ref).max() <= 1e-12 * np.abs(ref).max()
+        assert np.abs(lse[r] - (z.max(axis=1) + np.log(p.sum(axis=1)))).max() <= 1e-12
+    # swapped nibble order (a plausible slip) is caught
+    swapped = ((wl.k >> 4) | (wl.k << 4)).astype(np.uint8)
+    out_sw, _ = oracle.sparse_attn(b, wl.q, wl.kv_dtype, swapped, None, wl.kv_dtype, idx, wl.K,
+                                   wl.Hq, wl.Dqk, wl.Dv, wl.scale, **oracle.attn_kv_args(wl))
+    assert not np.allclose(out, out_sw)

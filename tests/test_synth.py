@@ -69,3 +69,30 @@ def test_fp8_query_quantisation():
     assert np.all(np.abs(deq - qa) <= amax / 448 * 16 + amax * 2.0 ** -8)
     # the rest of the workload is unchanged
     assert np.array_equal(a.k_idx, b.k_idx) and np.array_equal(a.q, b.q)
+
+
+def test_e2m1_quantisation_rounds_to_nearest_even_and_saturates():
+    """FP4 e2m1 codes: grid values map to themselves, halfway points go to the
+    even code (mantissa bit 0), values above 6 saturate, the sign is bit 3."""
+    x = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+                  0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, 100.0, -1.0, -0.74])
+    want = [0, 1, 2, 3, 4, 5, 6, 7,
+            0, 2, 2, 4, 4, 6, 6, 7, 7, 8 | 2, 8 | 1]
+    assert synth.f32_to_e2m1_codes(x).tolist() == want
+
+
+def test_nvfp4_blocks_bound_the_error():
+    """Each block of 16 gets scale e4m3(amax / 6); the dequantised value is
+    within half a grid step (at most 1 * scale, the 4 -> 6 gap) of the input,
+    plus the clipping of an e4m3 scale rounded below amax / 6."""
+    rng = np.random.default_rng(1)
+    rows = rng.standard_normal((50, 64)).astype(np.float32)
+    packed, scale = synth.quantize_blocks_nvfp4(rows)
+    assert packed.shape == (50, 32) and scale.shape == (50, 4)
+    codes = np.stack([packed & 15, packed >> 4], axis=-1).reshape(50, 64)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    deq = np.where(codes & 8, -1.0, 1.0) * grid[codes & 7] * np.repeat(scale, 16, axis=1)
+    amax = np.abs(rows.reshape(50, 4, 16)).max(axis=-1)
+    assert np.all(scale <= amax / 6 * (1 + 2.0 ** -4)) and np.all(scale >= amax / 6 * (1 - 2.0 ** -4))
+    bound = np.repeat(scale, 16, axis=1) * 1.0 + np.abs(rows) * 2.0 ** -3
+    assert np.all(np.abs(deq - rows) <= bound)
