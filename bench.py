@@ -54,14 +54,14 @@ def algorithmic_bytes(wl, out_bytes=2):
              output (`out_bytes` per element) and the indices read."""
     n_keys = int((wl.q_pos.astype("int64") + 1).sum())
     n_sel = int(sum(min(wl.K, int(p) + 1) for p in wl.q_pos))
-    esz = {"bf16": 2, "e4m3": 1}.get(wl.kv_dtype, 4)
+    esz = {"bf16": 2, "e4m3": 1, "e2m1": 0.5}.get(wl.kv_dtype, 4)
     kv_scale_b = 0 if getattr(wl, "kv_scale", None) is None else wl.kv_scale.shape[-1] * 4
     kesz = 1 if wl.k_idx_dtype == "e4m3" else 4
     idx_b = n_keys * (wl.Di * kesz + (4 if wl.k_scale is not None else 0)) \
         + wl.n_q * (wl.Hi * wl.Di * 2 + wl.Hi * 4) + n_keys * 4
     topk_b = n_keys * 4 + wl.n_q * wl.K * 4
     qesz = 2 if (getattr(wl, "attn_q_dtype", "") or wl.kv_dtype) == "bf16" else 4
-    attn_b = n_sel * (wl.Dqk * esz + kv_scale_b) + wl.n_q * wl.Hq * wl.Dqk * qesz \
+    attn_b = n_sel * int(wl.Dqk * esz + kv_scale_b) + wl.n_q * wl.Hq * wl.Dqk * qesz \
         + wl.n_q * wl.Hq * wl.Dv * out_bytes \
         + wl.n_q * wl.K * 4
     flops_idx = 2 * n_keys * wl.Hi * wl.Di
@@ -157,7 +157,7 @@ def whole_job_rate(world: int, n_q: int, ms_per_step: float) -> float:
 
 # Workload names of the committed ncu captures (profiles/*.md).
 PROFILE_WORKLOAD = {"c1": "decode b64 ctx8192", "c3": "decode b16 ctx131072",
-                    "c1:kv8": "decode b64 ctx8192 fp8 kv"}
+                    "c1:kv8": "decode b64 ctx8192 fp8 kv", "c1:kv4": "decode b64 ctx8192 fp4 kv"}
 
 
 def _kernel_traffic(kernel: str, source: str, workload: str):
@@ -467,7 +467,8 @@ def run_si(args):
         dist.init_process_group("nccl", device_id=dev)
 
     wl = synth.make(args.workload, seed=rank_seed(args.workload, rank),
-                    **({"kv_fp8": True} if args.kv_fp8 else {}))
+                    **({"kv_fp8": True} if args.kv_fp8 else {}),
+                    **({"kv_fp4": True} if args.kv_fp4 else {}))
     dw = si.upload(wl, dev)
     b, ix, at, K = dw.batch, dw.indexer, dw.attention, dw.k_top
     n_q = wl.n_q
@@ -600,7 +601,8 @@ def run_si(args):
     roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "peak_src": peaks["src"] + " (hbm_gbs, copy)",
-            "traffic": _kernel_traffic(kname, src, wl.name + (":kv8" if args.kv_fp8 else "")),
+            "traffic": _kernel_traffic(kname, src, wl.name + (":kv8" if args.kv_fp8 else
+                                                              ":kv4" if args.kv_fp4 else "")),
             "algorithmic_bytes_per_launch": algo[dom], "ms_per_launch": mean_k[dom]}
     total_bytes = algo["indexer"] + algo["topk"] + algo["attn"]
     step_gbs = total_bytes / (ms / 1e3) / 1e9
@@ -620,7 +622,7 @@ def run_si(args):
         "config": {"workload": _workload_name(wl), "batch": n_q, "context": ld, "top_k": K,
                    "indexer": f"{wl.Hi}x{wl.Di} e4m3 keys + fp32 scale, bf16 q",
                    "attention": f"{wl.Hq} heads x {wl.Dqk} (v {wl.Dv}) "
-                                f"{'e4m3 cache + fp32 scale per 128-entry tile, bf16 q' if args.kv_fp8 else 'bf16'}, "
+                                f"{'e4m3 cache + fp32 scale per 128-entry tile, bf16 q' if args.kv_fp8 else 'e2m1 cache + fp32 scale per 16-entry block, bf16 q' if args.kv_fp4 else 'bf16'}, "
                                 f"fp32 accumulate, {OUT_DTYPE} out",
                    "page": wl.page, "l2": "flushed between steps (512 MiB write)",
                    "step": "si_indexer_scores + si_topk + si_sparse_attn",
@@ -652,6 +654,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end legs")
+    ap.add_argument("--kv-fp4", action="store_true",
+                    help="store the latent KV cache in FP4 e2m1 (one scale per row and 16-entry "
+                         "block, the NVFP4 block)")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="store the latent KV cache in FP8 (one scale per row and 128-entry tile)")
     ap.add_argument("--prefill-only", action="store_true",

@@ -63,7 +63,11 @@ typedef enum si_status {
 typedef enum si_dtype {
     SI_F32 = 0,  /* IEEE float32 */
     SI_BF16 = 1, /* bfloat16 */
-    SI_E4M3 = 2  /* OCP FP8 e4m3 (finite, max 448) */
+    SI_E4M3 = 2, /* OCP FP8 e4m3 (finite, max 448) */
+    SI_E2M1 = 3  /* OCP FP4 e2m1 (max 6), two per byte, even element in the low
+                    nibble; attention caches only, with per-tile scales (the
+                    NVFP4 KV format of the vLLM article on DeepSeek-V4.1 uses
+                    blocks of 16 entries) */
 } si_dtype;
 
 /* Device status flags (sticky, OR-ed into the workspace status word). */
@@ -102,7 +106,9 @@ typedef struct si_batch {
 /* One paged cache: [n_blocks, page_size, row_stride] elements of dtype.
  * Dequantised entry d of a row = code * scale, the scale taken per row or per
  * tile of `scale_tile` consecutive entries (section 5.2 stores the KV cache in
- * FP8 per token and tile of 128 entries). */
+ * FP8 per token and tile of 128 entries).  row_dim and row_stride count
+ * elements; an SI_E2M1 row of row_stride entries takes row_stride / 2 bytes
+ * (row_stride even). */
 typedef struct si_paged {
     const void *data;    /* device; 16-byte aligned */
     const float *scale;  /* device dequantisation scales (> 0), or NULL for 1:

@@ -23,8 +23,8 @@ from . import _build
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = _build.LIB
 
-F32, BF16, E4M3 = 0, 1, 2
-DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3}
+F32, BF16, E4M3, E2M1 = 0, 1, 2, 3
+DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1}
 OP_INDEXER, OP_TOPK, OP_ATTN, OP_FUSED = 0, 1, 2, 3
 DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_INDEX, DEVFLAG_TIMEOUT = 1, 2, 4
 
@@ -161,14 +161,15 @@ class Paged:
     """Paged cache [n_blocks, page_size, row_stride] with optional scales: one
     per row, or one per `scale_tile` consecutive entries of a row."""
     data: torch.Tensor
-    dtype: str                  # "f32" | "bf16" | "e4m3"
+    dtype: str                  # "f32" | "bf16" | "e4m3" | "e2m1" (two per byte)
     row_dim: int
     scale: Optional[torch.Tensor] = None
     scale_tile: int = 0
 
     def c(self) -> c_paged:
+        stride = self.data.shape[-1] * (2 if self.dtype == "e2m1" else 1)  # in elements
         return c_paged(_ptr(self.data), _ptr(self.scale), DTYPES[self.dtype], self.row_dim,
-                       self.data.shape[-1], self.scale_tile)
+                       stride, self.scale_tile)
 
 
 @dataclasses.dataclass

@@ -86,8 +86,11 @@ si_status check_paged(const si_paged &p, const char *name, int need_dim)
         return fail(SI_ERR_INVALID_ARG, "%s.data is NULL", name);
     if (!aligned(p.data, 16))
         return fail(SI_ERR_INVALID_ARG, "%s.data is not 16-byte aligned", name);
-    if (p.dtype != SI_F32 && p.dtype != SI_BF16 && p.dtype != SI_E4M3)
+    if (p.dtype != SI_F32 && p.dtype != SI_BF16 && p.dtype != SI_E4M3 && p.dtype != SI_E2M1)
         return fail(SI_ERR_INVALID_ARG, "%s.dtype %d unknown", name, (int)p.dtype);
+    if (p.dtype == SI_E2M1 && (p.scale_tile < 1 || !p.scale || p.row_stride % 2 != 0))
+        return fail(SI_ERR_INVALID_ARG,
+                    "%s: e2m1 rows need per-tile scales and an even row_stride", name);
     if (p.row_dim < need_dim)
         return fail(SI_ERR_INVALID_ARG, "%s.row_dim %d < %d", name, p.row_dim, need_dim);
     if (p.row_stride < p.row_dim)
@@ -114,6 +117,8 @@ si_status check_indexer(const si_indexer *ix)
         return fail(SI_ERR_INVALID_ARG, "indexer head_dim %d outside 1..256", ix->head_dim);
     if (ix->k.scale_tile != 0)
         return fail(SI_ERR_UNSUPPORTED, "indexer keys take one scale per row (scale_tile 0)");
+    if (ix->k.dtype == SI_E2M1)
+        return fail(SI_ERR_UNSUPPORTED, "indexer keys are f32, bf16 or e4m3");
     return check_paged(ix->k, "indexer k", ix->head_dim);
 }
 
@@ -135,13 +140,15 @@ si_status check_attention(const si_attention *at)
     s = check_paged(at->v, "attention v", at->d_v);
     if (s != SI_OK)
         return s;
-    // keys and values: the dtype of q, or FP8 codes with scales (section 5.2)
+    // keys and values: the dtype of q, or FP8 / FP4 codes with scales (section
+    // 5.2; the vLLM article's NVFP4 KV)
     const bool fp8_kv = at->k.dtype == SI_E4M3 && at->v.dtype == SI_E4M3;
-    if (!fp8_kv && (at->k.dtype != at->q_dtype || at->v.dtype != at->q_dtype))
-        return fail(SI_ERR_UNSUPPORTED,
-                    "attention k and v must share q's dtype, or both be e4m3 with scales");
-    if (fp8_kv && (!at->k.scale || !at->v.scale))
-        return fail(SI_ERR_INVALID_ARG, "e4m3 attention k and v need scales");
+    const bool fp4_kv = at->k.dtype == SI_E2M1 && at->v.dtype == SI_E2M1;
+    if (!fp8_kv && !fp4_kv && (at->k.dtype != at->q_dtype || at->v.dtype != at->q_dtype))
+        return fail(SI_ERR_UNSUPPORTED, "attention k and v must share q's dtype, or both be "
+                                        "e4m3 or e2m1 with scales");
+    if ((fp8_kv || fp4_kv) && (!at->k.scale || !at->v.scale))
+        return fail(SI_ERR_INVALID_ARG, "e4m3 / e2m1 attention k and v need scales");
     return SI_OK;
 }
 

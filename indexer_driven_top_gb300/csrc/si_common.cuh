@@ -55,7 +55,18 @@ __device__ __forceinline__ int64_t page_row(const si_batch &b, int seq, int64_t 
     return (int64_t)blk * b.page_size + s % b.page_size;
 }
 
-// Scalar load of element i of a buffer of type t, widened to float.
+// OCP FP4 e2m1 code (low 4 bits): sign, 2 exponent bits with bias 1, 1
+// mantissa bit; exponent field 0 is subnormal (0 or 0.5).
+__device__ __forceinline__ float e2m1_to_float(unsigned c)
+{
+    const unsigned e = (c >> 1) & 3u, m = c & 1u;
+    const float v = e == 0 ? 0.5f * (float)m : (1.f + 0.5f * (float)m) * (float)(1u << (e - 1));
+    return (c & 8u) ? -v : v;
+}
+
+// Scalar load of element i of a buffer of type t, widened to float (e2m1:
+// element i is the low nibble of byte i / 2 when i is even, the high one when
+// it is odd).
 __device__ __forceinline__ float load_elem(const void *p, si_dtype t, int64_t i)
 {
     if (t == SI_F32)
@@ -64,13 +75,15 @@ __device__ __forceinline__ float load_elem(const void *p, si_dtype t, int64_t i)
         unsigned short u = __ldg(reinterpret_cast<const unsigned short *>(p) + i);
         return __uint_as_float((unsigned)u << 16);
     }
+    if (t == SI_E2M1) {
+        const unsigned byte = __ldg(reinterpret_cast<const unsigned char *>(p) + (i >> 1));
+        return e2m1_to_float((i & 1) ? byte >> 4 : byte & 15u);
+    }
     __nv_fp8_e4m3 v;
     v.__x = __ldg(reinterpret_cast<const unsigned char *>(p) + i);
     return float(v);
 }
 
-// Order-preserving map of a float score onto uint32 (larger score -> larger
-// key); -0 is folded onto +0 so that the two compare equal.
 // Dequantised entry d of physical row `row` of a paged cache: the stored
 // element times its scale (per row, or per tile of scale_tile entries).
 __device__ __forceinline__ float load_paged(const si_paged &p, int64_t row, int d)
@@ -87,6 +100,8 @@ __device__ __forceinline__ float load_paged(const si_paged &p, int64_t row, int 
     return x;
 }
 
+// Order-preserving map of a float score onto uint32 (larger score -> larger
+// key); -0 is folded onto +0 so that the two compare equal.
 __device__ __forceinline__ uint32_t order_key(float f)
 {
     f = f + 0.0f;

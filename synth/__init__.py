@@ -178,13 +178,15 @@ def f32_to_e2m1_codes(x: np.ndarray) -> np.ndarray:
     """OCP FP4 e2m1 codes (uint8, one per value) of x: round to nearest on
     the grid 0, 0.5, 1, 1.5, 2, 3, 4, 6, ties to the even code (mantissa bit
     0), saturating at 6; the sign is bit 3."""
-    a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), 6.0)
-    lo = np.searchsorted(E2M1_GRID, a, side="right") - 1       # largest grid value <= a
-    hi = np.minimum(lo + 1, 7)
-    dlo, dhi = a - E2M1_GRID[lo], E2M1_GRID[hi] - a
-    code = np.where(dlo < dhi, lo, np.where(dlo > dhi, hi, np.where(lo % 2 == 0, lo, hi)))
-    code = np.where(np.signbit(np.asarray(x, dtype=np.float64)) & (code != 0), code | 8, code)
-    return code.astype(np.uint8)
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x)
+    # count the midpoints below a; at a midpoint, ">" keeps the lower code and
+    # ">=" takes the upper, whichever of the two has mantissa bit 0
+    code = np.zeros(a.shape, dtype=np.uint8)
+    for mid, upper_even in ((0.25, False), (0.75, True), (1.25, False), (1.75, True),
+                            (2.5, False), (3.5, True), (5.0, False)):
+        code += (a >= mid) if upper_even else (a > mid)
+    return np.where(np.signbit(x) & (code != 0), code | 8, code).astype(np.uint8)
 
 
 def quantize_blocks_nvfp4(rows: np.ndarray, block: int = FP4_BLOCK):

@@ -160,6 +160,13 @@ def test_benchmark_workload_fp8_kv_cache(si):
     _run(si, wl, rows=[0, 31, 63])
 
 
+def test_benchmark_workload_fp4_kv_cache(si):
+    """The benchmarked decode step over an FP4 e2m1 latent cache (one scale
+    per row and 16-entry block)."""
+    wl = synth.make("c1", kv_fp4=True)
+    _run(si, wl, rows=[0, 31, 63])
+
+
 def test_long_context_fp8_kv_cache_split(si):
     """Long-context decode over an FP8 cache: few rows, so each row's key
     tiles are split over clusters and merged."""

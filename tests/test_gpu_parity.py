@@ -123,6 +123,14 @@ def test_fp8_kv_cache(si):
     _full_check(si, wl, ATOL_BF16)
 
 
+def test_fp4_kv_cache(si):
+    """Latent KV rows stored as FP4 e2m1 codes with one scale per block of 16
+    entries (the NVFP4 block): the whole path against the oracle on the
+    dequantised rows, through the CUDA-core attention kernel."""
+    wl = synth.make("c1", batch=3, ctx_list=[3001, 2048, 130], K=512, kv_fp4=True)
+    _full_check(si, wl, ATOL_BF16)
+
+
 def test_bf16_query_prefill_ragged_block(si):
     """Prefill indexer with a bf16 query: blocks of two rows, the last one
     holding a single row."""
