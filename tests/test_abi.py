@@ -149,3 +149,34 @@ def test_candidate_selection_host_validation_and_sizes(si):
     assert call(ws=P(ws + 16)) == 3
     assert lib.si_indexer_topk_cand(ctypes.byref(_batch(si, n_q=0)), ctypes.byref(ix), None, 0, 0,
                                     8, None, None, 0, None, 0, None) == 0
+
+
+def test_fp4_cache_host_validation(si):
+    """SI_E2M1 (FP4 codes, two per byte) is accepted for attention caches with
+    per-tile scales and an even row stride, and refused elsewhere."""
+    lib = si.load()
+    P = ctypes.c_void_p
+    fake = 1 << 20
+    ws = 256 << 20
+    b = ctypes.byref(_batch(si))
+    E2M1 = 3
+    # no per-tile scales
+    kp = si.c_paged(fake, None, E2M1, 64, 64)
+    at = si.c_attention(fake, si.BF16, 4, 64, 64, kp, kp, 0.125)
+    assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
+                              4096, None) == 1
+    assert b"e2m1" in lib.si_last_error()
+    # odd row stride
+    kp = si.c_paged(fake, fake, E2M1, 63, 63, 16)
+    at = si.c_attention(fake, si.BF16, 4, 63, 63, kp, kp, 0.125)
+    assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
+                              4096, None) == 1
+    # FP4 indexer keys are not supported
+    ix = si.c_indexer(fake, si.BF16, None, fake, 4, 32, si.c_paged(fake, fake, E2M1, 32, 32, 16))
+    assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) in (1, 2)
+    # FP4 keys and bf16 values do not mix
+    kp = si.c_paged(fake, fake, E2M1, 64, 64, 16)
+    vp = si.c_paged(fake, None, si.BF16, 64, 64)
+    at = si.c_attention(fake, si.BF16, 4, 64, 64, kp, vp, 0.125)
+    assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
+                              4096, None) == 2
