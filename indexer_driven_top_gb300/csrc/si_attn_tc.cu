@@ -14,8 +14,9 @@
 // columns) and enough rows in flight at once:
 //
 //   score CTA (rank 0) -- keeps the whole query in shared memory (128-byte
-//       swizzle) and streams the selected keys through a five-slot ring in
-//       "dim chunks" of 128 keys x 64 dims (16 KB).  Nine chunks build the
+//       swizzle) and streams the selected keys through a three-slot ring in
+//       "dim chunks" of 128 keys x 64 dims (16 KB; the FP8 cache's variant
+//       stages codes, below).  Nine chunks build the
 //       tile's logits S = q . k^T (UMMA M = 128 heads, N = 128 keys) in TMEM
 //       (double-buffered).  Eight softmax warps (two threads per head, each
 //       taking half of the tile's keys) turn a tile into weights P (f16) and
