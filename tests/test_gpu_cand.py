@@ -186,11 +186,12 @@ def test_long_candidate_lists_take_cluster_top_k(si):
     _check(wl, cand, g_idx, g_sc, o_idx, o_sc)
 
 
-def test_many_long_candidate_lists_take_streamed_top_k(si):
-    """160 rows with 17000 candidates each: too many rows for a cluster per
-    row, so the Top-K streams each row's slots.  Indexer shapes of 4 heads x
-    32 take the gather kernel and the CUDA-core indexer.  Eight sampled rows
-    are checked against the oracle."""
+def test_many_long_candidate_lists_take_one_cta_per_row(si):
+    """160 rows with 17000 candidates each: too many rows for a cluster of
+    several CTAs per row, so each row's slots take one CTA that caches 32
+    keys per thread in shared memory.  Indexer shapes of 4 heads x 32 take the
+    gather kernel and the CUDA-core indexer.  Eight sampled rows are checked
+    against the oracle."""
     wl = synth.make("c1", batch=160, ctx=17500, K=512, Hi=4, Di=32, Hq=1, Dqk=16, Dv=8)
     cand = synth.candidates(wl, 17000, seed=17)
     dw = si.upload(wl)

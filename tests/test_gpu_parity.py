@@ -237,14 +237,15 @@ def test_topk_exact_on_identical_scores(si):
 
 @pytest.mark.parametrize("ld", [16385, 40000, 131072])
 def test_topk_exact_long_rows_cluster(si, ld):
-    """Rows longer than one CTA's register cache take a cluster of CTAs
-    (one 16384-position segment each): bit-exact against the oracle with heavy
+    """Rows longer than one CTA's register cache (16384) take a cluster of
+    CTAs, each caching a 32768-position segment in shared memory (16385: one
+    CTA; 40000: two; 131072: four): bit-exact against the oracle with heavy
     ties spread over segments, rows that select everything, rows inside one
-    segment, and a row ending one past a segment boundary."""
+    segment, and rows ending at and one past a segment boundary."""
     rng = np.random.default_rng(ld)
     n_q = 12
-    pos = np.concatenate([rng.integers(0, ld, n_q - 5),
-                          [0, 100, 16383, 16384, ld - 1]]).astype(np.int32)
+    edges = np.minimum([0, 100, 16383, 16384, 32767, 32768], ld - 1)
+    pos = np.concatenate([rng.integers(0, ld, n_q - 7), edges, [ld - 1]]).astype(np.int32)
     sc = rng.integers(-30, 30, size=(n_q, ld)).astype(np.float32)   # many equal keys
     sc[1::3] = rng.standard_normal((len(sc[1::3]), ld)).astype(np.float32)
     sc[2, :5000] = -0.0
