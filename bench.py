@@ -435,6 +435,8 @@ def candidate_selection(si, dev, steps, n_cand=16384):
             "full_context": {"call": "si_indexer_scores + si_topk over all 131072 positions",
                              "ms_per_call": ms_full},
             "speedup_vs_full_context": ms_full / ms_c,
+            "indexer_dram_bytes_per_launch": _kernel_traffic(
+                "k_indexer_tc_cand", "si_indexer_tc.cu", "candidates b16 16384"),
             "l2": "flushed before every timed call (512 MiB write)"}
 
 
