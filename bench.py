@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -84,8 +85,11 @@ class ClockSampler:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            # the raw samples; SI_CLOCK_LOG_DIR keeps them somewhere other than the
+            # temporary directory
+            d = os.environ.get("SI_CLOCK_LOG_DIR") or tempfile.gettempdir()
+            os.makedirs(d, exist_ok=True)
+            self.path = os.path.join(d, f"si_clocks_{os.getpid()}.csv")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],

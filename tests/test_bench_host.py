@@ -57,3 +57,34 @@ def test_committed_captures_name_existing_sources():
         assert os.path.exists(os.path.join(ROOT, "indexer_driven_top_gb300", "csrc",
                                            rec["source"]))
         assert rec["dram_bytes_per_launch"] > 0
+
+
+def test_clock_sampler_reads_median_clock_and_active_reasons(tmp_path, monkeypatch):
+    """A stand-in nvidia-smi prints three samples (power cap active in one)
+    and then waits to be stopped, as the real one does under -lms."""
+    fake = tmp_path / "bin" / "nvidia-smi"
+    fake.parent.mkdir()
+    fake.write_text(
+        "#!/bin/sh\n"
+        "printf '0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\\n'\n"
+        "printf '0, 1980, 2070, 1390.7, 0x4, Not Active, Not Active, Not Active, Active\\n'\n"
+        "printf '0, 2055, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active\\n'\n"
+        "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{fake.parent}{os.pathsep}{os.environ['PATH']}")
+    monkeypatch.setenv("SI_CLOCK_LOG_DIR", str(tmp_path / "clocks"))
+    s = bench.ClockSampler(0)
+    s.start()
+    assert s.proc is not None and s.path.startswith(str(tmp_path / "clocks"))
+    import time
+    time.sleep(0.5)
+    got = s.stop()
+    assert got == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                   "samples": 3}
+
+
+def test_clock_sampler_without_nvidia_smi(monkeypatch, tmp_path):
+    monkeypatch.setenv("PATH", str(tmp_path))
+    s = bench.ClockSampler(0)
+    s.start()
+    assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
