@@ -74,6 +74,10 @@ typedef enum si_dtype {
 #define SI_DEVFLAG_BAD_BLOCK 0x1u /* block-table entry outside [0, n_blocks) */
 #define SI_DEVFLAG_BAD_INDEX 0x2u /* selected index outside [0, pos] (not -1) */
 #define SI_DEVFLAG_TIMEOUT 0x4u   /* a bounded on-chip wait gave up */
+#define SI_DEVFLAG_RANGE 0x8u     /* a value met an f16 operand outside its range
+                                     (|x| > 65504): the tensor-core attention
+                                     multiplies the f16 softmax weights with
+                                     f16 value entries, see si_sparse_attn */
 
 /* Workspace must be at least this aligned. */
 #define SI_WORKSPACE_ALIGN 256
@@ -192,7 +196,15 @@ si_status si_topk(const si_batch *b, const float *scores, int64_t ld_scores, int
  * out: device [n_q, n_heads, d_v] of out_dtype (SI_F32 or SI_BF16),
  *   out[r,h] = sum_j softmax_j(softmax_scale * q[r,h] . k[idx_j]) * v[idx_j];
  *   a row with no valid index gets zeros.
- * lse: device float [n_q, n_heads] natural-log sum-exp of the logits, or NULL. */
+ * lse: device float [n_q, n_heads] natural-log sum-exp of the logits, or NULL.
+ * Arithmetic of the tensor-core kernel (128 heads, 576-entry latent rows,
+ * V = the first 512 entries): logits from bf16 q and k with fp32
+ * accumulation; softmax weights rounded to f16 and multiplied with the value
+ * entries converted bf16 -> f16, accumulated in fp32.  Value entries (and,
+ * with an FP8 cache, query entries and dequantised key entries) must lie in
+ * the f16 range, |x| <= 65504: a larger one raises SI_DEVFLAG_RANGE and the
+ * output of its row is then undefined.  Below 2^-14 the f16 form is
+ * subnormal, an absolute error under 2^-25 per weighted entry. */
 si_status si_sparse_attn(const si_batch *b, const si_attention *at, const int32_t *idx,
                          int32_t k_top, void *out, si_dtype out_dtype, float *lse, void *ws,
                          size_t ws_bytes, void *stream);
@@ -253,17 +265,17 @@ si_status si_indexer_topk_cand(const si_batch *b, const si_indexer *ix, const in
  *   SI_OP_FUSED, i.e. 256 + 4 * max_ctx bytes rounded up) exceeds the scratch
  *   -- max_ctx above about 2.09 million positions -- returns
  *   SI_ERR_WORKSPACE before any CUDA call; use si_fused_decode for those.
- * Set-up: the first call on each device (with that device current) looks up
- *   the scratch address once (cudaGetSymbolAddress), which may load the
- *   library's device module.  Make that first call before any stream
- *   capture.
+ * Set-up: the first successful call on each device (with that device
+ *   current) looks up the scratch address (cudaGetSymbolAddress), which may
+ *   load the library's device module; a failed lookup is retried by the
+ *   next call.  Make that first call before any stream capture.
  * Concurrency: all calls on one device share the one scratch.  Calls issued
  *   in order on a single stream are fine; calls that overlap -- on different
  *   streams, or from several host threads without ordering -- race on the
  *   scratch and give undefined results.
  * scratch: if not NULL, *scratch receives the device address of the scratch
- *   (NULL on error), so si_workspace_status(*scratch, ...) reads the flags
- *   of the latest call. */
+ *   when the call returns SI_OK (NULL otherwise), so
+ *   si_workspace_status(*scratch, ...) reads the flags of the latest call. */
 #define SI_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 si_status si_fused_decode_noalloc(const si_batch *b, const si_indexer *ix,
                                   const si_attention *at, int32_t k_top, int32_t *idx,

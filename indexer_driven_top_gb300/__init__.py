@@ -26,7 +26,7 @@ LIB_PATH = _build.LIB
 F32, BF16, E4M3, E2M1 = 0, 1, 2, 3
 DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1}
 OP_INDEXER, OP_TOPK, OP_ATTN, OP_FUSED = 0, 1, 2, 3
-DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_INDEX, DEVFLAG_TIMEOUT = 1, 2, 4
+DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_INDEX, DEVFLAG_TIMEOUT, DEVFLAG_RANGE = 1, 2, 4, 8
 
 
 class SIError(RuntimeError):

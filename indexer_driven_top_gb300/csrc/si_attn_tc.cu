@@ -205,6 +205,13 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
     return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// true when either f16 half is infinite or NaN (exponent field all ones): a
+// value outside the f16 range met the conversion
+__device__ __forceinline__ bool f16x2_nonfinite(uint32_t w)
+{
+    return (w & 0x7C00u) == 0x7C00u || (w & 0x7C000000u) == 0x7C000000u;
+}
+
 // Two e4m3 codes (low byte first) times a scale, as two f16 (low, high).
 // The decode is exact; the product is rounded once to f16.
 __device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint32_t codes2, float sc)
@@ -214,13 +221,29 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint32_t codes2, float s
                       __half2float(__ushort_as_half(h.y)) * sc);
 }
 
-// 16 codes (one 16-byte unit) -> 16 f16 in two 16-byte units at dst0, dst1.
-__device__ __forceinline__ void dequant16(uint4 c, float sc, uint32_t dst0, uint32_t dst1)
+// 16 codes (one 16-byte unit) -> 16 f16 in two 16-byte units at dst0, dst1;
+// returns true if a product left the f16 range.
+__device__ __forceinline__ bool dequant16(uint4 c, float sc, uint32_t dst0, uint32_t dst1)
 {
-    st_shared_v4(dst0, e4m3x2_scaled_f16x2(c.x & 0xFFFFu, sc), e4m3x2_scaled_f16x2(c.x >> 16, sc),
-                 e4m3x2_scaled_f16x2(c.y & 0xFFFFu, sc), e4m3x2_scaled_f16x2(c.y >> 16, sc));
-    st_shared_v4(dst1, e4m3x2_scaled_f16x2(c.z & 0xFFFFu, sc), e4m3x2_scaled_f16x2(c.z >> 16, sc),
-                 e4m3x2_scaled_f16x2(c.w & 0xFFFFu, sc), e4m3x2_scaled_f16x2(c.w >> 16, sc));
+    const uint32_t a0 = e4m3x2_scaled_f16x2(c.x & 0xFFFFu, sc), a1 = e4m3x2_scaled_f16x2(c.x >> 16, sc),
+                   a2 = e4m3x2_scaled_f16x2(c.y & 0xFFFFu, sc), a3 = e4m3x2_scaled_f16x2(c.y >> 16, sc),
+                   b0 = e4m3x2_scaled_f16x2(c.z & 0xFFFFu, sc), b1 = e4m3x2_scaled_f16x2(c.z >> 16, sc),
+                   b2 = e4m3x2_scaled_f16x2(c.w & 0xFFFFu, sc), b3 = e4m3x2_scaled_f16x2(c.w >> 16, sc);
+    st_shared_v4(dst0, a0, a1, a2, a3);
+    st_shared_v4(dst1, b0, b1, b2, b3);
+    return f16x2_nonfinite(a0) | f16x2_nonfinite(a1) | f16x2_nonfinite(a2) |
+           f16x2_nonfinite(a3) | f16x2_nonfinite(b0) | f16x2_nonfinite(b1) |
+           f16x2_nonfinite(b2) | f16x2_nonfinite(b3);
+}
+
+// 16 bytes of bf16 -> f16 in place; returns true if a value left the f16 range.
+__device__ __forceinline__ bool to_f16_inplace(uint32_t a)
+{
+    const uint4 x = ld_shared_v4(a);
+    const uint32_t y0 = bf16x2_to_f16x2(x.x), y1 = bf16x2_to_f16x2(x.y), y2 = bf16x2_to_f16x2(x.z),
+                   y3 = bf16x2_to_f16x2(x.w);
+    st_shared_v4(a, y0, y1, y2, y3);
+    return f16x2_nonfinite(y0) | f16x2_nonfinite(y1) | f16x2_nonfinite(y2) | f16x2_nonfinite(y3);
 }
 
 // 4-byte global -> shared copy, asynchronous like cp_async_16 (zeros when
@@ -487,6 +510,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     cp_async_arrive(bars + B_STF8 + s8);
                 }
             } else {
+                bool range = false;
                 for (int g = 0; g < n_chunks; g++) {
                     const int tile = g / kQChunks, c = g % kQChunks, rs = tile % kRowSlots;
                     const int s8 = g % kStg8, slot = g % kRing8;
@@ -504,9 +528,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
 #pragma unroll
                     for (int m = 0; m < 4; m++) {
                         const int key = k0 + 32 * m;
-                        dequant16(ld_shared_v4(ssrc + key * 64), sc_t[key],
-                                  dst + sw128_offset(key, 2 * part),
-                                  dst + sw128_offset(key, 2 * part + 1));
+                        range |= dequant16(ld_shared_v4(ssrc + key * 64), sc_t[key],
+                                           dst + sw128_offset(key, 2 * part),
+                                           dst + sw128_offset(key, 2 * part + 1));
                     }
                     fence_async_smem();
                     mbar_arrive(bars + B_FULL + slot);
@@ -514,6 +538,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     if (c == kQChunks - 1)
                         mbar_arrive(bars + B_MEMPTY + rs);  // done with the tile's scales
                 }
+                if (range)
+                    raise_flag(st, SI_DEVFLAG_RANGE);
             }
         } else if (score_cta) {
             // physical rows come from the row table the row warp fills
@@ -685,11 +711,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                 // f16 too (one operand type per MMA; exact for |q| >= 2^-14)
                 mbar_wait(bars + B_QREADY, 0, st);
                 const int st_ = tid - kWarpSoft0 * 32;
-                for (int i = st_; i < (int)(kQChunks * kChunk / 16); i += kSoftmax) {
-                    const uint4 x = ld_shared_v4(base + kOffQ + i * 16);
-                    st_shared_v4(base + kOffQ + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
-                                 bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
-                }
+                bool range = false;
+                for (int i = st_; i < (int)(kQChunks * kChunk / 16); i += kSoftmax)
+                    range |= to_f16_inplace(base + kOffQ + i * 16);
+                if (range)
+                    raise_flag(st, SI_DEVFLAG_RANGE);
                 fence_async_smem();
                 mbar_arrive(bars + B_QCONV);
             }
@@ -924,6 +950,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
             // in place once their copies have landed (warps 12..15 and 17).
             const int ct = warp < kWarpMma ? tid - (kWarpQuad + 4) * 32 : 4 * 32 + lane;
             const int n_groups = kVGroups * T;
+            bool range = false;  // a value beyond the f16 range met the conversion
             if constexpr (KV8) {
                 // FP8 cache: staged codes times the key's scale into the f16
                 // group slot (two chunks of [128 keys x 64 dims], SW128), then
@@ -942,9 +969,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     for (int i = ct; i < kTile * 8; i += kConverters) {
                         const int key = i >> 3, uu = i & 7;  // 16 codes: dims 16 uu .. 16 uu + 15
                         const uint32_t d0 = dst + (uu >> 2) * kChunk;
-                        dequant16(ld_shared_v4(src + key * 128 + uu * 16), ksc[key],
-                                  d0 + sw128_offset(key, 2 * (uu & 3)),
-                                  d0 + sw128_offset(key, 2 * (uu & 3) + 1));
+                        range |= dequant16(ld_shared_v4(src + key * 128 + uu * 16), ksc[key],
+                                           d0 + sw128_offset(key, 2 * (uu & 3)),
+                                           d0 + sw128_offset(key, 2 * (uu & 3) + 1));
                     }
                     fence_async_smem();
                     mbar_arrive(bars + B_CONV + f);
@@ -956,14 +983,13 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                 if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingV) & 1, st))
                     break;
                 const uint32_t src = base + kOffRingV + slot * kGroup;
-                for (int i = ct; i < (int)(kGroup / 16); i += kConverters) {
-                    const uint4 x = ld_shared_v4(src + i * 16);
-                    st_shared_v4(src + i * 16, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
-                                 bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
-                }
+                for (int i = ct; i < (int)(kGroup / 16); i += kConverters)
+                    range |= to_f16_inplace(src + i * 16);
                 fence_async_smem();
                 mbar_arrive(bars + B_CONV + slot);
             }
+            if (range)
+                raise_flag(st, SI_DEVFLAG_RANGE);
         } else {
             // ------------------------------------------------------ O rescale
             const int h = tid - kWarpQuad * 32;  // head = TMEM lane
@@ -1262,13 +1288,26 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
                                  n_split, part_ml, st);
     if (e != cudaSuccess || n_split == 1)
         return e;
+    return launch_attn_combine(b, n_split, part_o, part_ml, out, out_dtype, lse, s);
+}
+
+cudaError_t launch_attn_combine(const si_batch &b, int n_split, const float *part_o,
+                                const float *part_ml, void *out, si_dtype out_dtype, float *lse,
+                                cudaStream_t s)
+{
     count_launch();
-    cudaLaunchConfig_t c2 = cfg;
-    c2.gridDim = dim3((unsigned)b.n_q, kHeads / kCombineHeads);
-    c2.blockDim = dim3(kCombineHeads * 32);
-    c2.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&c2, k_attn_combine, n_split, (const float *)part_o,
-                              (const float *)part_ml, out, out_dtype, lse);
+    // a programmatic dependent of the attention kernel (it waits for it
+    // before reading the partial results)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)b.n_q, kHeads / kCombineHeads);
+    cfg.blockDim = dim3(kCombineHeads * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_attn_combine, n_split, part_o, part_ml, out, out_dtype, lse);
 }
 
 }  // namespace si

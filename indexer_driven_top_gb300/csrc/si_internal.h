@@ -55,6 +55,13 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
                            int k_top, void *out, si_dtype out_dtype, float *lse, void *scratch,
                            size_t scratch_bytes, unsigned int *st, cudaStream_t s);
 
+// Merges the split partial results of the tensor-core attention kernels:
+// part_o [n_q * n_split * 128 heads, 512] unnormalised fp32 O and part_ml
+// [n_q * n_split * 128, 2] (running maximum in log2 units, row sum).
+cudaError_t launch_attn_combine(const si_batch &b, int n_split, const float *part_o,
+                                const float *part_ml, void *out, si_dtype out_dtype, float *lse,
+                                cudaStream_t s);
+
 // Radix select of the k_top best scores per row: among positions 0..q_pos[r],
 // or, with fixed_n > 0, among the first fixed_n entries of every row (q_pos
 // is then not read).  With `cand`, entry p of row r is slot p of the

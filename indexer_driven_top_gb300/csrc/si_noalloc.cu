@@ -26,9 +26,10 @@ constexpr size_t kScratchBytes = SI_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-std::once_flag g_once[si::kMaxDevices];
+// Scratch address per device, looked up on the first successful call; a
+// failed lookup is not remembered, so a later call retries it.
+std::mutex g_mu[si::kMaxDevices];
 void *g_addr[si::kMaxDevices];
-cudaError_t g_addr_err[si::kMaxDevices];
 
 using si::set_error;
 
@@ -61,19 +62,26 @@ si_status si_fused_decode_noalloc(const si_batch *b, const si_indexer *ix,
     if (dev < 0 || dev >= si::kMaxDevices)
         return set_error(SI_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev,
                          si::kMaxDevices);
-    std::call_once(g_once[dev], [dev] {
-        g_addr_err[dev] = cudaGetSymbolAddress(&g_addr[dev], g_scratch);
-    });
-    if (g_addr_err[dev] != cudaSuccess)
-        return set_error(SI_ERR_CUDA, "scratch address on device %d: %s", dev,
-                         cudaGetErrorString(g_addr_err[dev]));
-    e = cudaMemsetAsync(g_addr[dev], 0, si::kStatusBytes, (cudaStream_t)stream);
+    void *addr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu[dev]);
+        if (!g_addr[dev]) {
+            void *a = nullptr;
+            e = cudaGetSymbolAddress(&a, g_scratch);
+            if (e != cudaSuccess)
+                return set_error(SI_ERR_CUDA, "scratch address on device %d: %s", dev,
+                                 cudaGetErrorString(e));
+            g_addr[dev] = a;
+        }
+        addr = g_addr[dev];
+    }
+    e = cudaMemsetAsync(addr, 0, si::kStatusBytes, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return set_error(SI_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
-    if (scratch)
-        *scratch = g_addr[dev];
-    return si_fused_decode(b, ix, at, k_top, idx, out, out_dtype, lse, g_addr[dev],
-                           kScratchBytes, stream);
+    st = si_fused_decode(b, ix, at, k_top, idx, out, out_dtype, lse, addr, kScratchBytes, stream);
+    if (st == SI_OK && scratch)
+        *scratch = addr;
+    return st;
 }
 
 }  // extern "C"

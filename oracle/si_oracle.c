@@ -18,8 +18,8 @@
  *   3. attention reads only the selected K/V rows and returns the
  *      softmax-weighted sum of their values.
  *
- * Keys live in a paged cache ("reads data directly from the paged K-cache",
- * section 4.1): logical position s of sequence q is physical row
+ * Keys live in a paged cache, which the fused indexer of section 4.1 scores
+ * in place: logical position s of sequence q is physical row
  * block_table[q][s / page] * page + s % page.
  *
  * Storage codes: 0 = float32, 1 = bfloat16 bit patterns, 2 = FP8 e4m3 codes

@@ -1,8 +1,10 @@
 """Parity at full size: the decode workload the benchmark times (batch 64 x
 context 8192, indexer 64 x 128 FP8, Top-K 2048, 128 heads over 576-dim latent
 rows), run through exactly the calls the benchmark makes, checked against the
-oracle on sampled query rows.  Plus long-context and mixed/prefill workloads
-at full per-row size on fewer rows.
+oracle on every query row.  The long-context decode (16 x 131072) is checked on
+every row too; the causal prefill of 16384 on 256+ rows spread over the zigzag
+pairs of row blocks the prefill indexer deals out, and the mixed batch on all
+of its decode rows plus 64 rows of each prefill chunk.
 """
 import numpy as np
 import pytest
@@ -78,10 +80,10 @@ def _run(si, wl, rows):
     return dw
 
 
-def test_benchmark_workload_full_size_sampled_rows(si):
+def test_benchmark_workload_full_size_all_rows(si):
     wl = synth.make("c1")
     assert wl.n_q == 64 and wl.max_ctx == 8192 and wl.K == 2048
-    _run(si, wl, rows=[0, 31, 63])
+    _run(si, wl, rows=list(range(wl.n_q)))
 
 
 def _bf16_step(x):
@@ -105,7 +107,7 @@ def test_benchmark_workload_bf16_output(si):
     si.topk(b, scores, dw.k_top, idx, ws)
     si.sparse_attn(b, dw.attention, idx, dw.k_top, out, ws)
     assert si.workspace_status(ws) == 0
-    rows = [0, 40, 63]
+    rows = list(range(wl.n_q))
     g_idx = idx.cpu().numpy()
     g_out = out.float().cpu().numpy()
     ref, _ = oracle.sparse_attn(oracle.Batch.of(wl), wl.q, wl.kv_dtype, wl.k, wl.v, wl.kv_dtype,
@@ -122,53 +124,80 @@ def test_benchmark_workload_bf16_output(si):
 
 
 def test_long_context_planted_full_size(si):
-    """Batch 16 x context 131072 with 1 % planted keys; Top-K over 131072
-    scores takes the streaming path."""
+    """Batch 16 x context 131072 with 1 % planted keys, every row; Top-K over
+    131072 scores takes the cluster path, attention the split one."""
     wl = synth.make("c3")
     assert wl.n_q == 16 and wl.max_ctx == 131072
-    _run(si, wl, rows=[0, 7, 15])
+    _run(si, wl, rows=list(range(wl.n_q)))
+
+
+def _spread(lo, hi, n):
+    """n distinct rows spread over [lo, hi], both ends included."""
+    return sorted(set(int(x) for x in np.linspace(lo, hi, n).round()))
 
 
 def test_mixed_batch_full_size(si):
-    """32 requests with log-uniform contexts in [1024, 65536]: 28 decode rows
-    and 4 prefill chunks of 2048 rows that cross K = pos + 1 nowhere but
-    still span many tiles."""
+    """32 requests with log-uniform contexts in [1024, 65536]: all 28 decode
+    rows and 64 rows of each of the 4 prefill chunks of 2048 rows (first and
+    last rows included)."""
     wl = synth.make("c4")
     assert wl.n_q == 28 + 4 * 2048
-    _run(si, wl, rows=[0, 13, 27, 28, 28 + 2047, wl.n_q - 1])
+    rows = list(range(28))
+    for c in range(4):
+        rows += _spread(28 + 2048 * c, 28 + 2048 * c + 2047, 64)
+    _run(si, wl, rows=rows)
+
+
+def _prefill_rows(n_q, rows_per_block, k_top, n_pairs=128):
+    """Rows spread over the zigzag pairing of row blocks (block b goes with
+    block nb - 1 - b): the first row of block b and the last row of its
+    partner for n_pairs blocks b spread over the first half, plus the rows on
+    both sides of pos = K - 1 (where rows start to select) and the ends."""
+    nb = n_q // rows_per_block
+    rows = set()
+    for b in _spread(0, nb // 2 - 1, n_pairs):
+        rows.add(b * rows_per_block)
+        rows.add((nb - 1 - b) * rows_per_block + rows_per_block - 1)
+    rows.update(range(k_top - 3, k_top + 3))
+    rows.update((0, 1, n_q - 2, n_q - 1))
+    return sorted(rows)
 
 
 def test_causal_prefill_full_size(si):
     """Causal prefill of 16384 rows: rows below K = 2048 keep every position,
-    later rows select."""
+    later rows select.  The bf16 query takes blocks of two rows."""
     wl = synth.make("c2")
     assert wl.n_q == 16384
-    _run(si, wl, rows=[0, 100, 2047, 2048, 9000, 16383])
+    rows = _prefill_rows(wl.n_q, 2, wl.K)
+    assert len(rows) >= 256
+    _run(si, wl, rows=rows)
 
 
 def test_causal_prefill_full_size_fp8_query(si):
     """The same prefill with the indexer query stored in FP8 (per-(row, head)
     scale): the four-row prefill blocks at full size."""
     wl = synth.make("c2", q_idx_fp8=True)
-    _run(si, wl, rows=[0, 3, 4, 2047, 2048, 9001, 16383])
+    rows = _prefill_rows(wl.n_q, 4, wl.K)
+    assert len(rows) >= 256
+    _run(si, wl, rows=rows)
 
 
 def test_benchmark_workload_fp8_kv_cache(si):
     """The benchmarked decode step over an FP8 latent cache (one scale per row
     and 128-entry tile) on the tensor-core attention kernel."""
     wl = synth.make("c1", kv_fp8=True)
-    _run(si, wl, rows=[0, 31, 63])
+    _run(si, wl, rows=list(range(wl.n_q)))
 
 
 def test_benchmark_workload_fp4_kv_cache(si):
     """The benchmarked decode step over an FP4 e2m1 latent cache (one scale
     per row and 16-entry block)."""
     wl = synth.make("c1", kv_fp4=True)
-    _run(si, wl, rows=[0, 31, 63])
+    _run(si, wl, rows=list(range(wl.n_q)))
 
 
 def test_long_context_fp8_kv_cache_split(si):
     """Long-context decode over an FP8 cache: few rows, so each row's key
     tiles are split over clusters and merged."""
     wl = synth.make("c3", batch=4, ctx=40000, kv_fp8=True)
-    _run(si, wl, rows=[0, 3])
+    _run(si, wl, rows=list(range(wl.n_q)))

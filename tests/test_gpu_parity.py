@@ -287,6 +287,35 @@ def test_bad_block_and_bad_index_raise_flags(si):
     assert max_abs(out.cpu().numpy(), ref) <= ATOL_BF16
 
 
+def _large_entry(wl, seq, pos, entry, value):
+    """The workload with entry `entry` of the latent row at (seq, pos) set to
+    `value` (bf16)."""
+    k = wl.k.copy()
+    row = int(wl.block_table[seq, pos // wl.page]) * wl.page + pos % wl.page
+    k.reshape(-1, k.shape[-1])[row, entry] = synth.f32_to_bf16_bits(np.float32([value]))[0]
+    return synth.Workload(**{**wl.__dict__, "k": k})
+
+
+def test_value_beyond_f16_range_raises_flag(si):
+    """The tensor-core attention multiplies f16 softmax weights with value
+    entries converted bf16 -> f16.  A selected value above 65504 has no f16
+    form: the call must finish and raise SI_DEVFLAG_RANGE (no fault, no
+    trap); the same inputs without it raise nothing."""
+    wl = synth.make("c1", batch=2, ctx=300, K=2048)  # every position is selected
+    dw = si.upload(wl)
+    idx = torch.empty((2, 2048), dtype=torch.int32, device="cuda")
+    out = torch.empty((2, wl.Hq, wl.Dv), dtype=torch.float32, device="cuda")
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, dw.batch, dw.indexer, dw.attention, 2048))
+    si.fused_decode(dw.batch, dw.indexer, dw.attention, 2048, idx, out, ws)
+    assert si.workspace_status(ws) == 0
+    for entry in (3, 511):  # a value entry in each half of the row
+        big = si.upload(_large_entry(wl, 0, 5, entry, 1e5))
+        ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, big.batch, big.indexer,
+                                                  big.attention, 2048))
+        si.fused_decode(big.batch, big.indexer, big.attention, 2048, idx, out, ws)
+        assert si.workspace_status(ws) == si.DEVFLAG_RANGE, entry
+
+
 def test_empty_batch_is_noop(si):
     wl = synth.make("c0", L=64)
     dw = si.upload(wl)
