@@ -46,27 +46,40 @@ def _peaks():
 # ---------------------------------------------------------------- bytes/flops
 
 def algorithmic_bytes(wl, out_bytes=2):
-    """Bytes the method must move per step, by kernel (decode rows).
+    """Bytes the method must move per step, by kernel, and its FLOPs.
 
-    indexer: every visible key (e4m3 row + fp32 scale), the query's indexer
-             heads (bf16) and weights (fp32), and the fp32 scores written.
+    Keys and latent rows are counted once per sequence (the rows of a
+    prefill chunk share their sequence's cache; a decode row is the only row
+    of its request): a sequence's queries need its keys 0 .. max pos and at
+    most that many selected latent rows.
+    indexer: those keys (e4m3 row + fp32 scale), each row's indexer heads
+             (bf16) and weights (fp32), and the fp32 scores written.
     topk:    the scores read, the indices written.
     attn:    the selected latent rows (bf16), the query heads (bf16), the
              output (`out_bytes` per element) and the indices read."""
-    n_keys = int((wl.q_pos.astype("int64") + 1).sum())
-    n_sel = int(sum(min(wl.K, int(p) + 1) for p in wl.q_pos))
+    import numpy as np
+    pos = wl.q_pos.astype("int64")
+    n_keys_rows = int((pos + 1).sum())                         # scores per row
+    sel = np.minimum(wl.K, pos + 1)
+    n_sel_rows = int(sel.sum())                                # gathers per row
+    keys_seq = np.zeros(wl.n_seq, dtype=np.int64)
+    sel_seq = np.zeros(wl.n_seq, dtype=np.int64)
+    np.maximum.at(keys_seq, wl.q_seq, pos + 1)
+    np.add.at(sel_seq, wl.q_seq, sel)
+    n_keys = int(keys_seq.sum())
+    n_sel = int(np.minimum(sel_seq, keys_seq).sum())
     esz = {"bf16": 2, "e4m3": 1, "e2m1": 0.5}.get(wl.kv_dtype, 4)
     kv_scale_b = 0 if getattr(wl, "kv_scale", None) is None else wl.kv_scale.shape[-1] * 4
     kesz = 1 if wl.k_idx_dtype == "e4m3" else 4
     idx_b = n_keys * (wl.Di * kesz + (4 if wl.k_scale is not None else 0)) \
-        + wl.n_q * (wl.Hi * wl.Di * 2 + wl.Hi * 4) + n_keys * 4
-    topk_b = n_keys * 4 + wl.n_q * wl.K * 4
+        + wl.n_q * (wl.Hi * wl.Di * 2 + wl.Hi * 4) + n_keys_rows * 4
+    topk_b = n_keys_rows * 4 + wl.n_q * wl.K * 4
     qesz = 2 if (getattr(wl, "attn_q_dtype", "") or wl.kv_dtype) == "bf16" else 4
     attn_b = n_sel * int(wl.Dqk * esz + kv_scale_b) + wl.n_q * wl.Hq * wl.Dqk * qesz \
         + wl.n_q * wl.Hq * wl.Dv * out_bytes \
         + wl.n_q * wl.K * 4
-    flops_idx = 2 * n_keys * wl.Hi * wl.Di
-    flops_attn = 2 * n_sel * wl.Hq * (wl.Dqk + wl.Dv)
+    flops_idx = 2 * n_keys_rows * wl.Hi * wl.Di
+    flops_attn = 2 * n_sel_rows * wl.Hq * (wl.Dqk + wl.Dv)
     return {"indexer": idx_b, "topk": topk_b, "attn": attn_b,
             "flops_indexer": flops_idx, "flops_attn": flops_attn}
 
@@ -197,6 +210,93 @@ def _kernel_of(wl):
             else ("k_attn_generic", "si_generic.cu")}
 
 
+def roofline_of(kernel, wl, algo, ms, peaks, long_step, variant=""):
+    """Roofline of one kernel of the step: its algorithmic bytes and FLOPs over
+    its measured time, against the measured HBM copy bandwidth and the dense
+    tensor peak of its operand type (the indexer multiplies FP8 operands: the
+    measured bf16 peak x the nominal FP8/bf16 ratio of 2).  The bound reported
+    is the one the kernel is closer to; a kernel timed inside a step longer
+    than a millisecond is held to the sustained tensor figure."""
+    name, src = _kernel_of(wl)[kernel]
+    nbytes = algo[kernel]
+    flops = algo.get("flops_" + {"indexer": "indexer", "attn": "attn"}.get(kernel, ""), 0)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    tf_peak = peaks["bf16_tflops_sustained" if long_step else "bf16_tflops"]
+    if kernel == "indexer":
+        tf_peak *= 2.0
+    tfs = flops / (ms / 1e3) / 1e12 if flops else 0.0
+    hbm = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": gbs / peaks["hbm_gbs"], "peak_src": peaks["src"] + " (hbm_gbs, copy)"}
+    ten = {"bound": "tensor", "achieved": tfs, "peak": tf_peak, "unit": "TFLOP/s",
+           "frac": tfs / tf_peak,
+           "peak_src": peaks["src"] + (" (bf16_tflops_sustained" if long_step else " (bf16_tflops")
+                       + (" x 2 for FP8)" if kernel == "indexer" else ")")}
+    roof = dict(ten if ten["frac"] > hbm["frac"] else hbm)
+    roof.update({"kernel": name,
+                 "traffic": _kernel_traffic(name, src, wl.name + variant) if roof["bound"] == "hbm" else None,
+                 "algorithmic_bytes_per_launch": nbytes, "algorithmic_flop_per_launch": flops,
+                 "ms_per_launch": ms,
+                 "other_bound": {k: (ten if roof["bound"] == "hbm" else hbm)[k]
+                                 for k in ("bound", "achieved", "peak", "unit", "frac")}})
+    return roof
+
+
+def workload_record(si, dev, name, steps, warmup):
+    """One of the other configurations, timed the same way as the headline
+    step (three calls per step, L2 flushed before every step): queries/s, the
+    step's algorithmic bytes over its time, per-kernel times and the roofline
+    of the dominant kernel."""
+    import torch
+    import synth
+    wl = synth.make(name)
+    dw = si.upload(wl, dev)
+    b, ix, at, K = dw.batch, dw.indexer, dw.attention, dw.k_top
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, ix, at, K), dev)
+    scores = torch.empty((wl.n_q, b.max_ctx), dtype=torch.float32, device=dev)
+    idx = torch.empty((wl.n_q, K), dtype=torch.int32, device=dev)
+    out = torch.empty((wl.n_q, wl.Hq, wl.Dv), dtype=getattr(torch, OUT_DTYPE), device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev):
+        ev[0].record(stream)
+        si.indexer_scores(b, ix, scores, ws, stream)
+        ev[1].record(stream)
+        si.topk(b, scores, K, idx, ws, stream)
+        ev[2].record(stream)
+        si.sparse_attn(b, at, idx, K, out, ws, stream=stream)
+        ev[3].record(stream)
+
+    n = max(3, min(steps, 20))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for _ in range(max(3, warmup)):
+        step(evs[0])
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    assert si.workspace_status(ws, stream) == 0
+    kms = {"indexer": sum(e[0].elapsed_time(e[1]) for e in evs) / n,
+           "topk": sum(e[1].elapsed_time(e[2]) for e in evs) / n,
+           "attn": sum(e[2].elapsed_time(e[3]) for e in evs) / n}
+    ms = sum(e[0].elapsed_time(e[3]) for e in evs) / n
+    peaks = _peaks()
+    algo = algorithmic_bytes(wl, OUT_BYTES)
+    total = algo["indexer"] + algo["topk"] + algo["attn"]
+    gbs = total / (ms / 1e3) / 1e9
+    dom = max(kms, key=kms.get)
+    rec = {"workload": _workload_name(wl), "queries_per_s": wl.n_q / (ms / 1e3),
+           "ms_per_step": ms, "steps": n,
+           "hbm": {"algorithmic_bytes_per_step": total, "achieved_gbs": gbs,
+                   "frac_of_8tbs": gbs / NOMINAL_HBM_GBS, "frac_of_measured": gbs / peaks["hbm_gbs"]},
+           "kernels_ms": kms, "kernels": {k: v[0] for k, v in _kernel_of(wl).items()},
+           "roofline": roofline_of(dom, wl, algo, kms[dom], peaks, ms > 1.0),
+           "l2": "flushed between steps (512 MiB write)"}
+    del dw, ws, scores, idx, out, flush
+    torch.cuda.empty_cache()
+    return rec
+
+
 def cpu_baseline(wl, rows, threads):
     """The CPU oracle, as it stands, on a bounded sample of query rows."""
     import oracle
@@ -236,10 +336,11 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     per_q = sum(times) / (args.steps * len(rows))
     value = 1.0 / per_q
+    # ms_per_step is the time of one timed step as it ran: `rows` query rows
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * per_q * wl.n_q, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": 1e3 * sum(times) / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": _workload_name(wl), "rows_per_timed_step": len(rows)},
         "cpu_baseline": {"value": value, "unit": "queries/s", "cores": threads, "kind": "oracle",
@@ -250,32 +351,64 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+PREFILL_STRIP_ROWS = 1024  # 1024 rows x 16384 positions x 4 B = 64 MiB: the strip stays in L2
+
+
 def _prefill_once(si, dev, steps, q_fp8):
+    """The 16384-token causal prefill's indexer, run as the fused path runs it:
+    strips of PREFILL_STRIP_ROWS rows, each scored into a strip buffer that
+    stays in L2 and then consumed by the Top-K.  Returns (causal pairs,
+    algorithmic FLOPs, indexer ms per prefill: the sum over the strips of the
+    indexer launches' event-timed durations, ms of the whole strip loop)."""
     import torch
+    import indexer_driven_top_gb300 as si_mod
     import synth
     wl = synth.make("c2", Hq=1, Dqk=64, Dv=64, q_idx_fp8=q_fp8)
     dw = si.upload(wl, dev)
-    b, ix = dw.batch, dw.indexer
+    b, ix, K = dw.batch, dw.indexer, dw.k_top
     ld = b.max_ctx
-    scores = torch.empty((wl.n_q, ld), dtype=torch.float32, device=dev)
-    ws = si.alloc_workspace(4096, dev)
+    R = PREFILL_STRIP_ROWS
+    strip = torch.empty((R, ld), dtype=torch.float32, device=dev)
+    idx = torch.empty((wl.n_q, K), dtype=torch.int32, device=dev)
+    ws = si.alloc_workspace(si.workspace_size(si.OP_TOPK, b, ix, None, K), dev)
     stream = torch.cuda.current_stream(dev)
+    strips = []
+    for r0 in range(0, wl.n_q, R):
+        r1 = min(wl.n_q, r0 + R)
+        sb = si_mod.Batch(b.block_table, b.ctx_len, b.q_seq[r0:r1], b.q_pos[r0:r1], b.page_size,
+                          b.max_ctx, b.n_blocks, host_q_seq=wl.q_seq[r0:r1])
+        six = si_mod.Indexer(ix.q[r0:r1], ix.q_dtype, ix.w[r0:r1], ix.k,
+                             None if ix.q_scale is None else ix.q_scale[r0:r1])
+        strips.append((sb, six, strip[: r1 - r0], idx[r0:r1]))
+
+    def run(ev=None):
+        for i, (sb, six, sc, ib) in enumerate(strips):
+            if ev:
+                ev[2 * i].record(stream)
+            si.indexer_scores(sb, six, sc, ws, stream)
+            if ev:
+                ev[2 * i + 1].record(stream)
+            si.topk(sb, sc, K, ib, ws, stream)
+
     for _ in range(2):
-        si.indexer_scores(b, ix, scores, ws, stream)
+        run()
     torch.cuda.synchronize(dev)
-    n = max(3, min(steps, 20))
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    ev[0].record(stream)
-    for _ in range(n):
-        si.indexer_scores(b, ix, scores, ws, stream)
-    ev[1].record(stream)
+    n = max(3, min(steps, 10))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(strips))] for _ in range(n)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(n):
+        run(evs[k])
+    t1.record(stream)
     torch.cuda.synchronize(dev)
     assert si.workspace_status(ws, stream) == 0
-    ms = ev[0].elapsed_time(ev[1]) / n
+    ms = sum(e[2 * i].elapsed_time(e[2 * i + 1]) for e in evs for i in range(len(strips))) / n
+    ms_loop = t0.elapsed_time(t1) / n
     pairs = int((wl.q_pos.astype("int64") + 1).sum())
     flops = 2.0 * wl.Hi * wl.Di * pairs
-    del dw, scores, ws
-    return pairs, flops, ms
+    del dw, strip, idx, ws, strips
+    torch.cuda.empty_cache()
+    return pairs, flops, ms, ms_loop
 
 
 E2E_REPLICAS = 3
@@ -353,28 +486,36 @@ def e2e_pipelined(si, wl, dw, h_qidx, h_w, h_q, args, dev):
 def prefill_indexer(si, dev, steps):
     """Indexer throughput on the 16384-token causal prefill (every row scores
     all earlier positions): algorithmic TFLOP/s = 2 * Hi * Di * causal pairs /
-    kernel time.  The attention operands of that workload are not needed, so
-    they are generated at a token size (the indexer inputs are drawn first
-    and do not change).  Headline: the indexer query quantised to e4m3 with
-    one fp32 scale per (row, head), as the indexer prolog quantises it before
-    scoring (the oracle scores those same bytes).  Also timed: the exact bf16
-    query, which the tensor core runs as two e4m3 terms (twice the FP8 work)."""
+    indexer time, the indexer run strip by strip as the fused path runs it
+    (each 64 MiB score strip stays in L2 for the Top-K that follows).  The
+    attention operands of that workload are not needed, so they are generated
+    at a token size (the indexer inputs are drawn first and do not change).
+    Headline: the configuration's bf16 query, exact, which the tensor core
+    runs as two e4m3 terms (twice the algorithmic FP8 work).  Also timed, as a
+    labelled option: the query quantised to e4m3 with one fp32 scale per
+    (row, head), as the indexer prolog of section 4.3 quantises it (the oracle
+    scores those same bytes)."""
     peaks = _peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]   # measured bf16 burst x nominal fp8/bf16 ratio (2)
-    pairs, flops, ms8 = _prefill_once(si, dev, steps, True)
-    tflops8 = flops / (ms8 / 1e3) / 1e12
-    _, _, ms = _prefill_once(si, dev, steps, False)
+    pairs, flops, ms, ms_loop = _prefill_once(si, dev, steps, False)
     tflops = flops / (ms / 1e3) / 1e12
+    _, _, ms8, ms8_loop = _prefill_once(si, dev, steps, True)
+    tflops8 = flops / (ms8 / 1e3) / 1e12
     return {"workload": "causal prefill 16384 tokens, indexer 64x128, e4m3 keys + fp32 scale, "
-                        "e4m3 query + fp32 scale per (row, head)",
+                        "bf16 query",
             "kernel": "k_indexer_prefill",
-            "causal_pairs": pairs, "algorithmic_tflop": flops / 1e12, "ms_per_launch": ms8,
-            "tflops": tflops8, "fp8_peak_tflops": fp8_peak,
+            "timing": f"strips of {PREFILL_STRIP_ROWS} rows (64 MiB of scores, L2-resident), "
+                      "indexer then Top-K per strip; indexer launches event-timed and summed",
+            "causal_pairs": pairs, "algorithmic_tflop": flops / 1e12, "ms_per_prefill": ms,
+            "tflops": tflops, "fp8_peak_tflops": fp8_peak,
             "peak_src": peaks["src"] + " (bf16 burst x 2)",
-            "frac_of_fp8_peak": tflops8 / fp8_peak,
-            "bf16_query": {"ms_per_launch": ms, "tflops": tflops, "frac_of_fp8_peak": tflops / fp8_peak,
-                           "note": "exact bf16 query split into two e4m3 terms: the tensor core "
-                                   "executes twice the algorithmic FP8 work"}}
+            "frac_of_fp8_peak": tflops / fp8_peak,
+            "ms_strip_loop_with_topk": ms_loop,
+            "option_e4m3_query": {"ms_per_prefill": ms8, "tflops": tflops8,
+                                  "frac_of_fp8_peak": tflops8 / fp8_peak,
+                                  "ms_strip_loop_with_topk": ms8_loop,
+                                  "note": "query quantised to e4m3 + fp32 scale per (row, head); "
+                                          "not the configuration's query format"}}
 
 
 def candidate_selection(si, dev, steps, n_cand=16384):
@@ -602,18 +743,18 @@ def run_si(args):
     algo = algorithmic_bytes(wl, OUT_BYTES)
     mean_k = {k: sum(v) / len(v) for k, v in t_k.items()}
     dom = max(mean_k, key=mean_k.get)
-    kname, src = _kernel_of(wl)[dom]
-    achieved = algo[dom] / (mean_k[dom] / 1e3) / 1e9
-    roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-            "peak_src": peaks["src"] + " (hbm_gbs, copy)",
-            "traffic": _kernel_traffic(kname, src, wl.name + (":kv8" if args.kv_fp8 else
-                                                              ":kv4" if args.kv_fp4 else "")),
-            "algorithmic_bytes_per_launch": algo[dom], "ms_per_launch": mean_k[dom]}
+    roof = roofline_of(dom, wl, algo, mean_k[dom], peaks, ms > 1.0,
+                       ":kv8" if args.kv_fp8 else ":kv4" if args.kv_fp4 else "")
     total_bytes = algo["indexer"] + algo["topk"] + algo["attn"]
     step_gbs = total_bytes / (ms / 1e3) / 1e9
 
     prefill = None if args.no_prefill else prefill_indexer(si, dev, args.steps)
+    others = {}
+    if not args.no_other_workloads and args.workload == "c1" and not (args.kv_fp8 or args.kv_fp4):
+        del dw, ws, scores, idx, out, flush
+        torch.cuda.empty_cache()
+        others = {"long_context": workload_record(si, dev, "c3", args.steps, args.warmup),
+                  "mixed": workload_record(si, dev, "c4", args.steps, args.warmup)}
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -644,6 +785,7 @@ def run_si(args):
         "roofline": roof,
         "cpu_baseline": cpu,
         "prefill_indexer": prefill,
+        **others,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -660,6 +802,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end legs")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the long-context and mixed-batch records of the default line")
     ap.add_argument("--kv-fp4", action="store_true",
                     help="store the latent KV cache in FP4 e2m1 (one scale per row and 16-entry "
                          "block, the NVFP4 block)")

@@ -169,7 +169,8 @@ typedef enum si_op {
 
 /* Bytes of workspace the operation `op` wants for this batch (the status
  * word included).  For SI_OP_FUSED this is the size that scores all rows in
- * one strip, capped at 256 MiB; any workspace of at least
+ * one strip, capped at 64 MiB (a strip that stays in L2 between the indexer
+ * and the Top-K); any workspace of at least
  * si_workspace_min(SI_OP_FUSED, ...) works, with fewer rows per strip.
  * Arguments not used by `op` may be NULL.  Returns 0 on invalid arguments. */
 size_t si_workspace_size(si_op op, const si_batch *b, const si_indexer *ix,

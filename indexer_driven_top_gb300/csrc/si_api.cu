@@ -56,7 +56,9 @@ bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr size_t kFusedCap = (size_t)256 << 20;  // preferred fused workspace cap
+// Preferred fused workspace: the score strip stays in the GPU's L2 (about
+// 126 MB) between the indexer that writes it and the Top-K that reads it.
+constexpr size_t kFusedCap = (size_t)64 << 20;
 constexpr int kMaxTop = 16384;
 
 si_status check_batch(const si_batch *b)

@@ -1,6 +1,7 @@
 """Host logic of the benchmark that needs no GPU: the roofline's DRAM traffic
 is taken from a committed ncu capture only while the kernel's source is the
-one that was captured."""
+one that was captured; the roofline holds each kernel to the bound it is
+closer to; the clock sampler's parsing."""
 import hashlib
 import json
 import os
@@ -88,3 +89,49 @@ def test_clock_sampler_without_nvidia_smi(monkeypatch, tmp_path):
     s = bench.ClockSampler(0)
     s.start()
     assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+class _Wl:
+    """Shapes of a workload as the roofline needs them (decode-like)."""
+    name = "c1"
+    Hi, Di, Hq, Dqk, Dv = 64, 128, 128, 576, 512
+    q_idx_dtype, k_idx_dtype, kv_dtype = "bf16", "e4m3", "bf16"
+    n_seq, n_q = 64, 64
+
+
+def test_roofline_reports_the_closer_bound(monkeypatch):
+    """A kernel is held to the roof it is closer to: bytes against the
+    measured HBM copy bandwidth, FLOPs against the dense tensor peak of its
+    operands (FP8 for the indexer, the sustained figure inside a long step)."""
+    peaks = {"hbm_gbs": 1000.0, "bf16_tflops": 100.0, "bf16_tflops_sustained": 80.0,
+             "src": "measured"}
+    # 500 GB/s of bytes, 10 TFLOP/s of work: HBM-bound
+    r = bench.roofline_of("attn", _Wl, {"attn": 5e11, "flops_attn": 1e13}, 1000.0, peaks, False)
+    assert r["bound"] == "hbm" and abs(r["frac"] - 0.5) < 1e-12
+    assert r["other_bound"]["bound"] == "tensor" and abs(r["other_bound"]["frac"] - 0.1) < 1e-12
+    # 100 GB/s of bytes, 60 TFLOP/s of work inside a long step: tensor-bound,
+    # against the sustained peak
+    r = bench.roofline_of("attn", _Wl, {"attn": 1e11, "flops_attn": 6e13}, 1000.0, peaks, True)
+    assert r["bound"] == "tensor" and r["peak"] == 80.0 and abs(r["frac"] - 0.75) < 1e-12
+    assert r["traffic"] is None
+    # the indexer multiplies FP8 operands: twice the bf16 peak
+    r = bench.roofline_of("indexer", _Wl, {"indexer": 1e6, "flops_indexer": 1e16}, 1000.0, peaks,
+                          False)
+    assert r["bound"] == "tensor" and r["peak"] == 200.0
+
+
+def test_algorithmic_bytes_count_each_sequences_rows_once():
+    """A prefill's rows share their sequence's keys and latent rows: the
+    bytes the method must move count them once per sequence; decode rows
+    (one per request) count their own."""
+    import synth
+    wl = synth.make("c0")                         # one sequence, 256 causal rows, K = 32
+    a = bench.algorithmic_bytes(wl, out_bytes=4)
+    n = wl.n_q
+    q_b = n * wl.Hq * wl.Dqk * 4 + n * wl.Hq * wl.Dv * 4 + n * wl.K * 4
+    assert a["attn"] == 256 * wl.Dqk * 4 + q_b   # fp32 rows: each of the 256 positions once
+    assert a["flops_attn"] == 2 * sum(min(32, p + 1) for p in range(256)) * wl.Hq * (wl.Dqk + wl.Dv)
+    d = synth.make("c1", batch=3, ctx=100, K=64)  # three decode rows of 100 positions
+    a = bench.algorithmic_bytes(d)
+    row_b = d.Dqk * 2                            # bf16 latent row
+    assert a["attn"] == 3 * 64 * row_b + 3 * (d.Hq * d.Dqk * 2 + d.Hq * d.Dv * 2 + 64 * 4)
