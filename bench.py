@@ -197,10 +197,11 @@ def _kernel_traffic(kernel: str, source: str, workload: str):
 def _kernel_of(wl):
     """The CUDA kernel (and its source file) each step of the path runs for
     this workload: the tensor-core kernels where their shape conditions hold
-    (64 x 128 indexer with bf16 q and e4m3 keys; 128 heads x 576 bf16 latent
-    rows), the generic ones otherwise."""
+    (64 x 128 indexer with bf16 q and e4m3 keys; 128 heads x 576 latent rows
+    in bf16, FP8 or FP4), the generic ones otherwise."""
     tc_ix = wl.Hi == 64 and wl.Di == 128 and wl.q_idx_dtype == "bf16" and wl.k_idx_dtype == "e4m3"
-    tc_at = wl.Hq == 128 and wl.Dqk == 576 and wl.Dv == 512 and wl.kv_dtype in ("bf16", "e4m3")
+    tc_at = (wl.Hq == 128 and wl.Dqk == 576 and wl.Dv == 512
+             and wl.kv_dtype in ("bf16", "e4m3", "e2m1"))
     prefill = tc_ix and wl.n_seq == 1 and wl.n_q >= 64
     return {"indexer": ("k_indexer_prefill", "si_indexer_prefill.cu") if prefill
             else ("k_indexer_tc", "si_indexer_tc.cu") if tc_ix

@@ -48,12 +48,15 @@
 // unnormalised O and (m, l) per head to scratch, and k_attn_combine merges
 // the splits.
 //
-// FP8 cache (section 5.2: codes with one scale per token and tile of 128
-// entries; k_attn_tc<true>): the score CTA converts the query to f16 once and
-// dequantises key chunks to f16 (four warps gather codes into staging slots,
-// four dequantise them into the ring), the value CTA's converters dequantise
-// staged value groups; per-tile fp32 scales do not fold into bf16 exactly,
-// f16 keeps 11 significant bits.
+// Quantised caches (k_attn_tc<1>: section 5.2's FP8 codes with one scale per
+// token and tile of 128 entries; k_attn_tc<2>: the NVFP4 latent cache of the
+// vLLM article on DeepSeek-V4.1, e2m1 codes with one scale per 16-entry
+// block): the score CTA converts the query to f16 once and dequantises key
+// chunks to f16 (four warps gather codes -- and, for FP4, each chunk's block
+// scales -- into staging slots, four dequantise them into the ring), the
+// value CTA's converters dequantise staged value groups; per-tile or
+// per-block fp32 scales do not fold into bf16 exactly, f16 keeps 11
+// significant bits.
 //
 // Softmax: online in the log2 domain with fp32 state; the exponent reference
 // is only raised when a tile's maximum exceeds it by more than 8, so most
@@ -63,6 +66,7 @@
 // 0..pos get zero rows and zero weight.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <math.h>
 
@@ -123,6 +127,10 @@ static_assert(8 * kEpiBufs * 4096 <= kRingV * kGroup, "epilogue staging fits the
 // 128 entries): the score CTA dequantises each gathered chunk into an f16
 // ring slot itself, the value CTA's converters dequantise staged groups.
 constexpr int kKvTiles = 5;                                    // scales per 576-entry row
+// FP4 e2m1 cache: 288 bytes of codes per 576-entry row and one fp32 scale per
+// 16-entry block (36 per row); its staging needs less room than the FP8
+// cache's, in the same slots.
+constexpr int kKvBlocks4 = 36;
 constexpr int kRing8 = 3;                                      // score: f16 chunk slots
 constexpr int kStg8 = 3;                                       // score: fp8 chunk staging slots
 static_assert(kStg8 <= 5 && kRing8 <= 5, "barrier arrays");
@@ -140,6 +148,8 @@ constexpr uint32_t kOffVRing8 = (kOffVStg8 + kVStg8 * kVStgBytes8 + 1023u) & ~10
 constexpr uint32_t kOffF8 = kOffVRing8 + kVRing8 * kGroup;
 static_assert(kOffVStg8 == kOffRingV && kOffF8 - kOffVStg8 >= 8 * kEpiBufs * 4096,
               "epilogue staging fits the FP8 value buffers");
+static_assert(kTile * (32 + 16) <= kStgBytes8 && kTile * (64 + 32) <= kVStgBytes8,
+              "FP4 codes and block scales fit the FP8 staging slots");
 // both
 constexpr uint32_t kOffBar = std::max(
     std::max(kOffF + kPBufs * kHeads * 4, kOffMask + kRowSlots * 16),
@@ -234,6 +244,62 @@ __device__ __forceinline__ bool dequant16(uint4 c, float sc, uint32_t dst0, uint
     return f16x2_nonfinite(a0) | f16x2_nonfinite(a1) | f16x2_nonfinite(a2) |
            f16x2_nonfinite(a3) | f16x2_nonfinite(b0) | f16x2_nonfinite(b1) |
            f16x2_nonfinite(b2) | f16x2_nonfinite(b3);
+}
+
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
+// One byte of two e2m1 codes (even entry in the low nibble) times a block
+// scale, as two f16 (low, high): the decode is exact, the product is rounded
+// once to f16.
+__device__ __forceinline__ uint32_t e2m1x2_scaled_f16x2(uint32_t byte, float sc)
+{
+    return pack_f16x2(e2m1_to_float(byte & 15u) * sc, e2m1_to_float((byte >> 4) & 15u) * sc);
+}
+
+// One byte of two e2m1 codes -> two f16 (exact), by the hardware conversion.
+__device__ __forceinline__ __half2 e2m1x2_to_half2(uint32_t byte)
+{
+    const __half2_raw r = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)byte, __NV_E2M1);
+    return *reinterpret_cast<const __half2 *>(&r);
+}
+
+// One 16-entry e2m1 block (8 bytes) times its scale -> 16 f16 in two 16-byte
+// units at dst0, dst1; returns true if a product left the f16 range.  When
+// the scale is an f16 value (an NVFP4 block scale is an e4m3 value, so it
+// is), one packed f16 multiply rounds the exact product once -- the same
+// result as the fp32 product rounded to f16.
+__device__ __forceinline__ bool dequant16_e2m1(uint2 c, float sc, uint32_t dst0, uint32_t dst1)
+{
+    uint32_t w[8];
+    const __half hs = __float2half_rn(sc);
+    if (__half2float(hs) == sc) {
+        const __half2 s2 = __half2half2(hs);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const __half2 a = __hmul2(e2m1x2_to_half2((c.x >> (8 * i)) & 0xFFu), s2);
+            const __half2 b2 = __hmul2(e2m1x2_to_half2((c.y >> (8 * i)) & 0xFFu), s2);
+            w[i] = *reinterpret_cast<const uint32_t *>(&a);
+            w[4 + i] = *reinterpret_cast<const uint32_t *>(&b2);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            w[i] = e2m1x2_scaled_f16x2((c.x >> (8 * i)) & 0xFFu, sc);
+            w[4 + i] = e2m1x2_scaled_f16x2((c.y >> (8 * i)) & 0xFFu, sc);
+        }
+    }
+    st_shared_v4(dst0, w[0], w[1], w[2], w[3]);
+    st_shared_v4(dst1, w[4], w[5], w[6], w[7]);
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        bad |= f16x2_nonfinite(w[i]);
+    return bad;
 }
 
 // 16 bytes of bf16 -> f16 in place; returns true if a value left the f16 range.
@@ -375,12 +441,19 @@ __device__ __forceinline__ void issue_chunk(const LoaderState &ls, uint32_t dst,
     }
 }
 
-template <bool KV8>
+// KVT: the cache format -- 0 bf16 rows; 1 e4m3 codes with one fp32 scale
+// per row and 128-entry tile; 2 e2m1 codes (two per byte) with one fp32 scale
+// per row and 16-entry block.  The two quantised formats share the
+// dequantising pipeline (KV8 below) and differ only in how a gathered piece
+// of codes and scales becomes f16.
+template <int KVT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
           si_batch b, si_attention at, const int32_t *idx, int k_top, si_dtype out_dtype,
           float *lse, int n_split, float *part_ml, unsigned int *st)
 {
+    constexpr bool KV8 = KVT != 0;  // a quantised cache, dequantised to f16
+    constexpr bool KV4 = KVT == 2;  // ... from e2m1 codes
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
@@ -459,7 +532,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
     griddep_wait();
 
     const uint8_t *kv = static_cast<const uint8_t *>(at.k.data);
-    const int64_t row_bytes = at.k.row_stride * (KV8 ? 1 : 2);
+    const int64_t row_bytes = KV4 ? at.k.row_stride / 2 : at.k.row_stride * (KV8 ? 1 : 2);
     // value-CTA buffers as seen from the score CTA
     const uint32_t peer_p = mapa_shared(base + kOffP, 1);
     const uint32_t peer_f = mapa_shared(base + kOffF, 1);
@@ -500,13 +573,33 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                             rw[m] = rows[rs * kTile + k0 + 32 * m];
                         mbar_arrive(bars + B_MEMPTY + rs);
                     }
-                    const uint32_t sdst = base + kOffStg8 + s8 * kStgBytes8 + part * 16;
-                    const int64_t col = c * 64 + part * 16;
+                    if constexpr (KV4) {
+                        // per key: the chunk's 32 bytes of codes (units 0, 1)
+                        // and its four 16-entry block scales (unit 2)
+                        const uint32_t sc0 = base + kOffStg8 + s8 * kStgBytes8;
 #pragma unroll
-                    for (int m = 0; m < 4; m++)
-                        cp_async_16(sdst + (k0 + 32 * m) * 64,
-                                    rw[m] >= 0 ? kv + (int64_t)rw[m] * row_bytes + col : kv,
-                                    rw[m] >= 0 ? 16u : 0u);
+                        for (int m = 0; m < 4; m++) {
+                            const int key = k0 + 32 * m, r = rw[m];
+                            if (part < 2)
+                                cp_async_16(sc0 + key * 32 + part * 16,
+                                            r >= 0 ? kv + (int64_t)r * row_bytes + c * 32 + part * 16
+                                                   : kv,
+                                            r >= 0 ? 16u : 0u);
+                            else if (part == 2)
+                                cp_async_16(sc0 + kTile * 32 + key * 16,
+                                            r >= 0 ? at.k.scale + (int64_t)r * kKvBlocks4 + 4 * c
+                                                   : at.k.scale,
+                                            r >= 0 ? 16u : 0u);
+                        }
+                    } else {
+                        const uint32_t sdst = base + kOffStg8 + s8 * kStgBytes8 + part * 16;
+                        const int64_t col = c * 64 + part * 16;
+#pragma unroll
+                        for (int m = 0; m < 4; m++)
+                            cp_async_16(sdst + (k0 + 32 * m) * 64,
+                                        rw[m] >= 0 ? kv + (int64_t)rw[m] * row_bytes + col : kv,
+                                        rw[m] >= 0 ? 16u : 0u);
+                    }
                     cp_async_arrive(bars + B_STF8 + s8);
                 }
             } else {
@@ -522,15 +615,30 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                         (g >= kRing8 &&
                          !mbar_wait(bars + B_EMPTY + slot, (uint32_t)((g / kRing8) - 1) & 1, st)))
                         break;
-                    const uint32_t ssrc = base + kOffStg8 + s8 * kStgBytes8 + part * 16;
                     const uint32_t dst = base + kOffRing8 + slot * kChunk;
-                    const float *sc_t = scl + (rs * kKvTiles + c / 2) * kTile;
+                    if constexpr (KV4) {
+                        // one 16-entry block (8 bytes of codes) and its scale
+                        const uint32_t sc0 = base + kOffStg8 + s8 * kStgBytes8;
+                        const float *bsc = reinterpret_cast<const float *>(
+                            gbase + kOffStg8 + s8 * kStgBytes8 + kTile * 32);
 #pragma unroll
-                    for (int m = 0; m < 4; m++) {
-                        const int key = k0 + 32 * m;
-                        range |= dequant16(ld_shared_v4(ssrc + key * 64), sc_t[key],
-                                           dst + sw128_offset(key, 2 * part),
-                                           dst + sw128_offset(key, 2 * part + 1));
+                        for (int m = 0; m < 4; m++) {
+                            const int key = k0 + 32 * m;
+                            range |= dequant16_e2m1(ld_shared_v2(sc0 + key * 32 + part * 8),
+                                                    bsc[key * 4 + part],
+                                                    dst + sw128_offset(key, 2 * part),
+                                                    dst + sw128_offset(key, 2 * part + 1));
+                        }
+                    } else {
+                        const uint32_t ssrc = base + kOffStg8 + s8 * kStgBytes8 + part * 16;
+                        const float *sc_t = scl + (rs * kKvTiles + c / 2) * kTile;
+#pragma unroll
+                        for (int m = 0; m < 4; m++) {
+                            const int key = k0 + 32 * m;
+                            range |= dequant16(ld_shared_v4(ssrc + key * 64), sc_t[key],
+                                               dst + sw128_offset(key, 2 * part),
+                                               dst + sw128_offset(key, 2 * part + 1));
+                        }
                     }
                     fence_async_smem();
                     mbar_arrive(bars + B_FULL + slot);
@@ -590,13 +698,30 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                 for (int i = 0; i < kR; i++) {
                     const int key = kr0 + (kTile / kR) * i;
                     const int row = odd ? ls.rb1[i] : ls.rb0[i];
-                    cp_async_16(dst + key * 128 + u * 16,
-                                row >= 0 ? kv + (int64_t)row * row_bytes + j * 128 + u * 16 : kv,
-                                row >= 0 ? 16u : 0u);
-                    if (u == 0)
-                        cp_async_4(dst + kTile * 128 + key * 4,
-                                   row >= 0 ? kscale + (int64_t)row * kKvTiles + j : kscale,
-                                   row >= 0 ? 4u : 0u);
+                    if constexpr (KV4) {
+                        // per key: 64 bytes of codes (units 0..3) and the
+                        // group's eight 16-entry block scales (units 4, 5)
+                        if (u < 4)
+                            cp_async_16(dst + key * 64 + u * 16,
+                                        row >= 0 ? kv + (int64_t)row * row_bytes + j * 64 + u * 16
+                                                 : kv,
+                                        row >= 0 ? 16u : 0u);
+                        else if (u < 6)
+                            cp_async_16(dst + kTile * 64 + key * 32 + (u - 4) * 16,
+                                        row >= 0 ? kscale + (int64_t)row * kKvBlocks4 + 8 * j +
+                                                       4 * (u - 4)
+                                                 : kscale,
+                                        row >= 0 ? 16u : 0u);
+                    } else {
+                        cp_async_16(dst + key * 128 + u * 16,
+                                    row >= 0 ? kv + (int64_t)row * row_bytes + j * 128 + u * 16
+                                             : kv,
+                                    row >= 0 ? 16u : 0u);
+                        if (u == 0)
+                            cp_async_4(dst + kTile * 128 + key * 4,
+                                       row >= 0 ? kscale + (int64_t)row * kKvTiles + j : kscale,
+                                       row >= 0 ? 4u : 0u);
+                    }
                 }
                 cp_async_arrive(bars + B_FULL + slot);
             }
@@ -925,7 +1050,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     }
                     const int prow = ok ? blk[i] * b.page_size + sv[i] % b.page_size : -1;
                     rows[rs * kTile + 32 * i + lane] = prow;
-                    if constexpr (KV8) {
+                    if constexpr (KV8 && !KV4) {
                         // the key's scales of every 128-entry tile (0 for no key)
 #pragma unroll
                         for (int q5 = 0; q5 < kKvTiles; q5++)
@@ -962,16 +1087,21 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                          !mbar_wait(bars + B_F16E + f, (uint32_t)((g / kVRing8) - 1) & 1, st)))
                         break;
                     const uint32_t src = base + kOffVStg8 + s8 * kVStgBytes8;
-                    const float *ksc =
-                        reinterpret_cast<const float *>(gbase + kOffVStg8 + s8 * kVStgBytes8 +
-                                                        kTile * 128);
+                    const float *ksc = reinterpret_cast<const float *>(
+                        gbase + kOffVStg8 + s8 * kVStgBytes8 + kTile * (KV4 ? 64 : 128));
                     const uint32_t dst = base + kOffVRing8 + f * kGroup;
                     for (int i = ct; i < kTile * 8; i += kConverters) {
                         const int key = i >> 3, uu = i & 7;  // 16 codes: dims 16 uu .. 16 uu + 15
                         const uint32_t d0 = dst + (uu >> 2) * kChunk;
-                        range |= dequant16(ld_shared_v4(src + key * 128 + uu * 16), ksc[key],
-                                           d0 + sw128_offset(key, 2 * (uu & 3)),
-                                           d0 + sw128_offset(key, 2 * (uu & 3) + 1));
+                        if constexpr (KV4)
+                            range |= dequant16_e2m1(ld_shared_v2(src + key * 64 + uu * 8),
+                                                    ksc[key * 8 + uu],
+                                                    d0 + sw128_offset(key, 2 * (uu & 3)),
+                                                    d0 + sw128_offset(key, 2 * (uu & 3) + 1));
+                        else
+                            range |= dequant16(ld_shared_v4(src + key * 128 + uu * 16), ksc[key],
+                                               d0 + sw128_offset(key, 2 * (uu & 3)),
+                                               d0 + sw128_offset(key, 2 * (uu & 3) + 1));
                     }
                     fence_async_smem();
                     mbar_arrive(bars + B_CONV + f);
@@ -1217,7 +1347,12 @@ bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top)
                      at.v.scale == at.k.scale && at.k.scale_tile == 128 &&
                      at.v.scale_tile == 128 && at.k.row_stride == kDqk &&
                      ((uintptr_t)at.k.scale % 4) == 0;
-    return shape && (bf16 || fp8);
+    // e2m1 rows of 576 codes (288 bytes) with 36 block scales of 16 entries
+    const bool fp4 = at.k.dtype == SI_E2M1 && at.v.dtype == SI_E2M1 && at.k.scale &&
+                     at.v.scale == at.k.scale && at.k.scale_tile == 16 &&
+                     at.v.scale_tile == 16 && at.k.row_stride == kDqk &&
+                     ((uintptr_t)at.k.scale % 16) == 0;
+    return shape && (bf16 || fp8 || fp4);
 }
 
 cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int32_t *idx,
@@ -1236,10 +1371,13 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
     std::call_once(once[dev], [dev] {
         cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(k_attn_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            r = cudaFuncSetAttribute(k_attn_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(k_attn_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            r = cudaFuncSetAttribute(k_attn_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(k_attn_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemBytes);
         err_of[dev] = r;
     });
@@ -1282,9 +1420,12 @@ cudaError_t launch_attn_tc(const si_batch &b, const si_attention &at, const int3
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = at.k.dtype == SI_E4M3
-            ? cudaLaunchKernelEx(&cfg, k_attn_tc<true>, qmap, omap, b, at, idx, k_top, kdt, lse,
+            ? cudaLaunchKernelEx(&cfg, k_attn_tc<1>, qmap, omap, b, at, idx, k_top, kdt, lse,
                                  n_split, part_ml, st)
-            : cudaLaunchKernelEx(&cfg, k_attn_tc<false>, qmap, omap, b, at, idx, k_top, kdt, lse,
+        : at.k.dtype == SI_E2M1
+            ? cudaLaunchKernelEx(&cfg, k_attn_tc<2>, qmap, omap, b, at, idx, k_top, kdt, lse,
+                                 n_split, part_ml, st)
+            : cudaLaunchKernelEx(&cfg, k_attn_tc<0>, qmap, omap, b, at, idx, k_top, kdt, lse,
                                  n_split, part_ml, st);
     if (e != cudaSuccess || n_split == 1)
         return e;
