@@ -27,7 +27,7 @@ _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
 _lib = None
 _lock = threading.Lock()
 
-TYPE_CODE = {"f32": 0, "bf16": 1, "e4m3": 2, "e2m1": 3}
+TYPE_CODE = {"f32": 0, "bf16": 1, "e4m3": 2, "e2m1": 3, "mxe4m3": 4}
 
 
 def build(force: bool = False) -> str:
@@ -68,6 +68,15 @@ def _load():
             lib.oracle_sparse_attn.argtypes = [P, P, I32, I32, I32, I32, P, ctypes.c_int, P, P,
                                                ctypes.c_int, I64, I64, P, P, I32, I32, I32, P,
                                                I32, D, P, P, ctypes.c_int]
+            lib.oracle_indexer_scores_mx.argtypes = [P, P, I32, I32, I32, P, ctypes.c_int, P, P,
+                                                     P, P, I64, P, I64, ctypes.c_int]
+            lib.oracle_mx_quantize.argtypes = [P, ctypes.c_int, I64, I32, P, P]
+            lib.orc_mx_group.argtypes = [P, P]
+            lib.orc_mx_group.restype = ctypes.c_uint8
+            lib.orc_f64_to_e4m3_sat.argtypes = [D]
+            lib.orc_f64_to_e4m3_sat.restype = ctypes.c_uint8
+            lib.orc_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+            lib.orc_e8m0_to_f64.restype = D
             lib.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
             lib.orc_bf16_to_f64.restype = D
             lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
@@ -127,6 +136,36 @@ def e2m1_to_f64(code: int) -> float:
     return _load().orc_e2m1_to_f64(code)
 
 
+def e8m0_to_f64(code: int) -> float:
+    return _load().orc_e8m0_to_f64(code)
+
+
+def f64_to_e4m3(x: float) -> int:
+    """Nearest e4m3 code (ties to the even code, clamped to +-448, sign kept)."""
+    return _load().orc_f64_to_e4m3_sat(float(x))
+
+
+def mx_group(values):
+    """One MXFP8 group of 32 values: (codes uint8 [32], scale byte)."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    assert v.shape == (32,)
+    codes = np.empty(32, dtype=np.uint8)
+    sb = _load().orc_mx_group(_ptr(v), _ptr(codes))
+    return codes, int(sb)
+
+
+def mx_quantize(x, x_type: str):
+    """Rows of float32 values or bf16 bit patterns [..., dim] (dim a multiple
+    of 32) to MXFP8: (codes uint8 [..., dim], scale bytes uint8 [..., dim / 32])."""
+    x = _c(x)
+    dim = int(x.shape[-1])
+    n = int(x.size // dim) if dim else 0
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty(x.shape[:-1] + (dim // 32,), dtype=np.uint8)
+    _load().oracle_mx_quantize(_ptr(x), TYPE_CODE[x_type], n, dim, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
 def _elem_stride(a, type_: str) -> int:
     """Row stride in elements of a cache array (e2m1 packs two per byte)."""
     return a.shape[-1] * (2 if type_ == "e2m1" else 1)
@@ -141,9 +180,21 @@ def indexer_scores(b: Batch, q_idx, q_type: str, w, k, k_type: str, k_scale, Hi:
                    q_scale=None):
     """score[i, s] = sum_h w[r,h] * ReLU(q_idx[r,h,:] . k[s,:]) for s <= pos(r),
     -inf beyond; r = rows[i].  Keys are dequantised as code * k_scale[row];
-    with ``q_scale`` [n_q, Hi] the query too, as code * q_scale[r, h]."""
+    with ``q_scale`` [n_q, Hi] the query too, as code * q_scale[r, h].
+    MXFP8 keys (k_type "mxe4m3", k_scale the E8M0 bytes [..., Di / 32]) take
+    an MXFP8 query (q_scale its bytes [n_q, Hi, Di / 32]) or a float32 / bf16
+    one, converted per group of 32 first."""
     lib = _load()
     rr, n = _rows(rows, b.s.n_q)
+    if k_type == "mxe4m3":
+        q_idx, w, k = _c(q_idx), _c(w, np.float32), _c(k, np.uint8)
+        k_mx = _c(k_scale, np.uint8)
+        q_mx = None if q_type != "mxe4m3" else _c(q_scale, np.uint8)
+        out = np.empty((n, ld), dtype=np.float64)
+        lib.oracle_indexer_scores_mx(ctypes.byref(b.s), _ptr(rr), n, Hi, Di, _ptr(q_idx),
+                                     TYPE_CODE[q_type], _ptr(q_mx), _ptr(w), _ptr(k), _ptr(k_mx),
+                                     k.shape[-1], _ptr(out), ld, threads or default_threads())
+        return out
     q_idx, w, k, k_scale = _c(q_idx), _c(w, np.float32), _c(k), _c(k_scale, np.float32)
     q_scale = None if q_scale is None else _c(q_scale, np.float32)
     out = np.empty((n, ld), dtype=np.float64)

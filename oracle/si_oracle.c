@@ -26,7 +26,9 @@
  * (OCP definition: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits; code
  * S.1111.111 is NaN, there are no infinities), 3 = FP4 e2m1 codes, two per
  * byte with the even element in the low nibble (OCP definition: 1 sign, 2
- * exponent bits with bias 1, 1 mantissa bit; no NaN or infinity).
+ * exponent bits with bias 1, 1 mantissa bit; no NaN or infinity), 4 = MXFP8:
+ * e4m3 codes in groups of 32 consecutive entries of a row, each group with
+ * one E8M0 scale byte (section 5.1; see "MXFP8" below).
  *
  * No blocking, fusion or reordering: loops run in the order of the
  * definitions; a library sort (qsort) orders the candidates.
@@ -37,7 +39,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_E2M1 = 3 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_E2M1 = 3, ORC_MXE4M3 = 4 };
 
 typedef struct {
     int32_t n_seq;
@@ -88,7 +90,8 @@ double orc_e2m1_to_f64(uint8_t c)
     return sign ? -v : v;
 }
 
-/* element i of a buffer (for e2m1, i counts 4-bit elements) */
+/* element i of a buffer (for e2m1, i counts 4-bit elements; an MXFP8 buffer
+ * gives the bare e4m3 code value, without its group scale) */
 static double elem(const void *base, int type, int64_t i)
 {
     switch (type) {
@@ -100,6 +103,92 @@ static double elem(const void *base, int type, int64_t i)
     }
     default: return orc_e4m3_to_f64(((const uint8_t *)base)[i]);
     }
+}
+
+/* ------------------------------------------------------------------- MXFP8 */
+
+/* Section 5.1 of the page quantises the indexer's Q and K to MXFP8 with one
+ * scaling factor per group of 32 entries, computed from the data ("dynamic
+ * per-group").  MXFP8 is the OCP Microscaling (MX) v1.0 format: a group
+ * holds 32 e4m3 codes P_i and one E8M0 scale byte e, X = 2^(e - 127) (e = 255
+ * is NaN); entry i is X * P_i.  The page states no conversion rule, so the
+ * MX specification's own is taken:
+ *   shared exponent E = floor(log2(max_i |V_i|)) - 8 (8 is the exponent of
+ *   e4m3's largest normal, 448 = 1.75 * 2^8), clamped to [-127, 127]; an
+ *   all-zero group takes E = -127;
+ *   P_i = V_i / 2^E rounded to the nearest e4m3 value, ties to the even code,
+ *   magnitudes above 448 clamped to 448, the sign kept (a negative value that
+ *   rounds to zero gives -0).
+ * A group holding a NaN or an infinity gets e = 255 and NaN codes. */
+
+double orc_e8m0_to_f64(uint8_t e)
+{
+    return e == 255 ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+/* Nearest e4m3 code to x: the finite non-negative codes 0..126 are tried one
+ * by one; at equal distance the even code (mantissa bit 0 clear) wins; above
+ * 448 the largest code is taken; the sign bit is copied. */
+uint8_t orc_f64_to_e4m3_sat(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    double a = fabs(x);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 126; c++) {
+        double d = fabs(a - orc_e4m3_to_f64((uint8_t)c));
+        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
+            bd = d;
+            best = c;
+        }
+    }
+    if (a > 448.0)
+        best = 126;
+    return (uint8_t)(signbit(x) ? (best | 0x80) : best);
+}
+
+/* One group of 32 values: writes the 32 codes and returns the scale byte. */
+uint8_t orc_mx_group(const double *v, uint8_t *codes)
+{
+    double amax = 0.0;
+    int finite = 1;
+    for (int i = 0; i < 32; i++) {
+        if (!isfinite(v[i]))
+            finite = 0;
+        else if (fabs(v[i]) > amax)
+            amax = fabs(v[i]);
+    }
+    if (!finite) {
+        for (int i = 0; i < 32; i++)
+            codes[i] = 0x7F;
+        return 255;
+    }
+    int E = -127;
+    if (amax > 0.0) {
+        int ex;
+        frexp(amax, &ex);          /* amax = m * 2^ex, m in [0.5, 1): floor(log2) = ex - 1 */
+        E = ex - 1 - 8;
+        if (E < -127) E = -127;
+        if (E > 127) E = 127;
+    }
+    for (int i = 0; i < 32; i++)
+        codes[i] = orc_f64_to_e4m3_sat(ldexp(v[i], -E));
+    return (uint8_t)(E + 127);
+}
+
+/* Rows of `dim` entries (dim a multiple of 32) of a float32 or bf16 buffer
+ * to MXFP8 codes [n_rows, dim] and scale bytes [n_rows, dim / 32]. */
+void oracle_mx_quantize(const void *x, int type, int64_t n_rows, int32_t dim, uint8_t *codes,
+                        uint8_t *scales)
+{
+    double v[32];
+    for (int64_t r = 0; r < n_rows; r++)
+        for (int32_t g = 0; g < dim / 32; g++) {
+            for (int i = 0; i < 32; i++)
+                v[i] = elem(x, type, r * dim + g * 32 + i);
+            scales[r * (dim / 32) + g] = orc_mx_group(v, codes + r * dim + g * 32);
+        }
 }
 
 /* physical row of logical position s of sequence q */
@@ -205,6 +294,94 @@ void oracle_indexer_scores(const orc_batch *b, const int32_t *rows, int32_t n_ro
     idx_ctx c = { b, rows, Hi, Di, q_idx, q_type, q_scale, w, k, k_type, k_scale, k_stride,
                   scores, ld };
     orc_parallel(idx_row, &c, n_rows, nthreads);
+}
+
+/* ------------------------------------------------------- indexer, MXFP8 */
+
+/* Section 5.1's indexer: Q and K in MXFP8, one E8M0 scale per group of 32
+ * entries.  Section 4.3's prolog quantises the query per group (q8 =
+ * quant_per_group(q)) before the fused scoring; a query given in float32 or
+ * bf16 is converted here by the MX rule above, one (row, head) group at a
+ * time.  Each entry is then X * P (scale times code) and the score is the
+ * definition of section 2.2 over those values:
+ *   score(t,s) = sum_h w[t,h] * ReLU(sum_d q[t,h,d] * k[s,d]). */
+typedef struct {
+    const orc_batch *b;
+    const int32_t *rows;
+    int32_t Hi, Di;
+    const void *q_idx; int q_type;      /* [n_q, Hi, Di]: f32, bf16 or MX codes */
+    const uint8_t *q_mx;                /* [n_q, Hi, Di / 32] scale bytes (MX q) */
+    const float *w;                     /* [n_q, Hi] */
+    const uint8_t *k;                   /* paged MX codes [n_blocks, page, k_stride] */
+    const uint8_t *k_mx;                /* [n_blocks, page, k_stride / 32] scale bytes */
+    int64_t k_stride;
+    double *scores; int64_t ld;         /* [n_rows, ld] */
+} mx_ctx;
+
+/* The query of row r as MXFP8 values, [Hi * Di] doubles. */
+static void mx_query(const mx_ctx *c, int32_t r, double *q)
+{
+    int32_t G = c->Di / 32;
+    for (int32_t h = 0; h < c->Hi; h++)
+        for (int32_t g = 0; g < G; g++) {
+            int64_t off = ((int64_t)r * c->Hi + h) * c->Di + g * 32;
+            uint8_t codes[32], sb;
+            if (c->q_type == ORC_MXE4M3) {
+                memcpy(codes, (const uint8_t *)c->q_idx + off, 32);
+                sb = c->q_mx[((int64_t)r * c->Hi + h) * G + g];
+            } else {
+                double v[32];
+                for (int i = 0; i < 32; i++)
+                    v[i] = elem(c->q_idx, c->q_type, off + i);
+                sb = orc_mx_group(v, codes);
+            }
+            for (int i = 0; i < 32; i++)
+                q[(int64_t)h * c->Di + g * 32 + i] = orc_e4m3_to_f64(codes[i]) * orc_e8m0_to_f64(sb);
+        }
+}
+
+static double mx_score(const mx_ctx *c, int32_t r, const double *q, int64_t row)
+{
+    int32_t G = (int32_t)(c->k_stride / 32);
+    double score = 0.0;
+    for (int32_t h = 0; h < c->Hi; h++) {
+        double dot = 0.0;
+        for (int32_t d = 0; d < c->Di; d++) {
+            double kv = orc_e4m3_to_f64(c->k[row * c->k_stride + d]) *
+                        orc_e8m0_to_f64(c->k_mx[row * G + d / 32]);
+            dot += q[(int64_t)h * c->Di + d] * kv;
+        }
+        double relu = dot > 0.0 ? dot : 0.0;
+        score += (double)c->w[(int64_t)r * c->Hi + h] * relu;
+    }
+    return score + 0.0; /* -0.0 -> +0.0 */
+}
+
+static void mx_row(void *p, int64_t i)
+{
+    const mx_ctx *c = (const mx_ctx *)p;
+    const orc_batch *b = c->b;
+    int32_t r = c->rows ? c->rows[i] : (int32_t)i;
+    int32_t seq = b->q_seq[r];
+    int64_t pos = b->q_pos[r];
+    double *q = (double *)malloc(sizeof(double) * (size_t)c->Hi * (size_t)c->Di);
+    mx_query(c, r, q);
+    double *out = c->scores + i * c->ld;
+    for (int64_t s = 0; s < c->ld; s++)    /* causal: positions s <= pos only */
+        out[s] = s > pos ? -INFINITY : mx_score(c, r, q, page_row(b, seq, s));
+    free(q);
+}
+
+/* Scores of MXFP8 keys (codes `k`, scale bytes `k_mx`) against a query that is
+ * MXFP8 (q_type 4, scale bytes q_mx) or float32 / bf16 (converted per group),
+ * -inf past each row's position. */
+void oracle_indexer_scores_mx(const orc_batch *b, const int32_t *rows, int32_t n_rows, int32_t Hi,
+                              int32_t Di, const void *q_idx, int q_type, const uint8_t *q_mx,
+                              const float *w, const uint8_t *k, const uint8_t *k_mx,
+                              int64_t k_stride, double *scores, int64_t ld, int nthreads)
+{
+    mx_ctx c = { b, rows, Hi, Di, q_idx, q_type, q_mx, w, k, k_mx, k_stride, scores, ld };
+    orc_parallel(mx_row, &c, n_rows, nthreads);
 }
 
 /* ------------------------------------------------------------------ top-k */

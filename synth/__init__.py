@@ -23,6 +23,13 @@ Option ``q_idx_fp8=True`` (any config) stores the indexer query quantised the
 way the key cache is: e4m3 codes with one fp32 scale per (row, head), scale =
 max|q_h| / 448, drawn from the same q_idx values.
 
+Option ``idx_mx=True`` (bf16 configs) stores the indexer keys in MXFP8: e4m3
+codes in groups of 32 entries, each group with one E8M0 scale byte (2^(e -
+127)) set by the OCP MX rule, exponent floor(log2 max|group|) - 8, codes
+rounded to nearest even and clamped at 448 with the sign kept; unused slots
+hold NaN codes and scale byte 255.  With ``q_idx_mx=True`` as well the
+indexer query is stored the same way (otherwise it stays bf16).
+
 Option ``kv_fp8=True`` (latent-row configs) stores the attention KV cache as
 e4m3 codes with one fp32 scale per row and tile of 128 entries (576 entries:
 four full tiles and one of 64), scale = max|tile| / 448, quantised from the
@@ -49,7 +56,8 @@ from typing import Optional
 
 import numpy as np
 
-F32, BF16, E4M3, E2M1 = "f32", "bf16", "e4m3", "e2m1"
+F32, BF16, E4M3, E2M1, MXE4M3 = "f32", "bf16", "e4m3", "e2m1", "mxe4m3"
+MX_GROUP = 32                                    # entries per MXFP8 scale
 PAGE = 64
 E4M3_MAX = 448.0
 
@@ -101,18 +109,20 @@ class Workload:
     ctx_len: np.ndarray          # int32 [n_seq]
     q_seq: np.ndarray            # int32 [n_q]
     q_pos: np.ndarray            # int32 [n_q]
-    q_idx: np.ndarray            # f32, bf16 bits or e4m3 codes [n_q, Hi, Di]
+    q_idx: np.ndarray            # f32, bf16 bits or e4m3 / MX codes [n_q, Hi, Di]
     q_idx_dtype: str
     w: np.ndarray                # f32 [n_q, Hi]
-    k_idx: np.ndarray            # f32 or e4m3 codes [n_blocks, page, Di]
+    k_idx: np.ndarray            # f32 or e4m3 / MX codes [n_blocks, page, Di]
     k_idx_dtype: str
-    k_scale: Optional[np.ndarray]  # f32 [n_blocks, page] or None (=1)
+    k_scale: Optional[np.ndarray]  # f32 [n_blocks, page], None (=1), or for MX
+                                   # keys the E8M0 bytes uint8 [n_blocks, page, Di / 32]
     q: np.ndarray                # f32 or bf16 bits [n_q, Hq, Dqk]
     kv_dtype: str
     k: np.ndarray                # [n_blocks, page, Dqk] (row stride = last dim)
     v: Optional[np.ndarray]      # [n_blocks, page, Dv]; None = V is the first Dv cols of k
     planted: Optional[list] = None  # c3: per-sequence arrays of planted positions
-    q_scale: Optional[np.ndarray] = None  # f32 [n_q, Hi] when q_idx holds e4m3 codes
+    q_scale: Optional[np.ndarray] = None  # f32 [n_q, Hi] when q_idx holds e4m3 codes,
+                                          # uint8 E8M0 [n_q, Hi, Di / 32] for MX codes
     kv_scale: Optional[np.ndarray] = None  # f32 [n_blocks, page, n_tiles] for an e4m3 KV cache
     kv_scale_tile: int = 0                 # entries per KV scale tile (0: none)
     attn_q_dtype: str = ""                 # attention q storage ("" = kv_dtype)
@@ -239,6 +249,25 @@ def quantize_rows_e4m3(rows: np.ndarray):
     return codes, scale
 
 
+def quantize_groups_mx(x: np.ndarray):
+    """MXFP8 storage along the last axis (a multiple of 32): per group of 32,
+    exponent E = floor(log2 max|group|) - 8 clamped to [-127, 127] (-127 for
+    an all-zero group), codes = e4m3(x / 2^E) with the sign of x kept.
+    Returns (codes uint8 [..., D], E8M0 bytes uint8 [..., D / 32])."""
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    assert d % MX_GROUP == 0
+    g = x.reshape(x.shape[:-1] + (d // MX_GROUP, MX_GROUP)).astype(np.float64)
+    amax = np.abs(g).max(axis=-1)
+    _, ex = np.frexp(amax)                       # amax = m 2^ex, m in [0.5, 1)
+    E = np.where(amax > 0, ex.astype(np.int64) - 1 - 8, -127)
+    E = np.clip(E, -127, 127)
+    y = np.ldexp(g, -E[..., None]).astype(np.float32)
+    mag = f32_to_e4m3_bits(np.abs(y))
+    codes = np.where(np.signbit(g), mag | 0x80, mag).astype(np.uint8).reshape(x.shape)
+    return codes, (E + 127).astype(np.uint8)
+
+
 # ---------------------------------------------------------------- layout
 
 def _paged_pool(rng, ctx_len, page, spare=2):
@@ -327,8 +356,19 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
     # stored as e4m3 codes with one fp32 scale per (row, head)
     qi = _normal(rng, (n_q, Hi, Di), cfg["q_idx_std"])
     q8 = bool(cfg.get("q_idx_fp8", False))
+    mx = bool(cfg.get("idx_mx", False))
+    q_mx = bool(cfg.get("q_idx_mx", False))
+    if (mx or q_mx) and fp32:
+        raise ValueError("idx_mx applies to the bf16 configurations")
+    if q_mx and not mx:
+        raise ValueError("q_idx_mx needs idx_mx")
+    if q_mx and q8:
+        raise ValueError("q_idx_mx and q_idx_fp8 exclude each other")
     q_scale = None
-    if q8:
+    if q_mx:
+        q_idx, q_scale = quantize_groups_mx(qi)
+        q_idx_dtype = MXE4M3
+    elif q8:
         q_idx, q_scale = quantize_rows_e4m3(qi)
         q_idx_dtype = E4M3
     else:
@@ -340,7 +380,10 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
     k_idx = np.full((n_blocks, page, Di), np.nan if fp32 else 0, dtype=np.float32 if fp32 else np.uint8)
     if not fp32:
         k_idx[:] = 0x7F                       # e4m3 NaN in unused slots
-    k_scale = None if fp32 else np.full((n_blocks, page), np.nan, dtype=np.float32)
+    if mx:
+        k_scale = np.full((n_blocks, page, Di // MX_GROUP), 255, dtype=np.uint8)
+    else:
+        k_scale = None if fp32 else np.full((n_blocks, page), np.nan, dtype=np.float32)
     planted = None
     raw_keys = []
     for i in range(n_seq):
@@ -355,7 +398,7 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
             n_pl = int(round(cfg["planted"] * c))
             pos = np.sort(rng.choice(c, size=n_pl, replace=False)).astype(np.int32)
             rows = np.nonzero(q_seq == i)[0]
-            qmat = (qi[rows[-1]] if (fp32 or q8) else _bf16_bits_to_f32(q_idx[rows[-1]]))
+            qmat = (qi[rows[-1]] if (fp32 or q8 or q_mx) else _bf16_bits_to_f32(q_idx[rows[-1]]))
             qmat = qmat.astype(np.float64)
             target = 3.0 * np.linalg.norm(qmat, axis=1)
             delta = qmat.T @ np.linalg.solve(qmat @ qmat.T, target)   # min-norm solution
@@ -366,7 +409,7 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
         if fp32:
             _scatter_rows(k_idx, bt, i, raw_keys[i], page)
         else:
-            codes, sc = quantize_rows_e4m3(raw_keys[i])
+            codes, sc = (quantize_groups_mx if mx else quantize_rows_e4m3)(raw_keys[i])
             _scatter_rows(k_idx, bt, i, codes, page)
             _scatter_rows(k_scale, bt, i, sc, page)
     del raw_keys
@@ -434,7 +477,7 @@ def make(name: str, seed: Optional[int] = None, **over) -> Workload:
         name=name, Hi=Hi, Di=Di, Hq=Hq, Dqk=Dqk, Dv=Dv, K=int(cfg["K"]), page=page,
         scale=float(cfg["scale"]), block_table=bt, ctx_len=ctx_len, q_seq=q_seq,
         q_pos=q_pos, q_idx=q_idx, q_idx_dtype=q_idx_dtype, w=w,
-        k_idx=k_idx, k_idx_dtype=F32 if fp32 else E4M3, k_scale=k_scale, q=q,
+        k_idx=k_idx, k_idx_dtype=F32 if fp32 else (MXE4M3 if mx else E4M3), k_scale=k_scale, q=q,
         kv_dtype=kv_dtype, k=k, v=v, planted=planted, q_scale=q_scale, kv_scale=kv_scale,
         kv_scale_tile=(FP4_BLOCK if kv_dtype == E2M1 else KV_TILE) if kv_scale is not None else 0,
         attn_q_dtype=F32 if fp32 else BF16)

@@ -515,3 +515,182 @@ def test_fp4_kv_blocks_brute_force():
     out_sw, _ = oracle.sparse_attn(b, wl.q, wl.kv_dtype, swapped, None, wl.kv_dtype, idx, wl.K,
                                    wl.Hq, wl.Dqk, wl.Dv, wl.scale, **oracle.attn_kv_args(wl))
     assert not np.allclose(out, out_sw)
+
+
+# ------------------------------------------------------------------- MXFP8
+
+def test_e8m0_decoder_bytes():
+    """E8M0 (the MX scale type): byte e is 2^(e - 127), 255 is NaN."""
+    for e, v in ((0, 2.0 ** -127), (1, 2.0 ** -126), (126, 0.5), (127, 1.0), (128, 2.0),
+                 (254, 2.0 ** 127)):
+        assert oracle.e8m0_to_f64(e) == v
+    assert math.isnan(oracle.e8m0_to_f64(255))
+
+
+def test_e4m3_encoder_round_trips_every_finite_code():
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        assert oracle.f64_to_e4m3(oracle.e4m3_to_f64(c)) == c
+
+
+def test_e4m3_encoder_matches_torch_rounding():
+    """Round to nearest even into e4m3, checked against torch's float32 ->
+    float8_e4m3fn conversion on float32 inputs inside the finite range
+    (subnormals, exact midpoints and negative values that round to zero
+    included)."""
+    rng = np.random.default_rng(21)
+    x = np.concatenate([
+        rng.uniform(-448, 448, 4000), rng.standard_normal(4000) * 2.0 ** -7,
+        rng.standard_normal(2000) * 2.0 ** -12,
+        # midpoints between neighbouring codes
+        np.array([(oracle.e4m3_to_f64(c) + oracle.e4m3_to_f64(c + 1)) / 2 for c in range(126)]),
+    ]).astype(np.float32)
+    x = np.concatenate([x, -x])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.f64_to_e4m3(float(v)) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_encoder_ties_to_even_and_saturates():
+    for c in range(126):
+        lo, hi = oracle.e4m3_to_f64(c), oracle.e4m3_to_f64(c + 1)
+        mid = (lo + hi) / 2
+        assert oracle.f64_to_e4m3(mid) == (c if c % 2 == 0 else c + 1)
+        assert oracle.f64_to_e4m3(np.nextafter(mid, 0)) == c
+        assert oracle.f64_to_e4m3(np.nextafter(mid, 1000)) == c + 1
+    for v in (448.5, 480.0, 1e6, math.inf):
+        assert oracle.f64_to_e4m3(v) == 0x7E and oracle.f64_to_e4m3(-v) == 0xFE
+    assert oracle.f64_to_e4m3(-1e-30) == 0x80 and oracle.f64_to_e4m3(0.0) == 0x00
+
+
+def _mx_values(codes, sb):
+    """X * P for one group, decoded here from the formats' definitions."""
+    return _e4m3_by_definition(np.asarray(codes)) * 2.0 ** (int(sb) - 127)
+
+
+def test_mx_group_closed_forms():
+    """The MX conversion rule: exponent floor(log2 amax) - 8, so the largest
+    entry lands in [256, 512) before rounding and clamps to 448 beyond it."""
+    codes, sb = oracle.mx_group(np.zeros(32))
+    assert sb == 0 and (codes == 0).all()
+    for k in (-100, -20, -1, 0, 3, 60, 110):
+        v = np.zeros(32)
+        v[7] = 2.0 ** k
+        v[8] = -(2.0 ** k) / 3
+        codes, sb = oracle.mx_group(v)
+        assert sb == 127 + k - 8
+        assert codes[7] == 0x78                         # 256 = 1.0 * 2^8
+        assert codes[8] == 0x80 | oracle.f64_to_e4m3(256 / 3)
+    # just below the next power of two: 511/256 * 2^k scales to 511 -> 448
+    v = np.full(32, 0.25)
+    v[0] = 511 / 256 * 2.0 ** 5
+    codes, sb = oracle.mx_group(v)
+    assert sb == 127 + 5 - 8 and codes[0] == 0x7E
+    # values that are e4m3 numbers times 2^E with amax in [256, 448] come back exactly
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        E = int(rng.integers(-60, 60))
+        c = rng.integers(0, 0x7F, size=32).astype(np.uint8)
+        c[rng.integers(32)] = rng.integers(0x78, 0x7F)    # a code in [256, 448]
+        c = np.where(rng.random(32) < 0.5, c | 0x80, c).astype(np.uint8)
+        v = _e4m3_by_definition(c) * 2.0 ** E
+        codes, sb = oracle.mx_group(v)
+        assert sb == 127 + E
+        assert np.array_equal(_mx_values(codes, sb), v)
+
+
+def test_mx_group_symmetry_scaling_and_error_bound():
+    rng = np.random.default_rng(8)
+    for _ in range(200):
+        v = rng.standard_normal(32) * 2.0 ** rng.integers(-30, 30)
+        codes, sb = oracle.mx_group(v)
+        c2, s2 = oracle.mx_group(2 * v)
+        assert s2 == sb + 1 and np.array_equal(c2, codes)
+        c3, s3 = oracle.mx_group(-v)
+        assert s3 == sb and np.array_equal(c3, codes ^ 0x80)
+        X = 2.0 ** (sb - 127)
+        err = np.abs(_mx_values(codes, sb) - v)
+        y = np.abs(v) / X
+        normal = (y >= 2.0 ** -6) & (y <= 448)
+        # half an e4m3 step: 2^(floor(log2 y) - 4) in scaled units
+        assert (err[normal] <= 2.0 ** (np.floor(np.log2(y[normal])) - 4) * X).all()
+        assert (err[y < 2.0 ** -6] <= 2.0 ** -10 * X).all()
+        clip = y > 448
+        assert np.allclose(err[clip], np.abs(v[clip]) - 448 * X)
+
+
+def test_mx_quantize_rows_group_by_group():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((5, 3, 96)).astype(np.float32)
+    codes, scales = oracle.mx_quantize(x, "f32")
+    assert codes.shape == x.shape and scales.shape == (5, 3, 3)
+    for i in range(5):
+        for j in range(3):
+            for g in range(3):
+                c, s = oracle.mx_group(x[i, j, 32 * g: 32 * g + 32].astype(np.float64))
+                assert s == scales[i, j, g] and np.array_equal(c, codes[i, j, 32 * g: 32 * g + 32])
+    # bf16 input: the bit patterns decode first
+    xb = synth.f32_to_bf16_bits(x)
+    cb, sbb = oracle.mx_quantize(xb, "bf16")
+    c2, s2 = oracle.mx_quantize((xb.astype(np.uint32) << 16).view(np.float32), "f32")
+    assert np.array_equal(cb, c2) and np.array_equal(sbb, s2)
+
+
+def _mx_workload(q_mx, **over):
+    args = dict(batch=2, ctx_list=[70, 45], Hi=3, Di=64, Hq=2, Dqk=8, Dv=4, K=5, idx_mx=True,
+                q_idx_mx=q_mx)
+    args.update(over)
+    return synth.make("c1", **args)
+
+
+def test_mx_scores_equal_scores_of_the_dequantised_values():
+    """MXFP8 keys and query: the scores equal the oracle's float32 path on the
+    values X * P decoded here from the definitions (each is exact in float32
+    at these magnitudes), and brute force on two rows."""
+    wl = _mx_workload(True)
+    assert wl.k_scale.dtype == np.uint8 and wl.k_scale.shape[-1] == 2
+    b = oracle.Batch.of(wl)
+    sc = oracle.indexer_scores(b, wl.q_idx, "mxe4m3", wl.w, wl.k_idx, "mxe4m3", wl.k_scale,
+                               wl.Hi, wl.Di, wl.max_ctx, q_scale=wl.q_scale)
+
+    def deq(codes, sbytes):
+        """X * P; scale byte 255 (unused slots) is NaN"""
+        vals = _e4m3_by_definition(codes).reshape(codes.shape[:-1] + (-1, 32))
+        x = np.where(sbytes == 255, np.nan, 2.0 ** (sbytes.astype(np.float64) - 127))
+        return (vals * x[..., None]).reshape(codes.shape)
+
+    qd = deq(wl.q_idx, wl.q_scale)
+    kd = deq(wl.k_idx, wl.k_scale)
+    assert np.array_equal(qd.astype(np.float32).astype(np.float64), qd)
+    fin_k = np.isfinite(kd)
+    assert np.array_equal(kd[fin_k].astype(np.float32).astype(np.float64), kd[fin_k])
+    sc2 = oracle.indexer_scores(b, qd.astype(np.float32), "f32", wl.w, kd.astype(np.float32),
+                                "f32", None, wl.Hi, wl.Di, wl.max_ctx)
+    assert np.array_equal(np.isfinite(sc), np.isfinite(sc2))
+    fin = np.isfinite(sc)
+    assert np.allclose(sc[fin], sc2[fin], rtol=1e-12, atol=0)
+    for r in range(wl.n_q):
+        seq = wl.q_seq[r]
+        for s_ in range(0, int(wl.q_pos[r]) + 1, 7):
+            krow = kd[wl.block_table[seq, s_ // wl.page], s_ % wl.page]
+            ref = sum(float(wl.w[r, h]) * max(0.0, float(qd[r, h] @ krow)) for h in range(wl.Hi))
+            assert abs(sc[r, s_] - ref) <= 1e-12 * (abs(ref) + 1e-30)
+    # a scale taken from the wrong group (a plausible slip) changes the scores
+    bad = wl.k_scale[..., ::-1].copy()
+    sc_bad = oracle.indexer_scores(b, wl.q_idx, "mxe4m3", wl.w, wl.k_idx, "mxe4m3", bad,
+                                   wl.Hi, wl.Di, wl.max_ctx, q_scale=wl.q_scale)
+    assert not np.allclose(sc_bad[fin], sc[fin])
+
+
+def test_mx_bf16_query_is_converted_per_group_first():
+    """A bf16 query with MXFP8 keys is the MX query of the conversion rule."""
+    wl = _mx_workload(False)
+    assert wl.q_idx_dtype == "bf16"
+    b = oracle.Batch.of(wl)
+    sc = oracle.indexer_scores(b, wl.q_idx, "bf16", wl.w, wl.k_idx, "mxe4m3", wl.k_scale,
+                               wl.Hi, wl.Di, wl.max_ctx)
+    qc, qs = oracle.mx_quantize(wl.q_idx, "bf16")
+    sc2 = oracle.indexer_scores(b, qc, "mxe4m3", wl.w, wl.k_idx, "mxe4m3", wl.k_scale,
+                                wl.Hi, wl.Di, wl.max_ctx, q_scale=qs)
+    assert np.array_equal(sc, sc2)

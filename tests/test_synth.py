@@ -2,6 +2,7 @@
 import numpy as np
 import torch
 
+import oracle
 import synth
 
 
@@ -96,3 +97,27 @@ def test_nvfp4_blocks_bound_the_error():
     assert np.all(scale <= amax / 6 * (1 + 2.0 ** -4)) and np.all(scale >= amax / 6 * (1 - 2.0 ** -4))
     bound = np.repeat(scale, 16, axis=1) * 1.0 + np.abs(rows) * 2.0 ** -3
     assert np.all(np.abs(deq - rows) <= bound)
+
+
+def test_mx_keys_layout_and_encoder_agrees_with_the_oracle():
+    """MXFP8 keys: codes and E8M0 bytes per group of 32; unused slots hold NaN
+    codes and byte 255.  The generator's numpy encoder and the oracle's
+    conversion (separate code, written from the same rule) agree bit for bit,
+    negative values that round to zero included."""
+    wl = synth.make("c1", batch=3, ctx_list=[100, 64, 1], Hi=2, Di=128, Hq=2, Dqk=8, Dv=4, K=4,
+                    idx_mx=True)
+    assert wl.k_idx_dtype == "mxe4m3" and wl.k_scale.shape == wl.k_idx.shape[:2] + (4,)
+    used = np.zeros(wl.k_idx.shape[:2], dtype=bool)
+    for i, c in enumerate(wl.ctx_len):
+        for s in range(int(c)):
+            used[wl.block_table[i, s // wl.page], s % wl.page] = True
+    assert (wl.k_scale[~used] == 255).all() and (wl.k_idx[~used] == 0x7F).all()
+    assert (wl.k_scale[used] < 255).all()
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((64, 128)) * 2.0 ** rng.integers(-40, 40, (64, 1))).astype(np.float32)
+    x[0, :32] = 0
+    x[1, 3] = -1e-30
+    x[2, :32] = np.float32(-2.0 ** -130)
+    c1, s1 = synth.quantize_groups_mx(x)
+    c2, s2 = oracle.mx_quantize(x, "f32")
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2)
