@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define SI_VERSION 4
+#define SI_VERSION 5
 
 typedef enum si_status {
     SI_OK = 0,
@@ -64,10 +64,15 @@ typedef enum si_dtype {
     SI_F32 = 0,  /* IEEE float32 */
     SI_BF16 = 1, /* bfloat16 */
     SI_E4M3 = 2, /* OCP FP8 e4m3 (finite, max 448) */
-    SI_E2M1 = 3  /* OCP FP4 e2m1 (max 6), two per byte, even element in the low
+    SI_E2M1 = 3, /* OCP FP4 e2m1 (max 6), two per byte, even element in the low
                     nibble; attention caches only, with per-tile scales (the
                     NVFP4 KV format of the vLLM article on DeepSeek-V4.1 uses
                     blocks of 16 entries) */
+    SI_MXE4M3 = 4 /* MXFP8 (OCP Microscaling v1.0), section 5.1's indexer
+                     format: e4m3 codes in groups of 32 consecutive entries of
+                     a row, each group with one E8M0 scale byte e meaning
+                     2^(e - 127) (e = 255, NaN, is not allowed); entry =
+                     2^(e - 127) * code.  Indexer query and keys only. */
 } si_dtype;
 
 /* Device status flags (sticky, OR-ed into the workspace status word). */
@@ -115,12 +120,15 @@ typedef struct si_batch {
  * (row_stride even). */
 typedef struct si_paged {
     const void *data;    /* device; 16-byte aligned */
-    const float *scale;  /* device dequantisation scales (> 0), or NULL for 1:
+    const void *scale;   /* device dequantisation scales, or NULL for 1.
+                            float (> 0) for every dtype but SI_MXE4M3:
                             [n_blocks, page_size] when scale_tile == 0,
                             [n_blocks, page_size, ceil(row_stride / scale_tile)]
                             otherwise (entry d uses tile d / scale_tile; a
                             value cache that aliases the key rows shares their
-                            scales) */
+                            scales).  SI_MXE4M3: required, E8M0 bytes
+                            [n_blocks, page_size, row_stride / 32] with
+                            scale_tile = 32 and row_stride a multiple of 32. */
     si_dtype dtype;
     int32_t row_dim;     /* elements used per row */
     int64_t row_stride;  /* elements between consecutive rows, >= row_dim */
@@ -130,18 +138,30 @@ typedef struct si_paged {
 /* Indexer operands (section 2.2: lightweight multi-head indexer; section 5.1
  * stores its keys in FP8). */
 typedef struct si_indexer {
-    const void *q;       /* device [n_q, n_heads, head_dim], SI_F32, SI_BF16 or
-                            SI_E4M3 */
+    const void *q;       /* device [n_q, n_heads, head_dim], SI_F32, SI_BF16,
+                            SI_E4M3 or SI_MXE4M3 */
     si_dtype q_dtype;
-    const float *q_scale; /* device [n_q, n_heads] dequantisation scale (> 0) of
-                            an SI_E4M3 query, one per (row, head): the query is
-                            stored quantised per group as in section 4.3's
-                            prolog, a group being one head.  Required for
-                            SI_E4M3, ignored otherwise. */
+    const void *q_scale; /* SI_E4M3 query: device float [n_q, n_heads], one
+                            dequantisation scale (> 0) per (row, head) -- the
+                            query stored quantised per group as in section
+                            4.3's prolog, a group being one head.
+                            SI_MXE4M3 query: device E8M0 bytes [n_q, n_heads,
+                            head_dim / 32].  Required for those two dtypes,
+                            ignored otherwise. */
     const float *w;      /* device [n_q, n_heads] head weights */
     int32_t n_heads;     /* 1..128 */
     int32_t head_dim;    /* 1..256 */
-    si_paged k;          /* indexer keys: SI_F32, SI_BF16 or SI_E4M3 (+scale) */
+    si_paged k;          /* indexer keys: SI_F32, SI_BF16, SI_E4M3 (+ float
+                            scale per row) or SI_MXE4M3.  MXFP8 keys (section
+                            5.1) need head_dim a multiple of 32 and a query of
+                            SI_MXE4M3, SI_BF16 or SI_F32; a bf16 or f32 query
+                            is converted to MXFP8 on the device before scoring,
+                            exactly as si_quant_mxfp8 converts it, and the
+                            score is computed from the MXFP8 values:
+                              score(t,s) = sum_h w[t,h] *
+                                 ReLU(sum_d Xq[t,h,d/32] Pq[t,h,d] *
+                                            Xk[s,d/32] Pk[s,d]),
+                            fp32 accumulation of the exact group products. */
 } si_indexer;
 
 /* Sparse attention operands: one shared KV head (MQA / latent KV). */
@@ -282,6 +302,22 @@ si_status si_fused_decode_noalloc(const si_batch *b, const si_indexer *ix,
                                   const si_attention *at, int32_t k_top, int32_t *idx,
                                   void *out, si_dtype out_dtype, float *lse,
                                   const void **scratch, void *stream);
+
+/* MXFP8 conversion (section 4.3's prolog step q8 = quant_per_group(q), in
+ * section 5.1's format; the rule is the OCP MX specification's, the pages
+ * give none of their own).  Per group of 32 consecutive entries of a row:
+ *   E = floor(log2 max|x|) - 8, clamped to [-127, 127] (an all-zero group
+ *       takes -127); scale byte = E + 127;
+ *   code = e4m3(x / 2^E), round to nearest even, magnitudes above 448
+ *       clamped to 448, the sign kept (-0 for a negative value that rounds
+ *       to zero).
+ * x: device [n_rows, dim] of x_dtype (SI_F32 or SI_BF16), finite values;
+ *    a group holding an infinity or NaN gets scale byte 255 and NaN codes.
+ * codes: device uint8 [n_rows, dim]; scales: device uint8 [n_rows, dim / 32].
+ * dim: a multiple of 32, 32..65536.  x, codes and scales 16-byte aligned.
+ * Needs no workspace; raises no device flag. */
+si_status si_quant_mxfp8(const void *x, si_dtype x_dtype, int64_t n_rows, int32_t dim,
+                         uint8_t *codes, uint8_t *scales, void *stream);
 
 /* Synchronises `stream`, then reads the sticky device status word of `ws`
  * into *flags (SI_DEVFLAG_*).  Returns SI_ERR_DEVICE if any flag is set. */

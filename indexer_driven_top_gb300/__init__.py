@@ -23,8 +23,8 @@ from . import _build
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = _build.LIB
 
-F32, BF16, E4M3, E2M1 = 0, 1, 2, 3
-DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1}
+F32, BF16, E4M3, E2M1, MXE4M3 = 0, 1, 2, 3, 4
+DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1, "mxe4m3": MXE4M3}
 OP_INDEXER, OP_TOPK, OP_ATTN, OP_FUSED = 0, 1, 2, 3
 DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_INDEX, DEVFLAG_TIMEOUT, DEVFLAG_RANGE = 1, 2, 4, 8
 
@@ -91,6 +91,7 @@ def load() -> ctypes.CDLL:
         "si_last_error": (ctypes.c_char_p, []),
         "si_version": (I32, []),
         "si_launch_count": (ctypes.c_uint64, []),
+        "si_quant_mxfp8": (ctypes.c_int, [P, ctypes.c_int, I64, I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -106,7 +107,7 @@ EXPORTED = ("si_workspace_size", "si_workspace_min", "si_indexer_scores", "si_to
             "si_sparse_attn", "si_fused_decode", "si_fused_decode_noalloc",
             "si_workspace_size_cand", "si_indexer_topk_cand", "si_workspace_status",
             "si_status_string",
-            "si_last_error", "si_version", "si_launch_count")
+            "si_last_error", "si_version", "si_launch_count", "si_quant_mxfp8")
 
 
 def _check(status: int):
@@ -161,15 +162,17 @@ class Paged:
     """Paged cache [n_blocks, page_size, row_stride] with optional scales: one
     per row, or one per `scale_tile` consecutive entries of a row."""
     data: torch.Tensor
-    dtype: str                  # "f32" | "bf16" | "e4m3" | "e2m1" (two per byte)
+    dtype: str                  # "f32" | "bf16" | "e4m3" | "e2m1" (two per byte) | "mxe4m3"
     row_dim: int
     scale: Optional[torch.Tensor] = None
     scale_tile: int = 0
 
     def c(self) -> c_paged:
         stride = self.data.shape[-1] * (2 if self.dtype == "e2m1" else 1)  # in elements
+        # MXFP8 rows take one E8M0 byte per 32 entries
+        tile = 32 if self.dtype == "mxe4m3" else self.scale_tile
         return c_paged(_ptr(self.data), _ptr(self.scale), DTYPES[self.dtype], self.row_dim,
-                       stride, self.scale_tile)
+                       stride, tile)
 
 
 @dataclasses.dataclass
@@ -178,7 +181,8 @@ class Indexer:
     q_dtype: str
     w: torch.Tensor             # [n_q, n_heads] float32
     k: Paged
-    q_scale: Optional[torch.Tensor] = None   # [n_q, n_heads] float32 for an e4m3 query
+    q_scale: Optional[torch.Tensor] = None   # [n_q, n_heads] float32 for an e4m3 query,
+                                             # [n_q, n_heads, head_dim / 32] uint8 for mxe4m3
 
     def c(self) -> c_indexer:
         return c_indexer(_ptr(self.q), DTYPES[self.q_dtype], _ptr(self.q_scale), _ptr(self.w),
@@ -290,6 +294,23 @@ def fused_decode_noalloc(b: Batch, ix: Indexer, at: Attention, k_top: int, idx: 
                                           k_top, _ptr(idx), _ptr(out), _out_dtype(out),
                                           _ptr(lse), ctypes.byref(scratch), _stream(stream)))
     return int(scratch.value or 0)
+
+
+def quant_mxfp8(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, stream=None):
+    """MXFP8 conversion of the rows of x ([..., dim], float32 or bfloat16, dim
+    a multiple of 32) into codes (uint8, x's shape) and E8M0 scale bytes
+    (uint8 [..., dim / 32]): si_quant_mxfp8."""
+    dt = {torch.float32: F32, torch.bfloat16: BF16}.get(x.dtype)
+    if dt is None:
+        raise ValueError("x must be float32 or bfloat16")
+    dim = x.shape[-1]
+    n = x.numel() // dim if dim else 0
+    if codes.dtype != torch.uint8 or scales.dtype != torch.uint8:
+        raise ValueError("codes and scales are uint8")
+    if codes.numel() != x.numel() or scales.numel() * 32 != x.numel():
+        raise ValueError("codes / scales do not match x")
+    _check(load().si_quant_mxfp8(_ptr(x), dt, n, dim, _ptr(codes), _ptr(scales),
+                                 _stream(stream)))
 
 
 def workspace_status_at(addr: int, stream=None) -> int:

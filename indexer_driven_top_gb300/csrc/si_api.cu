@@ -88,8 +88,13 @@ si_status check_paged(const si_paged &p, const char *name, int need_dim)
         return fail(SI_ERR_INVALID_ARG, "%s.data is NULL", name);
     if (!aligned(p.data, 16))
         return fail(SI_ERR_INVALID_ARG, "%s.data is not 16-byte aligned", name);
-    if (p.dtype != SI_F32 && p.dtype != SI_BF16 && p.dtype != SI_E4M3 && p.dtype != SI_E2M1)
+    if (p.dtype != SI_F32 && p.dtype != SI_BF16 && p.dtype != SI_E4M3 && p.dtype != SI_E2M1 &&
+        p.dtype != SI_MXE4M3)
         return fail(SI_ERR_INVALID_ARG, "%s.dtype %d unknown", name, (int)p.dtype);
+    if (p.dtype == SI_MXE4M3 && (p.scale_tile != 32 || !p.scale || p.row_stride % 32 != 0))
+        return fail(SI_ERR_INVALID_ARG,
+                    "%s: MXFP8 rows need E8M0 scales with scale_tile 32 and a row_stride "
+                    "that is a multiple of 32", name);
     if (p.dtype == SI_E2M1 && (p.scale_tile < 1 || !p.scale || p.row_stride % 2 != 0))
         return fail(SI_ERR_INVALID_ARG,
                     "%s: e2m1 rows need per-tile scales and an even row_stride", name);
@@ -109,18 +114,31 @@ si_status check_indexer(const si_indexer *ix)
         return fail(SI_ERR_INVALID_ARG, "indexer operands are NULL");
     if (!ix->q || !ix->w)
         return fail(SI_ERR_INVALID_ARG, "indexer q or w is NULL");
-    if (ix->q_dtype != SI_F32 && ix->q_dtype != SI_BF16 && ix->q_dtype != SI_E4M3)
-        return fail(SI_ERR_INVALID_ARG, "indexer q dtype must be f32, bf16 or e4m3");
-    if (ix->q_dtype == SI_E4M3 && !ix->q_scale)
-        return fail(SI_ERR_INVALID_ARG, "an e4m3 indexer q needs q_scale");
+    if (ix->q_dtype != SI_F32 && ix->q_dtype != SI_BF16 && ix->q_dtype != SI_E4M3 &&
+        ix->q_dtype != SI_MXE4M3)
+        return fail(SI_ERR_INVALID_ARG, "indexer q dtype must be f32, bf16, e4m3 or mxe4m3");
+    if ((ix->q_dtype == SI_E4M3 || ix->q_dtype == SI_MXE4M3) && !ix->q_scale)
+        return fail(SI_ERR_INVALID_ARG, "an e4m3 or mxe4m3 indexer q needs q_scale");
     if (ix->n_heads < 1 || ix->n_heads > 128)
         return fail(SI_ERR_INVALID_ARG, "indexer n_heads %d outside 1..128", ix->n_heads);
     if (ix->head_dim < 1 || ix->head_dim > 256)
         return fail(SI_ERR_INVALID_ARG, "indexer head_dim %d outside 1..256", ix->head_dim);
-    if (ix->k.scale_tile != 0)
-        return fail(SI_ERR_UNSUPPORTED, "indexer keys take one scale per row (scale_tile 0)");
     if (ix->k.dtype == SI_E2M1)
-        return fail(SI_ERR_UNSUPPORTED, "indexer keys are f32, bf16 or e4m3");
+        return fail(SI_ERR_UNSUPPORTED, "indexer keys are f32, bf16, e4m3 or mxe4m3");
+    if (ix->k.dtype == SI_MXE4M3) {
+        // section 5.1: query and keys both in MXFP8 (a bf16 / f32 query is
+        // converted on the device)
+        if (ix->head_dim % 32 != 0)
+            return fail(SI_ERR_INVALID_ARG, "MXFP8 keys need head_dim a multiple of 32");
+        if (ix->q_dtype == SI_E4M3)
+            return fail(SI_ERR_UNSUPPORTED,
+                        "MXFP8 keys take an mxe4m3, bf16 or f32 query, not e4m3");
+    } else {
+        if (ix->q_dtype == SI_MXE4M3)
+            return fail(SI_ERR_UNSUPPORTED, "an mxe4m3 query needs mxe4m3 keys");
+        if (ix->k.scale_tile != 0)
+            return fail(SI_ERR_UNSUPPORTED, "indexer keys take one scale per row (scale_tile 0)");
+    }
     return check_paged(ix->k, "indexer k", ix->head_dim);
 }
 
@@ -194,8 +212,10 @@ si_indexer indexer_slice(const si_indexer &ix, int32_t r0)
     s.q = static_cast<const char *>(ix.q) +
           (size_t)r0 * ix.n_heads * ix.head_dim * dtype_bytes(ix.q_dtype);
     s.w = ix.w + (size_t)r0 * ix.n_heads;
-    if (ix.q_scale)
-        s.q_scale = ix.q_scale + (size_t)r0 * ix.n_heads;
+    if (ix.q_scale && ix.q_dtype == SI_MXE4M3)
+        s.q_scale = si::mxscale(ix.q_scale) + (size_t)r0 * ix.n_heads * (ix.head_dim / 32);
+    else if (ix.q_scale)
+        s.q_scale = si::fscale(ix.q_scale) + (size_t)r0 * ix.n_heads;
     return s;
 }
 
@@ -378,7 +398,8 @@ extern "C" {
 
 size_t si_workspace_size_cand(const si_batch *b, const si_indexer *ix, int32_t n_cand)
 {
-    if (check_batch(b) != SI_OK || check_indexer(ix) != SI_OK || n_cand < 1 || n_cand > kMaxCand)
+    if (check_batch(b) != SI_OK || check_indexer(ix) != SI_OK || n_cand < 1 || n_cand > kMaxCand ||
+        ix->k.dtype == SI_MXE4M3)
         return 0;
     return cand_layout(*b, *ix, n_cand, nullptr).total;
 }
@@ -393,6 +414,9 @@ si_status si_indexer_topk_cand(const si_batch *b, const si_indexer *ix, const in
         return st;
     if ((st = check_indexer(ix)) != SI_OK || (st = check_k(k_top)) != SI_OK)
         return st;
+    if (ix->k.dtype == SI_MXE4M3)
+        return fail(SI_ERR_UNSUPPORTED,
+                    "candidate-restricted selection takes f32, bf16 or e4m3 keys");
     if (!cand || !idx)
         return fail(SI_ERR_INVALID_ARG, "cand or idx is NULL");
     if (n_cand < 1 || n_cand > kMaxCand)

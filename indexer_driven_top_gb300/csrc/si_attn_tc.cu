@@ -587,8 +587,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                                             r >= 0 ? 16u : 0u);
                             else if (part == 2)
                                 cp_async_16(sc0 + kTile * 32 + key * 16,
-                                            r >= 0 ? at.k.scale + (int64_t)r * kKvBlocks4 + 4 * c
-                                                   : at.k.scale,
+                                            r >= 0 ? fscale(at.k.scale) + (int64_t)r * kKvBlocks4 + 4 * c
+                                                   : fscale(at.k.scale),
                                             r >= 0 ? 16u : 0u);
                         }
                     } else {
@@ -681,7 +681,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
             // value CTA, FP8 cache: unit u of group j's 128 codes per key into
             // a staging slot; lane u == 0 also copies its keys' scales of tile j
             loader_init(ls, b, idx_s, 0, k_top, T, n_valid, seq, pos, kr0);
-            const float *kscale = at.k.scale;
+            const float *kscale = fscale(at.k.scale);
             const int n_groups = kVGroups * T;
             for (int g = 0; g < n_groups; g++) {
                 const int slot = g % kVStg8, tile = g / kVGroups, j = g % kVGroups;
@@ -1055,7 +1055,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
 #pragma unroll
                         for (int q5 = 0; q5 < kKvTiles; q5++)
                             scl[(rs * kKvTiles + q5) * kTile + 32 * i + lane] =
-                                prow >= 0 ? __ldg(at.k.scale + (int64_t)prow * kKvTiles + q5) : 0.f;
+                                prow >= 0 ? __ldg(fscale(at.k.scale) + (int64_t)prow * kKvTiles + q5) : 0.f;
                     }
                     const uint32_t w = __ballot_sync(0xffffffffu, ok);
                     if (lane == i)

@@ -147,7 +147,7 @@ cudaError_t launch_cand_gather(const si_batch &b, const int32_t *cand, int64_t l
     const int grid = grid_for((int64_t)b.n_q * v.n_pad, 256);
     count_launch();
     k_cand_gather<<<grid, 256, 0, s>>>(b, cand, ld_cand, n_cand, v,
-                                       static_cast<const uint8_t *>(k.data), k.scale, keys,
+                                       static_cast<const uint8_t *>(k.data), fscale(k.scale), keys,
                                        scales, st);
     return cudaGetLastError();
 }

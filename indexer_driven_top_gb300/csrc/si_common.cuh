@@ -55,6 +55,61 @@ __device__ __forceinline__ int64_t page_row(const si_batch &b, int seq, int64_t 
     return (int64_t)blk * b.page_size + s % b.page_size;
 }
 
+// Float scales of a cache or query (every dtype but SI_MXE4M3).
+__host__ __device__ __forceinline__ const float *fscale(const void *p)
+{
+    return static_cast<const float *>(p);
+}
+
+// E8M0 scale bytes of an MXFP8 buffer.
+__host__ __device__ __forceinline__ const uint8_t *mxscale(const void *p)
+{
+    return static_cast<const uint8_t *>(p);
+}
+
+// ------------------------------------------------------------------ MXFP8
+// Section 5.1's indexer format, OCP Microscaling: groups of 32 entries, e4m3
+// codes, one E8M0 scale byte e = 2^(e - 127) per group.  Conversion rule (the
+// MX specification's): E = floor(log2 max|x|) - 8 clamped to [-127, 127],
+// code = e4m3(x / 2^E) with round-to-nearest-even and saturation at 448.
+//
+// |x| as bits: for non-negative floats the bit patterns order like the
+// values, and NaN patterns sort above infinity, so the unsigned maximum of
+// these over a group is the bits of max|x| (or marks a non-finite group).
+__device__ __forceinline__ uint32_t abs_bits(float x) { return __float_as_uint(x) & 0x7FFFFFFFu; }
+
+// Scale byte E + 127 of a group from the bits of its max|x|: for a normal
+// max, floor(log2) + 127 is the exponent field be, so the byte is be - 8,
+// and 0 (E = -127) when that is below zero (subnormal or zero max).  A group
+// holding an infinity or NaN gets 255.
+__device__ __forceinline__ uint32_t mx_scale_byte(uint32_t amax_bits)
+{
+    const uint32_t be = amax_bits >> 23;
+    return be == 255u ? 255u : (be > 8u ? be - 8u : 0u);
+}
+
+// 2^-E = 2^(127 - b) for a scale byte b <= 246 (every finite float group):
+// the exponent field 254 - b lies in [8, 254], a normal float.
+__device__ __forceinline__ float mx_inv_scale(uint32_t b) { return __uint_as_float((254u - b) << 23); }
+
+// 2^(b - 127) for a scale byte b < 255 (b = 0 is the subnormal 2^-127).
+__device__ __forceinline__ float mx_scale(uint32_t b)
+{
+    return b > 0 ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
+
+// Codes of x0 (low byte) and x1 (high byte) in a group with scale byte b:
+// the multiply by a power of two is exact, the conversion rounds to nearest
+// even and saturates; a non-finite group gets NaN codes.
+__device__ __forceinline__ uint32_t mx_codes2(float x0, float x1, uint32_t b)
+{
+    if (b == 255u)
+        return 0x7F7Fu;
+    const float m = mx_inv_scale(b);
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x0 * m, x1 * m), __NV_SATFINITE,
+                                              __NV_E4M3);
+}
+
 // OCP FP4 e2m1 code (low 4 bits): sign, 2 exponent bits with bias 1, 1
 // mantissa bit; exponent field 0 is subnormal (0 or 0.5).
 __device__ __forceinline__ float e2m1_to_float(unsigned c)
@@ -89,12 +144,14 @@ __device__ __forceinline__ float load_elem(const void *p, si_dtype t, int64_t i)
 __device__ __forceinline__ float load_paged(const si_paged &p, int64_t row, int d)
 {
     float x = load_elem(p.data, p.dtype, row * p.row_stride + d);
-    if (p.scale) {
+    if (p.dtype == SI_MXE4M3) {
+        x *= mx_scale(__ldg(mxscale(p.scale) + row * (p.row_stride / 32) + d / 32));
+    } else if (p.scale) {
         if (p.scale_tile > 0) {
             const int64_t nt = (p.row_stride + p.scale_tile - 1) / p.scale_tile;
-            x *= p.scale[row * nt + d / p.scale_tile];
+            x *= fscale(p.scale)[row * nt + d / p.scale_tile];
         } else {
-            x *= p.scale[row];
+            x *= fscale(p.scale)[row];
         }
     }
     return x;

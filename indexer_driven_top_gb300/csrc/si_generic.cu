@@ -21,6 +21,9 @@ constexpr int kIdxKeys = 64;  // keys per block of the generic indexer
 
 // One block scores 64 consecutive key positions of one query row.
 // Shared memory: q [H*D] | w [H] | keys transposed [D][64].
+// MXFP8 keys (section 5.1): entries are code * 2^(e - 127) with the group's
+// scale byte e; a bf16 / f32 query is first converted to MXFP8 per group of
+// 32 (one warp per group), so both operands hold MXFP8 values.
 __global__ void __launch_bounds__(kIdxKeys)
 k_indexer_generic(si_batch b, si_indexer ix, float *scores, int64_t ld, unsigned int *st)
 {
@@ -39,9 +42,26 @@ k_indexer_generic(si_batch b, si_indexer ix, float *scores, int64_t ld, unsigned
     const int pos = b.q_pos[r];
     const int seq = b.q_seq[r];
 
-    for (int i = tid; i < H * D; i += kIdxKeys)
-        q_s[i] = load_elem(ix.q, ix.q_dtype, (int64_t)r * H * D + i) *
-                 (ix.q_dtype == SI_E4M3 ? ix.q_scale[(int64_t)r * H + i / D] : 1.f);
+    const bool mx = ix.k.dtype == SI_MXE4M3;
+    for (int i = tid; i < H * D; i += kIdxKeys) {
+        float x = load_elem(ix.q, ix.q_dtype, (int64_t)r * H * D + i);
+        if (ix.q_dtype == SI_E4M3)
+            x *= fscale(ix.q_scale)[(int64_t)r * H + i / D];
+        else if (ix.q_dtype == SI_MXE4M3)  // D % 32 == 0: group (h, d / 32) is i / 32
+            x *= mx_scale(__ldg(mxscale(ix.q_scale) + (int64_t)r * (H * D / 32) + i / 32));
+        q_s[i] = x;
+    }
+    if (mx && ix.q_dtype != SI_MXE4M3) {
+        __syncthreads();
+        const int lane = tid & 31;
+        for (int g = tid >> 5; g < H * D / 32; g += kIdxKeys / 32) {
+            const float x = q_s[g * 32 + lane];
+            const uint32_t b = mx_scale_byte(__reduce_max_sync(0xffffffffu, abs_bits(x)));
+            __nv_fp8_e4m3 c;
+            c.__x = (__nv_fp8_storage_t)(mx_codes2(x, 0.f, b) & 0xFFu);
+            q_s[g * 32 + lane] = b == 255u ? __uint_as_float(0x7FC00000u) : float(c) * mx_scale(b);
+        }
+    }
     for (int i = tid; i < H; i += kIdxKeys)
         w_s[i] = ix.w[(int64_t)r * H + i];
     const int64_t s = s0 + tid;
@@ -50,8 +70,10 @@ k_indexer_generic(si_batch b, si_indexer ix, float *scores, int64_t ld, unsigned
     for (int i = tid; i < kIdxKeys * D; i += kIdxKeys) {
         const int j = i / D, d = i % D;
         const int64_t row = rows[j];
-        k_s[d * kIdxKeys + j] =
-            row >= 0 ? load_elem(ix.k.data, ix.k.dtype, row * ix.k.row_stride + d) : 0.f;
+        float x = row >= 0 ? load_elem(ix.k.data, ix.k.dtype, row * ix.k.row_stride + d) : 0.f;
+        if (mx && row >= 0)
+            x *= mx_scale(__ldg(mxscale(ix.k.scale) + row * (ix.k.row_stride / 32) + d / 32));
+        k_s[d * kIdxKeys + j] = x;
     }
     __syncthreads();
     if (s >= ld)
@@ -66,7 +88,7 @@ k_indexer_generic(si_batch b, si_indexer ix, float *scores, int64_t ld, unsigned
                 dot = fmaf(q_s[h * D + d], k_s[d * kIdxKeys + tid], dot);
             acc = fmaf(w_s[h], fmaxf(dot, 0.f), acc);  // head weight x ReLU
         }
-        const float sc = ix.k.scale ? ix.k.scale[row] : 1.f;
+        const float sc = (ix.k.scale && !mx) ? fscale(ix.k.scale)[row] : 1.f;
         out = acc * sc + 0.0f;
     }
     scores[(int64_t)r * ld + s] = out;

@@ -19,6 +19,13 @@
 //     indexer query before scoring): four rows per block, 64 heads each, the
 //     scale folded into the head weight: 4 x 64 B rows, twice the scores per
 //     UMMA and per TMEM column read.
+//   * MXFP8 query and keys (section 5.1; a bf16 query is converted per group
+//     of 32 by the q-prep threads, bit-identical to si_quant_mxfp8): the
+//     block-scaled kind::mxf8f6f4 UMMA applies each group's scales inside the
+//     tensor core.  Its scale factors take TMEM columns, so the accumulators
+//     are 192 wide (three rows of 64 heads per block) instead of 256; the
+//     keys' scale words land per stage in the 32 x 16-byte block tcgen05.cp
+//     copies to TMEM (row L: keys L, L+32, L+64, L+96), the rows' per block.
 // The causal triangle is balanced by dealing row blocks to CTAs in head/tail
 // pairs (block b together with block nb-1-b, the pairing section 6.3 uses for
 // context-parallel shards): every pair holds the same number of causal
@@ -59,12 +66,16 @@ using namespace sm100;
 constexpr int kKeys = 128;            // keys per tile = UMMA M
 constexpr int kHeads = 64;            // indexer heads
 constexpr int kDim = 128;             // head dim = bytes per e4m3 key row = UMMA K
-constexpr int kN = 256;               // UMMA N: B rows of one block's query rows
+constexpr int kN = 256;               // UMMA N (bf16 and FP8 query): B rows of one block
 constexpr int kMaxRows = 4;           // query rows per block, FP8 query
+// Query modes: a bf16 query split into q_hi / q_lo terms, an FP8 query with a
+// per-(row, head) scale, an MXFP8 query (block-scaled MMA).
+constexpr int kQBf16 = 0, kQFp8 = 1, kQMx = 2;
 // B rows per query row: a bf16 query takes 64 q_hi heads then 64 q_lo heads,
-// an FP8 query its 64 heads as stored.
-template <bool Q8> constexpr int row_n() { return Q8 ? kHeads : 2 * kHeads; }
-template <bool Q8> constexpr int rows_per_block() { return kN / row_n<Q8>(); }
+// an FP8 or MXFP8 query its 64 heads.
+template <int QM> constexpr int row_n() { return QM == kQBf16 ? 2 * kHeads : kHeads; }
+template <int QM> constexpr int mma_n() { return QM == kQMx ? 3 * kHeads : kN; }
+template <int QM> constexpr int rows_per_block() { return mma_n<QM>() / row_n<QM>(); }
 constexpr int kStages = 8;            // key-tile ring depth
 constexpr int kScStages = 4;          // scale ring depth per epilogue group
 constexpr int kThreads = 16 * 32;
@@ -78,9 +89,20 @@ constexpr uint32_t kOffQ = kOffStage + kStages * kTile;               // [2] B o
 constexpr uint32_t kOffW = kOffQ + 2 * kTileB;                         // [2][rows][64] w * s_h
 constexpr uint32_t kOffWin = kOffW + 2 * kMaxRows * kHeads * 4;        // 2 x 32 block-table entries
 constexpr uint32_t kOffSc = kOffWin + 2 * 32 * 4;                      // [2][kScStages][128]
-constexpr uint32_t kOffBar = kOffSc + 2 * kScStages * kKeys * 4;
+// MXFP8 scale words for tcgen05.cp (32 rows x 16 bytes per block): one block
+// per key stage, two per B buffer (B rows 0..127 and 128..255)
+constexpr uint32_t kSfBytes = 512;
+constexpr uint32_t kOffSfa = kOffSc + 2 * kScStages * kKeys * 4;       // [kStages]
+constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfBytes;             // [2][2]
+constexpr uint32_t kOffBar = kOffSfb + 4 * kSfBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;                  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// TMEM: two accumulators of mma_n columns; MXFP8 adds 4 scale columns per
+// accumulator (keys) and 8 per B buffer (query rows) after them.
+constexpr uint32_t kTmemCols = 2 * kN;  // 512
+constexpr uint32_t kColSfa = 2 * 3 * kHeads;
+constexpr uint32_t kColSfb = kColSfa + 2 * 4;
+static_assert(kColSfb + 2 * 8 <= kTmemCols, "TMEM columns");
 
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v)
 {
@@ -134,13 +156,16 @@ __device__ __forceinline__ void block_shape(const si_batch &b, int blk, int tile
     T = min(tiles_ld, (pmax + kKeys) / kKeys);
 }
 
-template <bool Q8>
+template <int QM>
 __global__ void __launch_bounds__(kThreads, 1)
 k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix,
                   float *scores, int64_t ld, int n_blocks_rows, unsigned int *st)
 {
-    constexpr int kRows = rows_per_block<Q8>();
-    constexpr int kRowN = row_n<Q8>();
+    constexpr bool Q8 = QM != kQBf16;  // B rows are the 64 heads of each row, no split
+    constexpr bool MX = QM == kQMx;
+    constexpr int kRows = rows_per_block<QM>();
+    constexpr int kRowN = row_n<QM>();
+    constexpr int nB = mma_n<QM>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
@@ -164,7 +189,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
 
     if (tid == 0) {
         for (int i = 0; i < kStages; i++) {
-            mbar_init(full_bar + i, 1);   // producer's expect_tx arrival
+            // producer's expect_tx arrival (MXFP8: and its 32 lanes' cp.async arrivals)
+            mbar_init(full_bar + i, MX ? 33 : 1);
             mbar_init(empty_bar + i, 1);  // MMA commit
         }
         for (int i = 0; i < 2; i++) {
@@ -180,7 +206,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
-        tmem_alloc(tmem_slot, 2 * kN);
+        tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -251,6 +277,26 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                 if (copy)
                     tma_load_2d(base + kOffStage + stg * kTile + k_lo * kDim, &tmap, 0, row,
                                 full_bar + stg);
+                if constexpr (MX) {
+                    // the keys' E8M0 words into the stage's tcgen05.cp block, row
+                    // `lane` = keys lane + 32 i; a key after the block's last
+                    // position or on an invalid page keeps a stale word (its
+                    // score is -inf)
+                    const uint32_t sfa = base + kOffSfa + stg * kSfBytes + lane * 16;
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int sk = s0 + lane + 32 * i;
+                        if (sk <= pmax) {
+                            const int lbk = sk >> lp;
+                            const int blkk = win_s[lbk - win];
+                            if (lbk < b.max_blocks && (unsigned)blkk < (unsigned)b.n_blocks)
+                                cp_async_4(sfa + 4 * i, mxscale(ix.k.scale) +
+                                                            (((int64_t)blkk << lp) + (sk & (P - 1))) *
+                                                                (kDim / 32));
+                        }
+                    }
+                    cp_async_arrive_noinc(full_bar + stg);
+                }
                 // scales of the tile's keys into the ring of epilogue group pw
                 const int g = pw;
                 const int64_t kit = it >> 1;
@@ -270,8 +316,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                         blk4 = v;
                 }
                 const uint32_t d = smem_u32(sc_s + (g * kScStages + ss) * kKeys + 4 * lane);
-                if (blk4 >= 0 && ix.k.scale) {
-                    cp_async_16(d, ix.k.scale + ((int64_t)blk4 << lp) + (s4 & (P - 1)));
+                if (blk4 >= 0 && ix.k.scale && !MX) {
+                    cp_async_16(d, fscale(ix.k.scale) + ((int64_t)blk4 << lp) + (s4 & (P - 1)));
                     cp_async_arrive_noinc(sf);
                 } else {
                     const uint32_t v = __float_as_uint(blk4 >= 0 ? 1.f : -1.f);
@@ -284,7 +330,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
         cp_async_wait<0>();  // nothing may land after the block has moved on
     } else if (warp == kWarpMma) {
         // ----------------------------------------------------------------- MMA
-        const uint32_t idesc = idesc_e4m3(kKeys, kN);
+        const uint32_t idesc = idesc_e4m3(kKeys, nB);
         BlockWalk walk(n_blocks_rows, G);
         int64_t it = 0;
         int bi = 0;
@@ -295,6 +341,18 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
             const int p = bi & 1;
             if (!mbar_wait(qfull_bar + p, (uint32_t)(bi >> 1) & 1, st))
                 break;
+            if constexpr (MX) {
+                // the block's query scales into TMEM (B rows 0..127, 128..255);
+                // the MMAs that read this buffer's columns last (block bi - 2)
+                // are done: the q-prep waited for their commit before writing
+                fence_async_smem();
+                if (lane == 0) {
+                    tmem_cp_32x128b_x4(tmem + kColSfb + p * 8, base + kOffSfb + (2 * p) * kSfBytes);
+                    tmem_cp_32x128b_x4(tmem + kColSfb + p * 8 + 4,
+                                       base + kOffSfb + (2 * p + 1) * kSfBytes);
+                }
+                __syncwarp();
+            }
             for (int t = 0; t < T; t++, it++) {
                 const int stg = (int)(it % kStages);
                 const int g = (int)(it & 1);
@@ -305,15 +363,31 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                     break;
                 }
                 tc_fence_after();
+                if constexpr (MX)
+                    fence_async_smem();  // the scale words landed by cp.async (generic proxy)
                 if (lane == 0) {
-                    const uint32_t dacc = tmem + g * kN;
+                    const uint32_t dacc = tmem + g * nB;
+                    if constexpr (MX) {
+                        const uint32_t sfa = tmem + kColSfa + g * 4, sfb = tmem + kColSfb + p * 8;
+                        tmem_cp_32x128b_x4(sfa, base + kOffSfa + stg * kSfBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kDim / 32; kk++) {
-                        const uint64_t ad = smem_desc(base + kOffStage + stg * kTile + kk * 32, 16,
-                                                      1024, kSwizzle128B);
-                        const uint64_t bd =
-                            smem_desc(base + kOffQ + p * kTileB + kk * 32, 16, 1024, kSwizzle128B);
-                        umma_f8_ss(dacc, ad, bd, idesc, kk > 0);
+                        for (int kk = 0; kk < kDim / 32; kk++) {
+                            const uint64_t ad = smem_desc(base + kOffStage + stg * kTile + kk * 32,
+                                                          16, 1024, kSwizzle128B);
+                            const uint64_t bd = smem_desc(base + kOffQ + p * kTileB + kk * 32, 16,
+                                                          1024, kSwizzle128B);
+                            umma_mx_ss(dacc, ad, bd, idesc_mx_e4m3(kKeys, nB, kk), sfa, sfb,
+                                       kk > 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kDim / 32; kk++) {
+                            const uint64_t ad = smem_desc(base + kOffStage + stg * kTile + kk * 32,
+                                                          16, 1024, kSwizzle128B);
+                            const uint64_t bd = smem_desc(base + kOffQ + p * kTileB + kk * 32, 16,
+                                                          1024, kSwizzle128B);
+                            umma_f8_ss(dacc, ad, bd, idesc, kk > 0);
+                        }
                     }
                     umma_commit(empty_bar + stg);
                     umma_commit(cfull_bar + g);
@@ -338,7 +412,81 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
             if (bi >= 2 && !mbar_wait(qempty_bar + p, (uint32_t)((bi - 2) >> 1) & 1, st))
                 break;
             const uint32_t qb = base + kOffQ + p * kTileB;
-            if constexpr (Q8) {
+            if constexpr (MX) {
+                // dims [64 half, +64) of head h of each row = MX groups 2 half,
+                // 2 half + 1; B row n = j * 64 + h
+                for (int j = 0; j < kRows; j++) {
+                    const bool have = j < nrows;
+                    const int64_t rh = (int64_t)(r0 + j) * kHeads + h;
+                    const uint32_t n = (uint32_t)(j * kRowN + h);
+                    uint32_t sbytes = 0;  // group 2 half in the low byte
+                    if (ix.q_dtype == SI_MXE4M3) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(
+                            static_cast<const uint8_t *>(ix.q) + rh * kDim + half * 64);
+#pragma unroll
+                        for (int c = 0; c < 4; c++) {
+                            const uint4 v = have ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                            st_shared_v4(qb + sw128_offset(n, (uint32_t)(half * 4 + c)), v.x, v.y,
+                                         v.z, v.w);
+                        }
+                        if (have) {
+                            const uint8_t *qs = mxscale(ix.q_scale) + rh * (kDim / 32) + 2 * half;
+                            sbytes = (uint32_t)__ldg(qs) | ((uint32_t)__ldg(qs + 1) << 8);
+                        }
+                    } else {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(
+                            static_cast<const uint16_t *>(ix.q) + rh * kDim + half * 64);
+#pragma unroll
+                        for (int gg = 0; gg < 2; gg++) {  // one MX group = 32 dims = 4 loads
+                            uint32_t q2[16];
+#pragma unroll
+                            for (int i = 0; i < 4; i++) {
+                                const uint4 v =
+                                    have ? __ldg(src + 4 * gg + i) : make_uint4(0u, 0u, 0u, 0u);
+                                q2[4 * i] = v.x;
+                                q2[4 * i + 1] = v.y;
+                                q2[4 * i + 2] = v.z;
+                                q2[4 * i + 3] = v.w;
+                            }
+                            uint32_t mb = 0;
+#pragma unroll
+                            for (int i = 0; i < 16; i++)
+                                mb = max(mb, max(abs_bits(__uint_as_float(q2[i] << 16)),
+                                                 abs_bits(__uint_as_float(q2[i] & 0xFFFF0000u))));
+                            const uint32_t sb = mx_scale_byte(mb);
+                            sbytes |= sb << (8 * gg);
+#pragma unroll
+                            for (int c = 0; c < 2; c++) {  // 16 dims per 16-byte unit
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int jj = 0; jj < 4; jj++) {
+                                    const uint32_t a = q2[8 * c + 2 * jj],
+                                                   bb = q2[8 * c + 2 * jj + 1];
+                                    w4[jj] = mx_codes2(__uint_as_float(a << 16),
+                                                       __uint_as_float(a & 0xFFFF0000u), sb) |
+                                             (mx_codes2(__uint_as_float(bb << 16),
+                                                        __uint_as_float(bb & 0xFFFF0000u), sb)
+                                              << 16);
+                                }
+                                st_shared_v4(qb + sw128_offset(n, (uint32_t)(half * 4 + 2 * gg + c)),
+                                             w4[0], w4[1], w4[2], w4[3]);
+                            }
+                        }
+                    }
+                    // B row n's scale word (byte g = group g) for tcgen05.cp:
+                    // block n / 128, row n % 32, word (n / 32) % 4
+                    const uint32_t other = __shfl_xor_sync(0xffffffffu, sbytes, 1);
+                    if (half == 0) {
+                        const uint32_t word = sbytes | (other << 16);
+                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(
+                                         base + kOffSfb + (2 * p + (n >> 7)) * kSfBytes +
+                                         (n & 31) * 16 + ((n >> 5) & 3) * 4),
+                                     "r"(word)
+                                     : "memory");
+                        w_s[(p * kRows + j) * kHeads + h] = have ? __ldg(ix.w + rh) : 0.f;
+                    }
+                }
+            } else if constexpr (Q8) {
                 // stored FP8 query: codes as they are, the scale joins the weight
                 for (int j = 0; j < kRows; j++) {
                     const bool have = j < nrows;
@@ -353,7 +501,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                     }
                     if (half == 0)
                         w_s[(p * kRows + j) * kHeads + h] =
-                            have ? __ldg(ix.w + rh) * __ldg(ix.q_scale + rh) : 0.f;
+                            have ? __ldg(ix.w + rh) * __ldg(fscale(ix.q_scale) + rh) : 0.f;
                 }
             } else {
                 for (int j = 0; j < kRows; j++) {
@@ -470,7 +618,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                 }
                 tc_fence_after();
                 const int s = t * kKeys + et;
-                const uint32_t acc = tmem + g * kN + lane_off;
+                const uint32_t acc = tmem + g * nB + lane_off;
                 // The accumulator is read in 32-register pieces (an FP8 query:
                 // 32 heads of one row; a bf16 query: 16 heads' q_hi and q_lo
                 // columns), each piece's load issued before the previous
@@ -555,7 +703,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpMma)
-        tmem_dealloc(tmem, 2 * kN);
+        tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -575,10 +723,13 @@ cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, floa
     std::call_once(once[dev], [dev] {
         cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(k_indexer_prefill<false>,
+            r = cudaFuncSetAttribute(k_indexer_prefill<kQBf16>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(k_indexer_prefill<true>,
+            r = cudaFuncSetAttribute(k_indexer_prefill<kQFp8>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(k_indexer_prefill<kQMx>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         err_of[dev] = r;
     });
@@ -590,18 +741,22 @@ cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, floa
                               (uint32_t)std::min(b.page_size, kKeys));
     if (e != cudaSuccess)
         return e;
-    const bool q8 = ix.q_dtype == SI_E4M3;
-    const int rows = q8 ? rows_per_block<true>() : rows_per_block<false>();
+    const int qm = ix.k.dtype == SI_MXE4M3 ? kQMx : (ix.q_dtype == SI_E4M3 ? kQFp8 : kQBf16);
+    const int rows = qm == kQMx ? rows_per_block<kQMx>()
+                                : (qm == kQFp8 ? rows_per_block<kQFp8>() : rows_per_block<kQBf16>());
     const int nb = (b.n_q + rows - 1) / rows;
     const int64_t npairs = (nb + 1) / 2;
     const int64_t grid = std::min<int64_t>(npairs, (int64_t)sms_of[dev]);
     count_launch();
-    if (q8)
-        k_indexer_prefill<true><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
+    if (qm == kQMx)
+        k_indexer_prefill<kQMx><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
                                                                              ld, nb, st);
-    else
-        k_indexer_prefill<false><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
+    else if (qm == kQFp8)
+        k_indexer_prefill<kQFp8><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
                                                                               ld, nb, st);
+    else
+        k_indexer_prefill<kQBf16><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
+                                                                               ld, nb, st);
     return cudaGetLastError();
 }
 

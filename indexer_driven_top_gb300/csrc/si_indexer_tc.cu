@@ -26,6 +26,20 @@
 // per-group quantisation, one group per head) needs no split: its codes are
 // q_hi, q_lo is zero and the scale multiplies the head weight.
 //
+// MXFP8 (k_indexer_tc<false, true>; section 5.1: query and keys quantised
+// per group of 32 entries with E8M0 scales).  The MMA is the block-scaled
+// kind::mxf8f6f4: B is the 64 query heads' codes (N = 64, no split), and the
+// tensor core applies each group's pair of scales to its 32-entry partial
+// dot product, so D[key, h] is already the MXFP8 dot product.  Scale factors
+// live in TMEM.  The producer lands each tile's key scale words (4 bytes per
+// key, one byte per group) with cp.async into a 32 x 16-byte block per stage,
+// row L holding keys L, L+32, L+64, L+96 -- the order tcgen05.cp spreads over
+// TMEM lanes and columns -- and the MMA thread copies that block (and, once
+// per query row, the query's block) into TMEM ahead of the tile's four MMAs;
+// copies and MMAs of one thread execute in order.  A bf16 query is converted
+// by the q-prep threads with the MX rule of section 4.3's quant_per_group
+// step, bit-identical to si_quant_mxfp8.
+//
 // One persistent CTA per SM runs a warp-specialised pipeline:
 //   2 producer warps -- per tile, TMA tensor copies of its key pages (128-byte
 //                       swizzle) into a ten-stage ring; tiles alternate
@@ -91,8 +105,20 @@ constexpr uint32_t kOffQ = kOffStage + kStages * kTile;            // [2]
 constexpr uint32_t kOffW = kOffQ + 2 * kTileB;                      // [2][64] fp32 (w * s_h)
 constexpr uint32_t kOffWin = kOffW + 2 * kHeads * 4;                // 2 producers x 32 int
 constexpr uint32_t kOffSc = kOffWin + 2 * 32 * 4;                   // [2][kScStages][128] fp32
-constexpr uint32_t kOffBar = kOffSc + 2 * kScStages * kKeys * 4;
+// MXFP8: scale words for tcgen05.cp, 32 rows x 16 bytes per block
+constexpr uint32_t kSfBytes = 512;
+constexpr uint32_t kOffSfa = kOffSc + 2 * kScStages * kKeys * 4;    // [kStages] key tiles
+constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfBytes;          // [2] query rows
+constexpr uint32_t kOffBar = kOffSfb + 2 * kSfBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 1024 + 1024;             // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// TMEM columns: accumulators from 0 (kN wide, or kHeads for MXFP8), then for
+// MXFP8 four scale columns per accumulator (keys) and per (pair, row buffer)
+// (query heads).
+constexpr uint32_t kTmemCols = kPairs * kAccPerPair * kN;  // 512
+constexpr uint32_t kColSfa = kPairs * kAccPerPair * kHeads;
+constexpr uint32_t kColSfb = kColSfa + 4 * kPairs * kAccPerPair;
+static_assert(kColSfb + 4 * kPairs * 2 <= kTmemCols, "TMEM columns");
 
 // Advances (row, tile) by `n` items of a row-major list with `tpr` tiles per row.
 __device__ __forceinline__ void advance(int &r, int &t, int n, int tpr)
@@ -170,11 +196,13 @@ __device__ __forceinline__ void cand_blocks(const si_batch &b, int r, CandLook &
     }
 }
 
-template <bool CAND>
+template <bool CAND, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
 k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix, float *scores,
              int64_t ld, int64_t total_items, int tiles_per_row, unsigned int *st, CandArgs ca)
 {
+    static_assert(!(CAND && MX), "candidate lists take FP8 keys with per-row scales");
+    constexpr int nB = MX ? kHeads : kN;  // B rows = accumulator columns
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
@@ -200,8 +228,9 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
 
     if (tid == 0) {
         for (int i = 0; i < kStages; i++) {
-            // producer's expect_tx arrival, or its 32 lanes' cp.async arrivals
-            mbar_init(full_bar + i, CAND ? 32 : 1);
+            // producer's expect_tx arrival, or its 32 lanes' cp.async arrivals,
+            // or (MXFP8) both
+            mbar_init(full_bar + i, CAND ? 32 : (MX ? 33 : 1));
             mbar_init(empty_bar + i, 1);    // MMA commit (or plain arrive)
         }
         for (int i = 0; i < kPairs * kAccPerPair; i++) {
@@ -219,7 +248,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
         fence_barrier_init();
     }
     if (warp == kWarpMma0) {
-        tmem_alloc(tmem_slot, kPairs * kAccPerPair * kN);
+        tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -297,7 +326,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
 #pragma unroll
             for (int i = 0; i < 4; i++)
                 cp_async_4(sd + (lane + 32 * i) * 4,
-                           prow[i] >= 0 ? (ix.k.scale ? ix.k.scale + prow[i] : &kScaleOne)
+                           prow[i] >= 0 ? (ix.k.scale ? fscale(ix.k.scale) + prow[i] : &kScaleOne)
                                         : &kScaleNone);
             cp_async_arrive_noinc(scfull_bar + pw * kScStages + ss);
             // shift the lookahead by one item of this producer
@@ -368,6 +397,26 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
             if (copy)
                 tma_load_2d(base + kOffStage + stg * kTile + k_lo * kDim, &tmap, 0, row,
                             full_bar + stg);
+            if constexpr (MX) {
+                // The keys' E8M0 words (byte g = group g) into the stage's block
+                // for tcgen05.cp: row `lane` holds keys lane + 32 i.  A key after
+                // the row's position or on an invalid page keeps a stale word;
+                // its score is -inf whatever the tensor core makes of it.
+                const uint32_t sfa = base + kOffSfa + stg * kSfBytes + lane * 16;
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int sk = s0 + lane + 32 * i;
+                    if (live && sk <= pf_pos) {
+                        const int lbk = sk >> lp;
+                        const int blk = win_s[lbk - win];
+                        if (lbk < b.max_blocks && (unsigned)blk < (unsigned)b.n_blocks)
+                            cp_async_4(sfa + 4 * i,
+                                       mxscale(ix.k.scale) +
+                                           (((int64_t)blk << lp) + (sk & (P - 1))) * (kDim / 32));
+                    }
+                }
+                cp_async_arrive_noinc(full_bar + stg);
+            }
             // The tile's per-key scales into this producer's scale ring (read
             // by the paired epilogue group): lane l copies keys s0 + 4 l .. +3
             // (one page), or writes -1 where the page has no valid block.
@@ -387,10 +436,10 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                         blk4 = v;
                 }
                 const uint32_t d = smem_u32(sc_s + (pw * kScStages + ss) * kKeys + 4 * lane);
-                if (blk4 >= 0 && ix.k.scale) {
-                    cp_async_16(d, ix.k.scale + ((int64_t)blk4 << lp) + (s4 & (P - 1)));
+                if (blk4 >= 0 && ix.k.scale && !MX) {
+                    cp_async_16(d, fscale(ix.k.scale) + ((int64_t)blk4 << lp) + (s4 & (P - 1)));
                     cp_async_arrive_noinc(sf);
-                } else {
+                } else {  // no per-key scale (MXFP8 scales are the tensor core's)
                     const uint32_t v = __float_as_uint(blk4 >= 0 ? 1.f : -1.f);
                     st_shared_v4(d, v, v, v, v);
                     mbar_arrive(sf);
@@ -404,6 +453,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
         const uint32_t idesc = idesc_e4m3(kKeys, kN);
         int r = (int)(j0 / tiles_per_row), t = (int)(j0 % tiles_per_row);
         int cur = -1, ri = -1, pos = -1, p = 0;
+        int sfb_row = -1;  // MXFP8: query row whose scales this pair's TMEM holds
         int64_t m = 0;  // live tiles of this pair so far
         for (int64_t it = 0; it < n_items; it++) {
             if (r != cur) {
@@ -422,7 +472,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
             if (mine) {
                 if (!mbar_wait(full_bar + stg, (uint32_t)(it / kStages) & 1, st))
                     break;
-                if constexpr (CAND)
+                if constexpr (CAND || MX)
                     fence_async_smem();  // cp.async pieces (generic proxy) -> tensor core
                 if (live) {
                     const int c = (int)(m % kAccPerPair);
@@ -433,14 +483,35 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                         break;
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t d = tmem + (pr * kAccPerPair + c) * kN;
+                        const uint32_t d = tmem + (pr * kAccPerPair + c) * nB;
+                        if constexpr (MX) {
+                            // scale factors first: the key tile's, and once per
+                            // query row this pair scores, the row's
+                            const uint32_t sfa = tmem + kColSfa + (pr * kAccPerPair + c) * 4;
+                            const uint32_t sfb = tmem + kColSfb + (pr * 2 + p) * 4;
+                            tmem_cp_32x128b_x4(sfa, base + kOffSfa + stg * kSfBytes);
+                            if (sfb_row != ri) {
+                                tmem_cp_32x128b_x4(sfb, base + kOffSfb + p * kSfBytes);
+                                sfb_row = ri;
+                            }
 #pragma unroll
-                        for (int kk = 0; kk < kDim / 32; kk++) {
-                            const uint64_t ad = smem_desc(base + kOffStage + stg * kTile + kk * 32,
-                                                          16, 1024, kSwizzle128B);
-                            const uint64_t bd = smem_desc(base + kOffQ + p * kTileB + kk * 32, 16,
-                                                          1024, kSwizzle128B);
-                            umma_f8_ss(d, ad, bd, idesc, kk > 0);
+                            for (int kk = 0; kk < kDim / 32; kk++) {
+                                const uint64_t ad = smem_desc(
+                                    base + kOffStage + stg * kTile + kk * 32, 16, 1024, kSwizzle128B);
+                                const uint64_t bd = smem_desc(base + kOffQ + p * kTileB + kk * 32,
+                                                              16, 1024, kSwizzle128B);
+                                umma_mx_ss(d, ad, bd, idesc_mx_e4m3(kKeys, nB, kk), sfa, sfb,
+                                           kk > 0);
+                            }
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < kDim / 32; kk++) {
+                                const uint64_t ad = smem_desc(
+                                    base + kOffStage + stg * kTile + kk * 32, 16, 1024, kSwizzle128B);
+                                const uint64_t bd = smem_desc(base + kOffQ + p * kTileB + kk * 32,
+                                                              16, 1024, kSwizzle128B);
+                                umma_f8_ss(d, ad, bd, idesc, kk > 0);
+                            }
                         }
                         umma_commit(empty_bar + stg);
                         umma_commit(cf);
@@ -466,6 +537,76 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
             if (ri >= 2 && !mbar_wait(qempty_bar + p, (uint32_t)((ri - 2) >> 1) & 1, st))
                 break;
             const uint32_t qb = base + kOffQ + p * kTileB;
+            if constexpr (MX) {
+                // dims [64 half, +64) of head h = MX groups 2 half, 2 half + 1
+                uint32_t sbytes;  // this thread's two scale bytes, group 2 half in the low one
+                if (ix.q_dtype == SI_MXE4M3) {
+                    const int64_t rh = (int64_t)r * kHeads + h;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        static_cast<const uint8_t *>(ix.q) + rh * kDim + half * 64);
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        const uint4 v = __ldg(src + c);
+                        st_shared_v4(qb + sw128_offset(h, (uint32_t)(half * 4 + c)), v.x, v.y, v.z,
+                                     v.w);
+                    }
+                    const uint8_t *qs = mxscale(ix.q_scale) + rh * (kDim / 32) + 2 * half;
+                    sbytes = (uint32_t)__ldg(qs) | ((uint32_t)__ldg(qs + 1) << 8);
+                } else {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        static_cast<const uint16_t *>(ix.q) + ((int64_t)r * kHeads + h) * kDim +
+                        half * 64);
+                    sbytes = 0;
+#pragma unroll
+                    for (int gg = 0; gg < 2; gg++) {  // one MX group = 32 dims = 4 loads
+                        uint32_t q2[16];
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const uint4 v = __ldg(src + 4 * gg + i);
+                            q2[4 * i] = v.x;
+                            q2[4 * i + 1] = v.y;
+                            q2[4 * i + 2] = v.z;
+                            q2[4 * i + 3] = v.w;
+                        }
+                        uint32_t mb = 0;
+#pragma unroll
+                        for (int i = 0; i < 16; i++)
+                            mb = max(mb, max(abs_bits(__uint_as_float(q2[i] << 16)),
+                                             abs_bits(__uint_as_float(q2[i] & 0xFFFF0000u))));
+                        const uint32_t sb = mx_scale_byte(mb);
+                        sbytes |= sb << (8 * gg);
+#pragma unroll
+                        for (int c = 0; c < 2; c++) {  // 16 dims per 16-byte unit
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int j = 0; j < 4; j++) {
+                                const uint32_t a = q2[8 * c + 2 * j], bb = q2[8 * c + 2 * j + 1];
+                                w4[j] = mx_codes2(__uint_as_float(a << 16),
+                                                  __uint_as_float(a & 0xFFFF0000u), sb) |
+                                        (mx_codes2(__uint_as_float(bb << 16),
+                                                   __uint_as_float(bb & 0xFFFF0000u), sb)
+                                         << 16);
+                            }
+                            st_shared_v4(qb + sw128_offset(h, (uint32_t)(half * 4 + 2 * gg + c)),
+                                         w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                }
+                // head h's scale word (byte g = group g) for tcgen05.cp: row
+                // h % 32, word h / 32 of the row buffer's block
+                const uint32_t other = __shfl_xor_sync(0xffffffffu, sbytes, 1);
+                if (half == 0) {
+                    const uint32_t word = sbytes | (other << 16);
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(base + kOffSfb + p * kSfBytes +
+                                                                 (h & 31) * 16 + (h >> 5) * 4),
+                                 "r"(word)
+                                 : "memory");
+                    w_s[p * kHeads + h] = __ldg(ix.w + (int64_t)r * kHeads + h);
+                }
+                fence_async_smem();
+                mbar_arrive(qfull_bar + p);
+                continue;
+            }
             if (ix.q_dtype == SI_E4M3) {
                 // Stored FP8 query: its codes are the B operand (q_lo = 0) and
                 // the per-(row, head) scale joins the head weight.
@@ -481,7 +622,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                 }
                 if (half == 0)
                     w_s[p * kHeads + h] = __ldg(ix.w + (int64_t)r * kHeads + h) *
-                                          __ldg(ix.q_scale + (int64_t)r * kHeads + h);
+                                          __ldg(fscale(ix.q_scale) + (int64_t)r * kHeads + h);
                 fence_async_smem();
                 mbar_arrive(qfull_bar + p);
                 continue;
@@ -582,11 +723,29 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                         break;
                     tc_fence_after();
                     const float4 *w4 = reinterpret_cast<const float4 *>(w_s + p * kHeads);
-                    const uint32_t acc = tmem + (g * kAccPerPair + c) * kN + lane_off;
+                    const uint32_t acc = tmem + (g * kAccPerPair + c) * nB + lane_off;
                     // partial head sums in two packed pairs (0.0f has all bits 0)
                     uint64_t p01 = 0, p23 = 0;
+                    if constexpr (MX) {
+                        // D[key, h] is the MXFP8 logit: w_h * ReLU(D), two heads per fma
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32(acc, v0);
+                        tmem_ld32(acc + 32, v1);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int hh = 0; hh < 2; hh++) {  // heads [32 hh, 32 hh + 32)
+                        for (int i = 0; i < 64; i += 4) {
+                            const float4 wv = w4[i >> 2];
+                            const uint32_t *v = i < 32 ? v0 + i : v1 + (i - 32);
+                            f32x2_fma(p01, f32x2_pack(wv.x, wv.y),
+                                      f32x2_pack(fmaxf(__uint_as_float(v[0]), 0.f),
+                                                 fmaxf(__uint_as_float(v[1]), 0.f)));
+                            f32x2_fma(p23, f32x2_pack(wv.z, wv.w),
+                                      f32x2_pack(fmaxf(__uint_as_float(v[2]), 0.f),
+                                                 fmaxf(__uint_as_float(v[3]), 0.f)));
+                        }
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < (MX ? 0 : 2); hh++) {  // heads [32 hh, 32 hh + 32)
                         uint32_t vh[32], vl[32];
                         tmem_ld32(acc + hh * 32, vh);
                         tmem_ld32(acc + kHeads + hh * 32, vl);
@@ -633,7 +792,7 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpMma0)
-        tmem_dealloc(tmem, kPairs * kAccPerPair * kN);
+        tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -644,8 +803,11 @@ bool indexer_tc_supported(const si_batch &b, const si_indexer &ix, int64_t ld)
     // whole pages are copied as tensor boxes: rows packed (stride 128 bytes),
     // page size a power of two >= 8, physical row indices within int32
     const bool pow2_page = b.page_size >= 8 && (b.page_size & (b.page_size - 1)) == 0;
-    const bool q_ok = ix.q_dtype == SI_BF16 || (ix.q_dtype == SI_E4M3 && ix.q_scale);
-    return pow2_page && q_ok && ix.k.dtype == SI_E4M3 && ix.n_heads == kHeads &&
+    const bool mx = ix.k.dtype == SI_MXE4M3;
+    const bool q_ok = mx ? (ix.q_dtype == SI_BF16 ||
+                            (ix.q_dtype == SI_MXE4M3 && ((uintptr_t)ix.q_scale % 4) == 0))
+                         : (ix.q_dtype == SI_BF16 || (ix.q_dtype == SI_E4M3 && ix.q_scale));
+    return pow2_page && q_ok && (ix.k.dtype == SI_E4M3 || mx) && ix.n_heads == kHeads &&
            ix.head_dim == kDim && ix.k.row_stride == kDim &&
            (int64_t)b.n_blocks * b.page_size < (int64_t)INT32_MAX &&
            ((uintptr_t)ix.q % 16) == 0 && ((uintptr_t)ix.k.data % 16) == 0 &&
@@ -670,10 +832,13 @@ cudaError_t launch_indexer_tc_any(const si_batch &b, const si_indexer &ix, const
     std::call_once(once[dev], [dev] {
         cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(k_indexer_tc<false>,
+            r = cudaFuncSetAttribute(k_indexer_tc<false, false>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(k_indexer_tc<true>,
+            r = cudaFuncSetAttribute(k_indexer_tc<true, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(k_indexer_tc<false, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         err_of[dev] = r;
     });
@@ -688,15 +853,18 @@ cudaError_t launch_indexer_tc_any(const si_batch &b, const si_indexer &ix, const
     const int tiles_per_row = (int)((ld + kKeys - 1) / kKeys);
     const int64_t total = (int64_t)b.n_q * tiles_per_row;
     const int64_t grid = std::min<int64_t>(total, (int64_t)sms_of[dev]);  // one CTA per SM
+    if (ca.cand && ix.k.dtype == SI_MXE4M3)
+        return cudaErrorNotSupported;  // candidate lists take per-row FP8 scales
     count_launch();
     if (ca.cand)
-        k_indexer_tc<true><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores, ld,
-                                                                        total, tiles_per_row, st,
-                                                                        ca);
+        k_indexer_tc<true, false><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
+            tmap, b, ix, scores, ld, total, tiles_per_row, st, ca);
+    else if (ix.k.dtype == SI_MXE4M3)
+        k_indexer_tc<false, true><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
+            tmap, b, ix, scores, ld, total, tiles_per_row, st, ca);
     else
-        k_indexer_tc<false><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores, ld,
-                                                                         total, tiles_per_row, st,
-                                                                         ca);
+        k_indexer_tc<false, false><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
+            tmap, b, ix, scores, ld, total, tiles_per_row, st, ca);
     return cudaGetLastError();
 }
 

@@ -412,6 +412,44 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N)
     return (1u << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::mxf8f6f4 (block-scaled, one E8M0 scale per
+// 32 entries of K) with e4m3 A and B, fp32 accumulate.  `sf_id` (0..3) picks
+// the byte of each 32-bit scale-factor word that this MMA's K-block uses, for
+// A (bits 29-30) and B (bits 4-5); bit 23 selects E8M0 scales.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(uint32_t M, uint32_t N, uint32_t sf_id)
+{
+    return (sf_id << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | (1u << 23) |
+           ((M >> 4) << 24) | (sf_id << 29);
+}
+
+// D[tmem] (+)= (A[smem] scaled by SFA) * (B[smem] scaled by SFB)^T, kind::mxf8f6f4
+// with one scale per 32 entries of K.  Scale factors live in TMEM: the word of
+// row m (A) or n (B) in column base + m / 32 at lane m % 32 of every lane
+// quarter, byte g for K-block g (selected by the descriptor's sf_id).
+__device__ __forceinline__ void umma_mx_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %6, 0; "
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copies 32 rows of 16 bytes from shared memory (plain row-major, 512 bytes,
+// 16-byte aligned) into 4 TMEM columns at `taddr`: row L lands in lane L of
+// every lane quarter (the scale-factor layout above).  Issued by one thread;
+// ordered before that thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint32_t saddr)
+{
+    // core matrices of 8 rows x 16 bytes, 8-row groups 128 bytes apart
+    const uint64_t d = smem_desc(saddr, 16, 128, kSwizzleNone);
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d)
+                 : "memory");
+}
+
 // Arrives on the mbarrier once every UMMA issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(si):
 
 def test_version_and_status_strings(si):
     lib = si.load()
-    assert lib.si_version() == 4
+    assert lib.si_version() == 5
     assert lib.si_status_string(0) == b"ok"
     assert lib.si_status_string(3) == b"workspace error"
 
@@ -180,3 +180,54 @@ def test_fp4_cache_host_validation(si):
     at = si.c_attention(fake, si.BF16, 4, 64, 64, kp, vp, 0.125)
     assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
                               4096, None) == 2
+
+
+def test_mxfp8_host_validation(si):
+    """SI_MXE4M3 (section 5.1's MXFP8 indexer format): keys need E8M0 scales
+    with scale_tile 32, head_dim a multiple of 32, and an mxe4m3, bf16 or f32
+    query; an mxe4m3 query needs MXFP8 keys; candidate lists refuse MXFP8
+    keys; attention caches refuse it.  si_quant_mxfp8 validates its shape,
+    dtype and alignment before any launch."""
+    lib = si.load()
+    P = ctypes.c_void_p
+    fake = 1 << 20
+    ws = 256 << 20
+    b = ctypes.byref(_batch(si))
+    MX = si.MXE4M3
+    good_k = si.c_paged(fake, fake, MX, 128, 128, 32)
+    # scales missing, wrong tile, ragged stride
+    for kp in (si.c_paged(fake, None, MX, 128, 128, 32), si.c_paged(fake, fake, MX, 128, 128, 0),
+               si.c_paged(fake, fake, MX, 100, 100, 32)):
+        ix = si.c_indexer(fake, si.BF16, None, fake, 64, 128, kp)
+        assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 1
+        assert b"MXFP8" in lib.si_last_error()
+    # head_dim not a multiple of 32
+    ix = si.c_indexer(fake, si.BF16, None, fake, 4, 48, si.c_paged(fake, fake, MX, 64, 64, 32))
+    assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 1
+    # an e4m3 (per-head scale) query with MXFP8 keys; an MX query with FP8 keys
+    ix = si.c_indexer(fake, si.E4M3, fake, fake, 64, 128, good_k)
+    assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 2
+    ix = si.c_indexer(fake, MX, fake, fake, 64, 128, si.c_paged(fake, fake, si.E4M3, 128, 128))
+    assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 2
+    # an MX query without its scale bytes
+    ix = si.c_indexer(fake, MX, None, fake, 64, 128, good_k)
+    assert lib.si_indexer_scores(b, ctypes.byref(ix), P(fake), 256, P(ws), 4096, None) == 1
+    # candidate lists
+    ix = si.c_indexer(fake, si.BF16, None, fake, 64, 128, good_k)
+    assert lib.si_workspace_size_cand(b, ctypes.byref(ix), 300) == 0
+    assert lib.si_indexer_topk_cand(b, ctypes.byref(ix), P(fake), 300, 300, 8, P(fake), None, 0,
+                                    P(ws), 1 << 20, None) == 2
+    # attention caches
+    at = si.c_attention(fake, si.BF16, 4, 64, 64, si.c_paged(fake, fake, MX, 64, 64, 32),
+                        si.c_paged(fake, fake, MX, 64, 64, 32), 0.125)
+    assert lib.si_sparse_attn(b, ctypes.byref(at), P(fake), 8, P(fake), si.F32, None, P(ws),
+                              4096, None) == 2
+    # si_quant_mxfp8
+    q = lib.si_quant_mxfp8
+    assert q(P(fake), si.BF16, 4, 48, P(fake), P(fake), None) == 1          # dim % 32
+    assert q(P(fake), si.BF16, 4, 0, P(fake), P(fake), None) == 1
+    assert q(P(fake), si.E4M3, 4, 64, P(fake), P(fake), None) == 1          # dtype
+    assert q(P(fake + 8), si.BF16, 4, 64, P(fake), P(fake), None) == 1      # alignment
+    assert q(None, si.BF16, 4, 64, P(fake), P(fake), None) == 1
+    assert q(P(fake), si.BF16, -1, 64, P(fake), P(fake), None) == 1
+    assert q(None, si.BF16, 0, 64, None, None, None) == 0                    # empty: no-op

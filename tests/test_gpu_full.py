@@ -201,3 +201,24 @@ def test_long_context_fp8_kv_cache_split(si):
     tiles are split over clusters and merged."""
     wl = synth.make("c3", batch=4, ctx=40000, kv_fp8=True)
     _run(si, wl, rows=list(range(wl.n_q)))
+
+
+def test_benchmark_workload_mxfp8_indexer(si):
+    """The benchmarked decode step with the MXFP8 indexer of section 5.1:
+    keys in groups of 32 with E8M0 scales, the bf16 query converted on the
+    device; every row."""
+    wl = synth.make("c1", idx_mx=True)
+    _run(si, wl, rows=list(range(wl.n_q)))
+
+
+def test_long_context_mxfp8_indexer(si):
+    wl = synth.make("c3", idx_mx=True)
+    _run(si, wl, rows=list(range(wl.n_q)))
+
+
+def test_causal_prefill_full_size_mxfp8(si):
+    """The 16384-row prefill with the MXFP8 indexer: blocks of three rows."""
+    wl = synth.make("c2", idx_mx=True)
+    rows = _prefill_rows(wl.n_q, 3, wl.K)
+    assert len(rows) >= 256
+    _run(si, wl, rows=rows)
