@@ -70,8 +70,11 @@ def algorithmic_bytes(wl, out_bytes=2):
     n_sel = int(np.minimum(sel_seq, keys_seq).sum())
     esz = {"bf16": 2, "e4m3": 1, "e2m1": 0.5}.get(wl.kv_dtype, 4)
     kv_scale_b = 0 if getattr(wl, "kv_scale", None) is None else wl.kv_scale.shape[-1] * 4
-    kesz = 1 if wl.k_idx_dtype == "e4m3" else 4
-    idx_b = n_keys * (wl.Di * kesz + (4 if wl.k_scale is not None else 0)) \
+    kesz = 1 if wl.k_idx_dtype in ("e4m3", "mxe4m3") else 4
+    # per key: one fp32 scale (e4m3 keys) or one E8M0 byte per 32 entries (MXFP8)
+    ksc = 0 if wl.k_scale is None else \
+        wl.k_scale.dtype.itemsize * (wl.k_scale.shape[-1] if wl.k_scale.ndim == 3 else 1)
+    idx_b = n_keys * (wl.Di * kesz + ksc) \
         + wl.n_q * (wl.Hi * wl.Di * 2 + wl.Hi * 4) + n_keys_rows * 4
     topk_b = n_keys_rows * 4 + wl.n_q * wl.K * 4
     qesz = 2 if (getattr(wl, "attn_q_dtype", "") or wl.kv_dtype) == "bf16" else 4
@@ -199,7 +202,9 @@ def _kernel_of(wl):
     this workload: the tensor-core kernels where their shape conditions hold
     (64 x 128 indexer with bf16 q and e4m3 keys; 128 heads x 576 latent rows
     in bf16, FP8 or FP4), the generic ones otherwise."""
-    tc_ix = wl.Hi == 64 and wl.Di == 128 and wl.q_idx_dtype == "bf16" and wl.k_idx_dtype == "e4m3"
+    tc_ix = wl.Hi == 64 and wl.Di == 128 and (
+        (wl.q_idx_dtype in ("bf16", "e4m3") and wl.k_idx_dtype == "e4m3")
+        or (wl.q_idx_dtype in ("bf16", "mxe4m3") and wl.k_idx_dtype == "mxe4m3"))
     tc_at = (wl.Hq == 128 and wl.Dqk == 576 and wl.Dv == 512
              and wl.kv_dtype in ("bf16", "e4m3", "e2m1"))
     prefill = tc_ix and wl.n_seq == 1 and wl.n_q >= 64
@@ -242,14 +247,14 @@ def roofline_of(kernel, wl, algo, ms, peaks, long_step, variant=""):
     return roof
 
 
-def workload_record(si, dev, name, steps, warmup):
+def workload_record(si, dev, name, steps, warmup, variant="", **over):
     """One of the other configurations, timed the same way as the headline
     step (three calls per step, L2 flushed before every step): queries/s, the
     step's algorithmic bytes over its time, per-kernel times and the roofline
-    of the dominant kernel."""
+    of the dominant kernel.  `over` are generator options (e.g. idx_mx)."""
     import torch
     import synth
-    wl = synth.make(name)
+    wl = synth.make(name, **over)
     dw = si.upload(wl, dev)
     b, ix, at, K = dw.batch, dw.indexer, dw.attention, dw.k_top
     ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, ix, at, K), dev)
@@ -291,8 +296,12 @@ def workload_record(si, dev, name, steps, warmup):
            "hbm": {"algorithmic_bytes_per_step": total, "achieved_gbs": gbs,
                    "frac_of_8tbs": gbs / NOMINAL_HBM_GBS, "frac_of_measured": gbs / peaks["hbm_gbs"]},
            "kernels_ms": kms, "kernels": {k: v[0] for k, v in _kernel_of(wl).items()},
-           "roofline": roofline_of(dom, wl, algo, kms[dom], peaks, ms > 1.0),
+           "roofline": roofline_of(dom, wl, algo, kms[dom], peaks, ms > 1.0, variant),
+           "indexer_roofline": roofline_of("indexer", wl, algo, kms["indexer"], peaks, ms > 1.0,
+                                           variant),
            "l2": "flushed between steps (512 MiB write)"}
+    if over:
+        rec["options"] = over
     del dw, ws, scores, idx, out, flush
     torch.cuda.empty_cache()
     return rec
@@ -355,16 +364,19 @@ def run_reference(args):
 PREFILL_STRIP_ROWS = 1024  # 1024 rows x 16384 positions x 4 B = 64 MiB: the strip stays in L2
 
 
-def _prefill_once(si, dev, steps, q_fp8):
+def _prefill_once(si, dev, steps, mode):
     """The 16384-token causal prefill's indexer, run as the fused path runs it:
     strips of PREFILL_STRIP_ROWS rows, each scored into a strip buffer that
     stays in L2 and then consumed by the Top-K.  Returns (causal pairs,
     algorithmic FLOPs, indexer ms per prefill: the sum over the strips of the
-    indexer launches' event-timed durations, ms of the whole strip loop)."""
+    indexer launches' event-timed durations, ms of the whole strip loop).
+    mode: "bf16" (the configuration: bf16 query, e4m3 keys + fp32 scale),
+    "e4m3" (query stored e4m3 + fp32 scale per (row, head)) or "mx" (MXFP8
+    keys, the bf16 query converted to MXFP8 inside the kernel)."""
     import torch
     import indexer_driven_top_gb300 as si_mod
     import synth
-    wl = synth.make("c2", Hq=1, Dqk=64, Dv=64, q_idx_fp8=q_fp8)
+    wl = synth.make("c2", Hq=1, Dqk=64, Dv=64, q_idx_fp8=mode == "e4m3", idx_mx=mode == "mx")
     dw = si.upload(wl, dev)
     b, ix, K = dw.batch, dw.indexer, dw.k_top
     ld = b.max_ctx
@@ -498,10 +510,12 @@ def prefill_indexer(si, dev, steps):
     scores those same bytes)."""
     peaks = _peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]   # measured bf16 burst x nominal fp8/bf16 ratio (2)
-    pairs, flops, ms, ms_loop = _prefill_once(si, dev, steps, False)
+    pairs, flops, ms, ms_loop = _prefill_once(si, dev, steps, "bf16")
     tflops = flops / (ms / 1e3) / 1e12
-    _, _, ms8, ms8_loop = _prefill_once(si, dev, steps, True)
+    _, _, ms8, ms8_loop = _prefill_once(si, dev, steps, "e4m3")
     tflops8 = flops / (ms8 / 1e3) / 1e12
+    _, _, msx, msx_loop = _prefill_once(si, dev, steps, "mx")
+    tflopsx = flops / (msx / 1e3) / 1e12
     return {"workload": "causal prefill 16384 tokens, indexer 64x128, e4m3 keys + fp32 scale, "
                         "bf16 query",
             "kernel": "k_indexer_prefill",
@@ -516,7 +530,13 @@ def prefill_indexer(si, dev, steps):
                                   "frac_of_fp8_peak": tflops8 / fp8_peak,
                                   "ms_strip_loop_with_topk": ms8_loop,
                                   "note": "query quantised to e4m3 + fp32 scale per (row, head); "
-                                          "not the configuration's query format"}}
+                                          "not the configuration's query format"},
+            "option_mxfp8": {"ms_per_prefill": msx, "tflops": tflopsx,
+                             "frac_of_fp8_peak": tflopsx / fp8_peak,
+                             "ms_strip_loop_with_topk": msx_loop,
+                             "note": "section 5.1's MXFP8 indexer: keys in groups of 32 with E8M0 "
+                                     "scales, the bf16 query converted to MXFP8 inside the kernel "
+                                     "(block-scaled UMMA, three rows per 192-wide block)"}}
 
 
 def candidate_selection(si, dev, steps, n_cand=16384):
@@ -755,7 +775,9 @@ def run_si(args):
         del dw, ws, scores, idx, out, flush
         torch.cuda.empty_cache()
         others = {"long_context": workload_record(si, dev, "c3", args.steps, args.warmup),
-                  "mixed": workload_record(si, dev, "c4", args.steps, args.warmup)}
+                  "mixed": workload_record(si, dev, "c4", args.steps, args.warmup),
+                  "mxfp8_indexer": workload_record(si, dev, "c1", args.steps, args.warmup,
+                                                   variant=":mx", idx_mx=True)}
 
     cpu = None
     if not args.no_cpu_baseline:

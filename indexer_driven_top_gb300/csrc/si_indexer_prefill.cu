@@ -12,9 +12,13 @@
 // (128 keys x 128 e4m3 bytes, UMMA A operand, landed by TMA) serves a block
 // of query rows at once, and the B operand is always 256 rows wide (UMMA N =
 // 256) so that every key byte brought in feeds a full-width UMMA:
-//   * bf16 query: two rows per block, each row's 64 heads split exactly into
+//   * bf16 query: four rows per block, each row's 64 heads split exactly into
 //     two e4m3 terms as in the decode indexer (q = s_h (q_hi + q_lo), s_h a
-//     power of two folded into the head weight): 2 x 128 B rows;
+//     power of two folded into the head weight).  The two terms are laid
+//     side by side along K (a q_hi tile and a q_lo tile), and eight UMMAs
+//     accumulate key . q_hi and key . q_lo into the same 64 columns per row,
+//     so the epilogue reads one logit per head (the key tile serves as A for
+//     both halves of K);
 //   * FP8 query with a per-(row, head) scale (section 4.3 quantises the
 //     indexer query before scoring): four rows per block, 64 heads each, the
 //     scale folded into the head weight: 4 x 64 B rows, twice the scores per
@@ -26,24 +30,33 @@
 //     are 192 wide (three rows of 64 heads per block) instead of 256; the
 //     keys' scale words land per stage in the 32 x 16-byte block tcgen05.cp
 //     copies to TMEM (row L: keys L, L+32, L+64, L+96), the rows' per block.
-// The causal triangle is balanced by dealing row blocks to CTAs in head/tail
-// pairs (block b together with block nb-1-b, the pairing section 6.3 uses for
-// context-parallel shards): every pair holds the same number of causal
-// (row, key) pairs.
+// The causal triangle is balanced by splitting the list of (row block, key
+// tile) items -- block by block, each block's live tiles (those at or before
+// its last position) -- into equal contiguous ranges, one per CTA: every CTA
+// gets the same number of tiles whatever the number of blocks, and a block
+// whose tiles straddle two CTAs has its query prepared by both.  Blocks are
+// listed head and tail alternately (0, nb-1, 1, nb-2, ...: the pairing
+// section 6.3 uses for context-parallel shards), so that every range mixes
+// short and long blocks and the per-block costs spread evenly too.
 //
 // One persistent CTA per SM, 16 warps:
 //   warps 0, 2  -- producers, alternate items (a bulk tensor copy holds its
 //                  issuing warp for several hundred cycles): per item (block,
-//                  key tile) the TMA copies of the tile's key pages into an
-//                  eight-stage ring, and the keys' scales into the ring of the
-//                  epilogue group that takes the item (cp.async);
-//   warp 1      -- MMA: four kind::f8f6f4 UMMAs (M 128, N 256, K 32) per item
-//                  into one of two TMEM accumulators (256 columns each);
+//                  key tile) the TMA copies of the tile's key pages into a
+//                  ring of key stages, and the keys' scales into the
+//                  producer's scale ring (cp.async);
+//   warp 1      -- MMA: four (bf16 query: eight) kind::f8f6f4 UMMAs (M 128,
+//                  N 256, K 32) per item into one of two TMEM accumulators
+//                  (256 columns each);
+//   warp 3      -- writes -inf into each block's score columns past its live
+//                  tiles with bulk copies from a -inf buffer in shared memory
+//                  (the copy engine does the writing, off the pipeline);
 //   warps 4..7  -- q-prep: writes each block's query rows into the B operand
-//                  (double-buffered) and -inf into the rows' score columns
-//                  past the block's last live tile;
+//                  (double-buffered);
 //   warps 8..15 -- two epilogue groups that take alternate items: per key
-//                  (TMEM lane) and row, ReLU, head weights, scale, store.
+//                  (TMEM lane) and row, ReLU, head weights, scale, store; an
+//                  item's accumulator is released as soon as its last piece
+//                  has been loaded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -67,36 +80,45 @@ constexpr int kKeys = 128;            // keys per tile = UMMA M
 constexpr int kHeads = 64;            // indexer heads
 constexpr int kDim = 128;             // head dim = bytes per e4m3 key row = UMMA K
 constexpr int kN = 256;               // UMMA N (bf16 and FP8 query): B rows of one block
-constexpr int kMaxRows = 4;           // query rows per block, FP8 query
+constexpr int kMaxRows = 4;           // query rows per block
 // Query modes: a bf16 query split into q_hi / q_lo terms, an FP8 query with a
-// per-(row, head) scale, an MXFP8 query (block-scaled MMA).
+// per-(row, head) scale, an MXFP8 query (block-scaled MMA).  Every mode puts
+// a row's 64 heads in 64 B rows (and accumulator columns).
 constexpr int kQBf16 = 0, kQFp8 = 1, kQMx = 2;
-// B rows per query row: a bf16 query takes 64 q_hi heads then 64 q_lo heads,
-// an FP8 or MXFP8 query its 64 heads.
-template <int QM> constexpr int row_n() { return QM == kQBf16 ? 2 * kHeads : kHeads; }
 template <int QM> constexpr int mma_n() { return QM == kQMx ? 3 * kHeads : kN; }
-template <int QM> constexpr int rows_per_block() { return mma_n<QM>() / row_n<QM>(); }
-constexpr int kStages = 8;            // key-tile ring depth
+template <int QM> constexpr int rows_per_block() { return mma_n<QM>() / kHeads; }
 constexpr int kScStages = 4;          // scale ring depth per epilogue group
 constexpr int kThreads = 16 * 32;
 constexpr int kWarpProd0 = 0, kWarpProd1 = 2;  // producers: items of parity 0 / 1
-constexpr int kWarpMma = 1, kWarpPrep0 = 4, kWarpEpi0 = 8;
+constexpr int kWarpMma = 1, kWarpTail = 3, kWarpPrep0 = 4, kWarpEpi0 = 8;
 
 constexpr uint32_t kTile = kKeys * kDim;    // 16 KB, SW128 K-major
 constexpr uint32_t kTileB = kN * kDim;      // 32 KB, SW128 K-major
-constexpr uint32_t kOffStage = 0;
-constexpr uint32_t kOffQ = kOffStage + kStages * kTile;               // [2] B operands
-constexpr uint32_t kOffW = kOffQ + 2 * kTileB;                         // [2][rows][64] w * s_h
-constexpr uint32_t kOffWin = kOffW + 2 * kMaxRows * kHeads * 4;        // 2 x 32 block-table entries
-constexpr uint32_t kOffSc = kOffWin + 2 * 32 * 4;                      // [2][kScStages][128]
 // MXFP8 scale words for tcgen05.cp (32 rows x 16 bytes per block): one block
 // per key stage, two per B buffer (B rows 0..127 and 128..255)
 constexpr uint32_t kSfBytes = 512;
-constexpr uint32_t kOffSfa = kOffSc + 2 * kScStages * kKeys * 4;       // [kStages]
-constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfBytes;             // [2][2]
-constexpr uint32_t kOffBar = kOffSfb + 4 * kSfBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;                  // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+constexpr uint32_t kNinfBytes = 4096;       // -inf source of the tail writer's copies
+
+// Shared-memory layout of one query mode: the key-tile ring, two B buffers
+// (a bf16 query takes a q_hi and a q_lo tile per buffer, so its ring is
+// shorter), head weights, block-table windows, the epilogue scale rings, the
+// MXFP8 scale blocks, the -inf buffer and the barriers.
+template <int QM> struct Lay {
+    static constexpr int kStages = QM == kQBf16 ? 5 : 8;
+    static constexpr uint32_t kQParts = QM == kQBf16 ? 2 : 1;
+    static constexpr uint32_t kQBuf = kQParts * kTileB;
+    static constexpr uint32_t kOffStage = 0;
+    static constexpr uint32_t kOffQ = kOffStage + kStages * kTile;             // [2] B operands
+    static constexpr uint32_t kOffW = kOffQ + 2 * kQBuf;                        // [2][rows][64]
+    static constexpr uint32_t kOffWin = kOffW + 2 * kMaxRows * kHeads * 4;      // 2 x 32 entries
+    static constexpr uint32_t kOffSc = kOffWin + 2 * 32 * 4;                    // [2][kScStages][128]
+    static constexpr uint32_t kOffSfa = kOffSc + 2 * kScStages * kKeys * 4;     // [kStages]
+    static constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfBytes;           // [2][2]
+    static constexpr uint32_t kOffNinf = kOffSfb + 4 * kSfBytes;
+    static constexpr uint32_t kOffBar = kOffNinf + kNinfBytes;
+    static constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;               // + alignment slack
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
 // TMEM: two accumulators of mma_n columns; MXFP8 adds 4 scale columns per
 // accumulator (keys) and 8 per B buffer (query rows) after them.
 constexpr uint32_t kTmemCols = 2 * kN;  // 512
@@ -115,35 +137,9 @@ __device__ __forceinline__ uint16_t float2_to_e4m3x2(float a, float b)
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-// The CTA's row blocks, in processing order: pairs p = blockIdx.x,
-// blockIdx.x + G, ...; within a pair block p, then block nb - 1 - p.
-struct BlockWalk {
-    int64_t pair, npairs, G;
-    int nb, side;
-    __device__ BlockWalk(int nb_, int64_t G_) : pair(blockIdx.x), npairs((nb_ + 1) / 2), G(G_),
-                                                nb(nb_), side(0) {}
-    // next block index, or -1 when done
-    __device__ int next()
-    {
-        for (;;) {
-            if (pair >= npairs)
-                return -1;
-            const int blk = side == 0 ? (int)pair : nb - 1 - (int)pair;
-            const bool dup = side == 1 && blk == (int)pair;
-            if (side == 0) {
-                side = 1;
-            } else {
-                side = 0;
-                pair += G;
-            }
-            if (!dup)
-                return blk;
-        }
-    }
-};
-
 // Rows of block `blk` and its live key tiles (those holding a key at or
-// before the block's last position).
+// before the block's last position; at least one, so that every block's
+// score rows are written).
 template <int kRows>
 __device__ __forceinline__ void block_shape(const si_batch &b, int blk, int tiles_ld, int &r0,
                                             int &nrows, int &T)
@@ -153,19 +149,121 @@ __device__ __forceinline__ void block_shape(const si_batch &b, int blk, int tile
     int pmax = -1;
     for (int j = 0; j < nrows; j++)
         pmax = max(pmax, __ldg(b.q_pos + r0 + j));
-    T = min(tiles_ld, (pmax + kKeys) / kKeys);
+    T = max(1, min(tiles_ld, (pmax + kKeys) / kKeys));
 }
+
+// Block at position i of the item list: head and tail blocks alternately.
+__device__ __forceinline__ int block_at(int i, int nb) { return (i & 1) ? nb - 1 - (i >> 1) : i >> 1; }
+
+// This CTA's range of the item list: from tile t0 of the block at list
+// position b0, n items.
+struct Span {
+    int b0, t0;
+    int64_t n;
+};
+
+// Found by all threads of the CTA together: thread i sums the tiles of
+// blocks [i m, (i + 1) m), a block-wide scan places those sums, and the
+// thread whose blocks hold the range's first item locates it.  `wsum` holds
+// kThreads / 32 + 2 entries of shared memory.
+template <int kRows>
+__device__ Span find_span(const si_batch &b, int nb, int tiles_ld, long long *wsum)
+{
+    constexpr int kWarps = kThreads / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int m = (nb + kThreads - 1) / kThreads;
+    const int lo = min(nb, tid * m), hi = min(nb, lo + m);
+    long long local = 0;
+    for (int i = lo; i < hi; i++) {
+        int r0, nrows, T;
+        block_shape<kRows>(b, block_at(i, nb), tiles_ld, r0, nrows, T);
+        local += T;
+    }
+    long long x = local;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        long long t = lane < kWarps ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o)
+                t += y;
+        }
+        if (lane < kWarps)
+            wsum[lane] = t;  // inclusive warp totals
+    }
+    __syncthreads();
+    const long long before = (warp > 0 ? wsum[warp - 1] : 0) + x - local;
+    const long long total = wsum[kWarps - 1];
+    const long long j0 = total * blockIdx.x / gridDim.x;
+    const long long j1 = total * (blockIdx.x + 1) / gridDim.x;
+    __syncthreads();  // every thread has read the totals before they are reused
+    if (j0 < j1 && before <= j0 && j0 < before + local) {
+        long long acc = before;
+        for (int i = lo; i < hi; i++) {
+            int r0, nrows, T;
+            block_shape<kRows>(b, block_at(i, nb), tiles_ld, r0, nrows, T);
+            if (j0 < acc + T) {
+                wsum[kWarps] = i;
+                wsum[kWarps + 1] = j0 - acc;
+                break;
+            }
+            acc += T;
+        }
+    }
+    __syncthreads();
+    Span sp{0, 0, j1 - j0};
+    if (sp.n > 0) {
+        sp.b0 = (int)wsum[kWarps];
+        sp.t0 = (int)wsum[kWarps + 1];
+    }
+    return sp;
+}
+
+// Walks a span block by block: the current list position `pos` (block
+// block_at(pos, nb)), its first tile in the span `t_first`, and the items
+// still to come.
+struct SpanWalk {
+    int pos, nb, t_first;
+    int64_t left;
+    __device__ SpanWalk(const Span &sp, int nb_) : pos(sp.b0), nb(nb_), t_first(sp.t0), left(sp.n) {}
+    __device__ bool more() const { return left > 0; }
+    __device__ int blk() const { return block_at(pos, nb); }
+    // one past the last tile of the current block (T tiles) inside the span
+    __device__ int end_of(int T) const
+    {
+        return (int64_t)T < t_first + left ? T : (int)(t_first + left);
+    }
+    __device__ void next(int t_end)
+    {
+        left -= t_end - t_first;
+        pos++;
+        t_first = 0;
+    }
+};
 
 template <int QM>
 __global__ void __launch_bounds__(kThreads, 1)
 k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix,
                   float *scores, int64_t ld, int n_blocks_rows, unsigned int *st)
 {
-    constexpr bool Q8 = QM != kQBf16;  // B rows are the 64 heads of each row, no split
     constexpr bool MX = QM == kQMx;
     constexpr int kRows = rows_per_block<QM>();
-    constexpr int kRowN = row_n<QM>();
+    constexpr int kRowN = kHeads;  // B rows (accumulator columns) per query row
     constexpr int nB = mma_n<QM>();
+    using L = Lay<QM>;
+    constexpr int kStages = L::kStages;
+    constexpr uint32_t kOffStage = L::kOffStage, kOffQ = L::kOffQ, kOffW = L::kOffW,
+                       kOffWin = L::kOffWin, kOffSc = L::kOffSc, kOffSfa = L::kOffSfa,
+                       kOffSfb = L::kOffSfb, kOffNinf = L::kOffNinf, kOffBar = L::kOffBar;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
@@ -184,7 +282,6 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     griddep_launch_dependents();  // the Top-K kernel may be scheduled as CTAs finish
-    const int64_t G = gridDim.x;
     const int tiles_ld = (int)((ld + kKeys - 1) / kKeys);
 
     if (tid == 0) {
@@ -216,6 +313,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
     const int P = b.page_size;
     const int lp = 31 - __clz(P);  // page_size is a power of two >= 8
     const int seq = __ldg(b.q_seq);  // every row belongs to this sequence
+    __shared__ long long span_scratch[kThreads / 32 + 2];
+    const Span work = find_span<kRows>(b, n_blocks_rows, tiles_ld, span_scratch);
 
     if (warp == kWarpProd0 || warp == kWarpProd1) {
         // ------------------------------------------------------------ producer
@@ -226,16 +325,18 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
         volatile int *win_s = win_all + pw * 32;
         const int span = min(P, kKeys);  // keys of one page inside one tile
         int win = -1;                    // window: win_s[l] = block-table entry win + l
-        BlockWalk walk(n_blocks_rows, G);
+        SpanWalk walk(work, n_blocks_rows);
         int64_t it = 0;
         bool ok = true;
-        for (int blk = walk.next(); ok && blk >= 0; blk = walk.next()) {
+        for (; ok && walk.more(); ) {
+            const int blk = walk.blk();
             int r0, nrows, T;
             block_shape<kRows>(b, blk, tiles_ld, r0, nrows, T);
             int pmax = -1;
             for (int j = 0; j < nrows; j++)
                 pmax = max(pmax, __ldg(b.q_pos + r0 + j));
-            for (int t = 0; t < T; t++, it++) {
+            const int t1 = walk.end_of(T);
+            for (int t = walk.t_first; t < t1; t++, it++) {
                 if ((int)(it & 1) != pw)
                     continue;
                 const int stg = (int)(it % kStages);
@@ -325,19 +426,21 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                     mbar_arrive(sf);
                 }
             }
+            walk.next(t1);
         }
         cp_async_commit();
         cp_async_wait<0>();  // nothing may land after the block has moved on
     } else if (warp == kWarpMma) {
         // ----------------------------------------------------------------- MMA
         const uint32_t idesc = idesc_e4m3(kKeys, nB);
-        BlockWalk walk(n_blocks_rows, G);
+        SpanWalk walk(work, n_blocks_rows);
         int64_t it = 0;
         int bi = 0;
         bool ok = true;
-        for (int blk = walk.next(); ok && blk >= 0; blk = walk.next(), bi++) {
+        for (; ok && walk.more(); bi++) {
             int r0, nrows, T;
-            block_shape<kRows>(b, blk, tiles_ld, r0, nrows, T);
+            block_shape<kRows>(b, walk.blk(), tiles_ld, r0, nrows, T);
+            const int t1 = walk.end_of(T);
             const int p = bi & 1;
             if (!mbar_wait(qfull_bar + p, (uint32_t)(bi >> 1) & 1, st))
                 break;
@@ -353,7 +456,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                 }
                 __syncwarp();
             }
-            for (int t = 0; t < T; t++, it++) {
+            for (int t = walk.t_first; t < t1; t++, it++) {
                 const int stg = (int)(it % kStages);
                 const int g = (int)(it & 1);
                 const int64_t mg = it >> 1;  // this accumulator's use count
@@ -374,18 +477,22 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                         for (int kk = 0; kk < kDim / 32; kk++) {
                             const uint64_t ad = smem_desc(base + kOffStage + stg * kTile + kk * 32,
                                                           16, 1024, kSwizzle128B);
-                            const uint64_t bd = smem_desc(base + kOffQ + p * kTileB + kk * 32, 16,
+                            const uint64_t bd = smem_desc(base + kOffQ + p * L::kQBuf + kk * 32, 16,
                                                           1024, kSwizzle128B);
                             umma_mx_ss(dacc, ad, bd, idesc_mx_e4m3(kKeys, nB, kk), sfa, sfb,
                                        kk > 0);
                         }
                     } else {
+                        // K blocks of the B buffer: q_hi (and, for a bf16 query,
+                        // then q_lo), each against the same K block of the keys
 #pragma unroll
-                        for (int kk = 0; kk < kDim / 32; kk++) {
-                            const uint64_t ad = smem_desc(base + kOffStage + stg * kTile + kk * 32,
+                        for (int kk = 0; kk < (int)L::kQParts * (kDim / 32); kk++) {
+                            const uint64_t ad =
+                                smem_desc(base + kOffStage + stg * kTile + (kk & 3) * 32, 16, 1024,
+                                          kSwizzle128B);
+                            const uint64_t bd = smem_desc(base + kOffQ + p * L::kQBuf +
+                                                              (kk >> 2) * kTileB + (kk & 3) * 32,
                                                           16, 1024, kSwizzle128B);
-                            const uint64_t bd = smem_desc(base + kOffQ + p * kTileB + kk * 32, 16,
-                                                          1024, kSwizzle128B);
                             umma_f8_ss(dacc, ad, bd, idesc, kk > 0);
                         }
                     }
@@ -397,21 +504,62 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
             if (ok && lane == 0)
                 umma_commit(qempty_bar + p);  // the block's B operand is free once read
             __syncwarp();
+            walk.next(t1);
         }
+    } else if (warp == kWarpTail) {
+        // -------------------------------------------------------- tail writer
+        // Score columns past a block's live tiles are -inf; the CTA that
+        // scores the block's last tile writes them.  The 16-byte aligned
+        // middle of each row's tail goes by bulk copies of a -inf buffer
+        // (lane l issues chunks l, l + 32, ...), the ragged ends by plain
+        // stores.
+        float *ninf_s = reinterpret_cast<float *>(gbase + kOffNinf);
+        for (int i = lane; i < (int)(kNinfBytes / 4); i += 32)
+            ninf_s[i] = -INFINITY;
+        fence_async_smem();  // generic-proxy writes -> the copy engine's reads
+        __syncwarp();
+        constexpr int64_t kChunk = kNinfBytes / 4;  // floats per copy
+        SpanWalk walk(work, n_blocks_rows);
+        for (; walk.more();) {
+            int r0, nrows, T;
+            block_shape<kRows>(b, walk.blk(), tiles_ld, r0, nrows, T);
+            const int t1 = walk.end_of(T);
+            walk.next(t1);
+            const int64_t c0 = (int64_t)T * kKeys;
+            if (t1 != T || c0 >= ld)
+                continue;
+            for (int j = 0; j < nrows; j++) {
+                float *row = scores + (int64_t)(r0 + j) * ld;
+                int64_t a = c0;  // first 16-byte aligned column at or after c0
+                while (a < ld && ((uintptr_t)(row + a) & 15) != 0)
+                    a++;
+                const int64_t nv = (ld - a) & ~(int64_t)3;  // floats of the aligned middle
+                if (lane < a - c0)
+                    row[c0 + lane] = -INFINITY;
+                if (lane < ld - (a + nv))
+                    row[a + nv + lane] = -INFINITY;
+                for (int64_t c = (int64_t)lane * kChunk; c < nv; c += 32 * kChunk)
+                    bulk_s2g(row + a + c, smem_u32(ninf_s),
+                             (uint32_t)(4 * (nv - c < kChunk ? nv - c : kChunk)));
+            }
+        }
+        bulk_commit();
+        bulk_wait<0>();  // every copy done before the block exits
     } else if (warp >= kWarpPrep0 && warp < kWarpEpi0) {
         // -------------------------------------------------------------- q-prep
         // Thread pt prepares dims [64 half, +64) of head h of every row.
         const int pt = tid - kWarpPrep0 * 32;
         const int h = pt >> 1, half = pt & 1;
-        BlockWalk walk(n_blocks_rows, G);
+        SpanWalk walk(work, n_blocks_rows);
         int bi = 0;
-        for (int blk = walk.next(); blk >= 0; blk = walk.next(), bi++) {
+        for (; walk.more(); bi++) {
             int r0, nrows, T;
-            block_shape<kRows>(b, blk, tiles_ld, r0, nrows, T);
+            block_shape<kRows>(b, walk.blk(), tiles_ld, r0, nrows, T);
+            walk.next(walk.end_of(T));
             const int p = bi & 1;
             if (bi >= 2 && !mbar_wait(qempty_bar + p, (uint32_t)((bi - 2) >> 1) & 1, st))
                 break;
-            const uint32_t qb = base + kOffQ + p * kTileB;
+            const uint32_t qb = base + kOffQ + p * L::kQBuf;
             if constexpr (MX) {
                 // dims [64 half, +64) of head h of each row = MX groups 2 half,
                 // 2 half + 1; B row n = j * 64 + h
@@ -486,7 +634,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                         w_s[(p * kRows + j) * kHeads + h] = have ? __ldg(ix.w + rh) : 0.f;
                     }
                 }
-            } else if constexpr (Q8) {
+            } else if constexpr (QM == kQFp8) {
                 // stored FP8 query: codes as they are, the scale joins the weight
                 for (int j = 0; j < kRows; j++) {
                     const bool have = j < nrows;
@@ -561,9 +709,10 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                             lo[jj] = lw;
                         }
                         const uint32_t u = (uint32_t)(half * 4 + c);
+                        // q_hi into the first K half, q_lo into the second
                         st_shared_v4(qb + sw128_offset(j * kRowN + h, u), hi[0], hi[1], hi[2],
                                      hi[3]);
-                        st_shared_v4(qb + sw128_offset(j * kRowN + kHeads + h, u), lo[0], lo[1],
+                        st_shared_v4(qb + kTileB + sw128_offset(j * kRowN + h, u), lo[0], lo[1],
                                      lo[2], lo[3]);
                     }
                     if (half == 0)
@@ -573,11 +722,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
             }
             fence_async_smem();
             mbar_arrive(qfull_bar + p);
-            // score columns past the block's live tiles are -inf
-            const int64_t c0 = (int64_t)T * kKeys;
-            for (int j = 0; j < nrows; j++)
-                for (int64_t c = c0 + pt; c < ld; c += 128)
-                    scores[(int64_t)(r0 + j) * ld + c] = -INFINITY;
+
         }
     } else if (warp >= kWarpEpi0) {
         // ------------------------------------------------------------ epilogue
@@ -586,13 +731,15 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
         const int g = (warp - kWarpEpi0) >> 2;
         const int et = (tid - kWarpEpi0 * 32) & 127;  // key row = TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        BlockWalk walk(n_blocks_rows, G);
+        SpanWalk walk(work, n_blocks_rows);
         int64_t it = 0;
         int bi = 0;
         bool ok = true;
-        for (int blk = walk.next(); ok && blk >= 0; blk = walk.next(), bi++) {
+        for (; ok && walk.more(); bi++) {
             int r0, nrows, T;
-            block_shape<kRows>(b, blk, tiles_ld, r0, nrows, T);
+            block_shape<kRows>(b, walk.blk(), tiles_ld, r0, nrows, T);
+            const int t0 = walk.t_first, t1 = walk.end_of(T);
+            walk.next(t1);
             const int p = bi & 1;
             int pos[kRows];
 #pragma unroll
@@ -600,7 +747,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                 pos[j] = j < nrows ? __ldg(b.q_pos + r0 + j) : -1;
             if (!mbar_wait(qfull_bar + p, (uint32_t)(bi >> 1) & 1, st))
                 break;
-            for (int t = 0; t < T; t++, it++) {
+            for (int t = t0; t < t1; t++, it++) {
                 if ((int)(it & 1) != g)
                     continue;
                 const int64_t kit = it >> 1;
@@ -619,21 +766,15 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                 tc_fence_after();
                 const int s = t * kKeys + et;
                 const uint32_t acc = tmem + g * nB + lane_off;
-                // The accumulator is read in 32-register pieces (an FP8 query:
-                // 32 heads of one row; a bf16 query: 16 heads' q_hi and q_lo
-                // columns), each piece's load issued before the previous
-                // piece is reduced.
-                constexpr int kPH = Q8 ? 32 : 16;          // heads per piece
+                // The accumulator is read in pieces of 32 heads of one row,
+                // each piece's load issued before the previous piece is
+                // reduced; the accumulator is released as soon as the last
+                // piece has landed in registers.
+                constexpr int kPH = 32;                    // heads per piece
                 constexpr int kPPR = kHeads / kPH;         // pieces per row
                 constexpr int kPieces = kRows * kPPR;
                 auto issue = [&](int pc, uint32_t(&v)[32]) {
-                    const uint32_t col = (uint32_t)((pc / kPPR) * kRowN + (pc % kPPR) * kPH);
-                    if constexpr (Q8) {
-                        tmem_ld32(acc + col, v);
-                    } else {
-                        tmem_ld16(acc + col, v);
-                        tmem_ld16(acc + col + kHeads, v + 16);
-                    }
+                    tmem_ld32(acc + (uint32_t)((pc / kPPR) * kRowN + (pc % kPPR) * kPH), v);
                 };
                 float sum[kRows];
                 // partial head sums in two packed pairs (0.0f has all bits 0)
@@ -646,46 +787,32 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                     uint32_t(&nxt)[32] = (pc & 1) ? va : vb;
                     tmem_wait_ld();
                     tmem_regs_ready(cur);
-                    if (pc + 1 < kPieces)
+                    if (pc + 1 < kPieces) {
                         issue(pc + 1, nxt);
+                    } else {
+                        tc_fence_before();
+                        mbar_arrive(cempty_bar + g);
+                    }
                     const int j = pc / kPPR, hq = pc % kPPR;
                     const float4 *w4 =
                         reinterpret_cast<const float4 *>(w_s + (p * kRows + j) * kHeads + hq * kPH);
 #pragma unroll
                     for (int i = 0; i < kPH; i += 4) {
                         const float4 wv = w4[i >> 2];
-                        float lg[4];
-                        if constexpr (Q8) {
-#pragma unroll
-                            for (int k = 0; k < 4; k++)
-                                lg[k] = __uint_as_float(cur[i + k]);
-                        } else {
-                            // logit = q_hi term + q_lo term, two heads per add
-#pragma unroll
-                            for (int k = 0; k < 4; k += 2) {
-                                const float2 s2 = f32x2_unpack(f32x2_add(
-                                    f32x2_pack(__uint_as_float(cur[i + k]),
-                                               __uint_as_float(cur[i + k + 1])),
-                                    f32x2_pack(__uint_as_float(cur[16 + i + k]),
-                                               __uint_as_float(cur[16 + i + k + 1]))));
-                                lg[k] = s2.x;
-                                lg[k + 1] = s2.y;
-                            }
-                        }
                         // w_h * ReLU(logit), two heads per fma
                         f32x2_fma(p01, f32x2_pack(wv.x, wv.y),
-                                  f32x2_pack(fmaxf(lg[0], 0.f), fmaxf(lg[1], 0.f)));
+                                  f32x2_pack(fmaxf(__uint_as_float(cur[i]), 0.f),
+                                             fmaxf(__uint_as_float(cur[i + 1]), 0.f)));
                         f32x2_fma(p23, f32x2_pack(wv.z, wv.w),
-                                  f32x2_pack(fmaxf(lg[2], 0.f), fmaxf(lg[3], 0.f)));
+                                  f32x2_pack(fmaxf(__uint_as_float(cur[i + 2]), 0.f),
+                                             fmaxf(__uint_as_float(cur[i + 3]), 0.f)));
                     }
                     if (hq == kPPR - 1) {
-                        const float2 a = f32x2_unpack(p01), c = f32x2_unpack(p23);
-                        sum[j] = (a.x + a.y) + (c.x + c.y);
+                        const float2 x01 = f32x2_unpack(p01), x23 = f32x2_unpack(p23);
+                        sum[j] = (x01.x + x01.y) + (x23.x + x23.y);
                         p01 = p23 = 0;
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(cempty_bar + g);
                 if (s < ld) {
 #pragma unroll
                     for (int j = 0; j < kRows; j++)
@@ -724,13 +851,16 @@ cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, floa
         cudaError_t r = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(k_indexer_prefill<kQBf16>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)Lay<kQBf16>::kSmemBytes);
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(k_indexer_prefill<kQFp8>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)Lay<kQFp8>::kSmemBytes);
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(k_indexer_prefill<kQMx>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)Lay<kQMx>::kSmemBytes);
         err_of[dev] = r;
     });
     if (err_of[dev] != cudaSuccess)
@@ -745,17 +875,18 @@ cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, floa
     const int rows = qm == kQMx ? rows_per_block<kQMx>()
                                 : (qm == kQFp8 ? rows_per_block<kQFp8>() : rows_per_block<kQBf16>());
     const int nb = (b.n_q + rows - 1) / rows;
-    const int64_t npairs = (nb + 1) / 2;
-    const int64_t grid = std::min<int64_t>(npairs, (int64_t)sms_of[dev]);
+    // every SM takes an equal share of the (block, tile) items
+    const int64_t tiles_ld = (ld + kKeys - 1) / kKeys;
+    const int64_t grid = std::min<int64_t>((int64_t)nb * tiles_ld, (int64_t)sms_of[dev]);
     count_launch();
     if (qm == kQMx)
-        k_indexer_prefill<kQMx><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
+        k_indexer_prefill<kQMx><<<(unsigned)grid, kThreads, Lay<kQMx>::kSmemBytes, s>>>(tmap, b, ix, scores,
                                                                              ld, nb, st);
     else if (qm == kQFp8)
-        k_indexer_prefill<kQFp8><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
+        k_indexer_prefill<kQFp8><<<(unsigned)grid, kThreads, Lay<kQFp8>::kSmemBytes, s>>>(tmap, b, ix, scores,
                                                                               ld, nb, st);
     else
-        k_indexer_prefill<kQBf16><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(tmap, b, ix, scores,
+        k_indexer_prefill<kQBf16><<<(unsigned)grid, kThreads, Lay<kQBf16>::kSmemBytes, s>>>(tmap, b, ix, scores,
                                                                                ld, nb, st);
     return cudaGetLastError();
 }

@@ -520,6 +520,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Contiguous shared -> global copy by the bulk-copy engine, tracked in the
+// issuing thread's bulk group (bulk_commit / bulk_wait).  dst and src 16-byte
+// aligned, bytes a multiple of 16; the source must be visible to the async
+// proxy (fence_async_smem after writing it).
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared described by a tensor map (the map
 // may apply a shared-memory swizzle); completion as transaction bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t c0, int32_t c1,

@@ -165,10 +165,10 @@ def _prefill_rows(n_q, rows_per_block, k_top, n_pairs=128):
 
 def test_causal_prefill_full_size(si):
     """Causal prefill of 16384 rows: rows below K = 2048 keep every position,
-    later rows select.  The bf16 query takes blocks of two rows."""
+    later rows select.  The bf16 query takes blocks of four rows."""
     wl = synth.make("c2")
     assert wl.n_q == 16384
-    rows = _prefill_rows(wl.n_q, 2, wl.K)
+    rows = _prefill_rows(wl.n_q, 4, wl.K)
     assert len(rows) >= 256
     _run(si, wl, rows=rows)
 
