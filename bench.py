@@ -649,6 +649,7 @@ def run_si(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
+        """The per-kernel pass: the three calls one by one."""
         if ev:
             ev[0].record(stream)
         si.indexer_scores(b, ix, scores, ws, stream)
@@ -661,17 +662,26 @@ def run_si(args):
         if ev:
             ev[3].record(stream)
 
+    ws_step = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, ix, at, K), dev)
+
+    def fused_step():
+        """The timed step: the whole path in one call on resident inputs."""
+        si.fused_decode(b, ix, at, K, idx, out, ws_step, stream=stream)
+
     for _ in range(max(3, args.warmup)):
         step()
+        fused_step()
     torch.cuda.synchronize(dev)
     assert si.workspace_status(ws, stream) == 0
+    assert si.workspace_status(ws_step, stream) == 0
 
-    # Two timed passes over K steps each, L2 flushed before every step.  The
-    # step pass brackets each step with two events only, so that the three
-    # launches follow one another as they do in use (the Top-K and attention
-    # kernels start while their predecessor drains); it gives `value`.  The
-    # kernel pass puts an event between the launches for the per-kernel
-    # breakdown and the roofline.
+    # Timed passes over K steps each, L2 flushed before every step.  The step
+    # pass times si_fused_decode, the whole path in one call (scores, Top-K --
+    # inside the indexer where the fused selection applies -- and attention),
+    # bracketed by two events; it gives `value`.  The kernel pass runs the
+    # three entry points one by one with an event between the launches for
+    # the per-kernel breakdown and the roofline; the select pass times
+    # si_indexer_topk (scores + Top-K as one operator) alone.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
@@ -683,7 +693,7 @@ def run_si(args):
     for i in range(args.steps):
         flush.fill_(i & 0xFF)            # evict the previous step's data from L2
         sevs[i][0].record(stream)
-        step()
+        fused_step()
         sevs[i][1].record(stream)
     torch.cuda.synchronize(dev)
     launches = si.launch_count() - launches0
@@ -696,9 +706,23 @@ def run_si(args):
     torch.cuda.synchronize(dev)
     assert si.workspace_status(ws, stream) == 0
 
+    assert si.workspace_status(ws_step, stream) == 0
     t_k = {"indexer": [e[0].elapsed_time(e[1]) for e in evs],
            "topk": [e[1].elapsed_time(e[2]) for e in evs],
            "attn": [e[2].elapsed_time(e[3]) for e in evs]}
+    # select pass: scores + Top-K as one operator (si_indexer_topk)
+    ws_s = si.alloc_workspace(si.workspace_size(si.OP_SELECT, b, ix, None, K), dev)
+    si.indexer_topk(b, ix, K, idx, ws_s, stream)
+    selv = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        selv[i][0].record(stream)
+        si.indexer_topk(b, ix, K, idx, ws_s, stream)
+        selv[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    assert si.workspace_status(ws_s, stream) == 0
+    sel_ms = sum(e[0].elapsed_time(e[1]) for e in selv) / args.steps
+    del ws_s
     ms = sum(e[0].elapsed_time(e[1]) for e in sevs) / args.steps
     ms_max = max_over_ranks(ms, world, dev)
     value = whole_job_rate(world, n_q, ms_max)
@@ -772,7 +796,7 @@ def run_si(args):
     prefill = None if args.no_prefill else prefill_indexer(si, dev, args.steps)
     others = {}
     if not args.no_other_workloads and args.workload == "c1" and not (args.kv_fp8 or args.kv_fp4):
-        del dw, ws, scores, idx, out, flush
+        del dw, ws, ws_step, scores, idx, out, flush
         torch.cuda.empty_cache()
         others = {"long_context": workload_record(si, dev, "c3", args.steps, args.warmup),
                   "mixed": workload_record(si, dev, "c4", args.steps, args.warmup),
@@ -795,12 +819,14 @@ def run_si(args):
                                 f"{'e4m3 cache + fp32 scale per 128-entry tile, bf16 q' if args.kv_fp8 else 'e2m1 cache + fp32 scale per 16-entry block, bf16 q' if args.kv_fp4 else 'bf16'}, "
                                 f"fp32 accumulate, {OUT_DTYPE} out",
                    "page": wl.page, "l2": "flushed between steps (512 MiB write)",
-                   "step": "si_indexer_scores + si_topk + si_sparse_attn",
+                   "step": "si_fused_decode (scores, Top-K, attention in one call) on "
+                           "resident inputs; kernels_ms from the three calls one by one",
                    "parallelism": f"dp{world} (independent requests per rank)"},
         "hbm": {"algorithmic_bytes_per_step": total_bytes, "achieved_gbs": step_gbs,
                 "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                 "frac_of_measured": step_gbs / peaks["hbm_gbs"]},
         "kernels_ms": mean_k,
+        "indexer_topk_ms": sel_ms,
         "kernels": {k: v[0] for k, v in _kernel_of(wl).items()},
         "clocks": clk,
         "e2e": e2e,

@@ -184,7 +184,8 @@ typedef enum si_op {
     SI_OP_INDEXER = 0,
     SI_OP_TOPK = 1,
     SI_OP_ATTN = 2,
-    SI_OP_FUSED = 3
+    SI_OP_FUSED = 3,
+    SI_OP_SELECT = 4  /* si_indexer_topk */
 } si_op;
 
 /* Bytes of workspace the operation `op` wants for this batch (the status
@@ -229,6 +230,16 @@ si_status si_topk(const si_batch *b, const float *scores, int64_t ld_scores, int
 si_status si_sparse_attn(const si_batch *b, const si_attention *at, const int32_t *idx,
                          int32_t k_top, void *out, si_dtype out_dtype, float *lse, void *ws,
                          size_t ws_bytes, void *stream);
+
+/* Section 4.1's fused indexer operator on its own (the indexer prolog of
+ * section 4.3 ends in idx = fused_topk(q8, k, g)): scores, head weighting and
+ * Top-K for every query row, the scores living only in the workspace, a strip
+ * of rows at a time, exactly as in si_fused_decode.  idx receives what
+ * si_indexer_scores followed by si_topk would give.  ws: at least
+ * si_workspace_min(SI_OP_SELECT, ...) bytes (si_workspace_size(SI_OP_SELECT,
+ * ...) scores every row in one strip, up to 64 MiB of scores). */
+si_status si_indexer_topk(const si_batch *b, const si_indexer *ix, int32_t k_top, int32_t *idx,
+                          void *ws, size_t ws_bytes, void *stream);
 
 /* The whole path in one call (section 4.1 fused indexer + 4.2 gather
  * attention): scores -> Top-K -> attention for every query row.  Scores

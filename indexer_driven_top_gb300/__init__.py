@@ -25,7 +25,7 @@ LIB_PATH = _build.LIB
 
 F32, BF16, E4M3, E2M1, MXE4M3 = 0, 1, 2, 3, 4
 DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "e2m1": E2M1, "mxe4m3": MXE4M3}
-OP_INDEXER, OP_TOPK, OP_ATTN, OP_FUSED = 0, 1, 2, 3
+OP_INDEXER, OP_TOPK, OP_ATTN, OP_FUSED, OP_SELECT = 0, 1, 2, 3, 4
 DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_INDEX, DEVFLAG_TIMEOUT, DEVFLAG_RANGE = 1, 2, 4, 8
 
 
@@ -92,6 +92,7 @@ def load() -> ctypes.CDLL:
         "si_version": (I32, []),
         "si_launch_count": (ctypes.c_uint64, []),
         "si_quant_mxfp8": (ctypes.c_int, [P, ctypes.c_int, I64, I32, P, P, P]),
+        "si_indexer_topk": (ctypes.c_int, [B, IX, I32, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -107,7 +108,8 @@ EXPORTED = ("si_workspace_size", "si_workspace_min", "si_indexer_scores", "si_to
             "si_sparse_attn", "si_fused_decode", "si_fused_decode_noalloc",
             "si_workspace_size_cand", "si_indexer_topk_cand", "si_workspace_status",
             "si_status_string",
-            "si_last_error", "si_version", "si_launch_count", "si_quant_mxfp8")
+            "si_last_error", "si_version", "si_launch_count", "si_quant_mxfp8",
+            "si_indexer_topk")
 
 
 def _check(status: int):
@@ -271,6 +273,14 @@ def sparse_attn(b: Batch, at: Attention, idx: torch.Tensor, k_top: int, out: tor
     _check(load().si_sparse_attn(ctypes.byref(cb), ctypes.byref(ca), _ptr(idx), k_top, _ptr(out),
                                  _out_dtype(out), _ptr(lse), _ptr(ws), ws.numel(),
                                  _stream(stream)))
+
+
+def indexer_topk(b: Batch, ix: Indexer, k_top: int, idx: torch.Tensor, ws: torch.Tensor,
+                 stream=None):
+    """Section 4.1's fused indexer operator: scores and Top-K in one call, the
+    scores kept in the workspace (si_indexer_topk)."""
+    _check(load().si_indexer_topk(ctypes.byref(b.c()), ctypes.byref(ix.c()), k_top, _ptr(idx),
+                                  _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def fused_decode(b: Batch, ix: Indexer, at: Attention, k_top: int, idx: torch.Tensor,

@@ -325,7 +325,7 @@ size_t ws_need(si_op op, const si_batch *b, const si_indexer *ix, const si_atten
     (void)ix;
     size_t n = si::kStatusBytes;
     size_t extra = 0;
-    if (op == SI_OP_FUSED && b->n_q > 0) {
+    if ((op == SI_OP_FUSED || op == SI_OP_SELECT) && b->n_q > 0) {
         const size_t row_bytes = (size_t)scores_ld(b) * sizeof(float);
         size_t rows = minimal ? 1 : (size_t)b->n_q;
         if (!minimal && rows * row_bytes > kFusedCap)
@@ -547,6 +547,55 @@ si_status si_sparse_attn(const si_batch *b, const si_attention *at, const int32_
                     status_word(ws), (cudaStream_t)stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Scores and Top-K strip by strip (section 4.1's fused operator); the strip
+// starts at ws + *head on return.
+si_status run_indexer_topk(const si_batch *b, const si_indexer *ix, int32_t k_top, int32_t *idx,
+                           void *ws, size_t ws_bytes, cudaStream_t s, size_t *head_out)
+{
+    si_status st = SI_OK;
+    unsigned int *stw = status_word(ws);
+    const int64_t ld = scores_ld(b);
+    const size_t row_bytes = (size_t)ld * sizeof(float);
+    const size_t head = si::kStatusBytes;
+    float *scores = reinterpret_cast<float *>(static_cast<char *>(ws) + head);
+    const int64_t strip = (int64_t)((ws_bytes - head) / row_bytes);
+    for (int64_t r0 = 0; r0 < b->n_q; r0 += strip) {
+        const int32_t n = (int32_t)std::min<int64_t>(strip, b->n_q - r0);
+        const si_batch sb = row_slice(*b, (int32_t)r0, n);
+        const si_indexer si_ = indexer_slice(*ix, (int32_t)r0);
+        if ((st = run_indexer(sb, si_, scores, ld, stw, s)) != SI_OK)
+            return st;
+        if ((st = run_topk(sb, scores, ld, k_top, idx + r0 * k_top, stw, s)) != SI_OK)
+            return st;
+    }
+    *head_out = head;
+    return SI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+si_status si_indexer_topk(const si_batch *b, const si_indexer *ix, int32_t k_top, int32_t *idx,
+                          void *ws, size_t ws_bytes, void *stream)
+{
+    si_status st = check_batch(b);
+    if (st != SI_OK || b->n_q == 0)
+        return st;
+    if ((st = check_indexer(ix)) != SI_OK || (st = check_k(k_top)) != SI_OK)
+        return st;
+    if (!idx)
+        return fail(SI_ERR_INVALID_ARG, "idx is NULL");
+    if ((st = check_ws(ws, ws_bytes, ws_need(SI_OP_SELECT, b, ix, nullptr, k_top, true))) != SI_OK)
+        return st;
+    size_t head = 0;
+    return run_indexer_topk(b, ix, k_top, idx, ws, ws_bytes, (cudaStream_t)stream, &head);
+}
+
 si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_attention *at,
                           int32_t k_top, int32_t *idx, void *out, si_dtype out_dtype,
                           float *lse, void *ws, size_t ws_bytes, void *stream)
@@ -557,24 +606,13 @@ si_status si_fused_decode(const si_batch *b, const si_indexer *ix, const si_atte
     if ((st = check_ws(ws, ws_bytes, ws_need(SI_OP_FUSED, b, ix, at, k_top, true))) != SI_OK)
         return st;
     cudaStream_t s = (cudaStream_t)stream;
-    unsigned int *stw = status_word(ws);
-    const int64_t ld = scores_ld(b);
-    const size_t row_bytes = (size_t)ld * sizeof(float);
-    float *scores = reinterpret_cast<float *>(static_cast<char *>(ws) + si::kStatusBytes);
-    const int64_t strip = (int64_t)((ws_bytes - si::kStatusBytes) / row_bytes);
-    for (int64_t r0 = 0; r0 < b->n_q; r0 += strip) {
-        const int32_t n = (int32_t)std::min<int64_t>(strip, b->n_q - r0);
-        const si_batch sb = row_slice(*b, (int32_t)r0, n);
-        const si_indexer si_ = indexer_slice(*ix, (int32_t)r0);
-        if ((st = run_indexer(sb, si_, scores, ld, stw, s)) != SI_OK)
-            return st;
-        if ((st = run_topk(sb, scores, ld, k_top, idx + r0 * k_top, stw, s)) != SI_OK)
-            return st;
-    }
+    size_t head = 0;
+    if ((st = run_indexer_topk(b, ix, k_top, idx, ws, ws_bytes, s, &head)) != SI_OK)
+        return st;
     // the score strip is free once every Top-K has run: it may hold the
     // attention's split partials
-    return run_attn(*b, *at, idx, k_top, out, out_dtype, lse, scores,
-                    ws_bytes - si::kStatusBytes, stw, s);
+    return run_attn(*b, *at, idx, k_top, out, out_dtype, lse, static_cast<char *>(ws) + head,
+                    ws_bytes - head, status_word(ws), s);
 }
 
 si_status si_workspace_status(const void *ws, uint32_t *flags, void *stream)

@@ -302,14 +302,31 @@ __device__ __forceinline__ bool dequant16_e2m1(uint2 c, float sc, uint32_t dst0,
     return bad;
 }
 
-// 16 bytes of bf16 -> f16 in place; returns true if a value left the f16 range.
-__device__ __forceinline__ bool to_f16_inplace(uint32_t a)
+// 16 bytes of bf16 -> f16 in place.
+__device__ __forceinline__ void to_f16_inplace(uint32_t a)
 {
     const uint4 x = ld_shared_v4(a);
-    const uint32_t y0 = bf16x2_to_f16x2(x.x), y1 = bf16x2_to_f16x2(x.y), y2 = bf16x2_to_f16x2(x.z),
-                   y3 = bf16x2_to_f16x2(x.w);
-    st_shared_v4(a, y0, y1, y2, y3);
-    return f16x2_nonfinite(y0) | f16x2_nonfinite(y1) | f16x2_nonfinite(y2) | f16x2_nonfinite(y3);
+    st_shared_v4(a, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                 bf16x2_to_f16x2(x.w));
+}
+
+// The same, folding the inputs' magnitude bits into `mag` (a per-half
+// maximum), which bf16_beyond_f16 tests once at the end.
+__device__ __forceinline__ void to_f16_inplace(uint32_t a, uint32_t &mag)
+{
+    const uint4 x = ld_shared_v4(a);
+    st_shared_v4(a, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                 bf16x2_to_f16x2(x.w));
+    mag = __vmaxu2(mag, __vmaxu2(__vmaxu2(x.x & 0x7FFF7FFFu, x.y & 0x7FFF7FFFu),
+                                 __vmaxu2(x.z & 0x7FFF7FFFu, x.w & 0x7FFF7FFFu)));
+}
+
+// A bf16 magnitude of 2^16 or more (bits 0x4780 and up, infinities and NaN
+// included) has no f16 form; every smaller bf16 does (the largest bf16 below
+// 2^16 is 65280 <= 65504).  `mag`: per-half maxima of magnitude bits.
+__device__ __forceinline__ bool bf16_beyond_f16(uint32_t mag)
+{
+    return (mag & 0xFFFFu) >= 0x4780u || (mag >> 16) >= 0x4780u;
 }
 
 // 4-byte global -> shared copy, asynchronous like cp_async_16 (zeros when
@@ -836,10 +853,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                 // f16 too (one operand type per MMA; exact for |q| >= 2^-14)
                 mbar_wait(bars + B_QREADY, 0, st);
                 const int st_ = tid - kWarpSoft0 * 32;
-                bool range = false;
+                uint32_t mag = 0;
                 for (int i = st_; i < (int)(kQChunks * kChunk / 16); i += kSoftmax)
-                    range |= to_f16_inplace(base + kOffQ + i * 16);
-                if (range)
+                    to_f16_inplace(base + kOffQ + i * 16, mag);
+                if (bf16_beyond_f16(mag))
                     raise_flag(st, SI_DEVFLAG_RANGE);
                 fence_async_smem();
                 mbar_arrive(bars + B_QCONV);
@@ -1113,8 +1130,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                 if (!mbar_wait(bars + B_FULL + slot, (uint32_t)(g / kRingV) & 1, st))
                     break;
                 const uint32_t src = base + kOffRingV + slot * kGroup;
+                // (a value beyond the f16 range becomes inf here and makes O
+                // non-finite; the epilogue checks O once per row)
                 for (int i = ct; i < (int)(kGroup / 16); i += kConverters)
-                    range |= to_f16_inplace(src + i * 16);
+                    to_f16_inplace(src + i * 16);
                 fence_async_smem();
                 mbar_arrive(bars + B_CONV + slot);
             }
@@ -1184,6 +1203,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
             const int orow = cl * kHeads + quarter * 32;
             const bool f32 = out_dtype == SI_F32;
             const int nblk = f32 ? 8 : 4;  // 32 fp32 or 64 bf16 columns per block
+            // O is finite unless a value left the f16 range in the conversion
+            // (inf times any weight, zero included, stays inf or becomes NaN):
+            // the maximum of the magnitude bits of every O entry read
+            uint32_t omag = 0;
 #pragma unroll 1
             for (int k = 0; k < nblk; k++) {
                 const uint32_t buf = stage + (uint32_t)(k % kEpiBufs) * 4096u;
@@ -1199,6 +1222,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                     if (good) {
                         tmem_ld32(tmem + lane_off + col0, w);
                         tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i++)
+                            omag = max(omag, w[i] & 0x7FFFFFFFu);
                     }
 #pragma unroll
                     for (int i = 0; i < 32; i++)
@@ -1212,6 +1238,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
                         if (good) {
                             tmem_ld32(tmem + lane_off + col0 + 32 * hh, v);
                             tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; i++)
+                                omag = max(omag, v[i] & 0x7FFFFFFFu);
                         }
 #pragma unroll
                         for (int i = 0; i < 16; i++)
@@ -1236,6 +1265,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUte
             }
             if (lane == 0)
                 bulk_wait<0>();
+            if (__any_sync(0xffffffffu, omag >= 0x7F800000u) && lane == 0)
+                raise_flag(st, SI_DEVFLAG_RANGE);
             __syncwarp();
         }
     }

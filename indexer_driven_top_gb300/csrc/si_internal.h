@@ -39,8 +39,8 @@ cudaError_t launch_indexer_tc_cand(const si_batch &b, const si_indexer &ix, cons
                                    unsigned int *st, cudaStream_t s);
 
 // Tensor-core indexer for query rows that all belong to one sequence (a
-// causal prefill or a prefill chunk): blocks of two (bf16 q) or four (FP8 q)
-// rows share each key tile.  Same operand conditions as above; the caller
+// causal prefill or a prefill chunk): blocks of four rows (bf16 or FP8 q) or
+// three (MXFP8) share each key tile.  Same operand conditions as above; the caller
 // guarantees the single sequence.
 cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, float *scores,
                                    int64_t ld, unsigned int *st, cudaStream_t s);

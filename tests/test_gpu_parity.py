@@ -314,6 +314,15 @@ def test_value_beyond_f16_range_raises_flag(si):
                                                   big.attention, 2048))
         si.fused_decode(big.batch, big.indexer, big.attention, 2048, idx, out, ws)
         assert si.workspace_status(ws) == si.DEVFLAG_RANGE, entry
+    # the boundary: 65280 (the largest bf16 below 2^16) has an f16 form,
+    # 65536 has none
+    for value, flag in ((65280.0, 0), (-65280.0, 0), (65536.0, si.DEVFLAG_RANGE),
+                        (-65536.0, si.DEVFLAG_RANGE)):
+        edge = si.upload(_large_entry(wl, 1, 7, 100, value))
+        ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, edge.batch, edge.indexer,
+                                                  edge.attention, 2048))
+        si.fused_decode(edge.batch, edge.indexer, edge.attention, 2048, idx, out, ws)
+        assert si.workspace_status(ws) == flag, value
 
 
 def test_empty_batch_is_noop(si):
@@ -366,3 +375,57 @@ def test_tensor_core_indexer_bad_block(si):
     ok[1, 128:192] = False
     fin = np.isfinite(o) & ok
     assert np.abs(g[fin] - o[fin]).max() <= 1e-5 * np.abs(o[fin]).max()
+
+
+def test_fused_workspace_reused_across_batch_shapes(si):
+    """One workspace serves fused calls on batches of other shapes in turn
+    (their score strips overlap): every result equals the separate indexer +
+    Top-K of the same batch."""
+    wls = [synth.make("c1", batch=5, ctx_list=[3000, 130, 2048, 4097, 777], K=512),
+           synth.make("c1", batch=9, ctx=1500, K=256, seed=7),
+           synth.make("c1", batch=5, ctx_list=[3000, 130, 2048, 4097, 777], K=512)]
+    size = max(si.workspace_size(si.OP_FUSED, d.batch, d.indexer, d.attention, d.k_top)
+               for d in (si.upload(w) for w in wls))
+    ws = si.alloc_workspace(size)
+    for wl in wls:
+        dw = si.upload(wl)
+        b = dw.batch
+        ref_sc = torch.empty((dw.n_q, b.max_ctx), dtype=torch.float32, device="cuda")
+        ref_idx = torch.empty((dw.n_q, dw.k_top), dtype=torch.int32, device="cuda")
+        ws2 = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, dw.indexer, dw.attention,
+                                                   dw.k_top))
+        si.indexer_scores(b, dw.indexer, ref_sc, ws2)
+        si.topk(b, ref_sc, dw.k_top, ref_idx, ws2)
+        idx = torch.empty_like(ref_idx)
+        out = torch.empty((dw.n_q, wl.Hq, wl.Dv), dtype=torch.float32, device="cuda")
+        for _ in range(2):
+            si.fused_decode(b, dw.indexer, dw.attention, dw.k_top, idx, out, ws)
+            assert si.workspace_status(ws) == 0
+            assert torch.equal(idx, ref_idx)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("c1", dict(batch=5, ctx_list=[3000, 130, 2048, 4097, 777], K=512)),  # select in the indexer
+    ("c3", dict(batch=2, ctx=9000, K=256)),                               # rows over 8192
+    ("c4", dict(n_req=6, n_prefill=2, chunk=200, ctx_lo=300, ctx_hi=2500, K=256)),  # planned
+    ("c0", {}),                                                           # generic kernels
+])
+def test_indexer_topk_equals_scores_then_topk(si, name, over):
+    """si_indexer_topk (section 4.1's fused operator) gives exactly the Top-K
+    of si_indexer_scores followed by si_topk, with the minimal and the full
+    workspace."""
+    wl = synth.make(name, **over)
+    dw = si.upload(wl)
+    b = dw.batch
+    ws = si.alloc_workspace(si.workspace_size(si.OP_FUSED, b, dw.indexer, dw.attention, dw.k_top))
+    sc = torch.empty((dw.n_q, b.max_ctx), dtype=torch.float32, device="cuda")
+    ref = torch.empty((dw.n_q, dw.k_top), dtype=torch.int32, device="cuda")
+    si.indexer_scores(b, dw.indexer, sc, ws)
+    si.topk(b, sc, dw.k_top, ref, ws)
+    for nbytes in (si.workspace_size(si.OP_SELECT, b, dw.indexer, None, dw.k_top),
+                   si.workspace_min(si.OP_SELECT, b, dw.indexer, None, dw.k_top)):
+        ws2 = si.alloc_workspace(nbytes)
+        idx = torch.empty_like(ref)
+        si.indexer_topk(b, dw.indexer, dw.k_top, idx, ws2)
+        assert si.workspace_status(ws2) == 0
+        assert torch.equal(idx, ref)
