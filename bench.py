@@ -177,7 +177,12 @@ def whole_job_rate(world: int, n_q: int, ms_per_step: float) -> float:
 
 # Workload names of the committed ncu captures (profiles/*.md).
 PROFILE_WORKLOAD = {"c1": "decode b64 ctx8192", "c3": "decode b16 ctx131072",
-                    "c1:kv8": "decode b64 ctx8192 fp8 kv", "c1:kv4": "decode b64 ctx8192 fp4 kv"}
+                    "c1:kv8": "decode b64 ctx8192 fp8 kv", "c1:kv4": "decode b64 ctx8192 fp4 kv",
+                    "c1:mx": "decode b64 ctx8192 mxfp8 indexer",
+                    "c4": "mixed 28 decode + 4 chunks"}
+# The step whose operand format each variant changes; the other kernels of a
+# variant run as on the plain workload.
+VARIANT_KERNEL = {":kv8": "attn", ":kv4": "attn", ":mx": "indexer"}
 
 
 def _kernel_traffic(kernel: str, source: str, workload: str):
@@ -239,7 +244,9 @@ def roofline_of(kernel, wl, algo, ms, peaks, long_step, variant=""):
                        + (" x 2 for FP8)" if kernel == "indexer" else ")")}
     roof = dict(ten if ten["frac"] > hbm["frac"] else hbm)
     roof.update({"kernel": name,
-                 "traffic": _kernel_traffic(name, src, wl.name + variant) if roof["bound"] == "hbm" else None,
+                 "traffic": _kernel_traffic(
+                     name, src, wl.name + (variant if VARIANT_KERNEL.get(variant) == kernel else ""))
+                 if roof["bound"] == "hbm" else None,
                  "algorithmic_bytes_per_launch": nbytes, "algorithmic_flop_per_launch": flops,
                  "ms_per_launch": ms,
                  "other_bound": {k: (ten if roof["bound"] == "hbm" else hbm)[k]
@@ -602,7 +609,7 @@ def candidate_selection(si, dev, steps, n_cand=16384):
                              "ms_per_call": ms_full},
             "speedup_vs_full_context": ms_full / ms_c,
             "indexer_dram_bytes_per_launch": _kernel_traffic(
-                "k_indexer_tc_cand", "si_indexer_tc.cu", "candidates b16 16384"),
+                "k_indexer_tc", "si_indexer_tc.cu", "candidates b16 16384"),
             "l2": "flushed before every timed call (512 MiB write)"}
 
 
@@ -636,7 +643,8 @@ def run_si(args):
 
     wl = synth.make(args.workload, seed=rank_seed(args.workload, rank),
                     **({"kv_fp8": True} if args.kv_fp8 else {}),
-                    **({"kv_fp4": True} if args.kv_fp4 else {}))
+                    **({"kv_fp4": True} if args.kv_fp4 else {}),
+                    **({"idx_mx": True} if args.idx_mx else {}))
     dw = si.upload(wl, dev)
     b, ix, at, K = dw.batch, dw.indexer, dw.attention, dw.k_top
     n_q = wl.n_q
@@ -789,13 +797,15 @@ def run_si(args):
     mean_k = {k: sum(v) / len(v) for k, v in t_k.items()}
     dom = max(mean_k, key=mean_k.get)
     roof = roofline_of(dom, wl, algo, mean_k[dom], peaks, ms > 1.0,
-                       ":kv8" if args.kv_fp8 else ":kv4" if args.kv_fp4 else "")
+                       ":kv8" if args.kv_fp8 else ":kv4" if args.kv_fp4 else
+                       ":mx" if args.idx_mx else "")
     total_bytes = algo["indexer"] + algo["topk"] + algo["attn"]
     step_gbs = total_bytes / (ms / 1e3) / 1e9
 
     prefill = None if args.no_prefill else prefill_indexer(si, dev, args.steps)
     others = {}
-    if not args.no_other_workloads and args.workload == "c1" and not (args.kv_fp8 or args.kv_fp4):
+    if (not args.no_other_workloads and args.workload == "c1" and
+            not (args.kv_fp8 or args.kv_fp4 or args.idx_mx)):
         del dw, ws, ws_step, scores, idx, out, flush
         torch.cuda.empty_cache()
         others = {"long_context": workload_record(si, dev, "c3", args.steps, args.warmup),
@@ -814,7 +824,9 @@ def run_si(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": _workload_name(wl), "batch": n_q, "context": ld, "top_k": K,
-                   "indexer": f"{wl.Hi}x{wl.Di} e4m3 keys + fp32 scale, bf16 q",
+                   "indexer": (f"{wl.Hi}x{wl.Di} MXFP8 keys (groups of 32, E8M0 scales), bf16 q "
+                               "converted to MXFP8 on the device" if args.idx_mx else
+                               f"{wl.Hi}x{wl.Di} e4m3 keys + fp32 scale, bf16 q"),
                    "attention": f"{wl.Hq} heads x {wl.Dqk} (v {wl.Dv}) "
                                 f"{'e4m3 cache + fp32 scale per 128-entry tile, bf16 q' if args.kv_fp8 else 'e2m1 cache + fp32 scale per 16-entry block, bf16 q' if args.kv_fp4 else 'bf16'}, "
                                 f"fp32 accumulate, {OUT_DTYPE} out",
@@ -853,6 +865,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end legs")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the long-context and mixed-batch records of the default line")
+    ap.add_argument("--idx-mx", action="store_true",
+                    help="indexer keys in MXFP8 (groups of 32, E8M0 scales); the bf16 query is "
+                         "converted on the device")
     ap.add_argument("--kv-fp4", action="store_true",
                     help="store the latent KV cache in FP4 e2m1 (one scale per row and 16-entry "
                          "block, the NVFP4 block)")
