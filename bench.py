@@ -622,7 +622,15 @@ def _workload_name(wl):
         "c4": "mixed batch: 28 decode rows + 4 prefill chunks of 2048 over contexts 1K-64K, "
               "indexer 64x128 fp8, top-k 2048, MLA 128x576 bf16",
     }
-    return names.get(wl.name, wl.name)
+    name = names.get(wl.name, wl.name)
+    # the indexer and cache formats the workload was generated with
+    if wl.k_idx_dtype == "mxe4m3":
+        name = name.replace("indexer 64x128 fp8", "indexer 64x128 MXFP8 keys, "
+                            + ("MXFP8" if wl.q_idx_dtype == "mxe4m3" else wl.q_idx_dtype) + " query")
+    if wl.kv_dtype in ("e4m3", "e2m1"):
+        name = name.replace("MLA 128x576 bf16", "MLA 128x576 "
+                            + {"e4m3": "FP8", "e2m1": "FP4"}[wl.kv_dtype] + " latent cache")
+    return name
 
 
 # ---------------------------------------------------------------- main arm

@@ -50,7 +50,9 @@
 //                  (256 columns each);
 //   warp 3      -- writes -inf into each block's score columns past its live
 //                  tiles with bulk copies from a -inf buffer in shared memory
-//                  (the copy engine does the writing, off the pipeline);
+//                  (the copy engine does the writing, off the pipeline); the
+//                  fused calls, whose Top-K reads only positions up to each
+//                  row's own, skip it;
 //   warps 4..7  -- q-prep: writes each block's query rows into the B operand
 //                  (double-buffered);
 //   warps 8..15 -- two epilogue groups that take alternate items: per key
@@ -253,7 +255,7 @@ struct SpanWalk {
 template <int QM>
 __global__ void __launch_bounds__(kThreads, 1)
 k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix,
-                  float *scores, int64_t ld, int n_blocks_rows, unsigned int *st)
+                  float *scores, int64_t ld, int n_blocks_rows, int fill_tail, unsigned int *st)
 {
     constexpr bool MX = QM == kQMx;
     constexpr int kRows = rows_per_block<QM>();
@@ -506,7 +508,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
             __syncwarp();
             walk.next(t1);
         }
-    } else if (warp == kWarpTail) {
+    } else if (warp == kWarpTail && fill_tail) {
         // -------------------------------------------------------- tail writer
         // Score columns past a block's live tiles are -inf; the CTA that
         // scores the block's last tile writes them.  The 16-byte aligned
@@ -836,7 +838,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
 }  // namespace
 
 cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, float *scores,
-                                   int64_t ld, unsigned int *st, cudaStream_t s)
+                                   int64_t ld, unsigned int *st, cudaStream_t s, bool fill_tail)
 {
     static std::once_flag once[kMaxDevices];
     static int sms_of[kMaxDevices];
@@ -881,13 +883,13 @@ cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, floa
     count_launch();
     if (qm == kQMx)
         k_indexer_prefill<kQMx><<<(unsigned)grid, kThreads, Lay<kQMx>::kSmemBytes, s>>>(tmap, b, ix, scores,
-                                                                             ld, nb, st);
+                                                                             ld, nb, fill_tail, st);
     else if (qm == kQFp8)
         k_indexer_prefill<kQFp8><<<(unsigned)grid, kThreads, Lay<kQFp8>::kSmemBytes, s>>>(tmap, b, ix, scores,
-                                                                              ld, nb, st);
+                                                                              ld, nb, fill_tail, st);
     else
         k_indexer_prefill<kQBf16><<<(unsigned)grid, kThreads, Lay<kQBf16>::kSmemBytes, s>>>(tmap, b, ix, scores,
-                                                                               ld, nb, st);
+                                                                               ld, nb, fill_tail, st);
     return cudaGetLastError();
 }
 

@@ -41,9 +41,11 @@ cudaError_t launch_indexer_tc_cand(const si_batch &b, const si_indexer &ix, cons
 // Tensor-core indexer for query rows that all belong to one sequence (a
 // causal prefill or a prefill chunk): blocks of four rows (bf16 or FP8 q) or
 // three (MXFP8) share each key tile.  Same operand conditions as above; the caller
-// guarantees the single sequence.
+// guarantees the single sequence.  With fill_tail false the columns past each
+// row's position are left unwritten (for a Top-K that reads 0..q_pos only).
 cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, float *scores,
-                                   int64_t ld, unsigned int *st, cudaStream_t s);
+                                   int64_t ld, unsigned int *st, cudaStream_t s,
+                                   bool fill_tail = true);
 
 // Tensor-core sparse attention: bf16, 128 heads, 576-dim latent rows (V = first 512).
 bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top);
