@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -185,16 +186,26 @@ PROFILE_WORKLOAD = {"c1": "decode b64 ctx8192", "c3": "decode b16 ctx131072",
 VARIANT_KERNEL = {":kv8": "attn", ":kv4": "attn", ":mx": "indexer"}
 
 
+def code_sha(text: str) -> str:
+    """sha256 (first 16 hex digits) of a CUDA source with its comments and
+    blank lines removed: an edit of comments alone keeps a capture's counters
+    valid, any change of code does not."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def _kernel_traffic(kernel: str, source: str, workload: str):
     """DRAM bytes per launch from the committed ncu capture of this kernel on
-    this workload, if the kernel's source is unchanged since the counters
-    were taken; else None."""
+    this workload, if the kernel's source code is unchanged since the
+    counters were taken; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(f"{kernel}@{PROFILE_WORKLOAD.get(workload, workload)}")
-        with open(os.path.join(ROOT, "indexer_driven_top_gb300", "csrc", source), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        with open(os.path.join(ROOT, "indexer_driven_top_gb300", "csrc", source)) as f:
+            sha = code_sha(f.read())
         if rec and rec.get("source_sha") == sha:
             return rec.get("dram_bytes_per_launch")
     except Exception:
@@ -424,11 +435,27 @@ def _prefill_once(si, dev, steps, mode):
     assert si.workspace_status(ws, stream) == 0
     ms = sum(e[2 * i].elapsed_time(e[2 * i + 1]) for e in evs for i in range(len(strips))) / n
     ms_loop = t0.elapsed_time(t1) / n
+    # the same work as one call of section 4.1's fused operator (si_indexer_topk:
+    # the strips inside the call, each after the first overlapping the
+    # previous Top-K's end); its selection must equal the strip loop's
+    ws_sel = si.alloc_workspace(si.workspace_size(si.OP_SELECT, b, ix, None, K), dev)
+    idx_sel = torch.empty_like(idx)
+    for _ in range(2):
+        si.indexer_topk(b, ix, K, idx_sel, ws_sel, stream)
+    torch.cuda.synchronize(dev)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(n):
+        si.indexer_topk(b, ix, K, idx_sel, ws_sel, stream)
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert si.workspace_status(ws_sel, stream) == 0 and torch.equal(idx_sel, idx)
+    ms_fused = f0.elapsed_time(f1) / n
     pairs = int((wl.q_pos.astype("int64") + 1).sum())
     flops = 2.0 * wl.Hi * wl.Di * pairs
-    del dw, strip, idx, ws, strips
+    del dw, strip, idx, ws, strips, ws_sel, idx_sel
     torch.cuda.empty_cache()
-    return pairs, flops, ms, ms_loop
+    return pairs, flops, ms, ms_loop, ms_fused
 
 
 E2E_REPLICAS = 3
@@ -517,30 +544,34 @@ def prefill_indexer(si, dev, steps):
     scores those same bytes)."""
     peaks = _peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]   # measured bf16 burst x nominal fp8/bf16 ratio (2)
-    pairs, flops, ms, ms_loop = _prefill_once(si, dev, steps, "bf16")
+    pairs, flops, ms, ms_loop, ms_fused = _prefill_once(si, dev, steps, "bf16")
     tflops = flops / (ms / 1e3) / 1e12
-    _, _, ms8, ms8_loop = _prefill_once(si, dev, steps, "e4m3")
+    _, _, ms8, ms8_loop, ms8_fused = _prefill_once(si, dev, steps, "e4m3")
     tflops8 = flops / (ms8 / 1e3) / 1e12
-    _, _, msx, msx_loop = _prefill_once(si, dev, steps, "mx")
+    _, _, msx, msx_loop, msx_fused = _prefill_once(si, dev, steps, "mx")
     tflopsx = flops / (msx / 1e3) / 1e12
     return {"workload": "causal prefill 16384 tokens, indexer 64x128, e4m3 keys + fp32 scale, "
                         "bf16 query",
             "kernel": "k_indexer_prefill",
             "timing": f"strips of {PREFILL_STRIP_ROWS} rows (64 MiB of scores, L2-resident), "
-                      "indexer then Top-K per strip; indexer launches event-timed and summed",
+                      "indexer then Top-K per strip; indexer launches event-timed and summed; "
+                      "ms_indexer_topk_call: the same prefill as one si_indexer_topk call",
             "causal_pairs": pairs, "algorithmic_tflop": flops / 1e12, "ms_per_prefill": ms,
             "tflops": tflops, "fp8_peak_tflops": fp8_peak,
             "peak_src": peaks["src"] + " (bf16 burst x 2)",
             "frac_of_fp8_peak": tflops / fp8_peak,
             "ms_strip_loop_with_topk": ms_loop,
+            "ms_indexer_topk_call": ms_fused,
             "option_e4m3_query": {"ms_per_prefill": ms8, "tflops": tflops8,
                                   "frac_of_fp8_peak": tflops8 / fp8_peak,
                                   "ms_strip_loop_with_topk": ms8_loop,
+                                  "ms_indexer_topk_call": ms8_fused,
                                   "note": "query quantised to e4m3 + fp32 scale per (row, head); "
                                           "not the configuration's query format"},
             "option_mxfp8": {"ms_per_prefill": msx, "tflops": tflopsx,
                              "frac_of_fp8_peak": tflopsx / fp8_peak,
                              "ms_strip_loop_with_topk": msx_loop,
+                             "ms_indexer_topk_call": msx_fused,
                              "note": "section 5.1's MXFP8 indexer: keys in groups of 32 with E8M0 "
                                      "scales, the bf16 query converted to MXFP8 inside the kernel "
                                      "(block-scaled UMMA, three rows per 192-wide block)"}}

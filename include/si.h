@@ -231,10 +231,11 @@ si_status si_sparse_attn(const si_batch *b, const si_attention *at, const int32_
                          int32_t k_top, void *out, si_dtype out_dtype, float *lse, void *ws,
                          size_t ws_bytes, void *stream);
 
-/* Section 4.1's fused indexer operator on its own (the indexer prolog of
- * section 4.3 ends in idx = fused_topk(q8, k, g)): scores, head weighting and
- * Top-K for every query row, the scores living only in the workspace, a strip
- * of rows at a time, exactly as in si_fused_decode.  idx receives what
+/* Section 4.1's fused indexer operator on its own (the last step of the
+ * indexer prolog in section 4.3, one operator that scores, weights and
+ * selects): scores, head weighting and Top-K for every query row, the scores
+ * living only in the workspace, a strip of rows at a time, exactly as in
+ * si_fused_decode.  idx receives what
  * si_indexer_scores followed by si_topk would give.  ws: at least
  * si_workspace_min(SI_OP_SELECT, ...) bytes (si_workspace_size(SI_OP_SELECT,
  * ...) scores every row in one strip, up to 64 MiB of scores). */
@@ -314,9 +315,10 @@ si_status si_fused_decode_noalloc(const si_batch *b, const si_indexer *ix,
                                   void *out, si_dtype out_dtype, float *lse,
                                   const void **scratch, void *stream);
 
-/* MXFP8 conversion (section 4.3's prolog step q8 = quant_per_group(q), in
- * section 5.1's format; the rule is the OCP MX specification's, the pages
- * give none of their own).  Per group of 32 consecutive entries of a row:
+/* MXFP8 conversion (section 4.3's per-group quantisation of the query in
+ * the indexer prolog, in section 5.1's format; the rule is the OCP MX
+ * specification's, the pages give none of their own).  Per group of 32
+ * consecutive entries of a row:
  *   E = floor(log2 max|x|) - 8, clamped to [-127, 127] (an all-zero group
  *       takes -127); scale byte = E + 127;
  *   code = e4m3(x / 2^E), round to nearest even, magnitudes above 448

@@ -224,11 +224,11 @@ unsigned int *status_word(void *ws) { return reinterpret_cast<unsigned int *>(ws
 constexpr int32_t kPrefillRun = 64;  // rows of one sequence worth a prefill launch
 
 cudaError_t launch_indexer_rows(const si_batch &b, const si_indexer &ix, float *scores,
-                                int64_t ld, bool one_sequence, bool fill_tail, unsigned int *st,
-                                cudaStream_t s)
+                                int64_t ld, bool one_sequence, bool fill_tail, bool after_own,
+                                unsigned int *st, cudaStream_t s)
 {
     if (one_sequence && b.n_q >= kPrefillRun && si::indexer_tc_supported(b, ix, ld))
-        return si::launch_indexer_prefill(b, ix, scores, ld, st, s, fill_tail);
+        return si::launch_indexer_prefill(b, ix, scores, ld, st, s, fill_tail, after_own);
     return si::indexer_tc_supported(b, ix, ld) ? si::launch_indexer_tc(b, ix, scores, ld, st, s)
                                                : si::launch_indexer_generic(b, ix, scores, ld, st, s);
 }
@@ -237,13 +237,15 @@ cudaError_t launch_indexer_rows(const si_batch &b, const si_indexer &ix, float *
 // one sequence goes to the prefill kernel, the rows between runs to the
 // decode kernels (one launch per maximal stretch).  fill_tail false: the
 // scores past each row's position may be left unwritten (the caller's Top-K
-// reads 0..q_pos only).
+// reads 0..q_pos only).  after_own: the stream's previous kernel is one of
+// this call's (a single prefill launch may then overlap its end).
 si_status run_indexer(const si_batch &b, const si_indexer &ix, float *scores, int64_t ld,
-                      unsigned int *st, cudaStream_t s, bool fill_tail = true)
+                      unsigned int *st, cudaStream_t s, bool fill_tail = true,
+                      bool after_own = false)
 {
     cudaError_t e = cudaSuccess;
     if (!b.host_q_seq || b.n_seq == 1 || b.n_q < kPrefillRun) {
-        e = launch_indexer_rows(b, ix, scores, ld, b.n_seq == 1, fill_tail, st, s);
+        e = launch_indexer_rows(b, ix, scores, ld, b.n_seq == 1, fill_tail, after_own, st, s);
         return e == cudaSuccess ? SI_OK : cuda_fail(e, "indexer launch");
     }
     const int32_t *hs = b.host_q_seq;
@@ -262,7 +264,7 @@ si_status run_indexer(const si_batch &b, const si_indexer &ix, float *scores, in
                 end = run_end(end);
         }
         e = launch_indexer_rows(row_slice(b, r, end - r), indexer_slice(ix, r),
-                                scores + (int64_t)r * ld, ld, chunk, fill_tail, st, s);
+                                scores + (int64_t)r * ld, ld, chunk, fill_tail, false, st, s);
         r = end;
     }
     return e == cudaSuccess ? SI_OK : cuda_fail(e, "indexer launch");
@@ -570,7 +572,7 @@ si_status run_indexer_topk(const si_batch *b, const si_indexer *ix, int32_t k_to
         const int32_t n = (int32_t)std::min<int64_t>(strip, b->n_q - r0);
         const si_batch sb = row_slice(*b, (int32_t)r0, n);
         const si_indexer si_ = indexer_slice(*ix, (int32_t)r0);
-        if ((st = run_indexer(sb, si_, scores, ld, stw, s, false)) != SI_OK)
+        if ((st = run_indexer(sb, si_, scores, ld, stw, s, false, r0 > 0)) != SI_OK)
             return st;
         if ((st = run_topk(sb, scores, ld, k_top, idx + r0 * k_top, stw, s)) != SI_OK)
             return st;

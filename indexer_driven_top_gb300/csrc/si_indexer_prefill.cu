@@ -89,6 +89,9 @@ constexpr int kMaxRows = 4;           // query rows per block
 constexpr int kQBf16 = 0, kQFp8 = 1, kQMx = 2;
 template <int QM> constexpr int mma_n() { return QM == kQMx ? 3 * kHeads : kN; }
 template <int QM> constexpr int rows_per_block() { return mma_n<QM>() / kHeads; }
+// What a block's query preparation costs, in tiles of work, when the balance
+// charges it to the CTA whose range holds the block.
+template <int QM> constexpr int block_cost() { return QM == kQFp8 ? 4 : 8; }
 constexpr int kScStages = 4;          // scale ring depth per epilogue group
 constexpr int kThreads = 16 * 32;
 constexpr int kWarpProd0 = 0, kWarpProd1 = 2;  // producers: items of parity 0 / 1
@@ -164,11 +167,16 @@ struct Span {
     int64_t n;
 };
 
-// Found by all threads of the CTA together: thread i sums the tiles of
-// blocks [i m, (i + 1) m), a block-wide scan places those sums, and the
-// thread whose blocks hold the range's first item locates it.  `wsum` holds
-// kThreads / 32 + 2 entries of shared memory.
-template <int kRows>
+// The CTAs' ranges are equal shares of a cost in which every block weighs
+// its tiles plus kCost: a block's query preparation is not hidden behind a
+// block of few tiles, and a range holding more blocks ends later.  Found by
+// all threads of the CTA together: thread i sums the tiles of blocks
+// [i m, (i + 1) m), a block-wide scan places those sums (the cost before
+// block j is the tiles before it plus kCost j), and the threads whose blocks
+// hold the range's two ends turn them into items: an end inside a block's
+// kCost part is that block's first tile.  `wsum` holds kThreads / 32 + 6
+// entries of shared memory.
+template <int kRows, int kCost>
 __device__ Span find_span(const si_batch &b, int nb, int tiles_ld, long long *wsum)
 {
     constexpr int kWarps = kThreads / 32;
@@ -203,29 +211,43 @@ __device__ Span find_span(const si_batch &b, int nb, int tiles_ld, long long *ws
             wsum[lane] = t;  // inclusive warp totals
     }
     __syncthreads();
-    const long long before = (warp > 0 ? wsum[warp - 1] : 0) + x - local;
+    const long long before = (warp > 0 ? wsum[warp - 1] : 0) + x - local;  // tiles
     const long long total = wsum[kWarps - 1];
-    const long long j0 = total * blockIdx.x / gridDim.x;
-    const long long j1 = total * (blockIdx.x + 1) / gridDim.x;
+    const long long cbefore = before + (long long)kCost * lo;               // cost
+    const long long clocal = local + (long long)kCost * (hi - lo);
+    const long long ctotal = total + (long long)kCost * nb;
+    const long long c0 = ctotal * blockIdx.x / gridDim.x;
+    const long long c1 = ctotal * (blockIdx.x + 1) / gridDim.x;
     __syncthreads();  // every thread has read the totals before they are reused
-    if (j0 < j1 && before <= j0 && j0 < before + local) {
-        long long acc = before;
+    // cost position c -> (list position, tile in block, item index)
+    auto locate = [&](long long c, int slot) {
+        long long acc = before, cacc = cbefore;
         for (int i = lo; i < hi; i++) {
             int r0, nrows, T;
             block_shape<kRows>(b, block_at(i, nb), tiles_ld, r0, nrows, T);
-            if (j0 < acc + T) {
-                wsum[kWarps] = i;
-                wsum[kWarps + 1] = j0 - acc;
-                break;
+            if (c < cacc + kCost + T) {
+                const long long t = c - cacc - kCost > 0 ? c - cacc - kCost : 0;
+                wsum[slot] = i;
+                wsum[slot + 1] = t;
+                wsum[slot + 2] = acc + t;
+                return;
             }
             acc += T;
+            cacc += kCost + T;
         }
-    }
+    };
+    if (cbefore <= c0 && c0 < cbefore + clocal)
+        locate(c0, kWarps);
+    if (cbefore <= c1 && c1 < cbefore + clocal)
+        locate(c1, kWarps + 3);
+    if (tid == 0 && c1 >= ctotal)
+        wsum[kWarps + 5] = total;  // the last range ends after the last item
     __syncthreads();
-    Span sp{0, 0, j1 - j0};
-    if (sp.n > 0) {
+    Span sp{0, 0, 0};
+    if (c0 < c1) {
         sp.b0 = (int)wsum[kWarps];
         sp.t0 = (int)wsum[kWarps + 1];
+        sp.n = wsum[kWarps + 5] - wsum[kWarps + 2];
     }
     return sp;
 }
@@ -315,8 +337,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
     const int P = b.page_size;
     const int lp = 31 - __clz(P);  // page_size is a power of two >= 8
     const int seq = __ldg(b.q_seq);  // every row belongs to this sequence
-    __shared__ long long span_scratch[kThreads / 32 + 2];
-    const Span work = find_span<kRows>(b, n_blocks_rows, tiles_ld, span_scratch);
+    __shared__ long long span_scratch[kThreads / 32 + 6];
+    const Span work = find_span<kRows, block_cost<QM>()>(b, n_blocks_rows, tiles_ld, span_scratch);
 
     if (warp == kWarpProd0 || warp == kWarpProd1) {
         // ------------------------------------------------------------ producer
@@ -520,6 +542,7 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
             ninf_s[i] = -INFINITY;
         fence_async_smem();  // generic-proxy writes -> the copy engine's reads
         __syncwarp();
+        griddep_wait();  // the score rows may still be read by the previous kernel
         constexpr int64_t kChunk = kNinfBytes / 4;  // floats per copy
         SpanWalk walk(work, n_blocks_rows);
         for (; walk.more();) {
@@ -690,6 +713,11 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
                         while (ldexpf(amax, -(e - 1)) <= 448.f)
                             e--;
                     }
+                    // x / s_h as one multiply by 2^-e when that is a normal
+                    // float (the same correctly rounded result as ldexpf)
+                    const bool pow2 = e >= -126 && e <= 126;
+                    const float inv_s = pow2 ? __int_as_float((127 - e) << 23) : 0.f;
+                    auto unscale = [&](float x) { return pow2 ? x * inv_s : ldexpf(x, -e); };
 #pragma unroll
                     for (int c = 0; c < 4; c++) {  // 16 dims per 16-byte unit
                         uint32_t hi[4], lo[4];
@@ -699,8 +727,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
 #pragma unroll
                             for (int pr2 = 0; pr2 < 2; pr2++) {
                                 const uint32_t word = q2[8 * c + 2 * jj + pr2];
-                                const float x0 = ldexpf(__uint_as_float(word << 16), -e);
-                                const float x1 = ldexpf(__uint_as_float(word & 0xFFFF0000u), -e);
+                                const float x0 = unscale(__uint_as_float(word << 16));
+                                const float x1 = unscale(__uint_as_float(word & 0xFFFF0000u));
                                 const uint16_t h2 = float2_to_e4m3x2(x0, x1);
                                 const float2 hf = e4m3x2_to_float2(h2);
                                 const uint16_t l2 = float2_to_e4m3x2(x0 - hf.x, x1 - hf.y);
@@ -733,6 +761,10 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
         const int g = (warp - kWarpEpi0) >> 2;
         const int et = (tid - kWarpEpi0 * 32) & 127;  // key row = TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        // Launched as a programmatic dependent, the kernel prepares queries,
+        // loads keys and fills both accumulators while the previous kernel
+        // (a Top-K reading the same score rows) finishes; the stores wait.
+        griddep_wait();
         SpanWalk walk(work, n_blocks_rows);
         int64_t it = 0;
         int bi = 0;
@@ -838,7 +870,8 @@ k_indexer_prefill(const __grid_constant__ CUtensorMap tmap, si_batch b, si_index
 }  // namespace
 
 cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, float *scores,
-                                   int64_t ld, unsigned int *st, cudaStream_t s, bool fill_tail)
+                                   int64_t ld, unsigned int *st, cudaStream_t s, bool fill_tail,
+                                   bool after_own_kernel)
 {
     static std::once_flag once[kMaxDevices];
     static int sms_of[kMaxDevices];
@@ -881,16 +914,32 @@ cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, floa
     const int64_t tiles_ld = (ld + kKeys - 1) / kKeys;
     const int64_t grid = std::min<int64_t>((int64_t)nb * tiles_ld, (int64_t)sms_of[dev]);
     count_launch();
-    if (qm == kQMx)
-        k_indexer_prefill<kQMx><<<(unsigned)grid, kThreads, Lay<kQMx>::kSmemBytes, s>>>(tmap, b, ix, scores,
-                                                                             ld, nb, fill_tail, st);
-    else if (qm == kQFp8)
-        k_indexer_prefill<kQFp8><<<(unsigned)grid, kThreads, Lay<kQFp8>::kSmemBytes, s>>>(tmap, b, ix, scores,
-                                                                              ld, nb, fill_tail, st);
-    else
-        k_indexer_prefill<kQBf16><<<(unsigned)grid, kThreads, Lay<kQBf16>::kSmemBytes, s>>>(tmap, b, ix, scores,
-                                                                               ld, nb, fill_tail, st);
-    return cudaGetLastError();
+    // After a kernel of the same call the launch may overlap its end
+    // (programmatic dependent launch): everything the kernel reads before its
+    // stores was written before the call.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_own_kernel ? 1 : 0;
+    const int fill = fill_tail ? 1 : 0;
+    if (qm == kQMx) {
+        cfg.dynamicSmemBytes = Lay<kQMx>::kSmemBytes;
+        return cudaLaunchKernelEx(&cfg, k_indexer_prefill<kQMx>, tmap, b, ix, scores, ld, nb, fill,
+                                  st);
+    }
+    if (qm == kQFp8) {
+        cfg.dynamicSmemBytes = Lay<kQFp8>::kSmemBytes;
+        return cudaLaunchKernelEx(&cfg, k_indexer_prefill<kQFp8>, tmap, b, ix, scores, ld, nb,
+                                  fill, st);
+    }
+    cfg.dynamicSmemBytes = Lay<kQBf16>::kSmemBytes;
+    return cudaLaunchKernelEx(&cfg, k_indexer_prefill<kQBf16>, tmap, b, ix, scores, ld, nb, fill,
+                              st);
 }
 
 }  // namespace si

@@ -37,8 +37,8 @@
 // TMEM lanes and columns -- and the MMA thread copies that block (and, once
 // per query row, the query's block) into TMEM ahead of the tile's four MMAs;
 // copies and MMAs of one thread execute in order.  A bf16 query is converted
-// by the q-prep threads with the MX rule of section 4.3's quant_per_group
-// step, bit-identical to si_quant_mxfp8.
+// by the q-prep threads with the MX rule of section 4.3's per-group query
+// quantisation, bit-identical to si_quant_mxfp8.
 //
 // One persistent CTA per SM runs a warp-specialised pipeline:
 //   2 producer warps -- per tile, TMA tensor copies of its key pages (128-byte
@@ -654,6 +654,11 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
                 while (ldexpf(amax, -(e - 1)) <= 448.f)
                     e--;
             }
+            // x / s_h as one multiply by 2^-e when that is a normal float (the
+            // same correctly rounded result as ldexpf)
+            const bool pow2 = e >= -126 && e <= 126;
+            const float inv_s = pow2 ? __int_as_float((127 - e) << 23) : 0.f;
+            auto unscale = [&](float x) { return pow2 ? x * inv_s : ldexpf(x, -e); };
 #pragma unroll
             for (int c = 0; c < 4; c++) {  // 16 dims per 16-byte unit
                 uint32_t hi[4], lo[4];
@@ -663,8 +668,8 @@ k_indexer_tc(const __grid_constant__ CUtensorMap tmap, si_batch b, si_indexer ix
 #pragma unroll
                     for (int pr2 = 0; pr2 < 2; pr2++) {
                         const uint32_t word = q2[8 * c + 2 * j + pr2];  // dims 16c+4j+2pr2, +1
-                        const float x0 = ldexpf(__uint_as_float(word << 16), -e);
-                        const float x1 = ldexpf(__uint_as_float(word & 0xFFFF0000u), -e);
+                        const float x0 = unscale(__uint_as_float(word << 16));
+                        const float x1 = unscale(__uint_as_float(word & 0xFFFF0000u));
                         const uint16_t h2 = float2_to_e4m3x2(x0, x1);
                         const float2 hf = e4m3x2_to_float2(h2);
                         const uint16_t l2 = float2_to_e4m3x2(x0 - hf.x, x1 - hf.y);

@@ -43,9 +43,12 @@ cudaError_t launch_indexer_tc_cand(const si_batch &b, const si_indexer &ix, cons
 // three (MXFP8) share each key tile.  Same operand conditions as above; the caller
 // guarantees the single sequence.  With fill_tail false the columns past each
 // row's position are left unwritten (for a Top-K that reads 0..q_pos only).
+// after_own_kernel: the previous kernel of the stream belongs to the same
+// call (its inputs were complete before the call), so the launch may overlap
+// that kernel's end; only the score stores wait for it.
 cudaError_t launch_indexer_prefill(const si_batch &b, const si_indexer &ix, float *scores,
                                    int64_t ld, unsigned int *st, cudaStream_t s,
-                                   bool fill_tail = true);
+                                   bool fill_tail = true, bool after_own_kernel = false);
 
 // Tensor-core sparse attention: bf16, 128 heads, 576-dim latent rows (V = first 512).
 bool attn_tc_supported(const si_batch &b, const si_attention &at, int k_top);

@@ -1,7 +1,8 @@
-// si_mx.cu -- MXFP8 conversion of rows (the prolog step q8 =
-// quant_per_group(q) of section 4.3 of "Day0 Inference Support and
-// Performance Optimization for New Architecture LLMs", in the indexer format
-// of its section 5.1: groups of 32 entries, one E8M0 scale each).
+// si_mx.cu -- MXFP8 conversion of rows (the per-group quantisation of the
+// indexer query that the prolog in section 4.3 of "Day0 Inference Support
+// and Performance Optimization for New Architecture LLMs" performs before
+// scoring, in the indexer format of its section 5.1: groups of 32 entries,
+// one E8M0 scale each).
 //
 // The pass is bound by HBM: 2 bytes read (bf16) and 1 + 1/32 written per
 // entry.  Each thread converts 8 consecutive entries (one 16-byte load of

@@ -241,28 +241,38 @@ k_topk_rows(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx
     }
 }
 
-// Long rows (16384 < n <= 32768 C): a cluster of C CTAs per row, CTA q
-// caching positions [32768 q, 32768 q + 32768) in shared memory (128 KB;
-// thread t owns positions 32 t .. 32 t + 31, stored at e * 1024 + t so that a
-// warp's accesses fall in distinct banks).  Holding 32768 keys per CTA keeps
-// the clusters at four CTAs for rows of 131072: clusters of eight CTAs that
+// Long rows (16384 < n <= 1024 E C): a cluster of C CTAs per row, CTA q
+// caching positions [1024 E q, 1024 E (q + 1)) in shared memory (4 KB per
+// key of a thread; thread t owns positions E t .. E t + E - 1, stored at
+// e * 1024 + t so that a warp's accesses fall in distinct banks).  With
+// E = 32 rows of 131072 take clusters of four: clusters of eight CTAs that
 // each fill an SM do not all fit on the GPU at once, and the second wave
-// starts only when the first has finished.  Each radix pass
+// starts only when the first has finished (clusters of eight with E = 16,
+// two CTAs per SM, all fit but were not faster: 32.9 against 31.0 us on 16
+// rows of 131072).  Each radix pass
 // adds every CTA's histogram into a per-pass histogram in CTA 0's shared
 // memory (distributed shared memory atomics), and every CTA then reads the
 // merged counts and takes the same decision.  The emit pass orders the CTAs'
 // selections by their segment: CTA q writes after the selections and the
 // tie quota of CTAs 0..q-1, whose counts it reads from CTA 0.
+// E keys per thread: 32 for the clusters of long rows; 16 (64 KB of keys, so
+// that two 1024-thread CTAs share an SM) for batches of more rows than SMs
+// whose rows of 8193..16384 fit one CTA (the register-cached row kernel holds
+// an SM alone).
 constexpr int kClusterE = 32;
 constexpr int kSegment = kClusterE * kTopkThreads;  // positions per CTA
 constexpr int kMaxCluster = 8;
 constexpr int kClusterSmem = kSegment * 4;          // the CTA's keys (dynamic shared memory)
+constexpr int kLeanE = 16;
+constexpr int kLeanSmem = kLeanE * kTopkThreads * 4;
 
+template <int E>
 __global__ void __launch_bounds__(kTopkThreads)
 k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *idx,
                int32_t fixed_n, SlotMap m)
 {
-    extern __shared__ uint32_t ks[];             // [kClusterE][kTopkThreads] keys
+    constexpr int kSeg = E * kTopkThreads;      // positions per CTA
+    extern __shared__ uint32_t ks[];             // [E][kTopkThreads] keys
     __shared__ uint32_t hist[kRadixBins];
     __shared__ uint32_t merged[3][kRadixBins];   // used in CTA 0: one histogram per pass
     __shared__ uint32_t counts[kMaxCluster][2];  // used in CTA 0: (above, ties) per CTA
@@ -294,11 +304,11 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
         cluster_sync();
         return;
     }
-    const int64_t p0 = (int64_t)q * kSegment + (int64_t)tid * kClusterE;
+    const int64_t p0 = (int64_t)q * kSeg + (int64_t)tid * E;
     uint32_t valid = 0;  // bit e: position p0 + e < n
-    if (p0 + kClusterE <= n && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    if (p0 + E <= n && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
 #pragma unroll
-        for (int e = 0; e < kClusterE; e += 4) {
+        for (int e = 0; e < E; e += 4) {
             const float4 v = __ldg(reinterpret_cast<const float4 *>(row + p0 + e));
             ks[(e + 0) * kTopkThreads + tid] = order_key(v.x);
             ks[(e + 1) * kTopkThreads + tid] = order_key(v.y);
@@ -308,7 +318,7 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
         valid = 0xffffffffu;
     } else {
 #pragma unroll
-        for (int e = 0; e < kClusterE; e++) {
+        for (int e = 0; e < E; e++) {
             const bool in = p0 + e < n;
             ks[e * kTopkThreads + tid] = in ? order_key(__ldg(row + p0 + e)) : 0u;
             valid |= (in ? 1u : 0u) << e;
@@ -325,7 +335,7 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
             hist[i] = 0;
         __syncthreads();
 #pragma unroll 8
-        for (int e = 0; e < kClusterE; e++) {
+        for (int e = 0; e < E; e++) {
             const uint32_t key = ks[e * kTopkThreads + tid];
             if (((valid >> e) & 1u) && (key & mask) == prefix)
                 atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
@@ -346,7 +356,7 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
     // emit
     int gt = 0, eq = 0;
 #pragma unroll 8
-    for (int e = 0; e < kClusterE; e++) {
+    for (int e = 0; e < E; e++) {
         const uint32_t key = ks[e * kTopkThreads + tid];
         const bool in = (valid >> e) & 1u;
         gt += in && key > prefix;
@@ -372,7 +382,7 @@ k_topk_cluster(si_batch b, const float *scores, int64_t ld, int k_top, int32_t *
     int total;
     int o = off + block_exclusive_scan(gt + take_eq, &total, sbuf);
 #pragma unroll 8
-    for (int e = 0; e < kClusterE; e++) {
+    for (int e = 0; e < E; e++) {
         const uint32_t key = ks[e * kTopkThreads + tid];
         const bool in = (valid >> e) & 1u;
         const bool tie = in && key == prefix;
@@ -408,7 +418,10 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
     // Rows longer than one CTA's register cache take a cluster of C CTAs per
     // row (b.max_ctx bounds every row's candidate count) when one CTA per row
     // would leave most of the GPU idle; a batch with many rows keeps one CTA
-    // per row and streams.
+    // per row: with keys in shared memory (two CTAs per SM) when the rows fit
+    // one CTA, outnumber the SMs and are longer than the 8-key register cache
+    // (a late prefill strip; shorter rows are faster from registers), else
+    // from registers or streaming.
     static int sms_of[kMaxDevices];
     static std::once_flag once[kMaxDevices];
     static cudaError_t err_of[kMaxDevices];
@@ -416,9 +429,13 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         dev = 0;
     std::call_once(once[dev], [dev] {
-        err_of[dev] = cudaFuncSetAttribute(k_topk_cluster,
+        err_of[dev] = cudaFuncSetAttribute(k_topk_cluster<kClusterE>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kClusterSmem);
+        if (err_of[dev] == cudaSuccess)
+            err_of[dev] = cudaFuncSetAttribute(k_topk_cluster<kLeanE>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kLeanSmem);
     });
     if (sms_of[dev] == 0 &&
         cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -436,9 +453,18 @@ cudaError_t launch_topk(const si_batch &b, const float *scores, int64_t ld, int 
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        return cudaLaunchKernelEx(&cfg, k_topk_cluster, b, scores, ld, k_top, idx, fixed_n, m);
+        return cudaLaunchKernelEx(&cfg, k_topk_cluster<kClusterE>, b, scores, ld, k_top, idx,
+                                  fixed_n, m);
     }
     cfg.gridDim = dim3((unsigned)b.n_q);
+    if (longest > 8 * kTopkThreads && longest <= (int64_t)kLeanE * kTopkThreads &&
+        b.n_q > sms_of[dev]) {
+        if (err_of[dev] != cudaSuccess)
+            return err_of[dev];
+        cfg.dynamicSmemBytes = kLeanSmem;  // a cluster of one CTA per row
+        return cudaLaunchKernelEx(&cfg, k_topk_cluster<kLeanE>, b, scores, ld, k_top, idx,
+                                  fixed_n, m);
+    }
     return cudaLaunchKernelEx(&cfg, k_topk_rows, b, scores, ld, k_top, idx, fixed_n, m);
 }
 

@@ -299,8 +299,8 @@ void oracle_indexer_scores(const orc_batch *b, const int32_t *rows, int32_t n_ro
 /* ------------------------------------------------------- indexer, MXFP8 */
 
 /* Section 5.1's indexer: Q and K in MXFP8, one E8M0 scale per group of 32
- * entries.  Section 4.3's prolog quantises the query per group (q8 =
- * quant_per_group(q)) before the fused scoring; a query given in float32 or
+ * entries.  Section 4.3's prolog quantises the query per group before the
+ * fused scoring; a query given in float32 or
  * bf16 is converted here by the MX rule above, one (row, head) group at a
  * time.  Each entry is then X * P (scale times code) and the score is the
  * definition of section 2.2 over those values:

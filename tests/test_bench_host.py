@@ -23,25 +23,40 @@ def _tree(tmp_path, src_text, rec_sha):
                                       "workload": "decode b64 ctx8192"}}))
 
 
+CODE = "// kernel\n__global__ void k(int *p) { p[0] = 1; }  // store\n"
+
+
 def test_traffic_is_reported_for_the_captured_source(tmp_path, monkeypatch):
-    text = "// kernel source\n"
-    _tree(tmp_path, text, hashlib.sha256(text.encode()).hexdigest()[:16])
+    _tree(tmp_path, CODE, bench.code_sha(CODE))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     # the configuration name maps to the workload the capture names
     assert bench._kernel_traffic("k_demo", "k.cu", "c1") == 1234.0
     assert bench._kernel_traffic("k_demo", "k.cu", "decode b64 ctx8192") == 1234.0
 
 
-def test_traffic_is_null_once_the_source_changes(tmp_path, monkeypatch):
-    _tree(tmp_path, "// kernel source, edited since the capture\n",
-          hashlib.sha256(b"// kernel source\n").hexdigest()[:16])
+def test_traffic_survives_a_comment_edit(tmp_path, monkeypatch):
+    edited = "/* what k does,\n   reworded */\n\n__global__ void k(int *p) { p[0] = 1; }\n"
+    _tree(tmp_path, edited, bench.code_sha(CODE))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._kernel_traffic("k_demo", "k.cu", "c1") == 1234.0
+
+
+def test_traffic_is_null_once_the_code_changes(tmp_path, monkeypatch):
+    _tree(tmp_path, CODE.replace("p[0] = 1", "p[0] = 2"), bench.code_sha(CODE))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench._kernel_traffic("k_demo", "k.cu", "c1") is None
 
 
+def test_code_sha_ignores_comments_only():
+    assert bench.code_sha("a; // x\n") == bench.code_sha("a;\n")
+    assert bench.code_sha("a; /* x */\n") == bench.code_sha("a;\n")
+    assert bench.code_sha("a;\n") != bench.code_sha("b;\n")
+    assert bench.code_sha("a;\n") == hashlib.sha256(b"a;").hexdigest()[:16]
+
+
 def test_traffic_is_null_without_a_capture(tmp_path, monkeypatch):
-    text = "// kernel source\n"
-    _tree(tmp_path, text, hashlib.sha256(text.encode()).hexdigest()[:16])
+    text = CODE
+    _tree(tmp_path, text, bench.code_sha(text))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench._kernel_traffic("k_other", "k.cu", "c1") is None
     assert bench._kernel_traffic("k_demo", "k.cu", "c3") is None

@@ -235,15 +235,46 @@ def test_topk_exact_on_identical_scores(si):
         assert np.array_equal(idx.cpu().numpy(), want), K
 
 
-@pytest.mark.parametrize("ld", [16385, 40000, 131072])
-def test_topk_exact_long_rows_cluster(si, ld):
+@pytest.mark.parametrize("ld", [3000, 12000, 16384])
+def test_topk_exact_many_rows_shared_memory(si, ld):
+    """A batch of more rows than the GPU has SMs: rows of up to 8192 keep
+    the register-cached kernel (3000), longer rows that fit one CTA (a late
+    prefill strip) take one CTA per row with its keys in shared memory, two
+    CTAs per SM (12000, 16384).  Bit-exact against the oracle with heavy
+    ties, -0/+0, rows that select everything and rows ending at the last
+    position."""
+    rng = np.random.default_rng(ld + 7)
+    n_q = 400
+    edges = np.minimum([0, 100, 2047, 2048, 2049, 8191, 8192, 16383], ld - 1)
+    pos = np.concatenate([rng.integers(0, ld, n_q - len(edges) - 1), edges, [ld - 1]]).astype(np.int32)
+    sc = rng.integers(-30, 30, size=(n_q, ld)).astype(np.float32)   # many equal keys
+    sc[1::3] = rng.standard_normal((len(sc[1::3]), ld)).astype(np.float32)
+    sc[2, :1000] = -0.0
+    sc[5, :] = 0.0
+    sc[5, ::2] = -0.0
+    import indexer_driven_top_gb300 as si_
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    nb = (ld + 63) // 64
+    b = si_.Batch(dev(np.zeros((1, nb), np.int32)), dev(np.array([ld], np.int32)),
+                  dev(np.zeros(n_q, np.int32)), dev(pos), 64, ld, nb)
+    ws = si_.alloc_workspace(256)
+    ob = oracle.Batch(np.zeros((1, nb), np.int32), [ld], np.zeros(n_q, np.int32), pos, 64)
+    for K in (1, 77, 2048):
+        idx = torch.empty((n_q, K), dtype=torch.int32, device="cuda")
+        si_.topk(b, dev(sc), K, idx, ws)
+        want = oracle.topk(ob, sc.astype(np.float64), K)
+        assert np.array_equal(idx.cpu().numpy(), want), K
+
+
+@pytest.mark.parametrize("ld,n_q", [(16385, 12), (40000, 12), (131072, 12), (131072, 40)])
+def test_topk_exact_long_rows_cluster(si, ld, n_q):
     """Rows longer than one CTA's register cache (16384) take a cluster of
     CTAs, each caching a 32768-position segment in shared memory (16385: one
-    CTA; 40000: two; 131072: four): bit-exact against the oracle with heavy
-    ties spread over segments, rows that select everything, rows inside one
-    segment, and rows ending at and one past a segment boundary."""
-    rng = np.random.default_rng(ld)
-    n_q = 12
+    CTA; 40000: two; 131072: four, with 12 and with 40 rows).  Bit-exact
+    against the oracle with heavy ties spread over segments, rows that select
+    everything, rows inside one segment, and rows ending at and one past a
+    segment boundary."""
+    rng = np.random.default_rng(ld + n_q)
     edges = np.minimum([0, 100, 16383, 16384, 32767, 32768], ld - 1)
     pos = np.concatenate([rng.integers(0, ld, n_q - 7), edges, [ld - 1]]).astype(np.int32)
     sc = rng.integers(-30, 30, size=(n_q, ld)).astype(np.float32)   # many equal keys
