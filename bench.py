@@ -15,9 +15,9 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import re
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -213,6 +213,20 @@ def _kernel_traffic(kernel: str, source: str, workload: str):
     return None
 
 
+def _topk_kernel(wl, sms=152):
+    """The Top-K kernel the library picks for this batch (the rule in
+    si_topk.cu's launcher): clusters for long rows in a small batch, one CTA
+    per row with its keys in shared memory for many rows of 8193..16384,
+    else one CTA per row from registers or streaming."""
+    longest = wl.max_ctx
+    C = -(-longest // 32768)
+    if longest > 16384 and C <= 8 and wl.n_q * C <= 2 * sms:
+        return "k_topk_cluster"
+    if 8192 < longest <= 16384 and wl.n_q > sms:
+        return "k_topk_cluster"
+    return "k_topk_rows"
+
+
 def _kernel_of(wl):
     """The CUDA kernel (and its source file) each step of the path runs for
     this workload: the tensor-core kernels where their shape conditions hold
@@ -224,10 +238,18 @@ def _kernel_of(wl):
     tc_at = (wl.Hq == 128 and wl.Dqk == 576 and wl.Dv == 512
              and wl.kv_dtype in ("bf16", "e4m3", "e2m1"))
     prefill = tc_ix and wl.n_seq == 1 and wl.n_q >= 64
+    # a planned mixed batch sends each run of >= 64 rows of one sequence (a
+    # prefill chunk) to the prefill kernel, the other rows to the decode one
+    import numpy as np
+    q_seq = np.asarray(wl.q_seq)
+    cuts = np.flatnonzero(np.diff(q_seq)) + 1
+    runs = np.diff(np.concatenate([[0], cuts, [len(q_seq)]]))
+    chunks = tc_ix and not prefill and bool((runs >= 64).any())
     return {"indexer": ("k_indexer_prefill", "si_indexer_prefill.cu") if prefill
+            else ("k_indexer_prefill + k_indexer_tc", "si_indexer_prefill.cu") if chunks
             else ("k_indexer_tc", "si_indexer_tc.cu") if tc_ix
             else ("k_indexer_generic", "si_generic.cu"),
-            "topk": ("k_topk_rows", "si_topk.cu"),
+            "topk": (_topk_kernel(wl), "si_topk.cu"),
             "attn": ("k_attn_tc", "si_attn_tc.cu") if tc_at
             else ("k_attn_generic", "si_generic.cu")}
 

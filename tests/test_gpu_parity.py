@@ -460,3 +460,30 @@ def test_indexer_topk_equals_scores_then_topk(si, name, over):
         si.indexer_topk(b, dw.indexer, dw.k_top, idx, ws2)
         assert si.workspace_status(ws2) == 0
         assert torch.equal(idx, ref)
+
+
+@pytest.mark.parametrize("q_fmt", ["bf16", "e4m3", "mx"])
+def test_indexer_topk_prefill_in_strips(si, q_fmt):
+    """A causal prefill through si_indexer_topk with a workspace of 256 score
+    rows: 12 strips on the prefill kernel, each after the first launched to
+    overlap the previous strip's Top-K, none writing the -inf tail.  The
+    selection equals si_indexer_scores (which writes the tail) followed by
+    si_topk, for each indexer query format."""
+    over = {"bf16": {}, "e4m3": {"q_idx_fp8": True}, "mx": {"idx_mx": True}}[q_fmt]
+    wl = synth.make("c2", L=3000, K=256, Hq=1, Dqk=64, Dv=64, **over)
+    dw = si.upload(wl)
+    b = dw.batch
+    sc = torch.empty((dw.n_q, b.max_ctx), dtype=torch.float32, device="cuda")
+    ref = torch.empty((dw.n_q, dw.k_top), dtype=torch.int32, device="cuda")
+    ws = si.alloc_workspace(4096)
+    si.indexer_scores(b, dw.indexer, sc, ws)
+    si.topk(b, sc, dw.k_top, ref, ws)
+    assert si.workspace_status(ws) == 0
+    assert np.isneginf(sc[0, 1:].cpu().numpy()).all()  # the tail of the separate call
+    row_bytes = 4 * ((b.max_ctx + 63) // 64 * 64)
+    ws2 = si.alloc_workspace(256 + 256 * row_bytes)
+    assert ws2.numel() >= si.workspace_min(si.OP_SELECT, b, dw.indexer, None, dw.k_top)
+    idx = torch.full_like(ref, -7)
+    si.indexer_topk(b, dw.indexer, dw.k_top, idx, ws2)
+    assert si.workspace_status(ws2) == 0
+    assert torch.equal(idx, ref)
