@@ -218,7 +218,7 @@ def _topk_kernel(wl, sms=152):
     si_topk.cu's launcher): clusters for long rows in a small batch, one CTA
     per row with its keys in shared memory for many rows of 8193..16384,
     else one CTA per row from registers or streaming."""
-    longest = wl.max_ctx
+    longest = getattr(wl, "max_ctx", 0)
     C = -(-longest // 32768)
     if longest > 16384 and C <= 8 and wl.n_q * C <= 2 * sms:
         return "k_topk_cluster"
@@ -241,7 +241,7 @@ def _kernel_of(wl):
     # a planned mixed batch sends each run of >= 64 rows of one sequence (a
     # prefill chunk) to the prefill kernel, the other rows to the decode one
     import numpy as np
-    q_seq = np.asarray(wl.q_seq)
+    q_seq = np.asarray(getattr(wl, "q_seq", np.zeros(0, np.int32)))
     cuts = np.flatnonzero(np.diff(q_seq)) + 1
     runs = np.diff(np.concatenate([[0], cuts, [len(q_seq)]]))
     chunks = tc_ix and not prefill and bool((runs >= 64).any())
