@@ -599,6 +599,47 @@ def prefill_indexer(si, dev, steps):
                                      "(block-scaled UMMA, three rows per 192-wide block)"}}
 
 
+def mxfp8_conversion(si, dev, steps):
+    """si_quant_mxfp8 (section 4.3's per-group quantisation of the indexer
+    query, in section 5.1's MXFP8 format) on the 16384-token prefill's query:
+    16384 rows x 64 heads x 128 bf16 entries (268 MB, larger than L2, so no
+    flush is needed between calls).  Algorithmic bytes: 2 read + 1 + 1/32
+    written per entry, over the event-timed call, against the measured HBM
+    copy bandwidth.  The values are seeded N(0, 1/128) draws made on the
+    device (the conversion is checked bit for bit against the oracle by the
+    tests, not here)."""
+    import torch
+    rows, dim = 16384 * 64, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(2)
+    x = (torch.randn((rows, dim), generator=g, device=dev) / dim ** 0.5).to(torch.bfloat16)
+    codes = torch.empty((rows, dim), dtype=torch.uint8, device=dev)
+    scales = torch.empty((rows, dim // 32), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        si.quant_mxfp8(x, codes, scales, stream)
+    torch.cuda.synchronize(dev)
+    n = max(10, min(steps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for e0, e1 in evs:
+        e0.record(stream)
+        si.quant_mxfp8(x, codes, scales, stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    nbytes = rows * dim * 3 + rows * dim // 32
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peaks = _peaks()
+    del x, codes, scales
+    torch.cuda.empty_cache()
+    return {"workload": "16384 x 64 x 128 bf16 indexer query rows (causal prefill 16384)",
+            "kernel": "k_quant_mxfp8", "call": "si_quant_mxfp8", "ms_per_call": ms,
+            "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
+            "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+            "l2": "input 268 MB, larger than L2"}
+
+
 def candidate_selection(si, dev, steps, n_cand=16384):
     """Candidate-restricted selection (the vLLM article on DeepSeek-V4.1,
     "Kernels": indexer logits over a fixed candidate set per query) on the
@@ -872,7 +913,8 @@ def run_si(args):
         others = {"long_context": workload_record(si, dev, "c3", args.steps, args.warmup),
                   "mixed": workload_record(si, dev, "c4", args.steps, args.warmup),
                   "mxfp8_indexer": workload_record(si, dev, "c1", args.steps, args.warmup,
-                                                   variant=":mx", idx_mx=True)}
+                                                   variant=":mx", idx_mx=True),
+                  "mxfp8_conversion": mxfp8_conversion(si, dev, args.steps)}
 
     cpu = None
     if not args.no_cpu_baseline:
