@@ -231,3 +231,21 @@ def test_mxfp8_host_validation(si):
     assert q(None, si.BF16, 4, 64, P(fake), P(fake), None) == 1
     assert q(P(fake), si.BF16, -1, 64, P(fake), P(fake), None) == 1
     assert q(None, si.BF16, 0, 64, None, None, None) == 0                    # empty: no-op
+
+
+def test_binding_refuses_to_import_without_the_library(tmp_path):
+    """No fallback: the Python binding, copied without libsi.so, raises at
+    import instead of running anything on the CPU."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "indexer_driven_top_gb300"
+    pkg.mkdir()
+    for fn in ("__init__.py", "_build.py"):
+        shutil.copy(os.path.join(ROOT, "indexer_driven_top_gb300", fn), pkg / fn)
+    code = ("import sys; sys.path.insert(0, sys.argv[1]); "
+            "import indexer_driven_top_gb300")
+    r = subprocess.run([sys.executable, "-c", code, str(tmp_path)], capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode != 0
+    assert "libsi.so is not built" in r.stderr
